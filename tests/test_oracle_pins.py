@@ -1,0 +1,347 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test checks one oracle function against brute force, a closed form, an invariant, a
+hand-worked example (tests/golden) or a special case that reduces to an independent library
+routine (torch), chosen so that a dropped term, a wrong sign or index, or a swapped operand
+in the oracle fails at least one of them.
+"""
+import itertools
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import bf16, moe_ref
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ----------------------------------------------------------------------------- bf16
+def test_bf16_round_matches_torch_conversion():
+    rng = np.random.default_rng(1)
+    v = np.concatenate([rng.standard_normal(20000) * 10.0 ** rng.integers(-30, 30, 20000),
+                        [0.0, -0.0, 1.0, 1 + 2 ** -8, 1 + 3 * 2 ** -8, -1 - 2 ** -8, 2.0 ** -130,
+                         3.3e38, -3.3e38]]).astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float64).numpy()
+    got = bf16.round_rne(v.astype(np.float64))
+    assert np.array_equal(got, ref)
+
+
+def test_bf16_ties_to_even_by_hand():
+    # bf16 spacing at 1.0 is 2^-7: 1 + 2^-8 is a tie -> 1.0 (even); 1 + 3*2^-8 -> 1 + 2^-6
+    assert bf16.round_rne(np.array([1 + 2 ** -8]))[0] == 1.0
+    assert bf16.round_rne(np.array([1 + 3 * 2 ** -8]))[0] == 1 + 2 ** -6
+    assert bf16.round_rne(np.array([-(1 + 3 * 2 ** -8)]))[0] == -(1 + 2 ** -6)
+
+
+def test_bf16_decode_matches_torch():
+    bits = np.arange(0, 65536, 7, dtype=np.uint16)
+    bits = bits[((bits >> 7) & 0xFF) != 0xFF]          # drop inf/nan encodings
+    ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).double().numpy()
+    assert np.array_equal(bf16.decode(bits), ref)
+
+
+# ----------------------------------------------------------------------------- router
+def test_router_logits_one_hot_rows_pick_router_rows():
+    H, E = 12, 5
+    w = np.random.default_rng(2).standard_normal((H, E))
+    x = np.eye(H)[[3, 0, 11]]
+    assert np.array_equal(moe_ref.router_logits(x, w), w[[3, 0, 11]])
+    b = np.arange(E, dtype=np.float64)
+    assert np.array_equal(moe_ref.router_logits(x, w, b), w[[3, 0, 11]] + b)
+
+
+def test_router_logits_not_transposed():
+    # x[T,H] @ W[H,E] with H != E: a transposed operand would not even broadcast the same
+    x = np.array([[1.0, 2.0, 3.0]])
+    w = np.array([[1.0, 0.0], [0.0, 10.0], [100.0, 0.0]])
+    assert np.array_equal(moe_ref.router_logits(x, w), [[301.0, 20.0]])
+
+
+# ----------------------------------------------------------------------------- top-k
+@pytest.mark.parametrize("E,k", [(4, 1), (5, 2), (6, 3), (8, 2), (8, 8), (7, 4)])
+def test_topk_matches_brute_force_over_subsets(E, k):
+    rng = np.random.default_rng(E * 10 + k)
+    for trial in range(60):
+        # integer scores give many exact ties, real scores none
+        s = rng.integers(0, 4, (3, E)).astype(np.float64) if trial % 2 else rng.standard_normal((3, E))
+        ids, gap = moe_ref.topk_select(s, k)
+        for t in range(3):
+            best = max(itertools.combinations(range(E), k),
+                       key=lambda c: (sum(s[t, list(c)]), [-i for i in c]))
+            assert tuple(ids[t]) == best
+            if k < E:
+                chosen = set(best)
+                kth = min(s[t, list(chosen)])
+                rest = max(s[t, e] for e in range(E) if e not in chosen)
+                assert gap[t] == kth - rest
+
+
+def test_topk_ties_go_to_lower_id():
+    ids, gap = moe_ref.topk_select(np.array([[1.0, 3.0, 3.0, 3.0]]), 2)
+    assert ids.tolist() == [[1, 2]] and gap[0] == 0.0
+
+
+# ----------------------------------------------------------------------------- gating
+def test_softmax_renorm_two_experts_is_logistic():
+    # w_0 = exp(l_0)/(exp(l_0)+exp(l_1)) = 1/(1+exp(l_1-l_0))
+    l = np.array([[0.3, -1.2, 5.0]])
+    ids = np.array([[0, 1]])
+    w = moe_ref.gate_weights(l, ids, "softmax_renorm")
+    assert np.allclose(w[0], [1 / (1 + np.exp(-1.5)), 1 / (1 + np.exp(1.5))], rtol=0, atol=1e-15)
+
+
+def test_softmax_no_renorm_uses_all_experts():
+    l = np.array([[0.0, 0.0, 0.0, np.log(5.0)]])     # exps 1,1,1,5 -> total 8
+    w = moe_ref.gate_weights(l, np.array([[0, 3]]), "softmax")
+    assert np.allclose(w[0], [1 / 8, 5 / 8], atol=1e-15)
+
+
+def test_sigmoid_renorm_scaled_weights():
+    l = np.array([[0.0, np.log(3.0), -7.0]])        # sigmoid: 1/2, 3/4
+    w = moe_ref.gate_weights(l, np.array([[0, 1]]), "sigmoid_bias_renorm", 2.5)
+    assert np.allclose(w[0], [2.5 * 0.5 / 1.25, 2.5 * 0.75 / 1.25], atol=1e-14)
+
+
+def test_sigmoid_selection_bias_steers_selection_not_weights():
+    l = np.array([[2.0, 0.0, -1.0]])
+    bias = np.array([-10.0, 0.0, 5.0])
+    s = moe_ref.selection_scores(l, "sigmoid_bias_renorm", bias)
+    assert np.allclose(s, 1 / (1 + np.exp(-l)) + bias)
+    ids, _ = moe_ref.topk_select(s, 2)
+    assert ids.tolist() == [[1, 2]]
+    w = moe_ref.gate_weights(l, ids, "sigmoid_bias_renorm", 1.0)
+    sg = 1 / (1 + np.exp(-np.array([0.0, -1.0])))
+    assert np.allclose(w[0], sg / sg.sum())
+
+
+# ----------------------------------------------------------------------------- dispatch
+def _read_golden(name):
+    rows = {}
+    for line in open(os.path.join(GOLDEN, name)):
+        if line.startswith("#") or not line.strip():
+            continue
+        key, *vals = line.split()
+        rows[key] = [int(v) for v in vals]
+    return rows
+
+
+def test_dispatch_hand_worked_example():
+    g = _read_golden("dispatch_tiny.txt")
+    E, k = g["E"][0], g["k"][0]
+    ids = np.array(g["ids"]).reshape(-1, k)
+    counts, offsets, pos, src = moe_ref.dispatch(ids, E)
+    assert counts.tolist() == g["counts"]
+    assert offsets.tolist() == g["offsets"]
+    assert pos.reshape(-1).tolist() == g["pos"]
+    assert src.tolist() == g["src"]
+
+
+@pytest.mark.parametrize("T,E,k", [(1, 8, 2), (37, 8, 2), (50, 60, 4), (9, 256, 8), (5, 3, 3)])
+def test_dispatch_invariants(T, E, k):
+    rng = np.random.default_rng(T + E + k)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts, offsets, pos, src = moe_ref.dispatch(ids, E)
+    assert counts.sum() == T * k
+    assert np.array_equal(counts, np.bincount(ids.ravel(), minlength=E))
+    assert offsets[0] == 0 and offsets[-1] == T * k and np.all(np.diff(offsets) == counts)
+    assert np.array_equal(np.sort(pos.ravel()), np.arange(T * k))      # bijection
+    assert np.array_equal(src[pos.ravel()], np.arange(T * k))
+    for e in range(E):                      # segment e holds exactly e's rows, tokens ascending
+        seg = src[offsets[e]:offsets[e + 1]]
+        assert np.all(ids[seg // k, seg % k] == e)
+        assert np.all(np.diff(seg // k) > 0)
+    xs = rng.standard_normal((T, 3))
+    assert np.array_equal(moe_ref.permute(xs, src, k), xs[src // k])
+
+
+# ----------------------------------------------------------------------------- FFN
+def _torch_swiglu(x, wg, wu, wd):
+    """Independent SwiGLU with torch's silu, rounding h and y through torch's bf16 cast."""
+    tx = torch.from_numpy(x)
+    h = (torch.nn.functional.silu(tx @ torch.from_numpy(wg)) * (tx @ torch.from_numpy(wu)))
+    h = h.float().to(torch.bfloat16).double()
+    return (h @ torch.from_numpy(wd)).float().to(torch.bfloat16).double().numpy()
+
+
+def test_swiglu_matches_torch_silu():
+    cfg = wl.custom("ffn", H=64, I=96)
+    w = wl.expert(cfg, 0, 3)
+    x = bf16.decode(wl.tokens(cfg, 11))
+    wg, wu, wd = moe_ref.expert_matrices(w)
+    y, h = moe_ref.swiglu_ffn(x, wg, wu, wd)
+    ref = _torch_swiglu(x, wg, wu, wd)
+    # torch rounds fp64 -> fp32 -> bf16 (can double-round); allow one bf16 ulp
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    assert np.all(np.abs(y - ref) <= ulp)
+    assert np.mean(y == ref) > 0.97
+
+
+def test_swiglu_scalar_closed_form():
+    # H = I = 1: g = 2, u = 3, silu(2) = 2/(1+e^-2); h = bf16(.), y = bf16(h * 0.5)
+    y, h = moe_ref.swiglu_ffn(np.array([[1.0]]), np.array([[2.0]]), np.array([[3.0]]),
+                              np.array([[0.5]]))
+    hv = 2.0 / (1.0 + np.exp(-2.0)) * 3.0
+    assert abs(h[0, 0] - hv) <= 2.0 ** -6 and h[0, 0] == 5.28125  # bf16 grid near 5.28
+    assert y[0, 0] == 5.28125 * 0.5
+
+
+def test_int4_dequant_multiple_of_scale():
+    cfg = wl.custom("q", H=256, I=128, wdtype="int4_g128")
+    w = wl.expert(cfg, 0, 1)
+    wg = moe_ref.dequant_int4(w.wg, w.sg, 128)
+    s = bf16.decode(w.sg)
+    assert w.wg.min() >= -7 and w.wg.max() <= 7
+    q = wg / np.repeat(s, 128, axis=0)
+    assert np.array_equal(q, w.wg.astype(np.float64))
+    # hand element: row 130 is in group 1
+    assert wg[130, 5] == w.wg[130, 5] * s[1, 5]
+    # down projection: reduction dim is I (rows of wd), scales [I/128, H]
+    wd = moe_ref.dequant_int4(w.wd, w.sd, 128)
+    assert wd[127, 200] == w.wd[127, 200] * bf16.decode(w.sd)[0, 200]
+
+
+# ----------------------------------------------------------------------------- combine
+def test_combine_by_hand():
+    y = np.array([[1.0, 2.0], [10.0, 20.0], [100.0, 200.0]])
+    pos = np.array([[2, 0], [1, 2]])
+    w = np.array([[0.5, 0.25], [1.0, 0.125]])
+    out = moe_ref.combine(y, pos, w)
+    assert out.tolist() == [[50.25, 100.5], [22.5, 45.0]]
+    sh = np.array([[1.0, 1.0], [2.0, 2.0]])
+    out2 = moe_ref.combine(y, pos, w, sh, np.array([0.5, 0.25]))
+    assert out2.tolist() == [[50.75, 101.0], [23.0, 45.5]]
+
+
+# ----------------------------------------------------------------------------- whole layer
+def _tiny(**kw):
+    base = dict(H=64, E=6, k=2, I=128, gating="softmax_renorm")
+    base.update(kw)
+    return wl.custom("pin", **base)
+
+
+def test_k_equals_E_is_dense_gate_weighted_mixture():
+    cfg = _tiny(k=6)
+    xb = wl.tokens(cfg, 9)
+    r = moe_ref.layer_forward(cfg, 0, xb)
+    x = bf16.decode(xb)
+    l = x @ wl.router(cfg, 0).astype(np.float64)
+    gates = np.exp(l - l.max(1, keepdims=True))
+    gates /= gates.sum(1, keepdims=True)
+    experts = [moe_ref.expert_matrices(wl.expert(cfg, 0, e)) for e in range(cfg.E)]
+    ref = moe_ref.dense_mixture(x, gates, experts)
+    err = np.abs(r["out"] - ref).max()
+    assert err <= 2e-2 * np.abs(ref).max()
+    assert np.abs(r["out"] - ref).sum() / np.abs(ref).sum() < 5e-3
+
+
+def _one_hot_inputs(cfg, T, star):
+    """Tokens and a router for which expert `star` beats every other logit by ~100.
+
+    W_r is zero except column `star` = 1, and each token is scaled so that its element sum
+    is +100: the star logit is ~100, all others 0, so softmax gives the star weight
+    1/(1 + e^-100), which is exactly 1.0 in fp64."""
+    x = bf16.decode(wl.tokens(cfg, T))
+    s = x.sum(1)
+    x = bf16.round_rne(x * (100.0 / np.where(np.abs(s) < 1e-3, 1e-3, s))[:, None])
+    w_r = np.zeros((cfg.H, cfg.E))
+    w_r[:, star] = 1.0
+    return bf16.to_bits(x), x, w_r
+
+
+def _with_router(w_r, fn):
+    import workloads
+    orig = workloads.router
+    workloads.router = lambda c, layer=0: w_r
+    try:
+        return fn()
+    finally:
+        workloads.router = orig
+
+
+def test_one_hot_router_reproduces_single_expert():
+    cfg = _tiny(k=1)
+    star = 4
+    xb, x, w_r = _one_hot_inputs(cfg, 7, star)
+    r = _with_router(w_r, lambda: moe_ref.layer_forward(cfg, 0, xb))
+    assert np.array_equal(r["ids"], np.full((7, 1), star))
+    assert np.all(r["w"] == 1.0)
+    wg, wu, wd = moe_ref.expert_matrices(wl.expert(cfg, 0, star))
+    ref = _torch_swiglu(x, wg, wu, wd)
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    assert np.all(np.abs(r["out"] - ref) <= ulp)
+    assert np.mean(r["out"] == ref) > 0.97
+
+
+def test_one_hot_router_selects_the_dominant_expert():
+    cfg = _tiny(k=2)
+    xb, x, w_r = _one_hot_inputs(cfg, 5, 2)
+    r = _with_router(w_r, lambda: moe_ref.layer_forward(cfg, 0, xb))
+    # the runner-up is a zero-logit tie among the others: lowest id (0); ids ascending
+    assert np.all(r["ids"][:, 0] == 0) and np.all(r["ids"][:, 1] == 2)
+    assert np.all(r["w"][:, 1] == 1.0) and np.all(r["w"][:, 0] < 1e-40)
+
+
+def test_token_permutation_invariance():
+    cfg = _tiny(E=8, k=3, gating="softmax")
+    xb = wl.tokens(cfg, 13)
+    perm = np.random.default_rng(0).permutation(13)
+    a = moe_ref.layer_forward(cfg, 0, xb)
+    b = moe_ref.layer_forward(cfg, 0, xb[perm])
+    assert np.array_equal(a["ids"][perm], b["ids"])
+    assert np.array_equal(a["out"][perm], b["out"])
+    assert a["counts"].sum() == 13 * 3
+
+
+def test_shared_expert_term_and_sigmoid_gate():
+    cfg = _tiny(Is=192, shared_gate="sigmoid")
+    xb = wl.tokens(cfg, 4)
+    x = bf16.decode(xb)
+    zero = wl.ExpertWeights("bf16", *(np.zeros_like(a) for a in
+                                     (wl.expert(cfg, 0, 0).wg, wl.expert(cfg, 0, 0).wu,
+                                      wl.expert(cfg, 0, 0).wd)))
+
+    def weights(layer, e, shared=False):
+        return wl.expert(cfg, layer, e, shared=True) if shared else zero
+    r = moe_ref.layer_forward(cfg, 0, xb, weights=weights)
+    wg, wu, wd = moe_ref.expert_matrices(wl.expert(cfg, 0, 0, shared=True))
+    s = _torch_swiglu(x, wg, wu, wd)
+    ws = bf16.decode(wl.shared_gate_vector(cfg, 0))
+    g = torch.sigmoid(torch.from_numpy(x @ ws)).numpy()
+    ref = g[:, None] * s
+    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(ref), 1e-30))) - 7)
+    assert np.all(np.abs(r["out"] - ref) <= 2 * ulp)
+
+
+def test_forced_ids_equal_selected_ids_reproduce_layer():
+    cfg = _tiny(E=8, k=2)
+    xb = wl.tokens(cfg, 10)
+    a = moe_ref.layer_forward(cfg, 0, xb)
+    b = moe_ref.layer_forward(cfg, 0, xb, forced_ids=a["ids"])
+    assert np.array_equal(a["out"], b["out"])
+
+
+def test_rows_subset_matches_full():
+    cfg = _tiny(E=8, k=2)
+    xb = wl.tokens(cfg, 17)
+    a = moe_ref.layer_forward(cfg, 0, xb)
+    rows = np.array([16, 0, 5])
+    b = moe_ref.layer_forward(cfg, 0, xb, rows=rows)
+    assert np.array_equal(a["out"][rows], b["out"])
+
+
+def test_int4_layer_uses_dequantised_weights():
+    cfg = _tiny(H=256, I=128, wdtype="int4_g128", gating="sigmoid_bias_renorm", scale=2.5,
+                k=2, E=6)
+    xb = wl.tokens(cfg, 3)
+    r = moe_ref.layer_forward(cfg, 0, xb)
+    assert np.allclose(r["w"].sum(1), 2.5)
+    # a bundle whose scale block comes from another expert gives a different output
+    def swapped(layer, e, shared=False):
+        w = wl.expert(cfg, layer, e)
+        other = wl.expert(cfg, layer, (e + 1) % cfg.E)
+        return wl.ExpertWeights(w.wdtype, w.wg, w.wu, w.wd, other.sg, other.su, other.sd)
+    r2 = moe_ref.layer_forward(cfg, 0, xb, weights=swapped)
+    assert np.abs(r2["out"] - r["out"]).max() > 0.05 * np.abs(r["out"]).max()
