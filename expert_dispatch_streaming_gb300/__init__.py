@@ -1,0 +1,298 @@
+"""Python binding of libmoe (the C ABI in include/moe.h), by ctypes.
+
+Argument marshalling only: every step of the MoE layer runs in the library's CUDA kernels.
+Device buffers are passed as integers (``tensor.data_ptr()``) or as torch tensors, streams
+as ``torch.cuda.Stream`` / raw handles.  The library is loaded eagerly from this directory;
+importing this package without a built ``libmoe.so`` raises ``ImportError`` (there is no
+fallback implementation).
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = -1
+MOE_ERR_CUDA = -2
+MOE_ERR_CAPACITY = -3
+MOE_ERR_TIMEOUT = -4
+MOE_ERR_CORRUPT = -5
+MOE_ERR_UNSUPPORTED = -6
+MOE_ERR_NO_MEMORY = -7
+
+MOE_GATING_SOFTMAX_RENORM = 0
+MOE_GATING_SOFTMAX = 1
+MOE_GATING_SIGMOID_BIAS_RENORM = 2
+GATING = {"softmax_renorm": 0, "softmax": 1, "sigmoid_bias_renorm": 2}
+
+MOE_W_BF16 = 0
+MOE_W_INT4_G128 = 1
+WDTYPE = {"bf16": 0, "int4_g128": 1}
+
+
+class MoEError(RuntimeError):
+    def __init__(self, status, fn):
+        self.status = status
+        cuda = _lib.moe_last_cuda_error() if status == MOE_ERR_CUDA else 0
+        super().__init__(f"{fn}: {_lib.moe_status_string(status).decode()}"
+                         + (f" (cudaError {cuda})" if cuda else ""))
+
+
+# ----------------------------------------------------------------------------- structs
+class moe_bundle_layout(C.Structure):
+    _fields_ = [("total_bytes", C.c_size_t), ("gate_up_offset", C.c_size_t),
+                ("down_offset", C.c_size_t), ("gate_up_scale_offset", C.c_size_t),
+                ("down_scale_offset", C.c_size_t)]
+
+
+class moe_host_bundle(C.Structure):
+    _fields_ = [("ptr", C.c_void_p), ("bytes", C.c_size_t), ("checksum", C.c_uint64)]
+
+
+class moe_expert_cache_config(C.Structure):
+    _fields_ = [("slot_bytes", C.c_size_t), ("capacity_bytes", C.c_size_t),
+                ("n_layers", C.c_int), ("n_experts", C.c_int),
+                ("bundles", C.POINTER(moe_host_bundle)), ("timeout_ms", C.c_int),
+                ("verify_checksums", C.c_int), ("device", C.c_int)]
+
+
+class moe_cache_event(C.Structure):
+    _fields_ = [("request", C.c_int64), ("layer", C.c_int32), ("expert", C.c_int32),
+                ("miss", C.c_int32), ("victim_layer", C.c_int32),
+                ("victim_expert", C.c_int32), ("slot", C.c_int32)]
+
+
+class moe_cache_stats(C.Structure):
+    _fields_ = [("requests", C.c_int64), ("hits", C.c_int64), ("misses", C.c_int64),
+                ("evictions", C.c_int64), ("bytes_h2d", C.c_int64), ("n_slots", C.c_int32),
+                ("resident", C.c_int32)]
+
+
+class moe_layer(C.Structure):
+    _fields_ = [("H", C.c_int), ("E", C.c_int), ("k", C.c_int), ("I", C.c_int), ("Is", C.c_int),
+                ("gating", C.c_int), ("scale", C.c_float), ("wdtype", C.c_int),
+                ("layer_index", C.c_int), ("shared_gate_sigmoid", C.c_int),
+                ("w_r", C.c_void_p), ("logit_bias", C.c_void_p), ("sel_bias", C.c_void_p),
+                ("w_gate", C.c_void_p), ("shared_bundle", C.c_void_p),
+                ("bundles", C.POINTER(C.c_void_p))]
+
+
+class moe_layer_stats(C.Structure):
+    _fields_ = [("n_unique", C.c_int32), ("n_missed", C.c_int32), ("n_refined", C.c_int32)]
+
+
+# ----------------------------------------------------------------------------- loading
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run "
+                      "`python -m expert_dispatch_streaming_gb300.build`")
+_lib = C.CDLL(LIB_PATH)
+
+_vp, _i, _f, _sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t
+_SIGS = {
+    "moe_last_cuda_error": (_i, []),
+    "moe_status_string": (C.c_char_p, [_i]),
+    "moe_version": (_i, []),
+    "moe_bundle_layout_of": (_i, [_i, _i, _i, C.POINTER(moe_bundle_layout)]),
+    "moe_bundle_bytes": (_sz, [_i, _i, _i]),
+    "moe_pack_bundle": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_checksum64": (C.c_uint64, [_vp, _sz]),
+    "moe_route_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "moe_route_topk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
+                            _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_permute": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
+    "moe_grouped_swiglu_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "moe_grouped_swiglu": (_i, [_vp, _vp, C.POINTER(_vp), _i, _i, _i, _i, _i, _vp, _vp, _sz,
+                                _vp]),
+    "moe_combine": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "moe_expert_cache_create": (_i, [C.POINTER(moe_expert_cache_config), C.POINTER(_vp),
+                                     C.POINTER(C.c_int64)]),
+    "moe_expert_cache_destroy": (_i, [_vp]),
+    "moe_expert_cache_request": (_i, [_vp, _i, _vp, _vp, _i, C.POINTER(_vp),
+                                      C.POINTER(C.c_int32)]),
+    "moe_expert_cache_wait_expert": (_i, [_vp, _i, _i, _vp]),
+    "moe_expert_cache_release": (_i, [_vp, _i, _vp]),
+    "moe_expert_cache_evict": (_i, [_vp, _i, _i]),
+    "moe_expert_cache_trace": (_i, [_vp, C.POINTER(moe_cache_event), _sz, C.POINTER(_sz)]),
+    "moe_expert_cache_reset_trace": (_i, [_vp]),
+    "moe_expert_cache_stats": (_i, [_vp, C.POINTER(moe_cache_stats)]),
+    "moe_expert_cache_sync": (_i, [_vp]),
+    "moe_layer_workspace_size": (_sz, [C.POINTER(moe_layer), _i]),
+    "moe_layer_forward": (_i, [C.POINTER(moe_layer), _vp, _i, _vp, _vp, _vp, _vp,
+                               C.POINTER(moe_layer_stats), _vp, _vp, _vp, _sz, _vp]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+EXPORTED = tuple(_SIGS)
+
+
+# ----------------------------------------------------------------------------- marshalling
+def ptr(x) -> int | None:
+    """Device/host address of a tensor / array / int (None -> NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        return x.data_ptr()
+    if hasattr(x, "ctypes"):
+        return x.ctypes.data
+    raise TypeError(type(x))
+
+
+def stream_handle(s) -> int | None:
+    if s is None:
+        try:
+            import torch
+            return torch.cuda.current_stream().cuda_stream
+        except Exception:
+            return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status, fn):
+    if status != MOE_OK:
+        raise MoEError(status, fn)
+    return status
+
+
+# ----------------------------------------------------------------------------- API
+def bundle_layout(H, I, wdtype) -> moe_bundle_layout:
+    out = moe_bundle_layout()
+    _check(_lib.moe_bundle_layout_of(H, I, WDTYPE.get(wdtype, wdtype), C.byref(out)),
+           "moe_bundle_layout_of")
+    return out
+
+
+def moe_bundle_bytes(H, I, wdtype) -> int:
+    return _lib.moe_bundle_bytes(H, I, WDTYPE.get(wdtype, wdtype))
+
+
+def moe_pack_bundle(H, I, wdtype, wg, wu, wd, sg, su, sd, dst) -> None:
+    _check(_lib.moe_pack_bundle(H, I, WDTYPE.get(wdtype, wdtype), ptr(wg), ptr(wu), ptr(wd),
+                                ptr(sg), ptr(su), ptr(sd), ptr(dst)), "moe_pack_bundle")
+
+
+def moe_checksum64(data, nbytes) -> int:
+    return _lib.moe_checksum64(ptr(data), nbytes)
+
+
+def moe_route_workspace_size(T, H, E, k) -> int:
+    return _lib.moe_route_workspace_size(T, H, E, k)
+
+
+def moe_route_topk(x, w_r, logit_bias, sel_bias, w_gate, forced_ids, T, H, E, k, gating, scale,
+                   ids, w, counts, offsets, pos, src, logits, shared_gate, tie_flags, ws,
+                   ws_bytes, stream=None) -> None:
+    _check(_lib.moe_route_topk(ptr(x), ptr(w_r), ptr(logit_bias), ptr(sel_bias), ptr(w_gate),
+                               ptr(forced_ids), T, H, E, k, GATING.get(gating, gating),
+                               float(scale), ptr(ids), ptr(w), ptr(counts), ptr(offsets),
+                               ptr(pos), ptr(src), ptr(logits), ptr(shared_gate),
+                               ptr(tie_flags), ptr(ws), ws_bytes, stream_handle(stream)),
+           "moe_route_topk")
+
+
+def moe_permute(x, src, T, k, H, x_perm, stream=None) -> None:
+    _check(_lib.moe_permute(ptr(x), ptr(src), T, k, H, ptr(x_perm), stream_handle(stream)),
+           "moe_permute")
+
+
+def moe_grouped_swiglu_workspace_size(max_rows, E, H, I, wdtype) -> int:
+    return _lib.moe_grouped_swiglu_workspace_size(max_rows, E, H, I, WDTYPE.get(wdtype, wdtype))
+
+
+def moe_grouped_swiglu(x_perm, offsets, bundles, E, H, I, wdtype, max_rows, y_perm, ws, ws_bytes,
+                       stream=None) -> None:
+    arr = (C.c_void_p * E)(*[ptr(b) for b in bundles])
+    _check(_lib.moe_grouped_swiglu(ptr(x_perm), ptr(offsets), arr, E, H, I,
+                                   WDTYPE.get(wdtype, wdtype), max_rows, ptr(y_perm), ptr(ws),
+                                   ws_bytes, stream_handle(stream)), "moe_grouped_swiglu")
+
+
+def moe_combine(y_perm, pos, w, T, k, H, shared, shared_gate, residual, out, stream=None) -> None:
+    _check(_lib.moe_combine(ptr(y_perm), ptr(pos), ptr(w), T, k, H, ptr(shared),
+                            ptr(shared_gate), ptr(residual), ptr(out), stream_handle(stream)),
+           "moe_combine")
+
+
+def moe_expert_cache_create(cfg: moe_expert_cache_config) -> int:
+    h = C.c_void_p()
+    bad = C.c_int64(-1)
+    st = _lib.moe_expert_cache_create(C.byref(cfg), C.byref(h), C.byref(bad))
+    if st != MOE_OK:
+        err = MoEError(st, "moe_expert_cache_create")
+        err.bad_index = bad.value
+        raise err
+    return h.value
+
+
+def moe_expert_cache_destroy(cache) -> None:
+    _check(_lib.moe_expert_cache_destroy(cache), "moe_expert_cache_destroy")
+
+
+def moe_expert_cache_request(cache, layer, used_mask, compute=None, defer_waits=0, E=None):
+    """used_mask: host uint8 array [E].  Returns (slot_ptrs list, n_missed)."""
+    E = E or len(used_mask)
+    slots = (C.c_void_p * E)()
+    nm = C.c_int32(0)
+    _check(_lib.moe_expert_cache_request(cache, layer, ptr(used_mask), stream_handle(compute),
+                                         defer_waits, slots, C.byref(nm)),
+           "moe_expert_cache_request")
+    return [s for s in slots], nm.value
+
+
+def moe_expert_cache_wait_expert(cache, layer, expert, compute=None) -> None:
+    _check(_lib.moe_expert_cache_wait_expert(cache, layer, expert, stream_handle(compute)),
+           "moe_expert_cache_wait_expert")
+
+
+def moe_expert_cache_release(cache, layer, compute=None) -> None:
+    _check(_lib.moe_expert_cache_release(cache, layer, stream_handle(compute)),
+           "moe_expert_cache_release")
+
+
+def moe_expert_cache_evict(cache, layer, expert) -> None:
+    _check(_lib.moe_expert_cache_evict(cache, layer, expert), "moe_expert_cache_evict")
+
+
+def moe_expert_cache_trace(cache) -> list[tuple]:
+    n = C.c_size_t(0)
+    _check(_lib.moe_expert_cache_trace(cache, None, 0, C.byref(n)), "moe_expert_cache_trace")
+    buf = (moe_cache_event * max(1, n.value))()
+    _check(_lib.moe_expert_cache_trace(cache, buf, n.value, C.byref(n)), "moe_expert_cache_trace")
+    return [(e.request, e.layer, e.expert, e.miss, e.victim_layer, e.victim_expert, e.slot)
+            for e in buf[:n.value]]
+
+
+def moe_expert_cache_reset_trace(cache) -> None:
+    _check(_lib.moe_expert_cache_reset_trace(cache), "moe_expert_cache_reset_trace")
+
+
+def moe_expert_cache_stats(cache) -> dict:
+    s = moe_cache_stats()
+    _check(_lib.moe_expert_cache_stats(cache, C.byref(s)), "moe_expert_cache_stats")
+    return {f: getattr(s, f) for f, _ in s._fields_}
+
+
+def moe_expert_cache_sync(cache) -> None:
+    _check(_lib.moe_expert_cache_sync(cache), "moe_expert_cache_sync")
+
+
+def moe_layer_workspace_size(layer: moe_layer, T) -> int:
+    return _lib.moe_layer_workspace_size(C.byref(layer), T)
+
+
+def moe_layer_forward(layer: moe_layer, x, T, forced_ids, residual, out, cache, ws, ws_bytes,
+                      stream=None, ids_out=None, w_out=None) -> moe_layer_stats:
+    st = moe_layer_stats()
+    _check(_lib.moe_layer_forward(C.byref(layer), ptr(x), T, ptr(forced_ids), ptr(residual),
+                                  ptr(out), cache, C.byref(st), ptr(ids_out), ptr(w_out),
+                                  ptr(ws), ws_bytes, stream_handle(stream)), "moe_layer_forward")
+    return st

@@ -1,0 +1,381 @@
+// C-ABI entry points of libmoe and the whole-layer forward.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstring>
+#include <vector>
+
+#include "cache.h"
+#include "common.cuh"
+#include "expert_ffn.cuh"
+#include "route.cuh"
+
+namespace moe {
+
+static thread_local int g_last_cuda = 0;
+
+void set_cuda_error(cudaError_t e) { g_last_cuda = (int)e; }
+int fail_cuda(cudaError_t e) {
+  set_cuda_error(e);
+  return MOE_ERR_CUDA;
+}
+
+int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+  }
+  return n;
+}
+
+int launch_combine(const uint16_t* y, const int32_t* pos, const float* w, int T, int k, int H,
+                   const uint16_t* shared, const float* shared_gate, const uint16_t* residual,
+                   uint16_t* out, cudaStream_t st);
+
+static bool valid_route_shape(int T, int H, int E, int k) {
+  return T >= 0 && H > 0 && H % 8 == 0 && E > 0 && E <= kMaxExperts && k >= 1 &&
+         k <= std::min(E, kMaxK);
+}
+
+// ------------------------------------------------------------------ layer plan
+struct LayerScratch {
+  RouteScratch rs;
+  int32_t *ids, *counts, *offsets, *pos, *src, *tie;
+  float *w, *shared_gate;
+  uint16_t *x_perm, *h, *y_perm, *h_s, *s;
+  float* part;
+  int32_t* counters;
+};
+
+struct LayerPlan {
+  RoutePlan rp;
+  GemmPlan gu, dn, sgu, sdn;
+  moe_bundle_layout lay, slay;
+};
+
+static GemmArgs gemm_args(const moe_bundle_layout& lay, int wdtype, bool fused, int K, int M,
+                          int E, int max_rows) {
+  GemmArgs a{};
+  a.K = K;
+  a.M = M;
+  a.E = E;
+  a.int4 = wdtype == MOE_W_INT4_G128;
+  a.fused = fused;
+  a.max_rows = max_rows;
+  a.w_off = fused ? lay.gate_up_offset : lay.down_offset;
+  a.s_off = fused ? lay.gate_up_scale_offset : lay.down_scale_offset;
+  a.host_n = -1;
+  return a;
+}
+
+static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
+  if (!L || !valid_route_shape(T, L->H, L->E, L->k) || L->I <= 0 || L->I % 128 ||
+      L->H % 128 || L->Is < 0 || L->Is % 128)
+    return MOE_ERR_INVALID_ARG;
+  if (moe_bundle_layout_of(L->H, L->I, L->wdtype, &P->lay) != MOE_OK) return MOE_ERR_INVALID_ARG;
+  if (L->Is && moe_bundle_layout_of(L->H, L->Is, L->wdtype, &P->slay) != MOE_OK)
+    return MOE_ERR_INVALID_ARG;
+  const int rows = T * L->k;
+  P->rp = plan_route(T, L->H, L->E, L->k, L->Is > 0 && L->shared_gate_sigmoid);
+  P->gu = plan_gemm(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows));
+  P->dn = plan_gemm(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows));
+  if (L->Is) {
+    P->sgu = plan_gemm(gemm_args(P->slay, L->wdtype, true, L->H, L->Is, 1, T));
+    P->sdn = plan_gemm(gemm_args(P->slay, L->wdtype, false, L->Is, L->H, 1, T));
+  }
+  return MOE_OK;
+}
+
+static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, LayerScratch* s) {
+  LayerScratch z{};
+  const size_t tk = (size_t)T * L->k;
+  route_scratch(c, P.rp, T, L->E, &z.rs);
+  z.ids = c.take<int32_t>(tk + 1);
+  z.w = c.take<float>(tk + 1);
+  z.counts = c.take<int32_t>(L->E);
+  z.offsets = c.take<int32_t>(L->E + 1);
+  z.pos = c.take<int32_t>(tk + 1);
+  z.src = c.take<int32_t>(tk + 1);
+  z.tie = c.take<int32_t>(T + 1);
+  z.shared_gate = c.take<float>(T + 1);
+  z.x_perm = c.take<uint16_t>(tk * L->H + 8);
+  z.h = c.take<uint16_t>(tk * L->I + 8);
+  z.y_perm = c.take<uint16_t>(tk * L->H + 8);
+  if (L->Is) {
+    z.h_s = c.take<uint16_t>((size_t)T * L->Is + 8);
+    z.s = c.take<uint16_t>((size_t)T * L->H + 8);
+  }
+  size_t pe = std::max({P.gu.part_elems, P.dn.part_elems, P.sgu.part_elems, P.sdn.part_elems,
+                        (size_t)1});
+  size_t ce = std::max({P.gu.counter_elems, P.dn.counter_elems, P.sgu.counter_elems,
+                        P.sdn.counter_elems, (size_t)1});
+  z.part = c.take<float>(pe);
+  z.counters = c.take<int32_t>(ce);
+  if (s) *s = z;
+  return c.used;
+}
+
+static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
+                       const BundleTable& tab, int T, int host_n, const int32_t* host_ids,
+                       cudaStream_t st) {
+  const int rows = T * L->k;
+  GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows);
+  gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = s.rs.active;
+  gu.n_active = s.rs.n_active; gu.tab = &tab; gu.out = s.h;
+  gu.host_n = host_n; gu.host_ids = host_ids;
+  GemmPlan pg = plan_gemm(gu);
+  int r = launch_gemm(gu, pg, s.part, s.counters, st);
+  if (r != MOE_OK) return r;
+  GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
+  dn.xin = s.h; dn.offsets = s.offsets; dn.active = s.rs.active;
+  dn.n_active = s.rs.n_active; dn.tab = &tab; dn.out = s.y_perm;
+  dn.host_n = host_n; dn.host_ids = host_ids;
+  GemmPlan pd = plan_gemm(dn);
+  return launch_gemm(dn, pd, s.part, s.counters, st);
+}
+
+static int run_shared(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
+                      const uint16_t* x, int T, cudaStream_t st) {
+  if (!L->Is) return MOE_OK;
+  BundleTable tab{};
+  tab.p[0] = L->shared_bundle;
+  const int32_t* meta = s.rs.shared_meta;
+  GemmArgs gu = gemm_args(P.slay, L->wdtype, true, L->H, L->Is, 1, T);
+  gu.xin = x; gu.offsets = meta; gu.active = meta + 2; gu.n_active = meta + 3;
+  gu.tab = &tab; gu.out = s.h_s;
+  int r = launch_gemm(gu, P.sgu, s.part, s.counters, st);
+  if (r != MOE_OK) return r;
+  GemmArgs dn = gemm_args(P.slay, L->wdtype, false, L->Is, L->H, 1, T);
+  dn.xin = s.h_s; dn.offsets = meta; dn.active = meta + 2; dn.n_active = meta + 3;
+  dn.tab = &tab; dn.out = s.s;
+  return launch_gemm(dn, P.sdn, s.part, s.counters, st);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_last_cuda_error(void) { return g_last_cuda; }
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_CAPACITY: return "MOE_ERR_CAPACITY";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_CORRUPT: return "MOE_ERR_CORRUPT";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_NO_MEMORY: return "MOE_ERR_NO_MEMORY";
+    default: return "MOE_ERR_UNKNOWN";
+  }
+}
+
+int moe_version(void) { return (1 << 16) | 0; }
+
+size_t moe_route_workspace_size(int T, int H, int E, int k) {
+  if (!valid_route_shape(T, H, E, k)) return 0;
+  WsCursor c(nullptr, 0);
+  return route_scratch(c, plan_route(T, H, E, k, true), T, E, nullptr);
+}
+
+int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
+                   const float* sel_bias, const uint16_t* w_gate, const int32_t* forced_ids,
+                   int T, int H, int E, int k, int gating, float scale, int32_t* ids, float* w,
+                   int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
+                   float* logits, float* shared_gate, int32_t* tie_flags, void* ws,
+                   size_t ws_bytes, void* stream) {
+  MOE_REQUIRE(valid_route_shape(T, H, E, k));
+  MOE_REQUIRE(gating >= 0 && gating <= 2);
+  MOE_REQUIRE(counts && offsets && ws);
+  MOE_REQUIRE(T == 0 || (x && w_r && ids && w && pos && src));
+  MOE_REQUIRE(!w_gate || shared_gate);
+  const RoutePlan rp = plan_route(T, H, E, k, w_gate != nullptr);
+  WsCursor c(ws, ws_bytes);
+  RouteScratch s{};
+  route_scratch(c, rp, T, E, &s);
+  MOE_REQUIRE(c.ok());
+  RouteArgs a{};
+  a.x = x; a.w_r = w_r; a.logit_bias = logit_bias; a.sel_bias = sel_bias; a.w_gate = w_gate;
+  a.forced = forced_ids; a.T = T; a.H = H; a.E = E; a.k = k; a.gating = gating;
+  a.scale = scale; a.ids = ids; a.counts = counts; a.offsets = offsets; a.pos = pos;
+  a.src = src; a.tie_flags = tie_flags; a.w = w; a.logits = logits;
+  a.shared_gate = shared_gate; a.x_perm = nullptr;
+  return launch_route(a, rp, s, (cudaStream_t)stream);
+}
+
+int moe_permute(const uint16_t* x, const int32_t* src, int T, int k, int H, uint16_t* x_perm,
+                void* stream) {
+  MOE_REQUIRE(T >= 0 && k >= 1 && H > 0 && H % 8 == 0);
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x && src && x_perm && aligned16(x) && aligned16(x_perm));
+  return launch_gather(x, src, T * k, k, H, x_perm, (cudaStream_t)stream);
+}
+
+size_t moe_grouped_swiglu_workspace_size(int max_rows, int E, int H, int I, int wdtype) {
+  moe_bundle_layout lay;
+  if (max_rows < 0 || E <= 0 || E > kMaxExperts || moe_bundle_layout_of(H, I, wdtype, &lay))
+    return 0;
+  WsCursor c(nullptr, 0);
+  GemmPlan a = plan_gemm(gemm_args(lay, wdtype, true, H, I, E, max_rows));
+  GemmPlan b = plan_gemm(gemm_args(lay, wdtype, false, I, H, E, max_rows));
+  c.take<uint16_t>((size_t)max_rows * I + 8);
+  c.take<int32_t>(kMaxExperts + 32);
+  c.take<float>(std::max({a.part_elems, b.part_elems, (size_t)1}));
+  c.take<int32_t>(std::max({a.counter_elems, b.counter_elems, (size_t)1}));
+  return c.used;
+}
+
+// experts that receive rows, computed on the device from offsets (standalone grouped call)
+__global__ void active_from_offsets_kernel(const int32_t* offsets, int E, int32_t* active,
+                                           int32_t* n_active) {
+  if (threadIdx.x != 0) return;
+  int n = 0;
+  for (int e = 0; e < E; ++e)
+    if (offsets[e + 1] > offsets[e]) active[n++] = e;
+  *n_active = n;
+}
+
+int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
+                       const void* const* bundles, int E, int H, int I, int wdtype,
+                       int max_rows, uint16_t* y_perm, void* ws, size_t ws_bytes,
+                       void* stream) {
+  moe_bundle_layout lay;
+  MOE_REQUIRE(E > 0 && E <= kMaxExperts && max_rows >= 0);
+  MOE_REQUIRE(moe_bundle_layout_of(H, I, wdtype, &lay) == MOE_OK);
+  if (max_rows == 0) return MOE_OK;
+  MOE_REQUIRE(x_perm && offsets && bundles && y_perm && ws);
+  MOE_REQUIRE(aligned16(x_perm) && aligned16(y_perm));
+  cudaStream_t st = (cudaStream_t)stream;
+  BundleTable tab{};
+  for (int e = 0; e < E; ++e) tab.p[e] = bundles[e];
+  WsCursor c(ws, ws_bytes);
+  uint16_t* h = c.take<uint16_t>((size_t)max_rows * I + 8);
+  int32_t* act = c.take<int32_t>(kMaxExperts + 32);
+  GemmArgs gu = gemm_args(lay, wdtype, true, H, I, E, max_rows);
+  GemmArgs dn = gemm_args(lay, wdtype, false, I, H, E, max_rows);
+  GemmPlan pg = plan_gemm(gu), pd = plan_gemm(dn);
+  float* part = c.take<float>(std::max({pg.part_elems, pd.part_elems, (size_t)1}));
+  int32_t* ctr = c.take<int32_t>(std::max({pg.counter_elems, pd.counter_elems, (size_t)1}));
+  MOE_REQUIRE(c.ok());
+  active_from_offsets_kernel<<<1, 32, 0, st>>>(offsets, E, act, act + kMaxExperts);
+  MOE_LAUNCH_CHECK();
+  gu.xin = x_perm; gu.offsets = offsets; gu.active = act; gu.n_active = act + kMaxExperts;
+  gu.tab = &tab; gu.out = h;
+  int r = launch_gemm(gu, pg, part, ctr, st);
+  if (r != MOE_OK) return r;
+  dn.xin = h; dn.offsets = offsets; dn.active = act; dn.n_active = act + kMaxExperts;
+  dn.tab = &tab; dn.out = y_perm;
+  return launch_gemm(dn, pd, part, ctr, st);
+}
+
+int moe_combine(const uint16_t* y_perm, const int32_t* pos, const float* w, int T, int k, int H,
+                const uint16_t* shared, const float* shared_gate, const uint16_t* residual,
+                uint16_t* out, void* stream) {
+  MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && H > 0 && H % 8 == 0);
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(y_perm && pos && w && out && aligned16(y_perm) && aligned16(out));
+  MOE_REQUIRE(!shared || aligned16(shared));
+  MOE_REQUIRE(!residual || aligned16(residual));
+  return launch_combine(y_perm, pos, w, T, k, H, shared, shared_gate, residual, out,
+                        (cudaStream_t)stream);
+}
+
+size_t moe_layer_workspace_size(const moe_layer* L, int T) {
+  LayerPlan P{};
+  if (make_plan(L, T, &P) != MOE_OK) return 0;
+  WsCursor c(nullptr, 0);
+  return carve(c, L, T, P, nullptr);
+}
+
+int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_t* forced_ids,
+                      const uint16_t* residual, uint16_t* out, moe_expert_cache* cache,
+                      moe_layer_stats* st, int32_t* ids_out, float* w_out, void* ws,
+                      size_t ws_bytes, void* stream) {
+  LayerPlan P{};
+  int r = make_plan(L, T, &P);
+  if (r != MOE_OK) return r;
+  MOE_REQUIRE(L->gating >= 0 && L->gating <= 2 && L->w_r && ws);
+  MOE_REQUIRE(!L->Is || L->shared_bundle);
+  MOE_REQUIRE(!(L->Is && L->shared_gate_sigmoid) || L->w_gate);
+  MOE_REQUIRE(cache || L->bundles);
+  MOE_REQUIRE(!cache || (cache->E == L->E && L->layer_index >= 0 && L->layer_index < cache->L &&
+                         cache->slot_bytes >= P.lay.total_bytes));
+  if (st) std::memset(st, 0, sizeof(*st));
+  if (T == 0) return MOE_OK;
+  MOE_REQUIRE(x && out && aligned16(x) && aligned16(out));
+  cudaStream_t s0 = (cudaStream_t)stream;
+  WsCursor c(ws, ws_bytes);
+  LayerScratch s{};
+  carve(c, L, T, P, &s);
+  MOE_REQUIRE(c.ok());
+
+  // A1-A4: route, dispatch and gather into expert order
+  RouteArgs ra{};
+  ra.x = x; ra.w_r = L->w_r; ra.logit_bias = L->logit_bias; ra.sel_bias = L->sel_bias;
+  ra.w_gate = (L->Is && L->shared_gate_sigmoid) ? L->w_gate : nullptr;
+  ra.forced = forced_ids; ra.T = T; ra.H = L->H; ra.E = L->E; ra.k = L->k;
+  ra.gating = L->gating; ra.scale = L->scale; ra.ids = s.ids; ra.counts = s.counts;
+  ra.offsets = s.offsets; ra.pos = s.pos; ra.src = s.src; ra.tie_flags = s.tie; ra.w = s.w;
+  ra.logits = nullptr; ra.shared_gate = s.shared_gate; ra.x_perm = s.x_perm;
+  r = launch_route(ra, P.rp, s.rs, s0);
+  if (r != MOE_OK) return r;
+  const float* sgate = (L->Is && L->shared_gate_sigmoid) ? s.shared_gate : nullptr;
+
+  if (!cache) {
+    BundleTable tab{};
+    for (int e = 0; e < L->E; ++e) tab.p[e] = L->bundles[e];
+    if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
+    if ((r = run_experts(L, P, s, tab, T, -1, nullptr, s0)) != MOE_OK) return r;
+  } else {
+    // A5: the layer's expert-use mask crosses to the host, the LRU decides, misses are copied
+    // on the cache's copy stream while the shared expert and the hit experts compute.
+    MOE_CUDA_TRY(cudaMemcpyAsync(cache->host_counts, s.counts, sizeof(int32_t) * L->E,
+                                 cudaMemcpyDeviceToHost, s0));
+    MOE_CUDA_TRY(cudaEventRecord(cache->d2h, s0));
+    if ((r = cache_wait_event(cache, cache->d2h)) != MOE_OK) return r;
+    uint8_t used[kMaxExperts];
+    for (int e = 0; e < L->E; ++e) used[e] = cache->host_counts[e] > 0;
+    const void* ptrs[kMaxExperts];
+    std::vector<int> hits, misses;
+    r = cache_request_split(cache, L->layer_index, used, s0, ptrs, &hits, &misses);
+    if (r != MOE_OK) return r;
+    BundleTable tab{};
+    for (int e = 0; e < L->E; ++e) tab.p[e] = ptrs[e];
+    if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
+    if (!hits.empty() &&
+        (r = run_experts(L, P, s, tab, T, (int)hits.size(), hits.data(), s0)) != MOE_OK)
+      return r;
+    if (!misses.empty()) {
+      MOE_CUDA_TRY(cudaStreamWaitEvent(s0, cache->last_copy, 0));
+      if ((r = run_experts(L, P, s, tab, T, (int)misses.size(), misses.data(), s0)) != MOE_OK)
+        return r;
+    }
+    if (st) {
+      st->n_unique = (int32_t)(hits.size() + misses.size());
+      st->n_missed = (int32_t)misses.size();
+    }
+  }
+  // A9
+  r = launch_combine(s.y_perm, s.pos, s.w, T, L->k, L->H, L->Is ? s.s : nullptr, sgate,
+                     residual, out, s0);
+  if (r != MOE_OK) return r;
+  if (cache) {
+    MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[L->layer_index], s0));
+    cache->layer_done_valid[L->layer_index] = 1;
+  }
+  if (ids_out)
+    MOE_CUDA_TRY(cudaMemcpyAsync(ids_out, s.ids, sizeof(int32_t) * T * L->k,
+                                 cudaMemcpyDeviceToDevice, s0));
+  if (w_out)
+    MOE_CUDA_TRY(cudaMemcpyAsync(w_out, s.w, sizeof(float) * T * L->k,
+                                 cudaMemcpyDeviceToDevice, s0));
+  return MOE_OK;
+}
+
+}  // extern "C"

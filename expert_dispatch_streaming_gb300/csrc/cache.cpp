@@ -1,0 +1,321 @@
+// Expert-slot cache: fixed VRAM slots filled on demand from pinned host bundles.
+//
+// Pages: "Running 35B MoE Models on 8GB GPUs: How vvllm-ms Caches Experts in System RAM",
+// section "Technical Insight" (router output is intercepted before expert computation,
+// residency of each expert bundle is checked, misses evict the least-recently-used bundles);
+// "The Billion-Token Bottleneck", sections "Tiered Memory" (HBM hot tier over a host tier)
+// and "2. Async Weight Streaming" (cudaMemcpyAsync of a missing expert's weights);
+// "NovaLLM: Running Massive MoE Models Fully In-Memory", "Optimization #2" (every bundle stays
+// resident in pinned host memory, so an evicted slot is simply dropped).
+//
+// Ordering on the GPU, without any host wait in the steady state:
+//  - a fill of slot s runs on the cache's copy stream after the event recorded when the
+//    layer that last read s released it (write-after-read guard);
+//  - each fill records ready[s]; compute work that reads s waits on it (or on last_copy,
+//    which follows every fill issued so far, since fills are serialised on one stream).
+// Every host wait on the GPU is a polling loop with a deadline (MOE_ERR_TIMEOUT).
+#include "cache.h"
+
+#include <chrono>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+#include "common.cuh"
+#include "route.cuh"
+
+namespace moe {
+
+int cache_wait_event(moe_expert_cache* c, cudaEvent_t ev) {
+  const auto t0 = std::chrono::steady_clock::now();
+  for (long spin = 0;; ++spin) {
+    const cudaError_t r = cudaEventQuery(ev);
+    if (r == cudaSuccess) return MOE_OK;
+    if (r != cudaErrorNotReady) return fail_cuda(r);
+    if (std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(c->timeout_ms))
+      return MOE_ERR_TIMEOUT;
+    if (spin > 64) std::this_thread::yield();
+  }
+}
+
+static void destroy_all(moe_expert_cache* c) {
+  if (!c) return;
+  int cur = -1;
+  cudaGetDevice(&cur);
+  cudaSetDevice(c->device);
+  if (c->copy) cudaStreamSynchronize(c->copy);
+  for (auto e : c->ready) if (e) cudaEventDestroy(e);
+  for (auto e : c->layer_done) if (e) cudaEventDestroy(e);
+  if (c->last_copy) cudaEventDestroy(c->last_copy);
+  if (c->d2h) cudaEventDestroy(c->d2h);
+  if (c->copy) cudaStreamDestroy(c->copy);
+  if (c->slab) cudaFree(c->slab);
+  if (c->host_counts) cudaFreeHost(c->host_counts);
+  if (cur >= 0) cudaSetDevice(cur);
+  delete c;
+}
+
+static long long key_of(const moe_expert_cache* c, int layer, int e) {
+  return (long long)layer * c->E + e;
+}
+
+// Picks the slot for a missing key: lowest free slot, else the LRU key not touched by this
+// request (touched keys sit at the MRU end, so this is the LRU key).
+static int take_slot(moe_expert_cache* c, long long req, int* vl, int* ve) {
+  *vl = *ve = -1;
+  if (!c->free_slots.empty()) {
+    const int s = *c->free_slots.begin();
+    c->free_slots.erase(c->free_slots.begin());
+    return s;
+  }
+  for (auto it = c->order.begin(); it != c->order.end(); ++it) {
+    const long long k = *it;
+    const int s = c->where[k].first;
+    if (c->slot_fill_req[s] == req) continue;  // (defensive) never a key of this request
+    *vl = (int)(k / c->E);
+    *ve = (int)(k % c->E);
+    c->where.erase(k);
+    c->order.erase(it);
+    c->slot_key[s] = -1;
+    c->st.evictions++;
+    return s;
+  }
+  return -1;
+}
+
+int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cudaStream_t compute,
+                        const void** slot_ptrs, std::vector<int>* hits,
+                        std::vector<int>* misses) {
+  if (!c || !used || layer < 0 || layer >= c->L) return MOE_ERR_INVALID_ARG;
+  int n_used = 0;
+  for (int e = 0; e < c->E; ++e) n_used += used[e] != 0;
+  if (n_used > c->n_slots) return MOE_ERR_CAPACITY;
+  const long long req = c->req++;
+  c->st.requests++;
+  std::vector<int>& ls = c->layer_slots[layer];
+  ls.clear();
+  std::vector<char> touched_slot(c->n_slots, 0);
+  bool any_miss = false;
+  for (int e = 0; e < c->E; ++e) {
+    if (slot_ptrs) slot_ptrs[e] = nullptr;
+    if (!used[e]) continue;
+    const long long k = key_of(c, layer, e);
+    moe_cache_event ev{};
+    ev.request = req;
+    ev.layer = layer;
+    ev.expert = e;
+    ev.victim_layer = ev.victim_expert = -1;
+    int slot;
+    auto f = c->where.find(k);
+    if (f != c->where.end()) {
+      slot = f->second.first;
+      c->order.erase(f->second.second);
+      c->order.push_back(k);
+      f->second.second = std::prev(c->order.end());
+      ev.miss = 0;
+      c->st.hits++;
+      if (hits) hits->push_back(e);
+    } else {
+      int vl, ve;
+      slot = take_slot(c, req, &vl, &ve);
+      if (slot < 0 || touched_slot[slot]) return MOE_ERR_CAPACITY;
+      c->order.push_back(k);
+      c->where[k] = {slot, std::prev(c->order.end())};
+      c->slot_key[slot] = k;
+      c->slot_fill_req[slot] = req;
+      ev.miss = 1;
+      ev.victim_layer = vl;
+      ev.victim_expert = ve;
+      c->st.misses++;
+      c->st.bytes_h2d += (int64_t)c->slot_bytes;
+      // write-after-read guard: the victim's layer must have finished reading this slot
+      if (vl >= 0 && c->layer_done_valid[vl])
+        MOE_CUDA_TRY(cudaStreamWaitEvent(c->copy, c->layer_done[vl], 0));
+      const moe_host_bundle& hb = c->bundles[(size_t)layer * c->E + e];
+      MOE_CUDA_TRY(cudaMemcpyAsync(c->slab + (size_t)slot * c->slot_bytes, hb.ptr, hb.bytes,
+                                   cudaMemcpyHostToDevice, c->copy));
+      MOE_CUDA_TRY(cudaEventRecord(c->ready[slot], c->copy));
+      any_miss = true;
+      if (misses) misses->push_back(e);
+    }
+    touched_slot[slot] = 1;
+    ev.slot = slot;
+    ls.push_back(slot);
+    c->trace.push_back(ev);
+    if (slot_ptrs) slot_ptrs[e] = c->slab + (size_t)slot * c->slot_bytes;
+  }
+  if (any_miss) MOE_CUDA_TRY(cudaEventRecord(c->last_copy, c->copy));
+  c->st.resident = (int32_t)c->where.size();
+  (void)compute;
+  return MOE_OK;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache** out,
+                            int64_t* bad_index) {
+  if (bad_index) *bad_index = -1;
+  if (!cfg || !out || cfg->slot_bytes == 0 || cfg->n_layers <= 0 || cfg->n_experts <= 0 ||
+      cfg->n_experts > kMaxExperts || !cfg->bundles)
+    return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  const size_t nb = (size_t)cfg->n_layers * cfg->n_experts;
+  for (size_t i = 0; i < nb; ++i)
+    if (!cfg->bundles[i].ptr || cfg->bundles[i].bytes != cfg->slot_bytes)
+      return MOE_ERR_INVALID_ARG;
+  const size_t n_slots = cfg->capacity_bytes / cfg->slot_bytes;
+  if (n_slots == 0 || n_slots > (1u << 30)) return MOE_ERR_INVALID_ARG;
+
+  if (cfg->verify_checksums) {
+    // bundles are hashed in parallel; each hash is the sequential FNV-1a of one bundle
+    std::vector<char> bad(nb, 0);
+    const unsigned nt = std::max(1u, std::min(32u, std::thread::hardware_concurrency()));
+    std::vector<std::thread> th;
+    for (unsigned w = 0; w < nt; ++w)
+      th.emplace_back([&, w] {
+        for (size_t i = w; i < nb; i += nt)
+          bad[i] = moe_checksum64(cfg->bundles[i].ptr, cfg->bundles[i].bytes) !=
+                   cfg->bundles[i].checksum;
+      });
+    for (auto& t : th) t.join();
+    for (size_t i = 0; i < nb; ++i)
+      if (bad[i]) {
+        if (bad_index) *bad_index = (int64_t)i;
+        return MOE_ERR_CORRUPT;
+      }
+  }
+
+  auto* c = new moe_expert_cache();
+  c->device = cfg->device;
+  c->slot_bytes = cfg->slot_bytes;
+  c->n_slots = (int)n_slots;
+  c->L = cfg->n_layers;
+  c->E = cfg->n_experts;
+  c->timeout_ms = cfg->timeout_ms > 0 ? cfg->timeout_ms : 10000;
+  c->bundles.assign(cfg->bundles, cfg->bundles + nb);
+  int cur = -1;
+  cudaGetDevice(&cur);
+  cudaError_t err = cudaSetDevice(c->device);
+  int status = MOE_OK;
+  auto check = [&](cudaError_t e) {
+    if (e != cudaSuccess && status == MOE_OK) {
+      status = (e == cudaErrorMemoryAllocation) ? MOE_ERR_NO_MEMORY : fail_cuda(e);
+      cudaGetLastError();
+    }
+  };
+  check(err);
+  if (status == MOE_OK) check(cudaMalloc(&c->slab, n_slots * cfg->slot_bytes));
+  if (status == MOE_OK) check(cudaStreamCreateWithFlags(&c->copy, cudaStreamNonBlocking));
+  if (status == MOE_OK) check(cudaMallocHost(&c->host_counts, sizeof(int32_t) * kMaxExperts));
+  c->ready.assign(n_slots, nullptr);
+  c->layer_done.assign(c->L, nullptr);
+  for (size_t s = 0; s < n_slots && status == MOE_OK; ++s)
+    check(cudaEventCreateWithFlags(&c->ready[s], cudaEventDisableTiming));
+  for (int l = 0; l < c->L && status == MOE_OK; ++l)
+    check(cudaEventCreateWithFlags(&c->layer_done[l], cudaEventDisableTiming));
+  if (status == MOE_OK) check(cudaEventCreateWithFlags(&c->last_copy, cudaEventDisableTiming));
+  if (status == MOE_OK) check(cudaEventCreateWithFlags(&c->d2h, cudaEventDisableTiming));
+  if (cur >= 0) cudaSetDevice(cur);
+  if (status != MOE_OK) {
+    destroy_all(c);
+    return status;
+  }
+  c->layer_done_valid.assign(c->L, 0);
+  for (int s = 0; s < c->n_slots; ++s) c->free_slots.insert(s);
+  c->slot_key.assign(n_slots, -1);
+  c->slot_fill_req.assign(n_slots, -1);
+  c->layer_slots.assign(c->L, {});
+  c->st.n_slots = c->n_slots;
+  *out = c;
+  return MOE_OK;
+}
+
+int moe_expert_cache_destroy(moe_expert_cache* cache) {
+  if (!cache) return MOE_ERR_INVALID_ARG;
+  destroy_all(cache);
+  return MOE_OK;
+}
+
+int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* used_mask,
+                             void* compute, int defer_waits, const void** slot_ptrs,
+                             int32_t* n_missed) {
+  if (!cache) return MOE_ERR_INVALID_ARG;
+  std::vector<int> misses;
+  const int r = cache_request_split(cache, layer, used_mask, (cudaStream_t)compute, slot_ptrs,
+                                    nullptr, &misses);
+  if (r != MOE_OK) return r;
+  if (n_missed) *n_missed = (int32_t)misses.size();
+  if (!defer_waits && !misses.empty())
+    MOE_CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)compute, cache->last_copy, 0));
+  return MOE_OK;
+}
+
+int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert,
+                                 void* compute) {
+  if (!cache || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
+    return MOE_ERR_INVALID_ARG;
+  auto f = cache->where.find(key_of(cache, layer, expert));
+  if (f == cache->where.end()) return MOE_ERR_INVALID_ARG;
+  const int slot = f->second.first;
+  if (cache->slot_fill_req[slot] == cache->req - 1)  // filled by the latest request
+    MOE_CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)compute, cache->ready[slot], 0));
+  return MOE_OK;
+}
+
+int moe_expert_cache_release(moe_expert_cache* cache, int layer, void* compute) {
+  if (!cache || layer < 0 || layer >= cache->L) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[layer], (cudaStream_t)compute));
+  cache->layer_done_valid[layer] = 1;
+  return MOE_OK;
+}
+
+int moe_expert_cache_evict(moe_expert_cache* cache, int layer, int expert) {
+  if (!cache || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
+    return MOE_ERR_INVALID_ARG;
+  auto f = cache->where.find(key_of(cache, layer, expert));
+  if (f == cache->where.end()) return MOE_OK;
+  if (cache->layer_done_valid[layer]) {
+    const int r = cache_wait_event(cache, cache->layer_done[layer]);
+    if (r != MOE_OK) return r;
+  }
+  const int slot = f->second.first;
+  cache->order.erase(f->second.second);
+  cache->where.erase(f);
+  cache->slot_key[slot] = -1;
+  cache->free_slots.insert(slot);
+  cache->st.evictions++;
+  cache->st.resident = (int32_t)cache->where.size();
+  return MOE_OK;
+}
+
+int moe_expert_cache_trace(const moe_expert_cache* cache, moe_cache_event* buf, size_t cap,
+                           size_t* n) {
+  if (!cache || !n) return MOE_ERR_INVALID_ARG;
+  *n = cache->trace.size();
+  if (buf) std::memcpy(buf, cache->trace.data(), sizeof(moe_cache_event) * std::min(cap, *n));
+  return MOE_OK;
+}
+
+int moe_expert_cache_reset_trace(moe_expert_cache* cache) {
+  if (!cache) return MOE_ERR_INVALID_ARG;
+  cache->trace.clear();
+  return MOE_OK;
+}
+
+int moe_expert_cache_stats(const moe_expert_cache* cache, moe_cache_stats* out) {
+  if (!cache || !out) return MOE_ERR_INVALID_ARG;
+  *out = cache->st;
+  return MOE_OK;
+}
+
+int moe_expert_cache_sync(moe_expert_cache* cache) {
+  if (!cache) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA_TRY(cudaEventRecord(cache->last_copy, cache->copy));
+  return cache_wait_event(cache, cache->last_copy);
+}
+
+}  // extern "C"

@@ -1,0 +1,527 @@
+// Routing: router logits (A1), top-k gating (A2), histogram + scan + stable rank (A3) and
+// the token gather into expert-contiguous order (A4).
+//
+// The router picks a handful of experts per token and only those experts run ("NovaLLM:
+// Running Massive MoE Models Fully In-Memory", section "2. Why MoE Is a Natural Breakthrough
+// Point"); work is then grouped by expert so a batch touches each selected expert once
+// (section "3. Optimization #1 -- Expert-Level Streaming").
+//
+// Kernels
+//   router_partial_kernel  fp32 logits of a (token tile, column tile, H slice); the H slices
+//                          let a small batch spread the router read over every SM.
+//   gate_topk_kernel       one warp per token: sums the slices in fixed order, scores, picks the
+//                          top-k with warp shuffles, re-scores the experts whose fp32 score is
+//                          within the error margin of the k-th in fp64, writes ids / weights
+//                          and bumps the per-tile expert histogram.
+//   scan_kernel            one CTA: per-expert counts, exclusive offsets, per-tile bases and
+//                          the list of experts that received rows.
+//   rank_permute_kernel    one CTA per 128-token tile: stable rank of each (t, j) within its
+//                          expert from per-expert token bitmasks, pos / src, and (optionally)
+//                          the row copy x -> x_perm with 16-byte vector loads and stores.
+#include "common.cuh"
+#include "route.cuh"
+
+#include <math_constants.h>
+
+namespace moe {
+
+// fp32 selection scores within this margin of the k-th are re-scored in fp64.  The fp32
+// logit is a sum of H <= 16384 products accumulated in fp32; for the workloads' magnitudes
+// its error stays below ~1e-5, so 1e-4 leaves a wide margin (sigmoid scores move by at most
+// a quarter of the logit error).
+constexpr float kTau = 1e-4f;
+constexpr double kNearTie = 1e-6;
+
+// ------------------------------------------------------------------------------ A1 router
+constexpr int R_BT = 32, R_BC = 64, R_KH = 32;
+
+__global__ void __launch_bounds__(256)
+router_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ w_r,
+                      const uint16_t* __restrict__ w_gate, int T, int H, int E, int C,
+                      int h_per_split, float* __restrict__ part, int32_t* __restrict__ hist,
+                      int hist_n) {
+  __shared__ float xs[R_KH][R_BT + 1];
+  __shared__ float wsm[R_KH][R_BC];
+  const int tid = threadIdx.x;
+  const int ty = tid >> 4, tx = tid & 15;
+  const int t0 = blockIdx.x * R_BT, c0 = blockIdx.y * R_BC, split = blockIdx.z;
+  const int h_lo = split * h_per_split, h_hi = min(H, h_lo + h_per_split);
+
+  // the first CTA clears the per-tile histogram the gating kernel accumulates into
+  if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
+    for (int i = tid; i < hist_n; i += blockDim.x) hist[i] = 0;
+
+  float acc[2][4] = {};
+  for (int h0 = h_lo; h0 < h_hi; h0 += R_KH) {
+    // x tile: 32 tokens x 32 h (bf16 -> fp32); 256 threads x 4 elements
+    for (int i = tid; i < R_BT * R_KH; i += 256) {
+      int tt = i / R_KH, hh = i % R_KH;
+      int t = t0 + tt, h = h0 + hh;
+      xs[hh][tt] = (t < T && h < h_hi) ? bf16_bits_to_float(x[(size_t)t * H + h]) : 0.f;
+    }
+    // weight tile: 32 h x 64 columns; column E is the shared-expert gate vector
+    for (int i = tid; i < R_KH * R_BC; i += 256) {
+      int hh = i / R_BC, cc = i % R_BC;
+      int h = h0 + hh, c = c0 + cc;
+      float v = 0.f;
+      if (h < h_hi) {
+        if (c < E) v = w_r[(size_t)h * E + c];
+        else if (c < C) v = bf16_bits_to_float(w_gate[h]);
+      }
+      wsm[hh][cc] = v;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < R_KH; ++kk) {
+      float a0 = xs[kk][ty], a1 = xs[kk][ty + 16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float b = wsm[kk][tx + 16 * q];
+        acc[0][q] = fmaf(a0, b, acc[0][q]);
+        acc[1][q] = fmaf(a1, b, acc[1][q]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    int t = t0 + ty + 16 * i;
+    if (t >= T) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      int c = c0 + tx + 16 * q;
+      if (c < C) part[((size_t)split * T + t) * C + c] = acc[i][q];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------ A2 gating
+constexpr int G_WARPS = 8, G_TOK_PER_WARP = 4;
+constexpr int EC = kMaxExperts / 32;  // expert slots per lane
+
+__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
+  return sa > sb || (sa == sb && ia < ib);
+}
+__device__ __forceinline__ bool better_d(double sa, int ia, double sb, int ib) {
+  return sa > sb || (sa == sb && ia < ib);
+}
+
+__device__ __forceinline__ void warp_argmax(float& s, int& id) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float so = __shfl_xor_sync(0xffffffffu, s, o);
+    int io = __shfl_xor_sync(0xffffffffu, id, o);
+    if (better(so, io, s, id)) { s = so; id = io; }
+  }
+}
+__device__ __forceinline__ void warp_argmax_d(double& s, int& id) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    double so = __shfl_xor_sync(0xffffffffu, s, o);
+    int io = __shfl_xor_sync(0xffffffffu, id, o);
+    if (better_d(so, io, s, id)) { s = so; id = io; }
+  }
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// fp64 selection score of expert b for token t (the refinement of near-boundary experts)
+__device__ double exact_score(const GateParams& p, int t, int b, int lane) {
+  double d = 0.0;
+  const uint16_t* xr = p.x + (size_t)t * p.H;
+  for (int h = lane; h < p.H; h += 32)
+    d = fma((double)bf16_bits_to_float(xr[h]), (double)p.w_r[(size_t)h * p.E + b], d);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+  if (p.logit_bias) d += (double)p.logit_bias[b];
+  if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
+    d = 1.0 / (1.0 + exp(-d));
+    if (p.sel_bias) d += (double)p.sel_bias[b];
+  }
+  return d;
+}
+
+__global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
+  __shared__ float lrow[G_WARPS][kMaxExperts];
+  __shared__ double exact_s[G_WARPS][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = p.E, k = p.k;
+
+  for (int it = 0; it < G_TOK_PER_WARP; ++it) {
+    const int t = (blockIdx.x * G_WARPS + warp) * G_TOK_PER_WARP + it;
+    if (t >= p.T) break;
+
+    // ---- logits: fixed-order sum of the H slices (+ logit bias), scores
+    float l[EC], sc[EC];
+#pragma unroll
+    for (int c = 0; c < EC; ++c) {
+      const int e = lane + 32 * c;
+      float v = -CUDART_INF_F, s = -CUDART_INF_F;
+      if (e < E) {
+        v = 0.f;
+        for (int sp = 0; sp < p.S; ++sp) v += p.part[((size_t)sp * p.T + t) * p.C + e];
+        if (p.logit_bias) v += p.logit_bias[e];
+        s = v;
+        if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
+          s = 1.f / (1.f + expf(-v));
+          if (p.sel_bias) s += p.sel_bias[e];
+        }
+        lrow[warp][e] = v;
+        if (p.logits) p.logits[(size_t)t * E + e] = v;
+      }
+      l[c] = v;
+      sc[c] = s;
+    }
+    if (lane == 0 && p.shared_gate && p.C > E) {
+      float z = 0.f;
+      for (int sp = 0; sp < p.S; ++sp) z += p.part[((size_t)sp * p.T + t) * p.C + E];
+      p.shared_gate[t] = 1.f / (1.f + expf(-z));
+    }
+
+    bool chosen[EC];
+#pragma unroll
+    for (int c = 0; c < EC; ++c) chosen[c] = false;
+    int flag = 0;
+
+    if (p.forced == nullptr) {
+      // ---- top-(k+1) by repeated warp argmax on (score desc, id asc)
+      bool taken[EC];
+#pragma unroll
+      for (int c = 0; c < EC; ++c) taken[c] = (lane + 32 * c) >= E;
+      float selsc[kMaxK + 1];
+      int selid[kMaxK + 1];
+      const int nsel = min(k + 1, E);
+#pragma unroll
+      for (int r = 0; r < kMaxK + 1; ++r) {
+        selsc[r] = -CUDART_INF_F;
+        selid[r] = 0x7fffffff;
+        if (r < nsel) {
+          float bs = -CUDART_INF_F;
+          int bi = 0x7fffffff;
+#pragma unroll
+          for (int c = 0; c < EC; ++c) {
+            const int e = lane + 32 * c;
+            if (!taken[c] && better(sc[c], e, bs, bi)) { bs = sc[c]; bi = e; }
+          }
+          warp_argmax(bs, bi);
+          selsc[r] = bs;
+          selid[r] = bi;
+#pragma unroll
+          for (int c = 0; c < EC; ++c)
+            if (lane + 32 * c == bi) { taken[c] = true; if (r < k) chosen[c] = true; }
+        }
+      }
+      // selsc[k-1] is the k-th score, selsc[k] the best unchosen one
+      float kth = -CUDART_INF_F, nxt = -CUDART_INF_F;
+#pragma unroll
+      for (int r = 0; r < kMaxK + 1; ++r) {
+        if (r == k - 1) kth = selsc[r];
+        if (r == k) nxt = selsc[r];
+      }
+      if (k < E && kth - nxt <= kTau) {
+        // ---- refinement: experts within the margin of the boundary are re-scored in fp64
+        flag = 1;
+        bool band[EC];
+        int n_def = 0;
+#pragma unroll
+        for (int r = 0; r < kMaxK; ++r)
+          if (r < k && selsc[r] - nxt > kTau) ++n_def;
+        const float thr = kth - kTau;
+#pragma unroll
+        for (int c = 0; c < EC; ++c) {
+          const int e = lane + 32 * c;
+          bool d = false;
+#pragma unroll
+          for (int r = 0; r < kMaxK; ++r)
+            if (r < n_def && selid[r] == e) d = true;
+          band[c] = (e < E) && !d && sc[c] >= thr;
+          chosen[c] = d;
+        }
+#pragma unroll
+        for (int c = 0; c < EC; ++c) {
+          unsigned m = __ballot_sync(0xffffffffu, band[c]);
+          while (m) {
+            const int b = 32 * c + __ffs(m) - 1;
+            m &= m - 1;
+            double s = exact_score(p, t, b, lane);
+            if (lane == 0) exact_s[warp][b] = s;
+          }
+        }
+        __syncwarp();
+        const int need = k - n_def;
+        double last = CUDART_INF;
+        for (int r = 0; r < need; ++r) {
+          double bs = -CUDART_INF;
+          int bi = 0x7fffffff;
+#pragma unroll
+          for (int c = 0; c < EC; ++c) {
+            const int e = lane + 32 * c;
+            if (band[c] && !chosen[c] && better_d(exact_s[warp][e], e, bs, bi)) {
+              bs = exact_s[warp][e];
+              bi = e;
+            }
+          }
+          warp_argmax_d(bs, bi);
+          last = bs;
+#pragma unroll
+          for (int c = 0; c < EC; ++c)
+            if (lane + 32 * c == bi) chosen[c] = true;
+        }
+        // exact gap to the best band member left out
+        double bs = -CUDART_INF;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int c = 0; c < EC; ++c) {
+          const int e = lane + 32 * c;
+          if (band[c] && !chosen[c] && better_d(exact_s[warp][e], e, bs, bi)) {
+            bs = exact_s[warp][e];
+            bi = e;
+          }
+        }
+        warp_argmax_d(bs, bi);
+        if (bi != 0x7fffffff && last - bs < kNearTie) flag = 2;
+      }
+    }
+    __syncwarp();
+
+    // ---- chosen list (ascending id, or the forced order) and weights (lane 0)
+    int my_ids[kMaxK];
+    if (p.forced) {
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        my_ids[j] = j < k ? min(max(p.forced[(size_t)t * k + j], 0), E - 1) : 0;
+    } else {
+      int n = 0;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) my_ids[j] = 0;
+#pragma unroll
+      for (int c = 0; c < EC; ++c) {
+        unsigned m = __ballot_sync(0xffffffffu, chosen[c]);
+        while (m) {
+          const int e = 32 * c + __ffs(m) - 1;
+          m &= m - 1;
+#pragma unroll
+          for (int j = 0; j < kMaxK; ++j)
+            if (j == n) my_ids[j] = e;
+          ++n;
+        }
+      }
+    }
+
+    // softmax over all E needs the warp-wide max and sum
+    float M = 0.f, Ssum = 1.f;
+    if (p.mode == MOE_GATING_SOFTMAX) {
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < EC; ++c) mx = fmaxf(mx, l[c]);
+      M = warp_max(mx);
+      float s = 0.f;
+#pragma unroll
+      for (int c = 0; c < EC; ++c)
+        if (lane + 32 * c < E) s += expf(l[c] - M);
+      Ssum = warp_sum(s);
+    }
+    __syncwarp();
+    if (lane == 0) {
+      float v[kMaxK];
+      float denom = 0.f, mx = -CUDART_INF_F;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) mx = fmaxf(mx, lrow[warp][my_ids[j]]);
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        v[j] = 0.f;
+        if (j < k) {
+          const float lj = lrow[warp][my_ids[j]];
+          if (p.mode == MOE_GATING_SOFTMAX_RENORM) v[j] = expf(lj - mx);
+          else if (p.mode == MOE_GATING_SOFTMAX) v[j] = expf(lj - M);
+          else v[j] = 1.f / (1.f + expf(-lj));
+          denom += v[j];
+        }
+      }
+      if (p.mode == MOE_GATING_SOFTMAX) denom = Ssum;
+      const float inv = p.scale / denom;
+      const int tile = t / kTileT;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        if (j < k) {
+          p.ids[(size_t)t * k + j] = my_ids[j];
+          p.w[(size_t)t * k + j] = v[j] * inv;
+          atomicAdd(&p.hist[tile * E + my_ids[j]], 1);
+        }
+      }
+      if (p.tie_flags) p.tie_flags[t] = flag;
+    }
+    __syncwarp();
+  }
+}
+
+// ------------------------------------------------------------------------------ A3 scan
+__global__ void __launch_bounds__(kMaxExperts)
+scan_kernel(const int32_t* __restrict__ hist, int ntiles, int E, int32_t* __restrict__ counts,
+            int32_t* __restrict__ offsets, int32_t* __restrict__ base,
+            int32_t* __restrict__ active, int32_t* __restrict__ n_active,
+            int32_t* __restrict__ shared_meta, int T) {
+  __shared__ int s_cnt[kMaxExperts], s_flag[kMaxExperts];
+  const int e = threadIdx.x;
+  if (shared_meta && e == 0) {
+    // a one-group dispatch of all T tokens for the shared expert: offsets {0, T}, active {0}
+    shared_meta[0] = 0;
+    shared_meta[1] = T;
+    shared_meta[2] = 0;
+    shared_meta[3] = 1;
+  }
+  int run = 0;
+  if (e < E) {
+    for (int tl = 0; tl < ntiles; ++tl) {
+      const int c = hist[tl * E + e];
+      base[tl * E + e] = run;
+      run += c;
+    }
+  }
+  s_cnt[e] = e < E ? run : 0;
+  s_flag[e] = (e < E && run > 0) ? 1 : 0;
+  __syncthreads();
+  // inclusive Hillis-Steele scan of both arrays
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    int a = e >= o ? s_cnt[e - o] : 0;
+    int b = e >= o ? s_flag[e - o] : 0;
+    __syncthreads();
+    s_cnt[e] += a;
+    s_flag[e] += b;
+    __syncthreads();
+  }
+  if (e < E) {
+    const int excl = s_cnt[e] - run;
+    counts[e] = run;
+    offsets[e] = excl;
+    if (e == E - 1) offsets[E] = s_cnt[e];
+    for (int tl = 0; tl < ntiles; ++tl) base[tl * E + e] += excl;
+    if (run > 0) active[s_flag[e] - 1] = e;
+    if (e == E - 1) *n_active = s_flag[e];
+  }
+}
+
+// ------------------------------------------------------------------------------ A3+A4
+__global__ void __launch_bounds__(256)
+rank_permute_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ base, int T,
+                    int k, int E, int H, const uint16_t* __restrict__ x,
+                    int32_t* __restrict__ pos, int32_t* __restrict__ src,
+                    uint16_t* __restrict__ x_perm) {
+  __shared__ uint32_t mask[kMaxExperts][kTileT / 32];
+  __shared__ int ptmp[kTileT * kMaxK];
+  const int tile = blockIdx.x, t0 = tile * kTileT, tid = threadIdx.x;
+  const int ntok = min(kTileT, T - t0);
+  for (int i = tid; i < kMaxExperts * (kTileT / 32); i += blockDim.x) (&mask[0][0])[i] = 0u;
+  __syncthreads();
+  if (tid < ntok)
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[(size_t)(t0 + tid) * k + j];
+      atomicOr(&mask[e][tid >> 5], 1u << (tid & 31));
+    }
+  __syncthreads();
+  if (tid < ntok) {
+    const int t = t0 + tid, w = tid >> 5;
+    for (int j = 0; j < k; ++j) {
+      const int e = ids[(size_t)t * k + j];
+      int rank = __popc(mask[e][w] & ((1u << (tid & 31)) - 1u));
+      for (int q = 0; q < w; ++q) rank += __popc(mask[e][q]);
+      const int pp = base[tile * E + e] + rank;
+      pos[(size_t)t * k + j] = pp;
+      src[pp] = t * k + j;
+      ptmp[tid * k + j] = pp;
+    }
+  }
+  if (x_perm == nullptr) return;
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31, nvec = H / 8;
+  for (int q = warp; q < ntok * k; q += blockDim.x / 32) {
+    const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)(t0 + q / k) * H);
+    uint4* d = reinterpret_cast<uint4*>(x_perm + (size_t)ptmp[q] * H);
+    for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
+  }
+}
+
+// x_perm[p] = x[src[p] / k]: one warp per destination row
+__global__ void __launch_bounds__(256)
+gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src, int rows,
+                   int k, int H, uint16_t* __restrict__ x_perm) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (warp >= rows) return;
+  const int nvec = H / 8;
+  const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)(src[warp] / k) * H);
+  uint4* d = reinterpret_cast<uint4*>(x_perm + (size_t)warp * H);
+  for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
+}
+
+// ------------------------------------------------------------------------------ host side
+RoutePlan plan_route(int T, int H, int E, int k, bool has_gate) {
+  RoutePlan r{};
+  r.C = E + (has_gate ? 1 : 0);
+  r.ntiles = ceil_div(T, kTileT);
+  const int tiles = ceil_div(T, R_BT) * ceil_div(r.C, R_BC);
+  const int target = 2 * sm_count();
+  int S = 1;
+  if (tiles < target) S = std::min(std::max(1, H / 256), ceil_div(target, std::max(tiles, 1)));
+  r.h_per_split = round_up(ceil_div(H, S), R_KH);
+  r.S = ceil_div(H, r.h_per_split);
+  return r;
+}
+
+size_t route_scratch(WsCursor& c, const RoutePlan& r, int T, int E, RouteScratch* out) {
+  RouteScratch s{};
+  s.part = c.take<float>((size_t)r.S * T * r.C);
+  s.hist = c.take<int32_t>((size_t)std::max(r.ntiles, 1) * E);
+  s.base = c.take<int32_t>((size_t)std::max(r.ntiles, 1) * E);
+  s.active = c.take<int32_t>(kMaxExperts);
+  s.n_active = c.take<int32_t>(32);
+  s.shared_meta = c.take<int32_t>(32);
+  if (out) *out = s;
+  return c.used;
+}
+
+int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
+                 cudaStream_t st) {
+  if (a.T > 0) {
+    dim3 g1(ceil_div(a.T, R_BT), ceil_div(r.C, R_BC), r.S);
+    router_partial_kernel<<<g1, 256, 0, st>>>(a.x, a.w_r, a.w_gate, a.T, a.H, a.E, r.C,
+                                              r.h_per_split, s.part, s.hist, r.ntiles * a.E);
+    MOE_LAUNCH_CHECK();
+    GateParams p{};
+    p.part = s.part; p.S = r.S; p.C = r.C;
+    p.x = a.x; p.w_r = a.w_r; p.logit_bias = a.logit_bias; p.sel_bias = a.sel_bias;
+    p.forced = a.forced; p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.mode = a.gating;
+    p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
+    p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = s.hist;
+    const int per_cta = G_WARPS * G_TOK_PER_WARP;
+    gate_topk_kernel<<<ceil_div(a.T, per_cta), G_WARPS * 32, 0, st>>>(p);
+    MOE_LAUNCH_CHECK();
+  }
+  scan_kernel<<<1, kMaxExperts, 0, st>>>(s.hist, r.ntiles, a.E, a.counts, a.offsets, s.base,
+                                         s.active, s.n_active, s.shared_meta, a.T);
+  MOE_LAUNCH_CHECK();
+  if (a.T > 0) {
+    rank_permute_kernel<<<r.ntiles, 256, 0, st>>>(a.ids, s.base, a.T, a.k, a.E, a.H, a.x,
+                                                  a.pos, a.src, a.x_perm);
+    MOE_LAUNCH_CHECK();
+  }
+  return MOE_OK;
+}
+
+int launch_gather(const uint16_t* x, const int32_t* src, int rows, int k, int H,
+                  uint16_t* x_perm, cudaStream_t st) {
+  if (rows <= 0) return MOE_OK;
+  gather_rows_kernel<<<ceil_div(rows * 32, 256), 256, 0, st>>>(x, src, rows, k, H, x_perm);
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+}  // namespace moe

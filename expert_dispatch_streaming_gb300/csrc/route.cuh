@@ -1,0 +1,67 @@
+// Routing kernels' host interface (internal to libmoe).
+#pragma once
+#include "common.cuh"
+#include <algorithm>
+
+namespace moe {
+
+constexpr int kMaxExperts = 256;  // E limit (expert slots per warp lane: 8)
+constexpr int kMaxK = 8;          // top-k limit
+constexpr int kTileT = 128;       // tokens per dispatch tile (histogram granularity)
+
+struct GateParams {
+  const float* part;
+  int S, C;
+  const uint16_t* x;
+  const float* w_r;
+  const float* logit_bias;
+  const float* sel_bias;
+  const int32_t* forced;
+  int T, H, E, k, mode;
+  float scale;
+  int32_t* ids;
+  float* w;
+  float* logits;
+  float* shared_gate;
+  int32_t* tie_flags;
+  int32_t* hist;
+};
+
+struct RoutePlan {
+  int C;            // logit columns (E, + 1 for the shared-expert gate)
+  int S;            // H slices of the router product
+  int h_per_split;
+  int ntiles;       // 128-token dispatch tiles
+};
+
+struct RouteScratch {
+  float* part;      // [S][T][C]
+  int32_t* hist;    // [ntiles][E]
+  int32_t* base;    // [ntiles][E]
+  int32_t* active;  // [E] experts with rows, ascending
+  int32_t* n_active;
+  int32_t* shared_meta;  // {0, T, 0, 1}: offsets / active list / count of the shared expert
+};
+
+struct RouteArgs {
+  const uint16_t* x;
+  const float* w_r;
+  const float* logit_bias;
+  const float* sel_bias;
+  const uint16_t* w_gate;
+  const int32_t* forced;
+  int T, H, E, k, gating;
+  float scale;
+  int32_t *ids, *counts, *offsets, *pos, *src, *tie_flags;
+  float *w, *logits, *shared_gate;
+  uint16_t* x_perm;  // nullable: fused gather into expert order
+};
+
+RoutePlan plan_route(int T, int H, int E, int k, bool has_gate);
+size_t route_scratch(WsCursor& c, const RoutePlan& r, int T, int E, RouteScratch* out);
+int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
+                 cudaStream_t st);
+int launch_gather(const uint16_t* x, const int32_t* src, int rows, int k, int H,
+                  uint16_t* x_perm, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,318 @@
+/*
+ * moe.h -- C ABI of libmoe: the Mixture-of-Experts layer forward with an expert-slot cache,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The layer (pages: "NovaLLM: Running Massive MoE Models Fully In-Memory", sections
+ * "2. Why MoE Is a Natural Breakthrough Point" and "3. Optimization #1 -- Expert-Level
+ * Streaming"; "Running 35B MoE Models on 8GB GPUs: How vvllm-ms Caches Experts in System
+ * RAM", section "Technical Insight") runs, per call:
+ *
+ *   router logits -> top-k gating -> per-expert histogram + prefix scan -> permutation into
+ *   expert-contiguous order -> grouped SwiGLU expert FFN -> gate-weighted combine,
+ *
+ * fed, when a cache is attached, by fixed VRAM slots that hold expert bundles copied on
+ * demand from pinned host memory under LRU eviction.
+ *
+ * Conventions (every entry point):
+ *  - Returns an int status: MOE_OK (0) or a negative MOE_ERR_* code.  No C++ exception
+ *    crosses this boundary.  After MOE_ERR_CUDA, moe_last_cuda_error() returns the
+ *    cudaError_t value that caused it.
+ *  - The caller owns every device and host buffer passed in (allocated however it likes);
+ *    the library never frees them.  Scratch memory is a caller-provided device buffer `ws`
+ *    of at least the bytes reported by the matching *_workspace_size() query; its contents
+ *    on entry do not matter and it must not be shared by calls that overlap on the GPU.
+ *    The only objects the library allocates are expert caches (moe_expert_cache_*).
+ *  - Device work is enqueued on the caller's CUDA stream `stream` (a cudaStream_t passed
+ *    as void*; NULL = the legacy default stream) and the call returns without waiting,
+ *    except where a function says it waits.
+ *  - Pointers documented "device" must be device-accessible global memory; "host" are
+ *    ordinary host pointers.  Device buffers must be 16-byte aligned; row strides are the
+ *    row lengths stated (dense, row-major).
+ *  - bf16 values are passed as uint16_t bit patterns.  INT4 weights are two's-complement
+ *    codes in [-7, 7], two per byte, the even reduction index in the low nibble.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ------------------------------------------------------------------ status codes */
+enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = -1, /* a null pointer, bad size, unsupported shape or misalignment */
+  MOE_ERR_CUDA = -2,        /* a CUDA runtime call failed; see moe_last_cuda_error()       */
+  MOE_ERR_CAPACITY = -3,    /* a cache request needs more distinct bundles than slots      */
+  MOE_ERR_TIMEOUT = -4,     /* a bounded host wait on GPU work ran out of time             */
+  MOE_ERR_CORRUPT = -5,     /* a host bundle failed its checksum at cache creation         */
+  MOE_ERR_UNSUPPORTED = -6, /* valid request this build does not implement                 */
+  MOE_ERR_NO_MEMORY = -7    /* the cache could not allocate its VRAM slots or events       */
+};
+
+/* The cudaError_t value of the last MOE_ERR_CUDA on this thread (0 if none). */
+int moe_last_cuda_error(void);
+/* A static string naming a status code. */
+const char* moe_status_string(int status);
+/* Library version, (major << 16) | minor. */
+int moe_version(void);
+
+/* ------------------------------------------------------------------ enums */
+/* Gating of the router scores (the workloads' three families):
+ *  SOFTMAX_RENORM:      choose top-k by logit; w = softmax over the chosen k   (Mixtral shape)
+ *  SOFTMAX:             choose top-k by logit; w = softmax over all E           (Qwen1.5-MoE)
+ *  SIGMOID_BIAS_RENORM: s = sigmoid(logit); choose top-k by s + sel_bias;
+ *                       w = s / sum of the chosen s                            (DeepSeek-V3)
+ * In every mode w is then multiplied by `scale`.  Selection order: larger score first, ties to
+ * the lower expert id.  The chosen set is written in ascending expert id order. */
+enum moe_gating {
+  MOE_GATING_SOFTMAX_RENORM = 0,
+  MOE_GATING_SOFTMAX = 1,
+  MOE_GATING_SIGMOID_BIAS_RENORM = 2
+};
+
+/* Expert weight storage inside a bundle. */
+enum moe_wdtype {
+  MOE_W_BF16 = 0,      /* bf16 weights                                                   */
+  MOE_W_INT4_G128 = 1  /* symmetric INT4 codes + one bf16 scale per 128 reduction elements */
+};
+
+/* ------------------------------------------------------------------ expert bundles
+ * An expert bundle is the single unit that is stored, checksummed, cached and copied: one
+ * contiguous byte block holding everything one SwiGLU expert needs -- weights and, for INT4,
+ * their group scales -- so that weights can never arrive without their scales ("Running 35B
+ * MoE Models on 8GB GPUs ...", section "Technical Insight").
+ *
+ * Layout (every section starts on a 256-byte boundary; offsets from moe_bundle_layout):
+ *   bf16:  [ gate_up : (2I) x H  bf16 ]  rows 0..I-1 = Wg^T, rows I..2I-1 = Wu^T (K-major)
+ *          [ down    :  H x I    bf16 ]  row h = column h of Wd (K-major)
+ *   int4:  [ gate_up codes : (2I) x H/2 bytes ] [ down codes : H x I/2 bytes ]
+ *          [ gate_up scales: (2I) x H/128 bf16 ] [ down scales: H x I/128 bf16 ]
+ * Constraints: H and I multiples of 128.  */
+typedef struct moe_bundle_layout {
+  size_t total_bytes;
+  size_t gate_up_offset, down_offset;               /* weights or codes               */
+  size_t gate_up_scale_offset, down_scale_offset;   /* INT4 only, else 0              */
+} moe_bundle_layout;
+
+/* Fills *out for an expert of hidden size H, intermediate size I and storage `wdtype`.
+ * Returns MOE_ERR_INVALID_ARG unless H, I are positive multiples of 128. */
+int moe_bundle_layout_of(int H, int I, int wdtype, moe_bundle_layout* out);
+/* Size in bytes of one bundle (0 for invalid arguments). */
+size_t moe_bundle_bytes(int H, int I, int wdtype);
+
+/* Packs one expert from its logical host tensors into a host bundle `dst` of
+ * moe_bundle_bytes() bytes (host memory, caller-owned; pinned or not).
+ *  bf16: wg, wu: [H][I] uint16 bf16 bits; wd: [I][H]; scale arguments NULL.
+ *  int4: wg, wu: [H][I] int8 codes in [-7,7]; wd: [I][H] int8 codes;
+ *        sg, su: [H/128][I] bf16 bits (scale of group h/128, column i); sd: [I/128][H].
+ * Host only, synchronous.  Returns MOE_ERR_INVALID_ARG on a code outside [-7, 7]. */
+int moe_pack_bundle(int H, int I, int wdtype, const void* wg, const void* wu, const void* wd,
+                    const uint16_t* sg, const uint16_t* su, const uint16_t* sd, void* dst);
+
+/* FNV-1a 64-bit hash of `bytes` bytes of host memory (the checksum expert caches verify). */
+uint64_t moe_checksum64(const void* data, size_t bytes);
+
+/* ------------------------------------------------------------------ step 1-3: routing
+ * moe_route_topk -- router logits, top-k gating and dispatch for T tokens.
+ *
+ *  x          device [T][H] bf16 activations
+ *  w_r        device [H][E] fp32 router weight (row-major)
+ *  logit_bias device [E] fp32 added to every token's logits, or NULL
+ *  sel_bias   device [E] fp32 added to sigmoid scores for selection only, or NULL
+ *             (SIGMOID_BIAS_RENORM only)
+ *  w_gate     device [H] bf16 shared-expert gate vector, or NULL; when given,
+ *             shared_gate[t] = sigmoid(x[t] . w_gate) is written to `shared_gate` (device [T] fp32)
+ *  forced_ids device [T][k] int32 expert ids to use instead of the router's selection (each
+ *             row k distinct ids in [0,E)), or NULL.  Weights are still the gating of the
+ *             router logits at those ids.
+ *  outputs (device): ids [T][k] int32 (ascending expert id within a token unless forced),
+ *             w [T][k] fp32, counts [E] int32, offsets [E+1] int32 (exclusive scan of counts),
+ *             pos [T][k] int32 (row of (t,j) in expert-contiguous order, stable in t),
+ *             src [T*k] int32 (src[pos[t][j]] = t*k + j),
+ *             logits [T][E] fp32 or NULL (the fp32 logits incl. logit_bias),
+ *             tie_flags [T] int32 or NULL: 0 = the k-th/(k+1)-th selection gap exceeded the
+ *             fp32 error margin; 1 = the experts near the boundary were re-scored in fp64;
+ *             2 = as 1 and the fp64 gap was still below 1e-6 (a logged near-tie).
+ *  ws         device scratch of moe_route_workspace_size(T, H, E, k) bytes.
+ * Limits: 1 <= k <= min(E, 8), E <= 256, T >= 0 (T == 0 writes zero counts/offsets),
+ * H a multiple of 8.  Exact selection: near-boundary experts are re-scored in fp64 on the
+ * GPU so that the chosen set equals that of exact arithmetic whenever the exact gap is not
+ * a tie.
+ * Defined by: "NovaLLM ...", "2. Why MoE Is a Natural Breakthrough Point" (the router picks a
+ * handful of experts per token); histogram / scan / stable rank are the standard dispatch. */
+size_t moe_route_workspace_size(int T, int H, int E, int k);
+int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
+                   const float* sel_bias, const uint16_t* w_gate, const int32_t* forced_ids,
+                   int T, int H, int E, int k, int gating, float scale,
+                   int32_t* ids, float* w, int32_t* counts, int32_t* offsets, int32_t* pos,
+                   int32_t* src, float* logits, float* shared_gate, int32_t* tie_flags,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ step 4: permute
+ * x_perm[p][:] = x[src[p] / k][:] for p in [0, T*k).
+ *  x device [T][H] bf16, src device [T*k] int32, x_perm device [T*k][H] bf16.
+ * H a multiple of 8. */
+int moe_permute(const uint16_t* x, const int32_t* src, int T, int k, int H, uint16_t* x_perm,
+                void* stream);
+
+/* ------------------------------------------------------------------ step 5: expert FFN
+ * moe_grouped_swiglu -- for every expert e with rows [offsets[e], offsets[e+1]) of x_perm:
+ *   h = bf16( silu(x Wg_e) * (x Wu_e) ),  y_perm[rows] = bf16( h Wd_e ),
+ * with fp32 accumulation (INT4: code x bf16 activation products, the group scale applied
+ * in fp32 or folded into a bf16 dequantised weight, see the design notes).
+ *  x_perm   device [rows_total][H] bf16, rows_total = offsets[E]
+ *  offsets  device [E+1] int32 (from moe_route_topk)
+ *  bundles  HOST array [E] of device pointers to packed bundles (NULL allowed for experts
+ *           that receive no rows); copied into the kernel parameters, so the array may be
+ *           reused as soon as the call returns
+ *  y_perm   device [rows_total][H] bf16
+ *  max_rows an upper bound of offsets[E] (T*k), used to size the launch
+ *  ws       device scratch of moe_grouped_swiglu_workspace_size(max_rows, E, H, I, wdtype)
+ * Limits: E <= 256, H and I multiples of 128. */
+size_t moe_grouped_swiglu_workspace_size(int max_rows, int E, int H, int I, int wdtype);
+int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
+                       const void* const* bundles, int E, int H, int I, int wdtype,
+                       int max_rows, uint16_t* y_perm, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------ step 6: combine
+ * out[t] = bf16( sum_{j<k} w[t][j] * y_perm[pos[t][j]] + g_t * shared[t] ), fp32 inside,
+ * j in order 0..k-1, g_t = shared_gate[t] (1 when shared_gate is NULL; the shared term is
+ * skipped when shared is NULL).  If `residual` is not NULL, out[t] = bf16(residual[t] +
+ * that bf16 value) (the residual stream of a stacked model).
+ *  y_perm device [T*k][H] bf16; pos, w device [T][k]; shared, residual, out device [T][H]. */
+int moe_combine(const uint16_t* y_perm, const int32_t* pos, const float* w, int T, int k,
+                int H, const uint16_t* shared, const float* shared_gate,
+                const uint16_t* residual, uint16_t* out, void* stream);
+
+/* ------------------------------------------------------------------ expert-slot cache
+ * A fixed pool of VRAM slots, each holding one expert bundle, filled from pinned host
+ * bundles by cudaMemcpyAsync on the cache's own copy stream under LRU eviction ("Running 35B
+ * MoE Models on 8GB GPUs ...", section "Technical Insight"; "The Billion-Token Bottleneck",
+ * sections "Tiered Memory" and "2. Async Weight Streaming").
+ *
+ * Policy (exactly reproducible): one LRU over keys (layer, expert).  A request processes its
+ * distinct experts in ascending id order; a hit moves the key to most-recently-used; a miss
+ * takes the lowest free slot, else evicts the least-recently-used key (never one this request
+ * already touched).  Eviction drops the slot (the pinned host copy stays).  A request that
+ * needs more distinct bundles than there are slots fails with MOE_ERR_CAPACITY and changes
+ * nothing. */
+typedef struct moe_expert_cache moe_expert_cache;
+
+typedef struct moe_host_bundle {
+  const void* ptr;    /* host bundle (pinned memory for asynchronous copies)          */
+  size_t bytes;       /* must equal the cache's slot_bytes                             */
+  uint64_t checksum;  /* moe_checksum64 of the bundle, verified at creation            */
+} moe_host_bundle;
+
+typedef struct moe_expert_cache_config {
+  size_t slot_bytes;        /* bytes of one bundle (moe_bundle_bytes)                  */
+  size_t capacity_bytes;    /* VRAM budget: n_slots = capacity_bytes / slot_bytes       */
+  int n_layers, n_experts;  /* key space                                               */
+  const moe_host_bundle* bundles; /* host array [n_layers * n_experts], layer-major    */
+  int timeout_ms;           /* deadline of every bounded host wait (<= 0: 10000 ms)     */
+  int verify_checksums;     /* 1: hash every bundle at creation (MOE_ERR_CORRUPT)      */
+  int device;               /* CUDA device ordinal of the slots                        */
+} moe_expert_cache_config;
+
+/* One trace record per distinct expert of every request, in processing order. */
+typedef struct moe_cache_event {
+  int64_t request;          /* running request number                                  */
+  int32_t layer, expert;
+  int32_t miss;             /* 0 = hit, 1 = miss                                       */
+  int32_t victim_layer, victim_expert;  /* -1 when no key was evicted                  */
+  int32_t slot;
+} moe_cache_event;
+
+typedef struct moe_cache_stats {
+  int64_t requests, hits, misses, evictions;
+  int64_t bytes_h2d;        /* = misses * slot_bytes                                   */
+  int32_t n_slots, resident;
+} moe_cache_stats;
+
+/* Creates a cache: allocates n_slots slots in one device allocation, a non-blocking copy
+ * stream and per-slot events, and (verify_checksums) hashes every host bundle.
+ * Errors: MOE_ERR_INVALID_ARG; MOE_ERR_CORRUPT when a bundle's hash differs from its
+ * checksum (the index of the first bad bundle goes to *bad_index when not NULL);
+ * MOE_ERR_NO_MEMORY; MOE_ERR_CUDA.  Nothing is left allocated on failure. */
+int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache** out,
+                            int64_t* bad_index);
+int moe_expert_cache_destroy(moe_expert_cache* cache);
+
+/* Makes every expert whose used_mask[e] != 0 resident for `layer`.  used_mask: HOST [E] bytes.
+ * On return slot_ptrs[e] (HOST array [E], caller-owned) holds the device address of expert
+ * e's bundle for every used e (NULL for unused e).  Misses are copied on the cache's copy
+ * stream, each after the previous readers of its slot have finished (write-after-read
+ * guard, per-slot last-use events).  If defer_waits == 0, stream `compute` is made to wait
+ * for every copied bundle before any work enqueued on it after this call; if defer_waits
+ * == 1 the caller adds those waits per expert with moe_expert_cache_wait_expert (so work on
+ * hit experts can start while misses are in flight).  n_missed (nullable) receives the
+ * number of misses.  Host-side and non-blocking. */
+int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* used_mask,
+                             void* compute, int defer_waits, const void** slot_ptrs,
+                             int32_t* n_missed);
+/* Makes stream `compute` wait until (layer, expert)'s bundle has arrived (no-op for a hit). */
+int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert, void* compute);
+/* Marks the end of `layer`'s use of its slots on stream `compute` (records last-use events
+ * that later copies into those slots wait for). */
+int moe_expert_cache_release(moe_expert_cache* cache, int layer, void* compute);
+/* Drops (layer, expert) from the cache; no-op when not resident.  Waits (bounded) for the
+ * slot's last reader. */
+int moe_expert_cache_evict(moe_expert_cache* cache, int layer, int expert);
+/* Copies up to `cap` trace records (oldest first, since creation or the last reset) into
+ * `buf` (host); *n receives the number of records available. */
+int moe_expert_cache_trace(const moe_expert_cache* cache, moe_cache_event* buf, size_t cap,
+                           size_t* n);
+int moe_expert_cache_reset_trace(moe_expert_cache* cache);
+int moe_expert_cache_stats(const moe_expert_cache* cache, moe_cache_stats* out);
+/* Bounded wait until every copy issued so far has completed (MOE_ERR_TIMEOUT on deadline). */
+int moe_expert_cache_sync(moe_expert_cache* cache);
+
+/* ------------------------------------------------------------------ whole layer */
+typedef struct moe_layer {
+  int H, E, k, I, Is;        /* Is = shared-expert intermediate size, 0 = none          */
+  int gating;                /* enum moe_gating                                          */
+  float scale;               /* routed weight multiplier                                 */
+  int wdtype;                /* enum moe_wdtype of routed and shared bundles            */
+  int layer_index;           /* cache key                                                */
+  int shared_gate_sigmoid;   /* 1: shared term scaled by sigmoid(x . w_gate), 0: by 1   */
+  const float* w_r;          /* device [H][E] fp32                                       */
+  const float* logit_bias;   /* device [E] fp32 or NULL                                  */
+  const float* sel_bias;     /* device [E] fp32 or NULL                                  */
+  const uint16_t* w_gate;    /* device [H] bf16, required when shared_gate_sigmoid       */
+  const void* shared_bundle; /* device bundle of the shared expert (H, Is), or NULL      */
+  const void* const* bundles;/* HOST array [E] of device bundles (all resident), or NULL
+                                when a cache is attached                                 */
+} moe_layer;
+
+typedef struct moe_layer_stats {
+  int32_t n_unique;          /* distinct experts used by this call                       */
+  int32_t n_missed;          /* cache misses (0 without a cache)                         */
+  int32_t n_refined;         /* tokens whose selection was re-scored in fp64 (needs sync) */
+} moe_layer_stats;
+
+/* Bytes of scratch moe_layer_forward needs for T tokens. */
+size_t moe_layer_workspace_size(const moe_layer* L, int T);
+
+/* The whole layer forward: out[T][H] (device bf16) from x[T][H] (device bf16).
+ *  forced_ids device [T][k] or NULL (routing trace injection, see moe_route_topk)
+ *  residual   device [T][H] bf16 or NULL (out = residual + layer output, see moe_combine)
+ *  cache      NULL: every bundle is resident (L->bundles); else bundles come from the cache:
+ *             the call reads the layer's expert-use mask back to the host (one small
+ *             device-to-host copy and a bounded wait), requests residency, and overlaps the
+ *             miss copies with the shared expert and with the experts that hit.
+ *  st         host, or NULL.
+ *  ids_out, w_out  device [T][k] or NULL: copies of the routing decision.
+ * With cache == NULL the call is fully asynchronous. */
+int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_t* forced_ids,
+                      const uint16_t* residual, uint16_t* out, moe_expert_cache* cache,
+                      moe_layer_stats* st, int32_t* ids_out, float* w_out, void* ws,
+                      size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,253 @@
+"""GPU parity: every step of the MoE layer, called through the C ABI, against the CPU oracle.
+
+Bit-exact: routing ids (except near-ties), counts, offsets, pos, src, the permuted rows.
+Tolerance (floating point): max |err| <= 2e-2 max |ref|, sum |err| / sum |ref| <= 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import bf16, moe_ref
+
+from gpu_util import assert_close, check_ids, oracle_scores
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    from expert_dispatch_streaming_gb300 import build
+    build.build()
+    import expert_dispatch_streaming_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def syn(moe):
+    from expert_dispatch_streaming_gb300 import synthetic
+    return synthetic
+
+
+SMALL = [
+    wl.TINY,
+    wl.custom("ragged", H=256, E=8, k=2, I=384),
+    wl.custom("qwenlike", cfg_id=101, H=512, E=60, k=4, I=256, gating="softmax", Is=384,
+              shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit"),
+    wl.custom("dslike", cfg_id=102, H=512, E=256, k=8, I=256, gating="sigmoid_bias_renorm",
+              scale=2.5, Is=256, shared_gate="one", wdtype="int4_g128", zipf_s=1.1,
+              bias_kind="select"),
+    wl.custom("int4small", cfg_id=103, H=256, E=16, k=4, I=384, gating="softmax_renorm",
+              wdtype="int4_g128"),
+]
+
+
+def _route(moe, cfg, T, forced=None):
+    dev = "cuda"
+    from expert_dispatch_streaming_gb300.synthetic import to_device_bits
+    xb = wl.tokens(cfg, T)
+    x = to_device_bits(xb)
+    w_r = torch.from_numpy(wl.router(cfg, 0)).to(dev)
+    b = wl.popularity_bias(cfg, 0)
+    lb = torch.from_numpy(b).to(dev) if (b is not None and cfg.bias_kind == "logit") else None
+    sb = torch.from_numpy(b).to(dev) if (b is not None and cfg.bias_kind == "select") else None
+    wsv = wl.shared_gate_vector(cfg, 0)
+    wg = to_device_bits(wsv) if wsv is not None else None
+    E, k = cfg.E, cfg.k
+    i32 = dict(dtype=torch.int32, device=dev)
+    ids = torch.full((T, k), -1, **i32)
+    w = torch.zeros((T, k), dtype=torch.float32, device=dev)
+    counts = torch.zeros(E, **i32)
+    offsets = torch.zeros(E + 1, **i32)
+    pos = torch.full((T, k), -1, **i32)
+    src = torch.full((T * k,), -1, **i32)
+    logits = torch.zeros((T, E), dtype=torch.float32, device=dev)
+    sg = torch.zeros(T, dtype=torch.float32, device=dev) if wg is not None else None
+    tie = torch.zeros(T, **i32)
+    nws = moe.moe_route_workspace_size(T, cfg.H, E, k)
+    ws = torch.empty(nws, dtype=torch.uint8, device=dev)
+    f = torch.from_numpy(np.ascontiguousarray(forced, np.int32)).to(dev) if forced is not None else None
+    moe.moe_route_topk(x, w_r, lb, sb, wg, f, T, cfg.H, E, k, cfg.gating, cfg.scale, ids, w,
+                       counts, offsets, pos, src, logits, sg, tie, ws, nws)
+    torch.cuda.synchronize()
+    out = dict(ids=ids.cpu().numpy(), w=w.cpu().numpy(), counts=counts.cpu().numpy(),
+               offsets=offsets.cpu().numpy(), pos=pos.cpu().numpy(), src=src.cpu().numpy(),
+               logits=logits.cpu().numpy(), tie=tie.cpu().numpy(),
+               sg=sg.cpu().numpy() if sg is not None else None)
+    return xb, out
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+@pytest.mark.parametrize("T", [1, 3, 17, 130, 300])
+def test_route_topk_dispatch(moe, cfg, T):
+    xb, g = _route(moe, cfg, T)
+    l, s = oracle_scores(cfg, xb)
+    assert np.abs(g["logits"] - l).max() < 1e-3
+    check_ids(cfg, g["ids"], g["tie"], xb)
+    # second stage: dispatch of the GPU's own ids must match the definition bit for bit
+    counts, offsets, pos, src = moe_ref.dispatch(g["ids"], cfg.E)
+    assert np.array_equal(g["counts"], counts) and np.array_equal(g["offsets"], offsets)
+    assert np.array_equal(g["pos"], pos) and np.array_equal(g["src"], src)
+    w_ref = moe_ref.gate_weights(l, g["ids"], cfg.gating, cfg.scale)
+    assert np.abs(g["w"] - w_ref).max() <= 1e-5 * max(1.0, cfg.scale)
+    if g["sg"] is not None:
+        x = bf16.decode(xb)
+        ref = moe_ref.sigmoid(x @ bf16.decode(wl.shared_gate_vector(cfg, 0)))
+        assert np.abs(g["sg"] - ref).max() < 1e-5
+
+
+def test_route_forced_ids(moe):
+    cfg = SMALL[2]
+    T = 37
+    rng = np.random.default_rng(5)
+    forced = np.stack([rng.choice(cfg.E, cfg.k, replace=False) for _ in range(T)]).astype(np.int32)
+    xb, g = _route(moe, cfg, T, forced=forced)
+    assert np.array_equal(g["ids"], forced)
+    l, _ = oracle_scores(cfg, xb)
+    assert np.abs(g["w"] - moe_ref.gate_weights(l, forced, cfg.gating, cfg.scale)).max() < 1e-5
+    counts, offsets, pos, src = moe_ref.dispatch(forced, cfg.E)
+    assert np.array_equal(g["pos"], pos) and np.array_equal(g["src"], src)
+
+
+def test_route_near_tie_refinement(moe):
+    # duplicate router columns: experts 1 and 2 tie exactly for every token, so the fp32
+    # margin test must send every token to fp64 re-scoring and report a near-tie
+    cfg = wl.custom("ties", H=256, E=8, k=2, I=128)
+    import workloads
+    w = wl.router(cfg, 0).copy()
+    w[:, 2] = w[:, 1]
+    w[:, 5] = w[:, 1] + 1.0                      # expert 5 always wins the first place
+    orig = workloads.router
+    workloads.router = lambda c, layer=0: w
+    try:
+        xb, g = _route(moe, cfg, 40)
+    finally:
+        workloads.router = orig
+    assert np.all(g["tie"] == 2)
+    assert np.all(g["ids"][:, 1] == 5) and np.all(g["ids"][:, 0] == 1)   # tie -> lower id
+
+
+@pytest.mark.parametrize("T,k,H", [(1, 2, 256), (37, 4, 512), (300, 8, 7168)])
+def test_permute_bit_exact(moe, T, k, H):
+    rng = np.random.default_rng(T)
+    x = torch.from_numpy(rng.integers(-32768, 32767, (T, H), dtype=np.int16)).cuda()
+    src = torch.from_numpy(rng.permutation(T * k).astype(np.int32)).cuda()
+    out = torch.empty((T * k, H), dtype=torch.int16, device="cuda")
+    moe.moe_permute(x, src, T, k, H, out)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), x.cpu()[src.cpu().long() // k])
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+def test_grouped_swiglu(moe, syn, cfg):
+    T = 57
+    xb, g = _route(moe, cfg, T)
+    x = bf16.decode(xb)
+    rows = T * cfg.k
+    x_perm = torch.from_numpy(xb.view(np.int16)[g["src"] // cfg.k].copy()).cuda()
+    offsets = torch.from_numpy(g["offsets"]).cuda()
+    dl = syn.DeviceLayer(cfg)
+    y = torch.zeros((rows, cfg.H), dtype=torch.int16, device="cuda")
+    nws = moe.moe_grouped_swiglu_workspace_size(rows, cfg.E, cfg.H, cfg.I, cfg.wdtype)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    moe.moe_grouped_swiglu(x_perm, offsets, [dl.routed[e] for e in range(cfg.E)], cfg.E, cfg.H,
+                           cfg.I, cfg.wdtype, rows, y, ws, nws)
+    torch.cuda.synchronize()
+    y = y.cpu().numpy().view(np.uint16)
+    ref = np.zeros((rows, cfg.H))
+    for e in range(cfg.E):
+        lo, hi = g["offsets"][e], g["offsets"][e + 1]
+        if hi > lo:
+            wg, wu, wd = moe_ref.expert_matrices(wl.expert(cfg, 0, e))
+            ref[lo:hi], _ = moe_ref.swiglu_ffn(x[g["src"][lo:hi] // cfg.k], wg, wu, wd)
+    assert_close(y, ref, f"{cfg.name} y_perm")
+
+
+def test_combine(moe):
+    rng = np.random.default_rng(3)
+    T, k, H = 77, 4, 512
+    y = wl.bf16_bits_from_f32(rng.standard_normal((T * k, H)).astype(np.float32))
+    s = wl.bf16_bits_from_f32(rng.standard_normal((T, H)).astype(np.float32))
+    res = wl.bf16_bits_from_f32(rng.standard_normal((T, H)).astype(np.float32))
+    pos = rng.permutation(T * k).astype(np.int32).reshape(T, k)
+    w = rng.random((T, k)).astype(np.float32)
+    gate = rng.random(T).astype(np.float32)
+    d = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a).cuda()  # noqa
+    out = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    out2 = torch.empty((T, H), dtype=torch.int16, device="cuda")
+    moe.moe_combine(d(y), d(pos), d(w), T, k, H, d(s), d(gate), None, out)
+    moe.moe_combine(d(y), d(pos), d(w), T, k, H, d(s), d(gate), d(res), out2)
+    torch.cuda.synchronize()
+    ref = moe_ref.combine(bf16.decode(y), pos, w.astype(np.float64), bf16.decode(s),
+                          gate.astype(np.float64))
+    got = out.cpu().numpy().view(np.uint16)
+    assert_close(got, ref, "combine")
+    # fp32 accumulation vs fp64: at most one bf16 step apart
+    assert np.mean(bf16.decode(got) == ref) > 0.98
+    ref2 = bf16.round_rne(bf16.decode(res) + ref)
+    assert_close(out2.cpu().numpy().view(np.uint16), ref2, "combine+residual")
+
+
+def _layer_case(syn, cfg, T, rows=None, check_selection=True):
+    dl = syn.DeviceLayer(cfg)
+    xb = wl.tokens(cfg, T)
+    x = syn.to_device_bits(xb)
+    ws = dl.workspace(T)
+    ids = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    out, _ = dl.forward(x, ws, ids_out=ids)
+    out2, _ = dl.forward(x, ws)
+    torch.cuda.synchronize()
+    got = syn.bits_of(out)
+    assert np.array_equal(got, syn.bits_of(out2)), "second run differs (nondeterminism)"
+    ids = ids.cpu().numpy()
+    if check_selection:
+        check_ids(cfg, ids, None, xb)
+    ref = moe_ref.layer_forward(cfg, 0, xb, forced_ids=ids, rows=rows)
+    sel = ref["rows"]
+    return assert_close(got[sel], ref["out"], f"{cfg.name} T={T}")
+
+
+@pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
+@pytest.mark.parametrize("T", [1, 16, 133])
+def test_layer_forward_small(syn, cfg, T):
+    _layer_case(syn, cfg, T)
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_layer_forward_mixtral(syn, T):
+    _layer_case(syn, wl.MIXTRAL, T)
+
+
+@pytest.mark.parametrize("T", [1, 16, 256])
+def test_layer_forward_qwen(syn, T):
+    _layer_case(syn, wl.QWEN, T)
+
+
+@pytest.mark.parametrize("T", [1, 32])
+def test_layer_forward_deepseek_int4(syn, T):
+    _layer_case(syn, wl.DEEPSEEK, T, rows=np.arange(min(T, 6)))
+
+
+def test_int4_bundle_with_foreign_scales_fails_parity(moe, syn):
+    """Scales travel with their weights: a bundle whose scale block comes from another expert
+    gives a wrong layer (the negative test of bundle atomicity)."""
+    cfg = SMALL[4]
+    hb = syn.host_bundles(cfg, 0, list(range(cfg.E)), pinned=False)
+    lay = moe.bundle_layout(cfg.H, cfg.I, cfg.wdtype)
+    a, b = lay.gate_up_scale_offset, lay.total_bytes
+    bad = hb.clone()
+    for e in range(cfg.E):
+        bad[e, a:b] = hb[(e + 1) % cfg.E, a:b]
+    T = 33
+    xb = wl.tokens(cfg, T)
+    x = syn.to_device_bits(xb)
+    good_l, bad_l = syn.DeviceLayer(cfg, bundles_override=hb), syn.DeviceLayer(cfg, bundles_override=bad)
+    ws = good_l.workspace(T)
+    ids = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    o1, _ = good_l.forward(x, ws, ids_out=ids)
+    o2, _ = bad_l.forward(x, ws)
+    torch.cuda.synchronize()
+    ref = moe_ref.layer_forward(cfg, 0, xb, forced_ids=ids.cpu().numpy())
+    assert_close(syn.bits_of(o1), ref["out"], "good bundles")
+    with pytest.raises(AssertionError):
+        assert_close(syn.bits_of(o2), ref["out"], "foreign scales")
