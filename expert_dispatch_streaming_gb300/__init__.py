@@ -85,9 +85,14 @@ class moe_layer_stats(C.Structure):
 
 
 # ----------------------------------------------------------------------------- loading
-if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run "
-                      "`python -m expert_dispatch_streaming_gb300.build`")
+from . import build as _build  # noqa: E402
+
+if not _build.up_to_date():
+    # compile in-tree on first import (nvcc is part of the toolchain on every machine used)
+    try:
+        _build.build()
+    except Exception as exc:  # no fallback path exists: fail loudly
+        raise ImportError(f"libmoe.so could not be built ({LIB_PATH}): {exc}") from exc
 _lib = C.CDLL(LIB_PATH)
 
 _vp, _i, _f, _sz = C.c_void_p, C.c_int, C.c_float, C.c_size_t

@@ -15,8 +15,6 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def moe():
-    from expert_dispatch_streaming_gb300 import build
-    build.build()
     import expert_dispatch_streaming_gb300 as m
     return m
 

@@ -17,8 +17,6 @@ pytestmark = pytest.mark.gpu
 
 @pytest.fixture(scope="module")
 def moe():
-    from expert_dispatch_streaming_gb300 import build
-    build.build()
     import expert_dispatch_streaming_gb300 as m
     return m
 
@@ -42,14 +40,14 @@ SMALL = [
 ]
 
 
-def _route(moe, cfg, T, forced=None):
+def _route(moe, cfg, T, forced=None, w_r=None, logit_bias=None):
     dev = "cuda"
     from expert_dispatch_streaming_gb300.synthetic import to_device_bits
     xb = wl.tokens(cfg, T)
     x = to_device_bits(xb)
-    w_r = torch.from_numpy(wl.router(cfg, 0)).to(dev)
-    b = wl.popularity_bias(cfg, 0)
-    lb = torch.from_numpy(b).to(dev) if (b is not None and cfg.bias_kind == "logit") else None
+    w_r = torch.from_numpy(wl.router(cfg, 0) if w_r is None else w_r).to(dev)
+    b = wl.popularity_bias(cfg, 0) if logit_bias is None else logit_bias
+    lb = torch.from_numpy(b).to(dev) if (b is not None and (cfg.bias_kind == "logit" or logit_bias is not None)) else None
     sb = torch.from_numpy(b).to(dev) if (b is not None and cfg.bias_kind == "select") else None
     wsv = wl.shared_gate_vector(cfg, 0)
     wg = to_device_bits(wsv) if wsv is not None else None
@@ -110,21 +108,17 @@ def test_route_forced_ids(moe):
 
 
 def test_route_near_tie_refinement(moe):
-    # duplicate router columns: experts 1 and 2 tie exactly for every token, so the fp32
-    # margin test must send every token to fp64 re-scoring and report a near-tie
+    # experts 1 and 2 have identical router columns and biases, expert 5 a bias far above
+    # everything: every token's k-th (2nd) place is an exact tie between 1 and 2, so every
+    # token must go through fp64 re-scoring, be logged as a near-tie and take the lower id
     cfg = wl.custom("ties", H=256, E=8, k=2, I=128)
-    import workloads
     w = wl.router(cfg, 0).copy()
     w[:, 2] = w[:, 1]
-    w[:, 5] = w[:, 1] + 1.0                      # expert 5 always wins the first place
-    orig = workloads.router
-    workloads.router = lambda c, layer=0: w
-    try:
-        xb, g = _route(moe, cfg, 40)
-    finally:
-        workloads.router = orig
+    bias = np.zeros(cfg.E, np.float32)
+    bias[5], bias[1], bias[2] = 20.0, 10.0, 10.0
+    xb, g = _route(moe, cfg, 40, w_r=w, logit_bias=bias)
     assert np.all(g["tie"] == 2)
-    assert np.all(g["ids"][:, 1] == 5) and np.all(g["ids"][:, 0] == 1)   # tie -> lower id
+    assert np.all(g["ids"][:, 0] == 1) and np.all(g["ids"][:, 1] == 5)   # ascending ids
 
 
 @pytest.mark.parametrize("T,k,H", [(1, 2, 256), (37, 4, 512), (300, 8, 7168)])
