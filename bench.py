@@ -1,0 +1,347 @@
+"""Benchmark of the MoE layer forward (libmoe on one GB300, replicas for N > 1).
+
+Headline workload: the Mixtral-8x7B-shaped MoE layer (H=4096, E=8, top-2 softmax, SwiGLU
+I=14336, bf16 weights N(0, 0.02), x ~ N(0, 1) bf16, router fp32 N(0, 0.02)), T = 4096 tokens
+per step, all experts VRAM-resident.  One step = one full layer forward (router, gating,
+dispatch, gather, grouped SwiGLU, combine) through the C ABI.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--T 4096] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  See the design notes for the roofline arithmetic.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as wl  # noqa: E402
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 7900.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            flat = {}
+
+            def walk(o, pre=""):
+                if isinstance(o, dict):
+                    for k, v in o.items():
+                        walk(v, f"{pre}{k}.")
+                elif isinstance(o, (int, float)):
+                    flat[pre[:-1]] = float(o)
+            walk(d)
+            get = lambda *names: next((flat[k] for k in flat for n in names if k.split(".")[-1] == n), None)  # noqa
+            hbm, tf, tfs = get("hbm_gbs"), get("bf16_tflops"), get("bf16_tflops_sustained")
+            if hbm and tf:
+                return {"hbm_gbs": hbm, "bf16_tflops": tf, "bf16_tflops_sustained": tfs or tf,
+                        "source": "measured"}
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS, source="fallback")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index, self.rows, self.proc = index, [], None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([c.strip() for c in line.split(",")])
+
+    def __exit__(self, *a):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm = [float(r[1]) for r in self.rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4)
+                          if len(r) > 5 + i and r[5 + i].lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
+
+
+def layer_work(cfg, T, n_unique):
+    """Algorithmic FLOPs and bytes of one layer call and of its two expert GEMMs."""
+    H, I, k, E = cfg.H, cfg.I, cfg.k, cfg.E
+    rows = T * k
+    bpw = 2.0 if cfg.wdtype == "bf16" else 0.5 + 2.0 / 128
+    gu_flops = 2.0 * rows * H * 2 * I
+    dn_flops = 2.0 * rows * I * H
+    gu_bytes = n_unique * 2 * I * H * bpw + rows * H * 2 + rows * I * 2
+    dn_bytes = n_unique * H * I * bpw + rows * I * 2 + rows * H * 2
+    flops = gu_flops + dn_flops + 2.0 * T * H * E
+    nbytes = n_unique * 3 * H * I * bpw + 4.0 * H * E + 2 * T * H * 2 + 2 * 2 * rows * H * 2
+    return dict(flops=flops, bytes=nbytes, gu=(gu_flops, gu_bytes), dn=(dn_flops, dn_bytes))
+
+
+def roofline_of(flops, nbytes, seconds, pk, sustained=False):
+    tf_peak = pk["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+    t_tc = flops / (tf_peak * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    if t_tc >= t_hbm:
+        ach = flops / seconds / 1e12
+        return {"bound": "tensor", "achieved": round(ach, 2), "peak": tf_peak, "unit": "TFLOP/s",
+                "frac": round(ach / tf_peak, 4)}
+    ach = nbytes / seconds / 1e9
+    return {"bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+            "frac": round(ach / pk["hbm_gbs"], 4)}
+
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import expert_dispatch_streaming_gb300 as moe
+    from expert_dispatch_streaming_gb300 import synthetic as syn
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    cfg = wl.MIXTRAL
+    pk = peaks()
+    layer = syn.DeviceLayer(cfg, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def measure(T, steps, warmup, with_e2e):
+        xb = wl.tokens(cfg, T)
+        x = syn.to_device_bits(xb, dev)
+        out = torch.empty_like(x)
+        ws = layer.workspace(T)
+        ids = torch.empty((T, cfg.k), dtype=torch.int32, device=dev)
+        with torch.cuda.stream(stream):
+            layer.forward(x, ws, out, stream=stream, ids_out=ids)
+        stream.synchronize()
+        n_unique = int(np.unique(ids.cpu().numpy()).size)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(moe.MOE_N_PHASE_EVENTS)]
+               for _ in range(steps)]
+        for row in evs:          # torch creates the CUDA events on first record
+            for ev in row:
+                ev.record(stream)
+        for _ in range(warmup):
+            layer.forward(x, ws, out, stream=stream)
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        launches = 0
+        with ClockSampler(local_rank) as clk:
+            t0.record(stream)
+            for i in range(steps):
+                _, st = layer.forward(x, ws, out, stream=stream, phase_events=evs[i])
+                launches += st.n_launches
+            t1.record(stream)
+            stream.synchronize()
+        torch.cuda.synchronize()
+        ms = t0.elapsed_time(t1)
+        if world > 1:
+            tt = torch.tensor([ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            ms = float(tt.item())
+            torch.distributed.barrier()
+        ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)]
+                       for i in range(steps)])
+        res = dict(T=T, ms_per_step=ms / steps, tokens_per_s=T * steps * world / (ms / 1e3),
+                   n_unique=n_unique, phase_ms=ph.mean(0).tolist(), launches=launches,
+                   clocks=clk.summary())
+        if with_e2e:
+            xh = torch.from_numpy(xb.view(np.int16)).pin_memory()
+            oh = torch.empty_like(xh).pin_memory()
+            for _ in range(2):
+                with torch.cuda.stream(stream):
+                    x.copy_(xh, non_blocking=True)
+                    layer.forward(x, ws, out, stream=stream)
+                    oh.copy_(out, non_blocking=True)
+            stream.synchronize()
+            if world > 1:
+                torch.distributed.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                for _ in range(steps):
+                    x.copy_(xh, non_blocking=True)
+                    layer.forward(x, ws, out, stream=stream)
+                    oh.copy_(out, non_blocking=True)
+            e1.record(stream)
+            stream.synchronize()
+            ems = e0.elapsed_time(e1)
+            if world > 1:
+                tt = torch.tensor([ems], device=dev)
+                torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+                ems = float(tt.item())
+            res["e2e"] = {"value": round(T * steps * world / (ems / 1e3), 1), "unit": "tokens/s",
+                          "h2d_bytes_per_step": int(xh.numel() * 2),
+                          "d2h_bytes_per_step": int(oh.numel() * 2)}
+        return res
+
+    head = measure(args.T, args.steps, args.warmup, True)
+    sweep = {}
+    if args.sweep:
+        for T in cfg.Ts:
+            if T == args.T:
+                continue
+            r = measure(T, max(5, min(args.steps, 20)), 3, False)
+            w = layer_work(cfg, T, r["n_unique"])
+            sw = {"tokens_per_s": round(r["tokens_per_s"], 1), "ms_per_step": round(r["ms_per_step"], 4),
+                  "n_unique": r["n_unique"],
+                  "layer_roofline": roofline_of(w["flops"], w["bytes"], r["ms_per_step"] / 1e3, pk)}
+            gu_ms = r["phase_ms"][2]
+            sw["gate_up_roofline"] = roofline_of(*w["gu"], gu_ms / 1e3, pk)
+            sweep[str(T)] = sw
+
+    w = layer_work(cfg, args.T, head["n_unique"])
+    names = ["route+dispatch+gather", "shared_expert", "gate_up_gemm", "down_gemm", "combine"]
+    share = np.array(head["phase_ms"]) / max(sum(head["phase_ms"]), 1e-9)
+    dom = int(np.argmax(share))
+    dom_work = {2: w["gu"], 3: w["dn"]}.get(dom, (w["flops"], w["bytes"]))
+    roof = roofline_of(*dom_work, head["phase_ms"][dom] / 1e3, pk)
+    roof.update({"kernel": names[dom], "traffic": None, "peak_source": pk["source"],
+                 "share_of_step": round(float(share[dom]), 4)})
+    result = {
+        "metric": "MoE-layer tokens/s (Mixtral-8x7B-shaped layer)",
+        "value": round(head["tokens_per_s"], 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms_per_step"], 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,0.02) weights, N(0,1) tokens)",
+        "config": {"workload": f"mixtral-8x7b-shaped MoE layer forward, T={args.T}",
+                   "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "T": args.T,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "expert weights (2.82 GB) exceed L2 and are streamed every step"},
+        "layer_roofline": roofline_of(w["flops"], w["bytes"], head["ms_per_step"] / 1e3, pk),
+        "roofline": roof,
+        "phase_ms": {n: round(v, 4) for n, v in zip(names, head["phase_ms"])},
+        "n_unique_experts": head["n_unique"],
+        "e2e": head.get("e2e"), "gpu_launches": head["launches"], "clocks": head["clocks"],
+        "sweep": sweep,
+    }
+    return result
+
+
+def oracle_sample(cfg, T_sample, weights_cache):
+    """One oracle layer forward on T_sample tokens; returns seconds."""
+    from oracle import moe_ref
+    xb = wl.tokens(cfg, T_sample, step=7)
+    t = time.perf_counter()
+    moe_ref.layer_forward(cfg, 0, xb, weights=lambda layer, e, sh=False: weights_cache(e, sh))
+    return time.perf_counter() - t
+
+
+def cpu_baseline(cfg, T_sample=16, reps=1):
+    cache = {}
+
+    def getw(e, sh):
+        if (e, sh) not in cache:
+            cache[(e, sh)] = wl.expert(cfg, 0, e, shared=sh)
+        return cache[(e, sh)]
+    for e in range(cfg.E):        # pre-generate (generation is not the oracle's work)
+        getw(e, False)
+    secs = [oracle_sample(cfg, T_sample, getw) for _ in range(reps)]
+    s = float(np.median(secs))
+    return {"value": round(T_sample / s, 3), "unit": "tokens/s",
+            "cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"fp64 NumPy oracle, full layer on {T_sample} tokens of the same workload "
+                      f"({s:.1f} s per sample)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--no-cpu", dest="cpu", action="store_false")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    cfg = wl.MIXTRAL
+
+    if args.impl == "reference":
+        # the reference arm is the CPU oracle, on rank 0 only
+        if rank != 0:
+            return
+        cache = {}
+
+        def getw(e, sh):
+            if (e, sh) not in cache:
+                cache[(e, sh)] = wl.expert(cfg, 0, e, shared=sh)
+            return cache[(e, sh)]
+        for e in range(cfg.E):
+            getw(e, False)
+        T_s = 8
+        for _ in range(min(args.warmup, 1)):
+            oracle_sample(cfg, T_s, getw)
+        secs = [oracle_sample(cfg, T_s, getw) for _ in range(args.steps)]
+        tot = float(np.sum(secs))
+        v = T_s * args.steps / tot
+        line = {"metric": "MoE-layer tokens/s (Mixtral-8x7B-shaped layer)", "value": round(v, 3),
+                "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(1e3 * tot / args.steps, 2), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "impl": "reference",
+                "config": {"workload": f"mixtral-8x7b-shaped MoE layer forward, T={args.T}",
+                           "sample_tokens_per_step": T_s},
+                "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "kind": "oracle",
+                                 "cores": len(os.sched_getaffinity(0)),
+                                 "sample": f"{T_s} tokens of the T={args.T} workload per step"},
+                "e2e": {"value": round(v, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if args.cpu:
+            res["cpu_baseline"] = cpu_baseline(cfg)
+        print(json.dumps(res))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -80,8 +80,12 @@ class moe_layer(C.Structure):
                 ("bundles", C.POINTER(C.c_void_p))]
 
 
+MOE_N_PHASE_EVENTS = 6
+
+
 class moe_layer_stats(C.Structure):
-    _fields_ = [("n_unique", C.c_int32), ("n_missed", C.c_int32), ("n_refined", C.c_int32)]
+    _fields_ = [("n_unique", C.c_int32), ("n_missed", C.c_int32), ("n_launches", C.c_int32),
+                ("reserved", C.c_int32), ("phase_events", C.POINTER(C.c_void_p))]
 
 
 # ----------------------------------------------------------------------------- loading
@@ -295,8 +299,14 @@ def moe_layer_workspace_size(layer: moe_layer, T) -> int:
 
 
 def moe_layer_forward(layer: moe_layer, x, T, forced_ids, residual, out, cache, ws, ws_bytes,
-                      stream=None, ids_out=None, w_out=None) -> moe_layer_stats:
+                      stream=None, ids_out=None, w_out=None, phase_events=None) -> moe_layer_stats:
+    """phase_events: None or a list of MOE_N_PHASE_EVENTS torch.cuda.Event (recorded by the
+    library on `stream` at phase boundaries)."""
     st = moe_layer_stats()
+    if phase_events is not None:
+        arr = (C.c_void_p * MOE_N_PHASE_EVENTS)(*[ev.cuda_event if ev is not None else None
+                                                  for ev in phase_events])
+        st.phase_events = arr
     _check(_lib.moe_layer_forward(C.byref(layer), ptr(x), T, ptr(forced_ids), ptr(residual),
                                   ptr(out), cache, C.byref(st), ptr(ids_out), ptr(w_out),
                                   ptr(ws), ws_bytes, stream_handle(stream)), "moe_layer_forward")

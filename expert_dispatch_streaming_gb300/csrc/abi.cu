@@ -3,6 +3,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <functional>
 #include <vector>
 
 #include "cache.h"
@@ -13,6 +14,7 @@
 namespace moe {
 
 static thread_local int g_last_cuda = 0;
+thread_local long long g_launches = 0;
 
 void set_cuda_error(cudaError_t e) { g_last_cuda = (int)e; }
 int fail_cuda(cudaError_t e) {
@@ -120,7 +122,7 @@ static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, 
 
 static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
                        const BundleTable& tab, int T, int host_n, const int32_t* host_ids,
-                       cudaStream_t st) {
+                       cudaStream_t st, std::function<int()> between) {
   const int rows = T * L->k;
   GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows);
   gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = s.rs.active;
@@ -129,6 +131,7 @@ static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratc
   GemmPlan pg = plan_gemm(gu);
   int r = launch_gemm(gu, pg, s.part, s.counters, st);
   if (r != MOE_OK) return r;
+  if (between && (r = between()) != MOE_OK) return r;
   GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
   dn.xin = s.h; dn.offsets = s.offsets; dn.active = s.rs.active;
   dn.n_active = s.rs.n_active; dn.tab = &tab; dn.out = s.y_perm;
@@ -264,6 +267,7 @@ int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
   int32_t* ctr = c.take<int32_t>(std::max({pg.counter_elems, pd.counter_elems, (size_t)1}));
   MOE_REQUIRE(c.ok());
   active_from_offsets_kernel<<<1, 32, 0, st>>>(offsets, E, act, act + kMaxExperts);
+  MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   gu.xin = x_perm; gu.offsets = offsets; gu.active = act; gu.n_active = act + kMaxExperts;
   gu.tab = &tab; gu.out = h;
@@ -306,7 +310,19 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   MOE_REQUIRE(cache || L->bundles);
   MOE_REQUIRE(!cache || (cache->E == L->E && L->layer_index >= 0 && L->layer_index < cache->L &&
                          cache->slot_bytes >= P.lay.total_bytes));
-  if (st) std::memset(st, 0, sizeof(*st));
+  void* const* pev = st ? st->phase_events : nullptr;
+  if (st) {
+    std::memset(st, 0, sizeof(*st));
+    st->phase_events = pev;
+  }
+  const long long launches0 = g_launches;
+  auto phase = [&](int i) -> int {
+    if (pev && pev[i]) {
+      const cudaError_t e = cudaEventRecord((cudaEvent_t)pev[i], (cudaStream_t)stream);
+      if (e != cudaSuccess) return fail_cuda(e);
+    }
+    return MOE_OK;
+  };
   if (T == 0) return MOE_OK;
   MOE_REQUIRE(x && out && aligned16(x) && aligned16(out));
   cudaStream_t s0 = (cudaStream_t)stream;
@@ -315,6 +331,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   carve(c, L, T, P, &s);
   MOE_REQUIRE(c.ok());
 
+  if ((r = phase(0)) != MOE_OK) return r;
   // A1-A4: route, dispatch and gather into expert order
   RouteArgs ra{};
   ra.x = x; ra.w_r = L->w_r; ra.logit_bias = L->logit_bias; ra.sel_bias = L->sel_bias;
@@ -325,13 +342,19 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   ra.logits = nullptr; ra.shared_gate = s.shared_gate; ra.x_perm = s.x_perm;
   r = launch_route(ra, P.rp, s.rs, s0);
   if (r != MOE_OK) return r;
+  if ((r = phase(1)) != MOE_OK) return r;
   const float* sgate = (L->Is && L->shared_gate_sigmoid) ? s.shared_gate : nullptr;
 
   if (!cache) {
     BundleTable tab{};
     for (int e = 0; e < L->E; ++e) tab.p[e] = L->bundles[e];
     if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
-    if ((r = run_experts(L, P, s, tab, T, -1, nullptr, s0)) != MOE_OK) return r;
+    if ((r = phase(2)) != MOE_OK) return r;
+    if ((r = run_experts(L, P, s, tab, T, -1, nullptr, s0, pev ? [&] { return phase(3); }
+                                                                 : std::function<int()>()))
+        != MOE_OK)
+      return r;
+    if ((r = phase(4)) != MOE_OK) return r;
   } else {
     // A5: the layer's expert-use mask crosses to the host, the LRU decides, misses are copied
     // on the cache's copy stream while the shared expert and the hit experts compute.
@@ -348,14 +371,18 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
     BundleTable tab{};
     for (int e = 0; e < L->E; ++e) tab.p[e] = ptrs[e];
     if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
-    if (!hits.empty() &&
-        (r = run_experts(L, P, s, tab, T, (int)hits.size(), hits.data(), s0)) != MOE_OK)
+    if ((r = phase(2)) != MOE_OK) return r;
+    if (!hits.empty() && (r = run_experts(L, P, s, tab, T, (int)hits.size(), hits.data(), s0,
+                                          std::function<int()>())) != MOE_OK)
       return r;
+    if ((r = phase(3)) != MOE_OK) return r;
     if (!misses.empty()) {
       MOE_CUDA_TRY(cudaStreamWaitEvent(s0, cache->last_copy, 0));
-      if ((r = run_experts(L, P, s, tab, T, (int)misses.size(), misses.data(), s0)) != MOE_OK)
+      if ((r = run_experts(L, P, s, tab, T, (int)misses.size(), misses.data(), s0,
+                           std::function<int()>())) != MOE_OK)
         return r;
     }
+    if ((r = phase(4)) != MOE_OK) return r;
     if (st) {
       st->n_unique = (int32_t)(hits.size() + misses.size());
       st->n_missed = (int32_t)misses.size();
@@ -365,6 +392,8 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   r = launch_combine(s.y_perm, s.pos, s.w, T, L->k, L->H, L->Is ? s.s : nullptr, sgate,
                      residual, out, s0);
   if (r != MOE_OK) return r;
+  if ((r = phase(5)) != MOE_OK) return r;
+  if (st) st->n_launches = (int32_t)(g_launches - launches0);
   if (cache) {
     MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[L->layer_index], s0));
     cache->layer_done_valid[L->layer_index] = 1;

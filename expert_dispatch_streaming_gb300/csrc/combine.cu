@@ -73,6 +73,7 @@ int launch_combine(const uint16_t* y, const int32_t* pos, const float* w, int T,
   if (T <= 0) return MOE_OK;
   combine_kernel<<<ceil_div(T * 32, 256), 256, 0, st>>>(y, pos, w, T, k, H, shared,
                                                         shared_gate, residual, out);
+  MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -46,6 +46,9 @@ struct WsCursor {
 };
 
 int sm_count();
+// kernels launched by this thread (the layer forward reports the difference)
+extern thread_local long long g_launches;
+#define MOE_COUNT_LAUNCH() (++::moe::g_launches)
 
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {

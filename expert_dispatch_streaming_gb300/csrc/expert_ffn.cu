@@ -291,6 +291,7 @@ int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* coun
     if (a.fused) launch_nt<false, true, 1>(g.nt, grid, kp, st);
     else launch_nt<false, false, 2>(g.nt, grid, kp, st);
   }
+  MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -494,6 +494,7 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     dim3 g1(ceil_div(a.T, R_BT), ceil_div(r.C, R_BC), r.S);
     router_partial_kernel<<<g1, 256, 0, st>>>(a.x, a.w_r, a.w_gate, a.T, a.H, a.E, r.C,
                                               r.h_per_split, s.part, s.hist, r.ntiles * a.E);
+    MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
     GateParams p{};
     p.part = s.part; p.S = r.S; p.C = r.C;
@@ -503,14 +504,17 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = s.hist;
     const int per_cta = G_WARPS * G_TOK_PER_WARP;
     gate_topk_kernel<<<ceil_div(a.T, per_cta), G_WARPS * 32, 0, st>>>(p);
+    MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
   }
   scan_kernel<<<1, kMaxExperts, 0, st>>>(s.hist, r.ntiles, a.E, a.counts, a.offsets, s.base,
                                          s.active, s.n_active, s.shared_meta, a.T);
+  MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   if (a.T > 0) {
     rank_permute_kernel<<<r.ntiles, 256, 0, st>>>(a.ids, s.base, a.T, a.k, a.E, a.H, a.x,
                                                   a.pos, a.src, a.x_perm);
+    MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
   }
   return MOE_OK;
@@ -520,6 +524,7 @@ int launch_gather(const uint16_t* x, const int32_t* src, int rows, int k, int H,
                   uint16_t* x_perm, cudaStream_t st) {
   if (rows <= 0) return MOE_OK;
   gather_rows_kernel<<<ceil_div(rows * 32, 256), 256, 0, st>>>(x, src, rows, k, H, x_perm);
+  MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }

@@ -84,12 +84,12 @@ class DeviceLayer:
         return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
 
     def forward(self, x: torch.Tensor, ws: torch.Tensor, out=None, forced_ids=None, residual=None,
-                cache=None, stream=None, ids_out=None, w_out=None):
+                cache=None, stream=None, ids_out=None, w_out=None, phase_events=None):
         T = x.shape[0]
         if out is None:
             out = torch.empty_like(x)
         st = moe_layer_forward(self.desc, x, T, forced_ids, residual, out, cache, ws, ws.numel(),
-                               stream, ids_out=ids_out, w_out=w_out)
+                               stream, ids_out=ids_out, w_out=w_out, phase_events=phase_events)
         return out, st
 
 

@@ -288,10 +288,20 @@ typedef struct moe_layer {
                                 when a cache is attached                                 */
 } moe_layer;
 
+/* Number of phase events moe_layer_forward can record (see moe_layer_stats). */
+#define MOE_N_PHASE_EVENTS 6
+
 typedef struct moe_layer_stats {
-  int32_t n_unique;          /* distinct experts used by this call                       */
-  int32_t n_missed;          /* cache misses (0 without a cache)                         */
-  int32_t n_refined;         /* tokens whose selection was re-scored in fp64 (needs sync) */
+  int32_t n_unique;          /* out: distinct experts used (cache path; 0 otherwise)      */
+  int32_t n_missed;          /* out: cache misses (0 without a cache)                     */
+  int32_t n_launches;        /* out: CUDA kernels this call launched                      */
+  int32_t reserved;
+  /* in: NULL, or a host array of MOE_N_PHASE_EVENTS cudaEvent_t handles created by the
+   * caller; the call records them on `stream` at phase boundaries:
+   *   [0] start  [1] routing + dispatch + gather done  [2] shared expert done
+   *   [3] routed gate/up GEMM done (cache path: hit experts' FFN done)
+   *   [4] routed down GEMM done (cache path: missed experts' FFN done)  [5] combine done */
+  void* const* phase_events;
 } moe_layer_stats;
 
 /* Bytes of scratch moe_layer_forward needs for T tokens. */
@@ -304,7 +314,7 @@ size_t moe_layer_workspace_size(const moe_layer* L, int T);
  *             the call reads the layer's expert-use mask back to the host (one small
  *             device-to-host copy and a bounded wait), requests residency, and overlaps the
  *             miss copies with the shared expert and with the experts that hit.
- *  st         host, or NULL.
+ *  st         host, or NULL (in: phase_events; out: counters).
  *  ids_out, w_out  device [T][k] or NULL: copies of the routing decision.
  * With cache == NULL the call is fully asynchronous. */
 int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_t* forced_ids,
