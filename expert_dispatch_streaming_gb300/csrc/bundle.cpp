@@ -15,33 +15,46 @@ namespace {
 
 size_t r256(size_t v) { return (v + 255) / 256 * 256; }
 
-// dst[c][r] = src[r][c] for a rows x cols row-major source of 2-byte elements (blocked)
-void transpose16(const uint16_t* src, size_t rows, size_t cols, uint16_t* dst) {
-  const size_t B = 64;
-  for (size_t r0 = 0; r0 < rows; r0 += B)
-    for (size_t c0 = 0; c0 < cols; c0 += B) {
-      const size_t r1 = std::min(rows, r0 + B), c1 = std::min(cols, c0 + B);
-      for (size_t r = r0; r < r1; ++r)
-        for (size_t c = c0; c < c1; ++c) dst[c * rows + r] = src[r * cols + c];
+// Tiled bf16 image of the K-major weight rows W[n][k] = src[k][n] (src is K x N row-major):
+// tiles of 128 rows x 64 k, tile (mt, kt) at ((mt * K/64) + kt) * 16384 bytes; inside a tile,
+// row r's 16-byte chunk c (k = kt*64 + 8c .. +7) sits at r*128 + ((c ^ (r & 7)) << 4), the
+// 128-byte-swizzled K-major layout the tensor cores read from shared memory.
+void pack_tiled_bf16(const uint16_t* src, size_t K, size_t N, uint16_t* dst) {
+  const size_t kt_n = K / 64;
+  for (size_t mt = 0; mt < N / 128; ++mt)
+    for (size_t kt = 0; kt < kt_n; ++kt) {
+      uint16_t* tile = dst + (mt * kt_n + kt) * 8192;
+      for (size_t kk = 0; kk < 64; ++kk) {
+        const uint16_t* s = src + (kt * 64 + kk) * N + mt * 128;
+        const size_t c = kk >> 3, e = kk & 7;
+        for (size_t r = 0; r < 128; ++r) tile[r * 64 + (((c ^ (r & 7)) << 3) | e)] = s[r];
+      }
     }
 }
 
-// INT4 rows of the transposed matrix: dst row c holds src[.][c] for r = 0..rows-1, two codes
-// per byte, even r in the low nibble.  Returns false on a code outside [-7, 7].
-bool pack_int4_transposed(const int8_t* src, size_t rows, size_t cols, uint8_t* dst) {
-  const size_t B = 64;
+// Tiled INT4 image of W[n][k] = codes[k][n] with group scales[k/128][n]: tiles of 128 rows x
+// 128 k (one scale group), tile (mt, kt) at ((mt * K/128) + kt) * 8448 bytes.  Inside a tile:
+// 16-byte chunk (c, r) at (c * 128 + r) * 16 holds codes k = kt*128 + 32c .. +31 of row r, two
+// per byte, even k in the low nibble; then the 128 rows' bf16 scales at 8192 + 2r.
+bool pack_tiled_int4(const int8_t* codes, const uint16_t* scales, size_t K, size_t N,
+                     uint8_t* dst) {
   bool ok = true;
-  for (size_t r0 = 0; r0 < rows; r0 += B)
-    for (size_t c0 = 0; c0 < cols; c0 += B) {
-      const size_t r1 = std::min(rows, r0 + B), c1 = std::min(cols, c0 + B);
-      for (size_t c = c0; c < c1; ++c)
-        for (size_t r = r0; r < r1; r += 2) {
-          const int8_t lo = src[r * cols + c], hi = src[(r + 1) * cols + c];
-          ok &= lo >= -7 && lo <= 7 && hi >= -7 && hi <= 7;
-          dst[c * (rows / 2) + r / 2] =
-              static_cast<uint8_t>((static_cast<uint8_t>(lo) & 0xFu) |
-                                   ((static_cast<uint8_t>(hi) & 0xFu) << 4));
+  const size_t kt_n = K / 128;
+  for (size_t mt = 0; mt < N / 128; ++mt)
+    for (size_t kt = 0; kt < kt_n; ++kt) {
+      uint8_t* tile = dst + (mt * kt_n + kt) * 8448;
+      for (size_t kk = 0; kk < 128; kk += 2) {
+        const int8_t* lo = codes + (kt * 128 + kk) * N + mt * 128;
+        const int8_t* hi = lo + N;
+        const size_t c = kk >> 5, byte = (kk & 31) >> 1;
+        for (size_t r = 0; r < 128; ++r) {
+          ok &= lo[r] >= -7 && lo[r] <= 7 && hi[r] >= -7 && hi[r] <= 7;
+          tile[(c * 128 + r) * 16 + byte] = static_cast<uint8_t>(
+              (static_cast<uint8_t>(lo[r]) & 0xFu) | ((static_cast<uint8_t>(hi[r]) & 0xFu) << 4));
         }
+      }
+      uint16_t* sc = reinterpret_cast<uint16_t*>(tile + 8192);
+      for (size_t r = 0; r < 128; ++r) sc[r] = scales[kt * N + mt * 128 + r];
     }
   return ok;
 }
@@ -59,11 +72,12 @@ int moe_bundle_layout_of(int H, int I, int wdtype, moe_bundle_layout* out) {
     L.down_offset = r256(2 * i * h * 2);
     L.total_bytes = r256(L.down_offset + h * i * 2);
   } else if (wdtype == MOE_W_INT4_G128) {
+    // scales live inside each 8448-byte tile; the scale offsets are those of the first tile
     L.gate_up_offset = 0;
-    L.down_offset = r256(2 * i * h / 2);
-    L.gate_up_scale_offset = r256(L.down_offset + h * i / 2);
-    L.down_scale_offset = r256(L.gate_up_scale_offset + 2 * i * (h / 128) * 2);
-    L.total_bytes = r256(L.down_scale_offset + h * (i / 128) * 2);
+    L.down_offset = r256((2 * i / 128) * (h / 128) * 8448);
+    L.gate_up_scale_offset = 8192;
+    L.down_scale_offset = L.down_offset + 8192;
+    L.total_bytes = r256(L.down_offset + (h / 128) * (i / 128) * 8448);
   } else {
     return MOE_ERR_INVALID_ARG;
   }
@@ -86,25 +100,20 @@ int moe_pack_bundle(int H, int I, int wdtype, const void* wg, const void* wu, co
   const size_t h = H, i = I;
   if (wdtype == MOE_W_BF16) {
     uint16_t* gu = reinterpret_cast<uint16_t*>(b + L.gate_up_offset);
-    transpose16(static_cast<const uint16_t*>(wg), h, i, gu);          // rows 0..I-1 = Wg^T
-    transpose16(static_cast<const uint16_t*>(wu), h, i, gu + i * h);  // rows I..2I-1 = Wu^T
-    transpose16(static_cast<const uint16_t*>(wd), i, h,
-                reinterpret_cast<uint16_t*>(b + L.down_offset));      // row h = Wd[:, h]
+    pack_tiled_bf16(static_cast<const uint16_t*>(wg), h, i, gu);          // rows 0..I-1
+    pack_tiled_bf16(static_cast<const uint16_t*>(wu), h, i, gu + i * h);  // rows I..2I-1
+    pack_tiled_bf16(static_cast<const uint16_t*>(wd), i, h,
+                    reinterpret_cast<uint16_t*>(b + L.down_offset));
     return MOE_OK;
   }
   if (!sg || !su || !sd) return MOE_ERR_INVALID_ARG;
   uint8_t* gu = reinterpret_cast<uint8_t*>(b + L.gate_up_offset);
-  bool ok = pack_int4_transposed(static_cast<const int8_t*>(wg), h, i, gu);
-  ok &= pack_int4_transposed(static_cast<const int8_t*>(wu), h, i, gu + i * (h / 2));
-  ok &= pack_int4_transposed(static_cast<const int8_t*>(wd), i, h,
-                             reinterpret_cast<uint8_t*>(b + L.down_offset));
-  if (!ok) return MOE_ERR_INVALID_ARG;
-  // scales, K-major per weight row: row n holds its H/128 (or I/128) group scales
-  uint16_t* sgu = reinterpret_cast<uint16_t*>(b + L.gate_up_scale_offset);
-  transpose16(sg, h / 128, i, sgu);
-  transpose16(su, h / 128, i, sgu + i * (h / 128));
-  transpose16(sd, i / 128, h, reinterpret_cast<uint16_t*>(b + L.down_scale_offset));
-  return MOE_OK;
+  const size_t half = (i / 128) * (h / 128) * 8448;
+  bool ok = pack_tiled_int4(static_cast<const int8_t*>(wg), sg, h, i, gu);
+  ok &= pack_tiled_int4(static_cast<const int8_t*>(wu), su, h, i, gu + half);
+  ok &= pack_tiled_int4(static_cast<const int8_t*>(wd), sd, i, h,
+                        reinterpret_cast<uint8_t*>(b + L.down_offset));
+  return ok ? MOE_OK : MOE_ERR_INVALID_ARG;
 }
 
 // FNV-1a, 64-bit (offset basis 14695981039346656037, prime 1099511628211), over bytes.

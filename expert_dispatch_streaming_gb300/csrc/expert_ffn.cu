@@ -94,13 +94,21 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
   const int m0 = mb * 64 + warp * 16;
   const int k_lo = split * p.k_per_split, k_hi = min(K, k_lo + p.k_per_split);
 
+  // weight row wr lives in row tile wr / 128 at row rr = wr % 128 (tiled bundle layout:
+  // bf16 tiles of 128 x 64 k, 128-byte swizzled; INT4 tiles of 128 x 128 k with scales)
   const char* wrow[NR];
-  const uint16_t* srow[NR];
+  int rsw[NR];
 #pragma unroll
   for (int r = 0; r < NR; ++r) {
     const int wr = m0 + g + 8 * (r & 1) + (r >= 2 ? M : 0);
-    wrow[r] = bundle + p.w_off + (INT4 ? (size_t)wr * (K / 2) : (size_t)wr * K * 2);
-    srow[r] = reinterpret_cast<const uint16_t*>(bundle + p.s_off) + (size_t)wr * (K / 128);
+    const int mt = wr >> 7, rr = wr & 127;
+    if (INT4) {
+      wrow[r] = bundle + p.w_off + (size_t)mt * (K / 128) * 8448 + rr * 16;
+      rsw[r] = rr;
+    } else {
+      wrow[r] = bundle + p.w_off + (size_t)mt * (K / 64) * 16384 + rr * 128;
+      rsw[r] = rr & 7;
+    }
   }
   const int MP = FUSED ? 2 * M : M;
 
@@ -122,11 +130,17 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
         for (int r = 0; r < NR; ++r) {
 #pragma unroll
           for (int v = 0; v < VPR; ++v) {
-            const char* ptr = INT4 ? wrow[r] + kbb / 2 + 16 * tq
-                                   : wrow[r] + ((size_t)kbb + 32 * tq) * 2 + 16 * v;
+            const char* ptr =
+                INT4 ? wrow[r] + (size_t)(kbb >> 7) * 8448 + tq * 2048
+                     : wrow[r] + (size_t)((kbb >> 6) + (tq >> 1)) * 16384 +
+                           ((((tq & 1) * 4 + v) ^ rsw[r]) << 4);
             A[uu][r][v] = ok ? ld_stream(ptr) : make_uint4(0, 0, 0, 0);
           }
-          sc[uu][r] = (INT4 && ok) ? bf16_bits_to_float(__ldg(srow[r] + kbb / 128)) : 0.f;
+          sc[uu][r] = (INT4 && ok)
+                          ? bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(
+                                wrow[r] - rsw[r] * 16 + (size_t)(kbb >> 7) * 8448 + 8192) +
+                                rsw[r]))
+                          : 0.f;
         }
       }
 #pragma unroll

@@ -86,11 +86,18 @@ enum moe_wdtype {
  * their group scales -- so that weights can never arrive without their scales ("Running 35B
  * MoE Models on 8GB GPUs ...", section "Technical Insight").
  *
- * Layout (every section starts on a 256-byte boundary; offsets from moe_bundle_layout):
- *   bf16:  [ gate_up : (2I) x H  bf16 ]  rows 0..I-1 = Wg^T, rows I..2I-1 = Wu^T (K-major)
- *          [ down    :  H x I    bf16 ]  row h = column h of Wd (K-major)
- *   int4:  [ gate_up codes : (2I) x H/2 bytes ] [ down codes : H x I/2 bytes ]
- *          [ gate_up scales: (2I) x H/128 bf16 ] [ down scales: H x I/128 bf16 ]
+ * Layout.  Weights are stored as "weight rows": the gate/up section holds 2I rows of K = H
+ * (rows 0..I-1 = columns of Wg, rows I..2I-1 = columns of Wu), the down section H rows of
+ * K = I (row h = column h of Wd).  Rows are grouped into 128-row tiles stored tile after
+ * tile, row-tile major then K-tile (each section starts on a 256-byte boundary):
+ *   bf16: tiles of 128 rows x 64 k (16384 B).  Inside a tile, row r's 16-byte chunk c
+ *         (elements k = 8c..8c+7 of the tile) is at byte r*128 + ((c ^ (r % 8)) * 16): the
+ *         128-byte-swizzled K-major image the tensor cores read from shared memory, so a
+ *         tile moves with one bulk copy.
+ *   int4: tiles of 128 rows x 128 k (one scale group, 8448 B): 16-byte chunk (c, r) at
+ *         (c*128 + r)*16 holds the 32 codes k = 32c..32c+31 of row r (two per byte, even k in
+ *         the low nibble), followed by the rows' bf16 group scales at 8192 + 2r.
+ *   gate_up_scale_offset / down_scale_offset give the scale block of the section's first tile.
  * Constraints: H and I multiples of 128.  */
 typedef struct moe_bundle_layout {
   size_t total_bytes;

@@ -49,44 +49,63 @@ def test_bundle_sizes(moe):
     assert moe.moe_bundle_bytes(100, 128, "bf16") == 0
 
 
+def _untile_bf16(buf, rows, K):
+    """Inverse of the tiled bf16 image: tiles of 128 rows x 64 k, chunk c of row r at
+    r*128 + ((c ^ (r % 8)) * 16) inside the tile."""
+    t = buf[:rows * K * 2].view(np.uint16).reshape(rows // 128, K // 64, 128, 8, 8)
+    r = np.arange(128)[:, None]
+    c = np.arange(8)[None, :]
+    src_chunk = c ^ (r % 8)                                  # stored position of chunk c
+    out = t[:, :, r, src_chunk, :]                           # [mt, kt, 128, 8, 8]
+    return out.transpose(0, 2, 1, 3, 4).reshape(rows, K)
+
+
+def _untile_int4(buf, rows, K):
+    """Inverse of the tiled INT4 image: 8448-byte tiles of 128 rows x 128 k; chunk (c, r) at
+    (c*128 + r)*16 holds k = 32c..32c+31 (even k in the low nibble); scales at 8192 + 2r."""
+    nt = (rows // 128) * (K // 128)
+    t = buf[:nt * 8448].reshape(rows // 128, K // 128, 8448)
+    codes = t[:, :, :8192].reshape(rows // 128, K // 128, 4, 128, 16)
+    lo = (codes & 0xF).astype(np.int8)
+    hi = (codes >> 4).astype(np.int8)
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    q = np.empty(codes.shape[:-1] + (32,), np.int8)
+    q[..., 0::2], q[..., 1::2] = lo, hi                     # [mt, kt, c, r, 32]
+    q = q.transpose(0, 3, 1, 2, 4).reshape(rows, K)
+    sc = t[:, :, 8192:8448].copy().view(np.uint16).reshape(rows // 128, K // 128, 128)
+    sc = sc.transpose(0, 2, 1).reshape(rows, K // 128)
+    return q, sc
+
+
 def test_pack_bf16_layout(moe):
-    cfg = wl.custom("pk", H=256, I=384)
+    H, I = 256, 384
+    cfg = wl.custom("pk", H=H, I=I)
     w = wl.expert(cfg, 0, 2)
-    lay = moe.bundle_layout(256, 384, "bf16")
+    lay = moe.bundle_layout(H, I, "bf16")
     buf = np.zeros(lay.total_bytes, np.uint8)
-    moe.moe_pack_bundle(256, 384, "bf16", w.wg, w.wu, w.wd, None, None, None, buf)
-    gu = buf[lay.gate_up_offset:lay.gate_up_offset + 2 * 384 * 256 * 2].view(np.uint16)
-    gu = gu.reshape(2 * 384, 256)
-    assert np.array_equal(gu[:384], w.wg.T) and np.array_equal(gu[384:], w.wu.T)
-    dn = buf[lay.down_offset:lay.down_offset + 256 * 384 * 2].view(np.uint16).reshape(256, 384)
-    assert np.array_equal(dn, w.wd.T)
+    moe.moe_pack_bundle(H, I, "bf16", w.wg, w.wu, w.wd, None, None, None, buf)
+    gu = _untile_bf16(buf[lay.gate_up_offset:], 2 * I, H)
+    assert np.array_equal(gu[:I], w.wg.T) and np.array_equal(gu[I:], w.wu.T)
+    assert np.array_equal(_untile_bf16(buf[lay.down_offset:], H, I), w.wd.T)
+    # hand check of one element: row 130 (tile 1, r = 2), k = 75 (tile 1, chunk 1, elem 3)
+    tile = buf[lay.gate_up_offset + (1 * (H // 64) + 1) * 16384:].view(np.uint16)
+    assert tile[(2 * 128 + ((1 ^ 2) << 4)) // 2 + 3] == w.wg[75, 130]
 
 
 def test_pack_int4_layout(moe):
-    cfg = wl.custom("pk4", H=256, I=384, wdtype="int4_g128")
-    w = wl.expert(cfg, 0, 1)
     H, I = 256, 384
+    cfg = wl.custom("pk4", H=H, I=I, wdtype="int4_g128")
+    w = wl.expert(cfg, 0, 1)
     lay = moe.bundle_layout(H, I, "int4_g128")
     buf = np.zeros(lay.total_bytes, np.uint8)
     moe.moe_pack_bundle(H, I, "int4_g128", w.wg, w.wu, w.wd, w.sg, w.su, w.sd, buf)
-
-    def unpack(off, rows, K):
-        b = buf[off:off + rows * K // 2].reshape(rows, K // 2)
-        lo = (b & 0xF).astype(np.int8)
-        hi = (b >> 4).astype(np.int8)
-        lo = np.where(lo >= 8, lo - 16, lo)
-        hi = np.where(hi >= 8, hi - 16, hi)
-        out = np.empty((rows, K), np.int8)
-        out[:, 0::2], out[:, 1::2] = lo, hi
-        return out
-    gu = unpack(lay.gate_up_offset, 2 * I, H)
-    assert np.array_equal(gu[:I], w.wg.T) and np.array_equal(gu[I:], w.wu.T)
-    assert np.array_equal(unpack(lay.down_offset, H, I), w.wd.T)
-    sg = buf[lay.gate_up_scale_offset:lay.gate_up_scale_offset + 2 * I * (H // 128) * 2]
-    sg = sg.view(np.uint16).reshape(2 * I, H // 128)
-    assert np.array_equal(sg[:I], w.sg.T) and np.array_equal(sg[I:], w.su.T)
-    sd = buf[lay.down_scale_offset:lay.down_scale_offset + H * (I // 128) * 2]
-    assert np.array_equal(sd.view(np.uint16).reshape(H, I // 128), w.sd.T)
+    q, sc = _untile_int4(buf[lay.gate_up_offset:], 2 * I, H)
+    assert np.array_equal(q[:I], w.wg.T) and np.array_equal(q[I:], w.wu.T)
+    assert np.array_equal(sc[:I], w.sg.T) and np.array_equal(sc[I:], w.su.T)
+    q, sc = _untile_int4(buf[lay.down_offset:], H, I)
+    assert np.array_equal(q, w.wd.T) and np.array_equal(sc, w.sd.T)
+    assert lay.total_bytes == 3 * (H // 128) * (I // 128) * 8448
 
 
 def test_pack_rejects_out_of_range_codes(moe):

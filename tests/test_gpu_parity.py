@@ -228,10 +228,12 @@ def test_int4_bundle_with_foreign_scales_fails_parity(moe, syn):
     cfg = SMALL[4]
     hb = syn.host_bundles(cfg, 0, list(range(cfg.E)), pinned=False)
     lay = moe.bundle_layout(cfg.H, cfg.I, cfg.wdtype)
-    a, b = lay.gate_up_scale_offset, lay.total_bytes
     bad = hb.clone()
-    for e in range(cfg.E):
-        bad[e, a:b] = hb[(e + 1) % cfg.E, a:b]
+    tiles = [lay.gate_up_offset + t * 8448 for t in range((2 * cfg.I // 128) * (cfg.H // 128))]
+    tiles += [lay.down_offset + t * 8448 for t in range((cfg.H // 128) * (cfg.I // 128))]
+    for e in range(cfg.E):                      # only the scale block of every tile is foreign
+        for t0 in tiles:
+            bad[e, t0 + 8192:t0 + 8448] = hb[(e + 1) % cfg.E, t0 + 8192:t0 + 8448]
     T = 33
     xb = wl.tokens(cfg, T)
     x = syn.to_device_bits(xb)
