@@ -104,6 +104,8 @@ _SIGS = {
     "moe_last_cuda_error": (_i, []),
     "moe_status_string": (C.c_char_p, [_i]),
     "moe_version": (_i, []),
+    "moe_set_option": (_i, [_i, _i]),
+    "moe_workspace_error": (_i, [_vp, C.POINTER(C.c_int32), _vp]),
     "moe_bundle_layout_of": (_i, [_i, _i, _i, C.POINTER(moe_bundle_layout)]),
     "moe_bundle_bytes": (_sz, [_i, _i, _i]),
     "moe_pack_bundle": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
@@ -173,6 +175,26 @@ def _check(status, fn):
 
 
 # ----------------------------------------------------------------------------- API
+MOE_OPT_FFN_KERNEL = 1
+FFN_KERNEL = {"auto": 0, "stream": 1, "tcgen05": 2}
+
+
+def moe_set_option(option, value) -> None:
+    _check(_lib.moe_set_option(option, value), "moe_set_option")
+
+
+def set_ffn_kernel(name: str) -> None:
+    """'auto' | 'stream' (mma.sync weight streaming) | 'tcgen05' (tensor-core kernel)."""
+    moe_set_option(MOE_OPT_FFN_KERNEL, FFN_KERNEL[name])
+
+
+def moe_workspace_error(ws, stream=None) -> int:
+    code = C.c_int32(0)
+    _check(_lib.moe_workspace_error(ptr(ws), C.byref(code), stream_handle(stream)),
+           "moe_workspace_error")
+    return code.value
+
+
 def bundle_layout(H, I, wdtype) -> moe_bundle_layout:
     out = moe_bundle_layout()
     _check(_lib.moe_bundle_layout_of(H, I, WDTYPE.get(wdtype, wdtype), C.byref(out)),

@@ -50,6 +50,7 @@ struct LayerScratch {
   uint16_t *x_perm, *h, *y_perm, *h_s, *s;
   float* part;
   int32_t* counters;
+  int32_t* err;     // device error word (first bytes of the workspace)
 };
 
 struct LayerPlan {
@@ -94,6 +95,7 @@ static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
 static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, LayerScratch* s) {
   LayerScratch z{};
   const size_t tk = (size_t)T * L->k;
+  z.err = c.take<int32_t>(64);
   route_scratch(c, P.rp, T, L->E, &z.rs);
   z.ids = c.take<int32_t>(tk + 1);
   z.w = c.take<float>(tk + 1);
@@ -129,7 +131,7 @@ static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratc
   gu.n_active = s.rs.n_active; gu.tab = &tab; gu.out = s.h;
   gu.host_n = host_n; gu.host_ids = host_ids;
   GemmPlan pg = plan_gemm(gu);
-  int r = launch_gemm(gu, pg, s.part, s.counters, st);
+  int r = launch_gemm(gu, pg, s.part, s.counters, s.err, st);
   if (r != MOE_OK) return r;
   if (between && (r = between()) != MOE_OK) return r;
   GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
@@ -137,7 +139,7 @@ static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratc
   dn.n_active = s.rs.n_active; dn.tab = &tab; dn.out = s.y_perm;
   dn.host_n = host_n; dn.host_ids = host_ids;
   GemmPlan pd = plan_gemm(dn);
-  return launch_gemm(dn, pd, s.part, s.counters, st);
+  return launch_gemm(dn, pd, s.part, s.counters, s.err, st);
 }
 
 static int run_shared(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
@@ -149,12 +151,12 @@ static int run_shared(const moe_layer* L, const LayerPlan& P, const LayerScratch
   GemmArgs gu = gemm_args(P.slay, L->wdtype, true, L->H, L->Is, 1, T);
   gu.xin = x; gu.offsets = meta; gu.active = meta + 2; gu.n_active = meta + 3;
   gu.tab = &tab; gu.out = s.h_s;
-  int r = launch_gemm(gu, P.sgu, s.part, s.counters, st);
+  int r = launch_gemm(gu, P.sgu, s.part, s.counters, s.err, st);
   if (r != MOE_OK) return r;
   GemmArgs dn = gemm_args(P.slay, L->wdtype, false, L->Is, L->H, 1, T);
   dn.xin = s.h_s; dn.offsets = meta; dn.active = meta + 2; dn.n_active = meta + 3;
   dn.tab = &tab; dn.out = s.s;
-  return launch_gemm(dn, P.sdn, s.part, s.counters, st);
+  return launch_gemm(dn, P.sdn, s.part, s.counters, s.err, st);
 }
 
 }  // namespace moe
@@ -180,6 +182,23 @@ const char* moe_status_string(int status) {
 }
 
 int moe_version(void) { return (1 << 16) | 0; }
+
+int moe_set_option(int option, int value) {
+  if (option == MOE_OPT_FFN_KERNEL) {
+    if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
+    g_ffn_path = value;
+    return MOE_OK;
+  }
+  return MOE_ERR_INVALID_ARG;
+}
+
+int moe_workspace_error(const void* ws, int32_t* code, void* stream) {
+  if (!ws || !code) return MOE_ERR_INVALID_ARG;
+  MOE_CUDA_TRY(cudaMemcpyAsync(code, ws, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                               (cudaStream_t)stream));
+  MOE_CUDA_TRY(cudaStreamSynchronize((cudaStream_t)stream));
+  return MOE_OK;
+}
 
 size_t moe_route_workspace_size(int T, int H, int E, int k) {
   if (!valid_route_shape(T, H, E, k)) return 0;
@@ -225,6 +244,7 @@ size_t moe_grouped_swiglu_workspace_size(int max_rows, int E, int H, int I, int 
   if (max_rows < 0 || E <= 0 || E > kMaxExperts || moe_bundle_layout_of(H, I, wdtype, &lay))
     return 0;
   WsCursor c(nullptr, 0);
+  c.take<int32_t>(64);
   GemmPlan a = plan_gemm(gemm_args(lay, wdtype, true, H, I, E, max_rows));
   GemmPlan b = plan_gemm(gemm_args(lay, wdtype, false, I, H, E, max_rows));
   c.take<uint16_t>((size_t)max_rows * I + 8);
@@ -258,6 +278,7 @@ int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
   BundleTable tab{};
   for (int e = 0; e < E; ++e) tab.p[e] = bundles[e];
   WsCursor c(ws, ws_bytes);
+  int32_t* err = c.take<int32_t>(64);
   uint16_t* h = c.take<uint16_t>((size_t)max_rows * I + 8);
   int32_t* act = c.take<int32_t>(kMaxExperts + 32);
   GemmArgs gu = gemm_args(lay, wdtype, true, H, I, E, max_rows);
@@ -266,16 +287,17 @@ int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
   float* part = c.take<float>(std::max({pg.part_elems, pd.part_elems, (size_t)1}));
   int32_t* ctr = c.take<int32_t>(std::max({pg.counter_elems, pd.counter_elems, (size_t)1}));
   MOE_REQUIRE(c.ok());
+  MOE_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int32_t), st));
   active_from_offsets_kernel<<<1, 32, 0, st>>>(offsets, E, act, act + kMaxExperts);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   gu.xin = x_perm; gu.offsets = offsets; gu.active = act; gu.n_active = act + kMaxExperts;
   gu.tab = &tab; gu.out = h;
-  int r = launch_gemm(gu, pg, part, ctr, st);
+  int r = launch_gemm(gu, pg, part, ctr, err, st);
   if (r != MOE_OK) return r;
   dn.xin = h; dn.offsets = offsets; dn.active = act; dn.n_active = act + kMaxExperts;
   dn.tab = &tab; dn.out = y_perm;
-  return launch_gemm(dn, pd, part, ctr, st);
+  return launch_gemm(dn, pd, part, ctr, err, st);
 }
 
 int moe_combine(const uint16_t* y_perm, const int32_t* pos, const float* w, int T, int k, int H,
@@ -330,6 +352,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   LayerScratch s{};
   carve(c, L, T, P, &s);
   MOE_REQUIRE(c.ok());
+  MOE_CUDA_TRY(cudaMemsetAsync(s.err, 0, sizeof(int32_t), s0));
 
   if ((r = phase(0)) != MOE_OK) return r;
   // A1-A4: route, dispatch and gather into expert order

@@ -24,8 +24,11 @@
 // finish a (expert, row block) -- found with one atomic counter, no waiting -- sums the splits
 // in split order and runs the epilogue, so results do not depend on scheduling.
 #include "expert_ffn.cuh"
+#include "tc_gemm.cuh"
 
 namespace moe {
+
+int g_ffn_path = 0;
 
 struct GemmKParams {
   const uint16_t* xin;
@@ -262,6 +265,11 @@ GemmPlan plan_gemm(const GemmArgs& a) {
   const size_t mp = (size_t)(a.fused ? 2 : 1) * a.M;
   g.part_elems = g.splits > 1 ? (size_t)g.splits * a.max_rows * mp : 0;
   g.counter_elems = g.splits > 1 ? (size_t)g.A_max * g.m_blocks : 0;
+  const bool tc_ok = tc_supported(a);
+  g.use_tc = tc_ok && (g_ffn_path == 2 || (g_ffn_path == 0 && avg >= 32));
+  g.tc = plan_tc(a);
+  g.part_elems = std::max(g.part_elems, g.tc.part_elems);
+  g.counter_elems = std::max(g.counter_elems, g.tc.counter_elems);
   return g;
 }
 
@@ -284,8 +292,9 @@ static void launch_nt(int nt, dim3 grid, const GemmKParams& kp, cudaStream_t st)
 }
 
 int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* counters,
-                cudaStream_t st) {
+                int32_t* err, cudaStream_t st) {
   if (a.max_rows <= 0) return MOE_OK;
+  if (g.use_tc) return launch_tc(a, g.tc, part, counters, err, st);
   GemmKParams kp{};
   kp.xin = a.xin; kp.offsets = a.offsets; kp.active = a.active; kp.n_active = a.n_active;
   kp.w_off = a.w_off; kp.s_off = a.s_off; kp.K = a.K; kp.M = a.M;

@@ -29,15 +29,26 @@ struct GemmArgs {
   uint16_t* out;            // [rows][M]
 };
 
+struct TcPlanLite {
+  int BN, S, kt_per_split;
+  size_t part_elems, counter_elems;
+};
+
 struct GemmPlan {
   int A_max;                // upper bound of experts with rows
   int m_blocks, splits, k_per_split, nt;
   size_t part_elems, counter_elems;
+  int use_tc;               // 1: tcgen05 kernel, 0: mma.sync streaming kernel
+  TcPlanLite tc;
 };
+
+// Process-wide choice of the expert FFN kernel: 0 = automatic, 1 = mma.sync streaming kernel,
+// 2 = tcgen05 kernel (where supported).
+extern int g_ffn_path;
 
 GemmPlan plan_gemm(const GemmArgs& a);
 size_t gemm_scratch(WsCursor& c, const GemmPlan& g, float** part, int32_t** counters);
 int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* counters,
-                cudaStream_t st);
+                int32_t* err, cudaStream_t st);
 
 }  // namespace moe

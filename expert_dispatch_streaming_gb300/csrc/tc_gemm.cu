@@ -1,0 +1,497 @@
+// Grouped expert GEMM on the 5th-generation tensor cores (tcgen05 + TMEM), sm_103a.
+//
+// Computes, for every expert e that received rows [r0, r0 + n_e) of the permuted activations,
+//   D[m][n] = sum_k W_e[m][k] * X[r0 + n][k]
+// with W_e the expert's weight rows (gate and up rows for the first GEMM, down rows for the
+// second) and X the token rows; the epilogue writes bf16(silu(gate) * up) (fused) or bf16(D).
+// This is the grouped SwiGLU FFN of the MoE layer: only experts a batch selected are touched
+// ("NovaLLM: Running Massive MoE Models Fully In-Memory", "3. Optimization #1 -- Expert-Level
+// Streaming").
+//
+// Persistent kernel, one CTA per SM, warp-specialised:
+//   warp 0      producer: per 64-wide K step, one 1-D bulk copy per 128-row weight tile (the
+//               bundle stores each tile as its 128-byte-swizzled shared-memory image) and one
+//               2-D TMA load of the BN token rows (128-byte swizzle), completing on an mbarrier;
+//   warp 1      MMA issuer: allocates TMEM, issues tcgen05.mma (M = 128 weight rows, N = BN
+//               tokens, K = 16) from shared-memory descriptors, commits stage release and
+//               accumulator-ready to mbarriers;
+//   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulators (each warp owns one 32-lane
+//               quarter of TMEM), SiLU * mul, bf16 stores (or fp32 split-K partials).
+// Work unit = (expert with rows, 128-row weight tile, K split, BN token tile); units are
+// enumerated with the token tile fastest so CTAs running at the same time share a weight
+// tile through L2.  With split K, each split stores fp32 partials and the last CTA to finish
+// a tile (one atomic counter, no waiting) sums the splits in order.
+//
+// Every mbarrier wait is bounded (wall clock, ~2 s); on timeout the kernel records an error
+// word and leaves its loop, releasing TMEM before exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "expert_ffn.cuh"
+#include "tc_gemm.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr uint64_t kWaitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait; false (and an error code recorded) after ~2 s.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, int code) {
+  if (mbar_try(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(bar, parity)) return true;
+    if ((i & 255) == 0 && globaltimer() - t0 > kWaitNs) {
+      atomicExch(err, code);
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                       uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;                 // leading byte offset (unused for this layout)
+  d |= (uint64_t)(1024 >> 4) << 32;       // stride byte offset
+  d |= (uint64_t)1 << 46;                 // descriptor version
+  d |= (uint64_t)2 << 61;                 // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor of kind::f16: bf16 A and B, fp32 D, both K-major, M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
+         ((uint32_t)(M >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+template <int BN, bool FUSED>
+struct Cfg {
+  static constexpr int A_BYTES = 16384;                       // 128 rows x 64 k bf16
+  static constexpr int B_BYTES = BN * 128;                    // BN rows x 64 k bf16
+  static constexpr int STAGE = (FUSED ? 2 : 1) * A_BYTES + B_BYTES;
+  static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
+  static constexpr int ACC = (FUSED ? 2 : 1) * BN;            // TMEM columns per tile
+  static constexpr int BUFS = (2 * ACC <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS = ACC * BUFS <= 32 ? 32 : ACC * BUFS <= 64 ? 64
+                                 : ACC * BUFS <= 128 ? 128 : ACC * BUFS <= 256 ? 256 : 512;
+  static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 4096 /*barriers, prefix*/;
+};
+
+struct Unit {
+  int a, e, r0, ne, mt, ks, nt, tile;
+};
+
+// Maps unit index u to its (expert, row tile, split, token tile), from the per-expert prefix
+// of unit counts kept in shared memory.
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, int n_act,
+                                            int u, int BN, int MT) {
+  int lo = 0, hi = n_act - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (pref[mid] <= u) lo = mid;
+    else hi = mid - 1;
+  }
+  Unit x;
+  x.a = lo;
+  x.e = p.host_n >= 0 ? p.host_ids[lo] : p.active[lo];
+  x.r0 = p.offsets[x.e];
+  x.ne = p.offsets[x.e + 1] - x.r0;
+  const int nt_n = (x.ne + BN - 1) / BN;
+  int rem = u - pref[lo];
+  x.nt = rem % nt_n;
+  rem /= nt_n;
+  x.ks = rem % p.S;
+  x.mt = rem / p.S;
+  x.tile = pref[lo] / p.S + x.mt * nt_n + x.nt;
+  return x;
+}
+
+template <int BN, bool FUSED>
+__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<BN, FUSED>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + C::STAGES;
+  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  int* pref = reinterpret_cast<int*>(tmem_slot + 4);   // [kMaxExperts + 1]
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int MT = p.M / 128;
+  const int KT = p.K / 64;
+  const int n_act = p.host_n >= 0 ? p.host_n : *p.n_active;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&tfull[b]), 1);
+      mbar_init(smem_u32(&tempty[b]), 4);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (warp == 2) {
+    // prefix of unit counts over the experts with rows
+    int carry = 0;
+    for (int base = 0; base < n_act; base += 32) {
+      const int a = base + lane;
+      int cnt = 0;
+      if (a < n_act) {
+        const int e = p.host_n >= 0 ? p.host_ids[a] : p.active[a];
+        const int ne = p.offsets[e + 1] - p.offsets[e];
+        cnt = MT * p.S * ((ne + BN - 1) / BN);
+      }
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (a < n_act) pref[a] = carry + incl - cnt;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) pref[n_act] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = pref[n_act];
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
+        const char* wb = static_cast<const char*>(p.tab.p[x.e]) + p.w_off;
+        const int kt_lo = x.ks * p.kt_per_split, kt_hi = min(KT, kt_lo + p.kt_per_split);
+        for (int kt = kt_lo; kt < kt_hi; ++kt) {
+          if (!(ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, 1))) break;
+          const uint32_t fb = smem_u32(&full[stage]);
+          uint8_t* st = smem + stage * C::STAGE;
+          mbar_expect_tx(fb, C::STAGE);
+          bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
+          if (FUSED)
+            bulk_g2s(smem_u32(st + C::A_BYTES),
+                     wb + ((size_t)(x.mt + MT) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
+          tma_2d(smem_u32(st + (FUSED ? 2 : 1) * C::A_BYTES), &p.tmap_b, kt * 64,
+                 x.r0 + x.nt * BN, fb);
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, BN);
+      int stage = 0, buf = 0;
+      uint32_t phase = 0, aphase = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+        const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
+        const int kt_lo = x.ks * p.kt_per_split, kt_hi = min(KT, kt_lo + p.kt_per_split);
+        if (!(ok = mbar_wait(smem_u32(&tempty[buf]), aphase ^ 1, p.err, 2))) break;
+        tc_fence_after();
+        const uint32_t dg = tmem_base + buf * C::ACC;
+        for (int kt = kt_lo; kt < kt_hi; ++kt) {
+          if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 3))) break;
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * C::STAGE);
+          const uint32_t sb = sa + (FUSED ? 2 : 1) * C::A_BYTES;
+          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sb);
+          const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t acc = (kt > kt_lo || j > 0) ? 1u : 0u;
+            mma_bf16(dg, da + 2 * j, db + 2 * j, idesc, acc);
+            if (FUSED) mma_bf16(dg + BN, du + 2 * j, db + 2 * j, idesc, acc);
+          }
+          mma_commit(smem_u32(&empty[stage]));
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        }
+        mma_commit(smem_u32(&tfull[buf]));
+        if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 2..5)
+    const int q = warp & 3;                       // TMEM lane quarter of this warp
+    const int et = threadIdx.x - 64;              // 0..127
+    int buf = 0;
+    uint32_t aphase = 0;
+    bool ok = true;
+    const int MP = FUSED ? 2 * p.M : p.M;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
+      if (!(ok = mbar_wait(smem_u32(&tfull[buf]), aphase, p.err, 4))) break;
+      tc_fence_after();
+      const int m = x.mt * 128 + q * 32 + lane;
+      const int n_here = min(BN, x.ne - x.nt * BN);
+      const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::ACC;
+#pragma unroll 1
+      for (int c0 = 0; c0 < BN; c0 += 32) {
+        if (c0 >= n_here) break;   // warp-uniform
+        uint32_t g[32], v[32];
+        tmem_ld32(ta + c0, g);
+        if (FUSED) tmem_ld32(ta + BN + c0, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int n = c0 + j;
+          if (n < n_here) {
+            const size_t row = (size_t)(x.r0 + x.nt * BN + n);
+            const float gv = __uint_as_float(g[j]);
+            if (p.S == 1) {
+              const float o = FUSED ? silu_mul(gv, __uint_as_float(v[j])) : gv;
+              p.out[row * p.M + m] = float_to_bf16_bits(o);
+            } else {
+              float* pr = p.part + ((size_t)x.ks * p.max_rows + row) * MP;
+              pr[m] = gv;
+              if (FUSED) pr[p.M + m] = __uint_as_float(v[j]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
+      if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
+
+      if (p.S > 1) {
+        // each warp counts its arrival; the warp completing the 4 * S arrivals of this tile
+        // sums the partials of all 128 rows in split order (no barrier, nothing waits)
+        __threadfence();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+          const int prev = atomicAdd(&p.counters[x.tile], 1);
+          last = prev == 4 * p.S - 1;
+          if (last) p.counters[x.tile] = 0;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
+          for (int qq = 0; qq < 4; ++qq) {
+            const int mm = x.mt * 128 + qq * 32 + lane;
+            for (int n = 0; n < n_here; ++n) {
+              const size_t row = (size_t)(x.r0 + x.nt * BN + n);
+              float gs = 0.f, us = 0.f;
+              for (int sp = 0; sp < p.S; ++sp) {
+                const float* pr = p.part + ((size_t)sp * p.max_rows + row) * MP;
+                gs += __ldcg(pr + mm);
+                if (FUSED) us += __ldcg(pr + p.M + mm);
+              }
+              p.out[row * p.M + mm] = float_to_bf16_bits(FUSED ? silu_mul(gs, us) : gs);
+            }
+          }
+        }
+      }
+    }
+    (void)et;
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(C::TMEM_COLS));
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+template <int BN, bool FUSED>
+int launch_bn(TcParams& kp, cudaStream_t st) {
+  using C = Cfg<BN, FUSED>;
+  static bool attr = false;
+  if (!attr) {
+    MOE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<BN, FUSED>,
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
+    attr = true;
+  }
+  tc_gemm_kernel<BN, FUSED><<<sm_count(), kThreads, C::SMEM, st>>>(kp);
+  MOE_COUNT_LAUNCH();
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
+}  // namespace
+
+bool tc_supported(const GemmArgs& a) { return !a.int4; }
+
+int tc_bn_for(const GemmArgs& a) {
+  const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
+                                          : std::min(a.E, a.max_rows));
+  const int avg = ceil_div(std::max(a.max_rows, 1), A);
+  if (a.fused) return avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+  return avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+}
+
+TcPlan plan_tc(const GemmArgs& a) {
+  TcPlan t{};
+  t.BN = tc_bn_for(a);
+  const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
+                                          : std::min(a.E, a.max_rows));
+  const int MT = a.M / 128, KT = a.K / 64;
+  const int ntiles_est = A * MT * std::max(1, ceil_div(a.max_rows, A * t.BN));
+  int S = 1;
+  if (ntiles_est < sm_count()) S = std::min(KT, ceil_div(sm_count(), ntiles_est));
+  t.kt_per_split = ceil_div(KT, S);
+  t.S = ceil_div(KT, t.kt_per_split);
+  const size_t mp = (size_t)(a.fused ? 2 : 1) * a.M;
+  t.part_elems = t.S > 1 ? (size_t)t.S * a.max_rows * mp : 0;
+  t.counter_elems = (size_t)MT * (ceil_div(a.max_rows, t.BN) + A) + 1;
+  return t;
+}
+
+int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters, int32_t* err,
+              cudaStream_t st) {
+  if (a.max_rows <= 0 || a.host_n == 0) return MOE_OK;
+  auto enc = encode_fn();
+  if (!enc) return MOE_ERR_UNSUPPORTED;
+  TcParams kp{};
+  cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.max_rows};
+  cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)t.BN};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.xin), dims,
+          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MOE_ERR_INVALID_ARG;
+  kp.offsets = a.offsets;
+  kp.active = a.active;
+  kp.n_active = a.n_active;
+  kp.host_n = a.host_n;
+  for (int i = 0; i < (a.host_n > 0 ? a.host_n : 0); ++i) kp.host_ids[i] = (int16_t)a.host_ids[i];
+  kp.tab = *a.tab;
+  kp.w_off = a.w_off;
+  kp.K = a.K;
+  kp.M = a.M;
+  kp.S = t.S;
+  kp.kt_per_split = t.kt_per_split;
+  kp.max_rows = a.max_rows;
+  kp.out = a.out;
+  kp.part = part;
+  kp.counters = counters;
+  kp.err = err;
+  MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, t.counter_elems * sizeof(int32_t), st));
+  if (a.fused) {
+    switch (t.BN) {
+      case 32: return launch_bn<32, true>(kp, st);
+      case 64: return launch_bn<64, true>(kp, st);
+      case 128: return launch_bn<128, true>(kp, st);
+      default: return launch_bn<256, true>(kp, st);
+    }
+  }
+  switch (t.BN) {
+    case 32: return launch_bn<32, false>(kp, st);
+    case 64: return launch_bn<64, false>(kp, st);
+    case 128: return launch_bn<128, false>(kp, st);
+    default: return launch_bn<256, false>(kp, st);
+  }
+}
+
+}  // namespace moe

@@ -60,6 +60,20 @@ const char* moe_status_string(int status);
 /* Library version, (major << 16) | minor. */
 int moe_version(void);
 
+/* Process-wide options (set before enqueueing work; not thread-safe).
+ *  MOE_OPT_FFN_KERNEL: which expert-FFN kernel runs: 0 = automatic (default: the tensor-core
+ *    tcgen05 kernel when experts receive >= 32 rows on average and weights are bf16, else the
+ *    mma.sync weight-streaming kernel), 1 = always the streaming kernel, 2 = tcgen05 wherever
+ *    it supports the weight type.  Both compute the same layer; tests use it to cover both. */
+enum moe_option { MOE_OPT_FFN_KERNEL = 1 };
+int moe_set_option(int option, int value);
+
+/* Reads the device error word kept in the first 4 bytes of a moe_layer_forward or
+ * moe_grouped_swiglu workspace into *code (host) and waits for `stream`.  0 = no error; a
+ * non-zero code means a bounded wait inside a kernel of the last call on that workspace ran
+ * out of time and that call's outputs are invalid.  Blocking (test and debug use). */
+int moe_workspace_error(const void* ws, int32_t* code, void* stream);
+
 /* ------------------------------------------------------------------ enums */
 /* Gating of the router scores (the workloads' three families):
  *  SOFTMAX_RENORM:      choose top-k by logit; w = softmax over the chosen k   (Mixtral shape)
