@@ -222,7 +222,7 @@ def run_ours(args, rank, world, local_rank):
             r = measure(T, max(5, min(args.steps, 20)), 3, False)
             w = layer_work(cfg, T, r["n_unique"])
             sw = {"tokens_per_s": round(r["tokens_per_s"], 1), "ms_per_step": round(r["ms_per_step"], 4),
-                  "n_unique": r["n_unique"],
+                  "n_unique": r["n_unique"], "phase_ms": [round(v, 4) for v in r["phase_ms"]],
                   "layer_roofline": roofline_of(w["flops"], w["bytes"], r["ms_per_step"] / 1e3, pk)}
             gu_ms = r["phase_ms"][2]
             sw["gate_up_roofline"] = roofline_of(*w["gu"], gu_ms / 1e3, pk)

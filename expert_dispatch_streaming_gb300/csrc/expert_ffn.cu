@@ -266,7 +266,7 @@ GemmPlan plan_gemm(const GemmArgs& a) {
   g.part_elems = g.splits > 1 ? (size_t)g.splits * a.max_rows * mp : 0;
   g.counter_elems = g.splits > 1 ? (size_t)g.A_max * g.m_blocks : 0;
   const bool tc_ok = tc_supported(a);
-  g.use_tc = tc_ok && (g_ffn_path == 2 || (g_ffn_path == 0 && avg >= 32));
+  g.use_tc = tc_ok && g_ffn_path != 1;
   g.tc = plan_tc(a);
   g.part_elems = std::max(g.part_elems, g.tc.part_elems);
   g.counter_elems = std::max(g.counter_elems, g.tc.counter_elems);

@@ -62,9 +62,9 @@ int moe_version(void);
 
 /* Process-wide options (set before enqueueing work; not thread-safe).
  *  MOE_OPT_FFN_KERNEL: which expert-FFN kernel runs: 0 = automatic (default: the tensor-core
- *    tcgen05 kernel when experts receive >= 32 rows on average and weights are bf16, else the
- *    mma.sync weight-streaming kernel), 1 = always the streaming kernel, 2 = tcgen05 wherever
- *    it supports the weight type.  Both compute the same layer; tests use it to cover both. */
+ *    tcgen05 kernel wherever it supports the weight type, else the mma.sync weight-streaming
+ *    kernel), 1 = always the streaming kernel, 2 = tcgen05 wherever supported.  Both compute
+ *    the same layer; tests use the option to cover both. */
 enum moe_option { MOE_OPT_FFN_KERNEL = 1 };
 int moe_set_option(int option, int value);
 
