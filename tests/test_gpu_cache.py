@@ -1,0 +1,152 @@
+"""GPU tests of the expert-slot cache feeding the layer forward.
+
+The cache's hit / miss / eviction / slot trace must equal the LRU simulator's bit for bit, the
+stacked layers' outputs must match the oracle, and H2D bytes must equal misses x bundle size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as wl
+from oracle import bf16, moe_ref
+from oracle.lru_sim import LRUSim, CapacityError
+
+from gpu_util import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import expert_dispatch_streaming_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def syn(moe):
+    from expert_dispatch_streaming_gb300 import synthetic
+    return synthetic
+
+
+def small_stack(layers=4):
+    return wl.custom("stack", cfg_id=130, H=256, E=16, k=4, I=256, gating="softmax", Is=256,
+                     shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", layers=layers)
+
+
+def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000):
+    store, table = syn.host_bundle_table(cfg, cfg.layers)
+    nb = store.shape[1]
+    c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=n_slots * nb,
+                                    n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
+                                    timeout_ms=timeout_ms, verify_checksums=1, device=0)
+    return moe.moe_expert_cache_create(c), store, table
+
+
+def run_stack(moe, syn, cfg, cache, trace, T, steps):
+    layers = [syn.DeviceLayer(cfg, layer=l, cached=True) for l in range(cfg.layers)]
+    ws = layers[0].workspace(T)
+    outs = []
+    n_missed = 0
+    for s in range(steps):
+        x = syn.to_device_bits(wl.stream_tokens(cfg, T, s))
+        for l in range(cfg.layers):
+            ids = torch.from_numpy(np.ascontiguousarray(trace[s, l])).cuda()
+            y = torch.empty_like(x)
+            _, st = layers[l].forward(x, ws, out=y, forced_ids=ids, residual=x, cache=cache)
+            n_missed += st.n_missed
+            x = y
+        torch.cuda.synchronize()
+        assert moe.moe_workspace_error(ws) == 0
+        outs.append(syn.bits_of(x))
+    return outs, n_missed
+
+
+def oracle_stack(cfg, trace, T, step):
+    x = wl.stream_tokens(cfg, T, step)
+    xv = bf16.decode(x)
+    for l in range(cfg.layers):
+        r = moe_ref.layer_forward(cfg, l, bf16.to_bits(xv), forced_ids=trace[step, l])
+        xv = bf16.round_rne(xv + r["out"])
+    return xv
+
+
+@pytest.mark.parametrize("T,n_slots", [(1, 6), (3, 12), (5, 40)])
+def test_cache_trace_and_outputs_match(moe, syn, T, n_slots):
+    cfg = small_stack()
+    steps = 6
+    trace = wl.stream_trace(cfg, T, steps=steps)
+    cache, store, table = make_cache(moe, syn, cfg, n_slots)
+    try:
+        outs, n_missed = run_stack(moe, syn, cfg, cache, trace, T, steps)
+        got = moe.moe_expert_cache_trace(cache)
+        stats = moe.moe_expert_cache_stats(cache)
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+    sim = LRUSim(n_slots)
+    for s in range(steps):
+        for l in range(cfg.layers):
+            sim.request(l, np.unique(trace[s, l]).tolist())
+    assert got == sim.trace
+    misses = sum(r[3] for r in sim.trace)
+    assert stats["misses"] == misses == n_missed
+    assert stats["bytes_h2d"] == misses * store.shape[1]
+    for s in (0, steps - 1):
+        assert_close(outs[s], oracle_stack(cfg, trace, T, s), f"stack step {s}")
+
+
+def test_cache_capacity_error_and_evict(moe, syn):
+    cfg = small_stack(layers=2)
+    cache, store, table = make_cache(moe, syn, cfg, 3)
+    try:
+        used = np.zeros(cfg.E, np.uint8)
+        used[[1, 2, 3, 4]] = 1
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_expert_cache_request(cache, 0, used)
+        assert ei.value.status == moe.MOE_ERR_CAPACITY
+        assert moe.moe_expert_cache_stats(cache)["requests"] == 0
+        used[:] = 0
+        used[[1, 5, 9]] = 1
+        ptrs, nm = moe.moe_expert_cache_request(cache, 0, used)
+        assert nm == 3 and sum(p is not None for p in ptrs) == 3
+        moe.moe_expert_cache_release(cache, 0)
+        moe.moe_expert_cache_evict(cache, 0, 5)
+        moe.moe_expert_cache_evict(cache, 0, 7)           # not resident: no-op
+        used[:] = 0
+        used[[2]] = 1
+        ptrs2, nm = moe.moe_expert_cache_request(cache, 0, used)
+        assert nm == 1 and ptrs2[2] == ptrs[5]               # the freed slot is reused
+        moe.moe_expert_cache_sync(cache)
+        # the bundle in the slot is exactly the host bundle (one contiguous copy per miss)
+        nb = store.shape[1]
+        dev = torch.empty(nb, dtype=torch.uint8, device="cuda")
+        torch.cuda.synchronize()
+        import ctypes
+        rt = None
+        for name in ("libcudart.so.13", "/usr/local/cuda/lib64/libcudart.so", "libcudart.so"):
+            try:
+                rt = ctypes.CDLL(name)
+                break
+            except OSError:
+                continue
+        assert rt is not None
+        rt.cudaMemcpy.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+        assert rt.cudaMemcpy(dev.data_ptr(), ptrs2[2], nb, 3) == 0    # device to device
+        torch.cuda.synchronize()
+        assert torch.equal(dev.cpu(), store[0 * cfg.E + 2])
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+    sim = LRUSim(3)
+    with pytest.raises(CapacityError):
+        sim.request(0, [1, 2, 3, 4])
+
+
+def test_cache_corrupt_bundle_rejected(moe, syn):
+    cfg = small_stack(layers=2)
+    store, table = syn.host_bundle_table(cfg, cfg.layers)
+    store[5, 100] ^= 1
+    c = moe.moe_expert_cache_config(slot_bytes=store.shape[1], capacity_bytes=4 * store.shape[1],
+                                    n_layers=2, n_experts=cfg.E, bundles=table, timeout_ms=1000,
+                                    verify_checksums=1, device=0)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_expert_cache_create(c)
+    assert ei.value.status == moe.MOE_ERR_CORRUPT and ei.value.bad_index == 5
