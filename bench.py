@@ -256,6 +256,121 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def run_streamed(args, local_rank):
+    """Expert-streamed decode: 16 Qwen1.5-MoE-shaped layers, every routed bundle (16.6 GB) in
+    pinned host memory, a 4 GiB VRAM slot cache under LRU, 256 decode steps per batch size,
+    routing injected from the seeded locality trace.  Also runs the same trace with every
+    bundle resident (a cache large enough for all bundles, pre-filled) for the overlap
+    fraction."""
+    import torch
+    import expert_dispatch_streaming_gb300 as moe
+    from expert_dispatch_streaming_gb300 import synthetic as syn
+
+    cfg = wl.STREAMED
+    dev = torch.device("cuda", local_rank)
+    t0 = time.time()
+    store, table = syn.host_bundle_table(cfg, cfg.layers)
+    nb = store.shape[1]
+    layers = [syn.DeviceLayer(cfg, layer=l, cached=True, device=dev) for l in range(cfg.layers)]
+    setup_s = time.time() - t0
+
+    def make(cap_bytes):
+        c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=cap_bytes,
+                                        n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
+                                        timeout_ms=20000, verify_checksums=1, device=local_rank,
+                                        time_copies=1)
+        return moe.moe_expert_cache_create(c)
+
+    # probe: pinned H2D bandwidth of one bundle-sized copy on this box
+    d = torch.empty(nb, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    for _ in range(3):
+        with torch.cuda.stream(s):
+            d.copy_(store[0], non_blocking=True)
+    s.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        e0.record(s)
+        for i in range(40):
+            d.copy_(store[i % store.shape[0]], non_blocking=True)
+        e1.record(s)
+    s.synchronize()
+    probe_gbs = 40 * nb / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del d
+
+    stream = torch.cuda.Stream(device=dev)
+    out = {"setup_s": round(setup_s, 1), "bundle_bytes": nb,
+           "cache_bytes": wl.STREAM_CACHE_BYTES, "slots": wl.STREAM_CACHE_BYTES // nb,
+           "probe_h2d_gbs": round(probe_gbs, 1), "steps": args.stream_steps, "T": {}}
+    for T in cfg.Ts:
+        trace = wl.stream_trace(cfg, T, steps=args.stream_steps)
+        ids_dev = torch.from_numpy(trace).to(dev)
+        xs = [syn.to_device_bits(wl.stream_tokens(cfg, T, st), dev) for st in range(args.stream_steps)]
+        ws = layers[0].workspace(T)
+        bufs = [torch.empty_like(xs[0]) for _ in range(2)]
+
+        def run(cache, steps):
+            with torch.cuda.stream(stream):
+                for st in range(steps):
+                    x = xs[st]
+                    for l in range(cfg.layers):
+                        y = bufs[l & 1]
+                        layers[l].forward(x, ws, out=y, forced_ids=ids_dev[st, l], residual=x,
+                                          cache=cache, stream=stream)
+                        x = y
+
+        res = {}
+        cache = make(wl.STREAM_CACHE_BYTES)
+        try:
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            w0 = time.perf_counter()
+            run(cache, args.stream_steps)
+            e1.record(stream)
+            stream.synchronize()
+            wall = time.perf_counter() - w0
+            t_stream = e0.elapsed_time(e1) / 1e3
+            st_ = moe.moe_expert_cache_stats(cache)
+            copy_ms, ncopies = moe.moe_expert_cache_copy_time(cache)
+            tr = moe.moe_expert_cache_trace(cache)
+        finally:
+            moe.moe_expert_cache_destroy(cache)
+        warm = [r for r in tr if r[0] >= 16 * cfg.layers]
+        res.update(tokens_per_s=round(T * args.stream_steps / t_stream, 1),
+                   ms_per_step=round(1e3 * t_stream / args.stream_steps, 3),
+                   wall_s=round(wall, 2),
+                   hit_rate=round(st_["hits"] / max(1, st_["hits"] + st_["misses"]), 4),
+                   hit_rate_after_step16=round(sum(1 - r[3] for r in warm) / max(1, len(warm)), 4),
+                   misses=st_["misses"], bytes_h2d=st_["bytes_h2d"],
+                   h2d_gbs=round(st_["bytes_h2d"] / max(copy_ms, 1e-9) / 1e6, 1),
+                   copy_busy_s=round(copy_ms / 1e3, 4))
+        res["h2d_frac_of_probe"] = round(res["h2d_gbs"] / probe_gbs, 4)
+        # the same ids with every bundle resident (pre-filled full-size cache)
+        full = make(cfg.layers * cfg.E * nb)
+        try:
+            run(full, min(args.stream_steps, 8))       # fill: every bundle copied once
+            stream.synchronize()
+            moe.moe_expert_cache_copy_time(full)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            run(full, args.stream_steps)
+            e1.record(stream)
+            stream.synchronize()
+            t_res = e0.elapsed_time(e1) / 1e3
+            assert moe.moe_expert_cache_stats(full)["misses"] <= cfg.layers * cfg.E
+        finally:
+            moe.moe_expert_cache_destroy(full)
+        res["resident_ms_per_step"] = round(1e3 * t_res / args.stream_steps, 3)
+        t_copy = copy_ms / 1e3
+        res["overlap_fraction"] = (round(min(1.0, max(0.0, 1 - (t_stream - t_res) / t_copy)), 4)
+                                   if t_copy > 0 else None)
+        out["T"][str(T)] = res
+        del xs, ids_dev, ws
+    del store
+    return out
+
+
 def oracle_sample(cfg, T_sample, weights_cache):
     """One oracle layer forward on T_sample tokens; returns seconds."""
     from oracle import moe_ref
@@ -292,6 +407,8 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
     ap.add_argument("--ffn-kernel", default="auto", choices=["auto", "stream", "tcgen05"])
+    ap.add_argument("--no-streamed", dest="streamed", action="store_false")
+    ap.add_argument("--stream-steps", type=int, default=wl.STREAM_STEPS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -336,6 +453,8 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_ours(args, rank, world, local_rank)
+    if args.streamed:
+        res["streamed_decode"] = run_streamed(args, local_rank)
     if rank == 0:
         if args.cpu:
             res["cpu_baseline"] = cpu_baseline(cfg)

@@ -56,7 +56,7 @@ class moe_expert_cache_config(C.Structure):
     _fields_ = [("slot_bytes", C.c_size_t), ("capacity_bytes", C.c_size_t),
                 ("n_layers", C.c_int), ("n_experts", C.c_int),
                 ("bundles", C.POINTER(moe_host_bundle)), ("timeout_ms", C.c_int),
-                ("verify_checksums", C.c_int), ("device", C.c_int)]
+                ("verify_checksums", C.c_int), ("device", C.c_int), ("time_copies", C.c_int)]
 
 
 class moe_cache_event(C.Structure):
@@ -130,6 +130,7 @@ _SIGS = {
     "moe_expert_cache_reset_trace": (_i, [_vp]),
     "moe_expert_cache_stats": (_i, [_vp, C.POINTER(moe_cache_stats)]),
     "moe_expert_cache_sync": (_i, [_vp]),
+    "moe_expert_cache_copy_time": (_i, [_vp, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
     "moe_layer_workspace_size": (_sz, [C.POINTER(moe_layer), _i]),
     "moe_layer_forward": (_i, [C.POINTER(moe_layer), _vp, _i, _vp, _vp, _vp, _vp,
                                C.POINTER(moe_layer_stats), _vp, _vp, _vp, _sz, _vp]),
@@ -314,6 +315,13 @@ def moe_expert_cache_stats(cache) -> dict:
 
 def moe_expert_cache_sync(cache) -> None:
     _check(_lib.moe_expert_cache_sync(cache), "moe_expert_cache_sync")
+
+
+def moe_expert_cache_copy_time(cache) -> tuple[float, int]:
+    ms, n = C.c_double(0), C.c_int64(0)
+    _check(_lib.moe_expert_cache_copy_time(cache, C.byref(ms), C.byref(n)),
+           "moe_expert_cache_copy_time")
+    return ms.value, n.value
 
 
 def moe_layer_workspace_size(layer: moe_layer, T) -> int:

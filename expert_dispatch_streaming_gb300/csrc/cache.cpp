@@ -45,6 +45,8 @@ static void destroy_all(moe_expert_cache* c) {
   cudaSetDevice(c->device);
   if (c->copy) cudaStreamSynchronize(c->copy);
   for (auto e : c->ready) if (e) cudaEventDestroy(e);
+  for (auto& pr : c->timed) { cudaEventDestroy(pr.first); cudaEventDestroy(pr.second); }
+  for (auto& pr : c->pool) { cudaEventDestroy(pr.first); cudaEventDestroy(pr.second); }
   for (auto e : c->layer_done) if (e) cudaEventDestroy(e);
   if (c->last_copy) cudaEventDestroy(c->last_copy);
   if (c->d2h) cudaEventDestroy(c->d2h);
@@ -132,8 +134,23 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
       if (vl >= 0 && c->layer_done_valid[vl])
         MOE_CUDA_TRY(cudaStreamWaitEvent(c->copy, c->layer_done[vl], 0));
       const moe_host_bundle& hb = c->bundles[(size_t)layer * c->E + e];
+      std::pair<cudaEvent_t, cudaEvent_t> tev{nullptr, nullptr};
+      if (c->time_copies) {
+        if (c->pool.empty()) {
+          MOE_CUDA_TRY(cudaEventCreate(&tev.first));
+          MOE_CUDA_TRY(cudaEventCreate(&tev.second));
+        } else {
+          tev = c->pool.back();
+          c->pool.pop_back();
+        }
+        MOE_CUDA_TRY(cudaEventRecord(tev.first, c->copy));
+      }
       MOE_CUDA_TRY(cudaMemcpyAsync(c->slab + (size_t)slot * c->slot_bytes, hb.ptr, hb.bytes,
                                    cudaMemcpyHostToDevice, c->copy));
+      if (c->time_copies) {
+        MOE_CUDA_TRY(cudaEventRecord(tev.second, c->copy));
+        c->timed.push_back(tev);
+      }
       MOE_CUDA_TRY(cudaEventRecord(c->ready[slot], c->copy));
       any_miss = true;
       if (misses) misses->push_back(e);
@@ -196,6 +213,7 @@ int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache
   c->L = cfg->n_layers;
   c->E = cfg->n_experts;
   c->timeout_ms = cfg->timeout_ms > 0 ? cfg->timeout_ms : 10000;
+  c->time_copies = cfg->time_copies;
   c->bundles.assign(cfg->bundles, cfg->bundles + nb);
   int cur = -1;
   cudaGetDevice(&cur);
@@ -316,6 +334,23 @@ int moe_expert_cache_sync(moe_expert_cache* cache) {
   if (!cache) return MOE_ERR_INVALID_ARG;
   MOE_CUDA_TRY(cudaEventRecord(cache->last_copy, cache->copy));
   return cache_wait_event(cache, cache->last_copy);
+}
+
+int moe_expert_cache_copy_time(moe_expert_cache* cache, double* ms, int64_t* n) {
+  if (!cache || !ms || !n) return MOE_ERR_INVALID_ARG;
+  *ms = 0.0;
+  *n = 0;
+  for (auto& pr : cache->timed) {
+    const int r = cache_wait_event(cache, pr.second);
+    if (r != MOE_OK) return r;
+    float t = 0.f;
+    MOE_CUDA_TRY(cudaEventElapsedTime(&t, pr.first, pr.second));
+    *ms += t;
+    ++*n;
+    cache->pool.push_back(pr);
+  }
+  cache->timed.clear();
+  return MOE_OK;
 }
 
 }  // extern "C"

@@ -33,6 +33,9 @@ struct moe_expert_cache {
   std::vector<moe_cache_event> trace;
   moe_cache_stats st{};
   long long req = 0;
+  // copy timing (time_copies): event pairs of copies not yet collected, and a free pool
+  int time_copies = 0;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed, pool;
 };
 
 namespace moe {

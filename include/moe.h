@@ -237,6 +237,7 @@ typedef struct moe_expert_cache_config {
   int timeout_ms;           /* deadline of every bounded host wait (<= 0: 10000 ms)     */
   int verify_checksums;     /* 1: hash every bundle at creation (MOE_ERR_CORRUPT)      */
   int device;               /* CUDA device ordinal of the slots                        */
+  int time_copies;          /* 1: bracket every miss copy with timing events           */
 } moe_expert_cache_config;
 
 /* One trace record per distinct expert of every request, in processing order. */
@@ -291,6 +292,10 @@ int moe_expert_cache_reset_trace(moe_expert_cache* cache);
 int moe_expert_cache_stats(const moe_expert_cache* cache, moe_cache_stats* out);
 /* Bounded wait until every copy issued so far has completed (MOE_ERR_TIMEOUT on deadline). */
 int moe_expert_cache_sync(moe_expert_cache* cache);
+/* With time_copies: waits (bounded) for the timed copies issued since the last call, then
+ * returns their summed copy-engine time in *ms and their count in *n (copy busy time, for
+ * the achieved H2D bandwidth).  Without time_copies: *ms = 0, *n = 0. */
+int moe_expert_cache_copy_time(moe_expert_cache* cache, double* ms, int64_t* n);
 
 /* ------------------------------------------------------------------ whole layer */
 typedef struct moe_layer {
