@@ -113,6 +113,8 @@ _SIGS = {
     "moe_route_workspace_size": (_sz, [_i, _i, _i, _i]),
     "moe_route_topk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
                             _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_route_topk_static": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_permute": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "moe_grouped_swiglu_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "moe_grouped_swiglu": (_i, [_vp, _vp, C.POINTER(_vp), _i, _i, _i, _i, _i, _vp, _vp, _sz,
@@ -229,6 +231,18 @@ def moe_route_topk(x, w_r, logit_bias, sel_bias, w_gate, forced_ids, T, H, E, k,
                                ptr(pos), ptr(src), ptr(logits), ptr(shared_gate),
                                ptr(tie_flags), ptr(ws), ws_bytes, stream_handle(stream)),
            "moe_route_topk")
+
+
+def moe_route_topk_static(x, w_r, logit_bias, sel_bias, w_gate, forced_ids, T, H, E, k, gating,
+                          scale, ids, w, counts, offsets, pos, src, logits, shared_gate,
+                          tie_flags, stream=None) -> None:
+    """moe_route_topk without a workspace (scratch in a fixed array of the library)."""
+    _check(_lib.moe_route_topk_static(ptr(x), ptr(w_r), ptr(logit_bias), ptr(sel_bias),
+                                      ptr(w_gate), ptr(forced_ids), T, H, E, k,
+                                      GATING.get(gating, gating), float(scale), ptr(ids), ptr(w),
+                                      ptr(counts), ptr(offsets), ptr(pos), ptr(src), ptr(logits),
+                                      ptr(shared_gate), ptr(tie_flags), stream_handle(stream)),
+           "moe_route_topk_static")
 
 
 def moe_permute(x, src, T, k, H, x_perm, stream=None) -> None:

@@ -173,6 +173,28 @@ int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
                    int32_t* src, float* logits, float* shared_gate, int32_t* tie_flags,
                    void* ws, size_t ws_bytes, void* stream);
 
+/* moe_route_topk_static -- moe_route_topk without a workspace, for callers that cannot
+ * allocate device memory.  The pages describe no counterpart; it exists for callers such as a
+ * plug-in inside a host framework that owns all device memory and forbids allocations of its
+ * own, or a latency-critical path where cudaMalloc / cudaFree (and the synchronisation they
+ * can cause) are not acceptable.
+ *
+ * Arguments, outputs and results are those of moe_route_topk; the scratch is a fixed 8 MiB
+ * array in the library's device memory (one per GPU that loads the library, held until the
+ * process exits).  Returns MOE_ERR_CAPACITY when moe_route_workspace_size(T, H, E, k) exceeds
+ * 8 MiB (for example T = 8192 with E = 256 needs more; T <= 2048 with E <= 256 fits).  Calls no
+ * allocating routine.  The first call on a device looks up the array's device address once
+ * (cudaGetSymbolAddress with that device current); make that first call before any stream
+ * capture.  Every call on a device shares the one array and it keeps the previous call's
+ * contents (the call clears what must start at zero itself): calls that can overlap on the
+ * GPU -- on different streams, or from different host threads -- race and must be serialised
+ * by the caller. */
+int moe_route_topk_static(const uint16_t* x, const float* w_r, const float* logit_bias,
+                          const float* sel_bias, const uint16_t* w_gate, const int32_t* forced_ids,
+                          int T, int H, int E, int k, int gating, float scale, int32_t* ids,
+                          float* w, int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
+                          float* logits, float* shared_gate, int32_t* tie_flags, void* stream);
+
 /* ------------------------------------------------------------------ step 4: permute
  * x_perm[p][:] = x[src[p] / k][:] for p in [0, T*k).
  *  x device [T][H] bf16, src device [T*k] int32, x_perm device [T*k][H] bf16.
