@@ -26,6 +26,9 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
+WORKLOADS = {"mixtral": wl.MIXTRAL, "qwen": wl.QWEN, "deepseek": wl.DEEPSEEK}
+WORKLOAD_NAMES = {"mixtral": "Mixtral-8x7B-shaped", "qwen": "Qwen1.5-MoE-A2.7B-shaped",
+                  "deepseek": "DeepSeek-V3-shaped INT4"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_HBM_GBS = 7900.0
 
@@ -108,8 +111,9 @@ def layer_work(cfg, T, n_unique):
     dn_flops = 2.0 * rows * I * H
     gu_bytes = n_unique * 2 * I * H * bpw + rows * H * 2 + rows * I * 2
     dn_bytes = n_unique * H * I * bpw + rows * I * 2 + rows * H * 2
-    flops = gu_flops + dn_flops + 2.0 * T * H * E
-    nbytes = n_unique * 3 * H * I * bpw + 4.0 * H * E + 2 * T * H * 2 + 2 * 2 * rows * H * 2
+    flops = gu_flops + dn_flops + 2.0 * T * H * E + 6.0 * T * H * cfg.Is
+    nbytes = (n_unique * 3 * H * I * bpw + 3 * H * cfg.Is * bpw + 4.0 * H * E + 2 * T * H * 2
+              + 2 * 2 * rows * H * 2)
     return dict(flops=flops, bytes=nbytes, gu=(gu_flops, gu_bytes), dn=(dn_flops, dn_bytes))
 
 
@@ -134,7 +138,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     moe.set_ffn_kernel(args.ffn_kernel)
-    cfg = wl.MIXTRAL
+    cfg = WORKLOADS[args.workload]
     pk = peaks()
     layer = syn.DeviceLayer(cfg, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -237,15 +241,16 @@ def run_ours(args, rank, world, local_rank):
     roof.update({"kernel": names[dom], "traffic": None, "peak_source": pk["source"],
                  "share_of_step": round(float(share[dom]), 4)})
     result = {
-        "metric": "MoE-layer tokens/s (Mixtral-8x7B-shaped layer)",
+        "metric": f"MoE-layer tokens/s ({WORKLOAD_NAMES[args.workload]} layer)",
         "value": round(head["tokens_per_s"], 1), "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(head["ms_per_step"], 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,0.02) weights, N(0,1) tokens)",
-        "config": {"workload": f"mixtral-8x7b-shaped MoE layer forward, T={args.T}",
-                   "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "T": args.T,
+        "config": {"workload": f"{WORKLOAD_NAMES[args.workload]} MoE layer forward, T={args.T}",
+                   "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I, "Is": cfg.Is,
+                   "weights": cfg.wdtype, "T": args.T,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "expert weights (2.82 GB) exceed L2 and are streamed every step"},
+                   "l2": "expert weights exceed L2 (126 MB) and are streamed every step"},
         "layer_roofline": roofline_of(w["flops"], w["bytes"], head["ms_per_step"] / 1e3, pk),
         "roofline": roof,
         "phase_ms": {n: round(v, 4) for n, v in zip(names, head["phase_ms"])},
@@ -402,7 +407,8 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--T", type=int, default=4096)
+    ap.add_argument("--T", type=int, default=None)
+    ap.add_argument("--workload", default="mixtral", choices=["mixtral", "qwen", "deepseek"])
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
@@ -411,10 +417,12 @@ def main():
     ap.add_argument("--stream-steps", type=int, default=wl.STREAM_STEPS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.T is None:
+        args.T = max(WORKLOADS[args.workload].Ts)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    cfg = wl.MIXTRAL
+    cfg = WORKLOADS[args.workload]
 
     if args.impl == "reference":
         # the reference arm is the CPU oracle, on rank 0 only
@@ -434,12 +442,12 @@ def main():
         secs = [oracle_sample(cfg, T_s, getw) for _ in range(args.steps)]
         tot = float(np.sum(secs))
         v = T_s * args.steps / tot
-        line = {"metric": "MoE-layer tokens/s (Mixtral-8x7B-shaped layer)", "value": round(v, 3),
+        line = {"metric": f"MoE-layer tokens/s ({WORKLOAD_NAMES[args.workload]} layer)", "value": round(v, 3),
                 "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(1e3 * tot / args.steps, 2), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "impl": "reference",
-                "config": {"workload": f"mixtral-8x7b-shaped MoE layer forward, T={args.T}",
+                "config": {"workload": f"{WORKLOAD_NAMES[args.workload]} MoE layer forward, T={args.T}",
                            "sample_tokens_per_step": T_s},
                 "cpu_baseline": {"value": round(v, 3), "unit": "tokens/s", "kind": "oracle",
                                  "cores": len(os.sched_getaffinity(0)),
