@@ -349,31 +349,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
 
       if (p.S > 1) {
-        // each warp counts its arrival; the warp completing the 4 * S arrivals of this tile
-        // sums the partials of all 128 rows in split order (no barrier, nothing waits)
+        // per (tile, lane quarter) arrival counter: the warp completing the S arrivals of its
+        // quarter sums that quarter's 32 rows over the splits in split order (no barrier,
+        // nothing waits, the four quarters reduce in parallel)
         __threadfence();
         __syncwarp();
         int last = 0;
+        int32_t* ctr = p.counters + (size_t)x.tile * 4 + q;
         if (lane == 0) {
-          const int prev = atomicAdd(&p.counters[x.tile], 1);
-          last = prev == 4 * p.S - 1;
-          if (last) p.counters[x.tile] = 0;
+          const int prev = atomicAdd(ctr, 1);
+          last = prev == p.S - 1;
+          if (last) *ctr = 0;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
-          for (int qq = 0; qq < 4; ++qq) {
-            const int mm = x.mt * 128 + qq * 32 + lane;
-            for (int n = 0; n < n_here; ++n) {
-              const size_t row = (size_t)(x.r0 + x.nt * BN + n);
-              float gs = 0.f, us = 0.f;
-              for (int sp = 0; sp < p.S; ++sp) {
-                const float* pr = p.part + ((size_t)sp * p.max_rows + row) * MP;
-                gs += __ldcg(pr + mm);
-                if (FUSED) us += __ldcg(pr + p.M + mm);
-              }
-              p.out[row * p.M + mm] = float_to_bf16_bits(FUSED ? silu_mul(gs, us) : gs);
+          for (int n = 0; n < n_here; ++n) {
+            const size_t row = (size_t)(x.r0 + x.nt * BN + n);
+            float gs = 0.f, us = 0.f;
+            for (int sp = 0; sp < p.S; ++sp) {
+              const float* pr = p.part + ((size_t)sp * p.max_rows + row) * MP;
+              gs += __ldcg(pr + m);
+              if (FUSED) us += __ldcg(pr + p.M + m);
             }
+            p.out[row * p.M + m] = float_to_bf16_bits(FUSED ? silu_mul(gs, us) : gs);
           }
         }
       }
@@ -435,15 +434,26 @@ TcPlan plan_tc(const GemmArgs& a) {
   t.BN = tc_bn_for(a);
   const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
                                           : std::min(a.E, a.max_rows));
-  const int MT = a.M / 128, KT = a.K / 64;
-  const int ntiles_est = A * MT * std::max(1, ceil_div(a.max_rows, A * t.BN));
+  const int MT = a.M / 128, KT = a.K / 64, sms = sm_count();
+  const int avg = ceil_div(std::max(a.max_rows, 1), A);
+  // narrower token tiles first (more tiles, weights re-read from L2 only), then split K
+  while (t.BN > 32 && A * MT * ceil_div(avg, t.BN) < sms &&
+         ceil_div(avg, t.BN / 2) > ceil_div(avg, t.BN))
+    t.BN /= 2;
+  const int ntiles_est = A * MT * std::max(1, ceil_div(avg, t.BN));
   int S = 1;
-  if (ntiles_est < sm_count()) S = std::min(KT, ceil_div(sm_count(), ntiles_est));
+  if (ntiles_est < sms) {
+    // split K, but keep the fp32 partial traffic below the weight bytes it parallelises
+    const double wbytes = (double)A * MT * 128 * a.K * 2.0 * (a.fused ? 2 : 1);
+    const double pbytes = (double)a.max_rows * (a.fused ? 2 : 1) * a.M * 8.0;
+    const int s_cap = std::max(1, (int)(wbytes / std::max(pbytes, 1.0)));
+    S = std::min({KT, ceil_div(sms, ntiles_est), s_cap});
+  }
   t.kt_per_split = ceil_div(KT, S);
   t.S = ceil_div(KT, t.kt_per_split);
   const size_t mp = (size_t)(a.fused ? 2 : 1) * a.M;
   t.part_elems = t.S > 1 ? (size_t)t.S * a.max_rows * mp : 0;
-  t.counter_elems = (size_t)MT * (ceil_div(a.max_rows, t.BN) + A) + 1;
+  t.counter_elems = 4 * ((size_t)MT * (ceil_div(a.max_rows, t.BN) + A) + 1);
   return t;
 }
 
