@@ -340,7 +340,15 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   const long long launches0 = g_launches;
   auto phase = [&](int i) -> int {
     if (pev && pev[i]) {
-      const cudaError_t e = cudaEventRecord((cudaEvent_t)pev[i], (cudaStream_t)stream);
+      // inside a stream capture an ordinary record only orders the graph; an external record
+      // makes the event fire on every replay of the caller's graph
+      cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+      cudaError_t e = cudaStreamIsCapturing((cudaStream_t)stream, &cs);
+      if (e != cudaSuccess) return fail_cuda(e);
+      e = cs == cudaStreamCaptureStatusActive
+              ? cudaEventRecordWithFlags((cudaEvent_t)pev[i], (cudaStream_t)stream,
+                                         cudaEventRecordExternal)
+              : cudaEventRecord((cudaEvent_t)pev[i], (cudaStream_t)stream);
       if (e != cudaSuccess) return fail_cuda(e);
     }
     return MOE_OK;
