@@ -441,13 +441,19 @@ TcPlan plan_tc(const GemmArgs& a) {
          ceil_div(avg, t.BN / 2) > ceil_div(avg, t.BN))
     t.BN /= 2;
   const int ntiles_est = A * MT * std::max(1, ceil_div(avg, t.BN));
+  // split K so that the units fill whole waves of the persistent grid: the time of a launch
+  // is ~ ceil(units / SMs) waves of 1/S of the K range each; fp32 partial traffic caps S
+  const double wbytes = (double)A * MT * 128 * a.K * 2.0 * (a.fused ? 2 : 1);
+  const double pbytes = (double)a.max_rows * (a.fused ? 2 : 1) * a.M * 8.0;
+  const int s_cap = std::min(KT, std::max(1, (int)(wbytes / std::max(pbytes, 1.0) / 4)));
   int S = 1;
-  if (ntiles_est < sms) {
-    // split K, but keep the fp32 partial traffic below the weight bytes it parallelises
-    const double wbytes = (double)A * MT * 128 * a.K * 2.0 * (a.fused ? 2 : 1);
-    const double pbytes = (double)a.max_rows * (a.fused ? 2 : 1) * a.M * 8.0;
-    const int s_cap = std::max(1, (int)(wbytes / std::max(pbytes, 1.0)));
-    S = std::min({KT, ceil_div(sms, ntiles_est), s_cap});
+  double best = (double)ceil_div(ntiles_est, sms);
+  for (int s = 2; s <= std::min(s_cap, 32); ++s) {
+    const double cost = (double)ceil_div(ntiles_est * s, sms) / s * (1.0 + 0.02 * (s - 1));
+    if (cost < best * 0.97) {
+      best = cost;
+      S = s;
+    }
   }
   t.kt_per_split = ceil_div(KT, S);
   t.S = ceil_div(KT, t.kt_per_split);
