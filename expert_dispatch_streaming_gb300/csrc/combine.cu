@@ -7,63 +7,71 @@
 #include "common.cuh"
 #include "route.cuh"
 
+#include <algorithm>
+
 namespace moe {
 
-__global__ void __launch_bounds__(256)
+constexpr int kCombineThreads = 128;  // one 16-byte vector (8 bf16) per thread
+
+// grid (ceil(H / 1024), T): block (c, t) covers elements [1024c, 1024c + 1024) of token t, so
+// every load of a block is issued at once, whatever T is
+__global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ pos,
                const float* __restrict__ w, int T, int k, int H,
                const uint16_t* __restrict__ shared, const float* __restrict__ shared_gate,
                const uint16_t* __restrict__ residual, uint16_t* __restrict__ out) {
-  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-  if (t >= T) return;
+  const int v = blockIdx.x * kCombineThreads + threadIdx.x;
+  if (v >= H / 8) return;
+  for (int t = blockIdx.y; t < T; t += gridDim.y) {
   int pj[kMaxK];
   float wj[kMaxK];
 #pragma unroll
   for (int j = 0; j < kMaxK; ++j) {
-    pj[j] = j < k ? pos[(size_t)t * k + j] : 0;
-    wj[j] = j < k ? w[(size_t)t * k + j] : 0.f;
+    pj[j] = j < k ? __ldg(pos + (size_t)t * k + j) : 0;
+    wj[j] = j < k ? __ldg(w + (size_t)t * k + j) : 0.f;
   }
-  const float gs = shared ? (shared_gate ? shared_gate[t] : 1.f) : 0.f;
-  const int nvec = H / 8;
-  for (int v = lane; v < nvec; v += 32) {
-    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  uint4 q[kMaxK];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(y + (size_t)pj[j] * H) + v);
-      const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+  for (int j = 0; j < kMaxK; ++j)
+    if (j < k) q[j] = __ldg(reinterpret_cast<const uint4*>(y + (size_t)pj[j] * H) + v);
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = bf16x2_to_float2(qw[i]);
-        acc[2 * i] = fmaf(wj[j], f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wj[j], f.y, acc[2 * i + 1]);
-      }
+  for (int j = 0; j < kMaxK; ++j) {
+    if (j >= k) break;
+    const uint32_t qw[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = bf16x2_to_float2(qw[i]);
+      acc[2 * i] = fmaf(wj[j], f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wj[j], f.y, acc[2 * i + 1]);
     }
-    if (shared) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(shared + (size_t)t * H) + v);
-      const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+  }
+  if (shared) {
+    const float gs = shared_gate ? __ldg(shared_gate + t) : 1.f;
+    const uint4 sq = __ldg(reinterpret_cast<const uint4*>(shared + (size_t)t * H) + v);
+    const uint32_t qw[4] = {sq.x, sq.y, sq.z, sq.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = bf16x2_to_float2(qw[i]);
-        acc[2 * i] = fmaf(gs, f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(gs, f.y, acc[2 * i + 1]);
-      }
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = bf16x2_to_float2(qw[i]);
+      acc[2 * i] = fmaf(gs, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(gs, f.y, acc[2 * i + 1]);
     }
-    uint32_t o[4];
-    if (residual) {
-      const uint4 q = __ldg(reinterpret_cast<const uint4*>(residual + (size_t)t * H) + v);
-      const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+  }
+  uint32_t o[4];
+  if (residual) {
+    const uint4 rq = __ldg(reinterpret_cast<const uint4*>(residual + (size_t)t * H) + v);
+    const uint32_t qw[4] = {rq.x, rq.y, rq.z, rq.w};
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 r = bf16x2_to_float2(qw[i]);
-        const float2 b = bf16x2_to_float2(float2_to_bf16x2(acc[2 * i], acc[2 * i + 1]));
-        o[i] = float2_to_bf16x2(r.x + b.x, r.y + b.y);
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) o[i] = float2_to_bf16x2(acc[2 * i], acc[2 * i + 1]);
+    for (int i = 0; i < 4; ++i) {
+      const float2 r = bf16x2_to_float2(qw[i]);
+      const float2 b = bf16x2_to_float2(float2_to_bf16x2(acc[2 * i], acc[2 * i + 1]));
+      o[i] = float2_to_bf16x2(r.x + b.x, r.y + b.y);
     }
-    reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o[i] = float2_to_bf16x2(acc[2 * i], acc[2 * i + 1]);
+  }
+  reinterpret_cast<uint4*>(out + (size_t)t * H)[v] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -71,8 +79,9 @@ int launch_combine(const uint16_t* y, const int32_t* pos, const float* w, int T,
                    const uint16_t* shared, const float* shared_gate, const uint16_t* residual,
                    uint16_t* out, cudaStream_t st) {
   if (T <= 0) return MOE_OK;
-  combine_kernel<<<ceil_div(T * 32, 256), 256, 0, st>>>(y, pos, w, T, k, H, shared,
-                                                        shared_gate, residual, out);
+  dim3 grid(ceil_div(H / 8, kCombineThreads), std::min(T, 65535));
+  combine_kernel<<<grid, kCombineThreads, 0, st>>>(y, pos, w, T, k, H, shared, shared_gate,
+                                                   residual, out);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;

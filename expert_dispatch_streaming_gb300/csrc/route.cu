@@ -133,6 +133,24 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// Sum of the S H-slice partials of one logit in a fixed order: four interleaved running sums
+// (slices s = 0, 4, 8, ... / 1, 5, ... / ...) combined as (a0 + a1) + (a2 + a3), so the loads
+// of four slices are in flight together and the result does not depend on scheduling.
+__device__ __forceinline__ float sum_slices(const float* p, int S, size_t stride) {
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+  int sp = 0;
+  for (; sp + 4 <= S; sp += 4) {
+    a0 += p[(size_t)sp * stride];
+    a1 += p[(size_t)(sp + 1) * stride];
+    a2 += p[(size_t)(sp + 2) * stride];
+    a3 += p[(size_t)(sp + 3) * stride];
+  }
+  if (sp < S) a0 += p[(size_t)sp * stride];
+  if (sp + 1 < S) a1 += p[(size_t)(sp + 1) * stride];
+  if (sp + 2 < S) a2 += p[(size_t)(sp + 2) * stride];
+  return (a0 + a1) + (a2 + a3);
+}
+
 // fp64 selection score of expert b for token t (the refinement of near-boundary experts)
 __device__ double exact_score(const GateParams& p, int t, int b, int lane) {
   double d = 0.0;
@@ -166,8 +184,7 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
       const int e = lane + 32 * c;
       float v = -CUDART_INF_F, s = -CUDART_INF_F;
       if (e < E) {
-        v = 0.f;
-        for (int sp = 0; sp < p.S; ++sp) v += p.part[((size_t)sp * p.T + t) * p.C + e];
+        v = sum_slices(p.part + (size_t)t * p.C + e, p.S, (size_t)p.T * p.C);
         if (p.logit_bias) v += p.logit_bias[e];
         s = v;
         if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
@@ -181,8 +198,7 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
       sc[c] = s;
     }
     if (lane == 0 && p.shared_gate && p.C > E) {
-      float z = 0.f;
-      for (int sp = 0; sp < p.S; ++sp) z += p.part[((size_t)sp * p.T + t) * p.C + E];
+      const float z = sum_slices(p.part + (size_t)t * p.C + E, p.S, (size_t)p.T * p.C);
       p.shared_gate[t] = 1.f / (1.f + expf(-z));
     }
 
@@ -469,8 +485,10 @@ RoutePlan plan_route(int T, int H, int E, int k, bool has_gate) {
   r.ntiles = ceil_div(T, kTileT);
   const int tiles = ceil_div(T, R_BT) * ceil_div(r.C, R_BC);
   const int target = 2 * sm_count();
+  // a small batch spreads the router read over the GPU in H slices of as few as 32 rows, so
+  // each CTA runs one or two load-compute iterations (the partials are summed by the gate)
   int S = 1;
-  if (tiles < target) S = std::min(std::max(1, H / 256), ceil_div(target, std::max(tiles, 1)));
+  if (tiles < target) S = std::min(std::max(1, H / R_KH), ceil_div(target, std::max(tiles, 1)));
   r.h_per_split = round_up(ceil_div(H, S), R_KH);
   r.S = ceil_div(H, r.h_per_split);
   return r;
