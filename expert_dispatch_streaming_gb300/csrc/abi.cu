@@ -202,8 +202,10 @@ int moe_workspace_error(const void* ws, int32_t* code, void* stream) {
 
 size_t moe_route_workspace_size(int T, int H, int E, int k) {
   if (!valid_route_shape(T, H, E, k)) return 0;
-  WsCursor c(nullptr, 0);
-  return route_scratch(c, plan_route(T, H, E, k, true), T, E, nullptr);
+  // the slice count depends on whether the shared-expert gate column is present: size for both
+  WsCursor a(nullptr, 0), b(nullptr, 0);
+  return std::max(route_scratch(a, plan_route(T, H, E, k, true), T, E, nullptr),
+                  route_scratch(b, plan_route(T, H, E, k, false), T, E, nullptr));
 }
 
 int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
