@@ -364,14 +364,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
+          const size_t stride = (size_t)p.max_rows * MP;
           for (int n = 0; n < n_here; ++n) {
             const size_t row = (size_t)(x.r0 + x.nt * BN + n);
-            float gs = 0.f, us = 0.f;
-            for (int sp = 0; sp < p.S; ++sp) {
-              const float* pr = p.part + ((size_t)sp * p.max_rows + row) * MP;
-              gs += __ldcg(pr + m);
-              if (FUSED) us += __ldcg(pr + p.M + m);
+            const float* pr = p.part + row * MP + m;
+            // four interleaved running sums keep four split loads in flight; fixed order
+            float g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f, u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
+            int sp = 0;
+            for (; sp + 4 <= p.S; sp += 4) {
+              g0 += __ldcg(pr + sp * stride);
+              g1 += __ldcg(pr + (sp + 1) * stride);
+              g2 += __ldcg(pr + (sp + 2) * stride);
+              g3 += __ldcg(pr + (sp + 3) * stride);
+              if (FUSED) {
+                u0 += __ldcg(pr + p.M + sp * stride);
+                u1 += __ldcg(pr + p.M + (sp + 1) * stride);
+                u2 += __ldcg(pr + p.M + (sp + 2) * stride);
+                u3 += __ldcg(pr + p.M + (sp + 3) * stride);
+              }
             }
+            for (; sp < p.S; ++sp) {
+              g0 += __ldcg(pr + sp * stride);
+              if (FUSED) u0 += __ldcg(pr + p.M + sp * stride);
+            }
+            const float gs = (g0 + g1) + (g2 + g3), us = (u0 + u1) + (u2 + u3);
             p.out[row * p.M + m] = float_to_bf16_bits(FUSED ? silu_mul(gs, us) : gs);
           }
         }
@@ -448,7 +464,7 @@ TcPlan plan_tc(const GemmArgs& a) {
   const int s_cap = std::min(KT, std::max(1, (int)(wbytes / std::max(pbytes, 1.0) / 4)));
   int S = 1;
   double best = (double)ceil_div(ntiles_est, sms);
-  for (int s = 2; s <= std::min(s_cap, 32); ++s) {
+  for (int s = 2; ntiles_est < sms && s <= std::min(s_cap, 32); ++s) {
     const double cost = (double)ceil_div(ntiles_est * s, sms) / s * (1.0 + 0.02 * (s - 1));
     if (cost < best * 0.97) {
       best = cost;
