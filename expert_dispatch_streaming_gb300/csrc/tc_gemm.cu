@@ -34,7 +34,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 192;
 constexpr uint64_t kWaitNs = 2000000000ull;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -141,16 +140,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
-template <int BN, bool FUSED>
+template <int BN, bool FUSED, bool INT4>
 struct Cfg {
+  static constexpr int NA = FUSED ? 2 : 1;                    // weight tiles per stage
   static constexpr int A_BYTES = 16384;                       // 128 rows x 64 k bf16
   static constexpr int B_BYTES = BN * 128;                    // BN rows x 64 k bf16
-  static constexpr int STAGE = (FUSED ? 2 : 1) * A_BYTES + B_BYTES;
+  // INT4: per 64-k step, half of an 8448-byte INT4 tile (4096 B of codes) + its 256 B scales
+  static constexpr int RAW_BYTES = INT4 ? 4096 + 256 : 0;
+  static constexpr int RAW_OFF = NA * A_BYTES + B_BYTES;
+  static constexpr int STAGE = (RAW_OFF + NA * RAW_BYTES + 1023) / 1024 * 1024;
+  static constexpr int TX = INT4 ? NA * RAW_BYTES + B_BYTES : NA * A_BYTES + B_BYTES;
   static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
-  static constexpr int ACC = (FUSED ? 2 : 1) * BN;            // TMEM columns per tile
+  static constexpr int ACC = NA * BN;                         // TMEM columns per tile
   static constexpr int BUFS = (2 * ACC <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = ACC * BUFS <= 32 ? 32 : ACC * BUFS <= 64 ? 64
                                  : ACC * BUFS <= 128 ? 128 : ACC * BUFS <= 256 ? 256 : 512;
+  static constexpr int THREADS = INT4 ? 320 : 192;            // + 4 dequant warps for INT4
   static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 4096 /*barriers, prefix*/;
 };
 
@@ -183,16 +188,18 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
   return x;
 }
 
-template <int BN, bool FUSED>
-__global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using C = Cfg<BN, FUSED>;
+template <int BN, bool FUSED, bool INT4>
+__global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ TcParams p) {
+  using C = Cfg<BN, FUSED, INT4>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
   uint64_t* full = bars;
   uint64_t* empty = bars + C::STAGES;
-  uint64_t* tfull = bars + 2 * C::STAGES;
+  uint64_t* afull = bars + 2 * C::STAGES;   // INT4: dequantised A tiles ready
+  uint64_t* tfull = bars + 3 * C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* pref = reinterpret_cast<int*>(tmem_slot + 4);   // [kMaxExperts + 1]
@@ -206,6 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
+      mbar_init(smem_u32(&afull[s]), 4);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -261,13 +269,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           if (!(ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, 1))) break;
           const uint32_t fb = smem_u32(&full[stage]);
           uint8_t* st = smem + stage * C::STAGE;
-          mbar_expect_tx(fb, C::STAGE);
-          bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
-          if (FUSED)
-            bulk_g2s(smem_u32(st + C::A_BYTES),
-                     wb + ((size_t)(x.mt + MT) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
-          tma_2d(smem_u32(st + (FUSED ? 2 : 1) * C::A_BYTES), &p.tmap_b, kt * 64,
-                 x.r0 + x.nt * BN, fb);
+          mbar_expect_tx(fb, C::TX);
+          if (INT4) {
+            // codes of this 64-k half of the 128-k INT4 tile, then the tile's row scales
+            for (int w = 0; w < C::NA; ++w) {
+              const char* tile = wb + ((size_t)(x.mt + w * MT) * (KT / 2) + (kt >> 1)) * 8448;
+              uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
+              bulk_g2s(smem_u32(raw), tile + (kt & 1) * 4096, 4096, fb);
+              bulk_g2s(smem_u32(raw + 4096), tile + 8192, 256, fb);
+            }
+          } else {
+            bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
+            if (FUSED)
+              bulk_g2s(smem_u32(st + C::A_BYTES),
+                       wb + ((size_t)(x.mt + MT) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
+          }
+          tma_2d(smem_u32(st + C::NA * C::A_BYTES), &p.tmap_b, kt * 64, x.r0 + x.nt * BN, fb);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -286,7 +303,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         tc_fence_after();
         const uint32_t dg = tmem_base + buf * C::ACC;
         for (int kt = kt_lo; kt < kt_hi; ++kt) {
-          if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 3))) break;
+          if (!(ok = mbar_wait(smem_u32(INT4 ? &afull[stage] : &full[stage]), phase, p.err, 3)))
+            break;
           tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * C::STAGE);
           const uint32_t sb = sa + (FUSED ? 2 : 1) * C::A_BYTES;
@@ -305,7 +323,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
       }
     }
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
     const int q = warp & 3;                       // TMEM lane quarter of this warp
     const int et = threadIdx.x - 64;              // 0..127
@@ -394,6 +412,58 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       }
     }
     (void)et;
+  } else if (INT4) {
+    // ------------------------------------------------------------ INT4 dequant (warps 6..9)
+    // thread = weight row r of the tile: 64 codes (two 16-byte chunks) -> bf16(code * scale),
+    // written as the row's eight 16-byte chunks of the 128-byte-swizzled K-major A image
+    const int r = threadIdx.x - 192;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    const uint32_t k136 = 0x43084308u;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
+      const int kt_lo = x.ks * p.kt_per_split, kt_hi = min(KT, kt_lo + p.kt_per_split);
+      for (int kt = kt_lo; kt < kt_hi; ++kt) {
+        if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
+        uint8_t* st = smem + stage * C::STAGE;
+#pragma unroll
+        for (int w = 0; w < C::NA; ++w) {
+          const uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
+          uint8_t* arow = st + w * C::A_BYTES + r * 128;
+          const uint32_t sb = *reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r);
+          const uint32_t s2 = sb | (sb << 16);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint4 q = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
+            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t v = qw[j];
+              uint32_t pr[4] = {(v & 0xFu) | ((v << 12) & 0xF0000u),
+                                ((v >> 8) & 0xFu) | ((v << 4) & 0xF0000u),
+                                ((v >> 16) & 0xFu) | ((v >> 4) & 0xF0000u),
+                                ((v >> 24) & 0xFu) | ((v >> 12) & 0xF0000u)};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                uint32_t b = (pr[i] ^ 0x00080008u) | 0x43004300u;  // 128 + code + 8
+                __nv_bfloat162 h = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&b),
+                                           *reinterpret_cast<const __nv_bfloat162*>(&k136));
+                h = __hmul2(h, *reinterpret_cast<const __nv_bfloat162*>(&s2));
+                pr[i] = *reinterpret_cast<uint32_t*>(&h);
+              }
+              const int oc = cc * 4 + j;
+              *reinterpret_cast<uint4*>(arow + ((oc ^ (r & 7)) << 4)) =
+                  make_uint4(pr[0], pr[1], pr[2], pr[3]);
+            }
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&afull[stage]));
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+      }
+    }
   }
 
   tc_fence_before();
@@ -418,31 +488,51 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BN, bool FUSED>
+template <int BN, bool FUSED, bool INT4>
 int launch_bn(TcParams& kp, cudaStream_t st) {
-  using C = Cfg<BN, FUSED>;
+  using C = Cfg<BN, FUSED, INT4>;
   static bool attr = false;
   if (!attr) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<BN, FUSED>,
+    MOE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<BN, FUSED, INT4>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr = true;
   }
-  tc_gemm_kernel<BN, FUSED><<<sm_count(), kThreads, C::SMEM, st>>>(kp);
+  tc_gemm_kernel<BN, FUSED, INT4><<<sm_count(), C::THREADS, C::SMEM, st>>>(kp);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
 
+template <bool INT4>
+int dispatch_bn(bool fused, int BN, TcParams& kp, cudaStream_t st) {
+  if (fused) {
+    switch (BN) {
+      case 32: return launch_bn<32, true, INT4>(kp, st);
+      case 64: return launch_bn<64, true, INT4>(kp, st);
+      case 128: return launch_bn<128, true, INT4>(kp, st);
+      default: return launch_bn<256, true, INT4>(kp, st);
+    }
+  }
+  switch (BN) {
+    case 32: return launch_bn<32, false, INT4>(kp, st);
+    case 64: return launch_bn<64, false, INT4>(kp, st);
+    case 128: return launch_bn<128, false, INT4>(kp, st);
+    default: return launch_bn<256, false, INT4>(kp, st);
+  }
+}
+
 }  // namespace
 
-bool tc_supported(const GemmArgs& a) { return !a.int4; }
+bool tc_supported(const GemmArgs& a) { return a.K % 128 == 0 && a.M % 128 == 0; }
 
 int tc_bn_for(const GemmArgs& a) {
   const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
                                           : std::min(a.E, a.max_rows));
   const int avg = ceil_div(std::max(a.max_rows, 1), A);
-  if (a.fused) return avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
-  return avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+  // fused INT4 stages carry two dequantised A tiles: cap the token tile at 128 to keep 3 stages
+  const int cap = (a.int4 && a.fused) ? 128 : 256;
+  const int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+  return std::min(bn, cap);
 }
 
 TcPlan plan_tc(const GemmArgs& a) {
@@ -459,7 +549,7 @@ TcPlan plan_tc(const GemmArgs& a) {
   const int ntiles_est = A * MT * std::max(1, ceil_div(avg, t.BN));
   // split K so that the units fill whole waves of the persistent grid: the time of a launch
   // is ~ ceil(units / SMs) waves of 1/S of the K range each; fp32 partial traffic caps S
-  const double wbytes = (double)A * MT * 128 * a.K * 2.0 * (a.fused ? 2 : 1);
+  const double wbytes = (double)A * MT * 128 * a.K * (a.int4 ? 0.53 : 2.0) * (a.fused ? 2 : 1);
   const double pbytes = (double)a.max_rows * (a.fused ? 2 : 1) * a.M * 8.0;
   const int s_cap = std::min(KT, std::max(1, (int)(wbytes / std::max(pbytes, 1.0) / 4)));
   int S = 1;
@@ -510,20 +600,7 @@ int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters
   kp.counters = counters;
   kp.err = err;
   MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, t.counter_elems * sizeof(int32_t), st));
-  if (a.fused) {
-    switch (t.BN) {
-      case 32: return launch_bn<32, true>(kp, st);
-      case 64: return launch_bn<64, true>(kp, st);
-      case 128: return launch_bn<128, true>(kp, st);
-      default: return launch_bn<256, true>(kp, st);
-    }
-  }
-  switch (t.BN) {
-    case 32: return launch_bn<32, false>(kp, st);
-    case 64: return launch_bn<64, false>(kp, st);
-    case 128: return launch_bn<128, false>(kp, st);
-    default: return launch_bn<256, false>(kp, st);
-  }
+  return a.int4 ? dispatch_bn<true>(a.fused, t.BN, kp, st) : dispatch_bn<false>(a.fused, t.BN, kp, st);
 }
 
 }  // namespace moe

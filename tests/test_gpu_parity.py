@@ -247,3 +247,14 @@ def test_int4_bundle_with_foreign_scales_fails_parity(moe, syn):
     assert_close(syn.bits_of(o1), ref["out"], "good bundles")
     with pytest.raises(AssertionError):
         assert_close(syn.bits_of(o2), ref["out"], "foreign scales")
+
+
+@pytest.mark.parametrize("cfg", [SMALL[1], SMALL[3], SMALL[4]], ids=lambda c: c.name)
+@pytest.mark.parametrize("T", [1, 133])
+def test_layer_forward_streaming_kernel(moe, syn, cfg, T):
+    """The mma.sync weight-streaming FFN kernel (forced), bf16 and INT4."""
+    moe.set_ffn_kernel("stream")
+    try:
+        _layer_case(syn, cfg, T)
+    finally:
+        moe.set_ffn_kernel("auto")
