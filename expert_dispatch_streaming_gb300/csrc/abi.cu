@@ -204,6 +204,8 @@ size_t moe_route_workspace_size(int T, int H, int E, int k) {
   if (!valid_route_shape(T, H, E, k)) return 0;
   // the slice count depends on whether the shared-expert gate column is present: size for both
   WsCursor a(nullptr, 0), b(nullptr, 0);
+  a.take<int32_t>(64);
+  b.take<int32_t>(64);
   return std::max(route_scratch(a, plan_route(T, H, E, k, true), T, E, nullptr),
                   route_scratch(b, plan_route(T, H, E, k, false), T, E, nullptr));
 }
@@ -221,15 +223,17 @@ int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
   MOE_REQUIRE(!w_gate || shared_gate);
   const RoutePlan rp = plan_route(T, H, E, k, w_gate != nullptr);
   WsCursor c(ws, ws_bytes);
+  int32_t* err = c.take<int32_t>(64);
   RouteScratch s{};
   route_scratch(c, rp, T, E, &s);
   MOE_REQUIRE(c.ok());
+  if (rp.tc) MOE_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int32_t), (cudaStream_t)stream));
   RouteArgs a{};
   a.x = x; a.w_r = w_r; a.logit_bias = logit_bias; a.sel_bias = sel_bias; a.w_gate = w_gate;
   a.forced = forced_ids; a.T = T; a.H = H; a.E = E; a.k = k; a.gating = gating;
   a.scale = scale; a.ids = ids; a.counts = counts; a.offsets = offsets; a.pos = pos;
   a.src = src; a.tie_flags = tie_flags; a.w = w; a.logits = logits;
-  a.shared_gate = shared_gate; a.x_perm = nullptr;
+  a.shared_gate = shared_gate; a.x_perm = nullptr; a.err = err;
   return launch_route(a, rp, s, (cudaStream_t)stream);
 }
 
@@ -372,7 +376,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   ra.forced = forced_ids; ra.T = T; ra.H = L->H; ra.E = L->E; ra.k = L->k;
   ra.gating = L->gating; ra.scale = L->scale; ra.ids = s.ids; ra.counts = s.counts;
   ra.offsets = s.offsets; ra.pos = s.pos; ra.src = s.src; ra.tie_flags = s.tie; ra.w = s.w;
-  ra.logits = nullptr; ra.shared_gate = s.shared_gate; ra.x_perm = s.x_perm;
+  ra.logits = nullptr; ra.shared_gate = s.shared_gate; ra.x_perm = s.x_perm; ra.err = s.err;
   r = launch_route(ra, P.rp, s.rs, s0);
   if (r != MOE_OK) return r;
   if ((r = phase(1)) != MOE_OK) return r;

@@ -20,6 +20,7 @@
 //                          the row copy x -> x_perm with 16-byte vector loads and stores.
 #include "common.cuh"
 #include "route.cuh"
+#include "tc_gemm.cuh"
 
 #include <math_constants.h>
 
@@ -153,10 +154,24 @@ __device__ __forceinline__ float sum_slices(const float* p, int S, size_t stride
 
 // fp64 selection score of expert b for token t (the refinement of near-boundary experts)
 __device__ double exact_score(const GateParams& p, int t, int b, int lane) {
-  double d = 0.0;
   const uint16_t* xr = p.x + (size_t)t * p.H;
-  for (int h = lane; h < p.H; h += 32)
-    d = fma((double)bf16_bits_to_float(xr[h]), (double)p.w_r[(size_t)h * p.E + b], d);
+  double d0 = 0.0, d1 = 0.0, d2 = 0.0, d3 = 0.0;
+  if (p.w_rT) {
+    // coalesced reads of the transposed router row; four interleaved fp64 sums (fixed order)
+    const float* wr = p.w_rT + (size_t)b * p.H;
+    int h = lane;
+    for (; h + 96 < p.H; h += 128) {
+      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wr[h], d0);
+      d1 = fma((double)bf16_bits_to_float(xr[h + 32]), (double)wr[h + 32], d1);
+      d2 = fma((double)bf16_bits_to_float(xr[h + 64]), (double)wr[h + 64], d2);
+      d3 = fma((double)bf16_bits_to_float(xr[h + 96]), (double)wr[h + 96], d3);
+    }
+    for (; h < p.H; h += 32) d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wr[h], d0);
+  } else {
+    for (int h = lane; h < p.H; h += 32)
+      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)p.w_r[(size_t)h * p.E + b], d0);
+  }
+  double d = (d0 + d1) + (d2 + d3);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
   if (p.logit_bias) d += (double)p.logit_bias[b];
@@ -165,6 +180,58 @@ __device__ double exact_score(const GateParams& p, int t, int b, int lane) {
     if (p.sel_bias) d += (double)p.sel_bias[b];
   }
   return d;
+}
+
+// Tensor-core router input: the router (and shared-expert gate vector as row E) split into three
+// bf16 pieces hi + mid + lo (each the bf16 rounding of what the previous pieces leave), which
+// represent the fp32 weight; written as a tiled 128-byte-swizzled bf16 image of [Mpad x 3H]
+// (piece p of row m at k-tile p * H/64 + k/64), plus the transposed fp32 router for the fp64
+// re-scoring.  Thread = (row m, 8-element chunk of k).  Block 0 also clears the histogram and
+// writes the one-group dispatch {0, T, 0, 1} the router GEMM runs over.
+__global__ void __launch_bounds__(256)
+router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w_gate, int H,
+                   int E, int Mpad, int T, uint16_t* __restrict__ img, float* __restrict__ w_rT,
+                   int32_t* __restrict__ hist, int hist_n, int32_t* __restrict__ meta) {
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < hist_n; i += blockDim.x) hist[i] = 0;
+    if (threadIdx.x == 0) { meta[0] = 0; meta[1] = T; meta[2] = 0; meta[3] = 1; }
+  }
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int chunks = H / 8;
+  if (idx >= (size_t)Mpad * chunks) return;
+  const int m = (int)(idx % Mpad), ch = (int)(idx / Mpad);
+  const int KTB = H / 64, mt = m >> 7, r = m & 127;
+  uint32_t pc[3][4];
+  float v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int h = ch * 8 + i;
+    v[i] = m < E ? w_r[(size_t)h * E + m]
+                 : (m == E && w_gate ? bf16_bits_to_float(w_gate[h]) : 0.f);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    float a = v[i], b = v[i + 1];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+      const uint32_t w = float2_to_bf16x2(a, b);
+      pc[q][i / 2] = w;
+      const float2 f = bf16x2_to_float2(w);
+      a -= f.x;
+      b -= f.y;
+    }
+  }
+  const int kt = ch >> 3, c = ch & 7;
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    uint16_t* tile = img + ((size_t)mt * (3 * KTB) + q * KTB + kt) * 8192;
+    *reinterpret_cast<uint4*>(tile + r * 64 + ((c ^ (r & 7)) << 3)) =
+        make_uint4(pc[q][0], pc[q][1], pc[q][2], pc[q][3]);
+  }
+  if (m < E && w_rT) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w_rT[(size_t)m * H + ch * 8 + i] = v[i];
+  }
 }
 
 __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
@@ -483,6 +550,13 @@ RoutePlan plan_route(int T, int H, int E, int k, bool has_gate) {
   RoutePlan r{};
   r.C = E + (has_gate ? 1 : 0);
   r.ntiles = ceil_div(T, kTileT);
+  if (T >= kTcRouterMinT && H % 64 == 0) {
+    r.tc = 1;
+    r.Mpad = (int)round_up(r.C, 128);
+    r.S = 1;
+    r.h_per_split = H;
+    return r;
+  }
   const int tiles = ceil_div(T, R_BT) * ceil_div(r.C, R_BC);
   const int target = 2 * sm_count();
   // a small batch spreads the router read over the GPU in H slices of as few as 32 rows, so
@@ -502,6 +576,12 @@ size_t route_scratch(WsCursor& c, const RoutePlan& r, int T, int E, RouteScratch
   s.active = c.take<int32_t>(kMaxExperts);
   s.n_active = c.take<int32_t>(32);
   s.shared_meta = c.take<int32_t>(32);
+  s.img = nullptr;
+  s.w_rT = nullptr;
+  if (r.tc) {
+    s.img = c.take<uint16_t>((size_t)3 * r.Mpad * r.h_per_split);
+    s.w_rT = c.take<float>((size_t)E * r.h_per_split);
+  }
   if (out) *out = s;
   return c.used;
 }
@@ -509,14 +589,26 @@ size_t route_scratch(WsCursor& c, const RoutePlan& r, int T, int E, RouteScratch
 int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
                  cudaStream_t st) {
   if (a.T > 0) {
-    dim3 g1(ceil_div(a.T, R_BT), ceil_div(r.C, R_BC), r.S);
-    router_partial_kernel<<<g1, 256, 0, st>>>(a.x, a.w_r, a.w_gate, a.T, a.H, a.E, r.C,
-                                              r.h_per_split, s.part, s.hist, r.ntiles * a.E);
-    MOE_COUNT_LAUNCH();
-    MOE_LAUNCH_CHECK();
+    if (r.tc) {
+      const size_t thr = (size_t)r.Mpad * (a.H / 8);
+      router_prep_kernel<<<(unsigned)ceil_div((int)thr, 256), 256, 0, st>>>(
+          a.w_r, a.w_gate, a.H, a.E, r.Mpad, a.T, s.img, s.w_rT, s.hist, r.ntiles * a.E,
+          s.shared_meta);
+      MOE_COUNT_LAUNCH();
+      MOE_LAUNCH_CHECK();
+      const int rr = launch_tc_router(a.x, a.T, a.H, s.img, r.Mpad, r.C, s.shared_meta, s.part,
+                                      a.err, st);
+      if (rr != MOE_OK) return rr;
+    } else {
+      dim3 g1(ceil_div(a.T, R_BT), ceil_div(r.C, R_BC), r.S);
+      router_partial_kernel<<<g1, 256, 0, st>>>(a.x, a.w_r, a.w_gate, a.T, a.H, a.E, r.C,
+                                                r.h_per_split, s.part, s.hist, r.ntiles * a.E);
+      MOE_COUNT_LAUNCH();
+      MOE_LAUNCH_CHECK();
+    }
     GateParams p{};
     p.part = s.part; p.S = r.S; p.C = r.C;
-    p.x = a.x; p.w_r = a.w_r; p.logit_bias = a.logit_bias; p.sel_bias = a.sel_bias;
+    p.x = a.x; p.w_r = a.w_r; p.w_rT = s.w_rT; p.logit_bias = a.logit_bias; p.sel_bias = a.sel_bias;
     p.forced = a.forced; p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.mode = a.gating;
     p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
     p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = s.hist;

@@ -14,6 +14,7 @@ struct GateParams {
   int S, C;
   const uint16_t* x;
   const float* w_r;
+  const float* w_rT;         // [E][H] transposed router (tensor-core router path) or NULL
   const float* logit_bias;
   const float* sel_bias;
   const int32_t* forced;
@@ -32,7 +33,12 @@ struct RoutePlan {
   int S;            // H slices of the router product
   int h_per_split;
   int ntiles;       // 128-token dispatch tiles
+  int tc;           // 1: router product on the tensor cores (bf16 x 3 pieces), S = 1
+  int Mpad;         // rows of the tensor-core router image (C rounded up to 128)
 };
+
+// batches of at least this many tokens compute the router product on the tensor cores
+constexpr int kTcRouterMinT = 256;
 
 struct RouteScratch {
   float* part;      // [S][T][C]
@@ -41,6 +47,8 @@ struct RouteScratch {
   int32_t* active;  // [E] experts with rows, ascending
   int32_t* n_active;
   int32_t* shared_meta;  // {0, T, 0, 1}: offsets / active list / count of the shared expert
+  uint16_t* img;         // tensor-core router: [Mpad x 3H] tiled bf16 pieces
+  float* w_rT;           // tensor-core router: [E][H] fp32
 };
 
 struct RouteArgs {
@@ -55,6 +63,7 @@ struct RouteArgs {
   int32_t *ids, *counts, *offsets, *pos, *src, *tie_flags;
   float *w, *logits, *shared_gate;
   uint16_t* x_perm;  // nullable: fused gather into expert order
+  int32_t* err;      // device error word (bounded waits of the tensor-core router)
 };
 
 RoutePlan plan_route(int T, int H, int E, int k, bool has_gate);

@@ -188,7 +188,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
   return x;
 }
 
-template <int BN, bool FUSED, bool INT4>
+template <int BN, bool FUSED, bool INT4, bool ROUTER = false>
 __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ TcParams p) {
   using C = Cfg<BN, FUSED, INT4>;
@@ -284,7 +284,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
               bulk_g2s(smem_u32(st + C::A_BYTES),
                        wb + ((size_t)(x.mt + MT) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
           }
-          tma_2d(smem_u32(st + C::NA * C::A_BYTES), &p.tmap_b, kt * 64, x.r0 + x.nt * BN, fb);
+          tma_2d(smem_u32(st + C::NA * C::A_BYTES), &p.tmap_b,
+                 (ROUTER ? kt % p.kb_mod : kt) * 64, x.r0 + x.nt * BN, fb);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
       }
@@ -350,7 +351,9 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
           if (n < n_here) {
             const size_t row = (size_t)(x.r0 + x.nt * BN + n);
             const float gv = __uint_as_float(g[j]);
-            if (p.S == 1) {
+            if (ROUTER) {
+              if (m < p.m_limit) p.out_f32[row * p.ldo + m] = gv;
+            } else if (p.S == 1) {
               const float o = FUSED ? silu_mul(gv, __uint_as_float(v[j])) : gv;
               p.out[row * p.M + m] = float_to_bf16_bits(o);
             } else {
@@ -488,16 +491,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BN, bool FUSED, bool INT4>
+template <int BN, bool FUSED, bool INT4, bool ROUTER = false>
 int launch_bn(TcParams& kp, cudaStream_t st) {
   using C = Cfg<BN, FUSED, INT4>;
   static bool attr = false;
   if (!attr) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<BN, FUSED, INT4>,
+    MOE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<BN, FUSED, INT4, ROUTER>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr = true;
   }
-  tc_gemm_kernel<BN, FUSED, INT4><<<sm_count(), C::THREADS, C::SMEM, st>>>(kp);
+  tc_gemm_kernel<BN, FUSED, INT4, ROUTER><<<sm_count(), C::THREADS, C::SMEM, st>>>(kp);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;
@@ -601,6 +604,40 @@ int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters
   kp.err = err;
   MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, t.counter_elems * sizeof(int32_t), st));
   return a.int4 ? dispatch_bn<true>(a.fused, t.BN, kp, st) : dispatch_bn<false>(a.fused, t.BN, kp, st);
+}
+
+int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,
+                     const int32_t* meta, float* logits, int32_t* err, cudaStream_t st) {
+  if (T <= 0) return MOE_OK;
+  auto enc = encode_fn();
+  if (!enc) return MOE_ERR_UNSUPPORTED;
+  constexpr int BN = 128;
+  TcParams kp{};
+  cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)BN};
+  cuuint32_t estr[2] = {1, 1};
+  if (enc(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(x), dims,
+          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return MOE_ERR_INVALID_ARG;
+  kp.offsets = meta;
+  kp.active = meta + 2;
+  kp.n_active = meta + 3;
+  kp.host_n = -1;
+  kp.tab.p[0] = img;
+  kp.w_off = 0;
+  kp.K = 3 * H;
+  kp.M = Mpad;
+  kp.S = 1;
+  kp.kt_per_split = 3 * H / 64;
+  kp.max_rows = T;
+  kp.err = err;
+  kp.kb_mod = H / 64;
+  kp.out_f32 = logits;
+  kp.ldo = C;
+  kp.m_limit = C;
+  return launch_bn<BN, false, false, true>(kp, st);
 }
 
 }  // namespace moe

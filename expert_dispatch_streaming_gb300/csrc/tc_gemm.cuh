@@ -20,6 +20,11 @@ struct TcParams {
   float* part;
   int32_t* counters;
   int32_t* err;
+  // router mode: A is a [M x K] image whose K range repeats the token columns kb_mod k-tiles
+  // apart (K = pieces x H); the fp32 result goes to out_f32[row * ldo + m] for m < m_limit
+  int kb_mod;
+  float* out_f32;
+  int ldo, m_limit;
 };
 
 using TcPlan = TcPlanLite;
@@ -28,5 +33,11 @@ bool tc_supported(const GemmArgs& a);
 TcPlan plan_tc(const GemmArgs& a);
 int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters, int32_t* err,
               cudaStream_t st);
+
+// Router logits on the tensor cores: logits[t][c] (c < C, fp32, row stride C) =
+// sum_k img[c][k] * x[t][k mod H] with img the [Mpad x 3H] tiled bf16 image of the three
+// router pieces (see router_prep in route.cu); one group of T rows (offsets {0, T}).
+int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,
+                     const int32_t* meta, float* logits, int32_t* err, cudaStream_t st);
 
 }  // namespace moe

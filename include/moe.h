@@ -182,7 +182,9 @@ int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
  * Arguments, outputs and results are those of moe_route_topk; the scratch is a fixed 8 MiB
  * array in the library's device memory (one per GPU that loads the library, held until the
  * process exits).  Returns MOE_ERR_CAPACITY when moe_route_workspace_size(T, H, E, k) exceeds
- * 8 MiB (for example T = 8192 with E = 256 needs more; T <= 2048 with E <= 256 fits).  Calls no
+ * 8 MiB: batches of fewer than 256 tokens fit for E <= 256 and H <= 8192, while larger batches
+ * route on the tensor cores, whose split router image needs 6*H*E' bytes (E' = E + 1 rounded up
+ * to 128) plus 4*H*E (for example 23 MiB at H = 7168, E = 256).  Calls no
  * allocating routine.  The first call on a device looks up the array's device address once
  * (cudaGetSymbolAddress with that device current); make that first call before any stream
  * capture.  Every call on a device shares the one array and it keeps the previous call's

@@ -94,6 +94,20 @@ def test_route_topk_dispatch(moe, cfg, T):
         assert np.abs(g["sg"] - ref).max() < 1e-5
 
 
+@pytest.mark.parametrize("cfg,T", [(wl.DEEPSEEK, 2048), (wl.QWEN, 4096), (wl.MIXTRAL, 1024)],
+                         ids=["deepseek-2048", "qwen-4096", "mixtral-1024"])
+def test_route_tensor_core_router_full_shapes(moe, cfg, T):
+    """Batches of >= 256 tokens compute the router product on the tensor cores (bf16 x 3
+    pieces); selection must still equal exact arithmetic away from near-ties."""
+    xb, g = _route(moe, cfg, T)
+    l, s = oracle_scores(cfg, xb)
+    assert np.abs(g["logits"] - l).max() < 1e-3
+    n_near = check_ids(cfg, g["ids"], g["tie"], xb)
+    counts, offsets, pos, src = moe_ref.dispatch(g["ids"], cfg.E)
+    assert np.array_equal(g["pos"], pos) and np.array_equal(g["src"], src)
+    assert n_near <= max(2, T // 500)
+
+
 def test_route_forced_ids(moe):
     cfg = SMALL[2]
     T = 37
