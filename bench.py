@@ -453,6 +453,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--T", type=int, default=None)
     ap.add_argument("--workload", default="mixtral", choices=["mixtral", "qwen", "deepseek"])
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override the routed expert count (smaller profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
@@ -464,6 +466,8 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.T is None:
         args.T = max(WORKLOADS[args.workload].Ts)
+    if args.experts:
+        WORKLOADS[args.workload] = WORKLOADS[args.workload].with_(E=args.experts)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
