@@ -34,8 +34,10 @@ void pack_tiled_bf16(const uint16_t* src, size_t K, size_t N, uint16_t* dst) {
 
 // Tiled INT4 image of W[n][k] = codes[k][n] with group scales[k/128][n]: tiles of 128 rows x
 // 128 k (one scale group), tile (mt, kt) at ((mt * K/128) + kt) * 8448 bytes.  Inside a tile:
-// 16-byte chunk (c, r) at (c * 128 + r) * 16 holds codes k = kt*128 + 32c .. +31 of row r, two
-// per byte, even k in the low nibble; then the 128 rows' bf16 scales at 8192 + 2r.
+// 16-byte chunk (c, r) at (c * 128 + r) * 16 holds codes k = kt*128 + 32c .. +31 of row r as four
+// little-endian 32-bit words of eight codes each; word w carries k = 8w + [0, 2, 4, 6, 1, 3, 5, 7]
+// in its nibbles 0..7, so nibbles j and j + 4 hold the consecutive pair (8w + 2j, 8w + 2j + 1).
+// Then the 128 rows' bf16 scales at 8192 + 2r.
 bool pack_tiled_int4(const int8_t* codes, const uint16_t* scales, size_t K, size_t N,
                      uint8_t* dst) {
   bool ok = true;
@@ -43,14 +45,16 @@ bool pack_tiled_int4(const int8_t* codes, const uint16_t* scales, size_t K, size
   for (size_t mt = 0; mt < N / 128; ++mt)
     for (size_t kt = 0; kt < kt_n; ++kt) {
       uint8_t* tile = dst + (mt * kt_n + kt) * 8448;
-      for (size_t kk = 0; kk < 128; kk += 2) {
-        const int8_t* lo = codes + (kt * 128 + kk) * N + mt * 128;
-        const int8_t* hi = lo + N;
-        const size_t c = kk >> 5, byte = (kk & 31) >> 1;
+      for (size_t kk = 0; kk < 128; ++kk) {
+        const int8_t* src = codes + (kt * 128 + kk) * N + mt * 128;
+        const size_t c = kk >> 5, kp = kk & 31, w = kp >> 3, j = kp & 7;
+        const size_t nib = (j & 1) ? 4 + (j >> 1) : (j >> 1);
+        const size_t byte = 4 * w + (nib >> 1), shift = (nib & 1) * 4;
         for (size_t r = 0; r < 128; ++r) {
-          ok &= lo[r] >= -7 && lo[r] <= 7 && hi[r] >= -7 && hi[r] <= 7;
-          tile[(c * 128 + r) * 16 + byte] = static_cast<uint8_t>(
-              (static_cast<uint8_t>(lo[r]) & 0xFu) | ((static_cast<uint8_t>(hi[r]) & 0xFu) << 4));
+          ok &= src[r] >= -7 && src[r] <= 7;
+          uint8_t& b = tile[(c * 128 + r) * 16 + byte];
+          b = static_cast<uint8_t>((b & ~(0xFu << shift)) |
+                                   ((static_cast<uint8_t>(src[r]) & 0xFu) << shift));
         }
       }
       uint16_t* sc = reinterpret_cast<uint16_t*>(tile + 8192);

@@ -63,7 +63,8 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
   return v;
 }
 
-// Two INT4 codes at bits 0-3 and 16-19 -> two bf16 integers (exact).  Offset-binary trick:
+// Two INT4 codes at bits 0-3 and 16-19 (a pair as stored in the tiled bundle: nibbles j and
+// j + 4 of a code word) -> two bf16 integers (exact).  Offset-binary trick:
 // code c has nibble u with u ^ 8 = c + 8, and the bf16 with bits 0x4300 | (c + 8) is 128 + c + 8.
 __device__ __forceinline__ uint32_t i4pair_to_bf16x2(uint32_t v) {
   uint32_t w = (v ^ 0x00080008u) | 0x43004300u;
@@ -157,10 +158,11 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
 #pragma unroll
           for (int r = 0; r < NR; ++r) {
             if (INT4) {
-              const uint32_t q = word_of(A[uu][r][0], s >> 1);
-              const uint32_t v = (s & 1) ? (q >> 16) : q;
-              af[s][r][0] = i4pair_to_bf16x2((v & 0xFu) | ((v << 12) & 0xF0000u));
-              af[s][r][1] = i4pair_to_bf16x2(((v >> 8) & 0xFu) | ((v << 4) & 0xF0000u));
+              // step s uses codes 4s..4s+3 of the thread's 32: word s/2, pairs (s&1)*2, +1,
+              // each pair in nibbles j and j + 4 of the word
+              const uint32_t q = word_of(A[uu][r][0], s >> 1) >> ((s & 1) * 8);
+              af[s][r][0] = i4pair_to_bf16x2(q & 0x000F000Fu);
+              af[s][r][1] = i4pair_to_bf16x2((q >> 4) & 0x000F000Fu);
             } else {
               af[s][r][0] = word_of(A[uu][r][s >> 1], (2 * s) & 3);
               af[s][r][1] = word_of(A[uu][r][s >> 1], (2 * s + 1) & 3);

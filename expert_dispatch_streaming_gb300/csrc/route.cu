@@ -542,6 +542,7 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ s
   const int nvec = H / 8;
   const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)(src[warp] / k) * H);
   uint4* d = reinterpret_cast<uint4*>(x_perm + (size_t)warp * H);
+#pragma unroll 4
   for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
 }
 
@@ -622,10 +623,17 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   if (a.T > 0) {
+    // small batches copy the rows inside the per-tile ranking kernel; large ones gather with
+    // one warp per destination row over the whole GPU (the per-tile grid is too small)
+    const bool fused_copy = a.x_perm && a.T < kSeparateGatherMinT;
     rank_permute_kernel<<<r.ntiles, 256, 0, st>>>(a.ids, s.base, a.T, a.k, a.E, a.H, a.x,
-                                                  a.pos, a.src, a.x_perm);
+                                                  a.pos, a.src, fused_copy ? a.x_perm : nullptr);
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
+    if (a.x_perm && !fused_copy) {
+      const int rr = launch_gather(a.x, a.src, a.T * a.k, a.k, a.H, a.x_perm, st);
+      if (rr != MOE_OK) return rr;
+    }
   }
   return MOE_OK;
 }

@@ -39,6 +39,8 @@ struct RoutePlan {
 
 // batches of at least this many tokens compute the router product on the tensor cores
 constexpr int kTcRouterMinT = 256;
+// batches of at least this many tokens gather x_perm in a separate, GPU-wide kernel
+constexpr int kSeparateGatherMinT = 1024;
 
 struct RouteScratch {
   float* part;      // [S][T][C]

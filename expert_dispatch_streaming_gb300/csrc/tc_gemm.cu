@@ -138,6 +138,17 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 template <int BN, bool FUSED, bool INT4>
@@ -155,7 +166,8 @@ struct Cfg {
   static constexpr int BUFS = (2 * ACC <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = ACC * BUFS <= 32 ? 32 : ACC * BUFS <= 64 ? 64
                                  : ACC * BUFS <= 128 ? 128 : ACC * BUFS <= 256 ? 256 : 512;
-  static constexpr int THREADS = INT4 ? 320 : 192;            // + 4 dequant warps for INT4
+  static constexpr int DQ_WARPS = 8;                          // INT4 dequant warps
+  static constexpr int THREADS = INT4 ? 192 + 32 * DQ_WARPS : 192;
   static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 4096 /*barriers, prefix*/;
 };
 
@@ -213,7 +225,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
-      mbar_init(smem_u32(&afull[s]), 4);
+      mbar_init(smem_u32(&afull[s]), C::DQ_WARPS);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -339,14 +351,21 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
       const int m = x.mt * 128 + q * 32 + lane;
       const int n_here = min(BN, x.ne - x.nt * BN);
       const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::ACC;
+      // columns per TMEM load: 32, or 16 in the INT4 kernels (more warps, fewer registers)
+      constexpr int CH = INT4 ? 16 : 32;
 #pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += 32) {
+      for (int c0 = 0; c0 < BN; c0 += CH) {
         if (c0 >= n_here) break;   // warp-uniform
-        uint32_t g[32], v[32];
-        tmem_ld32(ta + c0, g);
-        if (FUSED) tmem_ld32(ta + BN + c0, v);
+        uint32_t g[CH], v[CH];
+        if (CH == 32) {
+          tmem_ld32(ta + c0, *reinterpret_cast<uint32_t(*)[32]>(g));
+          if (FUSED) tmem_ld32(ta + BN + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+        } else {
+          tmem_ld16(ta + c0, g);
+          if (FUSED) tmem_ld16(ta + BN + c0, v);
+        }
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < CH; ++j) {
           const int n = c0 + j;
           if (n < n_here) {
             const size_t row = (size_t)(x.r0 + x.nt * BN + n);
@@ -416,10 +435,10 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     }
     (void)et;
   } else if (INT4) {
-    // ------------------------------------------------------------ INT4 dequant (warps 6..9)
-    // thread = weight row r of the tile: 64 codes (two 16-byte chunks) -> bf16(code * scale),
-    // written as the row's eight 16-byte chunks of the 128-byte-swizzled K-major A image
-    const int r = threadIdx.x - 192;
+    // ------------------------------------------------------------ INT4 dequant (warps 6..13)
+    // work item = (weight tile w, 32-code chunk cc, row r): one 16-byte load of codes + the
+    // row's scale -> four 16-byte chunks of bf16(code * scale) in the 128-byte-swizzled A image
+    const int td = threadIdx.x - 192;
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
@@ -431,34 +450,30 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
         uint8_t* st = smem + stage * C::STAGE;
 #pragma unroll
-        for (int w = 0; w < C::NA; ++w) {
+        for (int it = 0; it < C::NA; ++it) {
+          const int item = td + it * 32 * C::DQ_WARPS;
+          const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
           const uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
           uint8_t* arow = st + w * C::A_BYTES + r * 128;
           const uint32_t sb = *reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r);
           const uint32_t s2 = sb | (sb << 16);
+          const uint4 q = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
+          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            const uint4 q = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
-            const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+          for (int j = 0; j < 4; ++j) {
+            // word j holds codes 8j..8j+7; pair jp (codes 8j+2jp, +1) in nibbles jp and jp + 4
+            uint32_t pr[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint32_t v = qw[j];
-              uint32_t pr[4] = {(v & 0xFu) | ((v << 12) & 0xF0000u),
-                                ((v >> 8) & 0xFu) | ((v << 4) & 0xF0000u),
-                                ((v >> 16) & 0xFu) | ((v >> 4) & 0xF0000u),
-                                ((v >> 24) & 0xFu) | ((v >> 12) & 0xF0000u)};
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                uint32_t b = (pr[i] ^ 0x00080008u) | 0x43004300u;  // 128 + code + 8
-                __nv_bfloat162 h = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&b),
-                                           *reinterpret_cast<const __nv_bfloat162*>(&k136));
-                h = __hmul2(h, *reinterpret_cast<const __nv_bfloat162*>(&s2));
-                pr[i] = *reinterpret_cast<uint32_t*>(&h);
-              }
-              const int oc = cc * 4 + j;
-              *reinterpret_cast<uint4*>(arow + ((oc ^ (r & 7)) << 4)) =
-                  make_uint4(pr[0], pr[1], pr[2], pr[3]);
+            for (int jp = 0; jp < 4; ++jp) {
+              uint32_t b = ((qw[j] >> (4 * jp)) & 0x000F000Fu) ^ 0x43084308u;  // 128 + code + 8
+              __nv_bfloat162 h = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&b),
+                                         *reinterpret_cast<const __nv_bfloat162*>(&k136));
+              h = __hmul2(h, *reinterpret_cast<const __nv_bfloat162*>(&s2));
+              pr[jp] = *reinterpret_cast<uint32_t*>(&h);
             }
+            const int oc = cc * 4 + j;
+            *reinterpret_cast<uint4*>(arow + ((oc ^ (r & 7)) << 4)) =
+                make_uint4(pr[0], pr[1], pr[2], pr[3]);
           }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");

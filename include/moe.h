@@ -109,8 +109,10 @@ enum moe_wdtype {
  *         128-byte-swizzled K-major image the tensor cores read from shared memory, so a
  *         tile moves with one bulk copy.
  *   int4: tiles of 128 rows x 128 k (one scale group, 8448 B): 16-byte chunk (c, r) at
- *         (c*128 + r)*16 holds the 32 codes k = 32c..32c+31 of row r (two per byte, even k in
- *         the low nibble), followed by the rows' bf16 group scales at 8192 + 2r.
+ *         (c*128 + r)*16 holds the 32 codes k = 32c..32c+31 of row r as four little-endian
+ *         32-bit words; word w holds k = 8w + {0,2,4,6,1,3,5,7} in nibbles 0..7 (so nibbles j and
+ *         j+4 are the pair 8w+2j, 8w+2j+1, one shift and one mask apart), followed by the rows'
+ *         bf16 group scales at 8192 + 2r.
  *   gate_up_scale_offset / down_scale_offset give the scale block of the section's first tile.
  * Constraints: H and I multiples of 128.  */
 typedef struct moe_bundle_layout {

@@ -62,16 +62,18 @@ def _untile_bf16(buf, rows, K):
 
 def _untile_int4(buf, rows, K):
     """Inverse of the tiled INT4 image: 8448-byte tiles of 128 rows x 128 k; chunk (c, r) at
-    (c*128 + r)*16 holds k = 32c..32c+31 (even k in the low nibble); scales at 8192 + 2r."""
+    (c*128 + r)*16 holds k = 32c..32c+31 as four 32-bit words whose nibbles 0..7 carry
+    k = 8w + 0, 2, 4, 6, 1, 3, 5, 7; scales at 8192 + 2r."""
     nt = (rows // 128) * (K // 128)
     t = buf[:nt * 8448].reshape(rows // 128, K // 128, 8448)
-    codes = t[:, :, :8192].reshape(rows // 128, K // 128, 4, 128, 16)
+    codes = t[:, :, :8192].reshape(rows // 128, K // 128, 4, 128, 4, 4)   # [.., c, r, word, byte]
     lo = (codes & 0xF).astype(np.int8)
     hi = (codes >> 4).astype(np.int8)
-    lo = np.where(lo >= 8, lo - 16, lo)
-    hi = np.where(hi >= 8, hi - 16, hi)
-    q = np.empty(codes.shape[:-1] + (32,), np.int8)
-    q[..., 0::2], q[..., 1::2] = lo, hi                     # [mt, kt, c, r, 32]
+    nib = np.empty(codes.shape[:-1] + (8,), np.int8)                      # nibble i of the word
+    nib[..., 0::2], nib[..., 1::2] = lo, hi
+    nib = np.where(nib >= 8, nib - 16, nib)
+    order = [0, 4, 1, 5, 2, 6, 3, 7]          # code k = 8w + j lives in nibble order[j]
+    q = nib[..., order].reshape(codes.shape[:4] + (32,))                  # [mt, kt, c, r, 32]
     q = q.transpose(0, 3, 1, 2, 4).reshape(rows, K)
     sc = t[:, :, 8192:8448].copy().view(np.uint16).reshape(rows // 128, K // 128, 128)
     sc = sc.transpose(0, 2, 1).reshape(rows, K // 128)
