@@ -395,9 +395,13 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   } else {
     // A5: the layer's expert-use mask crosses to the host, the LRU decides, misses are copied
     // on the cache's copy stream while the shared expert and the hit experts compute.
+    // The shared expert needs no routed bundle: it is enqueued before the host waits for the
+    // read-back, so the GPU computes it during the round trip.
     MOE_CUDA_TRY(cudaMemcpyAsync(cache->host_counts, s.counts, sizeof(int32_t) * L->E,
                                  cudaMemcpyDeviceToHost, s0));
     MOE_CUDA_TRY(cudaEventRecord(cache->d2h, s0));
+    if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
+    if ((r = phase(2)) != MOE_OK) return r;
     if ((r = cache_wait_event(cache, cache->d2h)) != MOE_OK) return r;
     uint8_t used[kMaxExperts];
     for (int e = 0; e < L->E; ++e) used[e] = cache->host_counts[e] > 0;
@@ -407,8 +411,6 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
     if (r != MOE_OK) return r;
     BundleTable tab{};
     for (int e = 0; e < L->E; ++e) tab.p[e] = ptrs[e];
-    if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
-    if ((r = phase(2)) != MOE_OK) return r;
     if (!hits.empty() && (r = run_experts(L, P, s, tab, T, (int)hits.size(), hits.data(), s0,
                                           std::function<int()>())) != MOE_OK)
       return r;
