@@ -130,6 +130,21 @@ def roofline_of(flops, nbytes, seconds, pk, sustained=False):
             "frac": round(ach / pk["hbm_gbs"], 4)}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of every rank's value (timing: the job ends when its slowest replica ends)."""
+    if world <= 1:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: int, world: int, seconds: float) -> float:
+    """Whole-job throughput of N independent replicas: all ranks' units over the max time."""
+    return units_per_rank * world / seconds
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import expert_dispatch_streaming_gb300 as moe
@@ -175,15 +190,12 @@ def run_ours(args, rank, world, local_rank):
             t1.record(stream)
             stream.synchronize()
         torch.cuda.synchronize()
-        ms = t0.elapsed_time(t1)
+        ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
         if world > 1:
-            tt = torch.tensor([ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            ms = float(tt.item())
             torch.distributed.barrier()
         ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)]
                        for i in range(steps)])
-        res = dict(T=T, ms_per_step=ms / steps, tokens_per_s=T * steps * world / (ms / 1e3),
+        res = dict(T=T, ms_per_step=ms / steps, tokens_per_s=job_throughput(T * steps, world, ms / 1e3),
                    n_unique=n_unique, phase_ms=ph.mean(0).tolist(), launches=launches,
                    clocks=clk.summary(), mode="eager")
         if args.graph:
@@ -209,16 +221,12 @@ def run_ours(args, rank, world, local_rank):
                         g.replay()
                 t1.record(stream)
                 stream.synchronize()
-            gms = t0.elapsed_time(t1)
+            gms = max_over_ranks(t0.elapsed_time(t1), world, dev)
             # phase split of one replay (events inside the graph are re-recorded per replay)
             with torch.cuda.stream(stream):
                 g.replay()
             stream.synchronize()
             gph = [gevs[j].elapsed_time(gevs[j + 1]) for j in range(5)]
-            if world > 1:
-                tt = torch.tensor([gms], device=dev)
-                torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-                gms = float(tt.item())
             res["graph"] = dict(ms_per_step=gms / steps,
                                 tokens_per_s=T * steps * world / (gms / 1e3), phase_ms=gph,
                                 clocks=gclk.summary())
@@ -248,11 +256,7 @@ def run_ours(args, rank, world, local_rank):
                     oh.copy_(out, non_blocking=True)
             e1.record(stream)
             stream.synchronize()
-            ems = e0.elapsed_time(e1)
-            if world > 1:
-                tt = torch.tensor([ems], device=dev)
-                torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-                ems = float(tt.item())
+            ems = max_over_ranks(e0.elapsed_time(e1), world, dev)
             res["e2e"] = {"value": round(T * steps * world / (ems / 1e3), 1), "unit": "tokens/s",
                           "h2d_bytes_per_step": int(xh.numel() * 2),
                           "d2h_bytes_per_step": int(oh.numel() * 2)}
