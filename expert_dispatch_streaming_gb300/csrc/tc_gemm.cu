@@ -547,10 +547,10 @@ int tc_bn_for(const GemmArgs& a) {
   const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
                                           : std::min(a.E, a.max_rows));
   const int avg = ceil_div(std::max(a.max_rows, 1), A);
-  // fused tiles hold gate and up accumulators: a 256-token tile fills TMEM (no double buffer)
-  // and, with INT4, leaves room for only two stages -- cap at 128 for INT4 and for short K
-  // (K <= 2048), where the un-overlapped epilogue weighs most
-  const int cap = (a.fused && (a.int4 || a.K <= 2048)) ? 128 : 256;
+  // fused tiles hold gate and up accumulators: a 256-token tile would fill all of TMEM (no
+  // double buffer, epilogue not overlapped with the next tile's MMA) and, with INT4, leave room
+  // for two stages only; 128-token fused tiles measured faster at every shape tried
+  const int cap = a.fused ? 128 : 256;
   const int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
   return std::min(bn, cap);
 }
