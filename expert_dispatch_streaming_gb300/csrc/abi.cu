@@ -10,6 +10,7 @@
 #include "common.cuh"
 #include "expert_ffn.cuh"
 #include "route.cuh"
+#include "tc_gemm.cuh"
 
 namespace moe {
 
@@ -49,6 +50,7 @@ struct LayerScratch {
   float *w, *shared_gate;
   uint16_t *x_perm, *h, *y_perm, *h_s, *s;
   float* part;
+  float* part_s;    // split-K partials of the shared expert when it shares a launch
   int32_t* counters;
   int32_t* err;     // device error word (first bytes of the workspace)
 };
@@ -57,6 +59,8 @@ struct LayerPlan {
   RoutePlan rp;
   GemmPlan gu, dn, sgu, sdn;
   moe_bundle_layout lay, slay;
+  int merged;        // routed and shared expert share one tcgen05 launch per GEMM
+  TcPair mgu, mdn;
 };
 
 static GemmArgs gemm_args(const moe_bundle_layout& lay, int wdtype, bool fused, int K, int M,
@@ -86,8 +90,15 @@ static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
   P->gu = plan_gemm(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows));
   P->dn = plan_gemm(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows));
   if (L->Is) {
-    P->sgu = plan_gemm(gemm_args(P->slay, L->wdtype, true, L->H, L->Is, 1, T));
-    P->sdn = plan_gemm(gemm_args(P->slay, L->wdtype, false, L->Is, L->H, 1, T));
+    GemmArgs sgu = gemm_args(P->slay, L->wdtype, true, L->H, L->Is, 1, T);
+    GemmArgs sdn = gemm_args(P->slay, L->wdtype, false, L->Is, L->H, 1, T);
+    P->sgu = plan_gemm(sgu);
+    P->sdn = plan_gemm(sdn);
+    P->merged = P->gu.use_tc && P->dn.use_tc && P->sgu.use_tc && P->sdn.use_tc;
+    if (P->merged) {
+      P->mgu = plan_tc_pair(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows), sgu);
+      P->mdn = plan_tc_pair(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows), sdn);
+    }
   }
   return MOE_OK;
 }
@@ -113,10 +124,12 @@ static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, 
     z.s = c.take<uint16_t>((size_t)T * L->H + 8);
   }
   size_t pe = std::max({P.gu.part_elems, P.dn.part_elems, P.sgu.part_elems, P.sdn.part_elems,
-                        (size_t)1});
+                        P.mgu.t1.part_elems, P.mdn.t1.part_elems, (size_t)1});
   size_t ce = std::max({P.gu.counter_elems, P.dn.counter_elems, P.sgu.counter_elems,
-                        P.sdn.counter_elems, (size_t)1});
+                        P.sdn.counter_elems, P.mgu.t1.counter_elems, P.mdn.t1.counter_elems,
+                        (size_t)1});
   z.part = c.take<float>(pe);
+  z.part_s = c.take<float>(std::max({P.mgu.t2.part_elems, P.mdn.t2.part_elems, (size_t)1}));
   z.counters = c.take<int32_t>(ce);
   if (s) *s = z;
   return c.used;
@@ -140,6 +153,33 @@ static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratc
   dn.host_n = host_n; dn.host_ids = host_ids;
   GemmPlan pd = plan_gemm(dn);
   return launch_gemm(dn, pd, s.part, s.counters, s.err, st);
+}
+
+// Routed experts and the shared expert in one tcgen05 launch per GEMM (the shared expert is the
+// extra group: its rows are the T token rows of x, its output h_s / s).
+static int run_ffn_merged(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
+                          const BundleTable& tab, const uint16_t* x, int T, cudaStream_t st,
+                          std::function<int()> between) {
+  const int rows = T * L->k;
+  BundleTable stab{};
+  stab.p[0] = L->shared_bundle;
+  const int32_t* meta = s.rs.shared_meta;
+  GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows);
+  gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = s.rs.active;
+  gu.n_active = s.rs.n_active; gu.tab = &tab; gu.out = s.h;
+  GemmArgs sgu = gemm_args(P.slay, L->wdtype, true, L->H, L->Is, 1, T);
+  sgu.xin = x; sgu.offsets = meta; sgu.active = meta + 2; sgu.n_active = meta + 3;
+  sgu.tab = &stab; sgu.out = s.h_s;
+  int r = launch_tc_pair(gu, sgu, P.mgu, s.part, s.part_s, s.counters, s.err, st);
+  if (r != MOE_OK) return r;
+  if (between && (r = between()) != MOE_OK) return r;
+  GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
+  dn.xin = s.h; dn.offsets = s.offsets; dn.active = s.rs.active;
+  dn.n_active = s.rs.n_active; dn.tab = &tab; dn.out = s.y_perm;
+  GemmArgs sdn = gemm_args(P.slay, L->wdtype, false, L->Is, L->H, 1, T);
+  sdn.xin = s.h_s; sdn.offsets = meta; sdn.active = meta + 2; sdn.n_active = meta + 3;
+  sdn.tab = &stab; sdn.out = s.s;
+  return launch_tc_pair(dn, sdn, P.mdn, s.part, s.part_s, s.counters, s.err, st);
 }
 
 static int run_shared(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
@@ -385,12 +425,19 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   if (!cache) {
     BundleTable tab{};
     for (int e = 0; e < L->E; ++e) tab.p[e] = L->bundles[e];
-    if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
-    if ((r = phase(2)) != MOE_OK) return r;
-    if ((r = run_experts(L, P, s, tab, T, -1, nullptr, s0, pev ? [&] { return phase(3); }
-                                                                 : std::function<int()>()))
-        != MOE_OK)
-      return r;
+    if (P.merged) {
+      // phase 2 (shared expert) is empty: the shared expert runs inside the routed launches
+      if ((r = phase(2)) != MOE_OK) return r;
+      if ((r = run_ffn_merged(L, P, s, tab, x, T, s0,
+                              pev ? [&] { return phase(3); } : std::function<int()>())) != MOE_OK)
+        return r;
+    } else {
+      if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
+      if ((r = phase(2)) != MOE_OK) return r;
+      if ((r = run_experts(L, P, s, tab, T, -1, nullptr, s0,
+                           pev ? [&] { return phase(3); } : std::function<int()>())) != MOE_OK)
+        return r;
+    }
     if ((r = phase(4)) != MOE_OK) return r;
   } else {
     // A5: the layer's expert-use mask crosses to the host, the LRU decides, misses are copied

@@ -168,8 +168,27 @@ __device__ double exact_score(const GateParams& p, int t, int b, int lane) {
     }
     for (; h < p.H; h += 32) d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wr[h], d0);
   } else {
-    for (int h = lane; h < p.H; h += 32)
-      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)p.w_r[(size_t)h * p.E + b], d0);
+    // strided column reads (one row of W_r per lane): eight independent sums keep eight loads
+    // in flight; fixed combination order
+    const float* wc = p.w_r + b;
+    const size_t E = p.E;
+    double d4 = 0.0, d5 = 0.0, d6 = 0.0, d7 = 0.0;
+    int h = lane;
+    for (; h + 224 < p.H; h += 256) {
+      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wc[(size_t)h * E], d0);
+      d1 = fma((double)bf16_bits_to_float(xr[h + 32]), (double)wc[(size_t)(h + 32) * E], d1);
+      d2 = fma((double)bf16_bits_to_float(xr[h + 64]), (double)wc[(size_t)(h + 64) * E], d2);
+      d3 = fma((double)bf16_bits_to_float(xr[h + 96]), (double)wc[(size_t)(h + 96) * E], d3);
+      d4 = fma((double)bf16_bits_to_float(xr[h + 128]), (double)wc[(size_t)(h + 128) * E], d4);
+      d5 = fma((double)bf16_bits_to_float(xr[h + 160]), (double)wc[(size_t)(h + 160) * E], d5);
+      d6 = fma((double)bf16_bits_to_float(xr[h + 192]), (double)wc[(size_t)(h + 192) * E], d6);
+      d7 = fma((double)bf16_bits_to_float(xr[h + 224]), (double)wc[(size_t)(h + 224) * E], d7);
+    }
+    for (; h < p.H; h += 32) d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wc[(size_t)h * E], d0);
+    d0 += d4;
+    d1 += d5;
+    d2 += d6;
+    d3 += d7;
   }
   double d = (d0 + d1) + (d2 + d3);
 #pragma unroll

@@ -172,31 +172,65 @@ struct Cfg {
 };
 
 struct Unit {
-  int a, e, r0, ne, mt, ks, nt, tile;
+  const char* w;            // weight section of this unit's expert
+  const CUtensorMap* tm;    // its token rows
+  uint16_t* out;
+  float* part;
+  int M, KT, MT, S, kps, max_rows;
+  int r0, ne, mt, ks, nt, tile;
 };
 
 // Maps unit index u to its (expert, row tile, split, token tile), from the per-expert prefix
-// of unit counts kept in shared memory.
+// of unit counts kept in shared memory; units past the routed experts belong to the second
+// group (the shared expert) when there is one.
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, int n_act,
-                                            int u, int BN, int MT) {
-  int lo = 0, hi = n_act - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (pref[mid] <= u) lo = mid;
-    else hi = mid - 1;
-  }
+                                            int u, int BN) {
   Unit x;
-  x.a = lo;
-  x.e = p.host_n >= 0 ? p.host_ids[lo] : p.active[lo];
-  x.r0 = p.offsets[x.e];
-  x.ne = p.offsets[x.e + 1] - x.r0;
+  int base, tile_base;
+  if (p.g2 && u >= pref[n_act]) {
+    x.w = static_cast<const char*>(p.w2);
+    x.tm = &p.tmap_b2;
+    x.out = p.out2;
+    x.part = p.part2;
+    x.M = p.M2;
+    x.KT = p.K2 / 64;
+    x.S = p.S2;
+    x.kps = p.kt_per_split2;
+    x.max_rows = p.rows2;
+    x.r0 = 0;
+    x.ne = p.rows2;
+    base = pref[n_act];
+    tile_base = pref[n_act] / p.S;
+  } else {
+    int lo = 0, hi = n_act - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (pref[mid] <= u) lo = mid;
+      else hi = mid - 1;
+    }
+    const int e = p.host_n >= 0 ? p.host_ids[lo] : p.active[lo];
+    x.w = static_cast<const char*>(p.tab.p[e]) + p.w_off;
+    x.tm = &p.tmap_b;
+    x.out = p.out;
+    x.part = p.part;
+    x.M = p.M;
+    x.KT = p.K / 64;
+    x.S = p.S;
+    x.kps = p.kt_per_split;
+    x.max_rows = p.max_rows;
+    x.r0 = p.offsets[e];
+    x.ne = p.offsets[e + 1] - x.r0;
+    base = pref[lo];
+    tile_base = pref[lo] / p.S;
+  }
+  x.MT = x.M / 128;
   const int nt_n = (x.ne + BN - 1) / BN;
-  int rem = u - pref[lo];
+  int rem = u - base;
   x.nt = rem % nt_n;
   rem /= nt_n;
-  x.ks = rem % p.S;
-  x.mt = rem / p.S;
-  x.tile = pref[lo] / p.S + x.mt * nt_n + x.nt;
+  x.ks = rem % x.S;
+  x.mt = rem / x.S;
+  x.tile = tile_base + x.mt * nt_n + x.nt;
   return x;
 }
 
@@ -214,11 +248,10 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
   uint64_t* tfull = bars + 3 * C::STAGES;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  int* pref = reinterpret_cast<int*>(tmem_slot + 4);   // [kMaxExperts + 1]
+  int* pref = reinterpret_cast<int*>(tmem_slot + 4);   // [kMaxExperts + 2]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = p.M / 128;
-  const int KT = p.K / 64;
   const int n_act = p.host_n >= 0 ? p.host_n : *p.n_active;
 
   if (threadIdx.x == 0) {
@@ -259,13 +292,16 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
       if (a < n_act) pref[a] = carry + incl - cnt;
       carry += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (lane == 0) pref[n_act] = carry;
+    if (lane == 0) {
+      pref[n_act] = carry;
+      pref[n_act + 1] = carry + (p.g2 ? (p.M2 / 128) * p.S2 * ((p.rows2 + BN - 1) / BN) : 0);
+    }
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = pref[n_act];
+  const int total = pref[n_act + 1];
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -274,9 +310,10 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
       uint32_t phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
-        const char* wb = static_cast<const char*>(p.tab.p[x.e]) + p.w_off;
-        const int kt_lo = x.ks * p.kt_per_split, kt_hi = min(KT, kt_lo + p.kt_per_split);
+        const Unit x = decode_unit(p, pref, n_act, u, BN);
+        const char* wb = x.w;
+        const int KT = x.KT, MTx = x.MT;
+        const int kt_lo = x.ks * x.kps, kt_hi = min(KT, kt_lo + x.kps);
         for (int kt = kt_lo; kt < kt_hi; ++kt) {
           if (!(ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, 1))) break;
           const uint32_t fb = smem_u32(&full[stage]);
@@ -285,7 +322,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
           if (INT4) {
             // codes of this 64-k half of the 128-k INT4 tile, then the tile's row scales
             for (int w = 0; w < C::NA; ++w) {
-              const char* tile = wb + ((size_t)(x.mt + w * MT) * (KT / 2) + (kt >> 1)) * 8448;
+              const char* tile = wb + ((size_t)(x.mt + w * MTx) * (KT / 2) + (kt >> 1)) * 8448;
               uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
               bulk_g2s(smem_u32(raw), tile + (kt & 1) * 4096, 4096, fb);
               bulk_g2s(smem_u32(raw + 4096), tile + 8192, 256, fb);
@@ -294,9 +331,9 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
             bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
             if (FUSED)
               bulk_g2s(smem_u32(st + C::A_BYTES),
-                       wb + ((size_t)(x.mt + MT) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
+                       wb + ((size_t)(x.mt + MTx) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
           }
-          tma_2d(smem_u32(st + C::NA * C::A_BYTES), &p.tmap_b,
+          tma_2d(smem_u32(st + C::NA * C::A_BYTES), x.tm,
                  (ROUTER ? kt % p.kb_mod : kt) * 64, x.r0 + x.nt * BN, fb);
           if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
         }
@@ -310,8 +347,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
       uint32_t phase = 0, aphase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
-        const int kt_lo = x.ks * p.kt_per_split, kt_hi = min(KT, kt_lo + p.kt_per_split);
+        const Unit x = decode_unit(p, pref, n_act, u, BN);
+        const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
         if (!(ok = mbar_wait(smem_u32(&tempty[buf]), aphase ^ 1, p.err, 2))) break;
         tc_fence_after();
         const uint32_t dg = tmem_base + buf * C::ACC;
@@ -343,9 +380,9 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     int buf = 0;
     uint32_t aphase = 0;
     bool ok = true;
-    const int MP = FUSED ? 2 * p.M : p.M;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
+      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const int MP = FUSED ? 2 * x.M : x.M;
       if (!(ok = mbar_wait(smem_u32(&tfull[buf]), aphase, p.err, 4))) break;
       tc_fence_after();
       const int m = x.mt * 128 + q * 32 + lane;
@@ -372,13 +409,13 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
             const float gv = __uint_as_float(g[j]);
             if (ROUTER) {
               if (m < p.m_limit) p.out_f32[row * p.ldo + m] = gv;
-            } else if (p.S == 1) {
+            } else if (x.S == 1) {
               const float o = FUSED ? silu_mul(gv, __uint_as_float(v[j])) : gv;
-              p.out[row * p.M + m] = float_to_bf16_bits(o);
+              x.out[row * x.M + m] = float_to_bf16_bits(o);
             } else {
-              float* pr = p.part + ((size_t)x.ks * p.max_rows + row) * MP;
+              float* pr = x.part + ((size_t)x.ks * x.max_rows + row) * MP;
               pr[m] = gv;
-              if (FUSED) pr[p.M + m] = __uint_as_float(v[j]);
+              if (FUSED) pr[x.M + m] = __uint_as_float(v[j]);
             }
           }
         }
@@ -388,7 +425,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
       if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
 
-      if (p.S > 1) {
+      if (x.S > 1) {
         // per (tile, lane quarter) arrival counter: the warp completing the S arrivals of its
         // quarter sums that quarter's 32 rows over the splits in split order (no barrier,
         // nothing waits, the four quarters reduce in parallel)
@@ -398,37 +435,37 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         int32_t* ctr = p.counters + (size_t)x.tile * 4 + q;
         if (lane == 0) {
           const int prev = atomicAdd(ctr, 1);
-          last = prev == p.S - 1;
+          last = prev == x.S - 1;
           if (last) *ctr = 0;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
         if (last) {
           __threadfence();
-          const size_t stride = (size_t)p.max_rows * MP;
+          const size_t stride = (size_t)x.max_rows * MP;
           for (int n = 0; n < n_here; ++n) {
             const size_t row = (size_t)(x.r0 + x.nt * BN + n);
-            const float* pr = p.part + row * MP + m;
+            const float* pr = x.part + row * MP + m;
             // four interleaved running sums keep four split loads in flight; fixed order
             float g0 = 0.f, g1 = 0.f, g2 = 0.f, g3 = 0.f, u0 = 0.f, u1 = 0.f, u2 = 0.f, u3 = 0.f;
             int sp = 0;
-            for (; sp + 4 <= p.S; sp += 4) {
+            for (; sp + 4 <= x.S; sp += 4) {
               g0 += __ldcg(pr + sp * stride);
               g1 += __ldcg(pr + (sp + 1) * stride);
               g2 += __ldcg(pr + (sp + 2) * stride);
               g3 += __ldcg(pr + (sp + 3) * stride);
               if (FUSED) {
-                u0 += __ldcg(pr + p.M + sp * stride);
-                u1 += __ldcg(pr + p.M + (sp + 1) * stride);
-                u2 += __ldcg(pr + p.M + (sp + 2) * stride);
-                u3 += __ldcg(pr + p.M + (sp + 3) * stride);
+                u0 += __ldcg(pr + x.M + sp * stride);
+                u1 += __ldcg(pr + x.M + (sp + 1) * stride);
+                u2 += __ldcg(pr + x.M + (sp + 2) * stride);
+                u3 += __ldcg(pr + x.M + (sp + 3) * stride);
               }
             }
-            for (; sp < p.S; ++sp) {
+            for (; sp < x.S; ++sp) {
               g0 += __ldcg(pr + sp * stride);
-              if (FUSED) u0 += __ldcg(pr + p.M + sp * stride);
+              if (FUSED) u0 += __ldcg(pr + x.M + sp * stride);
             }
             const float gs = (g0 + g1) + (g2 + g3), us = (u0 + u1) + (u2 + u3);
-            p.out[row * p.M + m] = float_to_bf16_bits(FUSED ? silu_mul(gs, us) : gs);
+            x.out[row * x.M + m] = float_to_bf16_bits(FUSED ? silu_mul(gs, us) : gs);
           }
         }
       }
@@ -444,8 +481,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     bool ok = true;
     const uint32_t k136 = 0x43084308u;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit x = decode_unit(p, pref, n_act, u, BN, MT);
-      const int kt_lo = x.ks * p.kt_per_split, kt_hi = min(KT, kt_lo + p.kt_per_split);
+      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
       for (int kt = kt_lo; kt < kt_hi; ++kt) {
         if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
         uint8_t* st = smem + stage * C::STAGE;
@@ -589,20 +626,22 @@ TcPlan plan_tc(const GemmArgs& a) {
   return t;
 }
 
-int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters, int32_t* err,
-              cudaStream_t st) {
-  if (a.max_rows <= 0 || a.host_n == 0) return MOE_OK;
+static bool encode_tokens(CUtensorMap* m, const uint16_t* base, int K, int rows, int BN) {
   auto enc = encode_fn();
-  if (!enc) return MOE_ERR_UNSUPPORTED;
-  TcParams kp{};
-  cuuint64_t dims[2] = {(cuuint64_t)a.K, (cuuint64_t)a.max_rows};
-  cuuint64_t strides[1] = {(cuuint64_t)a.K * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)t.BN};
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)BN};
   cuuint32_t estr[2] = {1, 1};
-  if (enc(&kp.tmap_b, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(a.xin), dims,
-          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return MOE_ERR_INVALID_ARG;
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int fill_params(TcParams& kp, const GemmArgs& a, const TcPlan& t, float* part,
+                       int32_t* counters, int32_t* err) {
+  if (!encode_fn()) return MOE_ERR_UNSUPPORTED;
+  if (!encode_tokens(&kp.tmap_b, a.xin, a.K, a.max_rows, t.BN)) return MOE_ERR_INVALID_ARG;
   kp.offsets = a.offsets;
   kp.active = a.active;
   kp.n_active = a.n_active;
@@ -619,8 +658,80 @@ int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters
   kp.part = part;
   kp.counters = counters;
   kp.err = err;
+  return MOE_OK;
+}
+
+int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters, int32_t* err,
+              cudaStream_t st) {
+  if (a.max_rows <= 0 || a.host_n == 0) return MOE_OK;
+  TcParams kp{};
+  const int r = fill_params(kp, a, t, part, counters, err);
+  if (r != MOE_OK) return r;
   MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, t.counter_elems * sizeof(int32_t), st));
   return a.int4 ? dispatch_bn<true>(a.fused, t.BN, kp, st) : dispatch_bn<false>(a.fused, t.BN, kp, st);
+}
+
+TcPair plan_tc_pair(const GemmArgs& a1, const GemmArgs& a2) {
+  TcPair pp;
+  pp.t1 = plan_tc(a1);
+  pp.t2 = pp.t1;
+  const int BN = pp.t1.BN, sms = sm_count();
+  // tile counts of both groups at the routed group's token-tile width; one split count for
+  // both, chosen on the combined tile count like plan_tc does for one group
+  const int A = std::max(1, a1.host_n >= 0 ? std::min(a1.host_n, a1.max_rows)
+                                           : std::min(a1.E, a1.max_rows));
+  const int avg = ceil_div(std::max(a1.max_rows, 1), A);
+  const int KT1 = a1.K / 64, KT2 = a2.K / 64;
+  const int nt1 = A * (a1.M / 128) * std::max(1, ceil_div(avg, BN));
+  const int nt2 = (a2.M / 128) * ceil_div(std::max(a2.max_rows, 1), BN);
+  const int nt = nt1 + nt2;
+  const double wb = ((double)A * a1.M * a1.K + (double)a2.M * a2.K) *
+                    (a1.int4 ? 0.53 : 2.0) * (a1.fused ? 2 : 1);
+  const double pb = ((double)a1.max_rows * a1.M + (double)a2.max_rows * a2.M) *
+                    (a1.fused ? 2 : 1) * 8.0;
+  const int s_cap = std::min({KT1, KT2, std::max(1, (int)(wb / std::max(pb, 1.0) / 4))});
+  int S = 1;
+  double best = (double)ceil_div(nt, sms);
+  for (int sp = 2; nt < sms && sp <= std::min(s_cap, 32); ++sp) {
+    const double cost = (double)ceil_div(nt * sp, sms) / sp * (1.0 + 0.02 * (sp - 1));
+    if (cost < best * 0.97) {
+      best = cost;
+      S = sp;
+    }
+  }
+  pp.t1.kt_per_split = ceil_div(KT1, S);
+  pp.t1.S = ceil_div(KT1, pp.t1.kt_per_split);
+  pp.t2.kt_per_split = ceil_div(KT2, S);
+  pp.t2.S = ceil_div(KT2, pp.t2.kt_per_split);
+  const size_t mp1 = (size_t)(a1.fused ? 2 : 1) * a1.M, mp2 = (size_t)(a2.fused ? 2 : 1) * a2.M;
+  pp.t1.part_elems = pp.t1.S > 1 ? (size_t)pp.t1.S * a1.max_rows * mp1 : 0;
+  pp.t2.part_elems = pp.t2.S > 1 ? (size_t)pp.t2.S * a2.max_rows * mp2 : 0;
+  pp.t1.counter_elems = 4 * ((size_t)(a1.M / 128) * (ceil_div(a1.max_rows, BN) + A) + nt2 + 1);
+  return pp;
+}
+
+int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, float* part1,
+                   float* part2, int32_t* counters, int32_t* err, cudaStream_t st) {
+  if (a1.max_rows <= 0) return launch_tc(a2, pp.t2, part2, counters, err, st);
+  TcParams kp{};
+  int r = fill_params(kp, a1, pp.t1, part1, counters, err);
+  if (r != MOE_OK) return r;
+  if (a2.max_rows > 0) {
+    if (!encode_tokens(&kp.tmap_b2, a2.xin, a2.K, a2.max_rows, pp.t1.BN))
+      return MOE_ERR_INVALID_ARG;
+    kp.g2 = 1;
+    kp.w2 = static_cast<const char*>(a2.tab->p[0]) + a2.w_off;
+    kp.M2 = a2.M;
+    kp.K2 = a2.K;
+    kp.S2 = pp.t2.S;
+    kp.kt_per_split2 = pp.t2.kt_per_split;
+    kp.rows2 = a2.max_rows;
+    kp.out2 = a2.out;
+    kp.part2 = part2;
+  }
+  MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, pp.t1.counter_elems * sizeof(int32_t), st));
+  return a1.int4 ? dispatch_bn<true>(a1.fused, pp.t1.BN, kp, st)
+                 : dispatch_bn<false>(a1.fused, pp.t1.BN, kp, st);
 }
 
 int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,

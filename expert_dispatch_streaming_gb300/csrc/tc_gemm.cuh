@@ -25,6 +25,14 @@ struct TcParams {
   int kb_mod;
   float* out_f32;
   int ldo, m_limit;
+  // optional second group after the routed experts (the shared expert): rows2 token rows of its
+  // own token map, with its own weights (section base), shapes, split count and outputs
+  int g2;
+  CUtensorMap tmap_b2;
+  const void* w2;
+  int M2, K2, S2, kt_per_split2, rows2;
+  uint16_t* out2;
+  float* part2;
 };
 
 using TcPlan = TcPlanLite;
@@ -33,6 +41,16 @@ bool tc_supported(const GemmArgs& a);
 TcPlan plan_tc(const GemmArgs& a);
 int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters, int32_t* err,
               cudaStream_t st);
+
+// One launch for two groups: the routed experts of a1 and one extra group a2 (the shared
+// expert: a single expert whose rows are a2.max_rows consecutive token rows).  Both use the
+// same kernel variant (token tile, fused or not, weight type); each keeps its own split count.
+struct TcPair {
+  TcPlan t1, t2;
+};
+TcPair plan_tc_pair(const GemmArgs& a1, const GemmArgs& a2);
+int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, float* part1,
+                   float* part2, int32_t* counters, int32_t* err, cudaStream_t st);
 
 // Router logits on the tensor cores: logits[t][c] (c < C, fp32, row stride C) =
 // sum_k img[c][k] * x[t][k mod H] with img the [Mpad x 3H] tiled bf16 image of the three

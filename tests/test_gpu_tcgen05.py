@@ -105,3 +105,21 @@ def test_layer_tcgen05_mixtral_prefill_sampled(moe, syn):
     rows = np.array([0, 1, 777, 2048, 4095])
     ref = moe_ref.layer_forward(cfg, 0, xb, forced_ids=ids.cpu().numpy(), rows=rows)
     assert_close(got[rows], ref["out"], "mixtral T=4096 tcgen05 sampled rows")
+
+
+@pytest.mark.parametrize("T", [1, 40, 300])
+def test_layer_tcgen05_int4_with_shared_expert(moe, syn, T):
+    """INT4 routed + shared expert in one tcgen05 launch per GEMM (split K at small T)."""
+    cfg = wl.custom("ds_tc", cfg_id=122, H=512, E=64, k=8, I=256, gating="sigmoid_bias_renorm",
+                    scale=2.5, Is=384, shared_gate="one", wdtype="int4_g128", zipf_s=1.1,
+                    bias_kind="select")
+    dl = syn.DeviceLayer(cfg)
+    xb = wl.tokens(cfg, T)
+    x = syn.to_device_bits(xb)
+    ws = dl.workspace(T)
+    ids = torch.empty((T, cfg.k), dtype=torch.int32, device="cuda")
+    out, _ = dl.forward(x, ws, ids_out=ids)
+    torch.cuda.synchronize()
+    assert moe.moe_workspace_error(ws) == 0
+    ref = moe_ref.layer_forward(cfg, 0, xb, forced_ids=ids.cpu().numpy())
+    assert_close(syn.bits_of(out), ref["out"], f"int4 + shared T={T} tcgen05")
