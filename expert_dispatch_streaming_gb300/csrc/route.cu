@@ -96,8 +96,26 @@ router_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ 
   }
 }
 
+// Sums the S H-slice partials of every logit into slice 0, in place (fixed order: eight
+// interleaved running sums over the slices, combined pairwise).  One thread per (token,
+// column); used when a small batch was spread over many slices, so that the gate kernel reads
+// one value per logit instead of S.
+__global__ void __launch_bounds__(256)
+reduce_slices_kernel(float* __restrict__ part, int S, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  int sp = 0;
+  for (; sp + 8 <= S; sp += 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) a[j] += part[(size_t)(sp + j) * n + i];
+  }
+  for (int j = 0; sp < S; ++sp, ++j) a[j] += part[(size_t)sp * n + i];
+  part[i] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+}
+
 // ------------------------------------------------------------------------------ A2 gating
-constexpr int G_WARPS = 8, G_TOK_PER_WARP = 4;
+constexpr int G_WARPS = 8;
 constexpr int EC = kMaxExperts / 32;  // expert slots per lane
 
 __device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
@@ -259,8 +277,8 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
 
-  for (int it = 0; it < G_TOK_PER_WARP; ++it) {
-    const int t = (blockIdx.x * G_WARPS + warp) * G_TOK_PER_WARP + it;
+  for (int it = 0; it < p.tok_per_warp; ++it) {
+    const int t = (blockIdx.x * G_WARPS + warp) * p.tok_per_warp + it;
     if (t >= p.T) break;
 
     // ---- logits: fixed-order sum of the H slices (+ logit bias), scores
@@ -626,13 +644,23 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
     }
+    int S_gate = r.S;
+    if (r.S > 4) {
+      const int n = a.T * r.C;
+      reduce_slices_kernel<<<ceil_div(n, 256), 256, 0, st>>>(s.part, r.S, n);
+      MOE_COUNT_LAUNCH();
+      MOE_LAUNCH_CHECK();
+      S_gate = 1;
+    }
     GateParams p{};
-    p.part = s.part; p.S = r.S; p.C = r.C;
+    p.part = s.part; p.S = S_gate; p.C = r.C;
     p.x = a.x; p.w_r = a.w_r; p.w_rT = s.w_rT; p.logit_bias = a.logit_bias; p.sel_bias = a.sel_bias;
     p.forced = a.forced; p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.mode = a.gating;
     p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
     p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = s.hist;
-    const int per_cta = G_WARPS * G_TOK_PER_WARP;
+    // small batches: one token per warp (more CTAs); large: four, to amortise the CTA
+    p.tok_per_warp = a.T <= 1024 ? 1 : 4;
+    const int per_cta = G_WARPS * p.tok_per_warp;
     gate_topk_kernel<<<ceil_div(a.T, per_cta), G_WARPS * 32, 0, st>>>(p);
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();

@@ -26,6 +26,7 @@ struct GateParams {
   float* shared_gate;
   int32_t* tie_flags;
   int32_t* hist;
+  int tok_per_warp;
 };
 
 struct RoutePlan {
