@@ -672,7 +672,8 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
   if (a.T > 0) {
     // small batches copy the rows inside the per-tile ranking kernel; large ones gather with
     // one warp per destination row over the whole GPU (the per-tile grid is too small)
-    const bool fused_copy = a.x_perm && a.T < kSeparateGatherMinT;
+    const bool fused_copy =
+        a.x_perm && (size_t)a.T * a.k * a.H * 2 <= kFusedGatherMaxBytes && a.T < kSeparateGatherMinT;
     rank_permute_kernel<<<r.ntiles, 256, 0, st>>>(a.ids, s.base, a.T, a.k, a.E, a.H, a.x,
                                                   a.pos, a.src, fused_copy ? a.x_perm : nullptr);
     MOE_COUNT_LAUNCH();

@@ -42,6 +42,9 @@ struct RoutePlan {
 constexpr int kTcRouterMinT = 256;
 // batches of at least this many tokens gather x_perm in a separate, GPU-wide kernel
 constexpr int kSeparateGatherMinT = 1024;
+// ... and so do batches whose permuted rows exceed this many bytes (one CTA per 128-token tile
+// would copy them)
+constexpr size_t kFusedGatherMaxBytes = size_t(512) << 10;
 
 struct RouteScratch {
   float* part;      // [S][T][C]
