@@ -153,22 +153,32 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + 
 
 template <int BN, bool FUSED, bool INT4>
 struct Cfg {
-  static constexpr int NA = FUSED ? 2 : 1;                    // weight tiles per stage
+  static constexpr int NA = FUSED ? 2 : 1;                    // weight tiles per K step
   static constexpr int A_BYTES = 16384;                       // 128 rows x 64 k bf16
   static constexpr int B_BYTES = BN * 128;                    // BN rows x 64 k bf16
   // INT4: per 64-k step, half of an 8448-byte INT4 tile (4096 B of codes) + its 256 B scales
   static constexpr int RAW_BYTES = INT4 ? 4096 + 256 : 0;
-  static constexpr int RAW_OFF = NA * A_BYTES + B_BYTES;
-  static constexpr int STAGE = (RAW_OFF + NA * RAW_BYTES + 1023) / 1024 * 1024;
+  // ring 1 (filled by the producer): bf16 = A tile(s) + B tile; INT4 = B tile + raw codes.
+  // ring 2 (INT4 only): the dequantised bf16 A tile(s), written by the dequant warps.  The
+  // small raw + B slots make ring 1 deep (it hides the load latency) while the large bf16 A
+  // slots only need to stay a step or two ahead of the MMA.
+  static constexpr int R1 = INT4 ? (B_BYTES + NA * RAW_BYTES + 1023) / 1024 * 1024
+                                 : NA * A_BYTES + B_BYTES;
+  static constexpr int R2 = INT4 ? NA * A_BYTES : 0;
+  static constexpr int D2 = INT4 ? (NA == 2 ? 2 : 3) : 0;
+  static constexpr int D1_FIT = (200 * 1024 - D2 * R2) / R1;
+  static constexpr int D1 = D1_FIT > 8 ? 8 : D1_FIT;
+  static constexpr int RING1 = D2 * R2;                       // byte offset of ring 1
+  static constexpr int B_OFF = INT4 ? 0 : NA * A_BYTES;       // B tile inside a ring-1 slot
+  static constexpr int RAW_OFF = B_BYTES;                     // raw codes inside (INT4)
   static constexpr int TX = INT4 ? NA * RAW_BYTES + B_BYTES : NA * A_BYTES + B_BYTES;
-  static constexpr int STAGES = (200 * 1024) / STAGE > 8 ? 8 : (200 * 1024) / STAGE;
   static constexpr int ACC = NA * BN;                         // TMEM columns per tile
   static constexpr int BUFS = (2 * ACC <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = ACC * BUFS <= 32 ? 32 : ACC * BUFS <= 64 ? 64
                                  : ACC * BUFS <= 128 ? 128 : ACC * BUFS <= 256 ? 256 : 512;
   static constexpr int DQ_WARPS = 8;                          // INT4 dequant warps
   static constexpr int THREADS = INT4 ? 192 + 32 * DQ_WARPS : 192;
-  static constexpr int SMEM = STAGES * STAGE + 1024 /*align*/ + 4096 /*barriers, prefix*/;
+  static constexpr int SMEM = RING1 + D1 * R1 + 1024 /*align*/ + 4096 /*barriers, prefix*/;
 };
 
 struct Unit {
@@ -241,11 +251,12 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + C::STAGES;
-  uint64_t* afull = bars + 2 * C::STAGES;   // INT4: dequantised A tiles ready
-  uint64_t* tfull = bars + 3 * C::STAGES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING1 + C::D1 * C::R1);
+  uint64_t* full = bars;                    // ring 1: loaded
+  uint64_t* empty = bars + 8;               // ring 1: consumed by the MMA
+  uint64_t* afull = bars + 16;              // ring 2 (INT4): dequantised A ready
+  uint64_t* aempty = bars + 24;             // ring 2 (INT4): consumed by the MMA
+  uint64_t* tfull = bars + 32;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   int* pref = reinterpret_cast<int*>(tmem_slot + 4);   // [kMaxExperts + 2]
@@ -255,10 +266,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
   const int n_act = p.host_n >= 0 ? p.host_n : *p.n_active;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < C::STAGES; ++s) {
+    for (int s = 0; s < 8; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
       mbar_init(smem_u32(&afull[s]), C::DQ_WARPS);
+      mbar_init(smem_u32(&aempty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&tfull[b]), 1);
@@ -317,7 +329,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         for (int kt = kt_lo; kt < kt_hi; ++kt) {
           if (!(ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, 1))) break;
           const uint32_t fb = smem_u32(&full[stage]);
-          uint8_t* st = smem + stage * C::STAGE;
+          uint8_t* st = smem + C::RING1 + stage * C::R1;
           mbar_expect_tx(fb, C::TX);
           if (INT4) {
             // codes of this 64-k half of the 128-k INT4 tile, then the tile's row scales
@@ -333,9 +345,9 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
               bulk_g2s(smem_u32(st + C::A_BYTES),
                        wb + ((size_t)(x.mt + MTx) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
           }
-          tma_2d(smem_u32(st + C::NA * C::A_BYTES), x.tm,
+          tma_2d(smem_u32(st + C::B_OFF), x.tm,
                  (ROUTER ? kt % p.kb_mod : kt) * 64, x.r0 + x.nt * BN, fb);
-          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+          if (++stage == C::D1) { stage = 0; phase ^= 1; }
         }
       }
     }
@@ -343,8 +355,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t idesc = idesc_bf16(128, BN);
-      int stage = 0, buf = 0;
-      uint32_t phase = 0, aphase = 0;
+      int stage = 0, buf = 0, astage = 0;
+      uint32_t phase = 0, aphase = 0, a2phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit x = decode_unit(p, pref, n_act, u, BN);
@@ -353,11 +365,12 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         tc_fence_after();
         const uint32_t dg = tmem_base + buf * C::ACC;
         for (int kt = kt_lo; kt < kt_hi; ++kt) {
-          if (!(ok = mbar_wait(smem_u32(INT4 ? &afull[stage] : &full[stage]), phase, p.err, 3)))
-            break;
+          if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 3))) break;
+          if (INT4 && !(ok = mbar_wait(smem_u32(&afull[astage]), a2phase, p.err, 6))) break;
           tc_fence_after();
-          const uint32_t sa = smem_u32(smem + stage * C::STAGE);
-          const uint32_t sb = sa + (FUSED ? 2 : 1) * C::A_BYTES;
+          const uint32_t s1 = smem_u32(smem + C::RING1 + stage * C::R1);
+          const uint32_t sa = INT4 ? smem_u32(smem + astage * C::R2) : s1;
+          const uint32_t sb = s1 + C::B_OFF;
           const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sb);
           const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
 #pragma unroll
@@ -367,7 +380,9 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
             if (FUSED) mma_bf16(dg + BN, du + 2 * j, db + 2 * j, idesc, acc);
           }
           mma_commit(smem_u32(&empty[stage]));
-          if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+          if (INT4) mma_commit(smem_u32(&aempty[astage]));
+          if (++stage == C::D1) { stage = 0; phase ^= 1; }
+          if (INT4 && ++astage == C::D2) { astage = 0; a2phase ^= 1; }
         }
         mma_commit(smem_u32(&tfull[buf]));
         if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
@@ -476,8 +491,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     // work item = (weight tile w, 32-code chunk cc, row r): one 16-byte load of codes + the
     // row's scale -> four 16-byte chunks of bf16(code * scale) in the 128-byte-swizzled A image
     const int td = threadIdx.x - 192;
-    int stage = 0;
-    uint32_t phase = 0;
+    int stage = 0, astage = 0;
+    uint32_t phase = 0, a2phase = 0;
     bool ok = true;
     const uint32_t k136 = 0x43084308u;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
@@ -485,17 +500,27 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
       const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
       for (int kt = kt_lo; kt < kt_hi; ++kt) {
         if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
-        uint8_t* st = smem + stage * C::STAGE;
+        if (!(ok = mbar_wait(smem_u32(&aempty[astage]), a2phase ^ 1, p.err, 7))) break;
+        const uint8_t* st = smem + C::RING1 + stage * C::R1;
+        uint8_t* at = smem + astage * C::R2;
+        // issue every load of this step before converting
+        uint4 q[C::NA];
+        uint32_t s2[C::NA];
 #pragma unroll
         for (int it = 0; it < C::NA; ++it) {
           const int item = td + it * 32 * C::DQ_WARPS;
           const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
           const uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
-          uint8_t* arow = st + w * C::A_BYTES + r * 128;
+          q[it] = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
           const uint32_t sb = *reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r);
-          const uint32_t s2 = sb | (sb << 16);
-          const uint4 q = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
-          const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+          s2[it] = sb | (sb << 16);
+        }
+#pragma unroll
+        for (int it = 0; it < C::NA; ++it) {
+          const int item = td + it * 32 * C::DQ_WARPS;
+          const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
+          uint8_t* arow = at + w * C::A_BYTES + r * 128;
+          const uint32_t qw[4] = {q[it].x, q[it].y, q[it].z, q[it].w};
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
             // word j holds codes 8j..8j+7; pair jp (codes 8j+2jp, +1) in nibbles jp and jp + 4
@@ -505,7 +530,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
               uint32_t b = ((qw[j] >> (4 * jp)) & 0x000F000Fu) ^ 0x43084308u;  // 128 + code + 8
               __nv_bfloat162 h = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&b),
                                          *reinterpret_cast<const __nv_bfloat162*>(&k136));
-              h = __hmul2(h, *reinterpret_cast<const __nv_bfloat162*>(&s2));
+              h = __hmul2(h, *reinterpret_cast<const __nv_bfloat162*>(&s2[it]));
               pr[jp] = *reinterpret_cast<uint32_t*>(&h);
             }
             const int oc = cc * 4 + j;
@@ -515,8 +540,9 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&afull[stage]));
-        if (++stage == C::STAGES) { stage = 0; phase ^= 1; }
+        if (lane == 0) mbar_arrive(smem_u32(&afull[astage]));
+        if (++stage == C::D1) { stage = 0; phase ^= 1; }
+        if (++astage == C::D2) { astage = 0; a2phase ^= 1; }
       }
     }
   }
