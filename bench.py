@@ -334,21 +334,23 @@ def run_streamed(args, local_rank):
                                         time_copies=1)
         return moe.moe_expert_cache_create(c)
 
-    # probe: pinned H2D bandwidth of one bundle-sized copy on this machine
+    # probe: pinned H2D bandwidth of one bundle-sized copy on this machine (best of 3 rounds)
     d = torch.empty(nb, dtype=torch.uint8, device=dev)
     s = torch.cuda.Stream(device=dev)
+    probe_gbs = 0.0
     for _ in range(3):
         with torch.cuda.stream(s):
-            d.copy_(store[0], non_blocking=True)
-    s.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(s):
-        e0.record(s)
-        for i in range(40):
-            d.copy_(store[i % store.shape[0]], non_blocking=True)
-        e1.record(s)
-    s.synchronize()
-    probe_gbs = 40 * nb / (e0.elapsed_time(e1) / 1e3) / 1e9
+            for i in range(4):
+                d.copy_(store[i], non_blocking=True)
+        s.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(s):
+            e0.record(s)
+            for i in range(32):
+                d.copy_(store[i % store.shape[0]], non_blocking=True)
+            e1.record(s)
+        s.synchronize()
+        probe_gbs = max(probe_gbs, 32 * nb / (e0.elapsed_time(e1) / 1e3) / 1e9)
     del d
 
     stream = torch.cuda.Stream(device=dev)

@@ -272,3 +272,67 @@ def test_layer_forward_streaming_kernel(moe, syn, cfg, T):
         _layer_case(syn, cfg, T)
     finally:
         moe.set_ffn_kernel("auto")
+
+
+def test_layer_forward_empty_batch(moe, syn):
+    cfg = SMALL[2]
+    dl = syn.DeviceLayer(cfg)
+    x = torch.empty((0, cfg.H), dtype=torch.int16, device="cuda")
+    out = torch.empty((0, cfg.H), dtype=torch.int16, device="cuda")
+    ws = dl.workspace(1)
+    st = moe.moe_layer_forward(dl.desc, x, 0, None, None, out, None, ws, ws.numel())
+    assert st.n_launches == 0
+
+
+def test_layer_k_equals_E_is_dense_mixture_on_gpu(syn):
+    """Top-k with k = E (softmax renormalised over all) equals the dense gate-weighted mixture."""
+    cfg = wl.custom("dense", cfg_id=150, H=256, E=8, k=8, I=256)
+    _layer_case(syn, cfg, 37)
+    xb = wl.tokens(cfg, 37)
+    x = bf16.decode(xb)
+    l = x @ wl.router(cfg, 0).astype(np.float64)
+    gates = np.exp(l - l.max(1, keepdims=True))
+    gates /= gates.sum(1, keepdims=True)
+    experts = [moe_ref.expert_matrices(wl.expert(cfg, 0, e)) for e in range(cfg.E)]
+    ref = moe_ref.dense_mixture(x, gates, experts)
+    dl = syn.DeviceLayer(cfg)
+    out, _ = dl.forward(syn.to_device_bits(xb), dl.workspace(37))
+    torch.cuda.synchronize()
+    assert_close(syn.bits_of(out), ref, "k = E vs dense mixture")
+
+
+def test_layer_token_permutation_invariance_on_gpu(syn):
+    """Permuting tokens permutes the outputs bit for bit (no cross-token arithmetic)."""
+    cfg = SMALL[2]
+    T = 300
+    xb = wl.tokens(cfg, T)
+    perm = np.random.default_rng(7).permutation(T)
+    dl = syn.DeviceLayer(cfg)
+    ws = dl.workspace(T)
+    a, _ = dl.forward(syn.to_device_bits(xb), ws)
+    a = syn.bits_of(a)
+    b, _ = dl.forward(syn.to_device_bits(xb[perm]), ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(a[perm], syn.bits_of(b))
+
+
+def test_one_hot_router_on_gpu_reproduces_single_expert(moe, syn):
+    """A router whose column e* beats every other logit by ~100 sends every token to e* with
+    weight 1: the layer output is that expert's FFN (oracle SwiGLU of that expert)."""
+    cfg = wl.custom("onehot", cfg_id=151, H=256, E=8, k=1, I=256)
+    T, star = 21, 5
+    x = bf16.decode(wl.tokens(cfg, T))
+    s = x.sum(1)
+    x = bf16.round_rne(x * (100.0 / np.where(np.abs(s) < 1e-3, 1e-3, s))[:, None])
+    w_r = np.zeros((cfg.H, cfg.E), np.float32)
+    w_r[:, star] = 1.0
+    dl = syn.DeviceLayer(cfg)
+    dl.w_r.copy_(torch.from_numpy(w_r))
+    ids = torch.empty((T, 1), dtype=torch.int32, device="cuda")
+    w = torch.empty((T, 1), dtype=torch.float32, device="cuda")
+    out, _ = dl.forward(syn.to_device_bits(bf16.to_bits(x)), dl.workspace(T), ids_out=ids, w_out=w)
+    torch.cuda.synchronize()
+    assert np.all(ids.cpu().numpy() == star) and np.all(w.cpu().numpy() == 1.0)
+    wg, wu, wd = moe_ref.expert_matrices(wl.expert(cfg, 0, star))
+    y, _ = moe_ref.swiglu_ffn(x, wg, wu, wd)
+    assert_close(syn.bits_of(out), y, "one-hot router")
