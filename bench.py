@@ -421,6 +421,30 @@ def run_streamed(args, local_rank):
         res["overlap_fraction"] = (round(min(1.0, max(0.0, 1 - (t_stream - t_res) / t_copy)), 4)
                                    if t_copy > 0 else None)
         out["T"][str(T)] = res
+        if T == 8 and args.capacity_sweep:
+            # hit rate and throughput against the slot budget (the LRU thrash cliff): from
+            # a few layers' working set up to every bundle resident
+            sweep = {}
+            steps = min(args.stream_steps, 64)
+            for gib in (1, 2, 4, 8, 16):
+                cap = min(gib << 30, cfg.layers * cfg.E * nb)
+                c2 = make(cap)
+                try:
+                    torch.cuda.synchronize()
+                    e0.record(stream)
+                    run(c2, steps)
+                    e1.record(stream)
+                    stream.synchronize()
+                    t_c = e0.elapsed_time(e1) / 1e3
+                    st2 = moe.moe_expert_cache_stats(c2)
+                    moe.moe_expert_cache_copy_time(c2)
+                finally:
+                    moe.moe_expert_cache_destroy(c2)
+                sweep[f"{gib}GiB"] = {
+                    "slots": cap // nb, "steps": steps,
+                    "hit_rate": round(st2["hits"] / max(1, st2["hits"] + st2["misses"]), 4),
+                    "tokens_per_s": round(T * steps / t_c, 1)}
+            out["capacity_sweep_T8"] = sweep
         del xs, ids_dev, ws
     del store
     return out
@@ -468,6 +492,7 @@ def main():
     ap.add_argument("--no-streamed", dest="streamed", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--stream-steps", type=int, default=wl.STREAM_STEPS)
+    ap.add_argument("--no-capacity-sweep", dest="capacity_sweep", action="store_false")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.T is None:
