@@ -35,9 +35,13 @@ void pack_tiled_bf16(const uint16_t* src, size_t K, size_t N, uint16_t* dst) {
 // Tiled INT4 image of W[n][k] = codes[k][n] with group scales[k/128][n]: tiles of 128 rows x
 // 128 k (one scale group), tile (mt, kt) at ((mt * K/128) + kt) * 8448 bytes.  Inside a tile:
 // 16-byte chunk (c, r) at (c * 128 + r) * 16 holds codes k = kt*128 + 32c .. +31 of row r as four
-// little-endian 32-bit words of eight codes each; word w carries k = 8w + [0, 2, 4, 6, 1, 3, 5, 7]
-// in its nibbles 0..7, so nibbles j and j + 4 hold the consecutive pair (8w + 2j, 8w + 2j + 1).
-// Then the 128 rows' bf16 scales at 8192 + 2r.
+// little-endian 32-bit words of eight codes each.  Codes are stored sign-magnitude: in word
+// w, code k = 8w + 2p + h (pair p = 0..3, half h = 0/1) keeps its magnitude in bits
+// (4 + 16h + 4p) mod 32 .. +2 and its sign in bit (15 + 16h + 4p) mod 32.  Rotating the word
+// right by 4p therefore puts pair p's magnitudes at bits 4-6 / 20-22 and signs at bits 15 / 31:
+// two bf16 subnormals of value q * 2^-129, which one bf16 multiply by scale * 2^129 turns into
+// q * scale.  Then the 128 rows' bf16 scales at 8192 + 2r; |scale| < 0.5 keeps scale * 2^129
+// a finite bf16.
 bool pack_tiled_int4(const int8_t* codes, const uint16_t* scales, size_t K, size_t N,
                      uint8_t* dst) {
   bool ok = true;
@@ -47,18 +51,27 @@ bool pack_tiled_int4(const int8_t* codes, const uint16_t* scales, size_t K, size
       uint8_t* tile = dst + (mt * kt_n + kt) * 8448;
       for (size_t kk = 0; kk < 128; ++kk) {
         const int8_t* src = codes + (kt * 128 + kk) * N + mt * 128;
-        const size_t c = kk >> 5, kp = kk & 31, w = kp >> 3, j = kp & 7;
-        const size_t nib = (j & 1) ? 4 + (j >> 1) : (j >> 1);
-        const size_t byte = 4 * w + (nib >> 1), shift = (nib & 1) * 4;
+        const size_t c = kk >> 5, w = (kk & 31) >> 3, pr = (kk & 7) >> 1, h = kk & 1;
+        const unsigned mag_sh = static_cast<unsigned>((4 + 16 * h + 4 * pr) & 31);
+        const unsigned sgn_sh = static_cast<unsigned>((15 + 16 * h + 4 * pr) & 31);
         for (size_t r = 0; r < 128; ++r) {
-          ok &= src[r] >= -7 && src[r] <= 7;
-          uint8_t& b = tile[(c * 128 + r) * 16 + byte];
-          b = static_cast<uint8_t>((b & ~(0xFu << shift)) |
-                                   ((static_cast<uint8_t>(src[r]) & 0xFu) << shift));
+          const int q = src[r];
+          ok &= q >= -7 && q <= 7;
+          const uint32_t mag = static_cast<uint32_t>(q < 0 ? -q : q) & 7u;
+          const uint32_t bits = (mag << mag_sh) | (static_cast<uint32_t>(q < 0) << sgn_sh);
+          uint8_t* wp = tile + (c * 128 + r) * 16 + 4 * w;
+          uint32_t word;
+          std::memcpy(&word, wp, 4);
+          word |= bits;
+          std::memcpy(wp, &word, 4);
         }
       }
       uint16_t* sc = reinterpret_cast<uint16_t*>(tile + 8192);
-      for (size_t r = 0; r < 128; ++r) sc[r] = scales[kt * N + mt * 128 + r];
+      for (size_t r = 0; r < 128; ++r) {
+        const uint16_t s = scales[kt * N + mt * 128 + r];
+        ok &= ((s >> 7) & 0xFFu) < 126u;   // |scale| < 0.5 and finite
+        sc[r] = s;
+      }
     }
   return ok;
 }

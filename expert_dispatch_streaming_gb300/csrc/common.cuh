@@ -66,4 +66,33 @@ __device__ __forceinline__ uint32_t float2_to_bf16x2(float a, float b) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// ---------------------------------------------------------------- INT4 dequantisation
+// The bundle stores INT4 codes sign-magnitude so that pair p of a 32-bit code word, rotated
+// right by 4p and masked, is two bf16 subnormals of value q * 2^-129 (magnitude in mantissa
+// bits 4-6, sign in bit 15 of each half).  One bf16 multiply by (scale * 2^129) then gives
+// bf16(q * scale), rounded once, exactly as a multiply of the integer q by the scale would.
+// bf16 arithmetic keeps subnormal operands (there is no flush-to-zero form of it).
+
+// (scale * 2^129) in both halves; exact for every bf16 scale with |scale| < 0.5, which the
+// bundle packer enforces.
+__device__ __forceinline__ uint32_t int4_scale_pair(uint16_t scale_bits) {
+  const float f = bf16_bits_to_float(scale_bits) * 0x1p64f * 0x1p65f;
+  const uint32_t b = float_to_bf16_bits(f);
+  return b | (b << 16);
+}
+// Pair p (codes 8w + 2p, 8w + 2p + 1 of code word `word`) -> bf16x2 of q * scale.
+template <int P>
+__device__ __forceinline__ uint32_t int4_pair(uint32_t word, uint32_t scale_pair) {
+  const uint32_t v = (P == 0 ? word : __funnelshift_r(word, word, 4 * P)) & 0x80708070u;
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(scale_pair));
+  return d;
+}
+__device__ __forceinline__ uint32_t int4_pair_dyn(uint32_t word, int p, uint32_t scale_pair) {
+  const uint32_t v = __funnelshift_r(word, word, 4 * p) & 0x80708070u;
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(scale_pair));
+  return d;
+}
+
 }  // namespace moe

@@ -15,9 +15,9 @@
 // slice of two weight rows with 16-byte loads (a warp covers 8 rows x 64 contiguous bytes per
 // load instruction) and the same slice of each token row.  Because the slot -> k assignment
 // is the same for A and B, the MMA computes the exact dot product; only the summation order
-// changes.  INT4 codes (32 per thread per row = one 16-byte load) are widened exactly to bf16
-// integers, multiplied on the tensor cores, and the row's bf16 group scale (one per 128-block)
-// is applied to each block's fp32 partial sum.
+// changes.  INT4 codes (32 per thread per row = one 16-byte load) are dequantised in registers
+// to bf16(code * scale) with the row's group scale (one per 128-block), the same A values the
+// tcgen05 kernel builds in shared memory, and multiplied on the tensor cores.
 //
 // Work unit = (expert with rows, 64-row block of W, K slice).  When there are too few units
 // to fill the GPU the K range is split; every split writes fp32 partials and the last CTA to
@@ -29,6 +29,7 @@
 namespace moe {
 
 int g_ffn_path = 0;
+int g_fused_max_bn = 0;
 
 struct GemmKParams {
   const uint16_t* xin;
@@ -61,17 +62,6 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
   return v;
-}
-
-// Two INT4 codes at bits 0-3 and 16-19 (a pair as stored in the tiled bundle: nibbles j and
-// j + 4 of a code word) -> two bf16 integers (exact).  Offset-binary trick:
-// code c has nibble u with u ^ 8 = c + 8, and the bf16 with bits 0x4300 | (c + 8) is 128 + c + 8.
-__device__ __forceinline__ uint32_t i4pair_to_bf16x2(uint32_t v) {
-  uint32_t w = (v ^ 0x00080008u) | 0x43004300u;
-  const uint32_t k136 = 0x43084308u;  // (136, 136)
-  __nv_bfloat162 r = __hsub2(*reinterpret_cast<const __nv_bfloat162*>(&w),
-                             *reinterpret_cast<const __nv_bfloat162*>(&k136));
-  return *reinterpret_cast<uint32_t*>(&r);
 }
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
@@ -125,7 +115,7 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
 
     for (int kb = k_lo; kb < k_hi; kb += 128 * U) {
       uint4 A[U][NR][VPR];
-      float sc[U][NR];
+      uint32_t sc[U][NR];   // INT4: (scale * 2^129) pairs of the rows' group scales
 #pragma unroll
       for (int uu = 0; uu < U; ++uu) {
         const int kbb = kb + 128 * uu;
@@ -141,10 +131,10 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
             A[uu][r][v] = ok ? ld_stream(ptr) : make_uint4(0, 0, 0, 0);
           }
           sc[uu][r] = (INT4 && ok)
-                          ? bf16_bits_to_float(__ldg(reinterpret_cast<const uint16_t*>(
+                          ? int4_scale_pair(__ldg(reinterpret_cast<const uint16_t*>(
                                 wrow[r] - rsw[r] * 16 + (size_t)(kbb >> 7) * 8448 + 8192) +
                                 rsw[r]))
-                          : 0.f;
+                          : 0u;
         }
       }
 #pragma unroll
@@ -158,11 +148,10 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
 #pragma unroll
           for (int r = 0; r < NR; ++r) {
             if (INT4) {
-              // step s uses codes 4s..4s+3 of the thread's 32: word s/2, pairs (s&1)*2, +1,
-              // each pair in nibbles j and j + 4 of the word
-              const uint32_t q = word_of(A[uu][r][0], s >> 1) >> ((s & 1) * 8);
-              af[s][r][0] = i4pair_to_bf16x2(q & 0x000F000Fu);
-              af[s][r][1] = i4pair_to_bf16x2((q >> 4) & 0x000F000Fu);
+              // step s uses codes 4s..4s+3 of the thread's 32: word s/2, pairs (s&1)*2, +1
+              const uint32_t q = word_of(A[uu][r][0], s >> 1);
+              af[s][r][0] = int4_pair_dyn(q, (s & 1) * 2, sc[uu][r]);
+              af[s][r][1] = int4_pair_dyn(q, (s & 1) * 2 + 1, sc[uu][r]);
             } else {
               af[s][r][0] = word_of(A[uu][r][s >> 1], (2 * s) & 3);
               af[s][r][1] = word_of(A[uu][r][s >> 1], (2 * s + 1) & 3);
@@ -176,28 +165,14 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
               p.xin + (size_t)(r0 + min(n, ne - 1)) * K + kbb + 32 * tq);
 #pragma unroll
           for (int v = 0; v < 4; ++v) xb[v] = n < ne ? __ldg(xp + v) : make_uint4(0, 0, 0, 0);
-          float t0[4] = {0.f, 0.f, 0.f, 0.f}, t1[4] = {0.f, 0.f, 0.f, 0.f};
-          float(&dg)[4] = INT4 ? t0 : acc[j];
-          float(&du)[4] = INT4 ? t1 : accu[j];
 #pragma unroll
           for (int s = 0; s < 8; ++s) {
             const uint32_t b0 = word_of(xb[s >> 1], (2 * s) & 3);
             const uint32_t b1 = word_of(xb[s >> 1], (2 * s + 1) & 3);
-            mma_bf16_16816(dg, af[s][0][0], af[s][1][0], af[s][0][1], af[s][1][1], b0, b1);
+            mma_bf16_16816(acc[j], af[s][0][0], af[s][1][0], af[s][0][1], af[s][1][1], b0, b1);
             if (FUSED)
-              mma_bf16_16816(du, af[s][2][0], af[s][3][0], af[s][2][1], af[s][3][1], b0, b1);
-          }
-          if (INT4) {
-            acc[j][0] = fmaf(sc[uu][0], t0[0], acc[j][0]);
-            acc[j][1] = fmaf(sc[uu][0], t0[1], acc[j][1]);
-            acc[j][2] = fmaf(sc[uu][1], t0[2], acc[j][2]);
-            acc[j][3] = fmaf(sc[uu][1], t0[3], acc[j][3]);
-            if (FUSED) {
-              accu[j][0] = fmaf(sc[uu][2], t1[0], accu[j][0]);
-              accu[j][1] = fmaf(sc[uu][2], t1[1], accu[j][1]);
-              accu[j][2] = fmaf(sc[uu][3], t1[2], accu[j][2]);
-              accu[j][3] = fmaf(sc[uu][3], t1[3], accu[j][3]);
-            }
+              mma_bf16_16816(accu[j], af[s][2][0], af[s][3][0], af[s][2][1], af[s][3][1], b0,
+                             b1);
           }
         }
       }

@@ -36,6 +36,20 @@ namespace {
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 
+// INT4 dequantisation warps and how they share the K steps: the warps form DQ_GROUPS groups
+// and group g converts steps g, g + DQ_GROUPS, ..., so that several steps are converted at
+// once and the fixed latency of a step (barrier waits, shared loads, proxy fence) overlaps.
+#ifndef MOE_DQ_WARPS
+#define MOE_DQ_WARPS 8
+#endif
+#ifndef MOE_DQ_GROUPS
+#define MOE_DQ_GROUPS 1
+#endif
+// Suspend-time hint (ns) of the mbarrier waits; 0 = plain polling.
+#ifndef MOE_WAIT_HINT_NS
+#define MOE_WAIT_HINT_NS 0
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -56,12 +70,21 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#if MOE_WAIT_HINT_NS > 0
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(MOE_WAIT_HINT_NS)
+      : "memory");
+#else
   asm volatile(
       "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 // Bounded wait; false (and an error code recorded) after ~2 s.
@@ -165,9 +188,18 @@ struct Cfg {
   static constexpr int R1 = INT4 ? (B_BYTES + NA * RAW_BYTES + 1023) / 1024 * 1024
                                  : NA * A_BYTES + B_BYTES;
   static constexpr int R2 = INT4 ? NA * A_BYTES : 0;
-  static constexpr int D2 = INT4 ? (NA == 2 ? 2 : 3) : 0;
-  static constexpr int D1_FIT = (200 * 1024 - D2 * R2) / R1;
-  static constexpr int D1 = D1_FIT > 8 ? 8 : D1_FIT;
+  // dequantised stages: with one dequant group three (gate + up) or four (down), so the
+  // dequant warps can run ahead of the MMA; with G step-alternating groups the depths of both
+  // rings are multiples of G, so that every ring stage is always converted by the same group
+  // and each group waits on its own stages' barriers in order
+  static constexpr int G = INT4 ? MOE_DQ_GROUPS : 1;
+  static constexpr int D2 = INT4 ? (NA == 2 ? (G == 1 ? 3 : G) : 4) : 0;
+  static constexpr int BUDGET = (INT4 ? 220 : 200) * 1024;
+  static constexpr int D1_FIT0 = (BUDGET - D2 * R2) / R1;
+  static constexpr int D1_FIT = D1_FIT0 > 8 ? 8 : D1_FIT0;
+  static constexpr int D1 = D1_FIT / G * G;
+  static_assert(D1 >= 2, "ring 1 needs at least two stages");
+  static_assert(!INT4 || (D1 % G == 0 && D2 % G == 0 && D1 >= D2), "ring depths vs groups");
   static constexpr int RING1 = D2 * R2;                       // byte offset of ring 1
   static constexpr int B_OFF = INT4 ? 0 : NA * A_BYTES;       // B tile inside a ring-1 slot
   static constexpr int RAW_OFF = B_BYTES;                     // raw codes inside (INT4)
@@ -176,9 +208,15 @@ struct Cfg {
   static constexpr int BUFS = (2 * ACC <= 512) ? 2 : 1;
   static constexpr int TMEM_COLS = ACC * BUFS <= 32 ? 32 : ACC * BUFS <= 64 ? 64
                                  : ACC * BUFS <= 128 ? 128 : ACC * BUFS <= 256 ? 256 : 512;
-  static constexpr int DQ_WARPS = 8;                          // INT4 dequant warps
+  static constexpr int DQ_WARPS = MOE_DQ_WARPS;               // INT4 dequant warps
+  static constexpr int DQ_GROUPS = MOE_DQ_GROUPS;             // ... in step-alternating groups
+  static constexpr int DQ_GT = 32 * DQ_WARPS / DQ_GROUPS;     // threads of a group
+  static constexpr int DQ_ITEMS = NA * 256;                   // (tile, 32-k chunk, row) items
+  static constexpr int DQ_PER = (DQ_ITEMS + DQ_GT - 1) / DQ_GT;
+  static_assert(DQ_WARPS % DQ_GROUPS == 0, "dequant groups must split the warps evenly");
   static constexpr int THREADS = INT4 ? 192 + 32 * DQ_WARPS : 192;
   static constexpr int SMEM = RING1 + D1 * R1 + 1024 /*align*/ + 4096 /*barriers, prefix*/;
+  static_assert(SMEM <= 232448, "over the 227 KB shared-memory limit of a CTA");
 };
 
 struct Unit {
@@ -269,7 +307,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     for (int s = 0; s < 8; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
-      mbar_init(smem_u32(&afull[s]), C::DQ_WARPS);
+      mbar_init(smem_u32(&afull[s]), C::DQ_WARPS / C::DQ_GROUPS);
       mbar_init(smem_u32(&aempty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -354,13 +392,16 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, BN);
       int stage = 0, buf = 0, astage = 0;
       uint32_t phase = 0, aphase = 0, a2phase = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
         const Unit x = decode_unit(p, pref, n_act, u, BN);
         const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
+        // the last token tile of a group is ragged: multiply only its first N = n_here rounded
+        // up to 16 columns (the accumulator columns past it are never read)
+        const int n_here = min(BN, x.ne - x.nt * BN);
+        const uint32_t idesc = idesc_bf16(128, min(BN, (n_here + 15) & ~15));
         if (!(ok = mbar_wait(smem_u32(&tempty[buf]), aphase ^ 1, p.err, 2))) break;
         tc_fence_after();
         const uint32_t dg = tmem_base + buf * C::ACC;
@@ -487,60 +528,58 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     }
     (void)et;
   } else if (INT4) {
-    // ------------------------------------------------------------ INT4 dequant (warps 6..13)
+    // ------------------------------------------------------------ INT4 dequant (warps 6..)
     // work item = (weight tile w, 32-code chunk cc, row r): one 16-byte load of codes + the
-    // row's scale -> four 16-byte chunks of bf16(code * scale) in the 128-byte-swizzled A image
+    // row's scale -> four 16-byte chunks of bf16(code * scale) in the 128-byte-swizzled A image.
+    // Group g of the dequant warps converts every DQ_GROUPS-th K step, starting at step g.
     const int td = threadIdx.x - 192;
-    int stage = 0, astage = 0;
+    const int grp = td / C::DQ_GT, tg = td % C::DQ_GT;
+    int stage = 0, astage = 0, step = 0;
     uint32_t phase = 0, a2phase = 0;
     bool ok = true;
-    const uint32_t k136 = 0x43084308u;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit x = decode_unit(p, pref, n_act, u, BN);
       const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
-      for (int kt = kt_lo; kt < kt_hi; ++kt) {
-        if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
-        if (!(ok = mbar_wait(smem_u32(&aempty[astage]), a2phase ^ 1, p.err, 7))) break;
-        const uint8_t* st = smem + C::RING1 + stage * C::R1;
-        uint8_t* at = smem + astage * C::R2;
-        // issue every load of this step before converting
-        uint4 q[C::NA];
-        uint32_t s2[C::NA];
+      for (int kt = kt_lo; kt < kt_hi; ++kt, ++step) {
+        if (step % C::DQ_GROUPS == grp) {
+          if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
+          if (!(ok = mbar_wait(smem_u32(&aempty[astage]), a2phase ^ 1, p.err, 7))) break;
+          const uint8_t* st = smem + C::RING1 + stage * C::R1;
+          uint8_t* at = smem + astage * C::R2;
+          // issue every load of this step before converting
+          uint4 q[C::DQ_PER];
+          uint32_t s2[C::DQ_PER];
 #pragma unroll
-        for (int it = 0; it < C::NA; ++it) {
-          const int item = td + it * 32 * C::DQ_WARPS;
-          const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
-          const uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
-          q[it] = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
-          const uint32_t sb = *reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r);
-          s2[it] = sb | (sb << 16);
-        }
-#pragma unroll
-        for (int it = 0; it < C::NA; ++it) {
-          const int item = td + it * 32 * C::DQ_WARPS;
-          const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
-          uint8_t* arow = at + w * C::A_BYTES + r * 128;
-          const uint32_t qw[4] = {q[it].x, q[it].y, q[it].z, q[it].w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            // word j holds codes 8j..8j+7; pair jp (codes 8j+2jp, +1) in nibbles jp and jp + 4
-            uint32_t pr[4];
-#pragma unroll
-            for (int jp = 0; jp < 4; ++jp) {
-              uint32_t b = ((qw[j] >> (4 * jp)) & 0x000F000Fu) ^ 0x43084308u;  // 128 + code + 8
-              __nv_bfloat162 h = __hsub2(*reinterpret_cast<__nv_bfloat162*>(&b),
-                                         *reinterpret_cast<const __nv_bfloat162*>(&k136));
-              h = __hmul2(h, *reinterpret_cast<const __nv_bfloat162*>(&s2[it]));
-              pr[jp] = *reinterpret_cast<uint32_t*>(&h);
+          for (int it = 0; it < C::DQ_PER; ++it) {
+            const int item = tg + it * C::DQ_GT;
+            if (item < C::DQ_ITEMS) {
+              const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
+              const uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
+              q[it] = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
+              s2[it] = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r));
             }
-            const int oc = cc * 4 + j;
-            *reinterpret_cast<uint4*>(arow + ((oc ^ (r & 7)) << 4)) =
-                make_uint4(pr[0], pr[1], pr[2], pr[3]);
           }
+#pragma unroll
+          for (int it = 0; it < C::DQ_PER; ++it) {
+            const int item = tg + it * C::DQ_GT;
+            if (item < C::DQ_ITEMS) {
+              const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
+              uint8_t* arow = at + w * C::A_BYTES + r * 128;
+              const uint32_t qw[4] = {q[it].x, q[it].y, q[it].z, q[it].w};
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                // word j holds codes 8j..8j+7; output chunk = the four pairs in k order
+                const int oc = cc * 4 + j;
+                *reinterpret_cast<uint4*>(arow + ((oc ^ (r & 7)) << 4)) =
+                    make_uint4(int4_pair<0>(qw[j], s2[it]), int4_pair<1>(qw[j], s2[it]),
+                               int4_pair<2>(qw[j], s2[it]), int4_pair<3>(qw[j], s2[it]));
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&afull[astage]));
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&afull[astage]));
         if (++stage == C::D1) { stage = 0; phase ^= 1; }
         if (++astage == C::D2) { astage = 0; a2phase ^= 1; }
       }
@@ -610,10 +649,11 @@ int tc_bn_for(const GemmArgs& a) {
   const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
                                           : std::min(a.E, a.max_rows));
   const int avg = ceil_div(std::max(a.max_rows, 1), A);
-  // fused tiles hold gate and up accumulators: a 256-token tile would fill all of TMEM (no
-  // double buffer, epilogue not overlapped with the next tile's MMA) and, with INT4, leave room
-  // for two stages only; 128-token fused tiles measured faster at every shape tried
-  const int cap = a.fused ? 128 : 256;
+  // fused tiles hold gate and up accumulators: a 256-token tile fills all of TMEM (no double
+  // buffer, the epilogue is not overlapped with the next tile's MMA).  With bf16 weights
+  // 128-token fused tiles measured faster; with INT4 the wider tile halves the dequantisation
+  // work per token, the bound of that kernel.
+  const int cap = !a.fused ? 256 : g_fused_max_bn ? g_fused_max_bn : a.int4 ? 256 : 128;
   const int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
   return std::min(bn, cap);
 }

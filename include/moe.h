@@ -64,8 +64,11 @@ int moe_version(void);
  *  MOE_OPT_FFN_KERNEL: which expert-FFN kernel runs: 0 = automatic (default: the tensor-core
  *    tcgen05 kernel wherever it supports the weight type, else the mma.sync weight-streaming
  *    kernel), 1 = always the streaming kernel, 2 = tcgen05 wherever supported.  Both compute
- *    the same layer; tests use the option to cover both. */
-enum moe_option { MOE_OPT_FFN_KERNEL = 1 };
+ *    the same layer; tests use the option to cover both.
+ *  MOE_OPT_FUSED_MAX_BN: widest token tile of the tcgen05 gate/up kernel: 0 = automatic
+ *    (default: 256 for INT4 weights, whose dequantisation is shared by the tile's tokens, else
+ *    128), or 128 / 256.  A tuning knob: results are the same at either width. */
+enum moe_option { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FUSED_MAX_BN = 2 };
 int moe_set_option(int option, int value);
 
 /* Reads the device error word kept in the first 4 bytes of a moe_layer_forward or
@@ -110,9 +113,12 @@ enum moe_wdtype {
  *         tile moves with one bulk copy.
  *   int4: tiles of 128 rows x 128 k (one scale group, 8448 B): 16-byte chunk (c, r) at
  *         (c*128 + r)*16 holds the 32 codes k = 32c..32c+31 of row r as four little-endian
- *         32-bit words; word w holds k = 8w + {0,2,4,6,1,3,5,7} in nibbles 0..7 (so nibbles j and
- *         j+4 are the pair 8w+2j, 8w+2j+1, one shift and one mask apart), followed by the rows'
- *         bf16 group scales at 8192 + 2r.
+ *         32-bit words of eight codes, sign-magnitude: code k = 8w + 2p + h of word w (pair
+ *         p = 0..3, half h = 0/1) has its magnitude in bits (4 + 16h + 4p) mod 32 .. +2 and its
+ *         sign in bit (15 + 16h + 4p) mod 32.  The word rotated right by 4p and masked with
+ *         0x80708070 is pair p as two bf16 subnormals q * 2^-129, which one bf16 multiply by
+ *         scale * 2^129 dequantises.  The codes are followed by the rows' bf16 group scales
+ *         at 8192 + 2r.
  *   gate_up_scale_offset / down_scale_offset give the scale block of the section's first tile.
  * Constraints: H and I multiples of 128.  */
 typedef struct moe_bundle_layout {
@@ -132,7 +138,8 @@ size_t moe_bundle_bytes(int H, int I, int wdtype);
  *  bf16: wg, wu: [H][I] uint16 bf16 bits; wd: [I][H]; scale arguments NULL.
  *  int4: wg, wu: [H][I] int8 codes in [-7,7]; wd: [I][H] int8 codes;
  *        sg, su: [H/128][I] bf16 bits (scale of group h/128, column i); sd: [I/128][H].
- * Host only, synchronous.  Returns MOE_ERR_INVALID_ARG on a code outside [-7, 7]. */
+ * Host only, synchronous.  Returns MOE_ERR_INVALID_ARG on a code outside [-7, 7] or a scale
+ * that is not finite with magnitude below 0.5 (codes times scales then stay below 3.5). */
 int moe_pack_bundle(int H, int I, int wdtype, const void* wg, const void* wu, const void* wd,
                     const uint16_t* sg, const uint16_t* su, const uint16_t* sd, void* dst);
 

@@ -62,18 +62,21 @@ def _untile_bf16(buf, rows, K):
 
 def _untile_int4(buf, rows, K):
     """Inverse of the tiled INT4 image: 8448-byte tiles of 128 rows x 128 k; chunk (c, r) at
-    (c*128 + r)*16 holds k = 32c..32c+31 as four 32-bit words whose nibbles 0..7 carry
-    k = 8w + 0, 2, 4, 6, 1, 3, 5, 7; scales at 8192 + 2r."""
+    (c*128 + r)*16 holds k = 32c..32c+31 as four 32-bit words; code 8w + 2p + h of word w is
+    sign-magnitude, magnitude at bits (4 + 16h + 4p) mod 32 .. +2, sign at bit (15 + 16h + 4p)
+    mod 32;
+    scales at 8192 + 2r."""
     nt = (rows // 128) * (K // 128)
     t = buf[:nt * 8448].reshape(rows // 128, K // 128, 8448)
-    codes = t[:, :, :8192].reshape(rows // 128, K // 128, 4, 128, 4, 4)   # [.., c, r, word, byte]
-    lo = (codes & 0xF).astype(np.int8)
-    hi = (codes >> 4).astype(np.int8)
-    nib = np.empty(codes.shape[:-1] + (8,), np.int8)                      # nibble i of the word
-    nib[..., 0::2], nib[..., 1::2] = lo, hi
-    nib = np.where(nib >= 8, nib - 16, nib)
-    order = [0, 4, 1, 5, 2, 6, 3, 7]          # code k = 8w + j lives in nibble order[j]
-    q = nib[..., order].reshape(codes.shape[:4] + (32,))                  # [mt, kt, c, r, 32]
+    words = t[:, :, :8192].copy().view("<u4").reshape(rows // 128, K // 128, 4, 128, 4)
+    words = words.astype(np.int64)                                       # [mt, kt, c, r, word]
+    q = np.empty(words.shape + (8,), np.int8)
+    for j in range(8):
+        p, h = j >> 1, j & 1
+        mag = (words >> ((4 + 16 * h + 4 * p) % 32)) & 7
+        sgn = (words >> ((15 + 16 * h + 4 * p) % 32)) & 1
+        q[..., j] = np.where(sgn == 1, -mag, mag)
+    q = q.reshape(words.shape[:4] + (32,))                               # [mt, kt, c, r, 32]
     q = q.transpose(0, 3, 1, 2, 4).reshape(rows, K)
     sc = t[:, :, 8192:8448].copy().view(np.uint16).reshape(rows // 128, K // 128, 128)
     sc = sc.transpose(0, 2, 1).reshape(rows, K // 128)
@@ -108,6 +111,43 @@ def test_pack_int4_layout(moe):
     q, sc = _untile_int4(buf[lay.down_offset:], H, I)
     assert np.array_equal(q, w.wd.T) and np.array_equal(sc, w.sd.T)
     assert lay.total_bytes == 3 * (H // 128) * (I // 128) * 8448
+
+
+def test_int4_words_decode_as_bf16_subnormals(moe):
+    """The documented decode of a code word: rotated right by 4p and masked with 0x80708070,
+    pair p of the word is two bf16 subnormals of value q * 2^-129 (low half = the even code)."""
+    H, I = 128, 128
+    rng = np.random.default_rng(5)
+    q = rng.integers(-7, 8, (H, I)).astype(np.int8)
+    s = np.full((H // 128, I), 0x3F00, np.uint16)                        # 0.5 is not allowed,
+    s[:] = 0x3C00                                                        # 2^-7 is
+    buf = np.zeros(moe.moe_bundle_bytes(H, I, "int4_g128"), np.uint8)
+    moe.moe_pack_bundle(H, I, "int4_g128", q, q, q, s, s, s, buf)
+    words = buf[:8192].view("<u4").astype(np.uint64)                     # tile 0 of gate rows
+    for p in range(4):
+        rot = ((words >> (4 * p)) | (words << (32 - 4 * p))) & 0xFFFFFFFF if p else words
+        v = (rot & 0x80708070).astype(np.uint32)
+        lo = ((v & 0xFFFF) << 16).view(np.float32).astype(np.float64) * 2.0 ** 129
+        hi = (v & 0xFFFF0000).view(np.float32).astype(np.float64) * 2.0 ** 129
+        # word index -> (c, r, w); code k = 32c + 8w + 2p (+1) of row r
+        c, r, w = np.unravel_index(np.arange(2048), (4, 128, 4))
+        k = 32 * c + 8 * w + 2 * p
+        assert np.array_equal(lo, q[k, r].astype(np.float64))
+        assert np.array_equal(hi, q[k + 1, r].astype(np.float64))
+
+
+@pytest.mark.parametrize("bad", [0x3F00, 0xBF00, 0x7F80, 0x7FC0, 0x4000])
+def test_pack_rejects_int4_scales_of_half_or_more(moe, bad):
+    """|scale| must stay below 0.5 (and be finite): scale * 2^129 must be a finite bf16."""
+    H, I = 128, 128
+    q = np.zeros((H, I), np.int8)
+    s = np.full((1, I), 0x3C00, np.uint16)
+    s[0, 7] = bad
+    buf = np.zeros(moe.moe_bundle_bytes(H, I, "int4_g128"), np.uint8)
+    with pytest.raises(moe.MoEError):
+        moe.moe_pack_bundle(H, I, "int4_g128", q, q, q, s, s, s, buf)
+    s[0, 7] = 0x3EFF                                                     # just below 0.5
+    moe.moe_pack_bundle(H, I, "int4_g128", q, q, q, s, s, s, buf)
 
 
 def test_pack_rejects_out_of_range_codes(moe):
