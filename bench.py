@@ -153,7 +153,6 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     moe.set_ffn_kernel(args.ffn_kernel)
-    moe.set_fused_max_bn(args.fused_max_bn)
     cfg = WORKLOADS[args.workload]
     pk = peaks()
     layer = syn.DeviceLayer(cfg, device=dev)
@@ -490,7 +489,6 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
     ap.add_argument("--ffn-kernel", default="auto", choices=["auto", "stream", "tcgen05"])
-    ap.add_argument("--fused-max-bn", type=int, default=0, choices=[0, 128, 256])
     ap.add_argument("--no-streamed", dest="streamed", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--stream-steps", type=int, default=wl.STREAM_STEPS)

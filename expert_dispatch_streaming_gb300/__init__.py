@@ -179,7 +179,6 @@ def _check(status, fn):
 
 # ----------------------------------------------------------------------------- API
 MOE_OPT_FFN_KERNEL = 1
-MOE_OPT_FUSED_MAX_BN = 2
 FFN_KERNEL = {"auto": 0, "stream": 1, "tcgen05": 2}
 
 
@@ -190,11 +189,6 @@ def moe_set_option(option, value) -> None:
 def set_ffn_kernel(name: str) -> None:
     """'auto' | 'stream' (mma.sync weight streaming) | 'tcgen05' (tensor-core kernel)."""
     moe_set_option(MOE_OPT_FFN_KERNEL, FFN_KERNEL[name])
-
-
-def set_fused_max_bn(bn: int) -> None:
-    """Widest token tile of the tcgen05 gate/up kernel: 0 (automatic), 128 or 256."""
-    moe_set_option(MOE_OPT_FUSED_MAX_BN, bn)
 
 
 def moe_workspace_error(ws, stream=None) -> int:

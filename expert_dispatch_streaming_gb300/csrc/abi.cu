@@ -229,11 +229,6 @@ int moe_set_option(int option, int value) {
     g_ffn_path = value;
     return MOE_OK;
   }
-  if (option == MOE_OPT_FUSED_MAX_BN) {
-    if (value != 0 && value != 128 && value != 256) return MOE_ERR_INVALID_ARG;
-    g_fused_max_bn = value;
-    return MOE_OK;
-  }
   return MOE_ERR_INVALID_ARG;
 }
 

@@ -29,7 +29,6 @@
 namespace moe {
 
 int g_ffn_path = 0;
-int g_fused_max_bn = 0;
 
 struct GemmKParams {
   const uint16_t* xin;

@@ -45,8 +45,6 @@ struct GemmPlan {
 // Process-wide choice of the expert FFN kernel: 0 = automatic, 1 = mma.sync streaming kernel,
 // 2 = tcgen05 kernel (where supported).
 extern int g_ffn_path;
-// Widest token tile of the fused (gate/up) tcgen05 kernel: 0 = automatic, or 128 / 256.
-extern int g_fused_max_bn;
 
 GemmPlan plan_gemm(const GemmArgs& a);
 size_t gemm_scratch(WsCursor& c, const GemmPlan& g, float** part, int32_t** counters);

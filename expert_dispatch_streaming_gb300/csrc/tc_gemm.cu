@@ -10,13 +10,19 @@
 //
 // Persistent kernel, one CTA per SM, warp-specialised:
 //   warp 0      producer: per 64-wide K step, one 1-D bulk copy per 128-row weight tile (the
-//               bundle stores each tile as its 128-byte-swizzled shared-memory image) and one
-//               2-D TMA load of the BN token rows (128-byte swizzle), completing on an mbarrier;
+//               bundle stores each tile as its 128-byte-swizzled shared-memory image; INT4: the
+//               step's codes and the tile's scales) and one 2-D TMA load of the BN token rows
+//               (128-byte swizzle), completing on an mbarrier;
 //   warp 1      MMA issuer: allocates TMEM, issues tcgen05.mma (M = 128 weight rows, N = BN
-//               tokens, K = 16) from shared-memory descriptors, commits stage release and
-//               accumulator-ready to mbarriers;
+//               tokens, K = 16), commits stage release and accumulator-ready to mbarriers;
 //   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulators (each warp owns one 32-lane
-//               quarter of TMEM), SiLU * mul, bf16 stores (or fp32 split-K partials).
+//               quarter of TMEM), SiLU * mul, bf16 stores (or fp32 split-K partials);
+//   warps 6-13  (INT4 only) dequantisation: codes -> bf16(code * scale) written straight into
+//               tensor memory with tcgen05.st; the MMA takes its A operand from there.
+// Producer and MMA warps run their loops as whole, converged warps (warp-uniform descriptors,
+// warp-vote waits) and issue from one lane chosen by elect.sync: a warp that waits in one
+// divergent lane pays hundreds of cycles per step to reconverge, and an issue under a plain
+// per-lane predicate keeps the MMA operands off the uniform datapath.
 // Work unit = (expert with rows, 128-row weight tile, K split, BN token tile); units are
 // enumerated with the token tile fastest so CTAs running at the same time share a weight
 // tile through L2.  With split K, each split stores fp32 partials and the last CTA to finish
@@ -36,15 +42,6 @@ namespace {
 
 constexpr uint64_t kWaitNs = 2000000000ull;
 
-// INT4 dequantisation warps and how they share the K steps: the warps form DQ_GROUPS groups
-// and group g converts steps g, g + DQ_GROUPS, ..., so that several steps are converted at
-// once and the fixed latency of a step (barrier waits, shared loads, proxy fence) overlaps.
-#ifndef MOE_DQ_WARPS
-#define MOE_DQ_WARPS 8
-#endif
-#ifndef MOE_DQ_GROUPS
-#define MOE_DQ_GROUPS 1
-#endif
 // Suspend-time hint (ns) of the mbarrier waits; 0 = plain polling.
 #ifndef MOE_WAIT_HINT_NS
 #define MOE_WAIT_HINT_NS 0
@@ -60,10 +57,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 }
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
-               : "memory");
 }
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -87,17 +80,22 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 #endif
   return ok != 0;
 }
-// Bounded wait; false (and an error code recorded) after ~2 s.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int32_t* err, int code) {
-  if (mbar_try(bar, parity)) return true;
+// Bounded wait of a whole converged warp: every lane polls and warp votes decide, so the warp
+// never diverges (a divergent single-lane wait costs hundreds of cycles to reconverge).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int32_t* err, int code) {
+  if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (mbar_try(bar, parity)) return true;
-    if ((i & 255) == 0 && globaltimer() - t0 > kWaitNs) {
-      atomicExch(err, code);
+    if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+    if ((i & 255) == 0 && __any_sync(0xffffffffu, globaltimer() - t0 > kWaitNs)) {
+      if ((threadIdx.x & 31) == 0) atomicExch(err, code);
       return false;
     }
   }
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
                                          uint32_t bar) {
@@ -114,6 +112,15 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
       : "memory");
 }
+// One elected lane of a converged warp (elect.sync: the compiler can keep the issue path on
+// the uniform datapath, which a plain lane test does not allow).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n.reg .pred p;\n.reg .b32 r;\nelect.sync r|p, 0xffffffff;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
@@ -128,12 +135,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) |
          ((uint32_t)(M >> 4) << 24);
 }
+// tcgen05.mma of kind::f16 (bf16 A and B, fp32 accumulator in TMEM) from shared-memory
+// descriptors, and (_ts) with the A operand in tensor memory (128 lanes = rows, two bf16 of K
+// per column).
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate));
 }
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile(
@@ -172,6 +189,32 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Thread i of the warp writes registers r[0..N) into TMEM lane (taddr lane + i), columns
+// taddr column .. +N-1; then waits for the stores to complete.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31, %32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 template <int BN, bool FUSED, bool INT4>
@@ -181,41 +224,31 @@ struct Cfg {
   static constexpr int B_BYTES = BN * 128;                    // BN rows x 64 k bf16
   // INT4: per 64-k step, half of an 8448-byte INT4 tile (4096 B of codes) + its 256 B scales
   static constexpr int RAW_BYTES = INT4 ? 4096 + 256 : 0;
-  // ring 1 (filled by the producer): bf16 = A tile(s) + B tile; INT4 = B tile + raw codes.
-  // ring 2 (INT4 only): the dequantised bf16 A tile(s), written by the dequant warps.  The
-  // small raw + B slots make ring 1 deep (it hides the load latency) while the large bf16 A
-  // slots only need to stay a step or two ahead of the MMA.
+  // shared-memory ring (filled by the producer): bf16 = A tile(s) + B tile; INT4 = B tile +
+  // raw codes.  INT4 A tiles never touch shared memory: the dequant warps write them into
+  // tensor memory (tcgen05.st) and the MMA reads A from there.
   static constexpr int R1 = INT4 ? (B_BYTES + NA * RAW_BYTES + 1023) / 1024 * 1024
                                  : NA * A_BYTES + B_BYTES;
-  static constexpr int R2 = INT4 ? NA * A_BYTES : 0;
-  // dequantised stages: with one dequant group three (gate + up) or four (down), so the
-  // dequant warps can run ahead of the MMA; with G step-alternating groups the depths of both
-  // rings are multiples of G, so that every ring stage is always converted by the same group
-  // and each group waits on its own stages' barriers in order
-  static constexpr int G = INT4 ? MOE_DQ_GROUPS : 1;
-  static constexpr int D2 = INT4 ? (NA == 2 ? (G == 1 ? 3 : G) : 4) : 0;
-  static constexpr int BUDGET = (INT4 ? 220 : 200) * 1024;
-  static constexpr int D1_FIT0 = (BUDGET - D2 * R2) / R1;
-  static constexpr int D1_FIT = D1_FIT0 > 8 ? 8 : D1_FIT0;
-  static constexpr int D1 = D1_FIT / G * G;
-  static_assert(D1 >= 2, "ring 1 needs at least two stages");
-  static_assert(!INT4 || (D1 % G == 0 && D2 % G == 0 && D1 >= D2), "ring depths vs groups");
-  static constexpr int RING1 = D2 * R2;                       // byte offset of ring 1
-  static constexpr int B_OFF = INT4 ? 0 : NA * A_BYTES;       // B tile inside a ring-1 slot
+  static constexpr int D1_FIT = 200 * 1024 / R1;
+  static constexpr int D1 = D1_FIT > 8 ? 8 : D1_FIT;
+  static_assert(D1 >= 2, "the ring needs at least two stages");
+  static constexpr int B_OFF = INT4 ? 0 : NA * A_BYTES;       // B tile inside a ring slot
   static constexpr int RAW_OFF = B_BYTES;                     // raw codes inside (INT4)
   static constexpr int TX = INT4 ? NA * RAW_BYTES + B_BYTES : NA * A_BYTES + B_BYTES;
+  // tensor memory: accumulators (gate and up side by side when fused), double-buffered where
+  // they fit, then (INT4) D2 stages of dequantised A, 32 columns (64 bf16 of K) per tile
   static constexpr int ACC = NA * BN;                         // TMEM columns per tile
-  static constexpr int BUFS = (2 * ACC <= 512) ? 2 : 1;
-  static constexpr int TMEM_COLS = ACC * BUFS <= 32 ? 32 : ACC * BUFS <= 64 ? 64
-                                 : ACC * BUFS <= 128 ? 128 : ACC * BUFS <= 256 ? 256 : 512;
-  static constexpr int DQ_WARPS = MOE_DQ_WARPS;               // INT4 dequant warps
-  static constexpr int DQ_GROUPS = MOE_DQ_GROUPS;             // ... in step-alternating groups
-  static constexpr int DQ_GT = 32 * DQ_WARPS / DQ_GROUPS;     // threads of a group
-  static constexpr int DQ_ITEMS = NA * 256;                   // (tile, 32-k chunk, row) items
-  static constexpr int DQ_PER = (DQ_ITEMS + DQ_GT - 1) / DQ_GT;
-  static_assert(DQ_WARPS % DQ_GROUPS == 0, "dequant groups must split the warps evenly");
+  static constexpr int D2 = INT4 ? 4 : 0;
+  static constexpr int A_COLS = D2 * NA * 32;
+  static constexpr int BUFS = (2 * ACC + A_COLS <= 512) ? 2 : 1;
+  static constexpr int A_TMEM = ACC * BUFS;                   // first column of the A stages
+  static constexpr int USED = ACC * BUFS + A_COLS;
+  static_assert(USED <= 512, "tensor memory holds 512 columns");
+  static constexpr int TMEM_COLS = USED <= 32 ? 32 : USED <= 64 ? 64 : USED <= 128 ? 128
+                                 : USED <= 256 ? 256 : 512;
+  static constexpr int DQ_WARPS = 8;                          // INT4 dequant warps, 2 per quarter
   static constexpr int THREADS = INT4 ? 192 + 32 * DQ_WARPS : 192;
-  static constexpr int SMEM = RING1 + D1 * R1 + 1024 /*align*/ + 4096 /*barriers, prefix*/;
+  static constexpr int SMEM = D1 * R1 + 1024 /*align*/ + 4096 /*barriers, prefix*/;
   static_assert(SMEM <= 232448, "over the 227 KB shared-memory limit of a CTA");
 };
 
@@ -289,11 +322,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::RING1 + C::D1 * C::R1);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::D1 * C::R1);
   uint64_t* full = bars;                    // ring 1: loaded
   uint64_t* empty = bars + 8;               // ring 1: consumed by the MMA
-  uint64_t* afull = bars + 16;              // ring 2 (INT4): dequantised A ready
-  uint64_t* aempty = bars + 24;             // ring 2 (INT4): consumed by the MMA
+  uint64_t* afull = bars + 16;              // INT4: dequantised A stage in TMEM ready
+  uint64_t* aempty = bars + 24;             // INT4: A stage consumed by the MMA
   uint64_t* tfull = bars + 32;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
@@ -307,7 +340,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     for (int s = 0; s < 8; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 1);
-      mbar_init(smem_u32(&afull[s]), C::DQ_WARPS / C::DQ_GROUPS);
+      mbar_init(smem_u32(&afull[s]), C::DQ_WARPS);
       mbar_init(smem_u32(&aempty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -355,22 +388,25 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit x = decode_unit(p, pref, n_act, u, BN);
-        const char* wb = x.w;
-        const int KT = x.KT, MTx = x.MT;
-        const int kt_lo = x.ks * x.kps, kt_hi = min(KT, kt_lo + x.kps);
-        for (int kt = kt_lo; kt < kt_hi; ++kt) {
-          if (!(ok = mbar_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, 1))) break;
-          const uint32_t fb = smem_u32(&full[stage]);
-          uint8_t* st = smem + C::RING1 + stage * C::R1;
+    // The whole warp runs the loop (warp-uniform addresses, converged waits); one elected lane
+    // issues the copies.
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const char* wb = x.w;
+      const int KT = x.KT, MTx = x.MT;
+      const int kt_lo = x.ks * x.kps, kt_hi = min(KT, kt_lo + x.kps);
+      for (int kt = kt_lo; kt < kt_hi; ++kt) {
+        if (!(ok = warp_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, 1))) break;
+        const uint32_t fb = smem_u32(&full[stage]);
+        uint8_t* st = smem + stage * C::R1;
+        if (elect_one()) {
           mbar_expect_tx(fb, C::TX);
           if (INT4) {
             // codes of this 64-k half of the 128-k INT4 tile, then the tile's row scales
+#pragma unroll
             for (int w = 0; w < C::NA; ++w) {
               const char* tile = wb + ((size_t)(x.mt + w * MTx) * (KT / 2) + (kt >> 1)) * 8448;
               uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
@@ -378,56 +414,73 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
               bulk_g2s(smem_u32(raw + 4096), tile + 8192, 256, fb);
             }
           } else {
-            bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
+            bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES,
+                        C::A_BYTES, fb);
             if (FUSED)
               bulk_g2s(smem_u32(st + C::A_BYTES),
-                       wb + ((size_t)(x.mt + MTx) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
+                          wb + ((size_t)(x.mt + MTx) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
           }
-          tma_2d(smem_u32(st + C::B_OFF), x.tm,
-                 (ROUTER ? kt % p.kb_mod : kt) * 64, x.r0 + x.nt * BN, fb);
-          if (++stage == C::D1) { stage = 0; phase ^= 1; }
+          tma_2d(smem_u32(st + C::B_OFF), x.tm, (ROUTER ? kt % p.kb_mod : kt) * 64,
+                    x.r0 + x.nt * BN, fb);
         }
+        __syncwarp();
+        if (++stage == C::D1) { stage = 0; phase ^= 1; }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0, buf = 0, astage = 0;
-      uint32_t phase = 0, aphase = 0, a2phase = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-        const Unit x = decode_unit(p, pref, n_act, u, BN);
-        const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
-        // the last token tile of a group is ragged: multiply only its first N = n_here rounded
-        // up to 16 columns (the accumulator columns past it are never read)
-        const int n_here = min(BN, x.ne - x.nt * BN);
-        const uint32_t idesc = idesc_bf16(128, min(BN, (n_here + 15) & ~15));
-        if (!(ok = mbar_wait(smem_u32(&tempty[buf]), aphase ^ 1, p.err, 2))) break;
-        tc_fence_after();
-        const uint32_t dg = tmem_base + buf * C::ACC;
-        for (int kt = kt_lo; kt < kt_hi; ++kt) {
-          if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 3))) break;
-          if (INT4 && !(ok = mbar_wait(smem_u32(&afull[astage]), a2phase, p.err, 6))) break;
+    // As the producer: the converged warp computes the descriptors, one elected lane issues.
+    int stage = 0, buf = 0, astage = 0;
+    uint32_t phase = 0, aphase = 0, a2phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
+      // the last token tile of a group is ragged: multiply only its first N = n_here rounded
+      // up to 16 columns (the accumulator columns past it are never read)
+      const int n_here = min(BN, x.ne - x.nt * BN);
+      const uint32_t idesc = idesc_bf16(128, min(BN, (n_here + 15) & ~15));
+      if (!(ok = warp_wait(smem_u32(&tempty[buf]), aphase ^ 1, p.err, 2))) break;
+      const uint32_t dg = tmem_base + buf * C::ACC;
+      for (int kt = kt_lo; kt < kt_hi; ++kt) {
+        // INT4: the dequant warps arrive on afull only after they saw this stage's full
+        // barrier, so afull alone orders the B tile as well
+        if (!INT4 && !(ok = warp_wait(smem_u32(&full[stage]), phase, p.err, 3))) break;
+        if (INT4 && !(ok = warp_wait(smem_u32(&afull[astage]), a2phase, p.err, 6))) break;
+        const uint32_t s1 = smem_u32(smem + stage * C::R1);
+        const uint64_t db = sdesc_sw128(s1 + C::B_OFF);
+        if (elect_one()) {
           tc_fence_after();
-          const uint32_t s1 = smem_u32(smem + C::RING1 + stage * C::R1);
-          const uint32_t sa = INT4 ? smem_u32(smem + astage * C::R2) : s1;
-          const uint32_t sb = s1 + C::B_OFF;
-          const uint64_t da = sdesc_sw128(sa), db = sdesc_sw128(sb);
-          const uint64_t du = sdesc_sw128(sa + C::A_BYTES);
+          if (INT4) {
+            // A from tensor memory: tile w of this stage at columns A_TMEM + (astage*NA + w)*32,
+            // eight columns (16 k) per MMA
+            const uint32_t ta = tmem_base + C::A_TMEM + astage * C::NA * 32;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t acc = (kt > kt_lo || j > 0) ? 1u : 0u;
-            mma_bf16(dg, da + 2 * j, db + 2 * j, idesc, acc);
-            if (FUSED) mma_bf16(dg + BN, du + 2 * j, db + 2 * j, idesc, acc);
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t acc = (kt > kt_lo || j > 0) ? 1u : 0u;
+              mma_bf16_ts(dg, ta + 8 * j, db + 2 * j, idesc, acc);
+              if (FUSED) mma_bf16_ts(dg + BN, ta + 32 + 8 * j, db + 2 * j, idesc, acc);
+            }
+          } else {
+            const uint64_t da = sdesc_sw128(s1), du = sdesc_sw128(s1 + C::A_BYTES);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint32_t acc = (kt > kt_lo || j > 0) ? 1u : 0u;
+              mma_bf16(dg, da + 2 * j, db + 2 * j, idesc, acc);
+              if (FUSED) mma_bf16(dg + BN, du + 2 * j, db + 2 * j, idesc, acc);
+            }
           }
           mma_commit(smem_u32(&empty[stage]));
           if (INT4) mma_commit(smem_u32(&aempty[astage]));
-          if (++stage == C::D1) { stage = 0; phase ^= 1; }
-          if (INT4 && ++astage == C::D2) { astage = 0; a2phase ^= 1; }
         }
-        mma_commit(smem_u32(&tfull[buf]));
-        if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
+        __syncwarp();
+        if (++stage == C::D1) { stage = 0; phase ^= 1; }
+        if (INT4 && ++astage == C::D2) { astage = 0; a2phase ^= 1; }
       }
+      if (!ok) break;
+      if (elect_one()) mma_commit(smem_u32(&tfull[buf]));
+      __syncwarp();
+      if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ epilogue (warps 2..5)
@@ -439,7 +492,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit x = decode_unit(p, pref, n_act, u, BN);
       const int MP = FUSED ? 2 * x.M : x.M;
-      if (!(ok = mbar_wait(smem_u32(&tfull[buf]), aphase, p.err, 4))) break;
+      if (!(ok = warp_wait(smem_u32(&tfull[buf]), aphase, p.err, 4))) break;
       tc_fence_after();
       const int m = x.mt * 128 + q * 32 + lane;
       const int n_here = min(BN, x.ne - x.nt * BN);
@@ -528,58 +581,57 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     }
     (void)et;
   } else if (INT4) {
-    // ------------------------------------------------------------ INT4 dequant (warps 6..)
-    // work item = (weight tile w, 32-code chunk cc, row r): one 16-byte load of codes + the
-    // row's scale -> four 16-byte chunks of bf16(code * scale) in the 128-byte-swizzled A image.
-    // Group g of the dequant warps converts every DQ_GROUPS-th K step, starting at step g.
-    const int td = threadIdx.x - 192;
-    const int grp = td / C::DQ_GT, tg = td % C::DQ_GT;
-    int stage = 0, astage = 0, step = 0;
+    // ------------------------------------------------------------ INT4 dequant (warps 6..13)
+    // A warp may only touch its own quarter of the TMEM lanes (warp % 4), so two warps share
+    // each quarter: thread = weight row r = 32 * (warp % 4) + lane.  Fused: warps 6-9 convert
+    // the gate tile and warps 10-13 the up tile, each the row's 64 codes of the step (32
+    // columns); not fused: warps 6-9 codes 0-31 and warps 10-13 codes 32-63 (16 columns).
+    const int q = warp & 3, half = (warp - 6) >> 2, r = q * 32 + lane;
+    const int tile = FUSED ? half : 0;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    int stage = 0, astage = 0;
     uint32_t phase = 0, a2phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit x = decode_unit(p, pref, n_act, u, BN);
       const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
-      for (int kt = kt_lo; kt < kt_hi; ++kt, ++step) {
-        if (step % C::DQ_GROUPS == grp) {
-          if (!(ok = mbar_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
-          if (!(ok = mbar_wait(smem_u32(&aempty[astage]), a2phase ^ 1, p.err, 7))) break;
-          const uint8_t* st = smem + C::RING1 + stage * C::R1;
-          uint8_t* at = smem + astage * C::R2;
-          // issue every load of this step before converting
-          uint4 q[C::DQ_PER];
-          uint32_t s2[C::DQ_PER];
+      for (int kt = kt_lo; kt < kt_hi; ++kt) {
+        if (!(ok = warp_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
+        if (!(ok = warp_wait(smem_u32(&aempty[astage]), a2phase ^ 1, p.err, 7))) break;
+        tc_fence_after();
+        const uint8_t* raw = smem + stage * C::R1 + C::RAW_OFF + tile * C::RAW_BYTES;
+        const uint32_t s2 = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r));
+        const uint32_t ta = tmem_base + lane_base + C::A_TMEM + (astage * C::NA + tile) * 32;
+        if (FUSED) {
+          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 16);
+          const uint4 c1 = *reinterpret_cast<const uint4*>(raw + (128 + r) * 16);
+          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+          uint32_t v[32];
 #pragma unroll
-          for (int it = 0; it < C::DQ_PER; ++it) {
-            const int item = tg + it * C::DQ_GT;
-            if (item < C::DQ_ITEMS) {
-              const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
-              const uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
-              q[it] = *reinterpret_cast<const uint4*>(raw + (cc * 128 + r) * 16);
-              s2[it] = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r));
-            }
+          for (int j = 0; j < 8; ++j) {
+            // word j holds codes 8j..8j+7 of the row: columns 4j..4j+3 (pairs in k order)
+            v[4 * j + 0] = int4_pair<0>(w[j], s2);
+            v[4 * j + 1] = int4_pair<1>(w[j], s2);
+            v[4 * j + 2] = int4_pair<2>(w[j], s2);
+            v[4 * j + 3] = int4_pair<3>(w[j], s2);
           }
+          tmem_st32(ta, v);
+        } else {
+          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + (half * 128 + r) * 16);
+          const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
+          uint32_t v[16];
 #pragma unroll
-          for (int it = 0; it < C::DQ_PER; ++it) {
-            const int item = tg + it * C::DQ_GT;
-            if (item < C::DQ_ITEMS) {
-              const int w = item >> 8, cc = (item >> 7) & 1, r = item & 127;
-              uint8_t* arow = at + w * C::A_BYTES + r * 128;
-              const uint32_t qw[4] = {q[it].x, q[it].y, q[it].z, q[it].w};
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                // word j holds codes 8j..8j+7; output chunk = the four pairs in k order
-                const int oc = cc * 4 + j;
-                *reinterpret_cast<uint4*>(arow + ((oc ^ (r & 7)) << 4)) =
-                    make_uint4(int4_pair<0>(qw[j], s2[it]), int4_pair<1>(qw[j], s2[it]),
-                               int4_pair<2>(qw[j], s2[it]), int4_pair<3>(qw[j], s2[it]));
-              }
-            }
+          for (int j = 0; j < 4; ++j) {
+            v[4 * j + 0] = int4_pair<0>(w[j], s2);
+            v[4 * j + 1] = int4_pair<1>(w[j], s2);
+            v[4 * j + 2] = int4_pair<2>(w[j], s2);
+            v[4 * j + 3] = int4_pair<3>(w[j], s2);
           }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&afull[astage]));
+          tmem_st16(ta + half * 16, v);
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&afull[astage]));
         if (++stage == C::D1) { stage = 0; phase ^= 1; }
         if (++astage == C::D2) { astage = 0; a2phase ^= 1; }
       }
@@ -630,7 +682,11 @@ int dispatch_bn(bool fused, int BN, TcParams& kp, cudaStream_t st) {
       case 32: return launch_bn<32, true, INT4>(kp, st);
       case 64: return launch_bn<64, true, INT4>(kp, st);
       case 128: return launch_bn<128, true, INT4>(kp, st);
-      default: return launch_bn<256, true, INT4>(kp, st);
+      default:
+        // INT4 gate/up tiles stop at 128 tokens: their accumulators share tensor memory with
+        // the dequantised weight stages
+        if constexpr (INT4) return launch_bn<128, true, INT4>(kp, st);
+        else return launch_bn<256, true, INT4>(kp, st);
     }
   }
   switch (BN) {
@@ -649,11 +705,10 @@ int tc_bn_for(const GemmArgs& a) {
   const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
                                           : std::min(a.E, a.max_rows));
   const int avg = ceil_div(std::max(a.max_rows, 1), A);
-  // fused tiles hold gate and up accumulators: a 256-token tile fills all of TMEM (no double
-  // buffer, the epilogue is not overlapped with the next tile's MMA).  With bf16 weights
-  // 128-token fused tiles measured faster; with INT4 the wider tile halves the dequantisation
-  // work per token, the bound of that kernel.
-  const int cap = !a.fused ? 256 : g_fused_max_bn ? g_fused_max_bn : a.int4 ? 256 : 128;
+  // fused tiles hold gate and up accumulators: a 256-token tile would fill all of TMEM (no
+  // double buffer, the epilogue not overlapped with the next tile's MMA; with INT4 no room for
+  // the dequantised weight stages); 128-token fused tiles measured faster at every bf16 shape
+  const int cap = a.fused ? 128 : 256;
   const int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
   return std::min(bn, cap);
 }

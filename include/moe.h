@@ -64,11 +64,8 @@ int moe_version(void);
  *  MOE_OPT_FFN_KERNEL: which expert-FFN kernel runs: 0 = automatic (default: the tensor-core
  *    tcgen05 kernel wherever it supports the weight type, else the mma.sync weight-streaming
  *    kernel), 1 = always the streaming kernel, 2 = tcgen05 wherever supported.  Both compute
- *    the same layer; tests use the option to cover both.
- *  MOE_OPT_FUSED_MAX_BN: widest token tile of the tcgen05 gate/up kernel: 0 = automatic
- *    (default: 256 for INT4 weights, whose dequantisation is shared by the tile's tokens, else
- *    128), or 128 / 256.  A tuning knob: results are the same at either width. */
-enum moe_option { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_FUSED_MAX_BN = 2 };
+ *    the same layer; tests use the option to cover both. */
+enum moe_option { MOE_OPT_FFN_KERNEL = 1 };
 int moe_set_option(int option, int value);
 
 /* Reads the device error word kept in the first 4 bytes of a moe_layer_forward or
