@@ -53,6 +53,7 @@ struct LayerScratch {
   float* part_s;    // split-K partials of the shared expert when it shares a launch
   int32_t* counters;
   int32_t* err;     // device error word (first bytes of the workspace)
+  size_t ctl_bytes; // bytes of the control block at the start of the workspace
 };
 
 struct LayerPlan {
@@ -106,7 +107,14 @@ static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
 static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, LayerScratch* s) {
   LayerScratch z{};
   const size_t tk = (size_t)T * L->k;
+  // control block, zeroed by one memset per forward: error word and split-K counters (every
+  // launch leaves the counters it used at zero again)
   z.err = c.take<int32_t>(64);
+  size_t ce = std::max({P.gu.counter_elems, P.dn.counter_elems, P.sgu.counter_elems,
+                        P.sdn.counter_elems, P.mgu.t1.counter_elems, P.mdn.t1.counter_elems,
+                        (size_t)1});
+  z.counters = c.take<int32_t>(ce);
+  z.ctl_bytes = c.used;
   route_scratch(c, P.rp, T, L->E, &z.rs);
   z.ids = c.take<int32_t>(tk + 1);
   z.w = c.take<float>(tk + 1);
@@ -125,12 +133,8 @@ static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, 
   }
   size_t pe = std::max({P.gu.part_elems, P.dn.part_elems, P.sgu.part_elems, P.sdn.part_elems,
                         P.mgu.t1.part_elems, P.mdn.t1.part_elems, (size_t)1});
-  size_t ce = std::max({P.gu.counter_elems, P.dn.counter_elems, P.sgu.counter_elems,
-                        P.sdn.counter_elems, P.mgu.t1.counter_elems, P.mdn.t1.counter_elems,
-                        (size_t)1});
   z.part = c.take<float>(pe);
   z.part_s = c.take<float>(std::max({P.mgu.t2.part_elems, P.mdn.t2.part_elems, (size_t)1}));
-  z.counters = c.take<int32_t>(ce);
   if (s) *s = z;
   return c.used;
 }
@@ -293,10 +297,10 @@ size_t moe_grouped_swiglu_workspace_size(int max_rows, int E, int H, int I, int 
   c.take<int32_t>(64);
   GemmPlan a = plan_gemm(gemm_args(lay, wdtype, true, H, I, E, max_rows));
   GemmPlan b = plan_gemm(gemm_args(lay, wdtype, false, I, H, E, max_rows));
+  c.take<int32_t>(std::max({a.counter_elems, b.counter_elems, (size_t)1}));
   c.take<uint16_t>((size_t)max_rows * I + 8);
   c.take<int32_t>(kMaxExperts + 32);
   c.take<float>(std::max({a.part_elems, b.part_elems, (size_t)1}));
-  c.take<int32_t>(std::max({a.counter_elems, b.counter_elems, (size_t)1}));
   return c.used;
 }
 
@@ -324,16 +328,18 @@ int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
   BundleTable tab{};
   for (int e = 0; e < E; ++e) tab.p[e] = bundles[e];
   WsCursor c(ws, ws_bytes);
-  int32_t* err = c.take<int32_t>(64);
-  uint16_t* h = c.take<uint16_t>((size_t)max_rows * I + 8);
-  int32_t* act = c.take<int32_t>(kMaxExperts + 32);
   GemmArgs gu = gemm_args(lay, wdtype, true, H, I, E, max_rows);
   GemmArgs dn = gemm_args(lay, wdtype, false, I, H, E, max_rows);
   GemmPlan pg = plan_gemm(gu), pd = plan_gemm(dn);
-  float* part = c.take<float>(std::max({pg.part_elems, pd.part_elems, (size_t)1}));
+  // error word and split-K counters first: one memset zeroes both
+  int32_t* err = c.take<int32_t>(64);
   int32_t* ctr = c.take<int32_t>(std::max({pg.counter_elems, pd.counter_elems, (size_t)1}));
+  const size_t ctl_bytes = c.used;
+  uint16_t* h = c.take<uint16_t>((size_t)max_rows * I + 8);
+  int32_t* act = c.take<int32_t>(kMaxExperts + 32);
+  float* part = c.take<float>(std::max({pg.part_elems, pd.part_elems, (size_t)1}));
   MOE_REQUIRE(c.ok());
-  MOE_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int32_t), st));
+  MOE_CUDA_TRY(cudaMemsetAsync(err, 0, ctl_bytes, st));
   active_from_offsets_kernel<<<1, 32, 0, st>>>(offsets, E, act, act + kMaxExperts);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
@@ -406,7 +412,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   LayerScratch s{};
   carve(c, L, T, P, &s);
   MOE_REQUIRE(c.ok());
-  MOE_CUDA_TRY(cudaMemsetAsync(s.err, 0, sizeof(int32_t), s0));
+  MOE_CUDA_TRY(cudaMemsetAsync(s.err, 0, s.ctl_bytes, s0));
 
   if ((r = phase(0)) != MOE_OK) return r;
   // A1-A4: route, dispatch and gather into expert order

@@ -283,8 +283,6 @@ int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* coun
   kp.host_n = a.host_n;
   for (int i = 0; i < (a.host_n > 0 ? a.host_n : 0); ++i) kp.host_ids[i] = (int16_t)a.host_ids[i];
   if (a.host_n == 0) return MOE_OK;
-  if (g.splits > 1)
-    MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, g.counter_elems * sizeof(int32_t), st));
   dim3 grid(g.A_max * g.m_blocks * g.splits);
   if (a.int4) {
     if (a.fused) launch_nt<true, true, 2>(g.nt, grid, kp, st);

@@ -46,6 +46,7 @@ struct GemmPlan {
 // 2 = tcgen05 kernel (where supported).
 extern int g_ffn_path;
 
+// launch_gemm expects zeroed split-K counters and leaves them zero (see tc_gemm.cuh).
 GemmPlan plan_gemm(const GemmArgs& a);
 size_t gemm_scratch(WsCursor& c, const GemmPlan& g, float** part, int32_t** counters);
 int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* counters,

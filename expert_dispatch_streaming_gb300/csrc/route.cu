@@ -18,6 +18,8 @@
 //   rank_permute_kernel    one CTA per 128-token tile: stable rank of each (t, j) within its
 //                          expert from per-expert token bitmasks, pos / src, and (optionally)
 //                          the row copy x -> x_perm with 16-byte vector loads and stores.
+//   route_tail_kernel      for a batch of at most kSmallT tokens (decode), everything after
+//                          the router product in one CTA: two launches route the batch.
 #include "common.cuh"
 #include "route.cuh"
 #include "tc_gemm.cuh"
@@ -271,16 +273,15 @@ router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w
   }
 }
 
-__global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
-  __shared__ float lrow[G_WARPS][kMaxExperts];
-  __shared__ double exact_s[G_WARPS][kMaxExperts];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Gating of token t by one warp: scores, top-k with the fp64 refinement of near-boundary
+// experts, weights; writes ids / w / logits / shared gate / tie flag of t and adds the token's
+// experts to hist[(t / 128) * E + e].  `raw` = the token's C summed router outputs (or NULL:
+// sum the S slices of p.part); lrow / exact_s = this warp's shared-memory rows.
+__device__ void gate_token(const GateParams& p, int t, const float* raw, float* lrow,
+                           double* exact_s) {
+  const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
-
-  for (int it = 0; it < p.tok_per_warp; ++it) {
-    const int t = (blockIdx.x * G_WARPS + warp) * p.tok_per_warp + it;
-    if (t >= p.T) break;
-
+  {
     // ---- logits: fixed-order sum of the H slices (+ logit bias), scores
     float l[EC], sc[EC];
 #pragma unroll
@@ -288,21 +289,22 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
       const int e = lane + 32 * c;
       float v = -CUDART_INF_F, s = -CUDART_INF_F;
       if (e < E) {
-        v = sum_slices(p.part + (size_t)t * p.C + e, p.S, (size_t)p.T * p.C);
+        v = raw ? raw[e] : sum_slices(p.part + (size_t)t * p.C + e, p.S, (size_t)p.T * p.C);
         if (p.logit_bias) v += p.logit_bias[e];
         s = v;
         if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
           s = 1.f / (1.f + expf(-v));
           if (p.sel_bias) s += p.sel_bias[e];
         }
-        lrow[warp][e] = v;
+        lrow[e] = v;
         if (p.logits) p.logits[(size_t)t * E + e] = v;
       }
       l[c] = v;
       sc[c] = s;
     }
     if (lane == 0 && p.shared_gate && p.C > E) {
-      const float z = sum_slices(p.part + (size_t)t * p.C + E, p.S, (size_t)p.T * p.C);
+      const float z =
+          raw ? raw[E] : sum_slices(p.part + (size_t)t * p.C + E, p.S, (size_t)p.T * p.C);
       p.shared_gate[t] = 1.f / (1.f + expf(-z));
     }
 
@@ -372,7 +374,7 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
             const int b = 32 * c + __ffs(m) - 1;
             m &= m - 1;
             double s = exact_score(p, t, b, lane);
-            if (lane == 0) exact_s[warp][b] = s;
+            if (lane == 0) exact_s[b] = s;
           }
         }
         __syncwarp();
@@ -384,8 +386,8 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
 #pragma unroll
           for (int c = 0; c < EC; ++c) {
             const int e = lane + 32 * c;
-            if (band[c] && !chosen[c] && better_d(exact_s[warp][e], e, bs, bi)) {
-              bs = exact_s[warp][e];
+            if (band[c] && !chosen[c] && better_d(exact_s[e], e, bs, bi)) {
+              bs = exact_s[e];
               bi = e;
             }
           }
@@ -401,8 +403,8 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
 #pragma unroll
         for (int c = 0; c < EC; ++c) {
           const int e = lane + 32 * c;
-          if (band[c] && !chosen[c] && better_d(exact_s[warp][e], e, bs, bi)) {
-            bs = exact_s[warp][e];
+          if (band[c] && !chosen[c] && better_d(exact_s[e], e, bs, bi)) {
+            bs = exact_s[e];
             bi = e;
           }
         }
@@ -455,12 +457,12 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
       float denom = 0.f, mx = -CUDART_INF_F;
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j)
-        if (j < k) mx = fmaxf(mx, lrow[warp][my_ids[j]]);
+        if (j < k) mx = fmaxf(mx, lrow[my_ids[j]]);
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
         v[j] = 0.f;
         if (j < k) {
-          const float lj = lrow[warp][my_ids[j]];
+          const float lj = lrow[my_ids[j]];
           if (p.mode == MOE_GATING_SOFTMAX_RENORM) v[j] = expf(lj - mx);
           else if (p.mode == MOE_GATING_SOFTMAX) v[j] = expf(lj - M);
           else v[j] = 1.f / (1.f + expf(-lj));
@@ -481,6 +483,17 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
       if (p.tie_flags) p.tie_flags[t] = flag;
     }
     __syncwarp();
+  }
+}
+
+__global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
+  __shared__ float lrow[G_WARPS][kMaxExperts];
+  __shared__ double exact_s[G_WARPS][kMaxExperts];
+  const int warp = threadIdx.x >> 5;
+  for (int it = 0; it < p.tok_per_warp; ++it) {
+    const int t = (blockIdx.x * G_WARPS + warp) * p.tok_per_warp + it;
+    if (t >= p.T) break;
+    gate_token(p, t, nullptr, lrow[warp], exact_s[warp]);
   }
 }
 
@@ -583,6 +596,122 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ s
   for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
 }
 
+// ------------------------------------------------------------------------------ A2-A4, small T
+// Everything after the router product for a batch of at most kSmallT tokens, in one CTA: the
+// S slice partials of every logit summed in fixed order (a group of G lanes per logit, each
+// lane summing every G-th slice, then a shuffle tree), gating / top-k (one warp per token),
+// the expert histogram and scan, the stable ranks and the row copy into expert order.
+constexpr int kTailThreads = 1024;
+__global__ void __launch_bounds__(kTailThreads)
+route_tail_kernel(GateParams p, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                  int32_t* __restrict__ pos, int32_t* __restrict__ src,
+                  int32_t* __restrict__ active, int32_t* __restrict__ n_active,
+                  int32_t* __restrict__ shared_meta, uint16_t* __restrict__ x_perm) {
+  static_assert(kTailThreads >= kMaxExperts, "the scan takes one thread per expert");
+  __shared__ float lg[kSmallT * (kMaxExperts + 1)];   // summed router outputs of all tokens
+  __shared__ float lrow[G_WARPS][kMaxExperts];
+  __shared__ double exact_s[G_WARPS][kMaxExperts];
+  __shared__ int hist[kMaxExperts], excl[kMaxExperts], srow[kSmallT * kMaxK];
+  const int tid = threadIdx.x, lane = tid & 31, T = p.T, C = p.C, E = p.E, k = p.k;
+  const int S = p.S, n = T * C;
+  const size_t stride = (size_t)T * C;
+
+  // ---- logits: G lanes per logit (G a power of two <= 32)
+  int G = 32;
+  while (G > 1 && n * G > kTailThreads) G >>= 1;
+  const int per = kTailThreads / G, g = tid % G;
+  for (int li = tid / G; li < ((n + per - 1) / per) * per; li += per) {
+    float a0 = 0.f, a1 = 0.f;
+    if (li < n) {
+      int sp = g;
+      for (; sp + G < S; sp += 2 * G) {
+        a0 += __ldcg(p.part + (size_t)sp * stride + li);
+        a1 += __ldcg(p.part + (size_t)(sp + G) * stride + li);
+      }
+      if (sp < S) a0 += __ldcg(p.part + (size_t)sp * stride + li);
+    }
+    float v = a0 + a1;
+    for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (g == 0 && li < n) lg[li] = v;
+  }
+  for (int e = tid; e < kMaxExperts; e += kTailThreads) hist[e] = 0;
+  __syncthreads();
+
+  // ---- gating: warp w < G_WARPS takes tokens w, w + G_WARPS, ...
+  const int warp = tid >> 5;
+  if (warp < G_WARPS) {
+    GateParams q = p;
+    q.hist = hist;
+    for (int t = warp; t < T; t += G_WARPS)
+      gate_token(q, t, lg + (size_t)t * C, lrow[warp], exact_s[warp]);
+  }
+  __syncthreads();
+
+  // ---- scan over the experts: counts, exclusive offsets, list of experts with rows
+  const bool ex = tid < kMaxExperts;
+  int cnt = 0, flag = 0;
+  if (ex && tid < E) {
+    cnt = hist[tid];
+    flag = cnt > 0;
+  }
+  if (ex) excl[tid] = cnt;
+  __syncthreads();
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    const int v = (ex && tid >= o) ? excl[tid - o] : 0;
+    __syncthreads();
+    if (ex) excl[tid] += v;
+    __syncthreads();
+  }
+  const int incl = ex ? excl[tid] : 0;
+  __syncthreads();
+  if (ex) {
+    excl[tid] = incl - cnt;
+    hist[tid] = flag;
+  }
+  __syncthreads();
+  for (int o = 1; o < kMaxExperts; o <<= 1) {
+    const int v = (ex && tid >= o) ? hist[tid - o] : 0;
+    __syncthreads();
+    if (ex) hist[tid] += v;   // inclusive count of experts with rows
+    __syncthreads();
+  }
+  if (tid < E) {
+    counts[tid] = cnt;
+    offsets[tid] = excl[tid];
+    if (tid == E - 1) {
+      offsets[E] = excl[tid] + cnt;
+      *n_active = hist[tid];
+    }
+    if (flag) active[hist[tid] - 1] = tid;
+  }
+  if (tid == 0 && shared_meta) {
+    shared_meta[0] = 0;
+    shared_meta[1] = T;
+    shared_meta[2] = 0;
+    shared_meta[3] = 1;
+  }
+  // ---- stable ranks: pair i = t*k + j goes after every earlier pair routed to its expert
+  if (tid < T * k) {
+    const int e = p.ids[tid];
+    int rank = 0;
+    for (int i = 0; i < tid; ++i) rank += p.ids[i] == e;
+    const int pp = excl[e] + rank;
+    pos[tid] = pp;
+    src[pp] = tid;
+    srow[pp] = tid / k;
+  }
+  __syncthreads();
+  if (x_perm) {
+    const int nvec = p.H / 8;
+    for (int i = tid; i < T * k * nvec; i += kTailThreads) {
+      const int r = i / nvec, v = i % nvec;
+      reinterpret_cast<uint4*>(x_perm + (size_t)r * p.H)[v] =
+          __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)srow[r] * p.H) + v);
+    }
+  }
+  (void)lane;
+}
+
 // ------------------------------------------------------------------------------ host side
 RoutePlan plan_route(int T, int H, int E, int k, bool has_gate) {
   RoutePlan r{};
@@ -603,6 +732,7 @@ RoutePlan plan_route(int T, int H, int E, int k, bool has_gate) {
   if (tiles < target) S = std::min(std::max(1, H / R_KH), ceil_div(target, std::max(tiles, 1)));
   r.h_per_split = round_up(ceil_div(H, S), R_KH);
   r.S = ceil_div(H, r.h_per_split);
+  r.small = T >= 1 && T <= kSmallT;   // everything after the router product in one CTA
   return r;
 }
 
@@ -643,6 +773,21 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
                                                 r.h_per_split, s.part, s.hist, r.ntiles * a.E);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
+    }
+    if (r.small) {
+      GateParams p{};
+      p.part = s.part; p.S = r.S; p.C = r.C;
+      p.x = a.x; p.w_r = a.w_r; p.w_rT = nullptr; p.logit_bias = a.logit_bias;
+      p.sel_bias = a.sel_bias; p.forced = a.forced; p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k;
+      p.mode = a.gating; p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
+      p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = nullptr;
+      p.tok_per_warp = 1;
+      route_tail_kernel<<<1, kTailThreads, 0, st>>>(p, a.counts, a.offsets, a.pos, a.src,
+                                                    s.active, s.n_active, s.shared_meta,
+                                                    a.x_perm);
+      MOE_COUNT_LAUNCH();
+      MOE_LAUNCH_CHECK();
+      return MOE_OK;
     }
     int S_gate = r.S;
     if (r.S > 4) {

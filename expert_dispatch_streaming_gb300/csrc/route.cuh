@@ -36,10 +36,13 @@ struct RoutePlan {
   int ntiles;       // 128-token dispatch tiles
   int tc;           // 1: router product on the tensor cores (bf16 x 3 pieces), S = 1
   int Mpad;         // rows of the tensor-core router image (C rounded up to 128)
+  int small;        // 1: gating, scan, ranks and row copy in one CTA (T <= kSmallT)
 };
 
 // batches of at least this many tokens compute the router product on the tensor cores
 constexpr int kTcRouterMinT = 256;
+// batches of at most this many tokens run everything after the router product in one CTA
+constexpr int kSmallT = 16;
 // batches of at least this many tokens gather x_perm in a separate, GPU-wide kernel
 constexpr int kSeparateGatherMinT = 1024;
 // ... and so do batches whose permuted rows exceed this many bytes (one CTA per 128-token tile

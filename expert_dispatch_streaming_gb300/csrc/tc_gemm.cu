@@ -788,7 +788,6 @@ int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters
   TcParams kp{};
   const int r = fill_params(kp, a, t, part, counters, err);
   if (r != MOE_OK) return r;
-  MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, t.counter_elems * sizeof(int32_t), st));
   return a.int4 ? dispatch_bn<true>(a.fused, t.BN, kp, st) : dispatch_bn<false>(a.fused, t.BN, kp, st);
 }
 
@@ -850,7 +849,6 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
     kp.out2 = a2.out;
     kp.part2 = part2;
   }
-  MOE_CUDA_TRY(cudaMemsetAsync(counters, 0, pp.t1.counter_elems * sizeof(int32_t), st));
   return a1.int4 ? dispatch_bn<true>(a1.fused, pp.t1.BN, kp, st)
                  : dispatch_bn<false>(a1.fused, pp.t1.BN, kp, st);
 }

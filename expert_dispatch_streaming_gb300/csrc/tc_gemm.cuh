@@ -37,6 +37,9 @@ struct TcParams {
 
 using TcPlan = TcPlanLite;
 
+// The launches below expect `counters` (split-K arrival counters) to be zero; every launch
+// leaves the counters it used at zero again, so one memset before a sequence of launches
+// sharing the array suffices.
 bool tc_supported(const GemmArgs& a);
 TcPlan plan_tc(const GemmArgs& a);
 int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters, int32_t* err,
