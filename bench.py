@@ -12,6 +12,7 @@ Prints ONE JSON line (rank 0).  See the design notes for the roofline arithmetic
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import subprocess
@@ -27,6 +28,7 @@ sys.path.insert(0, ROOT)
 import workloads as wl  # noqa: E402
 
 WORKLOADS = {"mixtral": wl.MIXTRAL, "qwen": wl.QWEN, "deepseek": wl.DEEPSEEK}
+CANONICAL_E = {name: c.E for name, c in WORKLOADS.items()}   # before any --experts override
 WORKLOAD_NAMES = {"mixtral": "Mixtral-8x7B-shaped", "qwen": "Qwen1.5-MoE-A2.7B-shaped",
                   "deepseek": "DeepSeek-V3-shaped INT4"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -102,19 +104,59 @@ class ClockSampler:
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(self.rows)}
 
 
-def layer_work(cfg, T, n_unique):
-    """Algorithmic FLOPs and bytes of one layer call and of its two expert GEMMs."""
-    H, I, k, E = cfg.H, cfg.I, cfg.k, cfg.E
+def layer_work(cfg, T, n_unique, shared_merged=False):
+    """Algorithmic FLOPs and bytes of one layer call and of its two expert GEMM launches (which
+    include the shared expert when the library runs it inside the routed launches)."""
+    H, I, k, E, Is = cfg.H, cfg.I, cfg.k, cfg.E, cfg.Is
     rows = T * k
     bpw = 2.0 if cfg.wdtype == "bf16" else 0.5 + 2.0 / 128
     gu_flops = 2.0 * rows * H * 2 * I
     dn_flops = 2.0 * rows * I * H
     gu_bytes = n_unique * 2 * I * H * bpw + rows * H * 2 + rows * I * 2
     dn_bytes = n_unique * H * I * bpw + rows * I * 2 + rows * H * 2
-    flops = gu_flops + dn_flops + 2.0 * T * H * E + 6.0 * T * H * cfg.Is
-    nbytes = (n_unique * 3 * H * I * bpw + 3 * H * cfg.Is * bpw + 4.0 * H * E + 2 * T * H * 2
+    flops = gu_flops + dn_flops + 2.0 * T * H * E + 6.0 * T * H * Is
+    nbytes = (n_unique * 3 * H * I * bpw + 3 * H * Is * bpw + 4.0 * H * E + 2 * T * H * 2
               + 2 * 2 * rows * H * 2)
+    if shared_merged and Is:
+        gu_flops += 2.0 * T * H * 2 * Is
+        dn_flops += 2.0 * T * Is * H
+        gu_bytes += 2 * Is * H * bpw + T * H * 2 + T * Is * 2
+        dn_bytes += Is * H * bpw + T * Is * 2 + T * H * 2
     return dict(flops=flops, bytes=nbytes, gu=(gu_flops, gu_bytes), dn=(dn_flops, dn_bytes))
+
+
+KERNEL_SOURCES = ["expert_dispatch_streaming_gb300/csrc/tc_gemm.cu",
+                  "expert_dispatch_streaming_gb300/csrc/common.cuh"]
+PROFILE_FILES = {("mixtral", 4096, "gate_up_gemm"): "tc_gemm_gate_up_mixtral_T4096.md",
+                 ("mixtral", 4096, "down_gemm"): "tc_gemm_down_mixtral_T4096.md",
+                 ("qwen", 8192, "gate_up_gemm"): "tc_gemm_gate_up_qwen_T8192.md"}
+
+
+def profiled_traffic(workload, T, E, kernel):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary of the
+    same workload, or None when there is none or the kernel sources changed since it was taken
+    (the summary records the sources' sha256)."""
+    name = PROFILE_FILES.get((workload, T, kernel))
+    if name is None or E != CANONICAL_E[workload]:
+        return None
+    path = os.path.join(ROOT, "profiles", name)
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            key, val = line.strip().split(":", 1)
+            fields[key.strip()] = val.strip()
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    if fields.get("kernel_source_sha256") != h.hexdigest():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
 
 
 def roofline_of(flops, nbytes, seconds, pk, sustained=False):
@@ -182,11 +224,13 @@ def run_ours(args, rank, world, local_rank):
         t0 = torch.cuda.Event(enable_timing=True)
         t1 = torch.cuda.Event(enable_timing=True)
         launches = 0
+        merged = False
         with ClockSampler(local_rank) as clk:
             t0.record(stream)
             for i in range(steps):
                 _, st = layer.forward(x, ws, out, stream=stream, phase_events=evs[i])
                 launches += st.n_launches
+                merged = bool(st.shared_merged)
             t1.record(stream)
             stream.synchronize()
         torch.cuda.synchronize()
@@ -196,7 +240,7 @@ def run_ours(args, rank, world, local_rank):
         ph = np.array([[evs[i][j].elapsed_time(evs[i][j + 1]) for j in range(5)]
                        for i in range(steps)])
         res = dict(T=T, ms_per_step=ms / steps, tokens_per_s=job_throughput(T * steps, world, ms / 1e3),
-                   n_unique=n_unique, phase_ms=ph.mean(0).tolist(), launches=launches,
+                   n_unique=n_unique, phase_ms=ph.mean(0).tolist(), launches=launches, merged=merged,
                    clocks=clk.summary(), mode="eager")
         if args.graph:
             # the same call captured once in a CUDA graph (a resident-layer call is fully
@@ -269,7 +313,7 @@ def run_ours(args, rank, world, local_rank):
             if T == args.T:
                 continue
             r = measure(T, max(5, min(args.steps, 20)), 3, False)
-            w = layer_work(cfg, T, r["n_unique"])
+            w = layer_work(cfg, T, r["n_unique"], r["merged"])
             sw = {"tokens_per_s": round(r["tokens_per_s"], 1), "ms_per_step": round(r["ms_per_step"], 4),
                   "mode": r["mode"], "eager_ms_per_step": round(r.get("eager_ms_per_step", r["ms_per_step"]), 4),
                   "n_unique": r["n_unique"], "phase_ms": [round(v, 4) for v in r["phase_ms"]],
@@ -278,13 +322,15 @@ def run_ours(args, rank, world, local_rank):
             sw["gate_up_roofline"] = roofline_of(*w["gu"], gu_ms / 1e3, pk)
             sweep[str(T)] = sw
 
-    w = layer_work(cfg, args.T, head["n_unique"])
+    w = layer_work(cfg, args.T, head["n_unique"], head["merged"])
     names = ["route+dispatch+gather", "shared_expert", "gate_up_gemm", "down_gemm", "combine"]
     share = np.array(head["phase_ms"]) / max(sum(head["phase_ms"]), 1e-9)
     dom = 2 if share[2] >= share[3] else 3      # the dominant expert-FFN kernel
     dom_work = {2: w["gu"], 3: w["dn"]}.get(dom, (w["flops"], w["bytes"]))
     roof = roofline_of(*dom_work, head["phase_ms"][dom] / 1e3, pk)
-    roof.update({"kernel": names[dom], "traffic": None, "peak_source": pk["source"],
+    roof.update({"kernel": names[dom],
+                 "traffic": profiled_traffic(args.workload, args.T, cfg.E, names[dom]),
+                 "peak_source": pk["source"],
                  "share_of_step": round(float(share[dom]), 4)})
     result = {
         "metric": f"MoE-layer tokens/s ({WORKLOAD_NAMES[args.workload]} layer)",

@@ -85,7 +85,7 @@ MOE_N_PHASE_EVENTS = 6
 
 class moe_layer_stats(C.Structure):
     _fields_ = [("n_unique", C.c_int32), ("n_missed", C.c_int32), ("n_launches", C.c_int32),
-                ("reserved", C.c_int32), ("phase_events", C.POINTER(C.c_void_p))]
+                ("shared_merged", C.c_int32), ("phase_events", C.POINTER(C.c_void_p))]
 
 
 # ----------------------------------------------------------------------------- loading

@@ -433,6 +433,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
     for (int e = 0; e < L->E; ++e) tab.p[e] = L->bundles[e];
     if (P.merged) {
       // phase 2 (shared expert) is empty: the shared expert runs inside the routed launches
+      if (st) st->shared_merged = 1;
       if ((r = phase(2)) != MOE_OK) return r;
       if ((r = run_ffn_merged(L, P, s, tab, x, T, s0,
                               pev ? [&] { return phase(3); } : std::function<int()>())) != MOE_OK)

@@ -351,7 +351,9 @@ typedef struct moe_layer_stats {
   int32_t n_unique;          /* out: distinct experts used (cache path; 0 otherwise)      */
   int32_t n_missed;          /* out: cache misses (0 without a cache)                     */
   int32_t n_launches;        /* out: CUDA kernels this call launched                      */
-  int32_t reserved;
+  int32_t shared_merged;     /* out: 1 if the shared expert ran inside the routed GEMM
+                                launches (phase [2] is then empty and phases [3] / [4]
+                                include it), else 0                                      */
   /* in: NULL, or a host array of MOE_N_PHASE_EVENTS cudaEvent_t handles created by the
    * caller; the call records them on `stream` at phase boundaries:
    *   [0] start  [1] routing + dispatch + gather done  [2] shared expert done
