@@ -195,6 +195,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     moe.set_ffn_kernel(args.ffn_kernel)
+    moe.set_pdl(args.pdl)
     cfg = WORKLOADS[args.workload]
     pk = peaks()
     layer = syn.DeviceLayer(cfg, device=dev)
@@ -249,11 +250,17 @@ def run_ours(args, rank, world, local_rank):
             for ev in gevs:
                 ev.record(stream)
             stream.synchronize()
+            # the timed graph has no phase events (event nodes between the kernels would cut the
+            # programmatic launch edges between them); a second graph with events gives the split
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
+                layer.forward(x, ws, out, stream=stream)
+            gp = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gp, stream=stream):
                 layer.forward(x, ws, out, stream=stream, phase_events=gevs)
             for _ in range(warmup):
                 g.replay()
+                gp.replay()
             torch.cuda.synchronize()
             if world > 1:
                 torch.distributed.barrier()
@@ -268,7 +275,7 @@ def run_ours(args, rank, world, local_rank):
             gms = max_over_ranks(t0.elapsed_time(t1), world, dev)
             # phase split of one replay (events inside the graph are re-recorded per replay)
             with torch.cuda.stream(stream):
-                g.replay()
+                gp.replay()
             stream.synchronize()
             gph = [gevs[j].elapsed_time(gevs[j + 1]) for j in range(5)]
             res["graph"] = dict(ms_per_step=gms / steps,
@@ -278,7 +285,7 @@ def run_ours(args, rank, world, local_rank):
                 res.update(ms_per_step=gms / steps, tokens_per_s=T * steps * world / (gms / 1e3),
                            phase_ms=gph, clocks=gclk.summary(), mode="cuda_graph")
             res["eager_ms_per_step"] = ms / steps
-            del g
+            del g, gp
         if with_e2e:
             xh = torch.from_numpy(xb.view(np.int16)).pin_memory()
             oh = torch.empty_like(xh).pin_memory()
@@ -535,6 +542,8 @@ def main():
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
     ap.add_argument("--ffn-kernel", default="auto", choices=["auto", "stream", "tcgen05"])
+    ap.add_argument("--pdl", action="store_true",
+                    help="launch the layer's kernels with programmatic dependent launch")
     ap.add_argument("--no-streamed", dest="streamed", action="store_false")
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--stream-steps", type=int, default=wl.STREAM_STEPS)

@@ -179,6 +179,7 @@ def _check(status, fn):
 
 # ----------------------------------------------------------------------------- API
 MOE_OPT_FFN_KERNEL = 1
+MOE_OPT_PDL = 2
 FFN_KERNEL = {"auto": 0, "stream": 1, "tcgen05": 2}
 
 
@@ -189,6 +190,11 @@ def moe_set_option(option, value) -> None:
 def set_ffn_kernel(name: str) -> None:
     """'auto' | 'stream' (mma.sync weight streaming) | 'tcgen05' (tensor-core kernel)."""
     moe_set_option(MOE_OPT_FFN_KERNEL, FFN_KERNEL[name])
+
+
+def set_pdl(on: bool) -> None:
+    """Programmatic dependent launch of the layer's kernels (default off)."""
+    moe_set_option(MOE_OPT_PDL, 1 if on else 0)
 
 
 def moe_workspace_error(ws, stream=None) -> int:

@@ -15,6 +15,7 @@
 namespace moe {
 
 static thread_local int g_last_cuda = 0;
+int g_use_pdl = 0;
 thread_local long long g_launches = 0;
 
 void set_cuda_error(cudaError_t e) { g_last_cuda = (int)e; }
@@ -231,6 +232,11 @@ int moe_set_option(int option, int value) {
   if (option == MOE_OPT_FFN_KERNEL) {
     if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
     g_ffn_path = value;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_PDL) {
+    if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+    g_use_pdl = value;
     return MOE_OK;
   }
   return MOE_ERR_INVALID_ARG;

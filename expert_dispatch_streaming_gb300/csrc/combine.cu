@@ -20,6 +20,8 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ pos,
                const float* __restrict__ w, int T, int k, int H,
                const uint16_t* __restrict__ shared, const float* __restrict__ shared_gate,
                const uint16_t* __restrict__ residual, uint16_t* __restrict__ out) {
+  pdl_trigger();
+  pdl_wait();
   const int v = blockIdx.x * kCombineThreads + threadIdx.x;
   if (v >= H / 8) return;
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
@@ -80,8 +82,8 @@ int launch_combine(const uint16_t* y, const int32_t* pos, const float* w, int T,
                    uint16_t* out, cudaStream_t st) {
   if (T <= 0) return MOE_OK;
   dim3 grid(ceil_div(H / 8, kCombineThreads), std::min(T, 65535));
-  combine_kernel<<<grid, kCombineThreads, 0, st>>>(y, pos, w, T, k, H, shared, shared_gate,
-                                                   residual, out);
+  MOE_LAUNCH_PDL(combine_kernel, grid, dim3(kCombineThreads), 0, st, y, pos, w, T, k, H, shared,
+                 shared_gate, residual, out);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;

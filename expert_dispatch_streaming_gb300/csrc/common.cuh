@@ -6,6 +6,8 @@
 #include <stdint.h>
 #include <stddef.h>
 
+#include <utility>
+
 #include "../../include/moe.h"
 
 namespace moe {
@@ -46,6 +48,37 @@ struct WsCursor {
 };
 
 int sm_count();
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// With MOE_OPT_PDL set, the kernels of the layer are launched with programmatic stream
+// serialization (otherwise launch_pdl is a plain launch): a kernel may be
+// scheduled while its predecessor in the stream still runs (once every CTA of the predecessor
+// has called pdl_trigger), does its own setup, and calls pdl_wait before its first access to
+// memory that earlier work writes or reads.  griddepcontrol.wait returns once the predecessor
+// grid has completed and its writes are visible; it is a no-op for a kernel launched without a
+// programmatic predecessor (after a memset, a copy, or another library's kernel).
+extern int g_use_pdl;   // MOE_OPT_PDL
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = g_use_pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#define MOE_LAUNCH_PDL(kernel, grid, block, smem, st, ...) \
+  MOE_CUDA_TRY(::moe::launch_pdl(kernel, grid, block, smem, st, __VA_ARGS__))
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 // kernels launched by this thread (the layer forward reports the difference)
 extern thread_local long long g_launches;
 #define MOE_COUNT_LAUNCH() (++::moe::g_launches)

@@ -71,6 +71,8 @@ __device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
 
 template <bool INT4, bool FUSED, int NT, int U>
 __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant__ GemmKParams p) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NR = FUSED ? 4 : 2;   // weight rows per thread: g, g+8 (gate), g, g+8 (up)
   constexpr int VPR = INT4 ? 1 : 4;   // 16-byte vectors per row per 128-block
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, tq = lane & 3;
@@ -261,12 +263,12 @@ size_t gemm_scratch(WsCursor& c, const GemmPlan& g, float** part, int32_t** coun
 }
 
 template <bool INT4, bool FUSED, int U>
-static void launch_nt(int nt, dim3 grid, const GemmKParams& kp, cudaStream_t st) {
+static cudaError_t launch_nt(int nt, dim3 grid, const GemmKParams& kp, cudaStream_t st) {
   switch (nt) {
-    case 1: expert_gemm_kernel<INT4, FUSED, 1, U><<<grid, 128, 0, st>>>(kp); break;
-    case 2: expert_gemm_kernel<INT4, FUSED, 2, U><<<grid, 128, 0, st>>>(kp); break;
-    case 4: expert_gemm_kernel<INT4, FUSED, 4, U><<<grid, 128, 0, st>>>(kp); break;
-    default: expert_gemm_kernel<INT4, FUSED, 8, U><<<grid, 128, 0, st>>>(kp); break;
+    case 1: return launch_pdl(expert_gemm_kernel<INT4, FUSED, 1, U>, grid, dim3(128), 0, st, kp);
+    case 2: return launch_pdl(expert_gemm_kernel<INT4, FUSED, 2, U>, grid, dim3(128), 0, st, kp);
+    case 4: return launch_pdl(expert_gemm_kernel<INT4, FUSED, 4, U>, grid, dim3(128), 0, st, kp);
+    default: return launch_pdl(expert_gemm_kernel<INT4, FUSED, 8, U>, grid, dim3(128), 0, st, kp);
   }
 }
 
@@ -285,11 +287,11 @@ int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* coun
   if (a.host_n == 0) return MOE_OK;
   dim3 grid(g.A_max * g.m_blocks * g.splits);
   if (a.int4) {
-    if (a.fused) launch_nt<true, true, 2>(g.nt, grid, kp, st);
-    else launch_nt<true, false, 4>(g.nt, grid, kp, st);
+    if (a.fused) MOE_CUDA_TRY((launch_nt<true, true, 2>(g.nt, grid, kp, st)));
+    else MOE_CUDA_TRY((launch_nt<true, false, 4>(g.nt, grid, kp, st)));
   } else {
-    if (a.fused) launch_nt<false, true, 1>(g.nt, grid, kp, st);
-    else launch_nt<false, false, 2>(g.nt, grid, kp, st);
+    if (a.fused) MOE_CUDA_TRY((launch_nt<false, true, 1>(g.nt, grid, kp, st)));
+    else MOE_CUDA_TRY((launch_nt<false, false, 2>(g.nt, grid, kp, st)));
   }
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();

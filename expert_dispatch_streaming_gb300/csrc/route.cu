@@ -43,6 +43,8 @@ router_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ 
                       const uint16_t* __restrict__ w_gate, int T, int H, int E, int C,
                       int h_per_split, float* __restrict__ part, int32_t* __restrict__ hist,
                       int hist_n) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float xs[R_KH][R_BT + 1];
   __shared__ float wsm[R_KH][R_BC];
   const int tid = threadIdx.x;
@@ -104,6 +106,8 @@ router_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ 
 // one value per logit instead of S.
 __global__ void __launch_bounds__(256)
 reduce_slices_kernel(float* __restrict__ part, int S, int n) {
+  pdl_trigger();
+  pdl_wait();
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= n) return;
   float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -231,6 +235,8 @@ __global__ void __launch_bounds__(256)
 router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w_gate, int H,
                    int E, int Mpad, int T, uint16_t* __restrict__ img, float* __restrict__ w_rT,
                    int32_t* __restrict__ hist, int hist_n, int32_t* __restrict__ meta) {
+  pdl_trigger();
+  pdl_wait();
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < hist_n; i += blockDim.x) hist[i] = 0;
     if (threadIdx.x == 0) { meta[0] = 0; meta[1] = T; meta[2] = 0; meta[3] = 1; }
@@ -487,6 +493,8 @@ __device__ void gate_token(const GateParams& p, int t, const float* raw, float* 
 }
 
 __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float lrow[G_WARPS][kMaxExperts];
   __shared__ double exact_s[G_WARPS][kMaxExperts];
   const int warp = threadIdx.x >> 5;
@@ -503,6 +511,8 @@ scan_kernel(const int32_t* __restrict__ hist, int ntiles, int E, int32_t* __rest
             int32_t* __restrict__ offsets, int32_t* __restrict__ base,
             int32_t* __restrict__ active, int32_t* __restrict__ n_active,
             int32_t* __restrict__ shared_meta, int T) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int s_cnt[kMaxExperts], s_flag[kMaxExperts];
   const int e = threadIdx.x;
   if (shared_meta && e == 0) {
@@ -549,6 +559,8 @@ rank_permute_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__
                     int k, int E, int H, const uint16_t* __restrict__ x,
                     int32_t* __restrict__ pos, int32_t* __restrict__ src,
                     uint16_t* __restrict__ x_perm) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ uint32_t mask[kMaxExperts][kTileT / 32];
   __shared__ int ptmp[kTileT * kMaxK];
   const int tile = blockIdx.x, t0 = tile * kTileT, tid = threadIdx.x;
@@ -587,6 +599,8 @@ rank_permute_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src, int rows,
                    int k, int H, uint16_t* __restrict__ x_perm) {
+  pdl_trigger();
+  pdl_wait();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const int nvec = H / 8;
@@ -607,6 +621,8 @@ route_tail_kernel(GateParams p, int32_t* __restrict__ counts, int32_t* __restric
                   int32_t* __restrict__ pos, int32_t* __restrict__ src,
                   int32_t* __restrict__ active, int32_t* __restrict__ n_active,
                   int32_t* __restrict__ shared_meta, uint16_t* __restrict__ x_perm) {
+  pdl_trigger();
+  pdl_wait();
   static_assert(kTailThreads >= kMaxExperts, "the scan takes one thread per expert");
   __shared__ float lg[kSmallT * (kMaxExperts + 1)];   // summed router outputs of all tokens
   __shared__ float lrow[G_WARPS][kMaxExperts];
@@ -759,9 +775,9 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
   if (a.T > 0) {
     if (r.tc) {
       const size_t thr = (size_t)r.Mpad * (a.H / 8);
-      router_prep_kernel<<<(unsigned)ceil_div((int)thr, 256), 256, 0, st>>>(
-          a.w_r, a.w_gate, a.H, a.E, r.Mpad, a.T, s.img, s.w_rT, s.hist, r.ntiles * a.E,
-          s.shared_meta);
+      MOE_LAUNCH_PDL(router_prep_kernel, dim3((unsigned)ceil_div((int)thr, 256)), dim3(256), 0, st,
+                     a.w_r, a.w_gate, a.H, a.E, r.Mpad, a.T, s.img, s.w_rT, s.hist,
+                     r.ntiles * a.E, s.shared_meta);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
       const int rr = launch_tc_router(a.x, a.T, a.H, s.img, r.Mpad, r.C, s.shared_meta, s.part,
@@ -769,8 +785,8 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
       if (rr != MOE_OK) return rr;
     } else {
       dim3 g1(ceil_div(a.T, R_BT), ceil_div(r.C, R_BC), r.S);
-      router_partial_kernel<<<g1, 256, 0, st>>>(a.x, a.w_r, a.w_gate, a.T, a.H, a.E, r.C,
-                                                r.h_per_split, s.part, s.hist, r.ntiles * a.E);
+      MOE_LAUNCH_PDL(router_partial_kernel, g1, dim3(256), 0, st, a.x, a.w_r, a.w_gate, a.T, a.H,
+                     a.E, r.C, r.h_per_split, s.part, s.hist, r.ntiles * a.E);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
     }
@@ -782,9 +798,8 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
       p.mode = a.gating; p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
       p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = nullptr;
       p.tok_per_warp = 1;
-      route_tail_kernel<<<1, kTailThreads, 0, st>>>(p, a.counts, a.offsets, a.pos, a.src,
-                                                    s.active, s.n_active, s.shared_meta,
-                                                    a.x_perm);
+      MOE_LAUNCH_PDL(route_tail_kernel, dim3(1), dim3(kTailThreads), 0, st, p, a.counts,
+                     a.offsets, a.pos, a.src, s.active, s.n_active, s.shared_meta, a.x_perm);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
       return MOE_OK;
@@ -792,7 +807,8 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     int S_gate = r.S;
     if (r.S > 4) {
       const int n = a.T * r.C;
-      reduce_slices_kernel<<<ceil_div(n, 256), 256, 0, st>>>(s.part, r.S, n);
+      MOE_LAUNCH_PDL(reduce_slices_kernel, dim3(ceil_div(n, 256)), dim3(256), 0, st, s.part, r.S,
+                     n);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
       S_gate = 1;
@@ -806,12 +822,12 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     // small batches: one token per warp (more CTAs); large: four, to amortise the CTA
     p.tok_per_warp = a.T <= 1024 ? 1 : 4;
     const int per_cta = G_WARPS * p.tok_per_warp;
-    gate_topk_kernel<<<ceil_div(a.T, per_cta), G_WARPS * 32, 0, st>>>(p);
+    MOE_LAUNCH_PDL(gate_topk_kernel, dim3(ceil_div(a.T, per_cta)), dim3(G_WARPS * 32), 0, st, p);
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
   }
-  scan_kernel<<<1, kMaxExperts, 0, st>>>(s.hist, r.ntiles, a.E, a.counts, a.offsets, s.base,
-                                         s.active, s.n_active, s.shared_meta, a.T);
+  MOE_LAUNCH_PDL(scan_kernel, dim3(1), dim3(kMaxExperts), 0, st, s.hist, r.ntiles, a.E,
+                 a.counts, a.offsets, s.base, s.active, s.n_active, s.shared_meta, a.T);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   if (a.T > 0) {
@@ -819,8 +835,9 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     // one warp per destination row over the whole GPU (the per-tile grid is too small)
     const bool fused_copy =
         a.x_perm && (size_t)a.T * a.k * a.H * 2 <= kFusedGatherMaxBytes && a.T < kSeparateGatherMinT;
-    rank_permute_kernel<<<r.ntiles, 256, 0, st>>>(a.ids, s.base, a.T, a.k, a.E, a.H, a.x,
-                                                  a.pos, a.src, fused_copy ? a.x_perm : nullptr);
+    MOE_LAUNCH_PDL(rank_permute_kernel, dim3(r.ntiles), dim3(256), 0, st, a.ids, s.base, a.T,
+                   a.k, a.E, a.H, a.x, a.pos, a.src,
+                   fused_copy ? a.x_perm : static_cast<uint16_t*>(nullptr));
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
     if (a.x_perm && !fused_copy) {
@@ -834,7 +851,8 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
 int launch_gather(const uint16_t* x, const int32_t* src, int rows, int k, int H,
                   uint16_t* x_perm, cudaStream_t st) {
   if (rows <= 0) return MOE_OK;
-  gather_rows_kernel<<<ceil_div(rows * 32, 256), 256, 0, st>>>(x, src, rows, k, H, x_perm);
+  MOE_LAUNCH_PDL(gather_rows_kernel, dim3(ceil_div(rows * 32, 256)), dim3(256), 0, st, x, src,
+                 rows, k, H, x_perm);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;

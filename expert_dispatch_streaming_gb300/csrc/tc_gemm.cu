@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int MT = p.M / 128;
-  const int n_act = p.host_n >= 0 ? p.host_n : *p.n_active;
+  pdl_trigger();
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < 8; ++s) {
@@ -355,6 +355,10 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
                  "r"(C::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  // everything above touches no memory that earlier kernels write; from here on the routing
+  // results (offsets, expert list) and the token rows are read
+  pdl_wait();
+  const int n_act = p.host_n >= 0 ? p.host_n : *p.n_active;
   if (warp == 2) {
     // prefix of unit counts over the experts with rows
     int carry = 0;
@@ -669,7 +673,8 @@ int launch_bn(TcParams& kp, cudaStream_t st) {
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr = true;
   }
-  tc_gemm_kernel<BN, FUSED, INT4, ROUTER><<<sm_count(), C::THREADS, C::SMEM, st>>>(kp);
+  MOE_LAUNCH_PDL(tc_gemm_kernel<BN, FUSED, INT4, ROUTER>, dim3(sm_count()), dim3(C::THREADS),
+                 C::SMEM, st, kp);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;

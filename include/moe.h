@@ -64,8 +64,12 @@ int moe_version(void);
  *  MOE_OPT_FFN_KERNEL: which expert-FFN kernel runs: 0 = automatic (default: the tensor-core
  *    tcgen05 kernel wherever it supports the weight type, else the mma.sync weight-streaming
  *    kernel), 1 = always the streaming kernel, 2 = tcgen05 wherever supported.  Both compute
- *    the same layer; tests use the option to cover both. */
-enum moe_option { MOE_OPT_FFN_KERNEL = 1 };
+ *    the same layer; tests use the option to cover both.
+ *  MOE_OPT_PDL: 1 = launch the layer's kernels with programmatic dependent launch (a kernel
+ *    is scheduled while its predecessor finishes and waits in-kernel for its results); 0
+ *    (default) = plain stream-ordered launches, which measured as fast or faster on GB300 at
+ *    every workload tried.  Results are identical either way. */
+enum moe_option { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_PDL = 2 };
 int moe_set_option(int option, int value);
 
 /* Reads the device error word kept in the first 4 bytes of a moe_layer_forward or

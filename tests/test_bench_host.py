@@ -35,14 +35,28 @@ def test_layer_work_counts_the_shared_expert_only_when_merged(bench):
 
 
 def test_profiled_traffic_follows_the_kernel_sources(bench, tmp_path, monkeypatch):
-    # the committed summary matches the committed sources
-    assert isinstance(bench.profiled_traffic("mixtral", 4096, 8, "gate_up_gemm"), int)
+    import hashlib
+    # a repository copy with two kernel sources and one profile summary
+    srcs = []
+    for i, rel in enumerate(bench.KERNEL_SOURCES):
+        f = tmp_path / rel
+        f.parent.mkdir(parents=True, exist_ok=True)
+        f.write_text(f"// kernel source {i}\n")
+        srcs.append(f)
+    h = hashlib.sha256()
+    for f in srcs:
+        h.update(f.read_bytes())
+    prof = tmp_path / "profiles" / bench.PROFILE_FILES[("mixtral", 4096, "gate_up_gemm")]
+    prof.parent.mkdir(parents=True, exist_ok=True)
+    prof.write_text("# summary\n\n    traffic_bytes_per_launch: 123456\n"
+                    f"    kernel_source_sha256: {h.hexdigest()}\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    assert bench.profiled_traffic("mixtral", 4096, 8, "gate_up_gemm") == 123456
     # no summary for this workload / size / expert count
     assert bench.profiled_traffic("deepseek", 8192, 256, "gate_up_gemm") is None
     assert bench.profiled_traffic("mixtral", 512, 8, "gate_up_gemm") is None
     assert bench.profiled_traffic("mixtral", 4096, 4, "gate_up_gemm") is None
+    assert bench.profiled_traffic("mixtral", 4096, 8, "down_gemm") is None
     # a changed kernel source invalidates the stored counters
-    changed = tmp_path / "tc_gemm.cu"
-    changed.write_text("// changed\n")
-    monkeypatch.setattr(bench, "KERNEL_SOURCES", [str(changed)] + bench.KERNEL_SOURCES[1:])
+    srcs[0].write_text("// changed\n")
     assert bench.profiled_traffic("mixtral", 4096, 8, "gate_up_gemm") is None

@@ -123,3 +123,30 @@ def test_layer_tcgen05_int4_with_shared_expert(moe, syn, T):
     assert moe.moe_workspace_error(ws) == 0
     ref = moe_ref.layer_forward(cfg, 0, xb, forced_ids=ids.cpu().numpy())
     assert_close(syn.bits_of(out), ref["out"], f"int4 + shared T={T} tcgen05")
+
+
+@pytest.mark.parametrize("name,T", [("qwen", 1), ("qwen", 16), ("qwen", 700), ("ds", 40)])
+def test_layer_bits_identical_with_and_without_programmatic_launch(moe, syn, name, T):
+    """Programmatic dependent launch only moves when kernels are scheduled: every kernel waits
+    for its predecessor's results in-kernel, so the outputs are bit-identical to plain launches
+    (a missing wait would show up here as a race)."""
+    cfg = wl.QWEN if name == "qwen" else wl.custom(
+        "ds_pdl", cfg_id=123, H=512, E=64, k=8, I=256, gating="sigmoid_bias_renorm", scale=2.5,
+        Is=384, shared_gate="one", wdtype="int4_g128", zipf_s=1.1, bias_kind="select")
+    dl = syn.DeviceLayer(cfg)
+    xb = wl.tokens(cfg, T)
+    x = syn.to_device_bits(xb)
+    ws = dl.workspace(T)
+    outs = []
+    try:
+        for pdl in (True, False, True):
+            moe.set_pdl(pdl)
+            out, _ = dl.forward(x, ws)
+            out2, _ = dl.forward(out, ws)        # a second layer call fed by the first
+            torch.cuda.synchronize()
+            assert moe.moe_workspace_error(ws) == 0
+            outs.append((syn.bits_of(out), syn.bits_of(out2)))
+    finally:
+        moe.set_pdl(False)
+    for a, b in outs[1:]:
+        assert np.array_equal(a, outs[0][0]) and np.array_equal(b, outs[0][1])
