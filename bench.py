@@ -380,11 +380,11 @@ def run_streamed(args, local_rank):
     layers = [syn.DeviceLayer(cfg, layer=l, cached=True, device=dev) for l in range(cfg.layers)]
     setup_s = time.time() - t0
 
-    def make(cap_bytes):
+    def make(cap_bytes, prefetch=0):
         c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=cap_bytes,
                                         n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
                                         timeout_ms=20000, verify_checksums=1, device=local_rank,
-                                        time_copies=1)
+                                        time_copies=1, prefetch_next_layer=prefetch)
         return moe.moe_expert_cache_create(c)
 
     # probe: pinned H2D bandwidth of one bundle-sized copy on this machine (best of 3 rounds)
@@ -473,6 +473,31 @@ def run_streamed(args, local_rank):
         t_copy = copy_ms / 1e3
         res["overlap_fraction"] = (round(min(1.0, max(0.0, 1 - (t_stream - t_res) / t_copy)), 4)
                                    if t_copy > 0 else None)
+        # lookahead prefetch: each layer call ends by prefetching the next layer's experts,
+        # predicted from that layer's previous step (never from the trace's future)
+        pc = make(wl.STREAM_CACHE_BYTES, prefetch=1)
+        try:
+            torch.cuda.synchronize()
+            e0.record(stream)
+            run(pc, args.stream_steps)
+            e1.record(stream)
+            stream.synchronize()
+            t_pf = e0.elapsed_time(e1) / 1e3
+            sp = moe.moe_expert_cache_stats(pc)
+            pcopy_ms, _ = moe.moe_expert_cache_copy_time(pc)
+        finally:
+            moe.moe_expert_cache_destroy(pc)
+        res["prefetch"] = {
+            "tokens_per_s": round(T * args.stream_steps / t_pf, 1),
+            "ms_per_step": round(1e3 * t_pf / args.stream_steps, 3),
+            "hit_rate": round(sp["hits"] / max(1, sp["hits"] + sp["misses"]), 4),
+            "demand_misses": sp["misses"], "prefetch_fills": sp["prefetch_fills"],
+            "prefetch_used": sp["prefetch_used"],
+            "prefetch_accuracy": round(sp["prefetch_used"] / max(1, sp["prefetch_fills"]), 4),
+            "bytes_h2d": sp["bytes_h2d"],
+            "h2d_gbs": round(sp["bytes_h2d"] / max(pcopy_ms, 1e-9) / 1e6, 1),
+            "overlap_fraction": (round(min(1.0, max(0.0, 1 - (t_pf - t_res) / (pcopy_ms / 1e3))), 4)
+                                 if pcopy_ms > 0 else None)}
         out["T"][str(T)] = res
         if T == 8 and args.capacity_sweep:
             # hit rate and throughput against the slot budget (the LRU thrash cliff): from

@@ -56,19 +56,21 @@ class moe_expert_cache_config(C.Structure):
     _fields_ = [("slot_bytes", C.c_size_t), ("capacity_bytes", C.c_size_t),
                 ("n_layers", C.c_int), ("n_experts", C.c_int),
                 ("bundles", C.POINTER(moe_host_bundle)), ("timeout_ms", C.c_int),
-                ("verify_checksums", C.c_int), ("device", C.c_int), ("time_copies", C.c_int)]
+                ("verify_checksums", C.c_int), ("device", C.c_int), ("time_copies", C.c_int),
+                ("prefetch_next_layer", C.c_int)]
 
 
 class moe_cache_event(C.Structure):
     _fields_ = [("request", C.c_int64), ("layer", C.c_int32), ("expert", C.c_int32),
                 ("miss", C.c_int32), ("victim_layer", C.c_int32),
-                ("victim_expert", C.c_int32), ("slot", C.c_int32)]
+                ("victim_expert", C.c_int32), ("slot", C.c_int32), ("prefetch", C.c_int32)]
 
 
 class moe_cache_stats(C.Structure):
     _fields_ = [("requests", C.c_int64), ("hits", C.c_int64), ("misses", C.c_int64),
                 ("evictions", C.c_int64), ("bytes_h2d", C.c_int64), ("n_slots", C.c_int32),
-                ("resident", C.c_int32)]
+                ("resident", C.c_int32), ("prefetch_requests", C.c_int64),
+                ("prefetch_fills", C.c_int64), ("prefetch_used", C.c_int64)]
 
 
 class moe_layer(C.Structure):
@@ -125,6 +127,7 @@ _SIGS = {
     "moe_expert_cache_destroy": (_i, [_vp]),
     "moe_expert_cache_request": (_i, [_vp, _i, _vp, _vp, _i, C.POINTER(_vp),
                                       C.POINTER(C.c_int32)]),
+    "moe_expert_cache_prefetch": (_i, [_vp, _i, _vp, C.POINTER(C.c_int32)]),
     "moe_expert_cache_wait_expert": (_i, [_vp, _i, _i, _vp]),
     "moe_expert_cache_release": (_i, [_vp, _i, _vp]),
     "moe_expert_cache_evict": (_i, [_vp, _i, _i]),
@@ -300,6 +303,15 @@ def moe_expert_cache_request(cache, layer, used_mask, compute=None, defer_waits=
     return [s for s in slots], nm.value
 
 
+def moe_expert_cache_prefetch(cache, layer, mask=None) -> int:
+    """Prefetch request for `layer` (mask: host uint8 array [E], or None for the layer's
+    previous expert set); returns the number of copies issued."""
+    n = C.c_int32(0)
+    _check(_lib.moe_expert_cache_prefetch(cache, layer, ptr(mask), C.byref(n)),
+           "moe_expert_cache_prefetch")
+    return n.value
+
+
 def moe_expert_cache_wait_expert(cache, layer, expert, compute=None) -> None:
     _check(_lib.moe_expert_cache_wait_expert(cache, layer, expert, stream_handle(compute)),
            "moe_expert_cache_wait_expert")
@@ -319,8 +331,8 @@ def moe_expert_cache_trace(cache) -> list[tuple]:
     _check(_lib.moe_expert_cache_trace(cache, None, 0, C.byref(n)), "moe_expert_cache_trace")
     buf = (moe_cache_event * max(1, n.value))()
     _check(_lib.moe_expert_cache_trace(cache, buf, n.value, C.byref(n)), "moe_expert_cache_trace")
-    return [(e.request, e.layer, e.expert, e.miss, e.victim_layer, e.victim_expert, e.slot)
-            for e in buf[:n.value]]
+    return [(e.request, e.layer, e.expert, e.miss, e.victim_layer, e.victim_expert, e.slot,
+             e.prefetch) for e in buf[:n.value]]
 
 
 def moe_expert_cache_reset_trace(cache) -> None:

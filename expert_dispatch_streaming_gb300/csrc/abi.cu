@@ -466,9 +466,14 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
     uint8_t used[kMaxExperts];
     for (int e = 0; e < L->E; ++e) used[e] = cache->host_counts[e] > 0;
     const void* ptrs[kMaxExperts];
-    std::vector<int> hits, misses;
-    r = cache_request_split(cache, L->layer_index, used, s0, ptrs, &hits, &misses);
+    std::vector<int> hits, misses, waits;
+    r = cache_request_split(cache, L->layer_index, used, s0, ptrs, &hits, &misses, &waits);
     if (r != MOE_OK) return r;
+    // hits on bundles a prefetch copied: wait for those copies (usually long done)
+    for (int slot : waits) {
+      MOE_CUDA_TRY(cudaStreamWaitEvent(s0, cache->ready[slot], 0));
+      cache->slot_pending[slot] = 0;
+    }
     BundleTable tab{};
     for (int e = 0; e < L->E; ++e) tab.p[e] = ptrs[e];
     if (!hits.empty() && (r = run_experts(L, P, s, tab, T, (int)hits.size(), hits.data(), s0,
@@ -496,6 +501,12 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   if (cache) {
     MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[L->layer_index], s0));
     cache->layer_done_valid[L->layer_index] = 1;
+    // lookahead: copy the next layer's predicted experts while this layer still computes
+    // (after the last-use record above, so a prefetch that evicts one of this layer's slots
+    // waits for this layer)
+    if (cache->prefetch_next &&
+        (r = cache_prefetch(cache, (L->layer_index + 1) % cache->L, nullptr, nullptr)) != MOE_OK)
+      return r;
   }
   if (ids_out)
     MOE_CUDA_TRY(cudaMemcpyAsync(ids_out, s.ids, sizeof(int32_t) * T * L->k,

@@ -85,17 +85,23 @@ static int take_slot(moe_expert_cache* c, long long req, int* vl, int* ve) {
   return -1;
 }
 
-int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cudaStream_t compute,
-                        const void** slot_ptrs, std::vector<int>* hits,
-                        std::vector<int>* misses) {
+// One request over the distinct experts of `used` (ascending): the LRU update, slot choice and
+// miss copies shared by demand requests and prefetch requests.
+static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool prefetch,
+                   const void** slot_ptrs, std::vector<int>* hits, std::vector<int>* misses,
+                   std::vector<int>* wait_slots) {
   if (!c || !used || layer < 0 || layer >= c->L) return MOE_ERR_INVALID_ARG;
   int n_used = 0;
   for (int e = 0; e < c->E; ++e) n_used += used[e] != 0;
   if (n_used > c->n_slots) return MOE_ERR_CAPACITY;
   const long long req = c->req++;
-  c->st.requests++;
+  if (prefetch) c->st.prefetch_requests++;
+  else c->st.requests++;
   std::vector<int>& ls = c->layer_slots[layer];
-  ls.clear();
+  if (!prefetch) {
+    ls.clear();
+    c->layer_last[layer].clear();
+  }
   std::vector<char> touched_slot(c->n_slots, 0);
   bool any_miss = false;
   for (int e = 0; e < c->E; ++e) {
@@ -107,6 +113,7 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
     ev.layer = layer;
     ev.expert = e;
     ev.victim_layer = ev.victim_expert = -1;
+    ev.prefetch = prefetch ? 1 : 0;
     int slot;
     auto f = c->where.find(k);
     if (f != c->where.end()) {
@@ -115,8 +122,15 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
       c->order.push_back(k);
       f->second.second = std::prev(c->order.end());
       ev.miss = 0;
-      c->st.hits++;
-      if (hits) hits->push_back(e);
+      if (!prefetch) {
+        c->st.hits++;
+        if (c->slot_prefetched[slot]) {
+          c->st.prefetch_used++;
+          c->slot_prefetched[slot] = 0;
+        }
+        if (c->slot_pending[slot] && wait_slots) wait_slots->push_back(slot);
+        if (hits) hits->push_back(e);
+      }
     } else {
       int vl, ve;
       slot = take_slot(c, req, &vl, &ve);
@@ -128,7 +142,8 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
       ev.miss = 1;
       ev.victim_layer = vl;
       ev.victim_expert = ve;
-      c->st.misses++;
+      if (prefetch) c->st.prefetch_fills++;
+      else c->st.misses++;
       c->st.bytes_h2d += (int64_t)c->slot_bytes;
       // write-after-read guard: the victim's layer must have finished reading this slot
       if (vl >= 0 && c->layer_done_valid[vl])
@@ -152,19 +167,46 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
         c->timed.push_back(tev);
       }
       MOE_CUDA_TRY(cudaEventRecord(c->ready[slot], c->copy));
+      c->slot_pending[slot] = prefetch ? 1 : 0;   // a demand miss is waited for via last_copy
+      c->slot_prefetched[slot] = prefetch ? 1 : 0;
       any_miss = true;
       if (misses) misses->push_back(e);
     }
     touched_slot[slot] = 1;
     ev.slot = slot;
-    ls.push_back(slot);
+    if (!prefetch) {
+      ls.push_back(slot);
+      c->layer_last[layer].push_back(e);
+    }
     c->trace.push_back(ev);
     if (slot_ptrs) slot_ptrs[e] = c->slab + (size_t)slot * c->slot_bytes;
   }
   if (any_miss) MOE_CUDA_TRY(cudaEventRecord(c->last_copy, c->copy));
   c->st.resident = (int32_t)c->where.size();
-  (void)compute;
   return MOE_OK;
+}
+
+int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cudaStream_t compute,
+                        const void** slot_ptrs, std::vector<int>* hits,
+                        std::vector<int>* misses, std::vector<int>* wait_slots) {
+  (void)compute;
+  return process(c, layer, used, false, slot_ptrs, hits, misses, wait_slots);
+}
+
+int cache_prefetch(moe_expert_cache* c, int layer, const uint8_t* mask, int32_t* n_filled) {
+  if (n_filled) *n_filled = 0;
+  if (!c || layer < 0 || layer >= c->L) return MOE_ERR_INVALID_ARG;
+  std::vector<uint8_t> m(c->E, 0);
+  if (mask) {
+    for (int e = 0; e < c->E; ++e) m[e] = mask[e] != 0;
+  } else {
+    if (c->layer_last[layer].empty()) return MOE_OK;   // nothing to predict from yet
+    for (int e : c->layer_last[layer]) m[e] = 1;
+  }
+  std::vector<int> fills;
+  const int r = process(c, layer, m.data(), true, nullptr, nullptr, &fills, nullptr);
+  if (r == MOE_OK && n_filled) *n_filled = (int32_t)fills.size();
+  return r;
 }
 
 }  // namespace moe
@@ -247,6 +289,10 @@ int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache
   c->slot_key.assign(n_slots, -1);
   c->slot_fill_req.assign(n_slots, -1);
   c->layer_slots.assign(c->L, {});
+  c->layer_last.assign(c->L, {});
+  c->slot_pending.assign(n_slots, 0);
+  c->slot_prefetched.assign(n_slots, 0);
+  c->prefetch_next = cfg->prefetch_next_layer;
   c->st.n_slots = c->n_slots;
   *out = c;
   return MOE_OK;
@@ -262,14 +308,25 @@ int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* 
                              void* compute, int defer_waits, const void** slot_ptrs,
                              int32_t* n_missed) {
   if (!cache) return MOE_ERR_INVALID_ARG;
-  std::vector<int> misses;
+  std::vector<int> misses, waits;
   const int r = cache_request_split(cache, layer, used_mask, (cudaStream_t)compute, slot_ptrs,
-                                    nullptr, &misses);
+                                    nullptr, &misses, &waits);
   if (r != MOE_OK) return r;
   if (n_missed) *n_missed = (int32_t)misses.size();
-  if (!defer_waits && !misses.empty())
-    MOE_CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)compute, cache->last_copy, 0));
+  if (!defer_waits) {
+    if (!misses.empty())
+      MOE_CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)compute, cache->last_copy, 0));
+    for (int s : waits) {
+      MOE_CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)compute, cache->ready[s], 0));
+      cache->slot_pending[s] = 0;
+    }
+  }
   return MOE_OK;
+}
+
+int moe_expert_cache_prefetch(moe_expert_cache* cache, int layer, const uint8_t* mask,
+                              int32_t* n_filled) {
+  return cache_prefetch(cache, layer, mask, n_filled);
 }
 
 int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert,
@@ -279,8 +336,11 @@ int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert,
   auto f = cache->where.find(key_of(cache, layer, expert));
   if (f == cache->where.end()) return MOE_ERR_INVALID_ARG;
   const int slot = f->second.first;
-  if (cache->slot_fill_req[slot] == cache->req - 1)  // filled by the latest request
+  // filled by the latest request, or by a prefetch nothing has waited for yet
+  if (cache->slot_fill_req[slot] == cache->req - 1 || cache->slot_pending[slot]) {
     MOE_CUDA_TRY(cudaStreamWaitEvent((cudaStream_t)compute, cache->ready[slot], 0));
+    cache->slot_pending[slot] = 0;
+  }
   return MOE_OK;
 }
 
@@ -304,6 +364,7 @@ int moe_expert_cache_evict(moe_expert_cache* cache, int layer, int expert) {
   cache->order.erase(f->second.second);
   cache->where.erase(f);
   cache->slot_key[slot] = -1;
+  cache->slot_prefetched[slot] = 0;
   cache->free_slots.insert(slot);
   cache->st.evictions++;
   cache->st.resident = (int32_t)cache->where.size();

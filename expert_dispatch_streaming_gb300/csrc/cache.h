@@ -30,6 +30,10 @@ struct moe_expert_cache {
   std::vector<long long> slot_key;       // -1 = free
   std::vector<long long> slot_fill_req;  // request number of the slot's last fill
   std::vector<std::vector<int>> layer_slots;  // slots the layer's last request used
+  std::vector<std::vector<int>> layer_last;   // experts of the layer's last (demand) request
+  std::vector<char> slot_pending;        // filled, and no compute has waited for it yet
+  std::vector<char> slot_prefetched;     // filled by a prefetch, not yet used by a request
+  int prefetch_next = 0;
   std::vector<moe_cache_event> trace;
   moe_cache_stats st{};
   long long req = 0;
@@ -40,7 +44,12 @@ struct moe_expert_cache {
 
 namespace moe {
 int cache_wait_event(moe_expert_cache* c, cudaEvent_t ev);
-// Request with the hit/miss split reported (used by the layer forward).
+// Request with the hit/miss split reported (used by the layer forward).  wait_slots (nullable)
+// receives the slots of hits whose copy (a prefetch) no compute has waited for yet; the caller
+// makes its compute stream wait on their ready events before using them.
 int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cudaStream_t compute,
-                        const void** slot_ptrs, std::vector<int>* hits, std::vector<int>* misses);
+                        const void** slot_ptrs, std::vector<int>* hits, std::vector<int>* misses,
+                        std::vector<int>* wait_slots = nullptr);
+// Prefetch request (see moe_expert_cache_prefetch); mask NULL = the layer's last expert set.
+int cache_prefetch(moe_expert_cache* c, int layer, const uint8_t* mask, int32_t* n_filled);
 }  // namespace moe

@@ -254,7 +254,17 @@ int moe_combine(const uint16_t* y_perm, const int32_t* pos, const float* w, int 
  * takes the lowest free slot, else evicts the least-recently-used key (never one this request
  * already touched).  Eviction drops the slot (the pinned host copy stays).  A request that
  * needs more distinct bundles than there are slots fails with MOE_ERR_CAPACITY and changes
- * nothing. */
+ * nothing.
+ *
+ * Prefetch (lookahead: "NovaLLM ...", "3. Optimization #1 -- Expert-Level Streaming" reads the
+ * next layer ahead while the current one computes; "The Billion-Token Bottleneck", "Predictive
+ * Prefetching: Looking into the Future", copies predicted experts with cudaMemcpyAsync before
+ * the model reaches their layer -- its predictor is a trained draft router, which is not part
+ * of this library).  A prefetch request for a layer is processed exactly like a request (same
+ * order, same LRU updates, same slot choice) but only copies: nothing computes on it.  Its
+ * prediction is a caller-given expert mask or, by default, the set of experts the layer's
+ * previous request used (the previous decode step's routing of that layer).  A later request
+ * that hits a prefetched bundle waits for its copy. */
 typedef struct moe_expert_cache moe_expert_cache;
 
 typedef struct moe_host_bundle {
@@ -272,21 +282,27 @@ typedef struct moe_expert_cache_config {
   int verify_checksums;     /* 1: hash every bundle at creation (MOE_ERR_CORRUPT)      */
   int device;               /* CUDA device ordinal of the slots                        */
   int time_copies;          /* 1: bracket every miss copy with timing events           */
+  int prefetch_next_layer;  /* 1: moe_layer_forward on layer l ends by prefetching layer
+                               (l + 1) mod n_layers with that layer's previous expert set */
 } moe_expert_cache_config;
 
-/* One trace record per distinct expert of every request, in processing order. */
+/* One trace record per distinct expert of every request (and prefetch request), in
+ * processing order. */
 typedef struct moe_cache_event {
-  int64_t request;          /* running request number                                  */
+  int64_t request;          /* running request number (requests and prefetches share it)   */
   int32_t layer, expert;
-  int32_t miss;             /* 0 = hit, 1 = miss                                       */
+  int32_t miss;             /* 0 = hit, 1 = miss (a copy was issued)                       */
   int32_t victim_layer, victim_expert;  /* -1 when no key was evicted                  */
   int32_t slot;
+  int32_t prefetch;         /* 1 = record of a prefetch request                            */
 } moe_cache_event;
 
 typedef struct moe_cache_stats {
-  int64_t requests, hits, misses, evictions;
-  int64_t bytes_h2d;        /* = misses * slot_bytes                                   */
+  int64_t requests, hits, misses, evictions;  /* requests / hits / misses: demand requests */
+  int64_t bytes_h2d;        /* every copied bundle (misses and prefetch fills) * slot_bytes */
   int32_t n_slots, resident;
+  int64_t prefetch_requests, prefetch_fills;
+  int64_t prefetch_used;    /* demand hits on a prefetched bundle, counted on its first use */
 } moe_cache_stats;
 
 /* Creates a cache: allocates n_slots slots in one device allocation, a non-blocking copy
@@ -310,6 +326,13 @@ int moe_expert_cache_destroy(moe_expert_cache* cache);
 int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* used_mask,
                              void* compute, int defer_waits, const void** slot_ptrs,
                              int32_t* n_missed);
+/* Prefetch request for `layer`: mask = HOST [E] bytes (experts to make resident), or NULL for
+ * the experts of the layer's previous request (no-op when the layer has none yet).  Copies
+ * are issued on the copy stream after the copies already issued; each waits for the previous
+ * readers of its slot.  *n_filled (nullable) receives the number of copies.  Host-side and
+ * non-blocking.  MOE_ERR_CAPACITY as for a request. */
+int moe_expert_cache_prefetch(moe_expert_cache* cache, int layer, const uint8_t* mask,
+                              int32_t* n_filled);
 /* Makes stream `compute` wait until (layer, expert)'s bundle has arrived (no-op for a hit). */
 int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert, void* compute);
 /* Marks the end of `layer`'s use of its slots on stream `compute` (records last-use events

@@ -17,6 +17,13 @@ Readings of what the pages leave open:
   simply the LRU key);
 * a request that needs more distinct bundles than there are slots is a capacity error;
 * an explicit eviction frees the key's slot (no-op when the key is not resident).
+
+Prefetch (lookahead: "NovaLLM ...", "3. Optimization #1 -- Expert-Level Streaming" reads the
+next layer ahead while the current one computes; "The Billion-Token Bottleneck", "Predictive
+Prefetching: Looking into the Future"): a prefetch request is processed exactly like a request
+-- same order, same LRU updates, same slot choice, request numbers shared -- and its records
+are flagged.  Its prediction, unless given, is the expert set of the layer's previous
+(non-prefetch) request; a layer with no previous request prefetches nothing.
 """
 from __future__ import annotations
 
@@ -35,15 +42,30 @@ class LRUSim:
         self.free = list(range(n_slots))            # kept sorted ascending
         self.trace: list[tuple] = []
         self.n_req = 0
+        self.last: dict[int, list[int]] = {}        # layer -> experts of its last request
 
     def request(self, layer: int, experts) -> dict[int, int]:
         """Make every expert in ``experts`` resident for ``layer``; returns {expert: slot}.
 
         Appends one trace record per unique expert:
-        (request#, layer, expert, HIT|MISS, victim_layer, victim_expert, slot), with
-        victim = (-1, -1) when no key was evicted.
+        (request#, layer, expert, HIT|MISS, victim_layer, victim_expert, slot, 0), with
+        victim = (-1, -1) when no key was evicted (the last field is the prefetch flag).
         """
         uniq = sorted(set(int(e) for e in experts))
+        result = self._process(layer, uniq, 0)
+        self.last[layer] = uniq
+        return result
+
+    def prefetch(self, layer: int, experts=None) -> dict[int, int]:
+        """Prefetch request: like ``request`` (records flagged 1) for ``experts``, or for the
+        layer's previous request when ``experts`` is None."""
+        if experts is None:
+            experts = self.last.get(layer, [])
+            if not experts:
+                return {}
+        return self._process(layer, sorted(set(int(e) for e in experts)), 1)
+
+    def _process(self, layer: int, uniq: list[int], flag: int) -> dict[int, int]:
         if len(uniq) > self.n_slots:
             raise CapacityError(f"{len(uniq)} bundles requested, {self.n_slots} slots")
         touched = set()
@@ -53,7 +75,7 @@ class LRUSim:
             if key in self.slot_of:
                 self.order.remove(key)
                 self.order.append(key)
-                rec = (self.n_req, layer, e, HIT, -1, -1, self.slot_of[key])
+                rec = (self.n_req, layer, e, HIT, -1, -1, self.slot_of[key], flag)
             else:
                 if self.free:
                     slot = self.free.pop(0)
@@ -64,7 +86,7 @@ class LRUSim:
                     slot = self.slot_of.pop(victim)
                 self.slot_of[key] = slot
                 self.order.append(key)
-                rec = (self.n_req, layer, e, MISS, victim[0], victim[1], slot)
+                rec = (self.n_req, layer, e, MISS, victim[0], victim[1], slot, flag)
             touched.add(key)
             result[e] = self.slot_of[key]
             self.trace.append(rec)

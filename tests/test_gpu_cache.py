@@ -33,12 +33,13 @@ def small_stack(layers=4):
                      shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", layers=layers)
 
 
-def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000):
+def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000, prefetch=0):
     store, table = syn.host_bundle_table(cfg, cfg.layers)
     nb = store.shape[1]
     c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=n_slots * nb,
                                     n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
-                                    timeout_ms=timeout_ms, verify_checksums=1, device=0)
+                                    timeout_ms=timeout_ms, verify_checksums=1, device=0,
+                                    prefetch_next_layer=prefetch)
     return moe.moe_expert_cache_create(c), store, table
 
 
@@ -70,12 +71,15 @@ def oracle_stack(cfg, trace, T, step):
     return xv
 
 
+@pytest.mark.parametrize("prefetch", [0, 1])
 @pytest.mark.parametrize("T,n_slots", [(1, 6), (3, 12), (5, 40)])
-def test_cache_trace_and_outputs_match(moe, syn, T, n_slots):
+def test_cache_trace_and_outputs_match(moe, syn, T, n_slots, prefetch):
+    """With prefetch, every layer call ends with a prefetch request for the next layer
+    (predicted from that layer's previous request); the outputs must not change."""
     cfg = small_stack()
     steps = 6
     trace = wl.stream_trace(cfg, T, steps=steps)
-    cache, store, table = make_cache(moe, syn, cfg, n_slots)
+    cache, store, table = make_cache(moe, syn, cfg, n_slots, prefetch=prefetch)
     try:
         outs, n_missed = run_stack(moe, syn, cfg, cache, trace, T, steps)
         got = moe.moe_expert_cache_trace(cache)
@@ -86,10 +90,15 @@ def test_cache_trace_and_outputs_match(moe, syn, T, n_slots):
     for s in range(steps):
         for l in range(cfg.layers):
             sim.request(l, np.unique(trace[s, l]).tolist())
+            if prefetch:
+                sim.prefetch((l + 1) % cfg.layers)
     assert got == sim.trace
-    misses = sum(r[3] for r in sim.trace)
+    misses = sum(r[3] for r in sim.trace if r[7] == 0)
+    fills = sum(r[3] for r in sim.trace if r[7] == 1)
     assert stats["misses"] == misses == n_missed
-    assert stats["bytes_h2d"] == misses * store.shape[1]
+    assert stats["prefetch_fills"] == fills
+    assert (fills > 0) == bool(prefetch)
+    assert stats["bytes_h2d"] == (misses + fills) * store.shape[1]
     for s in (0, steps - 1):
         assert_close(outs[s], oracle_stack(cfg, trace, T, s), f"stack step {s}")
 
@@ -150,3 +159,32 @@ def test_cache_corrupt_bundle_rejected(moe, syn):
     with pytest.raises(moe.MoEError) as ei:
         moe.moe_expert_cache_create(c)
     assert ei.value.status == moe.MOE_ERR_CORRUPT and ei.value.bad_index == 5
+
+
+def test_explicit_prefetch_and_wait(moe, syn):
+    """A caller-driven prefetch: the bundle lands in the slot the simulator predicts, a later
+    request hits it (counted as a used prefetch) and waiting for it leaves the bytes intact."""
+    cfg = small_stack(layers=2)
+    cache, store, table = make_cache(moe, syn, cfg, 4)
+    try:
+        mask = np.zeros(cfg.E, np.uint8)
+        mask[[3, 7]] = 1
+        assert moe.moe_expert_cache_prefetch(cache, 1, mask) == 2
+        assert moe.moe_expert_cache_prefetch(cache, 0) == 0        # no previous request
+        used = np.zeros(cfg.E, np.uint8)
+        used[[7, 9]] = 1
+        ptrs, nm = moe.moe_expert_cache_request(cache, 1, used)   # waits for the prefetch
+        assert nm == 1
+        st = moe.moe_expert_cache_stats(cache)
+        assert st["prefetch_requests"] == 1 and st["prefetch_fills"] == 2
+        assert st["prefetch_used"] == 1 and st["hits"] == 1 and st["misses"] == 1
+        moe.moe_expert_cache_sync(cache)
+        torch.cuda.synchronize()
+        got = moe.moe_expert_cache_trace(cache)
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+    sim = LRUSim(4)
+    sim.prefetch(1, [3, 7])
+    sim.prefetch(0)
+    sim.request(1, [7, 9])
+    assert got == sim.trace

@@ -19,7 +19,7 @@ def test_hand_worked_trace_two_slots():
         _, layer, *experts = lhs.split()
         before = len(sim.trace)
         sim.request(int(layer), [int(e) for e in experts])
-        got = [r[2:] for r in sim.trace[before:]]
+        got = [r[2:7] for r in sim.trace[before:]]
         want = [tuple(int(v) for v in rec.split()) for rec in rhs.split(";")]
         assert got == want, line
 
@@ -73,7 +73,8 @@ def test_replay_matches_ordered_dict(slots, E, layers, k):
                 e = int(rng.integers(E))
                 a.evict(layer, e)
                 b.evict(layer, e)
-    assert a.trace == b.trace
+    assert [r[:7] for r in a.trace] == b.trace
+    assert all(r[7] == 0 for r in a.trace)
     assert dict(a.slot_of) == dict(b.od)
 
 
@@ -84,3 +85,45 @@ def test_hits_plus_misses_and_bytes_moved():
     misses = sum(r[3] == MISS for r in sim.trace)
     # [0,1] 2 misses; [1,2] 1; [3,4] 2 (evicts 0); [0,5] 2 (evict 1,2); [1,2] 2 (evict 3,4)
     assert len(sim.trace) == 10 and misses == 9
+
+
+def test_prefetch_is_a_flagged_request():
+    """A prefetch changes the cache exactly as the same request would: replaying a mixed
+    sequence with every prefetch turned into a request gives the same records but the flag."""
+    rng = np.random.default_rng(7)
+    a, b = LRUSim(10), LRUSim(10)
+    for step in range(100):
+        for layer in range(4):
+            ids = rng.choice(12, size=4, replace=False).tolist()
+            a.request(layer, ids)
+            b.request(layer, ids)
+            nxt = (layer + 1) % 4
+            pred = a.last.get(nxt)
+            if pred:
+                a.prefetch(nxt)                  # predicted from the layer's previous request
+                b.request(nxt, pred)
+                b.last[nxt] = pred               # a prefetch does not change the prediction
+    assert [r[:7] for r in a.trace] == [r[:7] for r in b.trace]
+    assert any(r[7] == 1 for r in a.trace) and all(r[7] == 0 for r in b.trace)
+
+
+def test_prefetch_hand_trace():
+    """Two slots, two layers.  request(0, {0}) fills slot 0; request(1, {0}) fills slot 1;
+    prefetch(0) (previous set {0}: resident) only refreshes it; request(1, {1}) evicts the LRU
+    key (1, 0); prefetch(0, {2}) evicts (0, 0), since (1, 1) is more recent; a prefetch of a
+    layer with no request yet does nothing."""
+    sim = LRUSim(2)
+    sim.request(0, [0])
+    sim.request(1, [0])
+    sim.prefetch(0)
+    sim.request(1, [1])
+    sim.prefetch(0, [2])
+    assert sim.prefetch(5) == {}
+    assert [r[1:] for r in sim.trace] == [
+        (0, 0, MISS, -1, -1, 0, 0),
+        (1, 0, MISS, -1, -1, 1, 0),
+        (0, 0, HIT, -1, -1, 0, 1),
+        (1, 1, MISS, 1, 0, 1, 0),
+        (0, 2, MISS, 0, 0, 0, 1),
+    ]
+    assert [r[0] for r in sim.trace] == [0, 1, 2, 3, 4]
