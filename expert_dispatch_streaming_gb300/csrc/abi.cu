@@ -140,21 +140,31 @@ static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, 
   return c.used;
 }
 
+// Device-side expert list and bundle table that replace the routing's list (device LRU).
+struct DevExperts {
+  const int32_t* active = nullptr;
+  const int32_t* n_active = nullptr;
+  const void* const* tab = nullptr;
+};
+
 static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
                        const BundleTable& tab, int T, int host_n, const int32_t* host_ids,
-                       cudaStream_t st, std::function<int()> between) {
+                       cudaStream_t st, std::function<int()> between,
+                       const DevExperts& dx = DevExperts()) {
   const int rows = T * L->k;
+  const int32_t* act = dx.active ? dx.active : s.rs.active;
+  const int32_t* nact = dx.active ? dx.n_active : s.rs.n_active;
   GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows);
-  gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = s.rs.active;
-  gu.n_active = s.rs.n_active; gu.tab = &tab; gu.out = s.h;
+  gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = act;
+  gu.n_active = nact; gu.tab = &tab; gu.out = s.h; gu.dev_tab = dx.tab;
   gu.host_n = host_n; gu.host_ids = host_ids;
   GemmPlan pg = plan_gemm(gu);
   int r = launch_gemm(gu, pg, s.part, s.counters, s.err, st);
   if (r != MOE_OK) return r;
   if (between && (r = between()) != MOE_OK) return r;
   GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
-  dn.xin = s.h; dn.offsets = s.offsets; dn.active = s.rs.active;
-  dn.n_active = s.rs.n_active; dn.tab = &tab; dn.out = s.y_perm;
+  dn.xin = s.h; dn.offsets = s.offsets; dn.active = act;
+  dn.n_active = nact; dn.tab = &tab; dn.out = s.y_perm; dn.dev_tab = dx.tab;
   dn.host_n = host_n; dn.host_ids = host_ids;
   GemmPlan pd = plan_gemm(dn);
   return launch_gemm(dn, pd, s.part, s.counters, s.err, st);
@@ -452,6 +462,30 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
         return r;
     }
     if ((r = phase(4)) != MOE_OK) return r;
+  } else if (cache->device_lru) {
+    // A5 on the GPU: the LRU kernel decides hits and misses from the routing counts, the copy
+    // kernel brings the misses in on the cache's stream while the shared expert and the hit
+    // experts compute; no host round trip
+    if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
+    if ((r = phase(2)) != MOE_OK) return r;
+    if ((r = cache_dev_request(cache, L->layer_index, s.counts, s0, s.err)) != MOE_OK) return r;
+    BundleTable none{};
+    DevExperts hx;
+    hx.active = dev_hit_list(cache);
+    hx.n_active = dev_n_hit(cache);
+    hx.tab = cache->d_ptrs;
+    if ((r = run_experts(L, P, s, none, T, -1, nullptr, s0, std::function<int()>(), hx)) !=
+        MOE_OK)
+      return r;
+    if ((r = phase(3)) != MOE_OK) return r;
+    if ((r = cache_dev_wait_copies(cache, s0)) != MOE_OK) return r;
+    DevExperts mx = hx;
+    mx.active = dev_miss_list(cache);
+    mx.n_active = dev_n_miss(cache);
+    if ((r = run_experts(L, P, s, none, T, -1, nullptr, s0, std::function<int()>(), mx)) !=
+        MOE_OK)
+      return r;
+    if ((r = phase(4)) != MOE_OK) return r;
   } else {
     // A5: the layer's expert-use mask crosses to the host, the LRU decides, misses are copied
     // on the cache's copy stream while the shared expert and the hit experts compute.
@@ -498,7 +532,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   if (r != MOE_OK) return r;
   if ((r = phase(5)) != MOE_OK) return r;
   if (st) st->n_launches = (int32_t)(g_launches - launches0);
-  if (cache) {
+  if (cache && !cache->device_lru) {
     MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[L->layer_index], s0));
     cache->layer_done_valid[L->layer_index] = 1;
     // lookahead: copy the next layer's predicted experts while this layer still computes

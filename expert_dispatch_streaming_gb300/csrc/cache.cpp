@@ -44,6 +44,7 @@ static void destroy_all(moe_expert_cache* c) {
   cudaGetDevice(&cur);
   cudaSetDevice(c->device);
   if (c->copy) cudaStreamSynchronize(c->copy);
+  if (c->device_lru) cache_dev_free(c);
   for (auto e : c->ready) if (e) cudaEventDestroy(e);
   for (auto& pr : c->timed) { cudaEventDestroy(pr.first); cudaEventDestroy(pr.second); }
   for (auto& pr : c->pool) { cudaEventDestroy(pr.first); cudaEventDestroy(pr.second); }
@@ -294,6 +295,18 @@ int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache
   c->slot_prefetched.assign(n_slots, 0);
   c->prefetch_next = cfg->prefetch_next_layer;
   c->st.n_slots = c->n_slots;
+  if (cfg->device_lru) {
+    c->device_lru = 1;
+    cur = -1;
+    cudaGetDevice(&cur);
+    cudaSetDevice(c->device);
+    const int r = cache_dev_init(c);
+    if (cur >= 0) cudaSetDevice(cur);
+    if (r != MOE_OK) {
+      destroy_all(c);
+      return r;
+    }
+  }
   *out = c;
   return MOE_OK;
 }
@@ -308,6 +321,7 @@ int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* 
                              void* compute, int defer_waits, const void** slot_ptrs,
                              int32_t* n_missed) {
   if (!cache) return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   std::vector<int> misses, waits;
   const int r = cache_request_split(cache, layer, used_mask, (cudaStream_t)compute, slot_ptrs,
                                     nullptr, &misses, &waits);
@@ -326,6 +340,7 @@ int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* 
 
 int moe_expert_cache_prefetch(moe_expert_cache* cache, int layer, const uint8_t* mask,
                               int32_t* n_filled) {
+  if (cache && cache->device_lru) return MOE_ERR_UNSUPPORTED;
   return cache_prefetch(cache, layer, mask, n_filled);
 }
 
@@ -333,6 +348,7 @@ int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert,
                                  void* compute) {
   if (!cache || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
     return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   auto f = cache->where.find(key_of(cache, layer, expert));
   if (f == cache->where.end()) return MOE_ERR_INVALID_ARG;
   const int slot = f->second.first;
@@ -346,6 +362,7 @@ int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert,
 
 int moe_expert_cache_release(moe_expert_cache* cache, int layer, void* compute) {
   if (!cache || layer < 0 || layer >= cache->L) return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[layer], (cudaStream_t)compute));
   cache->layer_done_valid[layer] = 1;
   return MOE_OK;
@@ -354,6 +371,7 @@ int moe_expert_cache_release(moe_expert_cache* cache, int layer, void* compute) 
 int moe_expert_cache_evict(moe_expert_cache* cache, int layer, int expert) {
   if (!cache || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
     return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   auto f = cache->where.find(key_of(cache, layer, expert));
   if (f == cache->where.end()) return MOE_OK;
   if (cache->layer_done_valid[layer]) {
@@ -371,9 +389,37 @@ int moe_expert_cache_evict(moe_expert_cache* cache, int layer, int expert) {
   return MOE_OK;
 }
 
+// Device-side LRU: copy its counters into the host stats / the trace into the host vector.
+static int dev_sync_state(moe_expert_cache* c) {
+  int64_t ctl[kDevCtl];
+  MOE_CUDA_TRY(cudaDeviceSynchronize());
+  MOE_CUDA_TRY(cudaMemcpy(ctl, c->d_ctl, sizeof(ctl), cudaMemcpyDeviceToHost));
+  c->st.requests = ctl[kReq];
+  c->st.hits = ctl[kHits];
+  c->st.misses = ctl[kMisses];
+  c->st.evictions = ctl[kEvictions];
+  c->st.bytes_h2d = ctl[kBytes];
+  const int64_t n = std::min(ctl[kTraceN], c->trace_cap);
+  c->trace.resize((size_t)n);
+  if (n > 0)
+    MOE_CUDA_TRY(cudaMemcpy(c->trace.data(), c->d_trace, sizeof(moe_cache_event) * n,
+                            cudaMemcpyDeviceToHost));
+  std::vector<int32_t> sk(c->n_slots);
+  MOE_CUDA_TRY(cudaMemcpy(sk.data(), c->d_slot_key, sizeof(int32_t) * c->n_slots,
+                          cudaMemcpyDeviceToHost));
+  int res = 0;
+  for (int32_t k : sk) res += k >= 0;
+  c->st.resident = res;
+  return MOE_OK;
+}
+
 int moe_expert_cache_trace(const moe_expert_cache* cache, moe_cache_event* buf, size_t cap,
                            size_t* n) {
   if (!cache || !n) return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) {
+    const int r = dev_sync_state(const_cast<moe_expert_cache*>(cache));
+    if (r != MOE_OK) return r;
+  }
   *n = cache->trace.size();
   if (buf) std::memcpy(buf, cache->trace.data(), sizeof(moe_cache_event) * std::min(cap, *n));
   return MOE_OK;
@@ -381,12 +427,20 @@ int moe_expert_cache_trace(const moe_expert_cache* cache, moe_cache_event* buf, 
 
 int moe_expert_cache_reset_trace(moe_expert_cache* cache) {
   if (!cache) return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) {
+    MOE_CUDA_TRY(cudaDeviceSynchronize());
+    MOE_CUDA_TRY(cudaMemset(cache->d_ctl + kTraceN, 0, sizeof(int64_t)));
+  }
   cache->trace.clear();
   return MOE_OK;
 }
 
 int moe_expert_cache_stats(const moe_expert_cache* cache, moe_cache_stats* out) {
   if (!cache || !out) return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) {
+    const int r = dev_sync_state(const_cast<moe_expert_cache*>(cache));
+    if (r != MOE_OK) return r;
+  }
   *out = cache->st;
   return MOE_OK;
 }

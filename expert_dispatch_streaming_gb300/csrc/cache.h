@@ -40,6 +40,19 @@ struct moe_expert_cache {
   // copy timing (time_copies): event pairs of copies not yet collected, and a free pool
   int time_copies = 0;
   std::vector<std::pair<cudaEvent_t, cudaEvent_t>> timed, pool;
+  // device-side LRU (device_lru): the policy state lives on the GPU and the layer forward
+  // needs no host round trip (see cache_dev.cu)
+  int device_lru = 0;
+  int64_t* d_ctl = nullptr;         // [kDevCtl] counters (DevCtl indices)
+  int32_t* d_slot_key = nullptr;    // [n_slots] key of the slot, -1 free
+  int64_t* d_last_use = nullptr;    // [n_slots] clock of the slot's last touch
+  int32_t* d_key_slot = nullptr;    // [L*E] slot of the key, -1 not resident
+  const void** d_src = nullptr;     // [L*E] device-visible address of each host bundle
+  const void** d_ptrs = nullptr;    // [E] bundle pointer table of the latest request
+  int32_t* d_lists = nullptr;       // hit list [E], n_hit, miss list [E], miss slots [E], n_miss
+  moe_cache_event* d_trace = nullptr;
+  int64_t trace_cap = 0;
+  cudaEvent_t dev_lru_done = nullptr, dev_copy_done = nullptr;
 };
 
 namespace moe {
@@ -52,4 +65,22 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
                         std::vector<int>* wait_slots = nullptr);
 // Prefetch request (see moe_expert_cache_prefetch); mask NULL = the layer's last expert set.
 int cache_prefetch(moe_expert_cache* c, int layer, const uint8_t* mask, int32_t* n_filled);
+
+// ---- device-side LRU (cache_dev.cu)
+enum DevCtl { kClock = 0, kReq, kTraceN, kOverflow, kHits, kMisses, kEvictions, kBytes, kDevCtl = 16 };
+// Allocates and initialises the device state (empty cache).
+int cache_dev_init(moe_expert_cache* c);
+void cache_dev_free(moe_expert_cache* c);
+// Enqueues, for `layer`, the LRU request over the experts with counts[e] > 0 (device [E]) on
+// stream `s0`, and the copies of its misses on the cache's copy stream (joined back later by
+// cache_dev_wait_copies).  Fills d_ptrs and the hit / miss lists.  A request that needs more
+// distinct bundles than slots records MOE_ERR_CAPACITY in *err and leaves the state alone.
+int cache_dev_request(moe_expert_cache* c, int layer, const int32_t* counts, cudaStream_t s0,
+                      int32_t* err);
+int cache_dev_wait_copies(moe_expert_cache* c, cudaStream_t s0);
+// Device lists of the latest request.
+inline const int32_t* dev_hit_list(const moe_expert_cache* c) { return c->d_lists; }
+inline const int32_t* dev_n_hit(const moe_expert_cache* c) { return c->d_lists + c->E; }
+inline const int32_t* dev_miss_list(const moe_expert_cache* c) { return c->d_lists + c->E + 1; }
+inline const int32_t* dev_n_miss(const moe_expert_cache* c) { return c->d_lists + 3 * c->E + 1; }
 }  // namespace moe

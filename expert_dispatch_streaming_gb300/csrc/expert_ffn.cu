@@ -43,6 +43,7 @@ struct GemmKParams {
   int host_n;
   int16_t host_ids[kMaxExperts];
   BundleTable tab;
+  const void* const* dev_tab;
 };
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
   if (a >= (p.host_n >= 0 ? p.host_n : *p.n_active)) return;
   const int e = p.host_n >= 0 ? p.host_ids[a] : p.active[a];
   const int r0 = p.offsets[e], ne = p.offsets[e + 1] - r0;
-  const char* bundle = static_cast<const char*>(p.tab.p[e]);
+  const char* bundle = static_cast<const char*>(p.dev_tab ? p.dev_tab[e] : p.tab.p[e]);
   if (ne <= 0 || bundle == nullptr) return;
   const int K = p.K, M = p.M;
   const int m0 = mb * 64 + warp * 16;
@@ -282,6 +283,7 @@ int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* coun
   kp.m_blocks = g.m_blocks; kp.splits = g.splits; kp.k_per_split = g.k_per_split;
   kp.max_rows = a.max_rows; kp.out = a.out; kp.part = part; kp.counters = counters;
   kp.tab = *a.tab;
+  kp.dev_tab = a.dev_tab;
   kp.host_n = a.host_n;
   for (int i = 0; i < (a.host_n > 0 ? a.host_n : 0); ++i) kp.host_ids[i] = (int16_t)a.host_ids[i];
   if (a.host_n == 0) return MOE_OK;

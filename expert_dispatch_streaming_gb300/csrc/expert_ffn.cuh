@@ -22,6 +22,7 @@ struct GemmArgs {
   int host_n;               // >= 0: use host_ids[0..host_n) instead of active/n_active
   const int32_t* host_ids;
   const BundleTable* tab;
+  const void* const* dev_tab; // device [E] bundle pointers (device-side cache), else NULL
   size_t w_off, s_off;      // byte offsets of weights/codes and of INT4 scales in a bundle
   int K, M, E;
   int int4, fused;

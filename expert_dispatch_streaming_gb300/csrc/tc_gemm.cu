@@ -290,7 +290,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
       else hi = mid - 1;
     }
     const int e = p.host_n >= 0 ? p.host_ids[lo] : p.active[lo];
-    x.w = static_cast<const char*>(p.tab.p[e]) + p.w_off;
+    x.w = static_cast<const char*>(p.dev_tab ? p.dev_tab[e] : p.tab.p[e]) + p.w_off;
     x.tm = &p.tmap_b;
     x.out = p.out;
     x.part = p.part;
@@ -774,6 +774,7 @@ static int fill_params(TcParams& kp, const GemmArgs& a, const TcPlan& t, float* 
   kp.host_n = a.host_n;
   for (int i = 0; i < (a.host_n > 0 ? a.host_n : 0); ++i) kp.host_ids[i] = (int16_t)a.host_ids[i];
   kp.tab = *a.tab;
+  kp.dev_tab = a.dev_tab;
   kp.w_off = a.w_off;
   kp.K = a.K;
   kp.M = a.M;

@@ -14,6 +14,7 @@ struct TcParams {
   int host_n;
   int16_t host_ids[kMaxExperts];
   BundleTable tab;
+  const void* const* dev_tab;   // device [E] bundle pointers, read instead of tab when set
   size_t w_off;
   int K, M, S, kt_per_split, max_rows;
   uint16_t* out;

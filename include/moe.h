@@ -284,6 +284,17 @@ typedef struct moe_expert_cache_config {
   int time_copies;          /* 1: bracket every miss copy with timing events           */
   int prefetch_next_layer;  /* 1: moe_layer_forward on layer l ends by prefetching layer
                                (l + 1) mod n_layers with that layer's previous expert set */
+  int device_lru;           /* 1: keep the LRU state on the GPU.  moe_layer_forward then
+                               decides hits and misses in a kernel and copies the misses with
+                               a copy kernel reading the host bundles over the host link (the
+                               bundles must be pinned, mapped and 16-byte aligned): no host
+                               round trip, the call is fully asynchronous and can be captured
+                               in a CUDA graph.  Same policy and trace as the host LRU.  The
+                               host-side request / wait / release / evict / prefetch calls
+                               return MOE_ERR_UNSUPPORTED; trace, stats and sync synchronise
+                               the device.  A layer that needs more bundles than slots records
+                               error 20 in the workspace error word instead of returning
+                               MOE_ERR_CAPACITY.                                        */
 } moe_expert_cache_config;
 
 /* One trace record per distinct expert of every request (and prefetch request), in

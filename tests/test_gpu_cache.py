@@ -33,13 +33,13 @@ def small_stack(layers=4):
                      shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", layers=layers)
 
 
-def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000, prefetch=0):
+def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000, prefetch=0, device_lru=0):
     store, table = syn.host_bundle_table(cfg, cfg.layers)
     nb = store.shape[1]
     c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=n_slots * nb,
                                     n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
                                     timeout_ms=timeout_ms, verify_checksums=1, device=0,
-                                    prefetch_next_layer=prefetch)
+                                    prefetch_next_layer=prefetch, device_lru=device_lru)
     return moe.moe_expert_cache_create(c), store, table
 
 
@@ -71,15 +71,18 @@ def oracle_stack(cfg, trace, T, step):
     return xv
 
 
-@pytest.mark.parametrize("prefetch", [0, 1])
+@pytest.mark.parametrize("mode", ["host", "prefetch", "device"])
 @pytest.mark.parametrize("T,n_slots", [(1, 6), (3, 12), (5, 40)])
-def test_cache_trace_and_outputs_match(moe, syn, T, n_slots, prefetch):
-    """With prefetch, every layer call ends with a prefetch request for the next layer
-    (predicted from that layer's previous request); the outputs must not change."""
+def test_cache_trace_and_outputs_match(moe, syn, T, n_slots, mode):
+    """host: the host LRU; prefetch: every layer call also ends with a prefetch request for the
+    next layer (predicted from that layer's previous request); device: the LRU runs on the GPU.
+    The trace follows the simulator and the outputs do not change."""
     cfg = small_stack()
     steps = 6
+    prefetch = mode == "prefetch"
     trace = wl.stream_trace(cfg, T, steps=steps)
-    cache, store, table = make_cache(moe, syn, cfg, n_slots, prefetch=prefetch)
+    cache, store, table = make_cache(moe, syn, cfg, n_slots, prefetch=int(prefetch),
+                                     device_lru=int(mode == "device"))
     try:
         outs, n_missed = run_stack(moe, syn, cfg, cache, trace, T, steps)
         got = moe.moe_expert_cache_trace(cache)
@@ -95,7 +98,8 @@ def test_cache_trace_and_outputs_match(moe, syn, T, n_slots, prefetch):
     assert got == sim.trace
     misses = sum(r[3] for r in sim.trace if r[7] == 0)
     fills = sum(r[3] for r in sim.trace if r[7] == 1)
-    assert stats["misses"] == misses == n_missed
+    assert stats["misses"] == misses
+    assert n_missed == (misses if mode != "device" else 0)   # the device LRU reports no host count
     assert stats["prefetch_fills"] == fills
     assert (fills > 0) == bool(prefetch)
     assert stats["bytes_h2d"] == (misses + fills) * store.shape[1]
@@ -188,3 +192,88 @@ def test_explicit_prefetch_and_wait(moe, syn):
     sim.prefetch(0)
     sim.request(1, [7, 9])
     assert got == sim.trace
+
+
+def test_device_lru_stack_replays_as_a_cuda_graph(moe, syn):
+    """With the LRU on the GPU a whole decode step of the stack (every layer, its cache
+    decisions and miss copies) is captured once and replayed: the outputs equal the eager run
+    bit for bit and the trace still follows the simulator."""
+    cfg = small_stack()
+    T, steps, n_slots = 2, 5, 10
+    trace = wl.stream_trace(cfg, T, steps=steps)
+    cache, store, table = make_cache(moe, syn, cfg, n_slots, device_lru=1)
+    layers = [syn.DeviceLayer(cfg, layer=l, cached=True) for l in range(cfg.layers)]
+    ws = layers[0].workspace(T)
+    x_in = torch.empty((T, cfg.H), dtype=torch.int16, device="cuda")
+    ids_in = torch.empty((cfg.layers, T, cfg.k), dtype=torch.int32, device="cuda")
+    bufs = [torch.empty_like(x_in) for _ in range(2)]
+    stream = torch.cuda.Stream()
+
+    def step():
+        x = x_in
+        for l in range(cfg.layers):
+            y = bufs[l & 1]
+            layers[l].forward(x, ws, out=y, forced_ids=ids_in[l], residual=x, cache=cache,
+                              stream=stream)
+            x = y
+        return x
+
+    outs = []
+    try:
+        with torch.cuda.stream(stream):
+            x_in.copy_(syn.to_device_bits(wl.stream_tokens(cfg, T, 0)))
+            ids_in.copy_(torch.from_numpy(np.ascontiguousarray(trace[0])))
+            y = step()                       # step 0 eagerly (also warms up the launches)
+        stream.synchronize()
+        outs.append(syn.bits_of(y).copy())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            y = step()
+        for s in range(1, steps):
+            with torch.cuda.stream(stream):
+                x_in.copy_(syn.to_device_bits(wl.stream_tokens(cfg, T, s)))
+                ids_in.copy_(torch.from_numpy(np.ascontiguousarray(trace[s])))
+                g.replay()
+            stream.synchronize()
+            outs.append(syn.bits_of(y).copy())
+        assert moe.moe_workspace_error(ws) == 0
+        got = moe.moe_expert_cache_trace(cache)
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+    sim = LRUSim(n_slots)
+    for s in range(steps):
+        for l in range(cfg.layers):
+            sim.request(l, np.unique(trace[s, l]).tolist())
+    assert got == sim.trace
+    # the same steps eagerly, each with a fresh device-LRU cache replaying the same history
+    cache2, _, _ = make_cache(moe, syn, cfg, n_slots, device_lru=1)
+    try:
+        for s in range(steps):
+            with torch.cuda.stream(stream):
+                x_in.copy_(syn.to_device_bits(wl.stream_tokens(cfg, T, s)))
+                ids_in.copy_(torch.from_numpy(np.ascontiguousarray(trace[s])))
+                y = step()
+            stream.synchronize()
+            assert np.array_equal(syn.bits_of(y), outs[s]), f"step {s}"
+    finally:
+        moe.moe_expert_cache_destroy(cache2)
+
+
+def test_device_lru_capacity_error_in_the_error_word(moe, syn):
+    cfg = small_stack(layers=1)
+    cache, store, table = make_cache(moe, syn, cfg, 2, device_lru=1)
+    try:
+        layer = syn.DeviceLayer(cfg, layer=0, cached=True)
+        T = 4
+        ws = layer.workspace(T)
+        x = syn.to_device_bits(wl.tokens(cfg, T))
+        ids = torch.tensor([[0, 1, 2, 3]] * T, dtype=torch.int32, device="cuda")
+        layer.forward(x, ws, forced_ids=ids, cache=cache)
+        torch.cuda.synchronize()
+        assert moe.moe_workspace_error(ws) == 20
+        assert moe.moe_expert_cache_stats(cache)["requests"] == 0
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_expert_cache_request(cache, 0, np.ones(cfg.E, np.uint8))
+        assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    finally:
+        moe.moe_expert_cache_destroy(cache)
