@@ -380,11 +380,12 @@ def run_streamed(args, local_rank):
     layers = [syn.DeviceLayer(cfg, layer=l, cached=True, device=dev) for l in range(cfg.layers)]
     setup_s = time.time() - t0
 
-    def make(cap_bytes, prefetch=0):
+    def make(cap_bytes, prefetch=0, device_lru=0):
         c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=cap_bytes,
                                         n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
                                         timeout_ms=20000, verify_checksums=1, device=local_rank,
-                                        time_copies=1, prefetch_next_layer=prefetch)
+                                        time_copies=1, prefetch_next_layer=prefetch,
+                                        device_lru=device_lru)
         return moe.moe_expert_cache_create(c)
 
     # probe: pinned H2D bandwidth of one bundle-sized copy on this machine (best of 3 rounds)
@@ -498,6 +499,51 @@ def run_streamed(args, local_rank):
             "h2d_gbs": round(sp["bytes_h2d"] / max(pcopy_ms, 1e-9) / 1e6, 1),
             "overlap_fraction": (round(min(1.0, max(0.0, 1 - (t_pf - t_res) / (pcopy_ms / 1e3))), 4)
                                  if pcopy_ms > 0 else None)}
+        # the LRU on the GPU: no host round trip per layer; one decode step (16 layers, their
+        # cache decisions and miss copies) captured once as a CUDA graph and replayed per step
+        # with that step's tokens and routing staged into the graph's input buffers
+        dc = make(wl.STREAM_CACHE_BYTES, device_lru=1)
+        try:
+            x_in = torch.empty_like(xs[0])
+            ids_in = torch.empty_like(ids_dev[0])
+
+            def dstep():
+                x = x_in
+                for l in range(cfg.layers):
+                    y = bufs[l & 1]
+                    layers[l].forward(x, ws, out=y, forced_ids=ids_in[l], residual=x,
+                                      cache=dc, stream=stream)
+                    x = y
+
+            with torch.cuda.stream(stream):
+                x_in.copy_(xs[0])
+                ids_in.copy_(ids_dev[0])
+                dstep()                                   # step 0 eagerly
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                dstep()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            with torch.cuda.stream(stream):
+                for st in range(1, args.stream_steps):
+                    x_in.copy_(xs[st], non_blocking=True)
+                    ids_in.copy_(ids_dev[st], non_blocking=True)
+                    g.replay()
+            e1.record(stream)
+            stream.synchronize()
+            t_dev = e0.elapsed_time(e1) / 1e3
+            sd = moe.moe_expert_cache_stats(dc)
+            del g
+        finally:
+            moe.moe_expert_cache_destroy(dc)
+        n_dev = args.stream_steps - 1
+        res["device_lru_graph"] = {
+            "tokens_per_s": round(T * n_dev / t_dev, 1),
+            "ms_per_step": round(1e3 * t_dev / n_dev, 3),
+            "hit_rate": round(sd["hits"] / max(1, sd["hits"] + sd["misses"]), 4),
+            "misses": sd["misses"], "bytes_h2d": sd["bytes_h2d"],
+            "steps_timed": n_dev}
         out["T"][str(T)] = res
         if T == 8 and args.capacity_sweep:
             # hit rate and throughput against the slot budget (the LRU thrash cliff): from

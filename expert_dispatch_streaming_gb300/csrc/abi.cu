@@ -174,14 +174,16 @@ static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratc
 // extra group: its rows are the T token rows of x, its output h_s / s).
 static int run_ffn_merged(const moe_layer* L, const LayerPlan& P, const LayerScratch& s,
                           const BundleTable& tab, const uint16_t* x, int T, cudaStream_t st,
-                          std::function<int()> between) {
+                          std::function<int()> between, const DevExperts& dx = DevExperts()) {
   const int rows = T * L->k;
   BundleTable stab{};
   stab.p[0] = L->shared_bundle;
   const int32_t* meta = s.rs.shared_meta;
+  const int32_t* act = dx.active ? dx.active : s.rs.active;
+  const int32_t* nact = dx.active ? dx.n_active : s.rs.n_active;
   GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows);
-  gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = s.rs.active;
-  gu.n_active = s.rs.n_active; gu.tab = &tab; gu.out = s.h;
+  gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = act;
+  gu.n_active = nact; gu.tab = &tab; gu.out = s.h; gu.dev_tab = dx.tab;
   GemmArgs sgu = gemm_args(P.slay, L->wdtype, true, L->H, L->Is, 1, T);
   sgu.xin = x; sgu.offsets = meta; sgu.active = meta + 2; sgu.n_active = meta + 3;
   sgu.tab = &stab; sgu.out = s.h_s;
@@ -189,8 +191,8 @@ static int run_ffn_merged(const moe_layer* L, const LayerPlan& P, const LayerScr
   if (r != MOE_OK) return r;
   if (between && (r = between()) != MOE_OK) return r;
   GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
-  dn.xin = s.h; dn.offsets = s.offsets; dn.active = s.rs.active;
-  dn.n_active = s.rs.n_active; dn.tab = &tab; dn.out = s.y_perm;
+  dn.xin = s.h; dn.offsets = s.offsets; dn.active = act;
+  dn.n_active = nact; dn.tab = &tab; dn.out = s.y_perm; dn.dev_tab = dx.tab;
   GemmArgs sdn = gemm_args(P.slay, L->wdtype, false, L->Is, L->H, 1, T);
   sdn.xin = s.h_s; sdn.offsets = meta; sdn.active = meta + 2; sdn.n_active = meta + 3;
   sdn.tab = &stab; sdn.out = s.s;
@@ -466,17 +468,25 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
     // A5 on the GPU: the LRU kernel decides hits and misses from the routing counts, the copy
     // kernel brings the misses in on the cache's stream while the shared expert and the hit
     // experts compute; no host round trip
-    if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
-    if ((r = phase(2)) != MOE_OK) return r;
     if ((r = cache_dev_request(cache, L->layer_index, s.counts, s0, s.err)) != MOE_OK) return r;
     BundleTable none{};
     DevExperts hx;
     hx.active = dev_hit_list(cache);
     hx.n_active = dev_n_hit(cache);
     hx.tab = cache->d_ptrs;
-    if ((r = run_experts(L, P, s, none, T, -1, nullptr, s0, std::function<int()>(), hx)) !=
-        MOE_OK)
-      return r;
+    if (P.merged) {
+      // the shared expert rides in the hit experts' launches
+      if ((r = phase(2)) != MOE_OK) return r;
+      if (st) st->shared_merged = 1;
+      if ((r = run_ffn_merged(L, P, s, none, x, T, s0, std::function<int()>(), hx)) != MOE_OK)
+        return r;
+    } else {
+      if ((r = run_shared(L, P, s, x, T, s0)) != MOE_OK) return r;
+      if ((r = phase(2)) != MOE_OK) return r;
+      if ((r = run_experts(L, P, s, none, T, -1, nullptr, s0, std::function<int()>(), hx)) !=
+          MOE_OK)
+        return r;
+    }
     if ((r = phase(3)) != MOE_OK) return r;
     if ((r = cache_dev_wait_copies(cache, s0)) != MOE_OK) return r;
     DevExperts mx = hx;
