@@ -204,42 +204,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
 
 template <int BN, bool FUSED, bool INT4>
 struct Cfg {
   static constexpr int NA = FUSED ? 2 : 1;                    // weight tiles per K step
+  // K per pipeline step: 64 for bf16 (one 128 x 64 tile image); 128 for INT4, one whole
+  // 8448-byte INT4 tile (codes + its scales), which halves the per-step cost per FLOP
+  static constexpr int KSTEP = INT4 ? 128 : 64;
   static constexpr int A_BYTES = 16384;                       // 128 rows x 64 k bf16
-  static constexpr int B_BYTES = BN * 128;                    // BN rows x 64 k bf16
-  // INT4: per 64-k step, half of an 8448-byte INT4 tile (4096 B of codes) + its 256 B scales
-  static constexpr int RAW_BYTES = INT4 ? 4096 + 256 : 0;
-  // shared-memory ring (filled by the producer): bf16 = A tile(s) + B tile; INT4 = B tile +
-  // raw codes.  INT4 A tiles never touch shared memory: the dequant warps write them into
-  // tensor memory (tcgen05.st) and the MMA reads A from there.
+  static constexpr int B_SUB = BN * 128;                      // BN rows x 64 k bf16 (one box)
+  static constexpr int B_BYTES = B_SUB * (KSTEP / 64);
+  static constexpr int RAW_BYTES = INT4 ? 8448 : 0;           // one INT4 tile per weight tile
+  // shared-memory ring (filled by the producer): bf16 = A tile(s) + B tile; INT4 = B tiles +
+  // raw INT4 tiles.  INT4 A tiles never touch shared memory: the dequant warps write them
+  // into tensor memory (tcgen05.st) and the MMA reads A from there.
   static constexpr int R1 = INT4 ? (B_BYTES + NA * RAW_BYTES + 1023) / 1024 * 1024
                                  : NA * A_BYTES + B_BYTES;
-  static constexpr int D1_FIT = 200 * 1024 / R1;
+  static constexpr int D1_FIT = (INT4 ? 220 : 200) * 1024 / R1;
   static constexpr int D1 = D1_FIT > 8 ? 8 : D1_FIT;
   static_assert(D1 >= 2, "the ring needs at least two stages");
   static constexpr int B_OFF = INT4 ? 0 : NA * A_BYTES;       // B tile inside a ring slot
   static constexpr int RAW_OFF = B_BYTES;                     // raw codes inside (INT4)
   static constexpr int TX = INT4 ? NA * RAW_BYTES + B_BYTES : NA * A_BYTES + B_BYTES;
   // tensor memory: accumulators (gate and up side by side when fused), double-buffered where
-  // they fit, then (INT4) D2 stages of dequantised A, 32 columns (64 bf16 of K) per tile
+  // they fit, then (INT4) D2 stages of dequantised A, 64 columns (128 bf16 of K) per tile
   static constexpr int ACC = NA * BN;                         // TMEM columns per tile
-  static constexpr int D2 = INT4 ? 4 : 0;
-  static constexpr int A_COLS = D2 * NA * 32;
+  static constexpr int D2 = INT4 ? (FUSED ? 2 : 4) : 0;
+  static constexpr int A_COLS = D2 * NA * (KSTEP / 2);
   static constexpr int BUFS = (2 * ACC + A_COLS <= 512) ? 2 : 1;
   static constexpr int A_TMEM = ACC * BUFS;                   // first column of the A stages
   static constexpr int USED = ACC * BUFS + A_COLS;
@@ -265,7 +258,7 @@ struct Unit {
 // of unit counts kept in shared memory; units past the routed experts belong to the second
 // group (the shared expert) when there is one.
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, int n_act,
-                                            int u, int BN) {
+                                            int u, int BN, int KSTEP) {
   Unit x;
   int base, tile_base;
   if (p.g2 && u >= pref[n_act]) {
@@ -274,7 +267,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
     x.out = p.out2;
     x.part = p.part2;
     x.M = p.M2;
-    x.KT = p.K2 / 64;
+    x.KT = p.K2 / KSTEP;
     x.S = p.S2;
     x.kps = p.kt_per_split2;
     x.max_rows = p.rows2;
@@ -295,7 +288,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
     x.out = p.out;
     x.part = p.part;
     x.M = p.M;
-    x.KT = p.K / 64;
+    x.KT = p.K / KSTEP;
     x.S = p.S;
     x.kps = p.kt_per_split;
     x.max_rows = p.max_rows;
@@ -398,7 +391,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     uint32_t phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const Unit x = decode_unit(p, pref, n_act, u, BN, C::KSTEP);
       const char* wb = x.w;
       const int KT = x.KT, MTx = x.MT;
       const int kt_lo = x.ks * x.kps, kt_hi = min(KT, kt_lo + x.kps);
@@ -409,14 +402,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         if (elect_one()) {
           mbar_expect_tx(fb, C::TX);
           if (INT4) {
-            // codes of this 64-k half of the 128-k INT4 tile, then the tile's row scales
+            // the whole 128-k INT4 tile (codes + row scales) of each weight tile
 #pragma unroll
-            for (int w = 0; w < C::NA; ++w) {
-              const char* tile = wb + ((size_t)(x.mt + w * MTx) * (KT / 2) + (kt >> 1)) * 8448;
-              uint8_t* raw = st + C::RAW_OFF + w * C::RAW_BYTES;
-              bulk_g2s(smem_u32(raw), tile + (kt & 1) * 4096, 4096, fb);
-              bulk_g2s(smem_u32(raw + 4096), tile + 8192, 256, fb);
-            }
+            for (int w = 0; w < C::NA; ++w)
+              bulk_g2s(smem_u32(st + C::RAW_OFF + w * C::RAW_BYTES),
+                       wb + ((size_t)(x.mt + w * MTx) * KT + kt) * 8448, 8448, fb);
           } else {
             bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES,
                         C::A_BYTES, fb);
@@ -424,8 +414,10 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
               bulk_g2s(smem_u32(st + C::A_BYTES),
                           wb + ((size_t)(x.mt + MTx) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
           }
-          tma_2d(smem_u32(st + C::B_OFF), x.tm, (ROUTER ? kt % p.kb_mod : kt) * 64,
-                    x.r0 + x.nt * BN, fb);
+#pragma unroll
+          for (int b = 0; b < C::KSTEP / 64; ++b)
+            tma_2d(smem_u32(st + C::B_OFF + b * C::B_SUB), x.tm,
+                   (ROUTER ? kt % p.kb_mod : kt) * C::KSTEP + b * 64, x.r0 + x.nt * BN, fb);
         }
         __syncwarp();
         if (++stage == C::D1) { stage = 0; phase ^= 1; }
@@ -438,7 +430,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     uint32_t phase = 0, aphase = 0, a2phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const Unit x = decode_unit(p, pref, n_act, u, BN, C::KSTEP);
       const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
       // the last token tile of a group is ragged: multiply only its first N = n_here rounded
       // up to 16 columns (the accumulator columns past it are never read)
@@ -456,14 +448,15 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         if (elect_one()) {
           tc_fence_after();
           if (INT4) {
-            // A from tensor memory: tile w of this stage at columns A_TMEM + (astage*NA + w)*32,
-            // eight columns (16 k) per MMA
-            const uint32_t ta = tmem_base + C::A_TMEM + astage * C::NA * 32;
+            // A from tensor memory: tile w of this stage at columns A_TMEM + (astage*NA + w)*64,
+            // eight columns (16 k) per MMA; B from the step's two 64-k boxes
+            const uint32_t ta = tmem_base + C::A_TMEM + astage * C::NA * 64;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
+            for (int j = 0; j < 8; ++j) {
               const uint32_t acc = (kt > kt_lo || j > 0) ? 1u : 0u;
-              mma_bf16_ts(dg, ta + 8 * j, db + 2 * j, idesc, acc);
-              if (FUSED) mma_bf16_ts(dg + BN, ta + 32 + 8 * j, db + 2 * j, idesc, acc);
+              const uint64_t bj = sdesc_sw128(s1 + C::B_OFF + (j >> 2) * C::B_SUB) + 2 * (j & 3);
+              mma_bf16_ts(dg, ta + 8 * j, bj, idesc, acc);
+              if (FUSED) mma_bf16_ts(dg + BN, ta + 64 + 8 * j, bj, idesc, acc);
             }
           } else {
             const uint64_t da = sdesc_sw128(s1), du = sdesc_sw128(s1 + C::A_BYTES);
@@ -494,7 +487,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     uint32_t aphase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const Unit x = decode_unit(p, pref, n_act, u, BN, C::KSTEP);
       const int MP = FUSED ? 2 * x.M : x.M;
       if (!(ok = warp_wait(smem_u32(&tfull[buf]), aphase, p.err, 4))) break;
       tc_fence_after();
@@ -588,8 +581,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     // ------------------------------------------------------------ INT4 dequant (warps 6..13)
     // A warp may only touch its own quarter of the TMEM lanes (warp % 4), so two warps share
     // each quarter: thread = weight row r = 32 * (warp % 4) + lane.  Fused: warps 6-9 convert
-    // the gate tile and warps 10-13 the up tile, each the row's 64 codes of the step (32
-    // columns); not fused: warps 6-9 codes 0-31 and warps 10-13 codes 32-63 (16 columns).
+    // the gate tile and warps 10-13 the up tile, each the row's 128 codes of the step (64
+    // columns); not fused: warps 6-9 codes 0-63 and warps 10-13 codes 64-127 (32 columns).
     const int q = warp & 3, half = (warp - 6) >> 2, r = q * 32 + lane;
     const int tile = FUSED ? half : 0;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
@@ -597,41 +590,35 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     uint32_t phase = 0, a2phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      const Unit x = decode_unit(p, pref, n_act, u, BN);
+      const Unit x = decode_unit(p, pref, n_act, u, BN, C::KSTEP);
       const int kt_lo = x.ks * x.kps, kt_hi = min(x.KT, kt_lo + x.kps);
       for (int kt = kt_lo; kt < kt_hi; ++kt) {
         if (!(ok = warp_wait(smem_u32(&full[stage]), phase, p.err, 5))) break;
         if (!(ok = warp_wait(smem_u32(&aempty[astage]), a2phase ^ 1, p.err, 7))) break;
         tc_fence_after();
         const uint8_t* raw = smem + stage * C::R1 + C::RAW_OFF + tile * C::RAW_BYTES;
-        const uint32_t s2 = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 4096 + 2 * r));
-        const uint32_t ta = tmem_base + lane_base + C::A_TMEM + (astage * C::NA + tile) * 32;
-        if (FUSED) {
-          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + r * 16);
-          const uint4 c1 = *reinterpret_cast<const uint4*>(raw + (128 + r) * 16);
-          const uint32_t w[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const uint32_t s2 = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 8192 + 2 * r));
+        const uint32_t ta = tmem_base + lane_base + C::A_TMEM + (astage * C::NA + tile) * 64;
+        // 32-code chunks c0, c0 + 1 of row r -> 32 TMEM columns (pairs in k order)
+        auto convert = [&](int c0, uint32_t col) {
+          const uint4 a = *reinterpret_cast<const uint4*>(raw + (c0 * 128 + r) * 16);
+          const uint4 b = *reinterpret_cast<const uint4*>(raw + ((c0 + 1) * 128 + r) * 16);
+          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
           uint32_t v[32];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
-            // word j holds codes 8j..8j+7 of the row: columns 4j..4j+3 (pairs in k order)
             v[4 * j + 0] = int4_pair<0>(w[j], s2);
             v[4 * j + 1] = int4_pair<1>(w[j], s2);
             v[4 * j + 2] = int4_pair<2>(w[j], s2);
             v[4 * j + 3] = int4_pair<3>(w[j], s2);
           }
-          tmem_st32(ta, v);
+          tmem_st32(ta + col, v);
+        };
+        if (FUSED) {
+          convert(0, 0);
+          convert(2, 32);
         } else {
-          const uint4 c0 = *reinterpret_cast<const uint4*>(raw + (half * 128 + r) * 16);
-          const uint32_t w[4] = {c0.x, c0.y, c0.z, c0.w};
-          uint32_t v[16];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            v[4 * j + 0] = int4_pair<0>(w[j], s2);
-            v[4 * j + 1] = int4_pair<1>(w[j], s2);
-            v[4 * j + 2] = int4_pair<2>(w[j], s2);
-            v[4 * j + 3] = int4_pair<3>(w[j], s2);
-          }
-          tmem_st16(ta + half * 16, v);
+          convert(2 * half, 32 * half);
         }
         tc_fence_before();
         __syncwarp();
@@ -723,7 +710,7 @@ TcPlan plan_tc(const GemmArgs& a) {
   t.BN = tc_bn_for(a);
   const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
                                           : std::min(a.E, a.max_rows));
-  const int MT = a.M / 128, KT = a.K / 64, sms = sm_count();
+  const int MT = a.M / 128, KT = a.K / (a.int4 ? 128 : 64), sms = sm_count();
   const int avg = ceil_div(std::max(a.max_rows, 1), A);
   // narrower token tiles first (more tiles, weights re-read from L2 only), then split K
   while (t.BN > 32 && A * MT * ceil_div(avg, t.BN) < sms &&
@@ -807,7 +794,8 @@ TcPair plan_tc_pair(const GemmArgs& a1, const GemmArgs& a2) {
   const int A = std::max(1, a1.host_n >= 0 ? std::min(a1.host_n, a1.max_rows)
                                            : std::min(a1.E, a1.max_rows));
   const int avg = ceil_div(std::max(a1.max_rows, 1), A);
-  const int KT1 = a1.K / 64, KT2 = a2.K / 64;
+  const int kstep = a1.int4 ? 128 : 64;
+  const int KT1 = a1.K / kstep, KT2 = a2.K / kstep;
   const int nt1 = A * (a1.M / 128) * std::max(1, ceil_div(avg, BN));
   const int nt2 = (a2.M / 128) * ceil_div(std::max(a2.max_rows, 1), BN);
   const int nt = nt1 + nt2;
