@@ -700,7 +700,9 @@ int tc_bn_for(const GemmArgs& a) {
   // fused tiles hold gate and up accumulators: a 256-token tile would fill all of TMEM (no
   // double buffer, the epilogue not overlapped with the next tile's MMA; with INT4 no room for
   // the dequantised weight stages); 128-token fused tiles measured faster at every bf16 shape
-  const int cap = a.fused ? 128 : 256;
+  // INT4 down tiles also stop at 128 tokens: at 256 the accumulator and the dequantised A
+  // stages fill TMEM without a second accumulator buffer, so the epilogue would not overlap
+  const int cap = (a.fused || a.int4) ? 128 : 256;
   const int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
   return std::min(bn, cap);
 }
