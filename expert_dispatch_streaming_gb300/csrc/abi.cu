@@ -96,6 +96,11 @@ static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
     GemmArgs sdn = gemm_args(P->slay, L->wdtype, false, L->Is, L->H, 1, T);
     P->sgu = plan_gemm(sgu);
     P->sdn = plan_gemm(sdn);
+    // the shared expert follows the routed experts' kernel choice, so the two share launches
+    if (P->gu.use_tc && P->dn.use_tc && tc_supported(sgu) && tc_supported(sdn)) {
+      P->sgu.use_tc = 1;
+      P->sdn.use_tc = 1;
+    }
     P->merged = P->gu.use_tc && P->dn.use_tc && P->sgu.use_tc && P->sdn.use_tc;
     if (P->merged) {
       P->mgu = plan_tc_pair(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows), sgu);

@@ -245,9 +245,10 @@ GemmPlan plan_gemm(const GemmArgs& a) {
   g.part_elems = g.splits > 1 ? (size_t)g.splits * a.max_rows * mp : 0;
   g.counter_elems = g.splits > 1 ? (size_t)g.A_max * g.m_blocks : 0;
   const bool tc_ok = tc_supported(a);
-  // INT4 decode (a few rows per expert) is dequant-bound in the tcgen05 kernel: the streaming
-  // kernel's in-register dequant with exact integer products is faster there
-  const bool int4_decode = a.int4 && avg <= 8;
+  // INT4 at the smallest batches (at most 64 routed rows, e.g. T <= 8 with k = 8): the
+  // streaming kernel's in-register dequantisation beats the tcgen05 kernel's per-step cost;
+  // from there on (measured at T = 32 with the DeepSeek-V3 shape) the tcgen05 kernel wins
+  const bool int4_decode = a.int4 && a.max_rows <= 64;
   g.use_tc = tc_ok && (g_ffn_path == 2 || (g_ffn_path == 0 && !int4_decode));
   g.tc = plan_tc(a);
   g.part_elems = std::max(g.part_elems, g.tc.part_elems);
