@@ -249,7 +249,12 @@ GemmPlan plan_gemm(const GemmArgs& a) {
   // streaming kernel's in-register dequantisation beats the tcgen05 kernel's per-step cost;
   // from there on (measured at T = 32 with the DeepSeek-V3 shape) the tcgen05 kernel wins
   const bool int4_decode = a.int4 && a.max_rows <= 64;
-  g.use_tc = tc_ok && (g_ffn_path == 2 || (g_ffn_path == 0 && !int4_decode));
+  // bf16 with a handful of rows and small expert matrices (measured: the Qwen1.5-MoE shape at
+  // T = 1, 4-12 MB per matrix) is launch-cost bound and the streaming kernel is faster there;
+  // the Mixtral shape (117-235 MB per matrix) and every larger batch stay on tcgen05
+  const double mat_bytes = (double)a.M * a.K * 2.0 * (a.fused ? 2 : 1);
+  const bool bf16_tiny = !a.int4 && a.max_rows <= 4 && mat_bytes <= 64e6;
+  g.use_tc = tc_ok && (g_ffn_path == 2 || (g_ffn_path == 0 && !int4_decode && !bf16_tiny));
   g.tc = plan_tc(a);
   g.part_elems = std::max(g.part_elems, g.tc.part_elems);
   g.counter_elems = std::max(g.counter_elems, g.tc.counter_elems);
