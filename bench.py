@@ -380,12 +380,13 @@ def run_streamed(args, local_rank):
     layers = [syn.DeviceLayer(cfg, layer=l, cached=True, device=dev) for l in range(cfg.layers)]
     setup_s = time.time() - t0
 
-    def make(cap_bytes, prefetch=0, device_lru=0):
+    def make(cap_bytes, prefetch=0, device_lru=0, copy_kernel=None):
+        ck = args.copy_kernel if copy_kernel is None else copy_kernel
         c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=cap_bytes,
                                         n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
                                         timeout_ms=20000, verify_checksums=1, device=local_rank,
                                         time_copies=1, prefetch_next_layer=prefetch,
-                                        device_lru=device_lru)
+                                        device_lru=device_lru, copy_kernel=int(ck))
         return moe.moe_expert_cache_create(c)
 
     # probe: pinned H2D bandwidth of one bundle-sized copy on this machine (best of 3 rounds)
@@ -455,6 +456,26 @@ def run_streamed(args, local_rank):
                    h2d_gbs=round(st_["bytes_h2d"] / max(copy_ms, 1e-9) / 1e6, 1),
                    copy_busy_s=round(copy_ms / 1e3, 4))
         res["h2d_frac_of_probe"] = round(res["h2d_gbs"] / probe_gbs, 4)
+        res["miss_copies"] = "fill kernel" if args.copy_kernel else "copy engine"
+        # the other copy path on the first quarter of the same trace, for comparison
+        alt_steps = max(1, args.stream_steps // 4)
+        alt = make(wl.STREAM_CACHE_BYTES, copy_kernel=1 - int(args.copy_kernel))
+        try:
+            torch.cuda.synchronize()
+            e0.record(stream)
+            run(alt, alt_steps)
+            e1.record(stream)
+            stream.synchronize()
+            t_alt = e0.elapsed_time(e1) / 1e3
+            sa = moe.moe_expert_cache_stats(alt)
+            acopy_ms, _ = moe.moe_expert_cache_copy_time(alt)
+        finally:
+            moe.moe_expert_cache_destroy(alt)
+        res["other_copy_path"] = {
+            "miss_copies": "copy engine" if args.copy_kernel else "fill kernel",
+            "steps": alt_steps, "tokens_per_s": round(T * alt_steps / t_alt, 1),
+            "ms_per_step": round(1e3 * t_alt / alt_steps, 3),
+            "h2d_gbs": round(sa["bytes_h2d"] / max(acopy_ms, 1e-9) / 1e6, 1)}
         # the same ids with every bundle resident (pre-filled full-size cache)
         full = make(cfg.layers * cfg.E * nb)
         try:
@@ -619,6 +640,8 @@ def main():
     ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--stream-steps", type=int, default=wl.STREAM_STEPS)
     ap.add_argument("--no-capacity-sweep", dest="capacity_sweep", action="store_false")
+    ap.add_argument("--copy-engine", dest="copy_kernel", action="store_false",
+                    help="host-LRU miss copies by cudaMemcpyAsync (default: the fill kernel)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.T is None:

@@ -57,7 +57,8 @@ class moe_expert_cache_config(C.Structure):
                 ("n_layers", C.c_int), ("n_experts", C.c_int),
                 ("bundles", C.POINTER(moe_host_bundle)), ("timeout_ms", C.c_int),
                 ("verify_checksums", C.c_int), ("device", C.c_int), ("time_copies", C.c_int),
-                ("prefetch_next_layer", C.c_int), ("device_lru", C.c_int)]
+                ("prefetch_next_layer", C.c_int), ("device_lru", C.c_int),
+                ("copy_kernel", C.c_int)]
 
 
 class moe_cache_event(C.Structure):

@@ -8,6 +8,11 @@
 // "NovaLLM: Running Massive MoE Models Fully In-Memory", "Optimization #2" (every bundle stays
 // resident in pinned host memory, so an evicted slot is simply dropped).
 //
+// A miss is copied by the copy engine (one cudaMemcpyAsync per bundle) or, with copy_kernel,
+// by one kernel per request that reads the bundles through their device-visible host
+// addresses (SM loads over the host link; on GB300's NVLink-C2C this held ~190 GB/s in every
+// run, where the copy engine reached 190 GB/s in some runs and 90-140 GB/s in others).
+//
 // Ordering on the GPU, without any host wait in the steady state:
 //  - a fill of slot s runs on the cache's copy stream after the event recorded when the
 //    layer that last read s released it (write-after-read guard);
@@ -38,13 +43,33 @@ int cache_wait_event(moe_expert_cache* c, cudaEvent_t ev) {
   }
 }
 
+// time_copies: an event pair around each copy (or fill kernel) on the copy stream
+static cudaError_t timed_copy_begin(moe_expert_cache* c) {
+  if (!c->time_copies) return cudaSuccess;
+  std::pair<cudaEvent_t, cudaEvent_t> tev{nullptr, nullptr};
+  if (c->pool.empty()) {
+    cudaError_t e = cudaEventCreate(&tev.first);
+    if (e == cudaSuccess) e = cudaEventCreate(&tev.second);
+    if (e != cudaSuccess) return e;
+  } else {
+    tev = c->pool.back();
+    c->pool.pop_back();
+  }
+  c->timed.push_back(tev);
+  return cudaEventRecord(tev.first, c->copy);
+}
+static cudaError_t timed_copy_end(moe_expert_cache* c) {
+  if (!c->time_copies) return cudaSuccess;
+  return cudaEventRecord(c->timed.back().second, c->copy);
+}
+
 static void destroy_all(moe_expert_cache* c) {
   if (!c) return;
   int cur = -1;
   cudaGetDevice(&cur);
   cudaSetDevice(c->device);
   if (c->copy) cudaStreamSynchronize(c->copy);
-  if (c->device_lru) cache_dev_free(c);
+  cache_dev_free(c);   // device LRU state and the bundle address table (if any)
   for (auto e : c->ready) if (e) cudaEventDestroy(e);
   for (auto& pr : c->timed) { cudaEventDestroy(pr.first); cudaEventDestroy(pr.second); }
   for (auto& pr : c->pool) { cudaEventDestroy(pr.first); cudaEventDestroy(pr.second); }
@@ -105,6 +130,7 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
   }
   std::vector<char> touched_slot(c->n_slots, 0);
   bool any_miss = false;
+  std::vector<int32_t> fill_key, fill_slot;   // copy_kernel: this request's fills
   for (int e = 0; e < c->E; ++e) {
     if (slot_ptrs) slot_ptrs[e] = nullptr;
     if (!used[e]) continue;
@@ -149,25 +175,17 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
       // write-after-read guard: the victim's layer must have finished reading this slot
       if (vl >= 0 && c->layer_done_valid[vl])
         MOE_CUDA_TRY(cudaStreamWaitEvent(c->copy, c->layer_done[vl], 0));
-      const moe_host_bundle& hb = c->bundles[(size_t)layer * c->E + e];
-      std::pair<cudaEvent_t, cudaEvent_t> tev{nullptr, nullptr};
-      if (c->time_copies) {
-        if (c->pool.empty()) {
-          MOE_CUDA_TRY(cudaEventCreate(&tev.first));
-          MOE_CUDA_TRY(cudaEventCreate(&tev.second));
-        } else {
-          tev = c->pool.back();
-          c->pool.pop_back();
-        }
-        MOE_CUDA_TRY(cudaEventRecord(tev.first, c->copy));
+      if (c->copy_kernel) {
+        fill_key.push_back((int32_t)((size_t)layer * c->E + e));   // copied after the loop
+        fill_slot.push_back(slot);
+      } else {
+        const moe_host_bundle& hb = c->bundles[(size_t)layer * c->E + e];
+        MOE_CUDA_TRY(timed_copy_begin(c));
+        MOE_CUDA_TRY(cudaMemcpyAsync(c->slab + (size_t)slot * c->slot_bytes, hb.ptr, hb.bytes,
+                                     cudaMemcpyHostToDevice, c->copy));
+        MOE_CUDA_TRY(timed_copy_end(c));
+        MOE_CUDA_TRY(cudaEventRecord(c->ready[slot], c->copy));
       }
-      MOE_CUDA_TRY(cudaMemcpyAsync(c->slab + (size_t)slot * c->slot_bytes, hb.ptr, hb.bytes,
-                                   cudaMemcpyHostToDevice, c->copy));
-      if (c->time_copies) {
-        MOE_CUDA_TRY(cudaEventRecord(tev.second, c->copy));
-        c->timed.push_back(tev);
-      }
-      MOE_CUDA_TRY(cudaEventRecord(c->ready[slot], c->copy));
       c->slot_pending[slot] = prefetch ? 1 : 0;   // a demand miss is waited for via last_copy
       c->slot_prefetched[slot] = prefetch ? 1 : 0;
       any_miss = true;
@@ -181,6 +199,20 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
     }
     c->trace.push_back(ev);
     if (slot_ptrs) slot_ptrs[e] = c->slab + (size_t)slot * c->slot_bytes;
+  }
+  if (!fill_key.empty()) {
+    // one kernel for all fills, after every victim's write-after-read guard above
+    MOE_CUDA_TRY(timed_copy_begin(c));
+    const int r = cache_fill_slots(c, (int)fill_key.size(), fill_key.data(), fill_slot.data());
+    if (r != MOE_OK) {
+      if (c->time_copies) {   // the pair's end was never recorded: back to the pool
+        c->pool.push_back(c->timed.back());
+        c->timed.pop_back();
+      }
+      return r;
+    }
+    MOE_CUDA_TRY(timed_copy_end(c));
+    for (int32_t sl : fill_slot) MOE_CUDA_TRY(cudaEventRecord(c->ready[sl], c->copy));
   }
   if (any_miss) MOE_CUDA_TRY(cudaEventRecord(c->last_copy, c->copy));
   c->st.resident = (int32_t)c->where.size();
@@ -295,12 +327,13 @@ int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache
   c->slot_prefetched.assign(n_slots, 0);
   c->prefetch_next = cfg->prefetch_next_layer;
   c->st.n_slots = c->n_slots;
-  if (cfg->device_lru) {
-    c->device_lru = 1;
+  if (cfg->device_lru || cfg->copy_kernel) {
+    c->device_lru = cfg->device_lru ? 1 : 0;
+    c->copy_kernel = cfg->copy_kernel ? 1 : 0;
     cur = -1;
     cudaGetDevice(&cur);
     cudaSetDevice(c->device);
-    const int r = cache_dev_init(c);
+    const int r = c->device_lru ? cache_dev_init(c) : cache_src_init(c);
     if (cur >= 0) cudaSetDevice(cur);
     if (r != MOE_OK) {
       destroy_all(c);

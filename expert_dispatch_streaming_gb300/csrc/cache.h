@@ -34,6 +34,7 @@ struct moe_expert_cache {
   std::vector<char> slot_pending;        // filled, and no compute has waited for it yet
   std::vector<char> slot_prefetched;     // filled by a prefetch, not yet used by a request
   int prefetch_next = 0;
+  int copy_kernel = 0;                   // host LRU: misses copied by slot_fill_kernel
   std::vector<moe_cache_event> trace;
   moe_cache_stats st{};
   long long req = 0;
@@ -66,7 +67,12 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
 // Prefetch request (see moe_expert_cache_prefetch); mask NULL = the layer's last expert set.
 int cache_prefetch(moe_expert_cache* c, int layer, const uint8_t* mask, int32_t* n_filled);
 
-// ---- device-side LRU (cache_dev.cu)
+// ---- copy kernels and the device-side LRU (cache_dev.cu)
+// Builds d_src, the device table of the host bundles' device-visible addresses.
+int cache_src_init(moe_expert_cache* c);
+// Enqueues on the copy stream one kernel that copies bundle keys[j] (layer * E + expert) from
+// the host store into slot slots[j], j < n <= kMaxExperts (needs d_src).
+int cache_fill_slots(moe_expert_cache* c, int n, const int32_t* keys, const int32_t* slots);
 enum DevCtl { kClock = 0, kReq, kTraceN, kOverflow, kHits, kMisses, kEvictions, kBytes, kDevCtl = 16 };
 // Allocates and initialises the device state (empty cache).
 int cache_dev_init(moe_expert_cache* c);

@@ -189,8 +189,23 @@ lru_request_kernel(DevArgs a, int layer, const int32_t* __restrict__ counts,
   }
 }
 
-// Copies the missed bundles of the latest request from the host store into their slots:
-// 16-byte loads from the bundles' device-visible host addresses (over the host link).
+// One bundle from its device-visible host address into a slot: 16-byte loads over the host
+// link, four in flight per thread, the grid striding through the bundle.
+__device__ __forceinline__ void copy_bundle(const uint4* __restrict__ s, uint4* __restrict__ d,
+                                            size_t n16) {
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
+  for (; i + 3 * stride < n16; i += 4 * stride) {
+    const uint4 v0 = s[i], v1 = s[i + stride], v2 = s[i + 2 * stride], v3 = s[i + 3 * stride];
+    d[i] = v0;
+    d[i + stride] = v1;
+    d[i + 2 * stride] = v2;
+    d[i + 3 * stride] = v3;
+  }
+  for (; i < n16; i += stride) d[i] = s[i];
+}
+
+// Copies the missed bundles of the latest request from the host store into their slots.
 __global__ void __launch_bounds__(kCopyThreads)
 bundle_copy_kernel(DevArgs a, int layer, const void* const* __restrict__ src) {
   const int E = a.E;
@@ -198,20 +213,25 @@ bundle_copy_kernel(DevArgs a, int layer, const void* const* __restrict__ src) {
   const int32_t* miss_list = a.lists + E + 1;
   const int32_t* miss_slot = a.lists + 2 * E + 1;
   const size_t n16 = a.slot_bytes / 16;
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  for (int j = 0; j < nm; ++j) {
-    const uint4* s = static_cast<const uint4*>(src[(size_t)layer * E + miss_list[j]]);
-    uint4* d = reinterpret_cast<uint4*>(a.slab + (size_t)miss_slot[j] * a.slot_bytes);
-    size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x;
-    for (; i + 3 * stride < n16; i += 4 * stride) {
-      const uint4 v0 = s[i], v1 = s[i + stride], v2 = s[i + 2 * stride], v3 = s[i + 3 * stride];
-      d[i] = v0;
-      d[i + stride] = v1;
-      d[i + 2 * stride] = v2;
-      d[i + 3 * stride] = v3;
-    }
-    for (; i < n16; i += stride) d[i] = s[i];
-  }
+  for (int j = 0; j < nm; ++j)
+    copy_bundle(static_cast<const uint4*>(src[(size_t)layer * E + miss_list[j]]),
+                reinterpret_cast<uint4*>(a.slab + (size_t)miss_slot[j] * a.slot_bytes), n16);
+}
+
+// The fills of one host-LRU request: keys (layer * E + expert) and their slots, by value.
+struct FillList {
+  int n;
+  int32_t key[kMaxExperts];
+  int32_t slot[kMaxExperts];
+};
+
+__global__ void __launch_bounds__(kCopyThreads)
+slot_fill_kernel(const void* const* __restrict__ src, char* __restrict__ slab, size_t slot_bytes,
+                 FillList f) {
+  const size_t n16 = slot_bytes / 16;
+  for (int j = 0; j < f.n; ++j)
+    copy_bundle(static_cast<const uint4*>(src[f.key[j]]),
+                reinterpret_cast<uint4*>(slab + (size_t)f.slot[j] * slot_bytes), n16);
 }
 
 __global__ void init_kernel(int32_t* slot_key, int n_slots, int64_t* last_use, int32_t* key_slot,
@@ -244,19 +264,10 @@ DevArgs args_of(moe_expert_cache* c) {
 
 }  // namespace
 
-int cache_dev_init(moe_expert_cache* c) {
+int cache_src_init(moe_expert_cache* c) {
   const size_t nk = (size_t)c->L * c->E;
-  MOE_CUDA_TRY(cudaMalloc(&c->d_ctl, sizeof(int64_t) * kDevCtl));
-  MOE_CUDA_TRY(cudaMalloc(&c->d_slot_key, sizeof(int32_t) * c->n_slots));
-  MOE_CUDA_TRY(cudaMalloc(&c->d_last_use, sizeof(int64_t) * c->n_slots));
-  MOE_CUDA_TRY(cudaMalloc(&c->d_key_slot, sizeof(int32_t) * nk));
+  if (c->slot_bytes % 16) return MOE_ERR_INVALID_ARG;
   MOE_CUDA_TRY(cudaMalloc(&c->d_src, sizeof(void*) * nk));
-  MOE_CUDA_TRY(cudaMalloc(&c->d_ptrs, sizeof(void*) * c->E));
-  MOE_CUDA_TRY(cudaMalloc(&c->d_lists, sizeof(int32_t) * (3 * c->E + 2)));
-  c->trace_cap = kTraceCap;
-  MOE_CUDA_TRY(cudaMalloc(&c->d_trace, sizeof(moe_cache_event) * c->trace_cap));
-  MOE_CUDA_TRY(cudaEventCreateWithFlags(&c->dev_lru_done, cudaEventDisableTiming));
-  MOE_CUDA_TRY(cudaEventCreateWithFlags(&c->dev_copy_done, cudaEventDisableTiming));
   // device-visible addresses of the host bundles (pinned memory is mapped)
   std::vector<const void*> src(nk);
   for (size_t i = 0; i < nk; ++i) {
@@ -269,6 +280,23 @@ int cache_dev_init(moe_expert_cache* c) {
     src[i] = dp;
   }
   MOE_CUDA_TRY(cudaMemcpy(c->d_src, src.data(), sizeof(void*) * nk, cudaMemcpyHostToDevice));
+  return MOE_OK;
+}
+
+int cache_dev_init(moe_expert_cache* c) {
+  const size_t nk = (size_t)c->L * c->E;
+  MOE_CUDA_TRY(cudaMalloc(&c->d_ctl, sizeof(int64_t) * kDevCtl));
+  MOE_CUDA_TRY(cudaMalloc(&c->d_slot_key, sizeof(int32_t) * c->n_slots));
+  MOE_CUDA_TRY(cudaMalloc(&c->d_last_use, sizeof(int64_t) * c->n_slots));
+  MOE_CUDA_TRY(cudaMalloc(&c->d_key_slot, sizeof(int32_t) * nk));
+  MOE_CUDA_TRY(cudaMalloc(&c->d_ptrs, sizeof(void*) * c->E));
+  MOE_CUDA_TRY(cudaMalloc(&c->d_lists, sizeof(int32_t) * (3 * c->E + 2)));
+  c->trace_cap = kTraceCap;
+  MOE_CUDA_TRY(cudaMalloc(&c->d_trace, sizeof(moe_cache_event) * c->trace_cap));
+  MOE_CUDA_TRY(cudaEventCreateWithFlags(&c->dev_lru_done, cudaEventDisableTiming));
+  MOE_CUDA_TRY(cudaEventCreateWithFlags(&c->dev_copy_done, cudaEventDisableTiming));
+  const int r = cache_src_init(c);
+  if (r != MOE_OK) return r;
   const int n = (int)std::max<size_t>(std::max<size_t>(nk, c->n_slots), kDevCtl);
   init_kernel<<<ceil_div(n, 256), 256>>>(c->d_slot_key, c->n_slots, c->d_last_use,
                                          c->d_key_slot, (int)nk, c->d_ctl);
@@ -277,9 +305,25 @@ int cache_dev_init(moe_expert_cache* c) {
   return MOE_OK;
 }
 
+int cache_fill_slots(moe_expert_cache* c, int n, const int32_t* keys, const int32_t* slots) {
+  if (n <= 0) return MOE_OK;
+  if (n > kMaxExperts || !c->d_src) return MOE_ERR_INVALID_ARG;
+  FillList f;
+  f.n = n;
+  for (int j = 0; j < n; ++j) {
+    f.key[j] = keys[j];
+    f.slot[j] = slots[j];
+  }
+  slot_fill_kernel<<<kCopyCtas, kCopyThreads, 0, c->copy>>>(c->d_src, c->slab, c->slot_bytes, f);
+  MOE_COUNT_LAUNCH();
+  MOE_LAUNCH_CHECK();
+  return MOE_OK;
+}
+
 void cache_dev_free(moe_expert_cache* c) {
   if (c->dev_lru_done) cudaEventDestroy(c->dev_lru_done);
   if (c->dev_copy_done) cudaEventDestroy(c->dev_copy_done);
+  c->dev_lru_done = c->dev_copy_done = nullptr;
   cudaFree(c->d_ctl);
   cudaFree(c->d_slot_key);
   cudaFree(c->d_last_use);

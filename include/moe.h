@@ -295,6 +295,13 @@ typedef struct moe_expert_cache_config {
                                the device.  A layer that needs more bundles than slots records
                                error 20 in the workspace error word instead of returning
                                MOE_ERR_CAPACITY.                                        */
+  int copy_kernel;          /* 1: the host LRU copies a request's misses with one kernel
+                               that reads the host bundles through their device-visible
+                               addresses (bundles pinned, mapped, 16-byte aligned, and
+                               slot_bytes a multiple of 16; else MOE_ERR_INVALID_ARG at
+                               creation) instead of one copy-engine cudaMemcpyAsync per
+                               bundle.  Same slots, events and trace.  The device LRU always
+                               copies this way.                                          */
 } moe_expert_cache_config;
 
 /* One trace record per distinct expert of every request (and prefetch request), in

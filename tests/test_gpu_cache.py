@@ -33,13 +33,14 @@ def small_stack(layers=4):
                      shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", layers=layers)
 
 
-def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000, prefetch=0, device_lru=0):
+def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000, prefetch=0, device_lru=0, copy_kernel=0):
     store, table = syn.host_bundle_table(cfg, cfg.layers)
     nb = store.shape[1]
     c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=n_slots * nb,
                                     n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
                                     timeout_ms=timeout_ms, verify_checksums=1, device=0,
-                                    prefetch_next_layer=prefetch, device_lru=device_lru)
+                                    prefetch_next_layer=prefetch, device_lru=device_lru,
+                                    copy_kernel=copy_kernel)
     return moe.moe_expert_cache_create(c), store, table
 
 
@@ -71,18 +72,20 @@ def oracle_stack(cfg, trace, T, step):
     return xv
 
 
-@pytest.mark.parametrize("mode", ["host", "prefetch", "device"])
+@pytest.mark.parametrize("mode", ["host", "host_kernel", "prefetch", "prefetch_kernel", "device"])
 @pytest.mark.parametrize("T,n_slots", [(1, 6), (3, 12), (5, 40)])
 def test_cache_trace_and_outputs_match(moe, syn, T, n_slots, mode):
     """host: the host LRU; prefetch: every layer call also ends with a prefetch request for the
-    next layer (predicted from that layer's previous request); device: the LRU runs on the GPU.
-    The trace follows the simulator and the outputs do not change."""
+    next layer (predicted from that layer's previous request); *_kernel: misses copied by the
+    fill kernel instead of the copy engine; device: the LRU runs on the GPU.  The trace follows
+    the simulator and the outputs do not change."""
     cfg = small_stack()
     steps = 6
-    prefetch = mode == "prefetch"
+    prefetch = mode.startswith("prefetch")
     trace = wl.stream_trace(cfg, T, steps=steps)
     cache, store, table = make_cache(moe, syn, cfg, n_slots, prefetch=int(prefetch),
-                                     device_lru=int(mode == "device"))
+                                     device_lru=int(mode == "device"),
+                                     copy_kernel=int(mode.endswith("_kernel")))
     try:
         outs, n_missed = run_stack(moe, syn, cfg, cache, trace, T, steps)
         got = moe.moe_expert_cache_trace(cache)
@@ -275,5 +278,33 @@ def test_device_lru_capacity_error_in_the_error_word(moe, syn):
         with pytest.raises(moe.MoEError) as ei:
             moe.moe_expert_cache_request(cache, 0, np.ones(cfg.E, np.uint8))
         assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+
+
+class _DeviceBytes:
+    """A raw device range as a CUDA-array-interface object (torch.as_tensor views it)."""
+
+    def __init__(self, addr, n):
+        self.__cuda_array_interface__ = {"shape": (n,), "typestr": "|u1", "data": (addr, False),
+                                         "version": 3}
+
+
+@pytest.mark.parametrize("copy_kernel", [0, 1])
+def test_filled_slots_hold_the_bundles(moe, syn, copy_kernel):
+    """The slots a request fills hold the host bundles byte for byte, whether the copy engine
+    or the fill kernel copied them."""
+    cfg = small_stack(layers=2)
+    cache, store, table = make_cache(moe, syn, cfg, 5, copy_kernel=copy_kernel)
+    try:
+        used = np.zeros(cfg.E, np.uint8)
+        used[[0, 3, 7, 15]] = 1
+        ptrs, nm = moe.moe_expert_cache_request(cache, 1, used)
+        assert nm == 4
+        moe.moe_expert_cache_sync(cache)
+        nb = store.shape[1]
+        for e in (0, 3, 7, 15):
+            got = torch.as_tensor(_DeviceBytes(ptrs[e], nb), device="cuda").cpu()
+            assert torch.equal(got, store[cfg.E + e].cpu()), f"expert {e}"
     finally:
         moe.moe_expert_cache_destroy(cache)
