@@ -30,7 +30,8 @@ GATING = {"softmax_renorm": 0, "softmax": 1, "sigmoid_bias_renorm": 2}
 
 MOE_W_BF16 = 0
 MOE_W_INT4_G128 = 1
-WDTYPE = {"bf16": 0, "int4_g128": 1}
+MOE_W_NVFP4 = 2
+WDTYPE = {"bf16": 0, "int4_g128": 1, "nvfp4": 2}
 
 
 class MoEError(RuntimeError):
@@ -45,7 +46,7 @@ class MoEError(RuntimeError):
 class moe_bundle_layout(C.Structure):
     _fields_ = [("total_bytes", C.c_size_t), ("gate_up_offset", C.c_size_t),
                 ("down_offset", C.c_size_t), ("gate_up_scale_offset", C.c_size_t),
-                ("down_scale_offset", C.c_size_t)]
+                ("down_scale_offset", C.c_size_t), ("global_scale_offset", C.c_size_t)]
 
 
 class moe_host_bundle(C.Structure):
@@ -112,6 +113,7 @@ _SIGS = {
     "moe_bundle_layout_of": (_i, [_i, _i, _i, C.POINTER(moe_bundle_layout)]),
     "moe_bundle_bytes": (_sz, [_i, _i, _i]),
     "moe_pack_bundle": (_i, [_i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_pack_bundle_nvfp4": (_i, [_i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_checksum64": (C.c_uint64, [_vp, _sz]),
     "moe_route_workspace_size": (_sz, [_i, _i, _i, _i]),
     "moe_route_topk": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
@@ -222,6 +224,13 @@ def moe_bundle_bytes(H, I, wdtype) -> int:
 def moe_pack_bundle(H, I, wdtype, wg, wu, wd, sg, su, sd, dst) -> None:
     _check(_lib.moe_pack_bundle(H, I, WDTYPE.get(wdtype, wdtype), ptr(wg), ptr(wu), ptr(wd),
                                 ptr(sg), ptr(su), ptr(sd), ptr(dst)), "moe_pack_bundle")
+
+
+def moe_pack_bundle_nvfp4(H, I, wg, wu, wd, sg, su, sd, gs, dst) -> None:
+    """wg/wu [H][I], wd [I][H]: uint8 E2M1 codes; sg/su [H/16][I], sd [I/16][H]: uint8 E4M3
+    block scales; gs: float32 [3] matrix scales (gate, up, down)."""
+    _check(_lib.moe_pack_bundle_nvfp4(H, I, ptr(wg), ptr(wu), ptr(wd), ptr(sg), ptr(su),
+                                      ptr(sd), ptr(gs), ptr(dst)), "moe_pack_bundle_nvfp4")
 
 
 def moe_checksum64(data, nbytes) -> int:

@@ -17,7 +17,8 @@ import torch
 import workloads as wl
 
 from . import (GATING, WDTYPE, moe_bundle_bytes, moe_checksum64, moe_host_bundle, moe_layer,
-               moe_layer_forward, moe_layer_workspace_size, moe_pack_bundle)
+               moe_layer_forward, moe_layer_workspace_size, moe_pack_bundle,
+               moe_pack_bundle_nvfp4)
 
 _POOL = ThreadPoolExecutor(max_workers=max(1, min(16, len(os.sched_getaffinity(0)))))
 
@@ -26,7 +27,10 @@ def pack_expert(cfg: wl.MoEConfig, layer: int, e: int, dst: np.ndarray, shared=F
     """Generate expert (layer, e) and pack it into the host byte array ``dst``."""
     w = wl.expert(cfg, layer, e, shared=shared)
     I = cfg.Is if shared else cfg.I
-    moe_pack_bundle(cfg.H, I, cfg.wdtype, w.wg, w.wu, w.wd, w.sg, w.su, w.sd, dst)
+    if cfg.wdtype == "nvfp4":
+        moe_pack_bundle_nvfp4(cfg.H, I, w.wg, w.wu, w.wd, w.sg, w.su, w.sd, w.gs, dst)
+    else:
+        moe_pack_bundle(cfg.H, I, cfg.wdtype, w.wg, w.wu, w.wd, w.sg, w.su, w.sd, dst)
 
 
 def host_bundles(cfg: wl.MoEConfig, layer: int, experts, pinned=True, shared=False) -> torch.Tensor:

@@ -28,8 +28,9 @@
  *  - Pointers documented "device" must be device-accessible global memory; "host" are
  *    ordinary host pointers.  Device buffers must be 16-byte aligned; row strides are the
  *    row lengths stated (dense, row-major).
- *  - bf16 values are passed as uint16_t bit patterns.  INT4 weights are two's-complement
- *    codes in [-7, 7], two per byte, the even reduction index in the low nibble.
+ *  - bf16 values are passed as uint16_t bit patterns.  INT4 weights are passed as int8 codes
+ *    in [-7, 7]; NVFP4 weights as one FP4 E2M1 code per byte and one FP8 E4M3 byte per block
+ *    scale (see moe_pack_bundle and moe_pack_bundle_nvfp4).
  */
 #ifndef MOE_H
 #define MOE_H
@@ -95,7 +96,9 @@ enum moe_gating {
 /* Expert weight storage inside a bundle. */
 enum moe_wdtype {
   MOE_W_BF16 = 0,      /* bf16 weights                                                   */
-  MOE_W_INT4_G128 = 1  /* symmetric INT4 codes + one bf16 scale per 128 reduction elements */
+  MOE_W_INT4_G128 = 1, /* symmetric INT4 codes + one bf16 scale per 128 reduction elements */
+  MOE_W_NVFP4 = 2      /* NVFP4: FP4 E2M1 codes, one FP8 E4M3 scale per 16 reduction
+                          elements, one fp32 scale per matrix (gate, up, down)            */
 };
 
 /* ------------------------------------------------------------------ expert bundles
@@ -120,12 +123,25 @@ enum moe_wdtype {
  *         0x80708070 is pair p as two bf16 subnormals q * 2^-129, which one bf16 multiply by
  *         scale * 2^129 dequantises.  The codes are followed by the rows' bf16 group scales
  *         at 8192 + 2r.
+ *   nvfp4: tiles of 128 rows x 128 k (9216 B): 16-byte chunk (c, r) at (c*128 + r)*16 holds
+ *         the 32 FP4 codes k = 32c..32c+31 of row r as four little-endian 32-bit words of
+ *         eight codes.  Code k = 8w + 2p + h of word w (pair p, half h) is a nibble
+ *         (sign, e1, e0, m) whose bits sit so that pair p, moved to bits m: 6 + 16h,
+ *         e0: 7 + 16h, e1: 8 + 16h, sign: 15 + 16h, is two bf16 numbers of value
+ *         E2M1(code) * 2^-126.  Pairs 0, 1, 2 get there by rotating the word right by 0, 6
+ *         and 12 and masking with 0x81C081C0; pair 3 by rotating right by 2 (e0, e1, sign;
+ *         mask 0x81808180) and by 10 (m; mask 0x00400040).  A bf16 multiply by
+ *         (block scale * 2^119) then gives E2M1 * scale * 2^-7 exactly (at most 6 significant
+ *         bits).  The codes are followed by each row's 8 E4M3 block scales (k = 16b..16b+15
+ *         of the tile) at 8192 + 8r + b.  The three fp32 matrix scales (gate, up, down)
+ *         follow the down section at global_scale_offset.
  *   gate_up_scale_offset / down_scale_offset give the scale block of the section's first tile.
  * Constraints: H and I multiples of 128.  */
 typedef struct moe_bundle_layout {
   size_t total_bytes;
   size_t gate_up_offset, down_offset;               /* weights or codes               */
-  size_t gate_up_scale_offset, down_scale_offset;   /* INT4 only, else 0              */
+  size_t gate_up_scale_offset, down_scale_offset;   /* INT4 / NVFP4, else 0           */
+  size_t global_scale_offset;                       /* NVFP4: 3 fp32, else 0          */
 } moe_bundle_layout;
 
 /* Fills *out for an expert of hidden size H, intermediate size I and storage `wdtype`.
@@ -143,6 +159,21 @@ size_t moe_bundle_bytes(int H, int I, int wdtype);
  * that is not finite with magnitude below 0.5 (codes times scales then stay below 3.5). */
 int moe_pack_bundle(int H, int I, int wdtype, const void* wg, const void* wu, const void* wd,
                     const uint16_t* sg, const uint16_t* su, const uint16_t* sd, void* dst);
+
+/* Packs one NVFP4 expert into a host bundle `dst` of moe_bundle_bytes(H, I, MOE_W_NVFP4)
+ * bytes.  The weight is W[k][n] = E2M1(code) * E4M3(block scale) * matrix scale, the block
+ * being 16 consecutive reduction elements k.
+ *  wg, wu: [H][I] uint8 FP4 E2M1 codes (bit 3 sign, bits 2-1 exponent, bit 0 mantissa; values
+ *          0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives); wd: [I][H].
+ *  sg, su: [H/16][I] FP8 E4M3 block scales (bias 7, subnormals; block k/16, column n);
+ *          sd: [I/16][H].
+ *  gs:     [3] fp32 matrix scales of gate, up and down.
+ * Host only, synchronous.  Returns MOE_ERR_INVALID_ARG on a code above 15, a block scale with
+ * the sign bit set or the NaN pattern 0x7F, or a matrix scale that is not finite or has
+ * magnitude 2^120 or more. */
+int moe_pack_bundle_nvfp4(int H, int I, const uint8_t* wg, const uint8_t* wu, const uint8_t* wd,
+                          const uint8_t* sg, const uint8_t* su, const uint8_t* sd,
+                          const float* gs, void* dst);
 
 /* FNV-1a 64-bit hash of `bytes` bytes of host memory (the checksum expert caches verify). */
 uint64_t moe_checksum64(const void* data, size_t bytes);
@@ -218,7 +249,8 @@ int moe_permute(const uint16_t* x, const int32_t* src, int T, int k, int H, uint
  * moe_grouped_swiglu -- for every expert e with rows [offsets[e], offsets[e+1]) of x_perm:
  *   h = bf16( silu(x Wg_e) * (x Wu_e) ),  y_perm[rows] = bf16( h Wd_e ),
  * with fp32 accumulation (INT4: code x bf16 activation products, the group scale applied
- * in fp32 or folded into a bf16 dequantised weight, see the design notes).
+ * in fp32 or folded into a bf16 dequantised weight; NVFP4: the exact bf16 product of code and
+ * block scale times the activation, the matrix scale applied to the fp32 sum).
  *  x_perm   device [rows_total][H] bf16, rows_total = offsets[E]
  *  offsets  device [E+1] int32 (from moe_route_topk)
  *  bundles  HOST array [E] of device pointers to packed bundles (NULL allowed for experts

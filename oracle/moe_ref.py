@@ -158,10 +158,47 @@ def dequant_int4(codes: np.ndarray, scales_bits: np.ndarray, group: int) -> np.n
     return q * np.repeat(s, group, axis=0)
 
 
+# NVFP4.  The expert-cache page names NVFP4 checkpoints ("Running 35B MoE Models on 8GB GPUs",
+# "Technical Insight": NVFP4/INT4 scales travel inside the expert bundle) without defining the
+# format; the reading here is the published NVFP4 definition: FP4 E2M1 elements, one FP8 E4M3
+# scale per 16 consecutive elements, one fp32 scale per tensor.
+
+
+def decode_e2m1(codes: np.ndarray) -> np.ndarray:
+    """FP4 E2M1 nibbles -> fp64: bit 3 sign, bits 2-1 exponent e (bias 1), bit 0 mantissa m;
+    value (-1)^sign * (m / 2) for e = 0 (subnormal), else 2^(e - 1) * (1 + m / 2)."""
+    c = np.asarray(codes).astype(np.int64)
+    sign = np.where((c >> 3) & 1, -1.0, 1.0)
+    e = (c >> 1) & 3
+    m = (c & 1).astype(np.float64)
+    mag = np.where(e == 0, m / 2.0, np.ldexp(1.0 + m / 2.0, (e - 1).astype(np.int64)))
+    return sign * mag
+
+
+def decode_e4m3(bytes_: np.ndarray) -> np.ndarray:
+    """FP8 E4M3 bytes -> fp64: bit 7 sign, bits 6-3 exponent e (bias 7), bits 2-0 mantissa m;
+    (-1)^sign * 2^-6 * (m / 8) for e = 0, else 2^(e - 7) * (1 + m / 8); 0x7F / 0xFF are NaN."""
+    b = np.asarray(bytes_).astype(np.int64)
+    sign = np.where((b >> 7) & 1, -1.0, 1.0)
+    e = (b >> 3) & 15
+    m = (b & 7).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(m / 8.0, -6), np.ldexp(1.0 + m / 8.0, (e - 7).astype(np.int64)))
+    return np.where((b & 0x7F) == 0x7F, np.nan, sign * mag)
+
+
+def dequant_nvfp4(codes: np.ndarray, scales: np.ndarray, g: float, block: int = 16) -> np.ndarray:
+    """W[r, c] = E2M1(code[r, c]) * E4M3(scale[r // block, c]) * g along the reduction
+    dimension r, in fp64 (exact)."""
+    return decode_e2m1(codes) * np.repeat(decode_e4m3(scales), block, axis=0) * float(g)
+
+
 def expert_matrices(w, group: int = 128):
     """(Wg[H, I], Wu[H, I], Wd[I, H]) as fp64 from a workloads.ExpertWeights."""
     if w.wdtype == "bf16":
         return bf16.decode(w.wg), bf16.decode(w.wu), bf16.decode(w.wd)
+    if w.wdtype == "nvfp4":
+        return (dequant_nvfp4(w.wg, w.sg, w.gs[0]), dequant_nvfp4(w.wu, w.su, w.gs[1]),
+                dequant_nvfp4(w.wd, w.sd, w.gs[2]))
     return (dequant_int4(w.wg, w.sg, group), dequant_int4(w.wu, w.su, group),
             dequant_int4(w.wd, w.sd, group))
 

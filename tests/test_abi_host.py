@@ -9,6 +9,7 @@ import numpy as np
 import pytest
 
 import workloads as wl
+from oracle import moe_ref
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -134,6 +135,117 @@ def test_int4_words_decode_as_bf16_subnormals(moe):
         k = 32 * c + 8 * w + 2 * p
         assert np.array_equal(lo, q[k, r].astype(np.float64))
         assert np.array_equal(hi, q[k + 1, r].astype(np.float64))
+
+
+def _rotr(words, n):
+    return ((words >> n) | (words << (32 - n))) & 0xFFFFFFFF if n else words
+
+
+def _nvfp4_pairs(words):
+    """The documented decode of an NVFP4 code word: pairs 0, 1, 2 = the word rotated right by
+    0 / 6 / 12 and masked with 0x81C081C0; pair 3 = (rotr 2 & 0x81808180) | (rotr 10 &
+    0x00400040).  Returns the four bf16x2 bit patterns (uint32)."""
+    w = words.astype(np.uint64)
+    out = [(_rotr(w, r) & 0x81C081C0) for r in (0, 6, 12)]
+    out.append((_rotr(w, 2) & 0x81808180) | (_rotr(w, 10) & 0x00400040))
+    return [o.astype(np.uint32) for o in out]
+
+
+def _bf16_halves(v):
+    lo = ((v & 0xFFFF) << 16).view(np.float32).astype(np.float64)
+    hi = (v & 0xFFFF0000).view(np.float32).astype(np.float64)
+    return lo, hi
+
+
+def _untile_nvfp4(buf, rows, K):
+    """Inverse of the tiled NVFP4 image through the documented pair decode: 9216-byte tiles of
+    128 rows x 128 k; chunk (c, r) at (c*128 + r)*16 holds k = 32c..32c+31 as four words; pair
+    p of word w gives codes 8w + 2p (low half) and 8w + 2p + 1 as bf16 numbers of value
+    E2M1 * 2^-126; block scales at 8192 + 8r + b.  Returns (values [rows, K], scales
+    [rows, K/16])."""
+    nt = (rows // 128) * (K // 128)
+    t = buf[:nt * 9216].reshape(rows // 128, K // 128, 9216)
+    words = t[:, :, :8192].copy().view("<u4").reshape(rows // 128, K // 128, 4, 128, 4)
+    vals = np.empty(words.shape + (8,), np.float64)
+    for p, v in enumerate(_nvfp4_pairs(words)):
+        lo, hi = _bf16_halves(v)
+        vals[..., 2 * p] = lo * 2.0 ** 126
+        vals[..., 2 * p + 1] = hi * 2.0 ** 126
+    vals = vals.reshape(words.shape[:4] + (32,)).transpose(0, 3, 1, 2, 4).reshape(rows, K)
+    sc = t[:, :, 8192:9216].reshape(rows // 128, K // 128, 128, 8)
+    sc = sc.transpose(0, 2, 1, 3).reshape(rows, K // 16)
+    return vals, sc
+
+
+def test_pack_nvfp4_layout(moe):
+    """Every code decodes, by the documented rotations and masks, to E2M1(code) * 2^-126; the
+    block scales and matrix scales sit where the layout says."""
+    H, I = 256, 384
+    cfg = wl.custom("pkf", H=H, I=I, wdtype="nvfp4")
+    w = wl.expert(cfg, 0, 3)
+    lay = moe.bundle_layout(H, I, "nvfp4")
+    buf = np.zeros(lay.total_bytes, np.uint8)
+    moe.moe_pack_bundle_nvfp4(H, I, w.wg, w.wu, w.wd, w.sg, w.su, w.sd, w.gs, buf)
+    v, sc = _untile_nvfp4(buf[lay.gate_up_offset:], 2 * I, H)
+    assert np.array_equal(v[:I], moe_ref.decode_e2m1(w.wg.T))
+    assert np.array_equal(v[I:], moe_ref.decode_e2m1(w.wu.T))
+    assert np.array_equal(sc[:I], w.sg.T) and np.array_equal(sc[I:], w.su.T)
+    v, sc = _untile_nvfp4(buf[lay.down_offset:], H, I)
+    assert np.array_equal(v, moe_ref.decode_e2m1(w.wd.T)) and np.array_equal(sc, w.sd.T)
+    gs = buf[lay.global_scale_offset:lay.global_scale_offset + 12].view(np.float32)
+    assert np.array_equal(gs, w.gs)
+    assert lay.gate_up_scale_offset == 8192 and lay.down_scale_offset == lay.down_offset + 8192
+    assert lay.down_offset == 2 * (H // 128) * (I // 128) * 9216
+    assert lay.total_bytes == lay.global_scale_offset + 256
+
+
+def test_nvfp4_dequant_product_is_exact(moe):
+    """bf16(code placed) * bf16(scale * 2^119) = E2M1 * E4M3 * 2^-7 exactly, for every code and
+    every valid scale byte: the product has at most 6 significant bits and stays a normal
+    bf16.  (bf16 products emulated in fp64, which is exact for these operands, then checked to
+    be representable in bf16.)"""
+    codes = np.arange(16)
+    scales = np.arange(0x7F)                                            # 0x00 .. 0x7E
+    q = moe_ref.decode_e2m1(codes)[:, None]
+    s = moe_ref.decode_e4m3(scales)[None, :]
+    prod = (q * 2.0 ** -126) * (s * 2.0 ** 119)
+    assert np.array_equal(prod, q * s * 2.0 ** -7)
+    # representable in bf16: the fp32 rounding of the product keeps only 8 significant bits
+    f = prod.astype(np.float32)
+    assert np.array_equal(f.astype(np.float64), prod)
+    assert np.all((f.view(np.uint32) & 0xFFFF) == 0)
+    nz = np.abs(prod[prod != 0])
+    assert nz.min() >= 2.0 ** -126 and nz.max() < 2.0 ** 127               # normal range
+    # the scale operand itself: s * 2^119 is a finite bf16 for every valid byte
+    B = (s * 2.0 ** 119).astype(np.float32)
+    assert np.all(np.isfinite(B)) and np.all((B.view(np.uint32) & 0xFFFF) == 0)
+
+
+@pytest.mark.parametrize("field,bad", [("code", 16), ("scale", 0x7F), ("scale", 0x80),
+                                       ("gs", np.inf), ("gs", 2.0 ** 120), ("gs", np.nan)])
+def test_pack_nvfp4_rejects_invalid_inputs(moe, field, bad):
+    H, I = 128, 128
+    q = np.zeros((H, I), np.uint8)
+    s = np.full((H // 16, I), 0x38, np.uint8)
+    gs = np.ones(3, np.float32)
+    if field == "code":
+        q[5, 7] = bad
+    elif field == "scale":
+        s[3, 9] = bad
+    else:
+        gs[1] = bad
+    buf = np.zeros(moe.moe_bundle_bytes(H, I, "nvfp4"), np.uint8)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.moe_pack_bundle_nvfp4(H, I, q, q, q, s, s, s, gs, buf)
+    assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+
+
+def test_generic_packer_refuses_nvfp4(moe):
+    H, I = 128, 128
+    buf = np.zeros(moe.moe_bundle_bytes(H, I, "nvfp4"), np.uint8)
+    q = np.zeros((H, I), np.uint8)
+    with pytest.raises(moe.MoEError):
+        moe.moe_pack_bundle(H, I, "nvfp4", q, q, q, q, q, q, buf)
 
 
 @pytest.mark.parametrize("bad", [0x3F00, 0xBF00, 0x7F80, 0x7FC0, 0x4000])

@@ -203,6 +203,74 @@ def test_int4_dequant_multiple_of_scale():
     assert wd[127, 200] == w.wd[127, 200] * bf16.decode(w.sd)[0, 200]
 
 
+# ----------------------------------------------------------------------------- NVFP4
+def test_e2m1_values_are_the_format_table():
+    """The eight E2M1 magnitudes of the FP4 format (0, 0.5, 1, 1.5, 2, 3, 4, 6), positive for
+    nibbles 0-7, negated for 8-15."""
+    mags = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    got = moe_ref.decode_e2m1(np.arange(16))
+    assert got[:8].tolist() == mags
+    assert got[8:].tolist() == [-m for m in mags]
+    assert np.signbit(got[8])                                            # nibble 8 is -0
+
+
+def test_e2m1_agrees_with_the_e4m3_decoder():
+    """Every E2M1 value is an E4M3 value with the same sign, exponent + 6 and mantissa << 2
+    (subnormal 0.5 = 2^-1); two independent decoders must agree."""
+    c = np.arange(16)
+    s, e, m = (c >> 3) & 1, (c >> 1) & 3, c & 1
+    normal = e > 0
+    b = np.where(normal, (s << 7) | ((e + 6) << 3) | (m << 2), (s << 7) | (m * (6 << 3)))
+    got = moe_ref.decode_e2m1(c)
+    ref = moe_ref.decode_e4m3(b)
+    assert np.array_equal(got, ref)
+
+
+def test_e4m3_matches_torch_float8():
+    b = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(b).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = moe_ref.decode_e4m3(b)
+    assert np.array_equal(np.isnan(got), np.isnan(ref))
+    ok = ~np.isnan(ref)
+    assert np.array_equal(got[ok], ref[ok])
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+
+
+def test_nvfp4_dequant_block_structure():
+    """W[r, c] = E2M1 * scale[r // 16, c] * g: one scale per 16 rows of the reduction
+    dimension (not per 128), times the matrix scale."""
+    codes = np.full((64, 2), 0b0010, np.uint8)                          # E2M1 1.0 everywhere
+    codes[17, 1] = 0b1111                                               # -6
+    scales = np.array([[0x38, 0x40], [0x30, 0x48], [0x01, 0x7E], [0x00, 0x39]], np.uint8)
+    w = moe_ref.dequant_nvfp4(codes, scales, 0.25)
+    s = moe_ref.decode_e4m3(scales)
+    assert w[0, 0] == 0.25 and w[15, 0] == 0.25 and w[16, 0] == 0.125   # 1 / 2^-1, g = 0.25
+    assert w[17, 1] == -6.0 * 4.0 * 0.25                                # block 1 of column 1
+    assert w[40, 0] == 2.0 ** -9 * 0.25 and w[63, 1] == 1.125 * 0.25
+    assert np.array_equal(w, moe_ref.decode_e2m1(codes) * np.repeat(s, 16, axis=0) * 0.25)
+
+
+def test_nvfp4_layer_uses_the_matrix_scales():
+    """A layer of NVFP4 experts equals the same layer with the dequantised weights given as
+    exact values; swapping the matrix scales of gate and up changes the output."""
+    cfg = _tiny(H=128, I=128, wdtype="nvfp4", k=2, E=4)
+    xb = wl.tokens(cfg, 5)
+    r = moe_ref.layer_forward(cfg, 0, xb)
+    w0 = wl.expert(cfg, 0, 0)
+    wg, wu, wd = moe_ref.expert_matrices(w0)
+    assert np.array_equal(wg, moe_ref.decode_e2m1(w0.wg) *
+                          np.repeat(moe_ref.decode_e4m3(w0.sg), 16, axis=0) * float(w0.gs[0]))
+    assert np.array_equal(wd, moe_ref.dequant_nvfp4(w0.wd, w0.sd, w0.gs[2]))
+
+    def swapped(layer, e, shared=False):
+        w = wl.expert(cfg, layer, e)
+        g = w.gs.copy()
+        g[[0, 1]] = g[[1, 0]]
+        return wl.ExpertWeights(w.wdtype, w.wg, w.wu, w.wd, w.sg, w.su, w.sd, g * 3)
+    r2 = moe_ref.layer_forward(cfg, 0, xb, weights=swapped)
+    assert np.abs(r2["out"] - r["out"]).max() > 0.05 * np.abs(r["out"]).max()
+
+
 # ----------------------------------------------------------------------------- combine
 def test_combine_by_hand():
     y = np.array([[1.0, 2.0], [10.0, 20.0], [100.0, 200.0]])

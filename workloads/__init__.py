@@ -13,7 +13,8 @@ big tensors can be drawn by several threads with identical results.
 
 bf16 values are carried as ``uint16`` bit patterns, rounded from fp32 samples with
 round-to-nearest-even.  INT4 weights are carried as ``int8`` codes in [-7, 7] in their
-logical layout; packing into a device bundle is the library's job.
+logical layout; NVFP4 weights as ``uint8`` FP4 E2M1 codes (0..15), ``uint8`` FP8 E4M3 block
+scales and three fp32 matrix scales; packing into a device bundle is the library's job.
 
 Workload shapes follow the five configurations of the task description (tiny, Mixtral-8x7B
 shaped, Qwen1.5-MoE-A2.7B shaped, DeepSeek-V3 shaped INT4, and the expert-streamed decode stack).
@@ -32,7 +33,8 @@ BLOCK = 1 << 22
 # tensor ids of the stream keys
 T_X, T_WR, T_RANK, T_WS, T_TRACE = 0, 1, 2, 3, 4
 T_WG, T_WU, T_WD = 10, 11, 12
-T_SG, T_SU, T_SD = 20, 21, 22          # INT4 group scales of gate / up / down
+T_SG, T_SU, T_SD = 20, 21, 22          # INT4 group / NVFP4 block scales of gate / up / down
+T_GS = 23                              # NVFP4 matrix scales
 T_PROBE = 40                           # calibration batches
 
 GATING = ("softmax_renorm", "softmax", "sigmoid_bias_renorm")
@@ -51,7 +53,7 @@ class MoEConfig:
     scale: float = 1.0          # routed weight multiplier (2.5 for the DeepSeek-V3 shape)
     Is: int = 0                 # shared-expert intermediate size, 0 = none
     shared_gate: str = "none"   # "none" | "sigmoid" (Qwen: sigmoid(x . w_s)) | "one"
-    wdtype: str = "bf16"        # "bf16" | "int4_g128"
+    wdtype: str = "bf16"        # "bf16" | "int4_g128" | "nvfp4"
     zipf_s: float = 0.0         # expert-popularity exponent, 0 = no popularity offsets
     bias_kind: str = "none"     # "none" | "logit" (added to logits) | "select" (selection only)
     layers: int = 1
@@ -74,11 +76,15 @@ QWEN = MoEConfig("qwen", 2, H=2048, E=60, k=4, I=1408, gating="softmax", Is=5632
 DEEPSEEK = MoEConfig("deepseek", 3, H=7168, E=256, k=8, I=2048, gating="sigmoid_bias_renorm",
                      scale=2.5, Is=2048, shared_gate="one", wdtype="int4_g128", zipf_s=1.1,
                      bias_kind="select", Ts=(1, 32, 512, 8192))
+# the same Qwen1.5-MoE shape with NVFP4 experts (the checkpoint format the expert-cache page runs)
+QWEN_NVFP4 = MoEConfig("qwen_nvfp4", 5, H=2048, E=60, k=4, I=1408, gating="softmax", Is=5632,
+                       shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", wdtype="nvfp4",
+                       Ts=(1, 16, 256, 2048, 8192))
 STREAMED = MoEConfig("streamed", 4, H=2048, E=60, k=4, I=1408, gating="softmax", Is=5632,
                      shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", layers=16,
                      Ts=(1, 8, 64))
 
-CONFIGS = {c.name: c for c in (TINY, MIXTRAL, QWEN, DEEPSEEK, STREAMED)}
+CONFIGS = {c.name: c for c in (TINY, MIXTRAL, QWEN, DEEPSEEK, STREAMED, QWEN_NVFP4)}
 
 # expert-streamed decode recipe: 256 steps, 4 GiB of VRAM slots, trace locality
 STREAM_STEPS = 256
@@ -179,6 +185,29 @@ def _int4_scales(key, shape, std):
     return _blocked(n, fill, key).reshape(shape)
 
 
+# NVFP4 recipe: E2M1 codes uniform over the 16 nibbles; E4M3 block scales uniform over the
+# bytes 0x60..0x7E (32 .. 448: scales near the top of the E4M3 range, as a per-tensor scale
+# chosen from the tensor's largest block leaves them); the matrix scale brings the weight's
+# standard deviation near `std` (E2M1 uniform: rms 2.93; these scales: rms ~178)
+FP4_SCALE_LO, FP4_SCALE_HI = 0x60, 0x7F
+
+
+def _fp4_codes(key, shape):
+    n = int(np.prod(shape))
+    return _blocked(n, lambda g, m: g.integers(0, 16, m, dtype=np.uint8), key).reshape(shape)
+
+
+def _e4m3_scales(key, shape):
+    n = int(np.prod(shape))
+    return _blocked(n, lambda g, m: g.integers(FP4_SCALE_LO, FP4_SCALE_HI, m, dtype=np.uint8),
+                    key).reshape(shape)
+
+
+def _matrix_scales(key, std):
+    g = _stream(*key).uniform(0.75, 1.25, 3)
+    return (g * (std / (2.93 * 178.0))).astype(np.float32)
+
+
 # ----------------------------------------------------------------------------- tensors
 def tokens(cfg: MoEConfig, T: int, step: int = 0) -> np.ndarray:
     """Activations x[T, H] as bf16 bits, N(0, x_std)."""
@@ -232,6 +261,8 @@ class ExpertWeights:
     int4_g128: ``wg``/``wu``/``wd`` int8 codes in the same logical layouts, and bf16 scales
     ``sg``/``su`` [H/group, I] and ``sd`` [I/group, H] (one per group of `group` consecutive
     elements along the reduction dimension).
+    nvfp4: ``wg``/``wu``/``wd`` uint8 E2M1 codes, ``sg``/``su`` [H/16, I] and ``sd`` [I/16, H]
+    uint8 E4M3 block scales, ``gs`` float32 [3] matrix scales (gate, up, down).
     """
     wdtype: str
     wg: np.ndarray
@@ -240,6 +271,7 @@ class ExpertWeights:
     sg: np.ndarray | None = None
     su: np.ndarray | None = None
     sd: np.ndarray | None = None
+    gs: np.ndarray | None = None
 
 
 def expert(cfg: MoEConfig, layer: int, e: int, shared: bool = False) -> ExpertWeights:
@@ -262,6 +294,16 @@ def expert(cfg: MoEConfig, layer: int, e: int, shared: bool = False) -> ExpertWe
                              _int4_scales(key(T_SG), (H // G, I), cfg.w_std),
                              _int4_scales(key(T_SU), (H // G, I), cfg.w_std),
                              _int4_scales(key(T_SD), (I // G, H), cfg.w_std))
+    if cfg.wdtype == "nvfp4":
+        assert H % 128 == 0 and I % 128 == 0
+        return ExpertWeights("nvfp4",
+                             _fp4_codes(key(T_WG), (H, I)),
+                             _fp4_codes(key(T_WU), (H, I)),
+                             _fp4_codes(key(T_WD), (I, H)),
+                             _e4m3_scales(key(T_SG), (H // 16, I)),
+                             _e4m3_scales(key(T_SU), (H // 16, I)),
+                             _e4m3_scales(key(T_SD), (I // 16, H)),
+                             _matrix_scales(key(T_GS), cfg.w_std))
     raise ValueError(cfg.wdtype)
 
 
