@@ -27,10 +27,12 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
-WORKLOADS = {"mixtral": wl.MIXTRAL, "qwen": wl.QWEN, "deepseek": wl.DEEPSEEK}
+WORKLOADS = {"mixtral": wl.MIXTRAL, "qwen": wl.QWEN, "deepseek": wl.DEEPSEEK,
+             "qwen_nvfp4": wl.QWEN_NVFP4}
 CANONICAL_E = {name: c.E for name, c in WORKLOADS.items()}   # before any --experts override
 WORKLOAD_NAMES = {"mixtral": "Mixtral-8x7B-shaped", "qwen": "Qwen1.5-MoE-A2.7B-shaped",
-                  "deepseek": "DeepSeek-V3-shaped INT4"}
+                  "deepseek": "DeepSeek-V3-shaped INT4",
+                  "qwen_nvfp4": "Qwen1.5-MoE-A2.7B-shaped NVFP4"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 NOMINAL_HBM_GBS = 7900.0
 
@@ -109,7 +111,8 @@ def layer_work(cfg, T, n_unique, shared_merged=False):
     include the shared expert when the library runs it inside the routed launches)."""
     H, I, k, E, Is = cfg.H, cfg.I, cfg.k, cfg.E, cfg.Is
     rows = T * k
-    bpw = 2.0 if cfg.wdtype == "bf16" else 0.5 + 2.0 / 128
+    # bytes per weight: bf16; INT4 codes + a bf16 scale per 128; NVFP4 codes + an E4M3 per 16
+    bpw = {"bf16": 2.0, "int4_g128": 0.5 + 2.0 / 128, "nvfp4": 0.5 + 1.0 / 16}[cfg.wdtype]
     gu_flops = 2.0 * rows * H * 2 * I
     dn_flops = 2.0 * rows * I * H
     gu_bytes = n_unique * 2 * I * H * bpw + rows * H * 2 + rows * I * 2
@@ -627,7 +630,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--T", type=int, default=None)
-    ap.add_argument("--workload", default="mixtral", choices=["mixtral", "qwen", "deepseek"])
+    ap.add_argument("--workload", default="mixtral", choices=list(WORKLOADS))
     ap.add_argument("--experts", type=int, default=None,
                     help="override the routed expert count (smaller profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])

@@ -72,10 +72,13 @@ static GemmArgs gemm_args(const moe_bundle_layout& lay, int wdtype, bool fused, 
   a.M = M;
   a.E = E;
   a.int4 = wdtype == MOE_W_INT4_G128;
+  a.fp4 = wdtype == MOE_W_NVFP4;
   a.fused = fused;
   a.max_rows = max_rows;
   a.w_off = fused ? lay.gate_up_offset : lay.down_offset;
   a.s_off = fused ? lay.gate_up_scale_offset : lay.down_scale_offset;
+  // NVFP4 matrix scales: gate, up, down fp32 at global_scale_offset
+  a.gs_rel = a.fp4 ? (long long)lay.global_scale_offset + (fused ? 0 : 8) - (long long)a.w_off : 0;
   a.host_n = -1;
   return a;
 }

@@ -128,4 +128,36 @@ __device__ __forceinline__ uint32_t int4_pair_dyn(uint32_t word, int p, uint32_t
   return d;
 }
 
+// ---------------------------------------------------------------- NVFP4 dequantisation
+// The bundle places the bits of each FP4 E2M1 code so that pair p of a 32-bit code word,
+// moved by fixed rotations and masks, is two bf16 numbers of value E2M1 * 2^-126 (exponent
+// e1 e0 in bf16 exponent bits 8-7, mantissa in bit 6, sign in bit 15: bf16 and E2M1 share
+// the same structure up to the exponent bias, 127 against 1).  One bf16 multiply by
+// (block scale * 2^119) gives E2M1 * scale * 2^-7, exact: at most 6 significant bits, and a
+// normal bf16 for every code and every E4M3 scale.  The matrix scale (times 2^7) is applied
+// to the fp32 accumulator.
+
+// (E4M3 scale * 2^119) in both halves.  The E4M3 bits shifted into fp32 position read as
+// scale * 2^-120 (E4M3 and fp32 share the structure up to the bias, 7 against 127, subnormals
+// included); two exact power-of-two multiplies (fp32 subnormals are kept: no flush to zero)
+// give scale * 2^119 <= 448 * 2^119, exact in bf16 (4 significant bits).
+__device__ __forceinline__ uint32_t fp4_scale_pair(uint32_t e4m3) {
+  const float f = __uint_as_float((e4m3 & 0x7Fu) << 20) * 0x1p120f * 0x1p119f;
+  const uint32_t b = float_to_bf16_bits(f);
+  return b | (b << 16);
+}
+// Pair p (codes 8w + 2p, 8w + 2p + 1 of code word `word`) -> bf16x2 of E2M1 * scale * 2^-7.
+template <int P>
+__device__ __forceinline__ uint32_t fp4_pair(uint32_t word, uint32_t scale_pair) {
+  uint32_t v;
+  if (P == 0) v = word & 0x81C081C0u;
+  else if (P == 1) v = __funnelshift_r(word, word, 6) & 0x81C081C0u;
+  else if (P == 2) v = __funnelshift_r(word, word, 12) & 0x81C081C0u;
+  else v = (__funnelshift_r(word, word, 2) & 0x81808180u) |
+           (__funnelshift_r(word, word, 10) & 0x00400040u);
+  uint32_t d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(scale_pair));
+  return d;
+}
+
 }  // namespace moe

@@ -253,8 +253,10 @@ GemmPlan plan_gemm(const GemmArgs& a) {
   // T = 1, 4-12 MB per matrix) is launch-cost bound and the streaming kernel is faster there;
   // the Mixtral shape (117-235 MB per matrix) and every larger batch stay on tcgen05
   const double mat_bytes = (double)a.M * a.K * 2.0 * (a.fused ? 2 : 1);
-  const bool bf16_tiny = !a.int4 && a.max_rows <= 4 && mat_bytes <= 64e6;
+  const bool bf16_tiny = !a.int4 && !a.fp4 && a.max_rows <= 4 && mat_bytes <= 64e6;
   g.use_tc = tc_ok && (g_ffn_path == 2 || (g_ffn_path == 0 && !int4_decode && !bf16_tiny));
+  // NVFP4 runs on the tcgen05 kernel only (the streaming kernel has no FP4 decode)
+  if (a.fp4) g.use_tc = tc_ok;
   g.tc = plan_tc(a);
   g.part_elems = std::max(g.part_elems, g.tc.part_elems);
   g.counter_elems = std::max(g.counter_elems, g.tc.counter_elems);
@@ -283,6 +285,7 @@ int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* coun
                 int32_t* err, cudaStream_t st) {
   if (a.max_rows <= 0) return MOE_OK;
   if (g.use_tc) return launch_tc(a, g.tc, part, counters, err, st);
+  if (a.fp4) return MOE_ERR_UNSUPPORTED;
   GemmKParams kp{};
   kp.xin = a.xin; kp.offsets = a.offsets; kp.active = a.active; kp.n_active = a.n_active;
   kp.w_off = a.w_off; kp.s_off = a.s_off; kp.K = a.K; kp.M = a.M;

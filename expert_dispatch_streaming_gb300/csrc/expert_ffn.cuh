@@ -24,8 +24,9 @@ struct GemmArgs {
   const BundleTable* tab;
   const void* const* dev_tab; // device [E] bundle pointers (device-side cache), else NULL
   size_t w_off, s_off;      // byte offsets of weights/codes and of INT4 scales in a bundle
+  long long gs_rel;         // NVFP4: byte offset of the matrix scale(s) from w_off
   int K, M, E;
-  int int4, fused;
+  int int4, fp4, fused;
   int max_rows;             // upper bound of offsets[E]
   uint16_t* out;            // [rows][M]
 };

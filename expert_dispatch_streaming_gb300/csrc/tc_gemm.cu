@@ -9,16 +9,17 @@
 // Streaming").
 //
 // Persistent kernel, one CTA per SM, warp-specialised:
-//   warp 0      producer: per 64-wide K step, one 1-D bulk copy per 128-row weight tile (the
-//               bundle stores each tile as its 128-byte-swizzled shared-memory image; INT4: the
-//               step's codes and the tile's scales) and one 2-D TMA load of the BN token rows
-//               (128-byte swizzle), completing on an mbarrier;
+//   warp 0      producer: per K step (64 wide; 128 for quantised weights), one 1-D bulk copy
+//               per 128-row weight tile (the bundle stores each tile as its 128-byte-swizzled
+//               shared-memory image; INT4 / NVFP4: the tile's codes and scales) and 2-D TMA
+//               loads of the BN token rows (128-byte swizzle), completing on an mbarrier;
 //   warp 1      MMA issuer: allocates TMEM, issues tcgen05.mma (M = 128 weight rows, N = BN
 //               tokens, K = 16), commits stage release and accumulator-ready to mbarriers;
 //   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulators (each warp owns one 32-lane
 //               quarter of TMEM), SiLU * mul, bf16 stores (or fp32 split-K partials);
-//   warps 6-13  (INT4 only) dequantisation: codes -> bf16(code * scale) written straight into
-//               tensor memory with tcgen05.st; the MMA takes its A operand from there.
+//   warps 6-13  (INT4 / NVFP4) dequantisation: codes -> bf16(code * scale) written straight
+//               into tensor memory with tcgen05.st; the MMA takes its A operand from there.
+//               NVFP4's matrix scale multiplies the fp32 accumulator in the epilogue.
 // Producer and MMA warps run their loops as whole, converged warps (warp-uniform descriptors,
 // warp-vote waits) and issue from one lane chosen by elect.sync: a warp that waits in one
 // divergent lane pays hundreds of cycles per step to reconverge, and an issue under a plain
@@ -205,18 +206,28 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+// silu(g) * u = g / (1 + e^-g) * u with the hardware exponential and reciprocal (relative error
+// ~1e-6, far below the bf16 rounding of the result); for g below about -88, e^-g overflows
+// to +inf and the quotient is -0, the limit of silu.
+__device__ __forceinline__ float silu_mul(float g, float u) {
+  return __fdividef(g, 1.f + __expf(-g)) * u;
+}
 
-template <int BN, bool FUSED, bool INT4>
+// Weight storage of a kernel variant: bf16 tile images, INT4 or NVFP4 tiles.
+enum WType { kBf16 = 0, kInt4 = 1, kFp4 = 2 };
+
+template <int BN, bool FUSED, int WT>
 struct Cfg {
+  static constexpr bool INT4 = WT != kBf16;                   // quantised: dequant warps
   static constexpr int NA = FUSED ? 2 : 1;                    // weight tiles per K step
-  // K per pipeline step: 64 for bf16 (one 128 x 64 tile image); 128 for INT4, one whole
-  // 8448-byte INT4 tile (codes + its scales), which halves the per-step cost per FLOP
+  // K per pipeline step: 64 for bf16 (one 128 x 64 tile image); 128 for quantised weights,
+  // one whole tile of 128 k (codes + its scales), which halves the per-step cost per FLOP
   static constexpr int KSTEP = INT4 ? 128 : 64;
   static constexpr int A_BYTES = 16384;                       // 128 rows x 64 k bf16
   static constexpr int B_SUB = BN * 128;                      // BN rows x 64 k bf16 (one box)
   static constexpr int B_BYTES = B_SUB * (KSTEP / 64);
-  static constexpr int RAW_BYTES = INT4 ? 8448 : 0;           // one INT4 tile per weight tile
+  // one quantised tile per weight tile: INT4 8448 bytes, NVFP4 9216 bytes
+  static constexpr int RAW_BYTES = WT == kInt4 ? 8448 : WT == kFp4 ? 9216 : 0;
   // shared-memory ring (filled by the producer): bf16 = A tile(s) + B tile; INT4 = B tiles +
   // raw INT4 tiles.  INT4 A tiles never touch shared memory: the dequant warps write them
   // into tensor memory (tcgen05.st) and the MMA reads A from there.
@@ -247,6 +258,7 @@ struct Cfg {
 
 struct Unit {
   const char* w;            // weight section of this unit's expert
+  const float* gs;          // NVFP4: the section's matrix scale(s) (gate, up or down)
   const CUtensorMap* tm;    // its token rows
   uint16_t* out;
   float* part;
@@ -263,6 +275,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
   int base, tile_base;
   if (p.g2 && u >= pref[n_act]) {
     x.w = static_cast<const char*>(p.w2);
+    x.gs = reinterpret_cast<const float*>(x.w + p.gs_rel2);
     x.tm = &p.tmap_b2;
     x.out = p.out2;
     x.part = p.part2;
@@ -284,6 +297,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
     }
     const int e = p.host_n >= 0 ? p.host_ids[lo] : p.active[lo];
     x.w = static_cast<const char*>(p.dev_tab ? p.dev_tab[e] : p.tab.p[e]) + p.w_off;
+    x.gs = reinterpret_cast<const float*>(x.w + p.gs_rel);
     x.tm = &p.tmap_b;
     x.out = p.out;
     x.part = p.part;
@@ -308,10 +322,11 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
   return x;
 }
 
-template <int BN, bool FUSED, bool INT4, bool ROUTER = false>
-__global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
+template <int BN, bool FUSED, int WT, bool ROUTER = false>
+__global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ TcParams p) {
-  using C = Cfg<BN, FUSED, INT4>;
+  using C = Cfg<BN, FUSED, WT>;
+  constexpr bool INT4 = C::INT4;   // any quantised weight type
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -402,11 +417,12 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         if (elect_one()) {
           mbar_expect_tx(fb, C::TX);
           if (INT4) {
-            // the whole 128-k INT4 tile (codes + row scales) of each weight tile
+            // the whole 128-k quantised tile (codes + row scales) of each weight tile
 #pragma unroll
             for (int w = 0; w < C::NA; ++w)
               bulk_g2s(smem_u32(st + C::RAW_OFF + w * C::RAW_BYTES),
-                       wb + ((size_t)(x.mt + w * MTx) * KT + kt) * 8448, 8448, fb);
+                       wb + ((size_t)(x.mt + w * MTx) * KT + kt) * C::RAW_BYTES, C::RAW_BYTES,
+                       fb);
           } else {
             bulk_g2s(smem_u32(st), wb + ((size_t)x.mt * KT + kt) * C::A_BYTES,
                         C::A_BYTES, fb);
@@ -489,6 +505,12 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
       const Unit x = decode_unit(p, pref, n_act, u, BN, C::KSTEP);
       const int MP = FUSED ? 2 * x.M : x.M;
+      // NVFP4: the accumulators hold sum(E2M1 * scale * 2^-7 * x); times matrix scale * 2^7
+      float gsc = 1.f, usc = 1.f;
+      if (WT == kFp4) {
+        gsc = __ldg(x.gs) * 128.f;
+        if (FUSED) usc = __ldg(x.gs + 1) * 128.f;
+      }
       if (!(ok = warp_wait(smem_u32(&tfull[buf]), aphase, p.err, 4))) break;
       tc_fence_after();
       const int m = x.mt * 128 + q * 32 + lane;
@@ -512,16 +534,16 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
           const int n = c0 + j;
           if (n < n_here) {
             const size_t row = (size_t)(x.r0 + x.nt * BN + n);
-            const float gv = __uint_as_float(g[j]);
+            const float gv = __uint_as_float(g[j]) * gsc;
             if (ROUTER) {
               if (m < p.m_limit) p.out_f32[row * p.ldo + m] = gv;
             } else if (x.S == 1) {
-              const float o = FUSED ? silu_mul(gv, __uint_as_float(v[j])) : gv;
+              const float o = FUSED ? silu_mul(gv, __uint_as_float(v[j]) * usc) : gv;
               x.out[row * x.M + m] = float_to_bf16_bits(o);
             } else {
               float* pr = x.part + ((size_t)x.ks * x.max_rows + row) * MP;
               pr[m] = gv;
-              if (FUSED) pr[x.M + m] = __uint_as_float(v[j]);
+              if (FUSED) pr[x.M + m] = __uint_as_float(v[j]) * usc;
             }
           }
         }
@@ -578,7 +600,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
     }
     (void)et;
   } else if (INT4) {
-    // ------------------------------------------------------------ INT4 dequant (warps 6..13)
+    // ------------------------------------------------------------ dequant (warps 6..13)
     // A warp may only touch its own quarter of the TMEM lanes (warp % 4), so two warps share
     // each quarter: thread = weight row r = 32 * (warp % 4) + lane.  Fused: warps 6-9 convert
     // the gate tile and warps 10-13 the up tile, each the row's 128 codes of the step (64
@@ -597,7 +619,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
         if (!(ok = warp_wait(smem_u32(&aempty[astage]), a2phase ^ 1, p.err, 7))) break;
         tc_fence_after();
         const uint8_t* raw = smem + stage * C::R1 + C::RAW_OFF + tile * C::RAW_BYTES;
-        const uint32_t s2 = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 8192 + 2 * r));
+        // INT4: one bf16 group scale per row and tile; NVFP4: eight E4M3 block scales (16 k)
+        uint32_t s2 = 0;
+        uint2 s8 = make_uint2(0, 0);
+        if (WT == kInt4) s2 = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 8192 + 2 * r));
+        else s8 = *reinterpret_cast<const uint2*>(raw + 8192 + 8 * r);
         const uint32_t ta = tmem_base + lane_base + C::A_TMEM + (astage * C::NA + tile) * 64;
         // 32-code chunks c0, c0 + 1 of row r -> 32 TMEM columns (pairs in k order)
         auto convert = [&](int c0, uint32_t col) {
@@ -605,12 +631,29 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, INT4>::THREADS, 1)
           const uint4 b = *reinterpret_cast<const uint4*>(raw + ((c0 + 1) * 128 + r) * 16);
           const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
           uint32_t v[32];
+          if (WT == kInt4) {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            v[4 * j + 0] = int4_pair<0>(w[j], s2);
-            v[4 * j + 1] = int4_pair<1>(w[j], s2);
-            v[4 * j + 2] = int4_pair<2>(w[j], s2);
-            v[4 * j + 3] = int4_pair<3>(w[j], s2);
+            for (int j = 0; j < 8; ++j) {
+              v[4 * j + 0] = int4_pair<0>(w[j], s2);
+              v[4 * j + 1] = int4_pair<1>(w[j], s2);
+              v[4 * j + 2] = int4_pair<2>(w[j], s2);
+              v[4 * j + 3] = int4_pair<3>(w[j], s2);
+            }
+          } else {
+            // words 2j', 2j'+1 of the two chunks share block 2 * c0 + j' of the row (16 k)
+            const uint32_t sw = c0 == 0 ? s8.x : s8.y;   // blocks 4*(c0/2) .. +3
+#pragma unroll
+            for (int jb = 0; jb < 4; ++jb) {
+              const uint32_t sp = fp4_scale_pair((sw >> (8 * jb)) & 0xFFu);
+#pragma unroll
+              for (int jj = 0; jj < 2; ++jj) {
+                const int j = 2 * jb + jj;
+                v[4 * j + 0] = fp4_pair<0>(w[j], sp);
+                v[4 * j + 1] = fp4_pair<1>(w[j], sp);
+                v[4 * j + 2] = fp4_pair<2>(w[j], sp);
+                v[4 * j + 3] = fp4_pair<3>(w[j], sp);
+              }
+            }
           }
           tmem_st32(ta + col, v);
         };
@@ -651,42 +694,50 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-template <int BN, bool FUSED, bool INT4, bool ROUTER = false>
+template <int BN, bool FUSED, int WT, bool ROUTER = false>
 int launch_bn(TcParams& kp, cudaStream_t st) {
-  using C = Cfg<BN, FUSED, INT4>;
+  using C = Cfg<BN, FUSED, WT>;
   static bool attr = false;
   if (!attr) {
-    MOE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<BN, FUSED, INT4, ROUTER>,
+    MOE_CUDA_TRY(cudaFuncSetAttribute(tc_gemm_kernel<BN, FUSED, WT, ROUTER>,
                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM));
     attr = true;
   }
-  MOE_LAUNCH_PDL(tc_gemm_kernel<BN, FUSED, INT4, ROUTER>, dim3(sm_count()), dim3(C::THREADS),
+  MOE_LAUNCH_PDL(tc_gemm_kernel<BN, FUSED, WT, ROUTER>, dim3(sm_count()), dim3(C::THREADS),
                  C::SMEM, st, kp);
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;
 }
 
-template <bool INT4>
+template <int WT>
 int dispatch_bn(bool fused, int BN, TcParams& kp, cudaStream_t st) {
   if (fused) {
     switch (BN) {
-      case 32: return launch_bn<32, true, INT4>(kp, st);
-      case 64: return launch_bn<64, true, INT4>(kp, st);
-      case 128: return launch_bn<128, true, INT4>(kp, st);
+      case 32: return launch_bn<32, true, WT>(kp, st);
+      case 64: return launch_bn<64, true, WT>(kp, st);
+      case 128: return launch_bn<128, true, WT>(kp, st);
       default:
-        // INT4 gate/up tiles stop at 128 tokens: their accumulators share tensor memory with
-        // the dequantised weight stages
-        if constexpr (INT4) return launch_bn<128, true, INT4>(kp, st);
-        else return launch_bn<256, true, INT4>(kp, st);
+        // quantised gate/up tiles stop at 128 tokens: their accumulators share tensor memory
+        // with the dequantised weight stages
+        if constexpr (WT != kBf16) return launch_bn<128, true, WT>(kp, st);
+        else return launch_bn<256, true, WT>(kp, st);
     }
   }
   switch (BN) {
-    case 32: return launch_bn<32, false, INT4>(kp, st);
-    case 64: return launch_bn<64, false, INT4>(kp, st);
-    case 128: return launch_bn<128, false, INT4>(kp, st);
-    default: return launch_bn<256, false, INT4>(kp, st);
+    case 32: return launch_bn<32, false, WT>(kp, st);
+    case 64: return launch_bn<64, false, WT>(kp, st);
+    case 128: return launch_bn<128, false, WT>(kp, st);
+    default:
+      if constexpr (WT != kBf16) return launch_bn<128, false, WT>(kp, st);
+      else return launch_bn<256, false, WT>(kp, st);
   }
+}
+
+int dispatch_wt(const GemmArgs& a, int BN, TcParams& kp, cudaStream_t st) {
+  if (a.fp4) return dispatch_bn<kFp4>(a.fused, BN, kp, st);
+  if (a.int4) return dispatch_bn<kInt4>(a.fused, BN, kp, st);
+  return dispatch_bn<kBf16>(a.fused, BN, kp, st);
 }
 
 }  // namespace
@@ -702,7 +753,7 @@ int tc_bn_for(const GemmArgs& a) {
   // the dequantised weight stages); 128-token fused tiles measured faster at every bf16 shape
   // INT4 down tiles also stop at 128 tokens: at 256 the accumulator and the dequantised A
   // stages fill TMEM without a second accumulator buffer, so the epilogue would not overlap
-  const int cap = (a.fused || a.int4) ? 128 : 256;
+  const int cap = (a.fused || a.int4 || a.fp4) ? 128 : 256;
   const int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
   return std::min(bn, cap);
 }
@@ -712,7 +763,8 @@ TcPlan plan_tc(const GemmArgs& a) {
   t.BN = tc_bn_for(a);
   const int A = std::max(1, a.host_n >= 0 ? std::min(a.host_n, a.max_rows)
                                           : std::min(a.E, a.max_rows));
-  const int MT = a.M / 128, KT = a.K / (a.int4 ? 128 : 64), sms = sm_count();
+  const bool q = a.int4 || a.fp4;
+  const int MT = a.M / 128, KT = a.K / (q ? 128 : 64), sms = sm_count();
   const int avg = ceil_div(std::max(a.max_rows, 1), A);
   // narrower token tiles first (more tiles, weights re-read from L2 only), then split K
   while (t.BN > 32 && A * MT * ceil_div(avg, t.BN) < sms &&
@@ -721,7 +773,8 @@ TcPlan plan_tc(const GemmArgs& a) {
   const int ntiles_est = A * MT * std::max(1, ceil_div(avg, t.BN));
   // split K so that the units fill whole waves of the persistent grid: the time of a launch
   // is ~ ceil(units / SMs) waves of 1/S of the K range each; fp32 partial traffic caps S
-  const double wbytes = (double)A * MT * 128 * a.K * (a.int4 ? 0.53 : 2.0) * (a.fused ? 2 : 1);
+  const double wbytes =
+      (double)A * MT * 128 * a.K * (a.fp4 ? 0.56 : a.int4 ? 0.52 : 2.0) * (a.fused ? 2 : 1);
   const double pbytes = (double)a.max_rows * (a.fused ? 2 : 1) * a.M * 8.0;
   const int s_cap = std::min(KT, std::max(1, (int)(wbytes / std::max(pbytes, 1.0) / 4)));
   int S = 1;
@@ -765,6 +818,7 @@ static int fill_params(TcParams& kp, const GemmArgs& a, const TcPlan& t, float* 
   kp.tab = *a.tab;
   kp.dev_tab = a.dev_tab;
   kp.w_off = a.w_off;
+  kp.gs_rel = a.gs_rel;
   kp.K = a.K;
   kp.M = a.M;
   kp.S = t.S;
@@ -783,7 +837,7 @@ int launch_tc(const GemmArgs& a, const TcPlan& t, float* part, int32_t* counters
   TcParams kp{};
   const int r = fill_params(kp, a, t, part, counters, err);
   if (r != MOE_OK) return r;
-  return a.int4 ? dispatch_bn<true>(a.fused, t.BN, kp, st) : dispatch_bn<false>(a.fused, t.BN, kp, st);
+  return dispatch_wt(a, t.BN, kp, st);
 }
 
 TcPair plan_tc_pair(const GemmArgs& a1, const GemmArgs& a2) {
@@ -796,13 +850,13 @@ TcPair plan_tc_pair(const GemmArgs& a1, const GemmArgs& a2) {
   const int A = std::max(1, a1.host_n >= 0 ? std::min(a1.host_n, a1.max_rows)
                                            : std::min(a1.E, a1.max_rows));
   const int avg = ceil_div(std::max(a1.max_rows, 1), A);
-  const int kstep = a1.int4 ? 128 : 64;
+  const int kstep = (a1.int4 || a1.fp4) ? 128 : 64;
   const int KT1 = a1.K / kstep, KT2 = a2.K / kstep;
   const int nt1 = A * (a1.M / 128) * std::max(1, ceil_div(avg, BN));
   const int nt2 = (a2.M / 128) * ceil_div(std::max(a2.max_rows, 1), BN);
   const int nt = nt1 + nt2;
   const double wb = ((double)A * a1.M * a1.K + (double)a2.M * a2.K) *
-                    (a1.int4 ? 0.53 : 2.0) * (a1.fused ? 2 : 1);
+                    (a1.fp4 ? 0.56 : a1.int4 ? 0.52 : 2.0) * (a1.fused ? 2 : 1);
   const double pb = ((double)a1.max_rows * a1.M + (double)a2.max_rows * a2.M) *
                     (a1.fused ? 2 : 1) * 8.0;
   const int s_cap = std::min({KT1, KT2, std::max(1, (int)(wb / std::max(pb, 1.0) / 4))});
@@ -837,6 +891,7 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
       return MOE_ERR_INVALID_ARG;
     kp.g2 = 1;
     kp.w2 = static_cast<const char*>(a2.tab->p[0]) + a2.w_off;
+    kp.gs_rel2 = a2.gs_rel;
     kp.M2 = a2.M;
     kp.K2 = a2.K;
     kp.S2 = pp.t2.S;
@@ -845,8 +900,7 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
     kp.out2 = a2.out;
     kp.part2 = part2;
   }
-  return a1.int4 ? dispatch_bn<true>(a1.fused, pp.t1.BN, kp, st)
-                 : dispatch_bn<false>(a1.fused, pp.t1.BN, kp, st);
+  return dispatch_wt(a1, pp.t1.BN, kp, st);
 }
 
 int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,
@@ -880,7 +934,7 @@ int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad,
   kp.out_f32 = logits;
   kp.ldo = C;
   kp.m_limit = C;
-  return launch_bn<BN, false, false, true>(kp, st);
+  return launch_bn<BN, false, kBf16, true>(kp, st);
 }
 
 }  // namespace moe

@@ -16,6 +16,7 @@ struct TcParams {
   BundleTable tab;
   const void* const* dev_tab;   // device [E] bundle pointers, read instead of tab when set
   size_t w_off;
+  long long gs_rel, gs_rel2;    // NVFP4: matrix scale(s) at section base + gs_rel (group 2: gs_rel2)
   int K, M, S, kt_per_split, max_rows;
   uint16_t* out;
   float* part;

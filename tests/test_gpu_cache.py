@@ -28,9 +28,10 @@ def syn(moe):
     return synthetic
 
 
-def small_stack(layers=4):
+def small_stack(layers=4, wdtype="bf16"):
     return wl.custom("stack", cfg_id=130, H=256, E=16, k=4, I=256, gating="softmax", Is=256,
-                     shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", layers=layers)
+                     shared_gate="sigmoid", zipf_s=1.0, bias_kind="logit", layers=layers,
+                     wdtype=wdtype)
 
 
 def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000, prefetch=0, device_lru=0, copy_kernel=0):
@@ -280,6 +281,29 @@ def test_device_lru_capacity_error_in_the_error_word(moe, syn):
         assert ei.value.status == moe.MOE_ERR_UNSUPPORTED
     finally:
         moe.moe_expert_cache_destroy(cache)
+
+
+@pytest.mark.parametrize("mode", ["host_kernel", "device"])
+def test_cache_nvfp4_bundles(moe, syn, mode):
+    """NVFP4 bundles (codes, block scales and matrix scales in one unit) through the expert
+    cache: the trace follows the simulator and the stacked outputs match the oracle."""
+    cfg = small_stack(wdtype="nvfp4")
+    T, n_slots, steps = 3, 12, 4
+    trace = wl.stream_trace(cfg, T, steps=steps)
+    cache, store, table = make_cache(moe, syn, cfg, n_slots, device_lru=int(mode == "device"),
+                                     copy_kernel=int(mode == "host_kernel"))
+    try:
+        outs, _ = run_stack(moe, syn, cfg, cache, trace, T, steps)
+        got = moe.moe_expert_cache_trace(cache)
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+    sim = LRUSim(n_slots)
+    for s_ in range(steps):
+        for l in range(cfg.layers):
+            sim.request(l, np.unique(trace[s_, l]).tolist())
+    assert got == sim.trace
+    for s_ in (0, steps - 1):
+        assert_close(outs[s_], oracle_stack(cfg, trace, T, s_), f"nvfp4 stack step {s_}")
 
 
 class _DeviceBytes:
