@@ -132,7 +132,8 @@ KERNEL_SOURCES = ["expert_dispatch_streaming_gb300/csrc/tc_gemm.cu",
                   "expert_dispatch_streaming_gb300/csrc/common.cuh"]
 PROFILE_FILES = {("mixtral", 4096, "gate_up_gemm"): "tc_gemm_gate_up_mixtral_T4096.md",
                  ("mixtral", 4096, "down_gemm"): "tc_gemm_down_mixtral_T4096.md",
-                 ("qwen", 8192, "gate_up_gemm"): "tc_gemm_gate_up_qwen_T8192.md"}
+                 ("qwen", 8192, "gate_up_gemm"): "tc_gemm_gate_up_qwen_T8192.md",
+                 ("qwen_nvfp4", 8192, "gate_up_gemm"): "tc_gemm_gate_up_nvfp4_qwen_T8192.md"}
 
 
 def profiled_traffic(workload, T, E, kernel):

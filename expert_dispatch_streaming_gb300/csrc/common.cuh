@@ -137,14 +137,17 @@ __device__ __forceinline__ uint32_t int4_pair_dyn(uint32_t word, int p, uint32_t
 // normal bf16 for every code and every E4M3 scale.  The matrix scale (times 2^7) is applied
 // to the fp32 accumulator.
 
-// (E4M3 scale * 2^119) in both halves.  The E4M3 bits shifted into fp32 position read as
-// scale * 2^-120 (E4M3 and fp32 share the structure up to the bias, 7 against 127, subnormals
-// included); two exact power-of-two multiplies (fp32 subnormals are kept: no flush to zero)
-// give scale * 2^119 <= 448 * 2^119, exact in bf16 (4 significant bits).
-__device__ __forceinline__ uint32_t fp4_scale_pair(uint32_t e4m3) {
-  const float f = __uint_as_float((e4m3 & 0x7Fu) << 20) * 0x1p120f * 0x1p119f;
-  const uint32_t b = float_to_bf16_bits(f);
-  return b | (b << 16);
+// (E4M3 scale * 2^119) in both halves of a bf16 pair, for scale byte jb of `four`: a byte
+// permute puts the byte in both halves, shifted left by 4 it sits in bf16 exponent / mantissa
+// position and reads scale * 2^-120 (E4M3 and bf16 share the structure up to the bias, 7
+// against 127, subnormals included); two exact bf16 multiplies by 2^120 and 2^119 give
+// scale * 2^119 <= 448 * 2^119 (4 significant bits).  The byte's sign bit is clear (packer).
+__device__ __forceinline__ uint32_t fp4_scale_pair(uint32_t four, int jb) {
+  const uint32_t t = __byte_perm(four, 0u, jb | 0x40 | (jb << 8) | 0x4000) << 4;
+  uint32_t a, d;
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(a) : "r"(t), "r"(0x7B807B80u));   // 2^120
+  asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(0x7B007B00u));   // 2^119
+  return d;
 }
 // Pair p (codes 8w + 2p, 8w + 2p + 1 of code word `word`) -> bf16x2 of E2M1 * scale * 2^-7.
 template <int P>

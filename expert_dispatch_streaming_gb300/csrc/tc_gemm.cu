@@ -190,8 +190,33 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// 16-column TMEM load without the wait (tcgen05.wait::ld follows before any use of r).
+__device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+// Waits for this thread's TMEM loads; the loaded registers are tied to the wait so that no
+// use of them is scheduled above it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&a)[16], uint32_t (&b)[16]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]),
+        "+r"(a[7]), "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]),
+        "+r"(a[13]), "+r"(a[14]), "+r"(a[15]), "+r"(b[0]), "+r"(b[1]), "+r"(b[2]), "+r"(b[3]),
+        "+r"(b[4]), "+r"(b[5]), "+r"(b[6]), "+r"(b[7]), "+r"(b[8]), "+r"(b[9]), "+r"(b[10]),
+        "+r"(b[11]), "+r"(b[12]), "+r"(b[13]), "+r"(b[14]), "+r"(b[15])
+      :
+      : "memory");
+}
+
 // Thread i of the warp writes registers r[0..N) into TMEM lane (taddr lane + i), columns
-// taddr column .. +N-1; then waits for the stores to complete.
+// taddr column .. +N-1 (the registers are read at issue); tcgen05.wait::st (tmem_wait_st)
+// must follow before the data is handed to the MMA.
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
@@ -203,6 +228,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
       "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
@@ -516,19 +543,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
       const int m = x.mt * 128 + q * 32 + lane;
       const int n_here = min(BN, x.ne - x.nt * BN);
       const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + buf * C::ACC;
-      // columns per TMEM load: 32, or 16 in the INT4 kernels (more warps, fewer registers)
+      // columns per TMEM load: 32, or 16 in the quantised kernels (more warps, fewer registers)
       constexpr int CH = INT4 ? 16 : 32;
-#pragma unroll 1
-      for (int c0 = 0; c0 < BN; c0 += CH) {
-        if (c0 >= n_here) break;   // warp-uniform
-        uint32_t g[CH], v[CH];
-        if (CH == 32) {
-          tmem_ld32(ta + c0, *reinterpret_cast<uint32_t(*)[32]>(g));
-          if (FUSED) tmem_ld32(ta + BN + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
-        } else {
-          tmem_ld16(ta + c0, g);
-          if (FUSED) tmem_ld16(ta + BN + c0, v);
-        }
+      // write-out of columns c0 .. c0 + CH - 1 (bf16 h / y, fp32 partials, or router logits)
+      // from the registers g (and v: the up accumulator)
+      auto emit = [&](int c0, const uint32_t* g, const uint32_t* v) {
 #pragma unroll
         for (int j = 0; j < CH; ++j) {
           const int n = c0 + j;
@@ -546,6 +565,43 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
               if (FUSED) pr[x.M + m] = __uint_as_float(v[j]) * usc;
             }
           }
+        }
+      };
+      if constexpr (INT4) {
+        // quantised kernels (16-column chunks): the next chunk's TMEM loads are in flight
+        // while this chunk is written out; the accumulator buffer is single here, so the
+        // epilogue is on the MMA's critical path
+        const int nch = (n_here + CH - 1) / CH;   // warp-uniform
+        uint32_t gA[CH], vA[CH], gB[CH], vB[CH];
+#pragma unroll
+        for (int j = 0; j < CH; ++j) vA[j] = vB[j] = 0u;
+        tmem_ld16_nw(ta, gA);
+        if (FUSED) tmem_ld16_nw(ta + BN, vA);
+        tmem_wait_ld(gA, vA);
+#pragma unroll 1
+        for (int c = 0; c < nch; c += 2) {
+          if (c + 1 < nch) {
+            tmem_ld16_nw(ta + (c + 1) * CH, gB);
+            if (FUSED) tmem_ld16_nw(ta + BN + (c + 1) * CH, vB);
+          }
+          emit(c * CH, gA, vA);
+          if (c + 1 >= nch) break;
+          tmem_wait_ld(gB, vB);
+          if (c + 2 < nch) {
+            tmem_ld16_nw(ta + (c + 2) * CH, gA);
+            if (FUSED) tmem_ld16_nw(ta + BN + (c + 2) * CH, vA);
+          }
+          emit((c + 1) * CH, gB, vB);
+          tmem_wait_ld(gA, vA);
+        }
+      } else {
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += CH) {
+          if (c0 >= n_here) break;   // warp-uniform
+          uint32_t g[CH], v[CH];
+          tmem_ld32(ta + c0, g);
+          if (FUSED) tmem_ld32(ta + BN + c0, v);
+          emit(c0, g, v);
         }
       }
       tc_fence_before();
@@ -644,7 +700,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
             const uint32_t sw = c0 == 0 ? s8.x : s8.y;   // blocks 4*(c0/2) .. +3
 #pragma unroll
             for (int jb = 0; jb < 4; ++jb) {
-              const uint32_t sp = fp4_scale_pair((sw >> (8 * jb)) & 0xFFu);
+              const uint32_t sp = fp4_scale_pair(sw, jb);
 #pragma unroll
               for (int jj = 0; jj < 2; ++jj) {
                 const int j = 2 * jb + jj;
@@ -663,6 +719,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
         } else {
           convert(2 * half, 32 * half);
         }
+        tmem_wait_st();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&afull[astage]));

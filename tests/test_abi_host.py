@@ -216,8 +216,13 @@ def test_nvfp4_dequant_product_is_exact(moe):
     assert np.all((f.view(np.uint32) & 0xFFFF) == 0)
     nz = np.abs(prod[prod != 0])
     assert nz.min() >= 2.0 ** -126 and nz.max() < 2.0 ** 127               # normal range
-    # the scale operand itself: s * 2^119 is a finite bf16 for every valid byte
-    B = (s * 2.0 ** 119).astype(np.float32)
+    # the scale operand as the kernel builds it: the byte shifted left by 4 into a bf16 half
+    # reads scale * 2^-120; times 2^120 (exact: back to the scale), times 2^119
+    b = scales.astype(np.uint32)
+    t = ((b << 4) << 16).view(np.float32).astype(np.float64)            # bf16 half as fp32
+    assert np.array_equal(t, moe_ref.decode_e4m3(scales) * 2.0 ** -120)
+    B = (t * 2.0 ** 120 * 2.0 ** 119).astype(np.float32)
+    assert np.array_equal(B.astype(np.float64), moe_ref.decode_e4m3(scales) * 2.0 ** 119)
     assert np.all(np.isfinite(B)) and np.all((B.view(np.uint32) & 0xFFFF) == 0)
 
 
