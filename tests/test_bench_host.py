@@ -60,3 +60,26 @@ def test_profiled_traffic_follows_the_kernel_sources(bench, tmp_path, monkeypatc
     # a changed kernel source invalidates the stored counters
     srcs[0].write_text("// changed\n")
     assert bench.profiled_traffic("mixtral", 4096, 8, "gate_up_gemm") is None
+
+
+@pytest.mark.parametrize("name", ["qwen", "deepseek", "qwen_nvfp4"])
+def test_weight_bytes_follow_the_bundle_size(bench, name):
+    """The bytes per weight that the roofline counts match the packed bundle size of the
+    workload's storage format (within the 256-byte section padding and the 12 bytes of NVFP4
+    matrix scales)."""
+    import expert_dispatch_streaming_gb300 as moe
+    cfg = bench.WORKLOADS[name]
+    nb = moe.moe_bundle_bytes(cfg.H, cfg.I, cfg.wdtype)
+    w = bench.layer_work(cfg, 1, 1)
+    w0 = bench.layer_work(cfg, 1, 0)
+    per_expert = w["bytes"] - w0["bytes"]                 # one more unique routed expert
+    assert abs(per_expert - nb) <= 3 * 256 + 12
+
+
+def test_committed_profiles_are_readable(bench):
+    """Every summary bench.py can read exists and carries both machine-read fields."""
+    for name in bench.PROFILE_FILES.values():
+        path = os.path.join(ROOT, "profiles", name)
+        assert os.path.exists(path), name
+        text = open(path).read()
+        assert "traffic_bytes_per_launch:" in text and "kernel_source_sha256:" in text, name
