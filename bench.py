@@ -366,6 +366,15 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def tier_bound_ms(resident_ms, miss_bytes_per_step, link_gbs):
+    """Lower bound on one streamed decode step from the two memory tiers it crosses ("The
+    Billion-Token Bottleneck", "Tiered Memory": hot experts in HBM, the rest streamed from system
+    RAM over the host link): the step's compute with every bundle resident, and its missed
+    bytes at the probed host-link rate.  Copies that overlap compute perfectly reach the larger
+    of the two."""
+    return max(resident_ms, miss_bytes_per_step / (link_gbs * 1e6))
+
+
 def run_streamed(args, local_rank):
     """Expert-streamed decode: 16 Qwen1.5-MoE-shaped layers, every routed bundle (16.6 GB) in
     pinned host memory, a 4 GiB VRAM slot cache under LRU, 256 decode steps per batch size,
@@ -496,6 +505,10 @@ def run_streamed(args, local_rank):
         finally:
             moe.moe_expert_cache_destroy(full)
         res["resident_ms_per_step"] = round(1e3 * t_res / args.stream_steps, 3)
+        bound = tier_bound_ms(1e3 * t_res / args.stream_steps,
+                              res["bytes_h2d"] / args.stream_steps, probe_gbs)
+        res["tier_bound_ms_per_step"] = round(bound, 3)
+        res["frac_of_tier_bound"] = round(bound / res["ms_per_step"], 4)
         t_copy = copy_ms / 1e3
         res["overlap_fraction"] = (round(min(1.0, max(0.0, 1 - (t_stream - t_res) / t_copy)), 4)
                                    if t_copy > 0 else None)
@@ -571,28 +584,36 @@ def run_streamed(args, local_rank):
             "steps_timed": n_dev}
         out["T"][str(T)] = res
         if T == 8 and args.capacity_sweep:
-            # hit rate and throughput against the slot budget (the LRU thrash cliff): from
-            # a few layers' working set up to every bundle resident
+            # hit rate and throughput against the slot budget (the LRU thrash cliff): from one
+            # layer call's working set (NovaLLM's load-before / free-after-compute mode, "3.
+            # Optimization #1": VRAM holds one layer's experts) up to every bundle resident
             sweep = {}
             steps = min(args.stream_steps, 64)
-            for gib in (1, 2, 4, 8, 16):
-                cap = min(gib << 30, cfg.layers * cfg.E * nb)
-                c2 = make(cap)
+            ws_max = max(int(np.unique(trace[s_, l_]).size)
+                         for s_ in range(steps) for l_ in range(cfg.layers))
+            points = [("layer_working_set", ws_max * nb)]
+            points += [(f"{gib}GiB", min(gib << 30, cfg.layers * cfg.E * nb))
+                       for gib in (1, 2, 4, 8, 16)]
+            for label, cap in points:
                 try:
-                    torch.cuda.synchronize()
-                    e0.record(stream)
-                    run(c2, steps)
-                    e1.record(stream)
-                    stream.synchronize()
-                    t_c = e0.elapsed_time(e1) / 1e3
-                    st2 = moe.moe_expert_cache_stats(c2)
-                    moe.moe_expert_cache_copy_time(c2)
-                finally:
-                    moe.moe_expert_cache_destroy(c2)
-                sweep[f"{gib}GiB"] = {
-                    "slots": cap // nb, "steps": steps,
-                    "hit_rate": round(st2["hits"] / max(1, st2["hits"] + st2["misses"]), 4),
-                    "tokens_per_s": round(T * steps / t_c, 1)}
+                    c2 = make(cap)
+                    try:
+                        torch.cuda.synchronize()
+                        e0.record(stream)
+                        run(c2, steps)
+                        e1.record(stream)
+                        stream.synchronize()
+                        t_c = e0.elapsed_time(e1) / 1e3
+                        st2 = moe.moe_expert_cache_stats(c2)
+                        moe.moe_expert_cache_copy_time(c2)
+                    finally:
+                        moe.moe_expert_cache_destroy(c2)
+                    sweep[label] = {
+                        "slots": cap // nb, "steps": steps,
+                        "hit_rate": round(st2["hits"] / max(1, st2["hits"] + st2["misses"]), 4),
+                        "tokens_per_s": round(T * steps / t_c, 1)}
+                except Exception as exc:          # a point that fails is reported, not fatal
+                    sweep[label] = {"slots": cap // nb, "error": str(exc)[:200]}
             out["capacity_sweep_T8"] = sweep
         del xs, ids_dev, ws
     del store

@@ -83,3 +83,11 @@ def test_committed_profiles_are_readable(bench):
         assert os.path.exists(path), name
         text = open(path).read()
         assert "traffic_bytes_per_launch:" in text and "kernel_source_sha256:" in text, name
+
+
+def test_tier_bound_is_the_slower_tier(bench):
+    # 5.09 GB of misses per step over a 205.5 GB/s link: 24.77 ms, above 2.7 ms of compute
+    assert bench.tier_bound_ms(2.7, 5.09e9, 205.5) == pytest.approx(24.769, rel=1e-4)
+    # few misses: the resident compute bounds the step
+    assert bench.tier_bound_ms(1.6, 91e6, 205.5) == 1.6
+    assert bench.tier_bound_ms(1.6, 0.0, 205.5) == 1.6
