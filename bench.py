@@ -130,37 +130,34 @@ def layer_work(cfg, T, n_unique, shared_merged=False):
 
 KERNEL_SOURCES = ["expert_dispatch_streaming_gb300/csrc/tc_gemm.cu",
                   "expert_dispatch_streaming_gb300/csrc/common.cuh"]
-PROFILE_FILES = {("mixtral", 4096, "gate_up_gemm"): "tc_gemm_gate_up_mixtral_T4096.md",
-                 ("mixtral", 4096, "down_gemm"): "tc_gemm_down_mixtral_T4096.md",
-                 ("qwen", 8192, "gate_up_gemm"): "tc_gemm_gate_up_qwen_T8192.md",
-                 ("qwen_nvfp4", 8192, "gate_up_gemm"): "tc_gemm_gate_up_nvfp4_qwen_T8192.md"}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-def profiled_traffic(workload, T, E, kernel):
-    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu summary of the
-    same workload, or None when there is none or the kernel sources changed since it was taken
-    (the summary records the sources' sha256)."""
-    name = PROFILE_FILES.get((workload, T, kernel))
-    if name is None or E != CANONICAL_E[workload]:
-        return None
-    path = os.path.join(ROOT, "profiles", name)
-    if not os.path.exists(path):
-        return None
-    fields = {}
-    for line in open(path):
-        if ":" in line:
-            key, val = line.strip().split(":", 1)
-            fields[key.strip()] = val.strip()
+def kernel_sources_sha256():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
-    if fields.get("kernel_source_sha256") != h.hexdigest():
+    return h.hexdigest()
+
+
+def profiled_traffic(workload, T, E, kernel):
+    """DRAM bytes (read + write) per launch of `kernel` from the committed ncu capture of the
+    same workload (profiles/traffic.json), or None when there is none or the kernel sources
+    changed since it was taken (each entry records the sources' sha256)."""
+    if E != CANONICAL_E.get(workload) or not os.path.exists(TRAFFIC_FILE):
         return None
     try:
-        return int(fields["traffic_bytes_per_launch"])
-    except (KeyError, ValueError):
+        entries = json.load(open(TRAFFIC_FILE))["entries"]
+    except (ValueError, KeyError):
         return None
+    sha = kernel_sources_sha256()
+    for e in entries:
+        if (e.get("workload"), e.get("T"), e.get("kernel")) == (workload, T, kernel):
+            if e.get("kernel_source_sha256") != sha:
+                return None
+            return int(e["traffic_bytes_per_launch"])
+    return None
 
 
 def roofline_of(flops, nbytes, seconds, pk, sustained=False):
@@ -430,17 +427,22 @@ def run_streamed(args, local_rank):
         ids_dev = torch.from_numpy(trace).to(dev)
         xs = [syn.to_device_bits(wl.stream_tokens(cfg, T, st), dev) for st in range(args.stream_steps)]
         ws = layers[0].workspace(T)
-        bufs = [torch.empty_like(xs[0]) for _ in range(2)]
+        bufs = [torch.empty_like(xs[0]) for _ in range(4)]
+
+        def stack(x0, ids_of, cache):
+            # pre-normalised stack: layer l reads u_l, adds to the residual stream x_l and
+            # writes x_{l+1} and u_{l+1} = rmsnorm(x_{l+1}) (u_0 = x_0)
+            x = u = x0
+            for l in range(cfg.layers):
+                y, un = bufs[l & 1], bufs[2 + (l & 1)]
+                layers[l].forward(u, ws, out=y, forced_ids=ids_of(l), residual=x, cache=cache,
+                                  stream=stream, out_normed=un)
+                x, u = y, un
 
         def run(cache, steps):
             with torch.cuda.stream(stream):
                 for st in range(steps):
-                    x = xs[st]
-                    for l in range(cfg.layers):
-                        y = bufs[l & 1]
-                        layers[l].forward(x, ws, out=y, forced_ids=ids_dev[st, l], residual=x,
-                                          cache=cache, stream=stream)
-                        x = y
+                    stack(xs[st], lambda l: ids_dev[st, l], cache)
 
         res = {}
         cache = make(wl.STREAM_CACHE_BYTES)
@@ -546,12 +548,7 @@ def run_streamed(args, local_rank):
             ids_in = torch.empty_like(ids_dev[0])
 
             def dstep():
-                x = x_in
-                for l in range(cfg.layers):
-                    y = bufs[l & 1]
-                    layers[l].forward(x, ws, out=y, forced_ids=ids_in[l], residual=x,
-                                      cache=dc, stream=stream)
-                    x = y
+                stack(x_in, lambda l: ids_in[l], dc)
 
             with torch.cuda.stream(stream):
                 x_in.copy_(xs[0])

@@ -81,7 +81,7 @@ class moe_layer(C.Structure):
                 ("layer_index", C.c_int), ("shared_gate_sigmoid", C.c_int),
                 ("w_r", C.c_void_p), ("logit_bias", C.c_void_p), ("sel_bias", C.c_void_p),
                 ("w_gate", C.c_void_p), ("shared_bundle", C.c_void_p),
-                ("bundles", C.POINTER(C.c_void_p))]
+                ("bundles", C.POINTER(C.c_void_p)), ("norm_eps", C.c_float)]
 
 
 MOE_N_PHASE_EVENTS = 6
@@ -120,11 +120,12 @@ _SIGS = {
                             _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_route_topk_static": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
                                    _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_route_static_error": (_i, [C.POINTER(C.c_int32), _vp]),
     "moe_permute": (_i, [_vp, _vp, _i, _i, _i, _vp, _vp]),
     "moe_grouped_swiglu_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "moe_grouped_swiglu": (_i, [_vp, _vp, C.POINTER(_vp), _i, _i, _i, _i, _i, _vp, _vp, _sz,
                                 _vp]),
-    "moe_combine": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "moe_combine": (_i, [_vp, _vp, _vp, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _f, _vp]),
     "moe_expert_cache_create": (_i, [C.POINTER(moe_expert_cache_config), C.POINTER(_vp),
                                      C.POINTER(C.c_int64)]),
     "moe_expert_cache_destroy": (_i, [_vp]),
@@ -140,7 +141,7 @@ _SIGS = {
     "moe_expert_cache_sync": (_i, [_vp]),
     "moe_expert_cache_copy_time": (_i, [_vp, C.POINTER(C.c_double), C.POINTER(C.c_int64)]),
     "moe_layer_workspace_size": (_sz, [C.POINTER(moe_layer), _i]),
-    "moe_layer_forward": (_i, [C.POINTER(moe_layer), _vp, _i, _vp, _vp, _vp, _vp,
+    "moe_layer_forward": (_i, [C.POINTER(moe_layer), _vp, _i, _vp, _vp, _vp, _vp, _vp,
                                C.POINTER(moe_layer_stats), _vp, _vp, _vp, _sz, _vp]),
 }
 for _name, (_res, _args) in _SIGS.items():
@@ -264,6 +265,14 @@ def moe_route_topk_static(x, w_r, logit_bias, sel_bias, w_gate, forced_ids, T, H
            "moe_route_topk_static")
 
 
+def moe_route_static_error(stream=None) -> int:
+    """Error word of moe_route_topk_static's fixed scratch on the current device (blocking)."""
+    code = C.c_int32(0)
+    _check(_lib.moe_route_static_error(C.byref(code), stream_handle(stream)),
+           "moe_route_static_error")
+    return code.value
+
+
 def moe_permute(x, src, T, k, H, x_perm, stream=None) -> None:
     _check(_lib.moe_permute(ptr(x), ptr(src), T, k, H, ptr(x_perm), stream_handle(stream)),
            "moe_permute")
@@ -281,9 +290,11 @@ def moe_grouped_swiglu(x_perm, offsets, bundles, E, H, I, wdtype, max_rows, y_pe
                                    ws_bytes, stream_handle(stream)), "moe_grouped_swiglu")
 
 
-def moe_combine(y_perm, pos, w, T, k, H, shared, shared_gate, residual, out, stream=None) -> None:
+def moe_combine(y_perm, pos, w, T, k, H, shared, shared_gate, residual, out, stream=None,
+                out_normed=None, norm_eps=1e-6) -> None:
     _check(_lib.moe_combine(ptr(y_perm), ptr(pos), ptr(w), T, k, H, ptr(shared),
-                            ptr(shared_gate), ptr(residual), ptr(out), stream_handle(stream)),
+                            ptr(shared_gate), ptr(residual), ptr(out), ptr(out_normed),
+                            float(norm_eps), stream_handle(stream)),
            "moe_combine")
 
 
@@ -371,15 +382,18 @@ def moe_layer_workspace_size(layer: moe_layer, T) -> int:
 
 
 def moe_layer_forward(layer: moe_layer, x, T, forced_ids, residual, out, cache, ws, ws_bytes,
-                      stream=None, ids_out=None, w_out=None, phase_events=None) -> moe_layer_stats:
+                      stream=None, ids_out=None, w_out=None, phase_events=None,
+                      out_normed=None) -> moe_layer_stats:
     """phase_events: None or a list of MOE_N_PHASE_EVENTS torch.cuda.Event (recorded by the
-    library on `stream` at phase boundaries)."""
+    library on `stream` at phase boundaries).  out_normed: None or a device [T][H] buffer for
+    the RMS-normalised output (the next layer's input of a pre-norm stack)."""
     st = moe_layer_stats()
     if phase_events is not None:
         arr = (C.c_void_p * MOE_N_PHASE_EVENTS)(*[ev.cuda_event if ev is not None else None
                                                   for ev in phase_events])
         st.phase_events = arr
     _check(_lib.moe_layer_forward(C.byref(layer), ptr(x), T, ptr(forced_ids), ptr(residual),
-                                  ptr(out), cache, C.byref(st), ptr(ids_out), ptr(w_out),
+                                  ptr(out), ptr(out_normed), cache, C.byref(st), ptr(ids_out),
+                                  ptr(w_out),
                                   ptr(ws), ws_bytes, stream_handle(stream)), "moe_layer_forward")
     return st

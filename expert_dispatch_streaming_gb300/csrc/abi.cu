@@ -37,7 +37,11 @@ int sm_count() {
 
 int launch_combine(const uint16_t* y, const int32_t* pos, const float* w, int T, int k, int H,
                    const uint16_t* shared, const float* shared_gate, const uint16_t* residual,
-                   uint16_t* out, cudaStream_t st);
+                   uint16_t* out, uint16_t* out_n, float eps, cudaStream_t st);
+
+// largest row length the fused RMS normalisation of the combine takes (1024 threads x 4
+// vectors of 8 elements)
+constexpr int kMaxNormH = 32768;
 
 static bool valid_route_shape(int T, int H, int E, int k) {
   return T >= 0 && H > 0 && H % 8 == 0 && E > 0 && E <= kMaxExperts && k >= 1 &&
@@ -297,7 +301,9 @@ int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
   RouteScratch s{};
   route_scratch(c, rp, T, E, &s);
   MOE_REQUIRE(c.ok());
-  if (rp.tc) MOE_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int32_t), (cudaStream_t)stream));
+  // the error word (first 4 bytes of ws) starts every call at zero; only the tensor-core
+  // router's bounded waits (T >= 256) can set it
+  MOE_CUDA_TRY(cudaMemsetAsync(err, 0, sizeof(int32_t), (cudaStream_t)stream));
   RouteArgs a{};
   a.x = x; a.w_r = w_r; a.logit_bias = logit_bias; a.sel_bias = sel_bias; a.w_gate = w_gate;
   a.forced = forced_ids; a.T = T; a.H = H; a.E = E; a.k = k; a.gating = gating;
@@ -380,14 +386,16 @@ int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
 
 int moe_combine(const uint16_t* y_perm, const int32_t* pos, const float* w, int T, int k, int H,
                 const uint16_t* shared, const float* shared_gate, const uint16_t* residual,
-                uint16_t* out, void* stream) {
+                uint16_t* out, uint16_t* out_normed, float norm_eps, void* stream) {
   MOE_REQUIRE(T >= 0 && k >= 1 && k <= kMaxK && H > 0 && H % 8 == 0);
+  MOE_REQUIRE(!out_normed || (H <= kMaxNormH && norm_eps >= 0.f));
   if (T == 0) return MOE_OK;
   MOE_REQUIRE(y_perm && pos && w && out && aligned16(y_perm) && aligned16(out));
   MOE_REQUIRE(!shared || aligned16(shared));
   MOE_REQUIRE(!residual || aligned16(residual));
-  return launch_combine(y_perm, pos, w, T, k, H, shared, shared_gate, residual, out,
-                        (cudaStream_t)stream);
+  MOE_REQUIRE(!out_normed || aligned16(out_normed));
+  return launch_combine(y_perm, pos, w, T, k, H, shared, shared_gate, residual, out, out_normed,
+                        norm_eps, (cudaStream_t)stream);
 }
 
 size_t moe_layer_workspace_size(const moe_layer* L, int T) {
@@ -398,9 +406,9 @@ size_t moe_layer_workspace_size(const moe_layer* L, int T) {
 }
 
 int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_t* forced_ids,
-                      const uint16_t* residual, uint16_t* out, moe_expert_cache* cache,
-                      moe_layer_stats* st, int32_t* ids_out, float* w_out, void* ws,
-                      size_t ws_bytes, void* stream) {
+                      const uint16_t* residual, uint16_t* out, uint16_t* out_normed,
+                      moe_expert_cache* cache, moe_layer_stats* st, int32_t* ids_out,
+                      float* w_out, void* ws, size_t ws_bytes, void* stream) {
   LayerPlan P{};
   int r = make_plan(L, T, &P);
   if (r != MOE_OK) return r;
@@ -408,7 +416,8 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   MOE_REQUIRE(!L->Is || L->shared_bundle);
   MOE_REQUIRE(!(L->Is && L->shared_gate_sigmoid) || L->w_gate);
   MOE_REQUIRE(cache || L->bundles);
-  MOE_REQUIRE(!cache || (cache->E == L->E && L->layer_index >= 0 && L->layer_index < cache->L &&
+  MOE_REQUIRE(!cache || (cache_live(cache) && cache->E == L->E && L->layer_index >= 0 &&
+                         L->layer_index < cache->L &&
                          cache->slot_bytes >= P.lay.total_bytes));
   void* const* pev = st ? st->phase_events : nullptr;
   if (st) {
@@ -433,6 +442,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   };
   if (T == 0) return MOE_OK;
   MOE_REQUIRE(x && out && aligned16(x) && aligned16(out));
+  MOE_REQUIRE(!out_normed || (aligned16(out_normed) && L->H <= kMaxNormH && L->norm_eps >= 0.f));
   cudaStream_t s0 = (cudaStream_t)stream;
   WsCursor c(ws, ws_bytes);
   LayerScratch s{};
@@ -519,26 +529,34 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
     for (int e = 0; e < L->E; ++e) used[e] = cache->host_counts[e] > 0;
     const void* ptrs[kMaxExperts];
     std::vector<int> hits, misses, waits;
+    // from the request on, the layer holds slots: a failure releases them before returning
+    // (the release follows whatever this call already enqueued on s0)
+    auto fail_released = [&](int code) {
+      cache_release(cache, L->layer_index, s0);
+      return code;
+    };
     r = cache_request_split(cache, L->layer_index, used, s0, ptrs, &hits, &misses, &waits);
-    if (r != MOE_OK) return r;
+    if (r != MOE_OK) return fail_released(r);
     // hits on bundles a prefetch copied: wait for those copies (usually long done)
     for (int slot : waits) {
-      MOE_CUDA_TRY(cudaStreamWaitEvent(s0, cache->ready[slot], 0));
+      const cudaError_t we = cudaStreamWaitEvent(s0, cache->ready[slot], 0);
+      if (we != cudaSuccess) return fail_released(fail_cuda(we));
       cache->slot_pending[slot] = 0;
     }
     BundleTable tab{};
     for (int e = 0; e < L->E; ++e) tab.p[e] = ptrs[e];
     if (!hits.empty() && (r = run_experts(L, P, s, tab, T, (int)hits.size(), hits.data(), s0,
                                           std::function<int()>())) != MOE_OK)
-      return r;
-    if ((r = phase(3)) != MOE_OK) return r;
+      return fail_released(r);
+    if ((r = phase(3)) != MOE_OK) return fail_released(r);
     if (!misses.empty()) {
-      MOE_CUDA_TRY(cudaStreamWaitEvent(s0, cache->last_copy, 0));
+      const cudaError_t we = cudaStreamWaitEvent(s0, cache->last_copy, 0);
+      if (we != cudaSuccess) return fail_released(fail_cuda(we));
       if ((r = run_experts(L, P, s, tab, T, (int)misses.size(), misses.data(), s0,
                            std::function<int()>())) != MOE_OK)
-        return r;
+        return fail_released(r);
     }
-    if ((r = phase(4)) != MOE_OK) return r;
+    if ((r = phase(4)) != MOE_OK) return fail_released(r);
     if (st) {
       st->n_unique = (int32_t)(hits.size() + misses.size());
       st->n_missed = (int32_t)misses.size();
@@ -546,13 +564,15 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   }
   // A9
   r = launch_combine(s.y_perm, s.pos, s.w, T, L->k, L->H, L->Is ? s.s : nullptr, sgate,
-                     residual, out, s0);
-  if (r != MOE_OK) return r;
+                     residual, out, out_normed, L->norm_eps, s0);
+  if (r != MOE_OK) {
+    if (cache && !cache->device_lru) cache_release(cache, L->layer_index, s0);
+    return r;
+  }
   if ((r = phase(5)) != MOE_OK) return r;
   if (st) st->n_launches = (int32_t)(g_launches - launches0);
   if (cache && !cache->device_lru) {
-    MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[L->layer_index], s0));
-    cache->layer_done_valid[L->layer_index] = 1;
+    if ((r = cache_release(cache, L->layer_index, s0)) != MOE_OK) return r;
     // lookahead: copy the next layer's predicted experts while this layer still computes
     // (after the last-use record above, so a prefetch that evicts one of this layer's slots
     // waits for this layer)

@@ -15,13 +15,17 @@
 //
 // Ordering on the GPU, without any host wait in the steady state:
 //  - a fill of slot s runs on the cache's copy stream after the event recorded when the
-//    layer that last read s released it (write-after-read guard);
+//    layer that last read s released it (write-after-read guard).  A slot whose reader has not
+//    been released yet is never evicted: a request that would evict one is refused
+//    (MOE_ERR_CAPACITY) before it changes anything, so the guard's event always exists;
 //  - each fill records ready[s]; compute work that reads s waits on it (or on last_copy,
 //    which follows every fill issued so far, since fills are serialised on one stream).
 // Every host wait on the GPU is a polling loop with a deadline (MOE_ERR_TIMEOUT).
 #include "cache.h"
 
 #include <chrono>
+#include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <thread>
 #include <vector>
@@ -80,6 +84,7 @@ static void destroy_all(moe_expert_cache* c) {
   if (c->slab) cudaFree(c->slab);
   if (c->host_counts) cudaFreeHost(c->host_counts);
   if (cur >= 0) cudaSetDevice(cur);
+  c->magic = 0;
   delete c;
 }
 
@@ -111,8 +116,55 @@ static int take_slot(moe_expert_cache* c, long long req, int* vl, int* ve) {
   return -1;
 }
 
+// True when processing `used` for `layer` would evict a slot still held by a demand request
+// that has not been released (its reads may still be in flight and no last-use event covers
+// them).  The victims are the keys take_slot would pick: once the free slots are used up, the
+// least-recently-used keys that are not hits of this request.
+static bool evicts_held_slot(const moe_expert_cache* c, int layer, const uint8_t* used) {
+  int n_miss = 0;
+  std::vector<char> hit(c->E, 0);
+  for (int e = 0; e < c->E; ++e) {
+    if (!used[e]) continue;
+    if (c->where.count(key_of(c, layer, e))) hit[e] = 1;
+    else ++n_miss;
+  }
+  int victims = n_miss - (int)c->free_slots.size();
+  for (auto it = c->order.begin(); victims > 0 && it != c->order.end(); ++it) {
+    const long long k = *it;
+    if (k / c->E == layer && hit[k % c->E]) continue;
+    if (c->slot_holder[c->where.at(k).first] >= 0) return true;
+    --victims;
+  }
+  return false;
+}
+
+// Host function of the delay hook: holds the copy stream for the given milliseconds.
+static void CUDART_CB sleep_on_stream(void* ms) {
+  std::this_thread::sleep_for(std::chrono::milliseconds((long)(intptr_t)ms));
+}
+
+// Drops `key` from slot `slot` (the slot becomes free); used when its fill could not be issued.
+static void drop_key(moe_expert_cache* c, long long key, int slot) {
+  auto f = c->where.find(key);
+  if (f != c->where.end()) {
+    c->order.erase(f->second.second);
+    c->where.erase(f);
+  }
+  c->slot_key[slot] = -1;
+  c->slot_pending[slot] = 0;
+  c->slot_prefetched[slot] = 0;
+  c->slot_holder[slot] = -1;
+  c->free_slots.insert(slot);
+}
+
 // One request over the distinct experts of `used` (ascending): the LRU update, slot choice and
 // miss copies shared by demand requests and prefetch requests.
+//
+// A miss whose copy cannot be issued ends the request with MOE_ERR_CUDA: its trace record (the
+// policy's decision, victim included) is kept, the key is then dropped again (its slot is
+// free, as after an explicit eviction), the experts after it are not processed, and the copies
+// of the misses before it are issued as usual.  The trace therefore stays that of the LRU
+// policy applied to the processed prefix followed by an eviction of the failed key.
 static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool prefetch,
                    const void** slot_ptrs, std::vector<int>* hits, std::vector<int>* misses,
                    std::vector<int>* wait_slots) {
@@ -120,6 +172,7 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
   int n_used = 0;
   for (int e = 0; e < c->E; ++e) n_used += used[e] != 0;
   if (n_used > c->n_slots) return MOE_ERR_CAPACITY;
+  if (evicts_held_slot(c, layer, used)) return MOE_ERR_CAPACITY;
   const long long req = c->req++;
   if (prefetch) c->st.prefetch_requests++;
   else c->st.requests++;
@@ -130,6 +183,7 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
   }
   std::vector<char> touched_slot(c->n_slots, 0);
   bool any_miss = false;
+  int status = MOE_OK;
   std::vector<int32_t> fill_key, fill_slot;   // copy_kernel: this request's fills
   for (int e = 0; e < c->E; ++e) {
     if (slot_ptrs) slot_ptrs[e] = nullptr;
@@ -171,21 +225,43 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
       ev.victim_expert = ve;
       if (prefetch) c->st.prefetch_fills++;
       else c->st.misses++;
-      c->st.bytes_h2d += (int64_t)c->slot_bytes;
       // write-after-read guard: the victim's layer must have finished reading this slot
       if (vl >= 0 && c->layer_done_valid[vl])
         MOE_CUDA_TRY(cudaStreamWaitEvent(c->copy, c->layer_done[vl], 0));
-      if (c->copy_kernel) {
-        fill_key.push_back((int32_t)((size_t)layer * c->E + e));   // copied after the loop
-        fill_slot.push_back(slot);
-      } else {
-        const moe_host_bundle& hb = c->bundles[(size_t)layer * c->E + e];
-        MOE_CUDA_TRY(timed_copy_begin(c));
-        MOE_CUDA_TRY(cudaMemcpyAsync(c->slab + (size_t)slot * c->slot_bytes, hb.ptr, hb.bytes,
-                                     cudaMemcpyHostToDevice, c->copy));
-        MOE_CUDA_TRY(timed_copy_end(c));
-        MOE_CUDA_TRY(cudaEventRecord(c->ready[slot], c->copy));
+      const long long nth = ++c->fault_misses;
+      if (nth == c->fault_delay_at)
+        MOE_CUDA_TRY(cudaLaunchHostFunc(c->copy, sleep_on_stream,
+                                        (void*)(intptr_t)c->fault_delay_ms));
+      cudaError_t ce = nth == c->fault_fail_at ? cudaErrorUnknown : cudaSuccess;
+      if (ce == cudaSuccess) {
+        if (c->copy_kernel) {
+          fill_key.push_back((int32_t)((size_t)layer * c->E + e));   // copied after the loop
+          fill_slot.push_back(slot);
+        } else {
+          const moe_host_bundle& hb = c->bundles[(size_t)layer * c->E + e];
+          ce = timed_copy_begin(c);
+          if (ce == cudaSuccess) {
+            ce = cudaMemcpyAsync(c->slab + (size_t)slot * c->slot_bytes, hb.ptr, hb.bytes,
+                                 cudaMemcpyHostToDevice, c->copy);
+            if (ce == cudaSuccess) ce = timed_copy_end(c);
+            if (ce != cudaSuccess && c->time_copies) {   // the timing pair never completed
+              c->pool.push_back(c->timed.back());
+              c->timed.pop_back();
+            }
+          }
+          if (ce == cudaSuccess) ce = cudaEventRecord(c->ready[slot], c->copy);
+        }
       }
+      if (ce != cudaSuccess) {
+        // the decision stands in the trace; the key does not stay resident without its bytes
+        ev.slot = slot;
+        c->trace.push_back(ev);
+        if (!prefetch) c->layer_last[layer].push_back(e);
+        drop_key(c, k, slot);
+        status = fail_cuda(ce);
+        break;
+      }
+      c->st.bytes_h2d += (int64_t)c->slot_bytes;
       c->slot_pending[slot] = prefetch ? 1 : 0;   // a demand miss is waited for via last_copy
       c->slot_prefetched[slot] = prefetch ? 1 : 0;
       any_miss = true;
@@ -196,6 +272,7 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
     if (!prefetch) {
       ls.push_back(slot);
       c->layer_last[layer].push_back(e);
+      c->slot_holder[slot] = layer;   // until the layer is released
     }
     c->trace.push_back(ev);
     if (slot_ptrs) slot_ptrs[e] = c->slab + (size_t)slot * c->slot_bytes;
@@ -216,7 +293,7 @@ static int process(moe_expert_cache* c, int layer, const uint8_t* used, bool pre
   }
   if (any_miss) MOE_CUDA_TRY(cudaEventRecord(c->last_copy, c->copy));
   c->st.resident = (int32_t)c->where.size();
-  return MOE_OK;
+  return status;
 }
 
 int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cudaStream_t compute,
@@ -224,6 +301,14 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
                         std::vector<int>* misses, std::vector<int>* wait_slots) {
   (void)compute;
   return process(c, layer, used, false, slot_ptrs, hits, misses, wait_slots);
+}
+
+int cache_release(moe_expert_cache* c, int layer, cudaStream_t compute) {
+  MOE_CUDA_TRY(cudaEventRecord(c->layer_done[layer], compute));
+  c->layer_done_valid[layer] = 1;
+  for (int& h : c->slot_holder)
+    if (h == layer) h = -1;
+  return MOE_OK;
 }
 
 int cache_prefetch(moe_expert_cache* c, int layer, const uint8_t* mask, int32_t* n_filled) {
@@ -323,9 +408,21 @@ int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache
   c->slot_fill_req.assign(n_slots, -1);
   c->layer_slots.assign(c->L, {});
   c->layer_last.assign(c->L, {});
+  c->slot_holder.assign(n_slots, -1);
   c->slot_pending.assign(n_slots, 0);
   c->slot_prefetched.assign(n_slots, 0);
   c->prefetch_next = cfg->prefetch_next_layer;
+  // failure-test hooks (host LRU only): MOE_TEST_FAIL_COPY=n fails the n-th miss copy,
+  // MOE_TEST_DELAY_COPY=n:ms holds the copy stream for ms milliseconds before the n-th
+  if (const char* f = std::getenv("MOE_TEST_FAIL_COPY")) c->fault_fail_at = std::atoll(f);
+  if (const char* d = std::getenv("MOE_TEST_DELAY_COPY")) {
+    long long n = 0;
+    int ms = 0;
+    if (std::sscanf(d, "%lld:%d", &n, &ms) == 2 && n > 0 && ms > 0) {
+      c->fault_delay_at = n;
+      c->fault_delay_ms = ms;
+    }
+  }
   c->st.n_slots = c->n_slots;
   if (cfg->device_lru || cfg->copy_kernel) {
     c->device_lru = cfg->device_lru ? 1 : 0;
@@ -340,12 +437,13 @@ int moe_expert_cache_create(const moe_expert_cache_config* cfg, moe_expert_cache
       return r;
     }
   }
+  c->magic = kCacheMagic;
   *out = c;
   return MOE_OK;
 }
 
 int moe_expert_cache_destroy(moe_expert_cache* cache) {
-  if (!cache) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache)) return MOE_ERR_INVALID_ARG;
   destroy_all(cache);
   return MOE_OK;
 }
@@ -353,7 +451,7 @@ int moe_expert_cache_destroy(moe_expert_cache* cache) {
 int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* used_mask,
                              void* compute, int defer_waits, const void** slot_ptrs,
                              int32_t* n_missed) {
-  if (!cache) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache)) return MOE_ERR_INVALID_ARG;
   if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   std::vector<int> misses, waits;
   const int r = cache_request_split(cache, layer, used_mask, (cudaStream_t)compute, slot_ptrs,
@@ -373,13 +471,14 @@ int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* 
 
 int moe_expert_cache_prefetch(moe_expert_cache* cache, int layer, const uint8_t* mask,
                               int32_t* n_filled) {
-  if (cache && cache->device_lru) return MOE_ERR_UNSUPPORTED;
+  if (!cache_live(cache)) return MOE_ERR_INVALID_ARG;
+  if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   return cache_prefetch(cache, layer, mask, n_filled);
 }
 
 int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert,
                                  void* compute) {
-  if (!cache || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
+  if (!cache_live(cache) || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
     return MOE_ERR_INVALID_ARG;
   if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   auto f = cache->where.find(key_of(cache, layer, expert));
@@ -394,24 +493,24 @@ int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert,
 }
 
 int moe_expert_cache_release(moe_expert_cache* cache, int layer, void* compute) {
-  if (!cache || layer < 0 || layer >= cache->L) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache) || layer < 0 || layer >= cache->L) return MOE_ERR_INVALID_ARG;
   if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
-  MOE_CUDA_TRY(cudaEventRecord(cache->layer_done[layer], (cudaStream_t)compute));
-  cache->layer_done_valid[layer] = 1;
-  return MOE_OK;
+  return cache_release(cache, layer, (cudaStream_t)compute);
 }
 
 int moe_expert_cache_evict(moe_expert_cache* cache, int layer, int expert) {
-  if (!cache || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
+  if (!cache_live(cache) || layer < 0 || layer >= cache->L || expert < 0 || expert >= cache->E)
     return MOE_ERR_INVALID_ARG;
   if (cache->device_lru) return MOE_ERR_UNSUPPORTED;
   auto f = cache->where.find(key_of(cache, layer, expert));
   if (f == cache->where.end()) return MOE_OK;
+  const int slot = f->second.first;
+  // a slot read by a request that has not been released: its reads may still be enqueued
+  if (cache->slot_holder[slot] >= 0) return MOE_ERR_INVALID_ARG;
   if (cache->layer_done_valid[layer]) {
     const int r = cache_wait_event(cache, cache->layer_done[layer]);
     if (r != MOE_OK) return r;
   }
-  const int slot = f->second.first;
   cache->order.erase(f->second.second);
   cache->where.erase(f);
   cache->slot_key[slot] = -1;
@@ -448,7 +547,7 @@ static int dev_sync_state(moe_expert_cache* c) {
 
 int moe_expert_cache_trace(const moe_expert_cache* cache, moe_cache_event* buf, size_t cap,
                            size_t* n) {
-  if (!cache || !n) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache) || !n) return MOE_ERR_INVALID_ARG;
   if (cache->device_lru) {
     const int r = dev_sync_state(const_cast<moe_expert_cache*>(cache));
     if (r != MOE_OK) return r;
@@ -459,7 +558,7 @@ int moe_expert_cache_trace(const moe_expert_cache* cache, moe_cache_event* buf, 
 }
 
 int moe_expert_cache_reset_trace(moe_expert_cache* cache) {
-  if (!cache) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache)) return MOE_ERR_INVALID_ARG;
   if (cache->device_lru) {
     MOE_CUDA_TRY(cudaDeviceSynchronize());
     MOE_CUDA_TRY(cudaMemset(cache->d_ctl + kTraceN, 0, sizeof(int64_t)));
@@ -469,7 +568,7 @@ int moe_expert_cache_reset_trace(moe_expert_cache* cache) {
 }
 
 int moe_expert_cache_stats(const moe_expert_cache* cache, moe_cache_stats* out) {
-  if (!cache || !out) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache) || !out) return MOE_ERR_INVALID_ARG;
   if (cache->device_lru) {
     const int r = dev_sync_state(const_cast<moe_expert_cache*>(cache));
     if (r != MOE_OK) return r;
@@ -479,13 +578,13 @@ int moe_expert_cache_stats(const moe_expert_cache* cache, moe_cache_stats* out) 
 }
 
 int moe_expert_cache_sync(moe_expert_cache* cache) {
-  if (!cache) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache)) return MOE_ERR_INVALID_ARG;
   MOE_CUDA_TRY(cudaEventRecord(cache->last_copy, cache->copy));
   return cache_wait_event(cache, cache->last_copy);
 }
 
 int moe_expert_cache_copy_time(moe_expert_cache* cache, double* ms, int64_t* n) {
-  if (!cache || !ms || !n) return MOE_ERR_INVALID_ARG;
+  if (!cache_live(cache) || !ms || !n) return MOE_ERR_INVALID_ARG;
   *ms = 0.0;
   *n = 0;
   for (auto& pr : cache->timed) {

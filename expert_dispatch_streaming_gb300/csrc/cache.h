@@ -9,7 +9,12 @@
 
 #include "../../include/moe.h"
 
+// Set by moe_expert_cache_create and cleared just before the object is freed, so that a call
+// on a destroyed cache is refused (best effort: the freed memory may have been reused).
+constexpr uint32_t kCacheMagic = 0x43454F4Du;
+
 struct moe_expert_cache {
+  uint32_t magic = 0;
   int device = 0;
   size_t slot_bytes = 0;
   int n_slots = 0, L = 0, E = 0;
@@ -31,10 +36,18 @@ struct moe_expert_cache {
   std::vector<long long> slot_fill_req;  // request number of the slot's last fill
   std::vector<std::vector<int>> layer_slots;  // slots the layer's last request used
   std::vector<std::vector<int>> layer_last;   // experts of the layer's last (demand) request
+  std::vector<int> slot_holder;          // layer whose demand request reads the slot and has
+                                         // not been released yet, -1 = none
   std::vector<char> slot_pending;        // filled, and no compute has waited for it yet
   std::vector<char> slot_prefetched;     // filled by a prefetch, not yet used by a request
   int prefetch_next = 0;
   int copy_kernel = 0;                   // host LRU: misses copied by slot_fill_kernel
+  // host-side fault hooks for failure tests (0 = off; set at creation from the environment):
+  // the fault_fail_at-th miss copy of this cache fails as if its copy could not be issued, and
+  // the fault_delay_at-th is preceded on the copy stream by a host function sleeping
+  // fault_delay_ms
+  long long fault_misses = 0, fault_fail_at = 0, fault_delay_at = 0;
+  int fault_delay_ms = 0;
   std::vector<moe_cache_event> trace;
   moe_cache_stats st{};
   long long req = 0;
@@ -57,6 +70,7 @@ struct moe_expert_cache {
 };
 
 namespace moe {
+inline bool cache_live(const moe_expert_cache* c) { return c && c->magic == kCacheMagic; }
 int cache_wait_event(moe_expert_cache* c, cudaEvent_t ev);
 // Request with the hit/miss split reported (used by the layer forward).  wait_slots (nullable)
 // receives the slots of hits whose copy (a prefetch) no compute has waited for yet; the caller
@@ -66,6 +80,9 @@ int cache_request_split(moe_expert_cache* c, int layer, const uint8_t* used, cud
                         std::vector<int>* wait_slots = nullptr);
 // Prefetch request (see moe_expert_cache_prefetch); mask NULL = the layer's last expert set.
 int cache_prefetch(moe_expert_cache* c, int layer, const uint8_t* mask, int32_t* n_filled);
+// End of `layer`'s reads of its slots on stream `compute`: records the layer's last-use event
+// (later fills of those slots wait for it) and lets its slots be evicted again.
+int cache_release(moe_expert_cache* c, int layer, cudaStream_t compute);
 
 // ---- copy kernels and the device-side LRU (cache_dev.cu)
 // Builds d_src, the device table of the host bundles' device-visible addresses.

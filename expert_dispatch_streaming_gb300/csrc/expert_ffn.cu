@@ -40,6 +40,7 @@ struct GemmKParams {
   uint16_t* out;
   float* part;
   int32_t* counters;
+  int32_t* err;
   int host_n;
   int16_t host_ids[kMaxExperts];
   BundleTable tab;
@@ -83,7 +84,13 @@ __global__ void __launch_bounds__(128) expert_gemm_kernel(const __grid_constant_
   const int mb = u % p.m_blocks, a = u / p.m_blocks;
   if (a >= (p.host_n >= 0 ? p.host_n : *p.n_active)) return;
   const int e = p.host_n >= 0 ? p.host_ids[a] : p.active[a];
-  const int r0 = p.offsets[e], ne = p.offsets[e + 1] - r0;
+  // the expert's rows, clipped to [0, max_rows) (offsets inconsistent with max_rows are
+  // reported as error 8 instead of indexing past the buffers sized by it)
+  int r0 = min(max(p.offsets[e], 0), p.max_rows);
+  const int ne = max(0, min(p.offsets[e + 1] - p.offsets[e], p.max_rows - r0));
+  if (threadIdx.x == 0 && mb == 0 && split == 0 &&
+      (r0 != p.offsets[e] || ne != p.offsets[e + 1] - p.offsets[e]))
+    atomicExch(p.err, 8);
   const char* bundle = static_cast<const char*>(p.dev_tab ? p.dev_tab[e] : p.tab.p[e]);
   if (ne <= 0 || bundle == nullptr) return;
   const int K = p.K, M = p.M;
@@ -291,6 +298,7 @@ int launch_gemm(const GemmArgs& a, const GemmPlan& g, float* part, int32_t* coun
   kp.w_off = a.w_off; kp.s_off = a.s_off; kp.K = a.K; kp.M = a.M;
   kp.m_blocks = g.m_blocks; kp.splits = g.splits; kp.k_per_split = g.k_per_split;
   kp.max_rows = a.max_rows; kp.out = a.out; kp.part = part; kp.counters = counters;
+  kp.err = err;
   kp.tab = *a.tab;
   kp.dev_tab = a.dev_tab;
   kp.host_n = a.host_n;

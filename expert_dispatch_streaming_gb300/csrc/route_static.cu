@@ -10,7 +10,10 @@
 // The array is a file-scope __device__ variable, so every GPU that loads the library holds it
 // until the process exits.  In host code its name is only a host-side stand-in for the device
 // variable, not a device address: the first call on each device, with that device current,
-// looks the real address up with cudaGetSymbolAddress and keeps it for later calls.
+// looks the real address up with cudaGetSymbolAddress and keeps it for later calls.  The kept
+// address belongs to the device's primary context: after cudaDeviceReset (or anything else that
+// destroys and recreates that context) it is stale, so these entry points must not be used
+// across a device reset.
 #include <mutex>
 
 #include "common.cuh"
@@ -66,4 +69,13 @@ extern "C" int moe_route_topk_static(const uint16_t* x, const float* w_r, const 
   return moe_route_topk(x, w_r, logit_bias, sel_bias, w_gate, forced_ids, T, H, E, k, gating,
                         scale, ids, w, counts, offsets, pos, src, logits, shared_gate,
                         tie_flags, scratch, moe::kStaticRouteScratchBytes, stream);
+}
+
+extern "C" int moe_route_static_error(int32_t* code, void* stream) {
+  if (!code) return MOE_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const int r = moe::static_scratch(&scratch);
+  if (r != MOE_OK) return r;
+  // moe_route_topk keeps its error word in the first 4 bytes of its scratch
+  return moe_workspace_error(scratch, code, stream);
 }

@@ -293,6 +293,18 @@ struct Unit {
   int r0, ne, mt, ks, nt, tile;
 };
 
+// Rows [r0, r0 + ne) of an expert as read from the offsets, clipped to the launch's
+// [0, max_rows) so that offsets inconsistent with max_rows can never index past the buffers
+// sized by it.  Returns true when the clip changed anything (the caller records error 8).
+__device__ __forceinline__ bool clip_rows(int& r0, int& ne, int max_rows) {
+  const int c0 = min(max(r0, 0), max_rows);
+  const int cn = max(0, min(ne, max_rows - c0));
+  const bool changed = c0 != r0 || cn != ne;
+  r0 = c0;
+  ne = cn;
+  return changed;
+}
+
 // Maps unit index u to its (expert, row tile, split, token tile), from the per-expert prefix
 // of unit counts kept in shared memory; units past the routed experts belong to the second
 // group (the shared expert) when there is one.
@@ -335,6 +347,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
     x.max_rows = p.max_rows;
     x.r0 = p.offsets[e];
     x.ne = p.offsets[e + 1] - x.r0;
+    clip_rows(x.r0, x.ne, p.max_rows);
     base = pref[lo];
     tile_base = pref[lo] / p.S;
   }
@@ -402,7 +415,8 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
       int cnt = 0;
       if (a < n_act) {
         const int e = p.host_n >= 0 ? p.host_ids[a] : p.active[a];
-        const int ne = p.offsets[e + 1] - p.offsets[e];
+        int r0 = p.offsets[e], ne = p.offsets[e + 1] - r0;
+        if (clip_rows(r0, ne, p.max_rows)) atomicExch(p.err, 8);
         cnt = MT * p.S * ((ne + BN - 1) / BN);
       }
       int incl = cnt;

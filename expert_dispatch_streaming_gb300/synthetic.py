@@ -80,6 +80,7 @@ class DeviceLayer:
         d.w_gate = self.w_gate.data_ptr() if self.w_gate is not None else None
         d.shared_bundle = self.shared.data_ptr() if self.shared is not None else None
         d.bundles = None if cached else self._ptrs
+        d.norm_eps = wl.STACK_NORM_EPS
         self.desc = d
         self.device = dev
 
@@ -88,12 +89,14 @@ class DeviceLayer:
         return torch.empty(max(n, 256), dtype=torch.uint8, device=self.device)
 
     def forward(self, x: torch.Tensor, ws: torch.Tensor, out=None, forced_ids=None, residual=None,
-                cache=None, stream=None, ids_out=None, w_out=None, phase_events=None):
+                cache=None, stream=None, ids_out=None, w_out=None, phase_events=None,
+                out_normed=None):
         T = x.shape[0]
         if out is None:
             out = torch.empty_like(x)
         st = moe_layer_forward(self.desc, x, T, forced_ids, residual, out, cache, ws, ws.numel(),
-                               stream, ids_out=ids_out, w_out=w_out, phase_events=phase_events)
+                               stream, ids_out=ids_out, w_out=w_out, phase_events=phase_events,
+                               out_normed=out_normed)
         return out, st
 
 

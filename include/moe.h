@@ -73,10 +73,14 @@ int moe_version(void);
 enum moe_option { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_PDL = 2 };
 int moe_set_option(int option, int value);
 
-/* Reads the device error word kept in the first 4 bytes of a moe_layer_forward or
- * moe_grouped_swiglu workspace into *code (host) and waits for `stream`.  0 = no error; a
- * non-zero code means a bounded wait inside a kernel of the last call on that workspace ran
- * out of time and that call's outputs are invalid.  Blocking (test and debug use). */
+/* Reads the device error word kept in the first 4 bytes of a moe_layer_forward,
+ * moe_grouped_swiglu or moe_route_topk workspace into *code (host) and waits for `stream`.
+ * 0 = no error; otherwise the last call on that workspace produced invalid outputs:
+ *   1-7  a bounded wait inside a tensor-core kernel ran out of time;
+ *   8    an expert's row range [offsets[e], offsets[e+1]) reached outside [0, max_rows)
+ *        (moe_grouped_swiglu) and was clipped to it;
+ *   20   a device-LRU cache request needed more distinct bundles than slots.
+ * Blocking (test and debug use). */
 int moe_workspace_error(const void* ws, int32_t* code, void* stream);
 
 /* ------------------------------------------------------------------ enums */
@@ -199,13 +203,21 @@ uint64_t moe_checksum64(const void* data, size_t bytes);
  *             tie_flags [T] int32 or NULL: 0 = the k-th/(k+1)-th selection gap exceeded the
  *             fp32 error margin; 1 = the experts near the boundary were re-scored in fp64;
  *             2 = as 1 and the fp64 gap was still below 1e-6 (a logged near-tie).
- *  ws         device scratch of moe_route_workspace_size(T, H, E, k) bytes.
+ *  ws         device scratch of moe_route_workspace_size(T, H, E, k) bytes.  Its first 4 bytes
+ *             hold an error word, cleared at the start of every call: 0 = no error; non-zero =
+ *             a bounded wait inside the tensor-core router (batches of T >= 256 tokens) ran out
+ *             of time and the call's outputs are invalid.  Read it with moe_workspace_error.
  * Limits: 1 <= k <= min(E, 8), E <= 256, T >= 0 (T == 0 writes zero counts/offsets),
- * H a multiple of 8.  Exact selection: near-boundary experts are re-scored in fp64 on the
- * GPU so that the chosen set equals that of exact arithmetic whenever the exact gap is not
- * a tie.
+ * H a multiple of 8.  Exact selection: experts whose fp32 selection score lies within 1e-4 of
+ * the k-th are re-scored in fp64 on the GPU, so the chosen set equals that of exact arithmetic
+ * (except ties closer than 1e-6, flagged 2) whenever the fp32 logits are within 1e-4 of the
+ * exact ones.  That holds for activations and router weights of the workloads' magnitudes
+ * (|x| ~ N(0, 1), W_r ~ N(0, 0.02), H <= 16384: observed fp32 error below 1e-5); inputs whose
+ * products x[h] * W_r[h][e] are much larger can have fp32 logit errors above the margin, and
+ * a choice near the boundary is then not guaranteed to be the exact one.
  * Defined by: "NovaLLM ...", "2. Why MoE Is a Natural Breakthrough Point" (the router picks a
- * handful of experts per token); histogram / scan / stable rank are the standard dispatch. */
+ * handful of experts per token); the histogram, exclusive scan and stable rank that follow are
+ * the standard counting-sort dispatch, which the pages do not spell out. */
 size_t moe_route_workspace_size(int T, int H, int E, int k);
 int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
                    const float* sel_bias, const uint16_t* w_gate, const int32_t* forced_ids,
@@ -231,17 +243,29 @@ int moe_route_topk(const uint16_t* x, const float* w_r, const float* logit_bias,
  * capture.  Every call on a device shares the one array and it keeps the previous call's
  * contents (the call clears what must start at zero itself): calls that can overlap on the
  * GPU -- on different streams, or from different host threads -- race and must be serialised
- * by the caller. */
+ * by the caller.  The cached address belongs to the device's primary context: do not use this
+ * entry point across cudaDeviceReset.
+ * Errors: as moe_route_topk; a timed-out wait of the tensor-core router (T >= 256) is reported
+ * through the array's error word, read with moe_route_static_error. */
 int moe_route_topk_static(const uint16_t* x, const float* w_r, const float* logit_bias,
                           const float* sel_bias, const uint16_t* w_gate, const int32_t* forced_ids,
                           int T, int H, int E, int k, int gating, float scale, int32_t* ids,
                           float* w, int32_t* counts, int32_t* offsets, int32_t* pos, int32_t* src,
                           float* logits, float* shared_gate, int32_t* tie_flags, void* stream);
+/* Reads the error word of moe_route_topk_static's fixed scratch on the current device into
+ * *code (host) after waiting for `stream`: 0 = the last call on this device ran without error;
+ * non-zero = a bounded wait of the tensor-core router ran out of time and that call's outputs
+ * are invalid.  Blocking.  The same sharing rule applies: a call still running on another
+ * stream can overwrite the word. */
+int moe_route_static_error(int32_t* code, void* stream);
 
 /* ------------------------------------------------------------------ step 4: permute
  * x_perm[p][:] = x[src[p] / k][:] for p in [0, T*k).
  *  x device [T][H] bf16, src device [T*k] int32, x_perm device [T*k][H] bf16.
- * H a multiple of 8. */
+ * H a multiple of 8.  The pages define no permutation step: it is the gather that puts each
+ * expert's tokens next to each other so that every selected expert's weights are read once per
+ * batch ("NovaLLM ...", "3. Optimization #1 -- Expert-Level Streaming" asks only that the
+ * experts a batch hits be loaded and run). */
 int moe_permute(const uint16_t* x, const int32_t* src, int T, int k, int H, uint16_t* x_perm,
                 void* stream);
 
@@ -257,9 +281,16 @@ int moe_permute(const uint16_t* x, const int32_t* src, int T, int k, int H, uint
  *           that receive no rows); copied into the kernel parameters, so the array may be
  *           reused as soon as the call returns
  *  y_perm   device [rows_total][H] bf16
- *  max_rows an upper bound of offsets[E] (T*k), used to size the launch
+ *  max_rows an upper bound of offsets[E] (T*k), used to size the launch; an expert whose rows
+ *           reach outside [0, max_rows) is clipped to it and error 8 is recorded in the
+ *           workspace error word (moe_workspace_error)
  *  ws       device scratch of moe_grouped_swiglu_workspace_size(max_rows, E, H, I, wdtype)
- * Limits: E <= 256, H and I multiples of 128. */
+ * Limits: E <= 256, H and I multiples of 128.
+ * Defined by: "NovaLLM ...", "3. Optimization #1 -- Expert-Level Streaming" (only the experts
+ * the batch selected are touched; each expert is the unit of storage and compute) and
+ * "Running 35B MoE Models on 8GB GPUs ...", "Technical Insight" (INT4 / NVFP4 expert weights
+ * travel with their scales in one bundle).  The SwiGLU form of an expert is that of the
+ * Mixtral-, Qwen1.5-MoE- and DeepSeek-V3-shaped models the workloads follow. */
 size_t moe_grouped_swiglu_workspace_size(int max_rows, int E, int H, int I, int wdtype);
 int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
                        const void* const* bundles, int E, int H, int I, int wdtype,
@@ -269,11 +300,17 @@ int moe_grouped_swiglu(const uint16_t* x_perm, const int32_t* offsets,
  * out[t] = bf16( sum_{j<k} w[t][j] * y_perm[pos[t][j]] + g_t * shared[t] ), fp32 inside,
  * j in order 0..k-1, g_t = shared_gate[t] (1 when shared_gate is NULL; the shared term is
  * skipped when shared is NULL).  If `residual` is not NULL, out[t] = bf16(residual[t] +
- * that bf16 value) (the residual stream of a stacked model).
- *  y_perm device [T*k][H] bf16; pos, w device [T][k]; shared, residual, out device [T][H]. */
+ * that bf16 value) (the residual stream of a stacked model).  If `out_normed` (device [T][H]
+ * bf16) is not NULL it also receives the next layer's input of a pre-norm stack,
+ *   out_normed[t] = bf16( out[t] / sqrt(mean_h out[t][h]^2 + norm_eps) )
+ * computed from the bf16 values of out[t] (sum of squares in fp32); H <= 32768 then.
+ *  y_perm device [T*k][H] bf16; pos, w device [T][k]; shared, residual, out device [T][H].
+ * The pages define no combine step: it is the gate-weighted sum that undoes the permutation,
+ * the usual form of a top-k MoE layer's output. */
 int moe_combine(const uint16_t* y_perm, const int32_t* pos, const float* w, int T, int k,
                 int H, const uint16_t* shared, const float* shared_gate,
-                const uint16_t* residual, uint16_t* out, void* stream);
+                const uint16_t* residual, uint16_t* out, uint16_t* out_normed, float norm_eps,
+                void* stream);
 
 /* ------------------------------------------------------------------ expert-slot cache
  * A fixed pool of VRAM slots, each holding one expert bundle, filled from pinned host
@@ -367,12 +404,16 @@ int moe_expert_cache_destroy(moe_expert_cache* cache);
 /* Makes every expert whose used_mask[e] != 0 resident for `layer`.  used_mask: HOST [E] bytes.
  * On return slot_ptrs[e] (HOST array [E], caller-owned) holds the device address of expert
  * e's bundle for every used e (NULL for unused e).  Misses are copied on the cache's copy
- * stream, each after the previous readers of its slot have finished (write-after-read
- * guard, per-slot last-use events).  If defer_waits == 0, stream `compute` is made to wait
- * for every copied bundle before any work enqueued on it after this call; if defer_waits
- * == 1 the caller adds those waits per expert with moe_expert_cache_wait_expert (so work on
- * hit experts can start while misses are in flight).  n_missed (nullable) receives the
- * number of misses.  Host-side and non-blocking. */
+ * stream, each after the release that ended the reads of the slot's previous bundle
+ * (write-after-read guard: the victim layer's last-use event, see moe_expert_cache_release).
+ * The slots of a request stay held until its layer is released: a request or prefetch that
+ * would have to evict a held slot returns MOE_ERR_CAPACITY and changes nothing, so call
+ * moe_expert_cache_release for a layer before any later request that could evict its slots
+ * (moe_layer_forward releases its layer itself).  If defer_waits == 0, stream `compute` is
+ * made to wait for every copied bundle before any work enqueued on it after this call; if
+ * defer_waits == 1 the caller adds those waits per expert with moe_expert_cache_wait_expert
+ * (so work on hit experts can start while misses are in flight).  n_missed (nullable)
+ * receives the number of misses.  Host-side and non-blocking. */
 int moe_expert_cache_request(moe_expert_cache* cache, int layer, const uint8_t* used_mask,
                              void* compute, int defer_waits, const void** slot_ptrs,
                              int32_t* n_missed);
@@ -385,11 +426,13 @@ int moe_expert_cache_prefetch(moe_expert_cache* cache, int layer, const uint8_t*
                               int32_t* n_filled);
 /* Makes stream `compute` wait until (layer, expert)'s bundle has arrived (no-op for a hit). */
 int moe_expert_cache_wait_expert(moe_expert_cache* cache, int layer, int expert, void* compute);
-/* Marks the end of `layer`'s use of its slots on stream `compute` (records last-use events
- * that later copies into those slots wait for). */
+/* Marks the end of `layer`'s use of its slots on stream `compute`: records the layer's
+ * last-use event, which later copies into those slots wait for, and releases the slots held by
+ * the layer's requests so that they can be evicted again. */
 int moe_expert_cache_release(moe_expert_cache* cache, int layer, void* compute);
-/* Drops (layer, expert) from the cache; no-op when not resident.  Waits (bounded) for the
- * slot's last reader. */
+/* Drops (layer, expert) from the cache; no-op when not resident.  Waits (bounded, else
+ * MOE_ERR_TIMEOUT) for the layer's last release.  MOE_ERR_INVALID_ARG when the bundle's slot
+ * is held by a request whose layer has not been released yet. */
 int moe_expert_cache_evict(moe_expert_cache* cache, int layer, int expert);
 /* Copies up to `cap` trace records (oldest first, since creation or the last reset) into
  * `buf` (host); *n receives the number of records available. */
@@ -419,6 +462,7 @@ typedef struct moe_layer {
   const void* shared_bundle; /* device bundle of the shared expert (H, Is), or NULL      */
   const void* const* bundles;/* HOST array [E] of device bundles (all resident), or NULL
                                 when a cache is attached                                 */
+  float norm_eps;            /* epsilon of the optional RMS-normalised output (out_normed) */
 } moe_layer;
 
 /* Number of phase events moe_layer_forward can record (see moe_layer_stats). */
@@ -445,17 +489,23 @@ size_t moe_layer_workspace_size(const moe_layer* L, int T);
 /* The whole layer forward: out[T][H] (device bf16) from x[T][H] (device bf16).
  *  forced_ids device [T][k] or NULL (routing trace injection, see moe_route_topk)
  *  residual   device [T][H] bf16 or NULL (out = residual + layer output, see moe_combine)
+ *  out_normed device [T][H] bf16 or NULL: out RMS-normalised with L->norm_eps (moe_combine),
+ *             the next layer's input when layers are stacked with pre-normalisation
  *  cache      NULL: every bundle is resident (L->bundles); else bundles come from the cache:
  *             the call reads the layer's expert-use mask back to the host (one small
  *             device-to-host copy and a bounded wait), requests residency, and overlaps the
  *             miss copies with the shared expert and with the experts that hit.
  *  st         host, or NULL (in: phase_events; out: counters).
  *  ids_out, w_out  device [T][k] or NULL: copies of the routing decision.
- * With cache == NULL the call is fully asynchronous. */
+ * With cache == NULL the call is fully asynchronous.
+ * Defined by: "NovaLLM ...", "2. Why MoE Is a Natural Breakthrough Point" and "3. Optimization
+ * #1 -- Expert-Level Streaming" (route, then run only the selected experts, whose weights are
+ * streamed in on demand and overlapped with compute); "Running 35B MoE Models on 8GB GPUs ...",
+ * "Technical Insight" (the cache sits between the router's output and the experts' compute). */
 int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_t* forced_ids,
-                      const uint16_t* residual, uint16_t* out, moe_expert_cache* cache,
-                      moe_layer_stats* st, int32_t* ids_out, float* w_out, void* ws,
-                      size_t ws_bytes, void* stream);
+                      const uint16_t* residual, uint16_t* out, uint16_t* out_normed,
+                      moe_expert_cache* cache, moe_layer_stats* st, int32_t* ids_out,
+                      float* w_out, void* ws, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

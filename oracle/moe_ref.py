@@ -230,6 +230,22 @@ def combine(y_perm: np.ndarray, pos: np.ndarray, w: np.ndarray, shared=None, sha
     return bf16.round_rne(acc)
 
 
+# ----------------------------------------------------------------------------- stacked layers
+
+
+def rms_normalize(x: np.ndarray, eps: float) -> np.ndarray:
+    """u[t] = bf16( x[t] / sqrt(mean_h x[t, h]^2 + eps) ), fp64 inside.
+
+    The input of layer l + 1 of a pre-normalised stack of MoE layers (the residual stream
+    x_{l+1} = x_l + layer_l(u_l) is RMS-normalised, with no learned scale, before each layer
+    after the first).  The pages stream a model layer by layer ("NovaLLM ...", "3. Optimization
+    #1 -- Expert-Level Streaming") but do not say how layers are chained; this is the
+    pre-normalised residual form of the MoE models the workloads follow."""
+    x = np.asarray(x, np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return bf16.round_rne(x / np.sqrt(ms + eps))
+
+
 # ----------------------------------------------------------------------------- whole layer
 
 

@@ -36,7 +36,8 @@ def test_layer_work_counts_the_shared_expert_only_when_merged(bench):
 
 def test_profiled_traffic_follows_the_kernel_sources(bench, tmp_path, monkeypatch):
     import hashlib
-    # a repository copy with two kernel sources and one profile summary
+    import json
+    # a repository copy with two kernel sources and one traffic entry
     srcs = []
     for i, rel in enumerate(bench.KERNEL_SOURCES):
         f = tmp_path / rel
@@ -46,13 +47,15 @@ def test_profiled_traffic_follows_the_kernel_sources(bench, tmp_path, monkeypatc
     h = hashlib.sha256()
     for f in srcs:
         h.update(f.read_bytes())
-    prof = tmp_path / "profiles" / bench.PROFILE_FILES[("mixtral", 4096, "gate_up_gemm")]
-    prof.parent.mkdir(parents=True, exist_ok=True)
-    prof.write_text("# summary\n\n    traffic_bytes_per_launch: 123456\n"
-                    f"    kernel_source_sha256: {h.hexdigest()}\n")
+    side = tmp_path / "profiles" / "traffic.json"
+    side.parent.mkdir(parents=True, exist_ok=True)
+    side.write_text(json.dumps({"entries": [
+        {"workload": "mixtral", "T": 4096, "kernel": "gate_up_gemm", "summary": "x.md",
+         "traffic_bytes_per_launch": 123456, "kernel_source_sha256": h.hexdigest()}]}))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(side))
     assert bench.profiled_traffic("mixtral", 4096, 8, "gate_up_gemm") == 123456
-    # no summary for this workload / size / expert count
+    # no entry for this workload / size / expert count
     assert bench.profiled_traffic("deepseek", 8192, 256, "gate_up_gemm") is None
     assert bench.profiled_traffic("mixtral", 512, 8, "gate_up_gemm") is None
     assert bench.profiled_traffic("mixtral", 4096, 4, "gate_up_gemm") is None
@@ -76,13 +79,15 @@ def test_weight_bytes_follow_the_bundle_size(bench, name):
     assert abs(per_expert - nb) <= 3 * 256 + 12
 
 
-def test_committed_profiles_are_readable(bench):
-    """Every summary bench.py can read exists and carries both machine-read fields."""
-    for name in bench.PROFILE_FILES.values():
-        path = os.path.join(ROOT, "profiles", name)
-        assert os.path.exists(path), name
-        text = open(path).read()
-        assert "traffic_bytes_per_launch:" in text and "kernel_source_sha256:" in text, name
+def test_committed_traffic_entries_are_readable(bench):
+    """Every entry of the traffic sidecar names a committed summary and carries its figures."""
+    import json
+    entries = json.load(open(bench.TRAFFIC_FILE))["entries"]
+    assert entries
+    for e in entries:
+        assert os.path.exists(os.path.join(ROOT, "profiles", e["summary"])), e["summary"]
+        assert int(e["traffic_bytes_per_launch"]) > 0
+        assert len(e["kernel_source_sha256"]) == 64
 
 
 def test_tier_bound_is_the_slower_tier(bench):

@@ -11,7 +11,8 @@ import workloads as wl
 from oracle import bf16, moe_ref
 from oracle.lru_sim import LRUSim, CapacityError
 
-from gpu_util import assert_close
+from gpu_util import (assert_close, check_stack_layers, oracle_stack, run_stack_step,
+                      run_stack_step_recorded, stack_buffers)
 
 pytestmark = pytest.mark.gpu
 
@@ -48,29 +49,22 @@ def make_cache(moe, syn, cfg, n_slots, timeout_ms=5000, prefetch=0, device_lru=0
 def run_stack(moe, syn, cfg, cache, trace, T, steps):
     layers = [syn.DeviceLayer(cfg, layer=l, cached=True) for l in range(cfg.layers)]
     ws = layers[0].workspace(T)
+    bufs = stack_buffers(T, cfg.H)
     outs = []
     n_missed = 0
     for s in range(steps):
-        x = syn.to_device_bits(wl.stream_tokens(cfg, T, s))
+        x = u = syn.to_device_bits(wl.stream_tokens(cfg, T, s))
         for l in range(cfg.layers):
             ids = torch.from_numpy(np.ascontiguousarray(trace[s, l])).cuda()
-            y = torch.empty_like(x)
-            _, st = layers[l].forward(x, ws, out=y, forced_ids=ids, residual=x, cache=cache)
+            y, un = bufs[l & 1], bufs[2 + (l & 1)]
+            _, st = layers[l].forward(u, ws, out=y, forced_ids=ids, residual=x, cache=cache,
+                                      out_normed=un)
             n_missed += st.n_missed
-            x = y
+            x, u = y, un
         torch.cuda.synchronize()
         assert moe.moe_workspace_error(ws) == 0
         outs.append(syn.bits_of(x))
     return outs, n_missed
-
-
-def oracle_stack(cfg, trace, T, step):
-    x = wl.stream_tokens(cfg, T, step)
-    xv = bf16.decode(x)
-    for l in range(cfg.layers):
-        r = moe_ref.layer_forward(cfg, l, bf16.to_bits(xv), forced_ids=trace[step, l])
-        xv = bf16.round_rne(xv + r["out"])
-    return xv
 
 
 @pytest.mark.parametrize("mode", ["host", "host_kernel", "prefetch", "prefetch_kernel", "device"])
@@ -210,29 +204,24 @@ def test_device_lru_stack_replays_as_a_cuda_graph(moe, syn):
     ws = layers[0].workspace(T)
     x_in = torch.empty((T, cfg.H), dtype=torch.int16, device="cuda")
     ids_in = torch.empty((cfg.layers, T, cfg.k), dtype=torch.int32, device="cuda")
-    bufs = [torch.empty_like(x_in) for _ in range(2)]
+    bufs = stack_buffers(T, cfg.H)
     stream = torch.cuda.Stream()
 
-    def step():
-        x = x_in
-        for l in range(cfg.layers):
-            y = bufs[l & 1]
-            layers[l].forward(x, ws, out=y, forced_ids=ids_in[l], residual=x, cache=cache,
+    def step(c):
+        return run_stack_step(layers, ws, x_in, lambda l: ids_in[l], bufs, cache=c,
                               stream=stream)
-            x = y
-        return x
 
     outs = []
     try:
         with torch.cuda.stream(stream):
             x_in.copy_(syn.to_device_bits(wl.stream_tokens(cfg, T, 0)))
             ids_in.copy_(torch.from_numpy(np.ascontiguousarray(trace[0])))
-            y = step()                       # step 0 eagerly (also warms up the launches)
+            y = step(cache)                  # step 0 eagerly (also warms up the launches)
         stream.synchronize()
         outs.append(syn.bits_of(y).copy())
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
-            y = step()
+            y = step(cache)
         for s in range(1, steps):
             with torch.cuda.stream(stream):
                 x_in.copy_(syn.to_device_bits(wl.stream_tokens(cfg, T, s)))
@@ -242,6 +231,7 @@ def test_device_lru_stack_replays_as_a_cuda_graph(moe, syn):
             outs.append(syn.bits_of(y).copy())
         assert moe.moe_workspace_error(ws) == 0
         got = moe.moe_expert_cache_trace(cache)
+        del g                                # its nodes address this cache's memory
     finally:
         moe.moe_expert_cache_destroy(cache)
     sim = LRUSim(n_slots)
@@ -256,7 +246,7 @@ def test_device_lru_stack_replays_as_a_cuda_graph(moe, syn):
             with torch.cuda.stream(stream):
                 x_in.copy_(syn.to_device_bits(wl.stream_tokens(cfg, T, s)))
                 ids_in.copy_(torch.from_numpy(np.ascontiguousarray(trace[s])))
-                y = step()
+                y = step(cache2)
             stream.synchronize()
             assert np.array_equal(syn.bits_of(y), outs[s]), f"step {s}"
     finally:
@@ -332,3 +322,112 @@ def test_filled_slots_hold_the_bundles(moe, syn, copy_kernel):
             assert torch.equal(got, store[cfg.E + e].cpu()), f"expert {e}"
     finally:
         moe.moe_expert_cache_destroy(cache)
+
+
+def test_unreleased_slots_are_not_evicted(moe, syn):
+    """Slots a request handed out stay held until the layer is released: a request (or a
+    prefetch) that would have to evict one is refused before it changes anything, so a fill
+    can never overwrite a bundle whose reads are still enqueued; after the release the same
+    request goes through and the trace is the simulator's."""
+    cfg = small_stack(layers=2)
+    cache, store, table = make_cache(moe, syn, cfg, 2)
+    try:
+        m01 = np.zeros(cfg.E, np.uint8)
+        m01[[1, 2]] = 1
+        moe.moe_expert_cache_request(cache, 0, m01)          # slots 0, 1 held by layer 0
+        m1 = np.zeros(cfg.E, np.uint8)
+        m1[3] = 1
+        before = moe.moe_expert_cache_stats(cache)
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_expert_cache_request(cache, 1, m1)       # would evict (0, 1)
+        assert ei.value.status == moe.MOE_ERR_CAPACITY
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_expert_cache_prefetch(cache, 1, m1)
+        assert ei.value.status == moe.MOE_ERR_CAPACITY
+        with pytest.raises(moe.MoEError) as ei:
+            moe.moe_expert_cache_evict(cache, 0, 2)
+        assert ei.value.status == moe.MOE_ERR_INVALID_ARG
+        assert moe.moe_expert_cache_stats(cache) == before
+        again = np.zeros(cfg.E, np.uint8)
+        again[2] = 1
+        moe.moe_expert_cache_request(cache, 0, again)        # a hit evicts nothing: allowed
+        moe.moe_expert_cache_release(cache, 0)
+        ptrs, nm = moe.moe_expert_cache_request(cache, 1, m1)
+        assert nm == 1
+        moe.moe_expert_cache_release(cache, 1)
+        moe.moe_expert_cache_evict(cache, 0, 2)              # released: allowed
+        moe.moe_expert_cache_sync(cache)
+        got = moe.moe_expert_cache_trace(cache)
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+    sim = LRUSim(2)
+    sim.request(0, [1, 2])
+    sim.request(0, [2])
+    sim.request(1, [3])
+    assert got == sim.trace
+
+
+# ------------------------------------------------------------------ the expert-streamed stack
+# at its stated size: 16 Qwen1.5-MoE-shaped layers, every routed bundle (16.6 GB) in pinned host
+# memory, 2^32 bytes of slots (248), 256 decode steps of the seeded locality trace.
+
+
+@pytest.fixture(scope="module")
+def streamed_store(syn):
+    cfg = wl.STREAMED
+    store, table = syn.host_bundle_table(cfg, cfg.layers)
+    layers = [syn.DeviceLayer(cfg, layer=l, cached=True) for l in range(cfg.layers)]
+    yield cfg, store, table, layers
+    del layers, store
+
+
+@pytest.mark.parametrize("mode", ["host", "device"])
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_streamed_stack_full_size(moe, syn, streamed_store, T, mode):
+    """The cache's whole 256-step trace equals the LRU simulator's bit for bit, the copied bytes
+    are misses x bundle size, and (T = 1 at steps 0 and 255, T = 8 at step 255) every layer of
+    the stack matches the oracle on its own input.  host: the host LRU with misses copied by the
+    fill kernel (the benchmark's default path); device: the LRU on the GPU."""
+    cfg, store, table, layers = streamed_store
+    nb = store.shape[1]
+    n_slots = wl.STREAM_CACHE_BYTES // nb
+    assert nb == 17301504 and n_slots == 248
+    steps = wl.STREAM_STEPS
+    trace = wl.stream_trace(cfg, T, steps=steps)
+    c = moe.moe_expert_cache_config(slot_bytes=nb, capacity_bytes=wl.STREAM_CACHE_BYTES,
+                                    n_layers=cfg.layers, n_experts=cfg.E, bundles=table,
+                                    timeout_ms=20000, verify_checksums=0, device=0,
+                                    device_lru=int(mode == "device"),
+                                    copy_kernel=int(mode == "host"))
+    cache = moe.moe_expert_cache_create(c)
+    check_steps = {0, steps - 1} if T == 1 else ({steps - 1} if T == 8 else set())
+    outs = {}
+    try:
+        ids_dev = torch.from_numpy(trace).cuda()
+        ws = layers[0].workspace(T)
+        bufs = stack_buffers(T, cfg.H)
+        for s in range(steps):
+            x0 = syn.to_device_bits(wl.stream_tokens(cfg, T, s))
+            if s in check_steps:
+                outs[s] = run_stack_step_recorded(syn, layers, ws, x0, lambda l: ids_dev[s, l],
+                                                  bufs, cache=cache)
+            else:
+                run_stack_step(layers, ws, x0, lambda l: ids_dev[s, l], bufs, cache=cache)
+        torch.cuda.synchronize()
+        assert moe.moe_workspace_error(ws) == 0
+        got = moe.moe_expert_cache_trace(cache)
+        stats = moe.moe_expert_cache_stats(cache)
+    finally:
+        moe.moe_expert_cache_destroy(cache)
+    sim = LRUSim(n_slots)
+    for s in range(steps):
+        for l in range(cfg.layers):
+            sim.request(l, np.unique(trace[s, l]).tolist())
+    assert len(got) == len(sim.trace)
+    assert got == sim.trace
+    misses = sum(r[3] for r in sim.trace)
+    assert stats["misses"] == misses and stats["hits"] == len(sim.trace) - misses
+    assert stats["requests"] == steps * cfg.layers
+    assert stats["bytes_h2d"] == misses * nb
+    for s, io in sorted(outs.items()):
+        check_stack_layers(cfg, trace, s, io, what=f"streamed stack T={T} step {s}")

@@ -12,7 +12,7 @@ import torch
 import workloads as wl
 from oracle import bf16, moe_ref
 
-from gpu_util import assert_close, check_ids
+from gpu_util import assert_close, check_ids, spread_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -85,6 +85,8 @@ def _layer_case(syn, cfg, T, rows=None):
     assert np.array_equal(got, syn.bits_of(out2)), "second run differs (nondeterminism)"
     ids = ids.cpu().numpy()
     check_ids(cfg, ids, None, xb)
+    if isinstance(rows, str) and rows == "spread":
+        rows = spread_rows(ids, cfg.E)
     ref = moe_ref.layer_forward(cfg, 0, xb, forced_ids=ids, rows=rows)
     return assert_close(got[ref["rows"]], ref["out"], f"{cfg.name} T={T}")
 
@@ -95,10 +97,10 @@ def test_layer_forward_nvfp4_small(syn, cfg, T):
     _layer_case(syn, cfg, T)
 
 
-@pytest.mark.parametrize("T", [1, 16, 256, 2048])
+@pytest.mark.parametrize("T", [1, 16, 256, 2048, 8192])
 def test_layer_forward_qwen_nvfp4(syn, T):
     """The full Qwen1.5-MoE shape with NVFP4 experts (routed and shared); sampled rows."""
-    _layer_case(syn, wl.QWEN_NVFP4, T, rows=np.arange(min(T, 8)))
+    _layer_case(syn, wl.QWEN_NVFP4, T, rows="spread")
 
 
 def test_every_e4m3_scale_byte(moe, syn):

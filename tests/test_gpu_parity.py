@@ -10,7 +10,7 @@ import torch
 import workloads as wl
 from oracle import bf16, moe_ref
 
-from gpu_util import assert_close, check_ids, oracle_scores
+from gpu_util import assert_close, check_ids, oracle_scores, spread_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -194,6 +194,24 @@ def test_combine(moe):
     assert np.mean(bf16.decode(got) == ref) > 0.98
     ref2 = bf16.round_rne(bf16.decode(res) + ref)
     assert_close(out2.cpu().numpy().view(np.uint16), ref2, "combine+residual")
+    # the RMS-normalised output of a pre-norm stack, from the bf16 values of out itself
+    for H2 in (H, 7168):
+        y2 = wl.bf16_bits_from_f32(rng.standard_normal((T * k, H2)).astype(np.float32))
+        r2 = wl.bf16_bits_from_f32(rng.standard_normal((T, H2)).astype(np.float32))
+        o3 = torch.empty((T, H2), dtype=torch.int16, device="cuda")
+        n3 = torch.empty((T, H2), dtype=torch.int16, device="cuda")
+        moe.moe_combine(d(y2), d(pos), d(w), T, k, H2, None, None, d(r2), o3, out_normed=n3,
+                        norm_eps=1e-6)
+        torch.cuda.synchronize()
+        got3 = o3.cpu().numpy().view(np.uint16)
+        ref3 = bf16.round_rne(bf16.decode(r2) + moe_ref.combine(bf16.decode(y2), pos,
+                                                                w.astype(np.float64)))
+        assert_close(got3, ref3, f"combine+residual H={H2}")
+        refn = moe_ref.rms_normalize(bf16.decode(got3), 1e-6)
+        gotn = bf16.decode(n3.cpu().numpy().view(np.uint16))
+        assert_close(n3.cpu().numpy().view(np.uint16), refn, f"normalised H={H2}")
+        assert np.abs(gotn - refn).max() <= 2 ** -7 * np.abs(refn).max()   # one bf16 step
+        assert np.mean(gotn == refn) > 0.98
 
 
 def _layer_case(syn, cfg, T, rows=None, check_selection=True):
@@ -210,6 +228,8 @@ def _layer_case(syn, cfg, T, rows=None, check_selection=True):
     ids = ids.cpu().numpy()
     if check_selection:
         check_ids(cfg, ids, None, xb)
+    if isinstance(rows, str) and rows == "spread":
+        rows = spread_rows(ids, cfg.E)
     ref = moe_ref.layer_forward(cfg, 0, xb, forced_ids=ids, rows=rows)
     sel = ref["rows"]
     return assert_close(got[sel], ref["out"], f"{cfg.name} T={T}")
@@ -231,9 +251,19 @@ def test_layer_forward_qwen(syn, T):
     _layer_case(syn, wl.QWEN, T)
 
 
-@pytest.mark.parametrize("T", [1, 32])
+@pytest.mark.parametrize("T", [1, 32, 512, 8192])
 def test_layer_forward_deepseek_int4(syn, T):
-    _layer_case(syn, wl.DEEPSEEK, T, rows=np.arange(min(T, 6)))
+    """The DeepSeek-V3-shaped INT4 layer (256 experts, top-8 sigmoid, shared expert) at every
+    batch size of the workload; rows spread over the batch (incl. the last token of the busiest
+    experts, whose ragged last token tile the first rows never reach)."""
+    _layer_case(syn, wl.DEEPSEEK, T, rows="spread")
+
+
+@pytest.mark.parametrize("T", [2048, 8192])
+def test_layer_forward_qwen_large(syn, T):
+    """The Qwen1.5-MoE-shaped layer (60 experts, shared expert) at the large batch sizes of
+    the workload, on rows spread over the batch."""
+    _layer_case(syn, wl.QWEN, T, rows="spread")
 
 
 def test_int4_bundle_with_foreign_scales_fails_parity(moe, syn):

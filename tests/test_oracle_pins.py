@@ -283,6 +283,28 @@ def test_combine_by_hand():
     assert out2.tolist() == [[50.75, 101.0], [23.0, 45.5]]
 
 
+# ----------------------------------------------------------------------------- stack norm
+def test_rms_normalize_by_hand_and_closed_form():
+    # [3, 4]: mean square 12.5, so u = [3, 4] / sqrt(12.5) = [0.8485..., 1.1313...] -> bf16
+    u = moe_ref.rms_normalize(np.array([[3.0, 4.0]]), 0.0)
+    assert u.tolist() == [[0.84765625, 1.1328125]]
+    # a constant row c: c / sqrt(c^2 + eps); with eps the magnitude stays below 1
+    c, eps = 0.001, 1e-6
+    u = moe_ref.rms_normalize(np.full((1, 8), c), eps)
+    assert np.all(u == bf16.round_rne(np.array(c / np.sqrt(c * c + eps))))
+    assert 0.5 < u[0, 0] < 1.0
+    # rows are independent and the result does not depend on the row's scale (eps = 0)
+    x = np.random.default_rng(4).standard_normal((5, 64))
+    assert np.array_equal(moe_ref.rms_normalize(x * 8.0, 0.0), moe_ref.rms_normalize(x, 0.0))
+    assert np.array_equal(moe_ref.rms_normalize(x, 0.0)[2:3], moe_ref.rms_normalize(x[2:3], 0.0))
+
+
+def test_rms_normalize_matches_torch_rms_norm():
+    x = np.random.default_rng(5).standard_normal((7, 256)) * 3.0
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (256,), eps=1e-6)
+    assert np.array_equal(moe_ref.rms_normalize(x, 1e-6), bf16.round_rne(ref.numpy()))
+
+
 # ----------------------------------------------------------------------------- whole layer
 def _tiny(**kw):
     base = dict(H=64, E=6, k=2, I=128, gating="softmax_renorm")

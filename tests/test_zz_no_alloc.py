@@ -78,6 +78,8 @@ def test_static_scratch_matches_workspace_call(moe, cfg, T):
         assert torch.allclose(got["logits"], ref["logits"], rtol=0, atol=1e-5)
         if wg is not None:
             assert torch.allclose(got["sg"], ref["sg"], rtol=0, atol=1e-6)
+        # the fixed array's error word (bounded waits of the tensor-core router) reads clean
+        assert moe.moe_route_static_error() == 0
 
 
 def test_static_scratch_rejects_oversized_request(moe):

@@ -91,6 +91,9 @@ STREAM_STEPS = 256
 STREAM_CACHE_BYTES = 1 << 32
 STREAM_REUSE_P = 0.8
 STREAM_TRACE_ZIPF = 1.1
+# the stack is pre-normalised: layer l >= 1 takes the residual stream RMS-normalised with this
+# epsilon (no learned scale); layer 0 takes the step's unit-scale draw as is
+STACK_NORM_EPS = 1e-6
 
 _CAL_PATH = os.path.join(os.path.dirname(__file__), "calibration.json")
 
