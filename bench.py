@@ -27,10 +27,10 @@ sys.path.insert(0, ROOT)
 
 import workloads as wl  # noqa: E402
 
-WORKLOADS = {"mixtral": wl.MIXTRAL, "qwen": wl.QWEN, "deepseek": wl.DEEPSEEK,
+WORKLOADS = {"tiny": wl.TINY, "mixtral": wl.MIXTRAL, "qwen": wl.QWEN, "deepseek": wl.DEEPSEEK,
              "qwen_nvfp4": wl.QWEN_NVFP4}
 CANONICAL_E = {name: c.E for name, c in WORKLOADS.items()}   # before any --experts override
-WORKLOAD_NAMES = {"mixtral": "Mixtral-8x7B-shaped", "qwen": "Qwen1.5-MoE-A2.7B-shaped",
+WORKLOAD_NAMES = {"tiny": "Tiny", "mixtral": "Mixtral-8x7B-shaped", "qwen": "Qwen1.5-MoE-A2.7B-shaped",
                   "deepseek": "DeepSeek-V3-shaped INT4",
                   "qwen_nvfp4": "Qwen1.5-MoE-A2.7B-shaped NVFP4"}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -202,7 +202,7 @@ def run_ours(args, rank, world, local_rank):
     layer = syn.DeviceLayer(cfg, device=dev)
     stream = torch.cuda.Stream(device=dev)
 
-    def measure(T, steps, warmup, with_e2e):
+    def measure(T, steps, warmup, with_e2e, layer=layer, cfg=cfg):
         xb = wl.tokens(cfg, T)
         x = syn.to_device_bits(xb, dev)
         out = torch.empty_like(x)
@@ -314,6 +314,29 @@ def run_ours(args, rank, world, local_rank):
                           "d2h_bytes_per_step": int(oh.numel() * 2)}
         return res
 
+    names = ["route+dispatch+gather", "shared_expert", "gate_up_gemm", "down_gemm", "combine"]
+
+    def dominant(wname, c, T, r):
+        """Roofline of the larger of the two expert-FFN phases (gate/up or down)."""
+        w = layer_work(c, T, r["n_unique"], r["merged"])
+        share = np.array(r["phase_ms"]) / max(sum(r["phase_ms"]), 1e-9)
+        dom = 2 if share[2] >= share[3] else 3
+        roof = roofline_of(*(w["gu"] if dom == 2 else w["dn"]), r["phase_ms"][dom] / 1e3, pk)
+        roof.update({"kernel": names[dom],
+                     "traffic": profiled_traffic(wname, T, c.E, names[dom]),
+                     "peak_source": pk["source"], "share_of_step": round(float(share[dom]), 4)})
+        return w, roof
+
+    def entry(wname, c, T, r):
+        w, roof = dominant(wname, c, T, r)
+        return {"tokens_per_s": round(r["tokens_per_s"], 1),
+                "ms_per_step": round(r["ms_per_step"], 4), "mode": r["mode"],
+                "eager_ms_per_step": round(r.get("eager_ms_per_step", r["ms_per_step"]), 4),
+                "n_unique": r["n_unique"], "phase_ms": [round(v, 4) for v in r["phase_ms"]],
+                "layer_roofline": roofline_of(w["flops"], w["bytes"], r["ms_per_step"] / 1e3, pk),
+                "gate_up_roofline": roofline_of(*w["gu"], r["phase_ms"][2] / 1e3, pk),
+                "dominant_roofline": roof}
+
     head = measure(args.T, args.steps, args.warmup, True)
     sweep = {}
     if args.sweep:
@@ -321,25 +344,30 @@ def run_ours(args, rank, world, local_rank):
             if T == args.T:
                 continue
             r = measure(T, max(5, min(args.steps, 20)), 3, False)
-            w = layer_work(cfg, T, r["n_unique"], r["merged"])
-            sw = {"tokens_per_s": round(r["tokens_per_s"], 1), "ms_per_step": round(r["ms_per_step"], 4),
-                  "mode": r["mode"], "eager_ms_per_step": round(r.get("eager_ms_per_step", r["ms_per_step"]), 4),
-                  "n_unique": r["n_unique"], "phase_ms": [round(v, 4) for v in r["phase_ms"]],
-                  "layer_roofline": roofline_of(w["flops"], w["bytes"], r["ms_per_step"] / 1e3, pk)}
-            gu_ms = r["phase_ms"][2]
-            sw["gate_up_roofline"] = roofline_of(*w["gu"], gu_ms / 1e3, pk)
-            sweep[str(T)] = sw
+            sweep[str(T)] = entry(args.workload, cfg, T, r)
+    del layer
+    torch.cuda.empty_cache()
 
-    w = layer_work(cfg, args.T, head["n_unique"], head["merged"])
-    names = ["route+dispatch+gather", "shared_expert", "gate_up_gemm", "down_gemm", "combine"]
-    share = np.array(head["phase_ms"]) / max(sum(head["phase_ms"]), 1e-9)
-    dom = 2 if share[2] >= share[3] else 3      # the dominant expert-FFN kernel
-    dom_work = {2: w["gu"], 3: w["dn"]}.get(dom, (w["flops"], w["bytes"]))
-    roof = roofline_of(*dom_work, head["phase_ms"][dom] / 1e3, pk)
-    roof.update({"kernel": names[dom],
-                 "traffic": profiled_traffic(args.workload, args.T, cfg.E, names[dom]),
-                 "peak_source": pk["source"],
-                 "share_of_step": round(float(share[dom]), 4)})
+    # every other workload of the task, each over its batch sizes (weights resident)
+    configs = {}
+    for wname in (args.configs.split(",") if args.configs else []):
+        if wname == args.workload or wname not in WORKLOADS:
+            continue
+        c = WORKLOADS[wname]
+        t0 = time.time()
+        lay = syn.DeviceLayer(c, device=dev)
+        per_t = {}
+        for T in c.Ts:
+            r = measure(T, max(5, min(args.steps, 10)), 3, False, layer=lay, cfg=c)
+            per_t[str(T)] = entry(wname, c, T, r)
+        configs[wname] = {"workload": f"{WORKLOAD_NAMES[wname]} MoE layer forward",
+                          "H": c.H, "E": c.E, "k": c.k, "I": c.I, "Is": c.Is,
+                          "weights": c.wdtype, "setup_s": round(time.time() - t0, 1),
+                          "T": per_t}
+        del lay
+        torch.cuda.empty_cache()
+
+    w, roof = dominant(args.workload, cfg, args.T, head)
     result = {
         "metric": f"MoE-layer tokens/s ({WORKLOAD_NAMES[args.workload]} layer)",
         "value": round(head["tokens_per_s"], 1), "unit": "tokens/s", "n_gpus": world,
@@ -359,6 +387,7 @@ def run_ours(args, rank, world, local_rank):
         "n_unique_experts": head["n_unique"],
         "e2e": head.get("e2e"), "gpu_launches": head["launches"], "clocks": head["clocks"],
         "sweep": sweep,
+        "configs": configs,
     }
     return result
 
@@ -643,6 +672,56 @@ def cpu_baseline(cfg, T_sample=16, reps=1):
                       f"({s:.1f} s per sample)"}
 
 
+def streamed_cpu_baseline(T=1, step=1):
+    """The oracle on one sampled decode step of the expert-streamed stack: the LRU simulator's
+    request for every layer and the oracle's pre-normalised stack of 16 layers (weights of the
+    step's experts generated beforehand: generation is not the oracle's work)."""
+    from oracle import bf16, moe_ref
+    from oracle.lru_sim import LRUSim
+    cfg = wl.STREAMED
+    trace = wl.stream_trace(cfg, T, steps=step + 1)
+    routed = {(l, int(e)): wl.expert(cfg, l, int(e))
+              for l in range(cfg.layers) for e in np.unique(trace[step, l])}
+    shared = {l: wl.expert(cfg, l, 0, shared=True) for l in range(cfg.layers)}
+    getw = lambda layer, e, sh=False: shared[layer] if sh else routed[(layer, e)]  # noqa: E731
+    import expert_dispatch_streaming_gb300 as moe
+    nb = moe.moe_bundle_bytes(cfg.H, cfg.I, cfg.wdtype)
+    t0 = time.perf_counter()
+    sim = LRUSim(wl.STREAM_CACHE_BYTES // nb)
+    x = bf16.decode(wl.stream_tokens(cfg, T, step))
+    u = x
+    for l in range(cfg.layers):
+        sim.request(l, np.unique(trace[step, l]).tolist())
+        r = moe_ref.layer_forward(cfg, l, bf16.to_bits(u), forced_ids=trace[step, l],
+                                  weights=getw)
+        x = bf16.round_rne(x + r["out"])
+        u = moe_ref.rms_normalize(x, wl.STACK_NORM_EPS)
+    sec = time.perf_counter() - t0
+    return {"value": round(T / sec, 3), "unit": "tokens/s", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"one decode step (step {step}, T={T}) of the 16-layer stack: the LRU "
+                      f"simulator's 16 requests and the fp64 oracle's layers ({sec:.1f} s)"}
+
+
+def free_port():
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def launch_replicas(n, argv):
+    """Runs this script as n ranks on this node (one process per GPU) through
+    torch.distributed.run, rendezvous on 127.0.0.1; rank 0 prints the JSON line.  Returns the
+    launcher's exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr", "127.0.0.1",
+           "--master-port", str(free_port()), os.path.abspath(__file__), *argv]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -654,6 +733,8 @@ def main():
                     help="override the routed expert count (smaller profiling cases)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-sweep", dest="sweep", action="store_false")
+    ap.add_argument("--configs", default="qwen,deepseek,qwen_nvfp4",
+                    help="other workloads measured over their batch sizes ('' = none)")
     ap.add_argument("--no-cpu", dest="cpu", action="store_false")
     ap.add_argument("--ffn-kernel", default="auto", choices=["auto", "stream", "tcgen05"])
     ap.add_argument("--pdl", action="store_true",
@@ -670,6 +751,9 @@ def main():
         args.T = max(WORKLOADS[args.workload].Ts)
     if args.experts:
         WORKLOADS[args.workload] = WORKLOADS[args.workload].with_(E=args.experts)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # N replicas, one process per GPU, as torchrun would start them
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -694,7 +778,7 @@ def main():
         tot = float(np.sum(secs))
         v = T_s * args.steps / tot
         line = {"metric": f"MoE-layer tokens/s ({WORKLOAD_NAMES[args.workload]} layer)", "value": round(v, 3),
-                "unit": "tokens/s", "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+                "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(1e3 * tot / args.steps, 2), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "impl": "reference",
@@ -712,14 +796,21 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_ours(args, rank, world, local_rank)
-    if args.streamed:
+    if args.streamed and rank == 0:
+        # the streamed decode pins every bundle of the stack (16.6 GB) in host memory: it runs
+        # on rank 0 only (one replica's figure), not once per rank
         res["streamed_decode"] = run_streamed(args, local_rank)
+        if world > 1:
+            res["streamed_decode"]["ranks"] = "rank 0 only"
+        if args.cpu:
+            res["streamed_decode"]["cpu_baseline"] = streamed_cpu_baseline()
     if rank == 0:
         if args.cpu:
             res["cpu_baseline"] = cpu_baseline(cfg)
         print(json.dumps(res))
     if world > 1:
         import torch
+        torch.distributed.barrier()
         torch.distributed.destroy_process_group()
 
 

@@ -57,3 +57,23 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.job_throughput(100, 1, 0.5) == 200.0
+
+
+@pytest.mark.timeout(600)
+def test_bench_gpus_2_launches_two_ranks_and_prints_one_line():
+    """`bench.py --gpus 2` without a launcher environment starts two ranks itself (as
+    torch.distributed.run would, rendezvous on 127.0.0.1); on the reference arm rank 0 alone
+    runs and prints, the other rank exits 0 without work."""
+    import json
+    import subprocess
+    env = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "tiny", "--gpus", "2", "--steps", "1", "--warmup", "0"],
+                       capture_output=True, text=True, timeout=540, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
