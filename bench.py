@@ -227,12 +227,14 @@ def run_ours(args, rank, world, local_rank):
         t1 = torch.cuda.Event(enable_timing=True)
         launches = 0
         merged = False
+        fused = False
         with ClockSampler(local_rank) as clk:
             t0.record(stream)
             for i in range(steps):
                 _, st = layer.forward(x, ws, out, stream=stream, phase_events=evs[i])
                 launches += st.n_launches
                 merged = bool(st.shared_merged)
+                fused = bool(st.fused_decode)
             t1.record(stream)
             stream.synchronize()
         torch.cuda.synchronize()
@@ -243,6 +245,7 @@ def run_ours(args, rank, world, local_rank):
                        for i in range(steps)])
         res = dict(T=T, ms_per_step=ms / steps, tokens_per_s=job_throughput(T * steps, world, ms / 1e3),
                    n_unique=n_unique, phase_ms=ph.mean(0).tolist(), launches=launches, merged=merged,
+                   fused=fused,
                    clocks=clk.summary(), mode="eager")
         if args.graph:
             # the same call captured once in a CUDA graph (a resident-layer call is fully
@@ -317,8 +320,14 @@ def run_ours(args, rank, world, local_rank):
     names = ["route+dispatch+gather", "shared_expert", "gate_up_gemm", "down_gemm", "combine"]
 
     def dominant(wname, c, T, r):
-        """Roofline of the larger of the two expert-FFN phases (gate/up or down)."""
+        """Roofline of the larger of the two expert-FFN phases (gate/up or down); with the
+        fused decode kernel, of that one launch (the whole layer)."""
         w = layer_work(c, T, r["n_unique"], r["merged"])
+        if r.get("fused"):
+            roof = roofline_of(w["flops"], w["bytes"], sum(r["phase_ms"]) / 1e3, pk)
+            roof.update({"kernel": "decode_layer_kernel (whole layer)", "traffic": None,
+                         "peak_source": pk["source"], "share_of_step": 1.0})
+            return w, roof
         share = np.array(r["phase_ms"]) / max(sum(r["phase_ms"]), 1e-9)
         dom = 2 if share[2] >= share[3] else 3
         roof = roofline_of(*(w["gu"] if dom == 2 else w["dn"]), r["phase_ms"][dom] / 1e3, pk)
@@ -334,7 +343,8 @@ def run_ours(args, rank, world, local_rank):
                 "eager_ms_per_step": round(r.get("eager_ms_per_step", r["ms_per_step"]), 4),
                 "n_unique": r["n_unique"], "phase_ms": [round(v, 4) for v in r["phase_ms"]],
                 "layer_roofline": roofline_of(w["flops"], w["bytes"], r["ms_per_step"] / 1e3, pk),
-                "gate_up_roofline": roofline_of(*w["gu"], r["phase_ms"][2] / 1e3, pk),
+                "gate_up_roofline": (roofline_of(*w["gu"], r["phase_ms"][2] / 1e3, pk)
+                                     if r["phase_ms"][2] > 0 else None),
                 "dominant_roofline": roof}
 
     head = measure(args.T, args.steps, args.warmup, True)

@@ -89,7 +89,8 @@ MOE_N_PHASE_EVENTS = 6
 
 class moe_layer_stats(C.Structure):
     _fields_ = [("n_unique", C.c_int32), ("n_missed", C.c_int32), ("n_launches", C.c_int32),
-                ("shared_merged", C.c_int32), ("phase_events", C.POINTER(C.c_void_p))]
+                ("shared_merged", C.c_int32), ("fused_decode", C.c_int32),
+                ("phase_events", C.POINTER(C.c_void_p))]
 
 
 # ----------------------------------------------------------------------------- loading
@@ -187,6 +188,7 @@ def _check(status, fn):
 # ----------------------------------------------------------------------------- API
 MOE_OPT_FFN_KERNEL = 1
 MOE_OPT_PDL = 2
+MOE_OPT_DECODE_KERNEL = 3
 FFN_KERNEL = {"auto": 0, "stream": 1, "tcgen05": 2}
 
 
@@ -197,6 +199,11 @@ def moe_set_option(option, value) -> None:
 def set_ffn_kernel(name: str) -> None:
     """'auto' | 'stream' (mma.sync weight streaming) | 'tcgen05' (tensor-core kernel)."""
     moe_set_option(MOE_OPT_FFN_KERNEL, FFN_KERNEL[name])
+
+
+def set_decode_kernel(on: bool) -> None:
+    """The fused decode kernel for small batches with resident bundles (default on)."""
+    moe_set_option(MOE_OPT_DECODE_KERNEL, 1 if on else 0)
 
 
 def set_pdl(on: bool) -> None:

@@ -8,6 +8,7 @@
 
 #include "cache.h"
 #include "common.cuh"
+#include "decode.cuh"
 #include "expert_ffn.cuh"
 #include "route.cuh"
 #include "tc_gemm.cuh"
@@ -15,6 +16,7 @@
 namespace moe {
 
 static thread_local int g_last_cuda = 0;
+int g_decode_path = 1;   // MOE_OPT_DECODE_KERNEL
 int g_use_pdl = 0;
 thread_local long long g_launches = 0;
 
@@ -56,6 +58,7 @@ struct LayerScratch {
   uint16_t *x_perm, *h, *y_perm, *h_s, *s;
   float* part;
   float* part_s;    // split-K partials of the shared expert when it shares a launch
+  float *dec_rpart, *dec_gpart, *dec_dpart, *dec_ss;   // fused decode kernel scratch
   int32_t* counters;
   int32_t* err;     // device error word (first bytes of the workspace)
   size_t ctl_bytes; // bytes of the control block at the start of the workspace
@@ -67,6 +70,7 @@ struct LayerPlan {
   moe_bundle_layout lay, slay;
   int merged;        // routed and shared expert share one tcgen05 launch per GEMM
   TcPair mgu, mdn;
+  DecodePlan dec;    // the fused decode kernel (small batches, resident bundles)
 };
 
 static GemmArgs gemm_args(const moe_bundle_layout& lay, int wdtype, bool fused, int K, int M,
@@ -114,6 +118,8 @@ static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
       P->mdn = plan_tc_pair(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows), sdn);
     }
   }
+  P->dec = plan_decode(T, L->H, L->E, L->k, L->I, L->Is, L->wdtype,
+                       L->Is > 0 && L->shared_gate_sigmoid);
   return MOE_OK;
 }
 
@@ -125,7 +131,7 @@ static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, 
   z.err = c.take<int32_t>(64);
   size_t ce = std::max({P.gu.counter_elems, P.dn.counter_elems, P.sgu.counter_elems,
                         P.sdn.counter_elems, P.mgu.t1.counter_elems, P.mdn.t1.counter_elems,
-                        (size_t)1});
+                        P.dec.ok ? P.dec.ctl_words : (size_t)1, (size_t)1});
   z.counters = c.take<int32_t>(ce);
   z.ctl_bytes = c.used;
   route_scratch(c, P.rp, T, L->E, &z.rs);
@@ -148,6 +154,16 @@ static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, 
                         P.mgu.t1.part_elems, P.mdn.t1.part_elems, (size_t)1});
   z.part = c.take<float>(pe);
   z.part_s = c.take<float>(std::max({P.mgu.t2.part_elems, P.mdn.t2.part_elems, (size_t)1}));
+  if (P.dec.ok) {
+    z.dec_rpart = c.take<float>((size_t)P.dec.S * T * P.dec.C);
+    z.dec_gpart = c.take<float>(P.dec.gpart_elems);
+    z.dec_dpart = c.take<float>(P.dec.dpart_elems);
+    z.dec_ss = c.take<float>((size_t)P.dec.NB * T + 1);
+    if (!L->Is) {   // the decode kernel's shared-expert buffers are never read without one
+      z.h_s = nullptr;
+      z.s = nullptr;
+    }
+  }
   if (s) *s = z;
   return c.used;
 }
@@ -256,6 +272,11 @@ int moe_set_option(int option, int value) {
   if (option == MOE_OPT_FFN_KERNEL) {
     if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
     g_ffn_path = value;
+    return MOE_OK;
+  }
+  if (option == MOE_OPT_DECODE_KERNEL) {
+    if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+    g_decode_path = value;
     return MOE_OK;
   }
   if (option == MOE_OPT_PDL) {
@@ -451,6 +472,40 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   MOE_CUDA_TRY(cudaMemsetAsync(s.err, 0, s.ctl_bytes, s0));
 
   if ((r = phase(0)) != MOE_OK) return r;
+  if (!cache && P.dec.ok && g_decode_path && (!L->Is || (s.h_s && s.s))) {
+    // small batch, every bundle resident: the whole layer in one cooperative launch
+    DecodeArgs da{};
+    da.x = x; da.residual = residual; da.forced = forced_ids; da.w_r = L->w_r;
+    da.logit_bias = L->logit_bias; da.sel_bias = L->sel_bias;
+    da.w_gate = (L->Is && L->shared_gate_sigmoid) ? L->w_gate : nullptr;
+    da.T = T; da.H = L->H; da.E = L->E; da.k = L->k; da.I = L->I; da.Is = L->Is;
+    da.gating = L->gating; da.wdtype = L->wdtype;
+    da.shared_sigmoid = (L->Is && L->shared_gate_sigmoid) ? 1 : 0;
+    da.scale = L->scale; da.eps = L->norm_eps;
+    for (int e = 0; e < L->E; ++e) da.tab.p[e] = L->bundles[e];
+    da.shared = L->shared_bundle; da.lay = P.lay; da.slay = P.slay;
+    da.out = out; da.out_n = out_normed;
+    da.ids = s.ids; da.counts = s.counts; da.offsets = s.offsets; da.pos = s.pos; da.src = s.src;
+    da.tie = s.tie; da.active = s.rs.active; da.n_active = s.rs.n_active; da.w = s.w;
+    da.shared_gate = s.shared_gate;
+    da.part = s.dec_rpart; da.gpart = s.dec_gpart; da.dpart = s.dec_dpart; da.ss = s.dec_ss;
+    da.h = s.h; da.y = s.y_perm; da.hs = s.h_s; da.ys = s.s;
+    da.ctl = s.counters; da.err = s.err;
+    if ((r = launch_decode(da, P.dec, s0)) != MOE_OK) return r;
+    for (int i = 1; i < MOE_N_PHASE_EVENTS; ++i)
+      if ((r = phase(i)) != MOE_OK) return r;
+    if (st) {
+      st->fused_decode = 1;
+      st->n_launches = (int32_t)(g_launches - launches0);
+    }
+    if (ids_out)
+      MOE_CUDA_TRY(cudaMemcpyAsync(ids_out, s.ids, sizeof(int32_t) * T * L->k,
+                                   cudaMemcpyDeviceToDevice, s0));
+    if (w_out)
+      MOE_CUDA_TRY(cudaMemcpyAsync(w_out, s.w, sizeof(float) * T * L->k,
+                                   cudaMemcpyDeviceToDevice, s0));
+    return MOE_OK;
+  }
   // A1-A4: route, dispatch and gather into expert order
   RouteArgs ra{};
   ra.x = x; ra.w_r = L->w_r; ra.logit_bias = L->logit_bias; ra.sel_bias = L->sel_bias;

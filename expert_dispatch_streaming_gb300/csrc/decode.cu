@@ -1,0 +1,998 @@
+// Fused small-batch (decode) layer forward: the whole MoE layer for T <= 16 tokens with every
+// bundle resident, in one cooperative launch.
+//
+// At decode batch sizes a layer moves a few hundred MB of expert weights and does almost no
+// arithmetic per byte, so the bound is HBM bandwidth ("The Billion-Token Bottleneck", "The
+// Engineering Challenge": MoE trades compute-bound problems for IO-bound ones) -- and, with
+// six dependent launches per layer, the latency of each launch boundary ("NovaLLM: Running
+// Massive MoE Models Fully In-Memory", "Optimization #2": memory bandwidth and kernel launch
+// overhead).  Here one persistent grid does everything and the steps meet at counters in
+// global memory instead of at kernel boundaries:
+//
+//   router    CTA b < S sums the router product over one H slice for all tokens (fp32
+//             partials); CTA t < T then sums token t's partials and gates it (the same
+//             device code as the routing kernels: top-k with fp64 re-scoring near the
+//             boundary); the last token to be gated builds the histogram, scan and stable
+//             ranks and raises a flag;
+//   experts   CTA units over one 128-row weight tile and a range of K: shared-expert gate/up
+//             (needs no routing, so it streams while routing runs), routed gate/up (after the
+//             flag), shared and routed down (each after the gate/up tiles of its expert).  A
+//             producer warp streams the unit's weight tiles with bulk asynchronous copies into
+//             a six-slot 216 KB shared-memory ring (full / empty mbarriers per slot); eight
+//             consumer warps each multiply 16 of the tile's rows on mma.m16n8k16 (weights as
+//             the M side, tokens on the narrow N side, INT4 / NVFP4 dequantised in registers).
+//             A unit's K range may be split: the last split to arrive sums the partials in
+//             split order;
+//   combine   per token, 256 columns per warp, once every down tile of the block has landed:
+//             the gate-weighted sum, the shared term and the residual, and the block's sum of
+//             squares; the optional RMS-normalised output once every block of the token is in.
+//
+// Every sum runs in a fixed order, so results do not depend on scheduling.  A warp waits only
+// for units of earlier steps, every CTA is resident (cooperative launch), and every wait is
+// bounded by the wall clock (~2 s): on timeout the kernel records error 9 in the workspace
+// error word, every later wait gives up at once, and the producer waits (bounded) for the
+// copies it issued before the CTA leaves.
+#include "decode.cuh"
+#include "gate.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kConsumerWarps = 8;                    // 8 x 16 = the 128 rows of a weight tile
+constexpr int kDecThreads = 32 * (kConsumerWarps + 1);   // + one producer warp
+constexpr int kColBlock = 256;                       // columns of a combine / norm unit
+constexpr unsigned long long kWaitNs = 2000000000ull;
+constexpr int32_t kErrDecodeWait = 9;
+constexpr int kSlots = 6;                            // ring slots per CTA
+constexpr int kBOff = 32768;                         // token rows after the weight tiles
+constexpr int kBRowMax = 256 + 16;                   // bytes of one token row's k range (+pad)
+constexpr int kSlotBytes = kBOff + kDecodeMaxT * kBRowMax;
+constexpr int kMaxSlices = 64;                       // router H slices
+constexpr int kSmemBytes = kSlots * kSlotBytes;      // the ring (the routing scratch aliases it)
+static_assert(sizeof(TailSmem) <= (size_t)kSmemBytes, "routing scratch fits in the ring");
+
+// control words: every counter that warps poll sits on its own 128-byte line (kLine words)
+constexpr int kLine = 32;
+enum : int {
+  kCtlRouterArrive = 0,
+  kCtlGateArrive = kLine,
+  kCtlRouteDone = 2 * kLine,
+  kCtlHead = 3 * kLine
+};
+
+struct DecParams {
+  GateParams g;
+  const uint16_t* x;
+  const uint16_t* w_gate;       // router column E: the shared-expert gate vector, or NULL
+  const uint16_t* residual;
+  uint16_t* out;
+  uint16_t* out_n;
+  float eps;
+  int32_t *counts, *offsets, *pos, *src, *active, *n_active;
+  BundleTable tab;
+  const char* shared;
+  int T, H, k, I, Is, shared_sigmoid;
+  long long gu_off, dn_off, gs_off, gu_off_s, dn_off_s, gs_off_s;   // bundle byte offsets
+  uint16_t *h, *y, *hs, *ys;
+  float *rpart, *gpart, *dpart, *ss;   // rpart: router partials [S][T][C] (= g.part)
+  int32_t *ctl, *err;
+  int S, hps, Umax, Sg, Sd, Sgs, Sds, NB, mtg;        // mtg: gate/up row tiles per slot
+  int o_gudone, o_gusplit, o_dnsplit, o_dnblk, o_combt;
+};
+
+__device__ __forceinline__ int ld_acquire(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release(int32_t* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long wall_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ bool any_error(const int32_t* err) {
+  return *reinterpret_cast<const volatile int32_t*>(err) != 0;
+}
+
+// The warp waits until *ctr >= target (lane 0 polls, backing off: many warps may poll one
+// line).  False when this or another wait of the launch gave up: the caller skips its unit.
+__device__ bool warp_wait_geq(const int32_t* ctr, int target, int32_t* err) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) {
+    const unsigned long long t0 = wall_ns();
+    unsigned ns = 128;
+    while (ld_acquire(ctr) < target) {
+      if (any_error(err)) {
+        ok = 0;
+        break;
+      }
+      if (wall_ns() - t0 > kWaitNs) {
+        atomicExch(err, kErrDecodeWait);
+        ok = 0;
+        break;
+      }
+      __nanosleep(ns);
+      ns = ns < 2048 ? 2 * ns : 2048;
+    }
+  }
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  __threadfence();
+  return ok != 0;
+}
+// Thread 0 polls until *ctr >= target; the result reaches every thread of the CTA.
+__device__ bool cta_wait_geq(const int32_t* ctr, int target, int32_t* err) {
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = wall_ns();
+    unsigned ns = 64;
+    while (ld_acquire(ctr) < target) {
+      if (any_error(err)) {
+        ok = 0;
+        break;
+      }
+      if (wall_ns() - t0 > kWaitNs) {
+        atomicExch(err, kErrDecodeWait);
+        ok = 0;
+        break;
+      }
+      __nanosleep(ns);
+      ns = ns < 1024 ? 2 * ns : 1024;
+    }
+  }
+  ok = __syncthreads_and(ok);
+  __threadfence();
+  return ok != 0;
+}
+// Barrier of the eight consumer warps only (named barrier 1; the producer warp never joins),
+// returning the AND / OR of `v` over them.
+__device__ __forceinline__ int cons_and(int v) {
+  int r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.and.pred q, 1, %2, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v), "n"(kConsumerWarps * 32)
+      : "memory");
+  return r;
+}
+__device__ __forceinline__ int cons_or(int v) {
+  int r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 p, %1, 0;\nbar.red.or.pred q, 1, %2, p;\n"
+      "selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(v), "n"(kConsumerWarps * 32)
+      : "memory");
+  return r;
+}
+__device__ __forceinline__ void cons_sync() {
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+// Consumer thread 0 polls until *ctr >= target; the result reaches every consumer thread.
+__device__ bool cons_wait_geq(const int32_t* ctr, int target, int32_t* err) {
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    const unsigned long long t0 = wall_ns();
+    unsigned ns = 64;
+    while (ld_acquire(ctr) < target) {
+      if (any_error(err)) {
+        ok = 0;
+        break;
+      }
+      if (wall_ns() - t0 > kWaitNs) {
+        atomicExch(err, kErrDecodeWait);
+        ok = 0;
+        break;
+      }
+      __nanosleep(ns);
+      ns = ns < 1024 ? 2 * ns : 1024;
+    }
+  }
+  ok = cons_and(ok);
+  __threadfence();
+  return ok != 0;
+}
+// Publishes the warp's writes, then counts one arrival.
+__device__ __forceinline__ void warp_signal(int32_t* ctr) {
+  __threadfence();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) atomicAdd(ctr, 1);
+}
+// ---------------------------------------------------------------------------- mbarrier / copies
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+// The same with an L2 cache policy (weights: evict first, so that the stream of expert weights
+// does not push the layer's activations, counters and the kernel's own code out of L2).
+__device__ __forceinline__ void bulk_g2s_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bounded wait of the whole warp for a stage's copies (false: timed out or an error elsewhere).
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, int32_t* err) {
+  if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+  const unsigned long long t0 = wall_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
+    if ((i & 63) == 0) {
+      const bool late = wall_ns() - t0 > kWaitNs;
+      if (__any_sync(0xffffffffu, late)) {
+        if ((threadIdx.x & 31) == 0) atomicExch(err, kErrDecodeWait);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t word_of(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+__device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.f + expf(-g)) * u; }
+
+// ---------------------------------------------------------------------------- CTA ring
+// Per (weight type, fused) a unit's K range is cut into blocks of KW k (one 64-k bf16 tile, one
+// 128-k quantised tile), and one ring slot holds BPS blocks of every row group (gate, up) --
+//   bf16 fused: 1 block x 2 tiles of 16 KB; bf16 down: 2 blocks x 1 tile;
+//   quantised fused: 1 block x 2 tiles of 8448 / 9216 B; quantised down: 1 block x 1 tile --
+// and, from kBOff, the same k range of the unit's token rows (rows BROW bytes apart), so the
+// consumers read both operands from shared memory.
+template <int WT, bool FUSED>
+struct Fmt {
+  static constexpr int NG = FUSED ? 2 : 1;
+  static constexpr int KW = WT == 0 ? 64 : 128;
+  static constexpr int TILE = WT == 0 ? 16384 : WT == 1 ? 8448 : 9216;
+  static constexpr int BPS = WT == 0 ? 2 / NG : 1;
+  static constexpr int BROW = BPS * KW * 2 + 16;   // +16: rows start in different banks
+  static_assert(BPS * NG * TILE <= kBOff, "the tiles fit before the token rows");
+  static_assert(BROW <= kBRowMax, "a token row fits its place");
+};
+
+// The unit a CTA runs: shared or routed expert (slot), 128-row tile mt, K blocks [kb_lo, kb_hi).
+struct UnitRef {
+  int type;        // 0 gate/up, 1 down, 2 combine, 3 normalisation, -1 nothing to do
+  bool sh;         // shared expert
+  int slot, mt, sp, S, kb_lo, kb_hi, t;
+  const char* wsec;   // weight section of the unit's expert
+  int e, r0, ne;
+};
+
+// ---------------------------------------------------------------------------- the kernel
+template <int WT, int NT>
+__global__ void __launch_bounds__(kDecThreads, 1)
+    decode_layer_kernel(const __grid_constant__ DecParams p) {
+  extern __shared__ __align__(1024) uint8_t dsm[];
+  __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots];
+  __shared__ int s_flag;
+  TailSmem& sm = *reinterpret_cast<TailSmem*>(dsm);   // routing only: aliases the ring
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int T = p.T, H = p.H, C = p.g.C, E = p.g.E, k = p.k, I = p.I, Is = p.Is;
+  int32_t* ctl = p.ctl;
+
+  // ------------------------------------------------ router product over this CTA's H slice
+  if ((int)blockIdx.x < p.S) {
+    const int h_lo = blockIdx.x * p.hps, h_hi = min(H, h_lo + p.hps);
+    float* xs = sm.lg;                         // [T][hps] of x
+    for (int i = tid; i < T * p.hps; i += kDecThreads) {
+      const int t = i / p.hps, hh = i % p.hps;
+      xs[i] = h_lo + hh < h_hi ? bf16_bits_to_float(p.x[(size_t)t * H + h_lo + hh]) : 0.f;
+    }
+    __syncthreads();
+    for (int c = tid; c < C; c += kDecThreads) {
+      float acc[kDecodeMaxT];
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.f;
+      for (int h0 = h_lo; h0 < h_hi; h0 += 32) {
+        float wv[32];   // every load of 32 rows in flight at once
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int h = h0 + i;
+          wv[i] = h >= h_hi ? 0.f
+                            : (c < E ? __ldg(p.g.w_r + (size_t)h * E + c)
+                                     : bf16_bits_to_float(__ldg(p.w_gate + h)));
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+#pragma unroll
+          for (int t = 0; t < kDecodeMaxT; ++t)
+            if (t < T) acc[t] = fmaf(xs[t * p.hps + (h0 - h_lo) + i], wv[i], acc[t]);
+      }
+#pragma unroll
+      for (int t = 0; t < kDecodeMaxT; ++t)
+        if (t < T) p.rpart[((size_t)blockIdx.x * T + t) * C + c] = acc[t];
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(ctl + kCtlRouterArrive, 1);
+    }
+  }
+
+  // ------------------------------------------------ gating of token t = blockIdx.x
+  if ((int)blockIdx.x < T) {
+    const int t = blockIdx.x;
+    __syncthreads();   // the router step's shared memory is free again
+    if (cta_wait_geq(ctl + kCtlRouterArrive, p.S, p.err)) {
+      // token t's logits: S slices summed in fixed order, the loads of a column in flight
+      for (int c = tid; c < C; c += kDecThreads) {
+        float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 16
+        for (int sp = 0; sp < p.S; ++sp)
+          a[sp & 3] += __ldcg(p.rpart + ((size_t)sp * T + t) * C + c);
+        sm.lg[c] = (a[0] + a[1]) + (a[2] + a[3]);
+      }
+      for (int e = tid; e < kMaxExperts; e += kDecThreads) sm.hist[e] = 0;
+      __syncthreads();
+      GateParams q = p.g;
+      q.hist = sm.hist;
+      gate_token_cta<kDecThreads>(q, t, sm.lg, sm);
+      if (tid == 0) {
+        __threadfence();
+        s_flag = atomicAdd(ctl + kCtlGateArrive, 1) == T - 1;
+      }
+      __syncthreads();
+      if (s_flag) {
+        // the last token gated: every id is visible; histogram, scan, ranks
+        __threadfence();
+        for (int e = tid; e < kMaxExperts; e += kDecThreads) sm.hist[e] = 0;
+        __syncthreads();
+        for (int i = tid; i < T * k; i += kDecThreads)
+          atomicAdd(&sm.hist[__ldcg(p.g.ids + i)], 1);
+        __syncthreads();
+        route_dispatch_block<kDecThreads>(p.g.ids, T, k, E, p.counts, p.offsets, p.pos, p.src,
+                                          p.active, p.n_active, nullptr, nullptr, p.x, H, sm);
+        __syncthreads();
+        if (tid == 0) {
+          __threadfence();
+          st_release(ctl + kCtlRouteDone, 1);
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------ the ring
+  __syncthreads();   // routing smem no longer in use
+  if (tid == 0) {
+    for (int s = 0; s < kSlots; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), kConsumerWarps);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  fence_proxy_async();
+  __syncthreads();
+
+  const int MTg = I / 128, MTs = Is / 128, MTd = H / 128;
+  const int nA = Is ? MTs * p.Sgs : 0;
+  const int nB = p.Umax * MTg * p.Sg;
+  const int nC = Is ? MTd * p.Sds : 0;
+  const int nD = p.Umax * MTd * p.Sd;
+  const int nE = T;
+  const int nF = p.out_n ? T : 0;
+  const int total = nA + nB + nC + nD + nE + nF;
+  const int shared_slot = p.Umax;
+  int32_t* gu_done = ctl + p.o_gudone;
+  int32_t* gu_split = ctl + p.o_gusplit;
+  int32_t* dn_split = ctl + p.o_dnsplit;
+  int32_t* dn_blk = ctl + p.o_dnblk;
+  int32_t* comb_t = ctl + p.o_combt;
+  const bool producer = warp == kConsumerWarps;
+
+  // The unit u of the static schedule (the same decoding in the producer and the consumers).
+  // Routed units resolve their expert from the routing (after the flag); a routed slot beyond
+  // the experts that received rows has nothing to do.
+  auto unit_of = [&](int u, bool wait_route) -> UnitRef {
+    UnitRef r{};
+    r.type = -1;
+    int v = u;
+    if (v < nA + nB) {
+      r.type = 0;
+      r.sh = v < nA;
+      if (!r.sh) v -= nA;
+      r.S = r.sh ? p.Sgs : p.Sg;
+      r.sp = v % r.S;
+      v /= r.S;
+      const int MT = r.sh ? MTs : MTg;
+      r.mt = v % MT;
+      r.slot = r.sh ? shared_slot : v / MT;
+      const int KB = H / Fmt<WT, true>::KW, per = (KB + r.S - 1) / r.S;
+      r.kb_lo = r.sp * per;
+      r.kb_hi = min(KB, r.kb_lo + per);
+    } else if (v < nA + nB + nC + nD) {
+      v -= nA + nB;
+      r.type = 1;
+      r.sh = v < nC;
+      if (!r.sh) v -= nC;
+      r.S = r.sh ? p.Sds : p.Sd;
+      r.sp = v % r.S;
+      v /= r.S;
+      r.mt = v % MTd;
+      r.slot = r.sh ? shared_slot : v / MTd;
+      const int KB = (r.sh ? Is : I) / Fmt<WT, false>::KW, per = (KB + r.S - 1) / r.S;
+      r.kb_lo = r.sp * per;
+      r.kb_hi = min(KB, r.kb_lo + per);
+    } else if (v < nA + nB + nC + nD + nE) {
+      r.type = 2;
+      r.t = v - (nA + nB + nC + nD);
+      return r;
+    } else {
+      r.type = 3;
+      r.t = v - (nA + nB + nC + nD + nE);
+      return r;
+    }
+    if (r.sh) {
+      r.e = -1;
+      r.r0 = 0;
+      r.ne = T;
+      r.wsec = p.shared + (r.type == 0 ? p.gu_off_s : p.dn_off_s);
+      return r;
+    }
+    if (!wait_route) return r;
+    if (__ldcg(p.n_active) <= r.slot) {
+      r.type = -1;
+      return r;
+    }
+    r.e = __ldcg(p.active + r.slot);
+    r.r0 = __ldcg(p.offsets + r.e);
+    r.ne = min(__ldcg(p.offsets + r.e + 1) - r.r0, 8 * NT);   // <= T: one row per token
+    r.wsec = static_cast<const char*>(p.tab.p[r.e]) + (r.type == 0 ? p.gu_off : p.dn_off);
+    return r;
+  };
+
+  if (producer) {
+    // ---------------------------------------------- producer: bulk copies of weight tiles
+    uint32_t used = 0, epar = 0;
+    int gs = 0;   // stages issued so far
+    const uint64_t wpol = policy_evict_first();
+    bool ok = true;
+    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
+      UnitRef r = unit_of(u, false);
+      if (r.type > 1) continue;
+      if (!r.sh) {
+        if (!warp_wait_geq(ctl + kCtlRouteDone, 1, p.err)) break;
+        r = unit_of(u, true);
+        if (r.type < 0) continue;
+      }
+      const bool fused = r.type == 0;
+      const int BPS = fused ? Fmt<WT, true>::BPS : Fmt<WT, false>::BPS;
+      const int BROW = fused ? Fmt<WT, true>::BROW : Fmt<WT, false>::BROW;
+      const int NG = fused ? 2 : 1;
+      constexpr int TILE = Fmt<WT, true>::TILE;
+      constexpr int KW = Fmt<WT, true>::KW;
+      const int K = fused ? H : (r.sh ? Is : I);
+      const int KT = K / KW;                                 // tiles along K per row tile
+      const int Mup = (r.sh ? Is : I) / 128;                 // up rows' first row tile
+      // this lane's token row (the unit's rows are its tokens' x rows, or its h rows)
+      const uint16_t* brow = nullptr;
+      if (lane < r.ne) {
+        if (fused) brow = p.x + (size_t)(r.sh ? lane : __ldcg(p.src + r.r0 + lane) / k) * H;
+        else brow = r.sh ? p.hs + (size_t)lane * Is : p.h + (size_t)(r.r0 + lane) * I;
+      }
+      if (!fused) {
+        // the h rows come from other CTAs' gate/up units: wait for them, then order those
+        // generic-proxy writes before this warp's bulk (async-proxy) reads of them
+        if (!warp_wait_geq(gu_done + r.slot * kLine, K / 128, p.err)) break;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+      }
+      for (int kb = r.kb_lo; kb < r.kb_hi; kb += BPS) {
+        const int s = gs % kSlots;
+        if ((used >> s) & 1u) {
+          if (!stage_wait(smem_u32(&empty[s]), (epar >> s) & 1u, p.err)) {
+            ok = false;
+            break;
+          }
+          epar ^= 1u << s;
+        }
+        used |= 1u << s;
+        const int nkb = min(BPS, r.kb_hi - kb);
+        const uint32_t bar = smem_u32(&full[s]), sb = smem_u32(dsm) + s * kSlotBytes;
+        const uint32_t brow_bytes = (uint32_t)nkb * KW * 2;
+        if (lane == 0) mbar_expect_tx(bar, (uint32_t)(nkb * NG * TILE) + r.ne * brow_bytes);
+        __syncwarp();
+        if (lane < nkb * NG) {
+          const int b = lane / NG, q = lane % NG;
+          const int rt = r.mt + (q ? Mup : 0);
+          const char* src = r.wsec + ((size_t)rt * KT + kb + b) * TILE;
+          bulk_g2s_hint(sb + (b * NG + q) * TILE, src, TILE, bar, wpol);
+        }
+        if (brow != nullptr) bulk_g2s(sb + kBOff + lane * BROW, brow + (size_t)kb * KW, brow_bytes, bar);
+        ++gs;
+      }
+    }
+    // no copy may land after the CTA is gone: wait (bounded) for the last fill of each slot
+    const unsigned long long t0 = wall_ns();
+    for (int s = 0; s < kSlots; ++s) {
+      const int n = gs / kSlots + (s < gs % kSlots ? 1 : 0);   // fills of slot s
+      if (n == 0) continue;
+      while (!__all_sync(0xffffffffu, mbar_try(smem_u32(&full[s]), (uint32_t)((n - 1) & 1))))
+        if (wall_ns() - t0 > kWaitNs) break;
+    }
+    return;
+  }
+
+  // ------------------------------------------------ consumers: 8 warps, 16 weight rows each
+  const int g = lane >> 2, tq = lane & 3;
+  uint32_t fpar = 0;
+  int cs = 0;   // stages consumed so far
+  for (int u = blockIdx.x; u < total; u += gridDim.x) {
+    if (any_error(p.err)) break;
+    UnitRef r = unit_of(u, false);
+    if (r.type < 0) continue;
+    if (r.type <= 1 && !r.sh) {
+      if (!cons_wait_geq(ctl + kCtlRouteDone, 1, p.err)) break;
+      r = unit_of(u, true);
+      if (r.type < 0) continue;
+    }
+    if (r.type <= 1) {
+      const bool fused = r.type == 0;
+      float acc[NT][4], accu[NT][4];
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[j][q] = accu[j][q] = 0.f;
+      const int BPS = fused ? Fmt<WT, true>::BPS : Fmt<WT, false>::BPS;
+      const int BROW = fused ? Fmt<WT, true>::BROW : Fmt<WT, false>::BROW;
+      const int NG = fused ? 2 : 1;
+      constexpr int TILE = Fmt<WT, true>::TILE;
+      constexpr int KW = Fmt<WT, true>::KW;
+      bool ok = true;
+      for (int kb = r.kb_lo; kb < r.kb_hi; kb += BPS) {
+        const int s = cs % kSlots;
+        if (!stage_wait(smem_u32(&full[s]), (fpar >> s) & 1u, p.err)) {
+          ok = false;
+          break;
+        }
+        fpar ^= 1u << s;
+        const uint32_t sbase = smem_u32(dsm) + s * kSlotBytes;
+        const int nkb = min(BPS, r.kb_hi - kb);
+        for (int b = 0; b < nkb; ++b) {
+          // token fragments: the lane's KW / 4 k of the block for token rows 8 j + g
+          constexpr int XV = KW / 32;   // 16-byte pieces per token row
+          uint4 xb[NT][XV];
+#pragma unroll
+          for (int j = 0; j < NT; ++j) {
+            const int n = 8 * j + g;
+#pragma unroll
+            for (int v = 0; v < XV; ++v) {
+              xb[j][v] = make_uint4(0, 0, 0, 0);
+              if (n < r.ne) {
+                const uint32_t addr =
+                    sbase + kBOff + n * BROW + (b * KW + (KW / 4) * tq) * 2 + v * 16;
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(xb[j][v].x), "=r"(xb[j][v].y), "=r"(xb[j][v].z),
+                               "=r"(xb[j][v].w)
+                             : "r"(addr));
+              }
+            }
+          }
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            if (q >= NG) break;
+            const uint32_t tb = sbase + (b * NG + q) * TILE;
+            // weight fragments of rows w*16 + g (+8) of this tile
+            uint32_t af[8][2][2];
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              const int rr = warp * 16 + g + 8 * h2;
+              if constexpr (WT == 0) {
+                uint4 a4[2];
+#pragma unroll
+                for (int v = 0; v < 2; ++v) {
+                  const int c = 2 * tq + v;
+                  const uint32_t addr = tb + rr * 128 + ((c ^ (rr & 7)) << 4);
+                  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                               : "=r"(a4[v].x), "=r"(a4[v].y), "=r"(a4[v].z), "=r"(a4[v].w)
+                               : "r"(addr));
+                }
+#pragma unroll
+                for (int st = 0; st < 4; ++st) {
+                  af[st][h2][0] = word_of(a4[st >> 1], (2 * st) & 3);
+                  af[st][h2][1] = word_of(a4[st >> 1], (2 * st + 1) & 3);
+                }
+              } else {
+                uint4 a4;
+                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(a4.x), "=r"(a4.y), "=r"(a4.z), "=r"(a4.w)
+                             : "r"(tb + (tq * 128 + rr) * 16));
+                uint32_t sp0, sp1;
+                if constexpr (WT == 1) {
+                  uint32_t sb;
+                  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sb) : "r"(tb + 8192 + 2 * rr));
+                  sp0 = sp1 = int4_scale_pair((uint16_t)sb);
+                } else {
+                  // the row's 8 block scales: the lane's are 2 tq and 2 tq + 1 (word tq / 2)
+                  uint32_t four;
+                  asm volatile("ld.shared.u32 %0, [%1];"
+                               : "=r"(four)
+                               : "r"(tb + 8192 + 8 * rr + 4 * (tq >> 1)));
+                  sp0 = fp4_scale_pair(four, (2 * tq) & 3);
+                  sp1 = fp4_scale_pair(four, ((2 * tq) & 3) + 1);
+                }
+#pragma unroll
+                for (int st = 0; st < 8; ++st) {
+                  // step st: codes 4st .. 4st+3 of the lane's 32 = word st / 2, pairs (st & 1) * 2, + 1
+                  const uint32_t wq = word_of(a4, st >> 1);
+                  const uint32_t scp = st < 4 ? sp0 : sp1;
+                  if constexpr (WT == 1) {
+                    af[st][h2][0] = int4_pair_dyn(wq, (st & 1) * 2, scp);
+                    af[st][h2][1] = int4_pair_dyn(wq, (st & 1) * 2 + 1, scp);
+                  } else if ((st & 1) == 0) {
+                    af[st][h2][0] = fp4_pair<0>(wq, scp);
+                    af[st][h2][1] = fp4_pair<1>(wq, scp);
+                  } else {
+                    af[st][h2][0] = fp4_pair<2>(wq, scp);
+                    af[st][h2][1] = fp4_pair<3>(wq, scp);
+                  }
+                }
+              }
+            }
+            constexpr int STEPS = KW / 16;
+#pragma unroll
+            for (int st = 0; st < STEPS; ++st)
+#pragma unroll
+              for (int j = 0; j < NT; ++j) {
+                const uint32_t b0 = word_of(xb[j][st >> 1], (2 * st) & 3);
+                const uint32_t b1 = word_of(xb[j][st >> 1], (2 * st + 1) & 3);
+                if (q == 0)
+                  mma16816(acc[j], af[st][0][0], af[st][1][0], af[st][0][1], af[st][1][1], b0, b1);
+                else
+                  mma16816(accu[j], af[st][0][0], af[st][1][0], af[st][0][1], af[st][1][1], b0, b1);
+              }
+          }
+        }
+        // the slot is read (the arrive releases the warp's reads of it to the producer)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
+        ++cs;
+      }
+      if (!ok) break;
+      // ---------------------------------------------- epilogue of a 128-row tile
+      const int Mo = fused ? (r.sh ? Is : I) : H;
+      float fa = 1.f, fb = 1.f;   // NVFP4 matrix scales (x 2^7)
+      if (WT == 2) {
+        const char* bb = r.sh ? p.shared : static_cast<const char*>(p.tab.p[r.e]);
+        const float* gsv = reinterpret_cast<const float*>(bb + (r.sh ? p.gs_off_s : p.gs_off));
+        fa = __ldg(gsv + (fused ? 0 : 2)) * 128.f;
+        fb = __ldg(gsv + 1) * 128.f;
+      }
+      uint16_t* outp = fused ? (r.sh ? p.hs : p.h) : (r.sh ? p.ys : p.y);
+      const int ne = r.ne;
+      if (r.S > 1) {
+        const int smax = fused ? max(p.Sg, p.Sgs) : max(p.Sd, p.Sds);
+        const int grp = r.slot * (fused ? p.mtg : MTd) + r.mt;
+        const int pw = fused ? 256 : 128;   // partial row: gate then up columns (fused)
+        float* base = (fused ? p.gpart : p.dpart) + (size_t)grp * smax * 16 * pw;
+        float* pp = base + (size_t)r.sp * 16 * pw;
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int n = 8 * j + 2 * tq + (q & 1), m = warp * 16 + g + 8 * (q >> 1);
+            if (n < ne) {
+              pp[n * pw + m] = acc[j][q];
+              if (fused) pp[n * pw + 128 + m] = accu[j][q];
+            }
+          }
+        __threadfence();
+        cons_sync();
+        int last = 0;
+        if (tid == 0) last = atomicAdd((fused ? gu_split : dn_split) + grp, 1) == r.S - 1;
+        if (!cons_or(last)) continue;
+        __threadfence();
+        for (int i = tid; i < ne * 128; i += kConsumerWarps * 32) {
+          const int n = i >> 7, m = i & 127;
+          float a0 = 0.f, a1 = 0.f;
+          for (int q = 0; q < r.S; ++q) {
+            a0 += __ldcg(base + ((size_t)q * 16 + n) * pw + m);
+            if (fused) a1 += __ldcg(base + ((size_t)q * 16 + n) * pw + 128 + m);
+          }
+          const float v = fused ? silu_mul(a0 * fa, a1 * fb) : a0 * fa;
+          outp[(size_t)(r.r0 + n) * Mo + r.mt * 128 + m] = float_to_bf16_bits(v);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int n = 8 * j + 2 * tq + (q & 1), m = warp * 16 + g + 8 * (q >> 1);
+            if (n < ne) {
+              const float v = fused ? silu_mul(acc[j][q] * fa, accu[j][q] * fb) : acc[j][q] * fa;
+              outp[(size_t)(r.r0 + n) * Mo + r.mt * 128 + m] = float_to_bf16_bits(v);
+            }
+          }
+      }
+      __threadfence();
+      cons_sync();
+      if (tid == 0) {
+        if (fused) atomicAdd(gu_done + r.slot * kLine, 1);
+        else atomicAdd(dn_blk + (r.mt * 128) / kColBlock * kLine, 1);
+      }
+    } else if (r.type == 2) {
+      // ---------------------------------------------- combine of token t, 256 columns per warp
+      const int t = r.t;
+      if (!cons_wait_geq(ctl + kCtlRouteDone, 1, p.err)) break;
+      const int n_act = __ldcg(p.n_active);
+      for (int b = warp; b < p.NB; b += kConsumerWarps) {
+        const int tiles = (min(kColBlock, H - b * kColBlock) + 127) / 128;
+        if (!warp_wait_geq(dn_blk + b * kLine, tiles * (n_act + (Is ? 1 : 0)), p.err)) break;
+        const int c = b * kColBlock + 8 * lane;
+        float ssq = 0.f;
+        if (c < H) {
+          float acc8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+          uint4 q4[kMaxK];
+          float wj[kMaxK];
+#pragma unroll
+          for (int j = 0; j < kMaxK; ++j) {
+            q4[j] = make_uint4(0, 0, 0, 0);
+            wj[j] = 0.f;
+            if (j < k) {
+              const int pj = __ldcg(p.pos + t * k + j);
+              wj[j] = __ldcg(p.g.w + t * k + j);
+              q4[j] = __ldcg(reinterpret_cast<const uint4*>(p.y + (size_t)pj * H + c));
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < kMaxK; ++j) {
+            if (j < k) {
+              const uint32_t qw[4] = {q4[j].x, q4[j].y, q4[j].z, q4[j].w};
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const float2 f = bf16x2_to_float2(qw[i]);
+                acc8[2 * i] = fmaf(wj[j], f.x, acc8[2 * i]);
+                acc8[2 * i + 1] = fmaf(wj[j], f.y, acc8[2 * i + 1]);
+              }
+            }
+          }
+          if (Is) {
+            const float gsh = p.shared_sigmoid ? __ldcg(p.g.shared_gate + t) : 1.f;
+            const uint4 s4 = __ldcg(reinterpret_cast<const uint4*>(p.ys + (size_t)t * H + c));
+            const uint32_t qw[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = bf16x2_to_float2(qw[i]);
+              acc8[2 * i] = fmaf(gsh, f.x, acc8[2 * i]);
+              acc8[2 * i + 1] = fmaf(gsh, f.y, acc8[2 * i + 1]);
+            }
+          }
+          uint4 rq = make_uint4(0, 0, 0, 0);
+          if (p.residual) rq = __ldg(reinterpret_cast<const uint4*>(p.residual + (size_t)t * H + c));
+          const uint32_t rw[4] = {rq.x, rq.y, rq.z, rq.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t bb = float2_to_bf16x2(acc8[2 * i], acc8[2 * i + 1]);
+            if (p.residual) {
+              const float2 rr = bf16x2_to_float2(rw[i]);
+              const float2 f = bf16x2_to_float2(bb);
+              bb = float2_to_bf16x2(rr.x + f.x, rr.y + f.y);
+            }
+            o[i] = bb;
+            const float2 f = bf16x2_to_float2(bb);
+            ssq = fmaf(f.x, f.x, fmaf(f.y, f.y, ssq));
+          }
+          reinterpret_cast<uint4*>(p.out + (size_t)t * H)[c / 8] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        if (p.out_n) {
+#pragma unroll
+          for (int d = 16; d > 0; d >>= 1) ssq += __shfl_xor_sync(0xffffffffu, ssq, d);
+          if (lane == 0) p.ss[(size_t)b * T + t] = ssq;
+          warp_signal(comb_t + t * kLine);
+        }
+      }
+    } else {
+      // ---------------------------------------------- RMS normalisation of token t
+      const int t = r.t;
+      if (!warp_wait_geq(comb_t + t * kLine, p.NB, p.err)) break;
+      float ssum = 0.f;
+      for (int i = lane; i < p.NB; i += 32) ssum += __ldcg(p.ss + (size_t)i * T + t);
+#pragma unroll
+      for (int d = 16; d > 0; d >>= 1) ssum += __shfl_xor_sync(0xffffffffu, ssum, d);
+      const float scale = 1.f / sqrtf(ssum / (float)H + p.eps);
+      for (int b = warp; b < p.NB; b += kConsumerWarps) {
+        const int c = b * kColBlock + 8 * lane;
+        if (c < H) {
+          const uint4 q4 = __ldcg(reinterpret_cast<const uint4*>(p.out + (size_t)t * H + c));
+          const uint32_t qw[4] = {q4.x, q4.y, q4.z, q4.w};
+          uint32_t o[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = bf16x2_to_float2(qw[i]);
+            o[i] = float2_to_bf16x2(f.x * scale, f.y * scale);
+          }
+          reinterpret_cast<uint4*>(p.out_n + (size_t)t * H)[c / 8] =
+              make_uint4(o[0], o[1], o[2], o[3]);
+        }
+      }
+    }
+  }
+}
+
+template <int WT, int NT>
+int blocks_per_sm() {
+  static int n = -1;
+  if (n < 0) {
+    int b = 0;
+    if (cudaFuncSetAttribute(decode_layer_kernel<WT, NT>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, decode_layer_kernel<WT, NT>,
+                                                      kDecThreads, kSmemBytes) != cudaSuccess) {
+      cudaGetLastError();
+      b = 0;
+    }
+    n = b;
+  }
+  return n;
+}
+
+template <int WT, int NT>
+cudaError_t launch_wt(const DecParams& dp, int grid, cudaStream_t st) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kDecThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_layer_kernel<WT, NT>, dp);
+}
+
+int bps_of(int wt, int nt) {
+  if (wt == 0) return nt == 1 ? blocks_per_sm<0, 1>() : blocks_per_sm<0, 2>();
+  if (wt == 1) return nt == 1 ? blocks_per_sm<1, 1>() : blocks_per_sm<1, 2>();
+  return nt == 1 ? blocks_per_sm<2, 1>() : blocks_per_sm<2, 2>();
+}
+
+// K split of `units` CTA units over `G` CTAs: the launch takes ~ ceil(units * S / G) waves of
+// 1/S of the K range each (the partial sums cost a little per extra split)
+int best_split(int units, int KB, int G) {
+  int best_s = 1;
+  double best = (double)ceil_div(units, G);
+  for (int s = 2; s <= std::min(KB, 32); ++s) {
+    const double c = (double)ceil_div(units * s, G) / s * (1.0 + 0.03 * (s - 1));
+    if (c < best * 0.97) {
+      best = c;
+      best_s = s;
+    }
+  }
+  const int per = ceil_div(KB, best_s);
+  return ceil_div(KB, per);
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int T, int H, int E, int k, int I, int Is, int wdtype, bool has_gate) {
+  DecodePlan p{};
+  p.ok = T >= 1 && T <= kDecodeMaxT && H % 128 == 0 && I % 128 == 0 && Is % 128 == 0 &&
+         E >= 1 && E <= kMaxExperts && k >= 1 && k <= kMaxK && k <= E && wdtype >= 0 &&
+         wdtype <= 2;
+  if (!p.ok) return p;
+  const int nt = T <= 8 ? 1 : 2;
+  if (bps_of(wdtype, nt) < 1) {   // one CTA (one 216 KB ring) per SM
+    p.ok = 0;
+    return p;
+  }
+  p.grid = sm_count();
+  p.C = E + (has_gate ? 1 : 0);
+  // router slices: at most kMaxSlices (token t's gating CTA sums S partials per logit), each a
+  // multiple of 32 rows, and a slice of x for all tokens must fit the routing scratch
+  const int S0 = std::min({kMaxSlices, p.grid, std::max(1, H / 32)});
+  p.hps = (int)round_up((size_t)ceil_div(H, S0), 32);
+  while ((size_t)T * p.hps > (size_t)kSmallT * (kMaxExperts + 1)) p.hps += 32;
+  p.S = ceil_div(H, p.hps);
+  p.Umax = std::min(E, T * k);
+  const int KW = wdtype == 0 ? 64 : 128;
+  const int ngu = p.Umax * (I / 128) + Is / 128;
+  p.Sg = best_split(ngu, H / KW, p.grid);
+  p.Sgs = p.Sg;
+  const int ndn = (p.Umax + (Is ? 1 : 0)) * (H / 128);
+  p.Sd = best_split(ndn, I / KW, p.grid);
+  p.Sds = Is ? best_split(ndn, Is / KW, p.grid) : 1;
+  p.NB = ceil_div(H, kColBlock);
+  const int mtg = std::max(I, Is) / 128;
+  const int slots = p.Umax + 1;
+  const int sgm = std::max(p.Sg, p.Sgs), sdm = std::max(p.Sd, p.Sds);
+  p.gpart_elems = sgm > 1 ? (size_t)slots * mtg * sgm * 16 * 256 : 1;
+  p.dpart_elems = sdm > 1 ? (size_t)slots * (H / 128) * sdm * 16 * 128 : 1;
+  p.ctl_words = kCtlHead + (size_t)slots * kLine + (size_t)slots * mtg +
+                (size_t)slots * (H / 128) + (size_t)p.NB * kLine + (size_t)T * kLine;
+  return p;
+}
+
+int launch_decode(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t st) {
+  if (!pl.ok) return MOE_ERR_UNSUPPORTED;
+  DecParams p{};
+  GateParams& gp = p.g;
+  gp.part = a.part; gp.S = pl.S; gp.C = pl.C;
+  gp.x = a.x; gp.w_r = a.w_r; gp.w_rT = nullptr; gp.logit_bias = a.logit_bias;
+  gp.sel_bias = a.sel_bias; gp.forced = a.forced; gp.T = a.T; gp.H = a.H; gp.E = a.E; gp.k = a.k;
+  gp.mode = a.gating; gp.scale = a.scale; gp.ids = a.ids; gp.w = a.w; gp.logits = nullptr;
+  gp.shared_gate = a.shared_gate; gp.tie_flags = a.tie; gp.hist = nullptr; gp.tok_per_warp = 1;
+  p.x = a.x; p.w_gate = a.w_gate; p.residual = a.residual; p.out = a.out; p.out_n = a.out_n;
+  p.eps = a.eps;
+  p.counts = a.counts; p.offsets = a.offsets; p.pos = a.pos; p.src = a.src;
+  p.active = a.active; p.n_active = a.n_active;
+  p.tab = a.tab;
+  p.shared = static_cast<const char*>(a.shared);
+  p.T = a.T; p.H = a.H; p.k = a.k; p.I = a.I; p.Is = a.Is; p.shared_sigmoid = a.shared_sigmoid;
+  p.gu_off = (long long)a.lay.gate_up_offset;
+  p.dn_off = (long long)a.lay.down_offset;
+  p.gs_off = (long long)a.lay.global_scale_offset;
+  p.gu_off_s = (long long)a.slay.gate_up_offset;
+  p.dn_off_s = (long long)a.slay.down_offset;
+  p.gs_off_s = (long long)a.slay.global_scale_offset;
+  p.h = a.h; p.y = a.y; p.hs = a.hs; p.ys = a.ys;
+  p.rpart = a.part; p.gpart = a.gpart; p.dpart = a.dpart; p.ss = a.ss;
+  p.ctl = a.ctl; p.err = a.err;
+  p.S = pl.S; p.hps = pl.hps; p.Umax = pl.Umax; p.Sg = pl.Sg; p.Sd = pl.Sd; p.Sgs = pl.Sgs;
+  p.Sds = pl.Sds; p.NB = pl.NB;
+  p.mtg = std::max(a.I, a.Is) / 128;
+  const int slots = pl.Umax + 1;
+  p.o_gudone = kCtlHead;
+  p.o_gusplit = p.o_gudone + slots * kLine;
+  p.o_dnsplit = p.o_gusplit + slots * p.mtg;
+  p.o_dnblk = p.o_dnsplit + slots * (a.H / 128);
+  p.o_combt = p.o_dnblk + pl.NB * kLine;
+  const int nt = a.T <= 8 ? 1 : 2;
+  cudaError_t e;
+  if (a.wdtype == 0) e = nt == 1 ? launch_wt<0, 1>(p, pl.grid, st) : launch_wt<0, 2>(p, pl.grid, st);
+  else if (a.wdtype == 1) e = nt == 1 ? launch_wt<1, 1>(p, pl.grid, st) : launch_wt<1, 2>(p, pl.grid, st);
+  else e = nt == 1 ? launch_wt<2, 1>(p, pl.grid, st) : launch_wt<2, 2>(p, pl.grid, st);
+  if (e != cudaSuccess) return fail_cuda(e);
+  MOE_COUNT_LAUNCH();
+  return MOE_OK;
+}
+
+}  // namespace moe

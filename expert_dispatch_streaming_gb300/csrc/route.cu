@@ -21,19 +21,12 @@
 //   route_tail_kernel      for a batch of at most kSmallT tokens (decode), everything after
 //                          the router product in one CTA: two launches route the batch.
 #include "common.cuh"
+#include "gate.cuh"
 #include "route.cuh"
 #include "tc_gemm.cuh"
 
-#include <math_constants.h>
-
 namespace moe {
 
-// fp32 selection scores within this margin of the k-th are re-scored in fp64.  The fp32
-// logit is a sum of H <= 16384 products accumulated in fp32; for the workloads' magnitudes
-// its error stays below ~1e-5, so 1e-4 leaves a wide margin (sigmoid scores move by at most
-// a quarter of the logit error).
-constexpr float kTau = 1e-4f;
-constexpr double kNearTie = 1e-6;
 
 // ------------------------------------------------------------------------------ A1 router
 constexpr int R_BT = 32, R_BC = 64, R_KH = 32;
@@ -120,111 +113,6 @@ reduce_slices_kernel(float* __restrict__ part, int S, int n) {
   part[i] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
 }
 
-// ------------------------------------------------------------------------------ A2 gating
-constexpr int G_WARPS = 8;
-constexpr int EC = kMaxExperts / 32;  // expert slots per lane
-
-__device__ __forceinline__ bool better(float sa, int ia, float sb, int ib) {
-  return sa > sb || (sa == sb && ia < ib);
-}
-__device__ __forceinline__ bool better_d(double sa, int ia, double sb, int ib) {
-  return sa > sb || (sa == sb && ia < ib);
-}
-
-__device__ __forceinline__ void warp_argmax(float& s, int& id) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    float so = __shfl_xor_sync(0xffffffffu, s, o);
-    int io = __shfl_xor_sync(0xffffffffu, id, o);
-    if (better(so, io, s, id)) { s = so; id = io; }
-  }
-}
-__device__ __forceinline__ void warp_argmax_d(double& s, int& id) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    double so = __shfl_xor_sync(0xffffffffu, s, o);
-    int io = __shfl_xor_sync(0xffffffffu, id, o);
-    if (better_d(so, io, s, id)) { s = so; id = io; }
-  }
-}
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
-}
-__device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
-}
-
-// Sum of the S H-slice partials of one logit in a fixed order: four interleaved running sums
-// (slices s = 0, 4, 8, ... / 1, 5, ... / ...) combined as (a0 + a1) + (a2 + a3), so the loads
-// of four slices are in flight together and the result does not depend on scheduling.
-__device__ __forceinline__ float sum_slices(const float* p, int S, size_t stride) {
-  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-  int sp = 0;
-  for (; sp + 4 <= S; sp += 4) {
-    a0 += p[(size_t)sp * stride];
-    a1 += p[(size_t)(sp + 1) * stride];
-    a2 += p[(size_t)(sp + 2) * stride];
-    a3 += p[(size_t)(sp + 3) * stride];
-  }
-  if (sp < S) a0 += p[(size_t)sp * stride];
-  if (sp + 1 < S) a1 += p[(size_t)(sp + 1) * stride];
-  if (sp + 2 < S) a2 += p[(size_t)(sp + 2) * stride];
-  return (a0 + a1) + (a2 + a3);
-}
-
-// fp64 selection score of expert b for token t (the refinement of near-boundary experts)
-__device__ double exact_score(const GateParams& p, int t, int b, int lane) {
-  const uint16_t* xr = p.x + (size_t)t * p.H;
-  double d0 = 0.0, d1 = 0.0, d2 = 0.0, d3 = 0.0;
-  if (p.w_rT) {
-    // coalesced reads of the transposed router row; four interleaved fp64 sums (fixed order)
-    const float* wr = p.w_rT + (size_t)b * p.H;
-    int h = lane;
-    for (; h + 96 < p.H; h += 128) {
-      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wr[h], d0);
-      d1 = fma((double)bf16_bits_to_float(xr[h + 32]), (double)wr[h + 32], d1);
-      d2 = fma((double)bf16_bits_to_float(xr[h + 64]), (double)wr[h + 64], d2);
-      d3 = fma((double)bf16_bits_to_float(xr[h + 96]), (double)wr[h + 96], d3);
-    }
-    for (; h < p.H; h += 32) d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wr[h], d0);
-  } else {
-    // strided column reads (one row of W_r per lane): eight independent sums keep eight loads
-    // in flight; fixed combination order
-    const float* wc = p.w_r + b;
-    const size_t E = p.E;
-    double d4 = 0.0, d5 = 0.0, d6 = 0.0, d7 = 0.0;
-    int h = lane;
-    for (; h + 224 < p.H; h += 256) {
-      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wc[(size_t)h * E], d0);
-      d1 = fma((double)bf16_bits_to_float(xr[h + 32]), (double)wc[(size_t)(h + 32) * E], d1);
-      d2 = fma((double)bf16_bits_to_float(xr[h + 64]), (double)wc[(size_t)(h + 64) * E], d2);
-      d3 = fma((double)bf16_bits_to_float(xr[h + 96]), (double)wc[(size_t)(h + 96) * E], d3);
-      d4 = fma((double)bf16_bits_to_float(xr[h + 128]), (double)wc[(size_t)(h + 128) * E], d4);
-      d5 = fma((double)bf16_bits_to_float(xr[h + 160]), (double)wc[(size_t)(h + 160) * E], d5);
-      d6 = fma((double)bf16_bits_to_float(xr[h + 192]), (double)wc[(size_t)(h + 192) * E], d6);
-      d7 = fma((double)bf16_bits_to_float(xr[h + 224]), (double)wc[(size_t)(h + 224) * E], d7);
-    }
-    for (; h < p.H; h += 32) d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wc[(size_t)h * E], d0);
-    d0 += d4;
-    d1 += d5;
-    d2 += d6;
-    d3 += d7;
-  }
-  double d = (d0 + d1) + (d2 + d3);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-  if (p.logit_bias) d += (double)p.logit_bias[b];
-  if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
-    d = 1.0 / (1.0 + exp(-d));
-    if (p.sel_bias) d += (double)p.sel_bias[b];
-  }
-  return d;
-}
-
 // Tensor-core router input: the router (and shared-expert gate vector as row E) split into three
 // bf16 pieces hi + mid + lo (each the bf16 rounding of what the previous pieces leave), which
 // represent the fp32 weight; written as a tiled 128-byte-swizzled bf16 image of [Mpad x 3H]
@@ -276,219 +164,6 @@ router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w
   if (m < E && w_rT) {
 #pragma unroll
     for (int i = 0; i < 8; ++i) w_rT[(size_t)m * H + ch * 8 + i] = v[i];
-  }
-}
-
-// Gating of token t by one warp: scores, top-k with the fp64 refinement of near-boundary
-// experts, weights; writes ids / w / logits / shared gate / tie flag of t and adds the token's
-// experts to hist[(t / 128) * E + e].  `raw` = the token's C summed router outputs (or NULL:
-// sum the S slices of p.part); lrow / exact_s = this warp's shared-memory rows.
-__device__ void gate_token(const GateParams& p, int t, const float* raw, float* lrow,
-                           double* exact_s) {
-  const int lane = threadIdx.x & 31;
-  const int E = p.E, k = p.k;
-  {
-    // ---- logits: fixed-order sum of the H slices (+ logit bias), scores
-    float l[EC], sc[EC];
-#pragma unroll
-    for (int c = 0; c < EC; ++c) {
-      const int e = lane + 32 * c;
-      float v = -CUDART_INF_F, s = -CUDART_INF_F;
-      if (e < E) {
-        v = raw ? raw[e] : sum_slices(p.part + (size_t)t * p.C + e, p.S, (size_t)p.T * p.C);
-        if (p.logit_bias) v += p.logit_bias[e];
-        s = v;
-        if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
-          s = 1.f / (1.f + expf(-v));
-          if (p.sel_bias) s += p.sel_bias[e];
-        }
-        lrow[e] = v;
-        if (p.logits) p.logits[(size_t)t * E + e] = v;
-      }
-      l[c] = v;
-      sc[c] = s;
-    }
-    if (lane == 0 && p.shared_gate && p.C > E) {
-      const float z =
-          raw ? raw[E] : sum_slices(p.part + (size_t)t * p.C + E, p.S, (size_t)p.T * p.C);
-      p.shared_gate[t] = 1.f / (1.f + expf(-z));
-    }
-
-    bool chosen[EC];
-#pragma unroll
-    for (int c = 0; c < EC; ++c) chosen[c] = false;
-    int flag = 0;
-
-    if (p.forced == nullptr) {
-      // ---- top-(k+1) by repeated warp argmax on (score desc, id asc)
-      bool taken[EC];
-#pragma unroll
-      for (int c = 0; c < EC; ++c) taken[c] = (lane + 32 * c) >= E;
-      float selsc[kMaxK + 1];
-      int selid[kMaxK + 1];
-      const int nsel = min(k + 1, E);
-#pragma unroll
-      for (int r = 0; r < kMaxK + 1; ++r) {
-        selsc[r] = -CUDART_INF_F;
-        selid[r] = 0x7fffffff;
-        if (r < nsel) {
-          float bs = -CUDART_INF_F;
-          int bi = 0x7fffffff;
-#pragma unroll
-          for (int c = 0; c < EC; ++c) {
-            const int e = lane + 32 * c;
-            if (!taken[c] && better(sc[c], e, bs, bi)) { bs = sc[c]; bi = e; }
-          }
-          warp_argmax(bs, bi);
-          selsc[r] = bs;
-          selid[r] = bi;
-#pragma unroll
-          for (int c = 0; c < EC; ++c)
-            if (lane + 32 * c == bi) { taken[c] = true; if (r < k) chosen[c] = true; }
-        }
-      }
-      // selsc[k-1] is the k-th score, selsc[k] the best unchosen one
-      float kth = -CUDART_INF_F, nxt = -CUDART_INF_F;
-#pragma unroll
-      for (int r = 0; r < kMaxK + 1; ++r) {
-        if (r == k - 1) kth = selsc[r];
-        if (r == k) nxt = selsc[r];
-      }
-      if (k < E && kth - nxt <= kTau) {
-        // ---- refinement: experts within the margin of the boundary are re-scored in fp64
-        flag = 1;
-        bool band[EC];
-        int n_def = 0;
-#pragma unroll
-        for (int r = 0; r < kMaxK; ++r)
-          if (r < k && selsc[r] - nxt > kTau) ++n_def;
-        const float thr = kth - kTau;
-#pragma unroll
-        for (int c = 0; c < EC; ++c) {
-          const int e = lane + 32 * c;
-          bool d = false;
-#pragma unroll
-          for (int r = 0; r < kMaxK; ++r)
-            if (r < n_def && selid[r] == e) d = true;
-          band[c] = (e < E) && !d && sc[c] >= thr;
-          chosen[c] = d;
-        }
-#pragma unroll
-        for (int c = 0; c < EC; ++c) {
-          unsigned m = __ballot_sync(0xffffffffu, band[c]);
-          while (m) {
-            const int b = 32 * c + __ffs(m) - 1;
-            m &= m - 1;
-            double s = exact_score(p, t, b, lane);
-            if (lane == 0) exact_s[b] = s;
-          }
-        }
-        __syncwarp();
-        const int need = k - n_def;
-        double last = CUDART_INF;
-        for (int r = 0; r < need; ++r) {
-          double bs = -CUDART_INF;
-          int bi = 0x7fffffff;
-#pragma unroll
-          for (int c = 0; c < EC; ++c) {
-            const int e = lane + 32 * c;
-            if (band[c] && !chosen[c] && better_d(exact_s[e], e, bs, bi)) {
-              bs = exact_s[e];
-              bi = e;
-            }
-          }
-          warp_argmax_d(bs, bi);
-          last = bs;
-#pragma unroll
-          for (int c = 0; c < EC; ++c)
-            if (lane + 32 * c == bi) chosen[c] = true;
-        }
-        // exact gap to the best band member left out
-        double bs = -CUDART_INF;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int c = 0; c < EC; ++c) {
-          const int e = lane + 32 * c;
-          if (band[c] && !chosen[c] && better_d(exact_s[e], e, bs, bi)) {
-            bs = exact_s[e];
-            bi = e;
-          }
-        }
-        warp_argmax_d(bs, bi);
-        if (bi != 0x7fffffff && last - bs < kNearTie) flag = 2;
-      }
-    }
-    __syncwarp();
-
-    // ---- chosen list (ascending id, or the forced order) and weights (lane 0)
-    int my_ids[kMaxK];
-    if (p.forced) {
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        my_ids[j] = j < k ? min(max(p.forced[(size_t)t * k + j], 0), E - 1) : 0;
-    } else {
-      int n = 0;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) my_ids[j] = 0;
-#pragma unroll
-      for (int c = 0; c < EC; ++c) {
-        unsigned m = __ballot_sync(0xffffffffu, chosen[c]);
-        while (m) {
-          const int e = 32 * c + __ffs(m) - 1;
-          m &= m - 1;
-#pragma unroll
-          for (int j = 0; j < kMaxK; ++j)
-            if (j == n) my_ids[j] = e;
-          ++n;
-        }
-      }
-    }
-
-    // softmax over all E needs the warp-wide max and sum
-    float M = 0.f, Ssum = 1.f;
-    if (p.mode == MOE_GATING_SOFTMAX) {
-      float mx = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < EC; ++c) mx = fmaxf(mx, l[c]);
-      M = warp_max(mx);
-      float s = 0.f;
-#pragma unroll
-      for (int c = 0; c < EC; ++c)
-        if (lane + 32 * c < E) s += expf(l[c] - M);
-      Ssum = warp_sum(s);
-    }
-    __syncwarp();
-    if (lane == 0) {
-      float v[kMaxK];
-      float denom = 0.f, mx = -CUDART_INF_F;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if (j < k) mx = fmaxf(mx, lrow[my_ids[j]]);
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        v[j] = 0.f;
-        if (j < k) {
-          const float lj = lrow[my_ids[j]];
-          if (p.mode == MOE_GATING_SOFTMAX_RENORM) v[j] = expf(lj - mx);
-          else if (p.mode == MOE_GATING_SOFTMAX) v[j] = expf(lj - M);
-          else v[j] = 1.f / (1.f + expf(-lj));
-          denom += v[j];
-        }
-      }
-      if (p.mode == MOE_GATING_SOFTMAX) denom = Ssum;
-      const float inv = p.scale / denom;
-      const int tile = t / kTileT;
-#pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j < k) {
-          p.ids[(size_t)t * k + j] = my_ids[j];
-          p.w[(size_t)t * k + j] = v[j] * inv;
-          atomicAdd(&p.hist[tile * E + my_ids[j]], 1);
-        }
-      }
-      if (p.tie_flags) p.tie_flags[t] = flag;
-    }
-    __syncwarp();
   }
 }
 
@@ -611,10 +286,8 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ s
 }
 
 // ------------------------------------------------------------------------------ A2-A4, small T
-// Everything after the router product for a batch of at most kSmallT tokens, in one CTA: the
-// S slice partials of every logit summed in fixed order (a group of G lanes per logit, each
-// lane summing every G-th slice, then a shuffle tree), gating / top-k (one warp per token),
-// the expert histogram and scan, the stable ranks and the row copy into expert order.
+// Everything after the router product for a batch of at most kSmallT tokens, in one CTA (the
+// body is route_tail_block in gate.cuh, shared with the fused decode kernel).
 constexpr int kTailThreads = 1024;
 __global__ void __launch_bounds__(kTailThreads)
 route_tail_kernel(GateParams p, int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
@@ -623,109 +296,9 @@ route_tail_kernel(GateParams p, int32_t* __restrict__ counts, int32_t* __restric
                   int32_t* __restrict__ shared_meta, uint16_t* __restrict__ x_perm) {
   pdl_trigger();
   pdl_wait();
-  static_assert(kTailThreads >= kMaxExperts, "the scan takes one thread per expert");
-  __shared__ float lg[kSmallT * (kMaxExperts + 1)];   // summed router outputs of all tokens
-  __shared__ float lrow[G_WARPS][kMaxExperts];
-  __shared__ double exact_s[G_WARPS][kMaxExperts];
-  __shared__ int hist[kMaxExperts], excl[kMaxExperts], srow[kSmallT * kMaxK];
-  const int tid = threadIdx.x, lane = tid & 31, T = p.T, C = p.C, E = p.E, k = p.k;
-  const int S = p.S, n = T * C;
-  const size_t stride = (size_t)T * C;
-
-  // ---- logits: G lanes per logit (G a power of two <= 32)
-  int G = 32;
-  while (G > 1 && n * G > kTailThreads) G >>= 1;
-  const int per = kTailThreads / G, g = tid % G;
-  for (int li = tid / G; li < ((n + per - 1) / per) * per; li += per) {
-    float a0 = 0.f, a1 = 0.f;
-    if (li < n) {
-      int sp = g;
-      for (; sp + G < S; sp += 2 * G) {
-        a0 += __ldcg(p.part + (size_t)sp * stride + li);
-        a1 += __ldcg(p.part + (size_t)(sp + G) * stride + li);
-      }
-      if (sp < S) a0 += __ldcg(p.part + (size_t)sp * stride + li);
-    }
-    float v = a0 + a1;
-    for (int o = G >> 1; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    if (g == 0 && li < n) lg[li] = v;
-  }
-  for (int e = tid; e < kMaxExperts; e += kTailThreads) hist[e] = 0;
-  __syncthreads();
-
-  // ---- gating: warp w < G_WARPS takes tokens w, w + G_WARPS, ...
-  const int warp = tid >> 5;
-  if (warp < G_WARPS) {
-    GateParams q = p;
-    q.hist = hist;
-    for (int t = warp; t < T; t += G_WARPS)
-      gate_token(q, t, lg + (size_t)t * C, lrow[warp], exact_s[warp]);
-  }
-  __syncthreads();
-
-  // ---- scan over the experts: counts, exclusive offsets, list of experts with rows
-  const bool ex = tid < kMaxExperts;
-  int cnt = 0, flag = 0;
-  if (ex && tid < E) {
-    cnt = hist[tid];
-    flag = cnt > 0;
-  }
-  if (ex) excl[tid] = cnt;
-  __syncthreads();
-  for (int o = 1; o < kMaxExperts; o <<= 1) {
-    const int v = (ex && tid >= o) ? excl[tid - o] : 0;
-    __syncthreads();
-    if (ex) excl[tid] += v;
-    __syncthreads();
-  }
-  const int incl = ex ? excl[tid] : 0;
-  __syncthreads();
-  if (ex) {
-    excl[tid] = incl - cnt;
-    hist[tid] = flag;
-  }
-  __syncthreads();
-  for (int o = 1; o < kMaxExperts; o <<= 1) {
-    const int v = (ex && tid >= o) ? hist[tid - o] : 0;
-    __syncthreads();
-    if (ex) hist[tid] += v;   // inclusive count of experts with rows
-    __syncthreads();
-  }
-  if (tid < E) {
-    counts[tid] = cnt;
-    offsets[tid] = excl[tid];
-    if (tid == E - 1) {
-      offsets[E] = excl[tid] + cnt;
-      *n_active = hist[tid];
-    }
-    if (flag) active[hist[tid] - 1] = tid;
-  }
-  if (tid == 0 && shared_meta) {
-    shared_meta[0] = 0;
-    shared_meta[1] = T;
-    shared_meta[2] = 0;
-    shared_meta[3] = 1;
-  }
-  // ---- stable ranks: pair i = t*k + j goes after every earlier pair routed to its expert
-  if (tid < T * k) {
-    const int e = p.ids[tid];
-    int rank = 0;
-    for (int i = 0; i < tid; ++i) rank += p.ids[i] == e;
-    const int pp = excl[e] + rank;
-    pos[tid] = pp;
-    src[pp] = tid;
-    srow[pp] = tid / k;
-  }
-  __syncthreads();
-  if (x_perm) {
-    const int nvec = p.H / 8;
-    for (int i = tid; i < T * k * nvec; i += kTailThreads) {
-      const int r = i / nvec, v = i % nvec;
-      reinterpret_cast<uint4*>(x_perm + (size_t)r * p.H)[v] =
-          __ldg(reinterpret_cast<const uint4*>(p.x + (size_t)srow[r] * p.H) + v);
-    }
-  }
-  (void)lane;
+  __shared__ TailSmem sm;
+  route_tail_block<kTailThreads>(p, counts, offsets, pos, src, active, n_active, shared_meta,
+                                 x_perm, sm);
 }
 
 // ------------------------------------------------------------------------------ host side

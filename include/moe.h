@@ -69,14 +69,19 @@ int moe_version(void);
  *  MOE_OPT_PDL: 1 = launch the layer's kernels with programmatic dependent launch (a kernel
  *    is scheduled while its predecessor finishes and waits in-kernel for its results); 0
  *    (default) = plain stream-ordered launches, which measured as fast or faster on GB300 at
- *    every workload tried.  Results are identical either way. */
-enum moe_option { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_PDL = 2 };
+ *    every workload tried.  Results are identical either way.
+ *  MOE_OPT_DECODE_KERNEL: 1 (default) = moe_layer_forward runs a batch of at most 16 tokens
+ *    with every bundle resident (no cache) as one cooperative launch that routes, runs the
+ *    shared and routed experts and combines; 0 = the step-by-step kernels.  Both compute the
+ *    same layer (same roundings; sums in a different fixed order). */
+enum moe_option { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_PDL = 2, MOE_OPT_DECODE_KERNEL = 3 };
 int moe_set_option(int option, int value);
 
 /* Reads the device error word kept in the first 4 bytes of a moe_layer_forward,
  * moe_grouped_swiglu or moe_route_topk workspace into *code (host) and waits for `stream`.
  * 0 = no error; otherwise the last call on that workspace produced invalid outputs:
  *   1-7  a bounded wait inside a tensor-core kernel ran out of time;
+ *   9    a bounded wait inside the fused decode kernel ran out of time;
  *   8    an expert's row range [offsets[e], offsets[e+1]) reached outside [0, max_rows)
  *        (moe_grouped_swiglu) and was clipped to it;
  *   20   a device-LRU cache request needed more distinct bundles than slots.
@@ -475,6 +480,9 @@ typedef struct moe_layer_stats {
   int32_t shared_merged;     /* out: 1 if the shared expert ran inside the routed GEMM
                                 launches (phase [2] is then empty and phases [3] / [4]
                                 include it), else 0                                      */
+  int32_t fused_decode;      /* out: 1 if the whole layer ran as one fused decode launch
+                                (phases [1]-[5] are then recorded together after it, so
+                                phase [0]-[1] is the whole layer)                         */
   /* in: NULL, or a host array of MOE_N_PHASE_EVENTS cudaEvent_t handles created by the
    * caller; the call records them on `stream` at phase boundaries:
    *   [0] start  [1] routing + dispatch + gather done  [2] shared expert done

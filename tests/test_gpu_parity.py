@@ -298,9 +298,11 @@ def test_int4_bundle_with_foreign_scales_fails_parity(moe, syn):
 def test_layer_forward_streaming_kernel(moe, syn, cfg, T):
     """The mma.sync weight-streaming FFN kernel (forced), bf16 and INT4."""
     moe.set_ffn_kernel("stream")
+    moe.set_decode_kernel(False)
     try:
         _layer_case(syn, cfg, T)
     finally:
+        moe.set_decode_kernel(True)
         moe.set_ffn_kernel("auto")
 
 

@@ -19,7 +19,9 @@ pytestmark = pytest.mark.gpu
 def moe():
     import expert_dispatch_streaming_gb300 as m
     m.set_ffn_kernel("tcgen05")
+    m.set_decode_kernel(False)          # small batches too run the step-by-step kernels here
     yield m
+    m.set_decode_kernel(True)
     m.set_ffn_kernel("auto")
 
 
