@@ -155,7 +155,7 @@ static size_t carve(WsCursor& c, const moe_layer* L, int T, const LayerPlan& P, 
   z.part = c.take<float>(pe);
   z.part_s = c.take<float>(std::max({P.mgu.t2.part_elems, P.mdn.t2.part_elems, (size_t)1}));
   if (P.dec.ok) {
-    z.dec_rpart = c.take<float>((size_t)P.dec.S * T * P.dec.C);
+    z.dec_rpart = c.take<float>((size_t)P.dec.S * T * P.dec.Cp);
     z.dec_gpart = c.take<float>(P.dec.gpart_elems);
     z.dec_dpart = c.take<float>(P.dec.dpart_elems);
     z.dec_ss = c.take<float>((size_t)P.dec.NB * T + 1);
@@ -463,6 +463,7 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   };
   if (T == 0) return MOE_OK;
   MOE_REQUIRE(x && out && aligned16(x) && aligned16(out));
+  MOE_REQUIRE(ws && reinterpret_cast<uintptr_t>(ws) % 256 == 0);
   MOE_REQUIRE(!out_normed || (aligned16(out_normed) && L->H <= kMaxNormH && L->norm_eps >= 0.f));
   cudaStream_t s0 = (cudaStream_t)stream;
   WsCursor c(ws, ws_bytes);
@@ -472,7 +473,10 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   MOE_CUDA_TRY(cudaMemsetAsync(s.err, 0, s.ctl_bytes, s0));
 
   if ((r = phase(0)) != MOE_OK) return r;
-  if (!cache && P.dec.ok && g_decode_path && (!L->Is || (s.h_s && s.s))) {
+  // (the fused kernel bulk-copies the router slice: W_r and the gate column 16-byte aligned)
+  const bool dec_aligned = aligned16(L->w_r) && (!L->w_gate || aligned16(L->w_gate)) &&
+                           (!residual || aligned16(residual));
+  if (!cache && P.dec.ok && g_decode_path && dec_aligned && (!L->Is || (s.h_s && s.s))) {
     // small batch, every bundle resident: the whole layer in one cooperative launch
     DecodeArgs da{};
     da.x = x; da.residual = residual; da.forced = forced_ids; da.w_r = L->w_r;

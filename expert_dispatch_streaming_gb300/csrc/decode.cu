@@ -47,9 +47,19 @@ constexpr int kSlots = 6;                            // ring slots per CTA
 constexpr int kBOff = 32768;                         // token rows after the weight tiles
 constexpr int kBRowMax = 256 + 16;                   // bytes of one token row's k range (+pad)
 constexpr int kSlotBytes = kBOff + kDecodeMaxT * kBRowMax;
-constexpr int kMaxSlices = 64;                       // router H slices
-constexpr int kSmemBytes = kSlots * kSlotBytes;      // the ring (the routing scratch aliases it)
-static_assert(sizeof(TailSmem) <= (size_t)kSmemBytes, "routing scratch fits in the ring");
+constexpr int kSmemBytes = kSlots * kSlotBytes;      // the ring
+// In a routing CTA the last kResSlots slots first hold the router slice (weights, x, shared
+// gate column) and then the gating scratch; the producer fills them only once routing in the
+// CTA is over.
+constexpr int kResSlots = 2;
+constexpr int kResOff = (kSlots - kResSlots) * kSlotBytes;
+constexpr int kResBytes = kResSlots * kSlotBytes;
+static_assert(sizeof(TailSmem) <= (size_t)kResBytes, "gating scratch fits in the reserved slots");
+static_assert(kResOff % 16 == 0, "the reserved region is 16-byte aligned");
+constexpr int kRouteEntry = 8;                       // route table words per expert slot
+constexpr unsigned kBackoffMaxNs = 256;              // polling back-off cap
+constexpr int kGroupsMax = 32;                       // slice groups of the logit sums
+constexpr int kQueue = 4;                            // unit descriptors in flight per CTA
 
 // control words: every counter that warps poll sits on its own 128-byte line (kLine words)
 constexpr int kLine = 32;
@@ -57,7 +67,8 @@ enum : int {
   kCtlRouterArrive = 0,
   kCtlGateArrive = kLine,
   kCtlRouteDone = 2 * kLine,
-  kCtlHead = 3 * kLine
+  kCtlNextUnit = 3 * kLine,   // the work queue: next unit to hand out
+  kCtlHead = 4 * kLine   // then the route table: per expert slot {e, r0, rows, 0, 16 token bytes}
 };
 
 struct DecParams {
@@ -76,8 +87,9 @@ struct DecParams {
   uint16_t *h, *y, *hs, *ys;
   float *rpart, *gpart, *dpart, *ss;   // rpart: router partials [S][T][C] (= g.part)
   int32_t *ctl, *err;
-  int S, hps, Umax, Sg, Sd, Sgs, Sds, NB, mtg;        // mtg: gate/up row tiles per slot
-  int o_gudone, o_gusplit, o_dnsplit, o_dnblk, o_combt;
+  int S, hps, Cp, Umax, Sg, Sd, Sgs, Sds, NB, mtg;    // Cp: C rounded up to 4; mtg: gate/up
+                                                      // row tiles per slot
+  int o_rt, o_tdone, o_gusplit, o_dnsplit, o_dnblk, o_combt;
 };
 
 __device__ __forceinline__ int ld_acquire(const int32_t* p) {
@@ -103,7 +115,7 @@ __device__ bool warp_wait_geq(const int32_t* ctr, int target, int32_t* err) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) {
     const unsigned long long t0 = wall_ns();
-    unsigned ns = 128;
+    unsigned ns = 32;
     while (ld_acquire(ctr) < target) {
       if (any_error(err)) {
         ok = 0;
@@ -115,36 +127,11 @@ __device__ bool warp_wait_geq(const int32_t* ctr, int target, int32_t* err) {
         break;
       }
       __nanosleep(ns);
-      ns = ns < 2048 ? 2 * ns : 2048;
+      ns = ns < kBackoffMaxNs ? 2 * ns : kBackoffMaxNs;
     }
   }
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  __threadfence();
-  return ok != 0;
-}
-// Thread 0 polls until *ctr >= target; the result reaches every thread of the CTA.
-__device__ bool cta_wait_geq(const int32_t* ctr, int target, int32_t* err) {
-  int ok = 1;
-  if (threadIdx.x == 0) {
-    const unsigned long long t0 = wall_ns();
-    unsigned ns = 64;
-    while (ld_acquire(ctr) < target) {
-      if (any_error(err)) {
-        ok = 0;
-        break;
-      }
-      if (wall_ns() - t0 > kWaitNs) {
-        atomicExch(err, kErrDecodeWait);
-        ok = 0;
-        break;
-      }
-      __nanosleep(ns);
-      ns = ns < 1024 ? 2 * ns : 1024;
-    }
-  }
-  ok = __syncthreads_and(ok);
-  __threadfence();
+  ok = __shfl_sync(0xffffffffu, ok, 0);   // (lane 0's acquire + the warp barrier order the
+  __syncwarp();                          //  other lanes' later loads)
   return ok != 0;
 }
 // Barrier of the eight consumer warps only (named barrier 1; the producer warp never joins),
@@ -177,7 +164,7 @@ __device__ bool cons_wait_geq(const int32_t* ctr, int target, int32_t* err) {
   int ok = 1;
   if (threadIdx.x == 0) {
     const unsigned long long t0 = wall_ns();
-    unsigned ns = 64;
+    unsigned ns = 32;
     while (ld_acquire(ctr) < target) {
       if (any_error(err)) {
         ok = 0;
@@ -189,18 +176,61 @@ __device__ bool cons_wait_geq(const int32_t* ctr, int target, int32_t* err) {
         break;
       }
       __nanosleep(ns);
-      ns = ns < 1024 ? 2 * ns : 1024;
+      ns = ns < kBackoffMaxNs ? 2 * ns : kBackoffMaxNs;
     }
   }
-  ok = cons_and(ok);
-  __threadfence();
+  ok = cons_and(ok);   // (thread 0's acquire + the barrier order the other threads' loads)
   return ok != 0;
+}
+// The routing flag holds the number of experts with rows + 1 once routing is over.  The warp
+// (cons_: the consumer threads) waits for it and gets that number, or -1 when a wait gave up.
+__device__ int warp_wait_route(const int32_t* flag, int32_t* err) {
+  return warp_wait_geq(flag, 1, err) ? __ldcg(flag) - 1 : -1;
+}
+__device__ int cons_wait_route(const int32_t* flag, int32_t* err) {
+  return cons_wait_geq(flag, 1, err) ? __ldcg(flag) - 1 : -1;
+}
+// The warp waits until flags f[0 .. n) are all set (each lane polls its share).
+__device__ bool warp_wait_flags(const int32_t* f, int n, int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  const unsigned long long t0 = wall_ns();
+  unsigned ns = 32;
+  for (;;) {
+    bool mine = true;
+    for (int i = lane; i < n; i += 32) mine = mine && ld_acquire(f + i) >= 1;
+    if (__all_sync(0xffffffffu, mine)) break;
+    int stop = 0;
+    if (lane == 0) {
+      if (any_error(err)) {
+        stop = 1;
+      } else if (wall_ns() - t0 > kWaitNs) {
+        atomicExch(err, kErrDecodeWait);
+        stop = 1;
+      }
+    }
+    if (__shfl_sync(0xffffffffu, stop, 0)) return false;
+    __nanosleep(ns);
+    ns = ns < kBackoffMaxNs ? 2 * ns : kBackoffMaxNs;
+  }
+  __syncwarp();
+  return true;
+}
+// Counter updates with release (acq_rel) semantics at GPU scope.  Issued by one thread after a
+// barrier of the threads whose writes they publish: the release is cumulative over the writes
+// ordered before it by the barrier.
+__device__ __forceinline__ void red_release_add(int32_t* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int atom_acq_rel_add(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
 }
 // Publishes the warp's writes, then counts one arrival.
 __device__ __forceinline__ void warp_signal(int32_t* ctr) {
-  __threadfence();
   __syncwarp();
-  if ((threadIdx.x & 31) == 0) atomicAdd(ctr, 1);
+  if ((threadIdx.x & 31) == 0) red_release_add(ctr, 1);
 }
 // ---------------------------------------------------------------------------- mbarrier / copies
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -250,13 +280,20 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// Bounded wait of the whole warp for a stage's copies (false: timed out or an error elsewhere).
+// Bounded wait of the whole warp for an mbarrier phase (false: timed out).  After a few quick
+// tries the warp sleeps between tries, so that a waiting warp does not take issue slots from
+// the warps of its SM sub-partition that have work.
 __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, int32_t* err) {
   if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   const unsigned long long t0 = wall_ns();
+  unsigned ns = 16;
   for (uint32_t i = 1;; ++i) {
     if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
-    if ((i & 63) == 0) {
+    if (i >= 4) {
+      __nanosleep(ns);
+      ns = ns < 128 ? 2 * ns : 128;
+    }
+    if ((i & 15) == 0) {
       const bool late = wall_ns() - t0 > kWaitNs;
       if (__any_sync(0xffffffffu, late)) {
         if ((threadIdx.x & 31) == 0) atomicExch(err, kErrDecodeWait);
@@ -304,6 +341,7 @@ struct UnitRef {
   int slot, mt, sp, S, kb_lo, kb_hi, t;
   const char* wsec;   // weight section of the unit's expert
   int e, r0, ne;
+  int4 tok;           // the token of each of the unit's rows (bytes, row order)
 };
 
 // ---------------------------------------------------------------------------- the kernel
@@ -311,196 +349,363 @@ template <int WT, int NT>
 __global__ void __launch_bounds__(kDecThreads, 1)
     decode_layer_kernel(const __grid_constant__ DecParams p) {
   extern __shared__ __align__(1024) uint8_t dsm[];
-  __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots];
+  __shared__ __align__(8) uint64_t full[kSlots], empty[kSlots], rcopy, rfree;
+  __shared__ __align__(8) uint64_t qfull[kQueue], qempty[kQueue];
+  __shared__ int qdesc[kQueue][2];   // unit, experts with rows (or -1: not known yet)
   __shared__ int s_flag;
-  TailSmem& sm = *reinterpret_cast<TailSmem*>(dsm);   // routing only: aliases the ring
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int T = p.T, H = p.H, C = p.g.C, E = p.g.E, k = p.k, I = p.I, Is = p.Is;
   int32_t* ctl = p.ctl;
+  // roles: CTAs [0, S) each take one H slice of the router product; the last T CTAs gate one
+  // token each (gating CTA t = blockIdx.x - (gridDim.x - T)); both use the reserved slots first
+  const bool routing = (int)blockIdx.x < p.S;
+  const bool gating = (int)blockIdx.x >= (int)gridDim.x - T;
+  const int h_lo = blockIdx.x * p.hps, h_rows = routing ? min(H, h_lo + p.hps) - h_lo : 0;
+  // the router slice in the reserved slots: W_r rows [h_lo, h_lo + h_rows) (fp32, E per row),
+  // then x[t][h_lo ..] for every token and the shared-expert gate column (bf16)
+  uint8_t* res = dsm + kResOff;
+  const float* rw = reinterpret_cast<const float*>(res);
+  const uint16_t* rx = reinterpret_cast<const uint16_t*>(res + (size_t)p.hps * E * 4);
+  const uint16_t* rg = rx + (size_t)T * p.hps;
+  TailSmem& sm = *reinterpret_cast<TailSmem*>(res);   // gating, after the router step
+  const bool producer = warp == kConsumerWarps;
 
-  // ------------------------------------------------ router product over this CTA's H slice
-  if ((int)blockIdx.x < p.S) {
-    const int h_lo = blockIdx.x * p.hps, h_hi = min(H, h_lo + p.hps);
-    float* xs = sm.lg;                         // [T][hps] of x
-    for (int i = tid; i < T * p.hps; i += kDecThreads) {
-      const int t = i / p.hps, hh = i % p.hps;
-      xs[i] = h_lo + hh < h_hi ? bf16_bits_to_float(p.x[(size_t)t * H + h_lo + hh]) : 0.f;
-    }
-    __syncthreads();
-    for (int c = tid; c < C; c += kDecThreads) {
-      float acc[kDecodeMaxT];
-#pragma unroll
-      for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.f;
-      for (int h0 = h_lo; h0 < h_hi; h0 += 32) {
-        float wv[32];   // every load of 32 rows in flight at once
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int h = h0 + i;
-          wv[i] = h >= h_hi ? 0.f
-                            : (c < E ? __ldg(p.g.w_r + (size_t)h * E + c)
-                                     : bf16_bits_to_float(__ldg(p.w_gate + h)));
-        }
-#pragma unroll
-        for (int i = 0; i < 32; ++i)
-#pragma unroll
-          for (int t = 0; t < kDecodeMaxT; ++t)
-            if (t < T) acc[t] = fmaf(xs[t * p.hps + (h0 - h_lo) + i], wv[i], acc[t]);
-      }
-#pragma unroll
-      for (int t = 0; t < kDecodeMaxT; ++t)
-        if (t < T) p.rpart[((size_t)blockIdx.x * T + t) * C + c] = acc[t];
-    }
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      atomicAdd(ctl + kCtlRouterArrive, 1);
-    }
-  }
-
-  // ------------------------------------------------ gating of token t = blockIdx.x
-  if ((int)blockIdx.x < T) {
-    const int t = blockIdx.x;
-    __syncthreads();   // the router step's shared memory is free again
-    if (cta_wait_geq(ctl + kCtlRouterArrive, p.S, p.err)) {
-      // token t's logits: S slices summed in fixed order, the loads of a column in flight
-      for (int c = tid; c < C; c += kDecThreads) {
-        float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 16
-        for (int sp = 0; sp < p.S; ++sp)
-          a[sp & 3] += __ldcg(p.rpart + ((size_t)sp * T + t) * C + c);
-        sm.lg[c] = (a[0] + a[1]) + (a[2] + a[3]);
-      }
-      for (int e = tid; e < kMaxExperts; e += kDecThreads) sm.hist[e] = 0;
-      __syncthreads();
-      GateParams q = p.g;
-      q.hist = sm.hist;
-      gate_token_cta<kDecThreads>(q, t, sm.lg, sm);
-      if (tid == 0) {
-        __threadfence();
-        s_flag = atomicAdd(ctl + kCtlGateArrive, 1) == T - 1;
-      }
-      __syncthreads();
-      if (s_flag) {
-        // the last token gated: every id is visible; histogram, scan, ranks
-        __threadfence();
-        for (int e = tid; e < kMaxExperts; e += kDecThreads) sm.hist[e] = 0;
-        __syncthreads();
-        for (int i = tid; i < T * k; i += kDecThreads)
-          atomicAdd(&sm.hist[__ldcg(p.g.ids + i)], 1);
-        __syncthreads();
-        route_dispatch_block<kDecThreads>(p.g.ids, T, k, E, p.counts, p.offsets, p.pos, p.src,
-                                          p.active, p.n_active, nullptr, nullptr, p.x, H, sm);
-        __syncthreads();
-        if (tid == 0) {
-          __threadfence();
-          st_release(ctl + kCtlRouteDone, 1);
-        }
-      }
-    }
-  }
-
-  // ------------------------------------------------ the ring
-  __syncthreads();   // routing smem no longer in use
   if (tid == 0) {
     for (int s = 0; s < kSlots; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), kConsumerWarps);
     }
+    mbar_init(smem_u32(&rcopy), 1);
+    mbar_init(smem_u32(&rfree), 1);
+    for (int i = 0; i < kQueue; ++i) {
+      mbar_init(smem_u32(&qfull[i]), 1);
+      mbar_init(smem_u32(&qempty[i]), kConsumerWarps);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   fence_proxy_async();
-  __syncthreads();
+  __syncthreads();   // the last CTA-wide barrier: from here on the producer warp runs apart
+
+  if (producer && routing) {
+    // the router slice first, ahead of any weight tile, so that routing is not queued behind
+    // the weight stream
+    const uint32_t wbytes = (uint32_t)h_rows * E * 4, xbytes = (uint32_t)h_rows * 2;
+    const uint32_t bar = smem_u32(&rcopy), rb = smem_u32(res);
+    if (lane == 0)
+      mbar_expect_tx(bar, wbytes + (uint32_t)T * xbytes + (p.w_gate ? xbytes : 0u));
+    __syncwarp();
+    constexpr uint32_t kChunk = 16384;
+    const char* wsrc = reinterpret_cast<const char*>(p.g.w_r + (size_t)h_lo * E);
+    for (uint32_t o = lane * kChunk; o < wbytes; o += 32 * kChunk)
+      bulk_g2s(rb + o, wsrc + o, min(kChunk, wbytes - o), bar);
+    if (lane < T)
+      bulk_g2s(rb + p.hps * E * 4 + lane * p.hps * 2, p.x + (size_t)lane * H + h_lo, xbytes, bar);
+    if (lane == 31 && p.w_gate)
+      bulk_g2s(rb + p.hps * E * 4 + T * p.hps * 2, p.w_gate + h_lo, xbytes, bar);
+  }
+
+  if (!producer && (routing || gating)) {
+    // ---------------------------------------------- router product over this CTA's H slice
+    float lbv = 0.f, sbv = 0.f;   // token gating: the biases, loaded ahead
+    if (gating && tid < E) {
+      if (p.g.logit_bias) lbv = __ldg(p.g.logit_bias + tid);
+      if (p.g.sel_bias) sbv = __ldg(p.g.sel_bias + tid);
+    }
+    bool ok = !routing || stage_wait(smem_u32(&rcopy), 0, p.err);
+    if (routing && ok) {
+      for (int c = tid; c < C; c += kConsumerWarps * 32) {
+        float acc[kDecodeMaxT];
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t) acc[t] = 0.f;
+        for (int h = 0; h < h_rows; ++h) {
+          const float wv = c < E ? rw[h * E + c] : bf16_bits_to_float(rg[h]);
+#pragma unroll
+          for (int t = 0; t < kDecodeMaxT; ++t)
+            if (t < T) acc[t] = fmaf(bf16_bits_to_float(rx[t * p.hps + h]), wv, acc[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < kDecodeMaxT; ++t)
+          if (t < T) p.rpart[((size_t)blockIdx.x * T + t) * p.Cp + c] = acc[t];
+      }
+    }
+    cons_sync();   // the router slice is read
+    if (tid == 0 && routing && ok) red_release_add(ctl + kCtlRouterArrive, 1);
+    // ---------------------------------------------- gating of token t
+    // Two passes over the same code: pass 0, at the start of the launch while the router runs
+    // elsewhere, sums whatever the partials hold and gates made-up logits (distinct, far from
+    // any tie) into scratch, so that the instructions of the logit sums, the gating and the
+    // dispatch are cached on this SM when pass 1 runs on the real partials.  (Run once per
+    // launch, that code is otherwise fetched cold, line by line, while the weight stream loads
+    // the memory system.)
+    int* scr = reinterpret_cast<int*>(sm.exact_s) + 1024;   // pass-0 outputs (8 KB)
+#pragma unroll 1
+    for (int pass = gating ? 0 : 2; pass < 2; ++pass) {
+      const bool real = pass == 1;
+      const int t = real ? (int)blockIdx.x - ((int)gridDim.x - T) : 0, Tn = real ? T : 1;
+      if (real && !cons_wait_geq(ctl + kCtlRouterArrive, p.S, p.err)) break;
+      {
+        // token t's logits: the S slice partials of four columns at a time, slice group g of
+        // a quad summed by one thread in slice order (eight loads in flight), then the G
+        // groups in order
+        const int Cp = p.Cp, Q = Cp / 4, G = min(kGroupsMax, (kConsumerWarps * 32) / Q);
+        float4* gsum = reinterpret_cast<float4*>(sm.exact_s);   // [G][Q]
+        if (tid < G * Q) {
+          const int q = tid % Q, g = tid / Q;
+          const float4* src = reinterpret_cast<const float4*>(p.rpart + (size_t)t * Cp) + q;
+          const size_t stride = (size_t)T * Cp / 4;
+          float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+          int sp = g;
+          for (; sp + 7 * G < p.S; sp += 8 * G) {
+            float4 v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = __ldcg(src + (size_t)(sp + i * G) * stride);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              a.x += v[i].x; a.y += v[i].y; a.z += v[i].z; a.w += v[i].w;
+            }
+          }
+          for (; sp < p.S; sp += G) {
+            const float4 v = __ldcg(src + (size_t)sp * stride);
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+          }
+          gsum[g * Q + q] = a;
+        }
+        cons_sync();
+        if (tid < Q) {
+          float4 a = gsum[tid];
+          for (int g = 1; g < G; ++g) {
+            const float4 v = gsum[g * Q + tid];
+            a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+          }
+          reinterpret_cast<float4*>(sm.lg)[tid] = a;
+        }
+      }
+      if (!real) {
+        cons_sync();
+        for (int c = tid; c < C; c += kConsumerWarps * 32) sm.lg[c] = -0.5f * (float)c;
+      }
+      for (int e = tid; e < kMaxExperts; e += kConsumerWarps * 32) {
+        sm.hist[e] = 0;
+        sm.gc.lb[e] = real ? lbv : 0.f;
+        sm.gc.sb[e] = real ? sbv : 0.f;
+      }
+      cons_sync();
+      GateParams q = p.g;
+      q.hist = sm.hist;
+      int* ids_s = sm.srow;                         // Tn * k ids
+      if (Tn == 1) q.ids_local = ids_s;
+      // where this pass writes: the real outputs, or scratch
+      int32_t* o_counts = real ? p.counts : scr + 16;
+      int32_t* o_offsets = real ? p.offsets : scr + 272;
+      int32_t* o_active = real ? p.active : scr + 529;
+      int32_t* o_pos = real ? p.pos : scr + 785;
+      int32_t* o_src = real ? p.src : scr + 913;
+      int32_t* o_nact = real ? p.n_active : scr + 1041;
+      int32_t* o_rt = real ? ctl + p.o_rt : scr + 1042;
+      if (!real) {
+        q.ids = scr;
+        q.w = reinterpret_cast<float*>(scr + 8);
+        q.forced = nullptr;
+        q.logits = nullptr;
+        q.shared_gate = nullptr;
+        q.tie_flags = nullptr;
+      }
+      gate_token_cta<kConsumerWarps * 32>(q, t, sm.lg, sm, [] { cons_sync(); });
+      if (tid == 0) s_flag = Tn == 1 || atom_acq_rel_add(ctl + kCtlGateArrive, 1) == T - 1;
+      cons_sync();
+      if (s_flag) {
+        // the last token gated: every id is visible.  Histogram, scan, ranks, route table.
+        int* rt = reinterpret_cast<int*>(sm.lrow);    // route table being built
+        if (Tn > 1)
+          for (int i = tid; i < Tn * k; i += kConsumerWarps * 32) ids_s[i] = __ldcg(p.g.ids + i);
+        for (int e = tid; e < kMaxExperts; e += kConsumerWarps * 32) sm.hist[e] = 0;
+        cons_sync();
+        for (int i = tid; i < Tn * k; i += kConsumerWarps * 32) atomicAdd(&sm.hist[ids_s[i]], 1);
+        cons_sync();
+        // one pass of scans over the experts: rows (low 16 bits) and experts with rows
+        static_assert(kConsumerWarps * 32 >= kMaxExperts, "one thread per expert");
+        const int cnt = tid < E ? sm.hist[tid] : 0;
+        int v = cnt + (cnt > 0 ? 0x10000 : 0);
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, v, o);
+          if (lane >= o) v += y;
+        }
+        if (lane == 31) sm.excl[warp] = v;
+        cons_sync();
+        int base = 0;
+        for (int w = 0; w < warp; ++w) base += sm.excl[w];
+        v += base;                                   // inclusive
+        const int off = (v & 0xffff) - cnt, slot = (v >> 16) - 1;
+        cons_sync();
+        if (tid < E) {
+          sm.excl[tid] = off;
+          o_counts[tid] = cnt;
+          o_offsets[tid] = off;
+          if (tid == E - 1) {
+            o_offsets[E] = off + cnt;
+            *o_nact = slot + 1;
+            s_flag = slot + 1;
+          }
+          if (cnt > 0) {
+            o_active[slot] = tid;
+            int* en = rt + slot * kRouteEntry;
+            en[0] = tid;
+            en[1] = off;
+            en[2] = cnt;
+            en[3] = en[4] = en[5] = en[6] = en[7] = 0;
+            sm.gc.rank[tid] = slot;                     // expert -> slot
+          }
+        }
+        cons_sync();
+        // stable ranks: pair i goes after every earlier pair routed to its expert
+        for (int i = tid; i < Tn * k; i += kConsumerWarps * 32) {
+          const int e = ids_s[i];
+          int rank = 0;
+          for (int j = 0; j < i; ++j) rank += ids_s[j] == e;
+          const int pp = sm.excl[e] + rank;
+          o_pos[i] = pp;
+          o_src[pp] = i;
+          if (rank < kDecodeMaxT)   // (forced ids may repeat an expert within a token)
+            reinterpret_cast<uint8_t*>(rt + sm.gc.rank[e] * kRouteEntry + 4)[rank] = (uint8_t)(i / k);
+        }
+        cons_sync();
+        const int n_act = s_flag;
+        for (int w = tid; w < n_act * kRouteEntry; w += kConsumerWarps * 32) o_rt[w] = rt[w];
+        cons_sync();
+        if (tid == 0 && real) st_release(ctl + kCtlRouteDone, n_act + 1);
+      }
+      cons_sync();
+    }
+    cons_sync();
+    if (tid == 0) mbar_arrive(smem_u32(&rfree));   // the reserved slots go to the ring
+  }
 
   const int MTg = I / 128, MTs = Is / 128, MTd = H / 128;
-  const int nA = Is ? MTs * p.Sgs : 0;
-  const int nB = p.Umax * MTg * p.Sg;
-  const int nC = Is ? MTd * p.Sds : 0;
-  const int nD = p.Umax * MTd * p.Sd;
+  const int nA = Is ? MTs * p.Sgs : 0;   // shared gate/up
+  const int nC = Is ? MTd * p.Sds : 0;   // shared down
+  const int nB = p.Umax * MTg * p.Sg;    // routed gate/up
+  const int nD = p.Umax * MTd * p.Sd;    // routed down
   const int nE = T;
   const int nF = p.out_n ? T : 0;
-  const int total = nA + nB + nC + nD + nE + nF;
+  const int total = nA + nC + nB + nD + nE + nF;
   const int shared_slot = p.Umax;
-  int32_t* gu_done = ctl + p.o_gudone;
+  const int32_t* rtab = ctl + p.o_rt;
+  int32_t* tdone = ctl + p.o_tdone;
   int32_t* gu_split = ctl + p.o_gusplit;
   int32_t* dn_split = ctl + p.o_dnsplit;
   int32_t* dn_blk = ctl + p.o_dnblk;
   int32_t* comb_t = ctl + p.o_combt;
-  const bool producer = warp == kConsumerWarps;
 
-  // The unit u of the static schedule (the same decoding in the producer and the consumers).
-  // Routed units resolve their expert from the routing (after the flag); a routed slot beyond
-  // the experts that received rows has nothing to do.
-  auto unit_of = [&](int u, bool wait_route) -> UnitRef {
+  // The unit u of the static schedule, in the order shared gate/up, shared down, routed
+  // gate/up, routed down, combine, normalisation (the same decoding in the producer and the
+  // consumers): the shared expert needs no routing, so it streams while routing runs.  Routed
+  // units resolve their expert from the route table (n_act >= 0: routing is over, n_act experts
+  // have rows); a routed slot beyond them has nothing to do.
+  auto unit_of = [&](int u, int n_act) -> UnitRef {
     UnitRef r{};
     r.type = -1;
     int v = u;
-    if (v < nA + nB) {
-      r.type = 0;
-      r.sh = v < nA;
-      if (!r.sh) v -= nA;
-      r.S = r.sh ? p.Sgs : p.Sg;
-      r.sp = v % r.S;
-      v /= r.S;
-      const int MT = r.sh ? MTs : MTg;
-      r.mt = v % MT;
-      r.slot = r.sh ? shared_slot : v / MT;
-      const int KB = H / Fmt<WT, true>::KW, per = (KB + r.S - 1) / r.S;
-      r.kb_lo = r.sp * per;
-      r.kb_hi = min(KB, r.kb_lo + per);
-    } else if (v < nA + nB + nC + nD) {
-      v -= nA + nB;
-      r.type = 1;
-      r.sh = v < nC;
-      if (!r.sh) v -= nC;
-      r.S = r.sh ? p.Sds : p.Sd;
-      r.sp = v % r.S;
-      v /= r.S;
-      r.mt = v % MTd;
-      r.slot = r.sh ? shared_slot : v / MTd;
-      const int KB = (r.sh ? Is : I) / Fmt<WT, false>::KW, per = (KB + r.S - 1) / r.S;
-      r.kb_lo = r.sp * per;
-      r.kb_hi = min(KB, r.kb_lo + per);
-    } else if (v < nA + nB + nC + nD + nE) {
+    bool down;
+    if (v < nA + nC) {
+      r.sh = true;
+      down = v >= nA;
+      if (down) v -= nA;
+    } else if (v < nA + nC + nB + nD) {
+      r.sh = false;
+      v -= nA + nC;
+      down = v >= nB;
+      if (down) v -= nB;
+    } else if (v < nA + nC + nB + nD + nE) {
       r.type = 2;
-      r.t = v - (nA + nB + nC + nD);
+      r.t = v - (nA + nC + nB + nD);
       return r;
     } else {
       r.type = 3;
-      r.t = v - (nA + nB + nC + nD + nE);
+      r.t = v - (nA + nC + nB + nD + nE);
       return r;
     }
+    r.type = down ? 1 : 0;
+    r.S = down ? (r.sh ? p.Sds : p.Sd) : (r.sh ? p.Sgs : p.Sg);
+    r.sp = v % r.S;
+    v /= r.S;
+    const int MT = down ? MTd : (r.sh ? MTs : MTg);
+    r.mt = v % MT;
+    r.slot = r.sh ? shared_slot : v / MT;
+    const int KW = down ? Fmt<WT, false>::KW : Fmt<WT, true>::KW;
+    const int KB = (down ? (r.sh ? Is : I) : H) / KW, per = (KB + r.S - 1) / r.S;
+    r.kb_lo = r.sp * per;
+    r.kb_hi = min(KB, r.kb_lo + per);
     if (r.sh) {
       r.e = -1;
       r.r0 = 0;
       r.ne = T;
-      r.wsec = p.shared + (r.type == 0 ? p.gu_off_s : p.dn_off_s);
+      r.tok = make_int4(0x03020100, 0x07060504, 0x0b0a0908, 0x0f0e0d0c);
+      r.wsec = p.shared + (down ? p.dn_off_s : p.gu_off_s);
       return r;
     }
-    if (!wait_route) return r;
-    if (__ldcg(p.n_active) <= r.slot) {
+    if (n_act < 0) return r;
+    if (n_act <= r.slot) {
       r.type = -1;
       return r;
     }
-    r.e = __ldcg(p.active + r.slot);
-    r.r0 = __ldcg(p.offsets + r.e);
-    r.ne = min(__ldcg(p.offsets + r.e + 1) - r.r0, 8 * NT);   // <= T: one row per token
-    r.wsec = static_cast<const char*>(p.tab.p[r.e]) + (r.type == 0 ? p.gu_off : p.dn_off);
+    const int4 a = __ldcg(reinterpret_cast<const int4*>(rtab + r.slot * kRouteEntry));
+    r.tok = __ldcg(reinterpret_cast<const int4*>(rtab + r.slot * kRouteEntry + 4));
+    r.e = a.x;
+    r.r0 = a.y;
+    r.ne = min(a.z, 8 * NT);   // <= T: one row per token
+    r.wsec = static_cast<const char*>(p.tab.p[r.e]) + (down ? p.dn_off : p.gu_off);
     return r;
   };
 
   if (producer) {
     // ---------------------------------------------- producer: bulk copies of weight tiles
-    uint32_t used = 0, epar = 0;
-    int gs = 0;   // stages issued so far
+    // Units come from one work queue for the whole grid (a counter in global memory), in the
+    // order of the schedule; each is announced to the consumers through a shared-memory
+    // descriptor queue before its tiles are issued.  A CTA that gates a token takes its first
+    // unit only once gating is over, so no unit that others wait for sits behind it.
+    uint32_t used = 0, epar = 0, qused = 0, qpar = 0;
+    int gs = 0, qi = 0;   // stages issued, descriptors pushed
     const uint64_t wpol = policy_evict_first();
-    bool ok = true;
-    for (int u = blockIdx.x; u < total && ok; u += gridDim.x) {
-      UnitRef r = unit_of(u, false);
-      if (r.type > 1) continue;
-      if (!r.sh) {
-        if (!warp_wait_geq(ctl + kCtlRouteDone, 1, p.err)) break;
-        r = unit_of(u, true);
-        if (r.type < 0) continue;
+    bool ok = true, res_free = !(routing || gating);
+    int n_act = -1;
+    auto push = [&](int u, int na) -> bool {
+      const int i = qi % kQueue;
+      if ((qused >> i) & 1u) {
+        if (!stage_wait(smem_u32(&qempty[i]), (qpar >> i) & 1u, p.err)) return false;
+        qpar ^= 1u << i;
+      }
+      qused |= 1u << i;
+      if (lane == 0) {
+        qdesc[i][0] = u;
+        qdesc[i][1] = na;
+        mbar_arrive(smem_u32(&qfull[i]));
+      }
+      __syncwarp();
+      ++qi;
+      return true;
+    };
+    auto grab = [&]() -> int {
+      int v = 0;
+      if (lane == 0) v = atomicAdd(ctl + kCtlNextUnit, 1);
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    if (gating) {
+      ok = stage_wait(smem_u32(&rfree), 0, p.err);
+      res_free = true;
+    }
+    int u = ok ? grab() : total;
+    while (ok && u < total) {
+      const int u_next = grab();   // (its latency overlaps this unit's issue)
+      UnitRef r = unit_of(u, -1);
+      if ((r.type <= 1 && !r.sh) || r.type == 2) {
+        if (n_act < 0 && (n_act = warp_wait_route(ctl + kCtlRouteDone, p.err)) < 0) break;
+        r = unit_of(u, n_act);
+      }
+      if (r.type < 0 || r.type > 1) {
+        if (r.type >= 0 && !push(u, n_act)) break;
+        u = u_next;
+        continue;
       }
       const bool fused = r.type == 0;
       const int BPS = fused ? Fmt<WT, true>::BPS : Fmt<WT, false>::BPS;
@@ -514,17 +719,29 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       // this lane's token row (the unit's rows are its tokens' x rows, or its h rows)
       const uint16_t* brow = nullptr;
       if (lane < r.ne) {
-        if (fused) brow = p.x + (size_t)(r.sh ? lane : __ldcg(p.src + r.r0 + lane) / k) * H;
+        const int tw = lane < 8 ? (lane < 4 ? r.tok.x : r.tok.y) : (lane < 12 ? r.tok.z : r.tok.w);
+        const int tok = (tw >> (8 * (lane & 3))) & 0xff;
+        if (fused) brow = p.x + (size_t)tok * H;
         else brow = r.sh ? p.hs + (size_t)lane * Is : p.h + (size_t)(r.r0 + lane) * I;
       }
       if (!fused) {
-        // the h rows come from other CTAs' gate/up units: wait for them, then order those
-        // generic-proxy writes before this warp's bulk (async-proxy) reads of them
-        if (!warp_wait_geq(gu_done + r.slot * kLine, K / 128, p.err)) break;
+        // the unit's K range of h comes from other CTAs' gate/up tiles: wait for those, then
+        // order their generic-proxy writes before this warp's bulk (async-proxy) reads
+        const int t_lo = r.kb_lo * KW / 128, t_hi = (r.kb_hi * KW + 127) / 128;
+        if (!warp_wait_flags(tdone + r.slot * p.mtg + t_lo, t_hi - t_lo, p.err)) break;
         asm volatile("fence.proxy.async.global;" ::: "memory");
       }
+      if (!push(u, n_act)) break;
       for (int kb = r.kb_lo; kb < r.kb_hi; kb += BPS) {
         const int s = gs % kSlots;
+        if (!res_free && s >= kSlots - kResSlots) {
+          // the reserved slots: only once routing in this CTA is over
+          if (!stage_wait(smem_u32(&rfree), 0, p.err)) {
+            ok = false;
+            break;
+          }
+          res_free = true;
+        }
         if ((used >> s) & 1u) {
           if (!stage_wait(smem_u32(&empty[s]), (epar >> s) & 1u, p.err)) {
             ok = false;
@@ -547,9 +764,15 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (brow != nullptr) bulk_g2s(sb + kBOff + lane * BROW, brow + (size_t)kb * KW, brow_bytes, bar);
         ++gs;
       }
+      u = u_next;
     }
-    // no copy may land after the CTA is gone: wait (bounded) for the last fill of each slot
+    push(-1, 0);   // the end of this CTA's units
+    // no copy may land after the CTA is gone: wait (bounded) for the router slice and the
+    // last fill of each slot
     const unsigned long long t0 = wall_ns();
+    if (routing)
+      while (!__all_sync(0xffffffffu, mbar_try(smem_u32(&rcopy), 0)))
+        if (wall_ns() - t0 > kWaitNs) break;
     for (int s = 0; s < kSlots; ++s) {
       const int n = gs / kSlots + (s < gs % kSlots ? 1 : 0);   // fills of slot s
       if (n == 0) continue;
@@ -561,17 +784,20 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 
   // ------------------------------------------------ consumers: 8 warps, 16 weight rows each
   const int g = lane >> 2, tq = lane & 3;
-  uint32_t fpar = 0;
-  int cs = 0;   // stages consumed so far
-  for (int u = blockIdx.x; u < total; u += gridDim.x) {
-    if (any_error(p.err)) break;
-    UnitRef r = unit_of(u, false);
+  uint32_t fpar = 0, qpar = 0;
+  int cs = 0, qi = 0;   // stages consumed, descriptors taken
+  for (;;) {
+    // the next unit from the producer (routed ones already resolved)
+    const int qs = qi % kQueue;
+    if (!stage_wait(smem_u32(&qfull[qs]), (qpar >> qs) & 1u, p.err)) break;
+    qpar ^= 1u << qs;
+    const int u = qdesc[qs][0], n_act = qdesc[qs][1];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&qempty[qs]));
+    ++qi;
+    if (u < 0) break;
+    const UnitRef r = unit_of(u, n_act);
     if (r.type < 0) continue;
-    if (r.type <= 1 && !r.sh) {
-      if (!cons_wait_geq(ctl + kCtlRouteDone, 1, p.err)) break;
-      r = unit_of(u, true);
-      if (r.type < 0) continue;
-    }
     if (r.type <= 1) {
       const bool fused = r.type == 0;
       float acc[NT][4], accu[NT][4];
@@ -722,12 +948,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
               if (fused) pp[n * pw + 128 + m] = accu[j][q];
             }
           }
-        __threadfence();
         cons_sync();
         int last = 0;
-        if (tid == 0) last = atomicAdd((fused ? gu_split : dn_split) + grp, 1) == r.S - 1;
+        if (tid == 0) last = atom_acq_rel_add((fused ? gu_split : dn_split) + grp, 1) == r.S - 1;
         if (!cons_or(last)) continue;
-        __threadfence();
         for (int i = tid; i < ne * 128; i += kConsumerWarps * 32) {
           const int n = i >> 7, m = i & 127;
           float a0 = 0.f, a1 = 0.f;
@@ -750,17 +974,14 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             }
           }
       }
-      __threadfence();
       cons_sync();
       if (tid == 0) {
-        if (fused) atomicAdd(gu_done + r.slot * kLine, 1);
-        else atomicAdd(dn_blk + (r.mt * 128) / kColBlock * kLine, 1);
+        if (fused) st_release(tdone + r.slot * p.mtg + r.mt, 1);
+        else red_release_add(dn_blk + (r.mt * 128) / kColBlock * kLine, 1);
       }
     } else if (r.type == 2) {
       // ---------------------------------------------- combine of token t, 256 columns per warp
       const int t = r.t;
-      if (!cons_wait_geq(ctl + kCtlRouteDone, 1, p.err)) break;
-      const int n_act = __ldcg(p.n_active);
       for (int b = warp; b < p.NB; b += kConsumerWarps) {
         const int tiles = (min(kColBlock, H - b * kColBlock) + 127) / 128;
         if (!warp_wait_geq(dn_blk + b * kLine, tiles * (n_act + (Is ? 1 : 0)), p.err)) break;
@@ -926,12 +1147,20 @@ DecodePlan plan_decode(int T, int H, int E, int k, int I, int Is, int wdtype, bo
   }
   p.grid = sm_count();
   p.C = E + (has_gate ? 1 : 0);
-  // router slices: at most kMaxSlices (token t's gating CTA sums S partials per logit), each a
-  // multiple of 32 rows, and a slice of x for all tokens must fit the routing scratch
-  const int S0 = std::min({kMaxSlices, p.grid, std::max(1, H / 32)});
-  p.hps = (int)round_up((size_t)ceil_div(H, S0), 32);
-  while ((size_t)T * p.hps > (size_t)kSmallT * (kMaxExperts + 1)) p.hps += 32;
+  p.Cp = (int)round_up((size_t)p.C, 4);
+  // router slices: one per CTA, each a multiple of 8 rows (16-byte bulk copies of the bf16
+  // x and gate columns), and the slice (W_r rows, x and gate columns) must fit the reserved slots
+  p.hps = (int)round_up((size_t)ceil_div(H, p.grid - T), 8);
+  auto slice_bytes = [&](int hps) { return (size_t)hps * (E * 4 + (T + 1) * 2); };
+  if (slice_bytes(p.hps) > (size_t)kResBytes) {
+    p.ok = 0;
+    return p;
+  }
   p.S = ceil_div(H, p.hps);
+  if (p.S > p.grid - T) {   // the gating CTAs take no router slice
+    p.ok = 0;
+    return p;
+  }
   p.Umax = std::min(E, T * k);
   const int KW = wdtype == 0 ? 64 : 128;
   const int ngu = p.Umax * (I / 128) + Is / 128;
@@ -946,7 +1175,7 @@ DecodePlan plan_decode(int T, int H, int E, int k, int I, int Is, int wdtype, bo
   const int sgm = std::max(p.Sg, p.Sgs), sdm = std::max(p.Sd, p.Sds);
   p.gpart_elems = sgm > 1 ? (size_t)slots * mtg * sgm * 16 * 256 : 1;
   p.dpart_elems = sdm > 1 ? (size_t)slots * (H / 128) * sdm * 16 * 128 : 1;
-  p.ctl_words = kCtlHead + (size_t)slots * kLine + (size_t)slots * mtg +
+  p.ctl_words = kCtlHead + (size_t)p.Umax * kRouteEntry + 2 * (size_t)slots * mtg +
                 (size_t)slots * (H / 128) + (size_t)p.NB * kLine + (size_t)T * kLine;
   return p;
 }
@@ -976,12 +1205,13 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t st) {
   p.h = a.h; p.y = a.y; p.hs = a.hs; p.ys = a.ys;
   p.rpart = a.part; p.gpart = a.gpart; p.dpart = a.dpart; p.ss = a.ss;
   p.ctl = a.ctl; p.err = a.err;
-  p.S = pl.S; p.hps = pl.hps; p.Umax = pl.Umax; p.Sg = pl.Sg; p.Sd = pl.Sd; p.Sgs = pl.Sgs;
+  p.S = pl.S; p.hps = pl.hps; p.Cp = pl.Cp; p.Umax = pl.Umax; p.Sg = pl.Sg; p.Sd = pl.Sd; p.Sgs = pl.Sgs;
   p.Sds = pl.Sds; p.NB = pl.NB;
   p.mtg = std::max(a.I, a.Is) / 128;
   const int slots = pl.Umax + 1;
-  p.o_gudone = kCtlHead;
-  p.o_gusplit = p.o_gudone + slots * kLine;
+  p.o_rt = kCtlHead;
+  p.o_tdone = p.o_rt + pl.Umax * kRouteEntry;
+  p.o_gusplit = p.o_tdone + slots * p.mtg;
   p.o_dnsplit = p.o_gusplit + slots * p.mtg;
   p.o_dnblk = p.o_dnsplit + slots * (a.H / 128);
   p.o_combt = p.o_dnblk + pl.NB * kLine;

@@ -14,7 +14,8 @@ struct DecodePlan {
   int ok;                  // 1: the shape is supported
   int grid;                // CTAs (all resident: cooperative launch)
   int S, hps;              // router H slices and rows per slice
-  int C;                   // router columns (E, + 1 for the shared-expert gate)
+  int C, Cp;               // router columns (E, + 1 for the shared-expert gate); C rounded
+                           // up to 4 (the row pitch of the router partials)
   int Umax;                // upper bound of experts with rows, min(E, T*k)
   int Sg, Sd, Sgs, Sds;    // K splits: routed gate/up, routed down, shared gate/up, shared down
   int NB;                  // 256-column blocks of H (combine / normalisation units)

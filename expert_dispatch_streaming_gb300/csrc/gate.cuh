@@ -77,7 +77,7 @@ static __device__ __forceinline__ float sum_slices(const float* p, int S, size_t
 }
 
 // fp64 selection score of expert b for token t (the refinement of near-boundary experts)
-static __device__ double exact_score(const GateParams& p, int t, int b, int lane) {
+static __device__ __forceinline__ double exact_score(const GateParams& p, int t, int b, int lane) {
   const uint16_t* xr = p.x + (size_t)t * p.H;
   double d0 = 0.0, d1 = 0.0, d2 = 0.0, d3 = 0.0;
   if (p.w_rT) {
@@ -195,6 +195,7 @@ static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
       for (int j = 0; j < kMaxK; ++j) {
         if (j < k) {
           p.ids[(size_t)t * k + j] = my_ids[j];
+          if (p.ids_local) p.ids_local[j] = my_ids[j];
           p.w[(size_t)t * k + j] = v[j] * inv;
           atomicAdd(&p.hist[tile * E + my_ids[j]], 1);
         }
@@ -205,19 +206,20 @@ static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
     }
 }
 
-// Gating of token t by one warp: scores, top-k with the fp64 refinement of near-boundary
-// experts, weights; writes ids / w / logits / shared gate / tie flag of t and adds the token's
-// experts to hist[(t / 128) * E + e].  `raw` = the token's C summed router outputs (or NULL:
-// sum the S slices of p.part); lrow / exact_s = this warp's shared-memory rows.
-// Inlined into each kernel, so that the parameter block's fields stay in registers instead of
-// being reloaded from local memory after every store through lrow / ids / w.
-static __device__ __forceinline__ void gate_token(const GateParams& p, int t, const float* raw,
-                                                  float* lrow, double* exact_s) {
+// Selection for token t by one warp: scores, top-k with the fp64 refinement of near-boundary
+// experts.  Out: the lane's logits l[c] and chosen flags (experts lane + 32 c), the tie flag;
+// writes the token's logits row lrow, logits and shared gate.  `raw` = the token's C summed
+// router outputs (or NULL: sum the S slices of p.part); lrow / exact_s = this warp's
+// shared-memory rows.  Inlined into each kernel, so that the parameter block's fields and the
+// lane arrays stay in registers.
+static __device__ __forceinline__ void gate_select(const GateParams& p, int t, const float* raw,
+                                                   float* lrow, double* exact_s, float (&l)[EC],
+                                                   bool (&chosen)[EC], int& flag_out) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   {
     // ---- logits: fixed-order sum of the H slices (+ logit bias), scores
-    float l[EC], sc[EC];
+    float sc[EC];
 #pragma unroll
     for (int c = 0; c < EC; ++c) {
       const int e = lane + 32 * c;
@@ -242,23 +244,20 @@ static __device__ __forceinline__ void gate_token(const GateParams& p, int t, co
       p.shared_gate[t] = 1.f / (1.f + expf(-z));
     }
 
-    bool chosen[EC];
 #pragma unroll
     for (int c = 0; c < EC; ++c) chosen[c] = false;
     int flag = 0;
 
     if (p.forced == nullptr) {
-      // ---- top-(k+1) by repeated warp argmax on (score desc, id asc)
+      // ---- top-(k+1) by repeated warp argmax on (score desc, id asc); kth = the k-th score,
+      // nxt = the best unchosen one (scalars, so that nothing here is indexed at run time)
       bool taken[EC];
 #pragma unroll
       for (int c = 0; c < EC; ++c) taken[c] = (lane + 32 * c) >= E;
-      float selsc[kMaxK + 1];
-      int selid[kMaxK + 1];
+      float kth = -CUDART_INF_F, nxt = -CUDART_INF_F;
       const int nsel = min(k + 1, E);
 #pragma unroll
       for (int r = 0; r < kMaxK + 1; ++r) {
-        selsc[r] = -CUDART_INF_F;
-        selid[r] = 0x7fffffff;
         if (r < nsel) {
           float bs = -CUDART_INF_F;
           int bi = 0x7fffffff;
@@ -268,38 +267,27 @@ static __device__ __forceinline__ void gate_token(const GateParams& p, int t, co
             if (!taken[c] && better(sc[c], e, bs, bi)) { bs = sc[c]; bi = e; }
           }
           warp_argmax(bs, bi);
-          selsc[r] = bs;
-          selid[r] = bi;
+          if (r == k - 1) kth = bs;
+          if (r == k) nxt = bs;
 #pragma unroll
           for (int c = 0; c < EC; ++c)
             if (lane + 32 * c == bi) { taken[c] = true; if (r < k) chosen[c] = true; }
         }
       }
-      // selsc[k-1] is the k-th score, selsc[k] the best unchosen one
-      float kth = -CUDART_INF_F, nxt = -CUDART_INF_F;
-#pragma unroll
-      for (int r = 0; r < kMaxK + 1; ++r) {
-        if (r == k - 1) kth = selsc[r];
-        if (r == k) nxt = selsc[r];
-      }
       if (k < E && kth - nxt <= kTau) {
-        // ---- refinement: experts within the margin of the boundary are re-scored in fp64
+        // ---- refinement: experts within the margin of the boundary are re-scored in fp64;
+        // chosen experts clear of it (score - nxt > kTau) stay chosen
         flag = 1;
         bool band[EC];
         int n_def = 0;
-#pragma unroll
-        for (int r = 0; r < kMaxK; ++r)
-          if (r < k && selsc[r] - nxt > kTau) ++n_def;
         const float thr = kth - kTau;
 #pragma unroll
         for (int c = 0; c < EC; ++c) {
           const int e = lane + 32 * c;
-          bool d = false;
-#pragma unroll
-          for (int r = 0; r < kMaxK; ++r)
-            if (r < n_def && selid[r] == e) d = true;
+          const bool d = chosen[c] && sc[c] - nxt > kTau;
           band[c] = (e < E) && !d && sc[c] >= thr;
           chosen[c] = d;
+          n_def += __popc(__ballot_sync(0xffffffffu, d));
         }
 #pragma unroll
         for (int c = 0; c < EC; ++c) {
@@ -347,9 +335,20 @@ static __device__ __forceinline__ void gate_token(const GateParams& p, int t, co
       }
     }
     __syncwarp();
-
-    gate_finish(p, t, l, chosen, lrow, flag);
+    flag_out = flag;
   }
+}
+
+// Gating of token t by one warp: gate_select, then the chosen list and weights (gate_finish);
+// writes ids / w / logits / shared gate / tie flag of t and adds the token's experts to
+// hist[(t / 128) * E + e].
+static __device__ __forceinline__ void gate_token(const GateParams& p, int t, const float* raw,
+                                                  float* lrow, double* exact_s) {
+  float l[EC];
+  bool chosen[EC];
+  int flag = 0;
+  gate_select(p, t, raw, lrow, exact_s, l, chosen, flag);
+  gate_finish(p, t, l, chosen, lrow, flag);
 }
 
 // ------------------------------------------------------------------------------ A2-A4, small T
@@ -358,8 +357,9 @@ static __device__ __forceinline__ void gate_token(const GateParams& p, int t, co
 // logit, each lane summing every G-th slice, then a shuffle tree), gating / top-k (one warp per
 // token), the expert histogram and scan, the stable ranks and (x_perm not NULL) the row copy
 // into expert order.
-struct GateCtaSmem {
+struct alignas(16) GateCtaSmem {
   float l[kMaxExperts], s[kMaxExperts];   // one token's logits and selection scores
+  float lb[kMaxExperts], sb[kMaxExperts]; // logit / selection biases (loaded ahead by the caller)
   int rank[kMaxExperts];
   float kth, nxt;                         // k-th and (k+1)-th selection scores
 };
@@ -372,59 +372,71 @@ struct TailSmem {
   GateCtaSmem gc;
 };
 
-// Gating of token t by a whole CTA of NT threads (small batches, where one token's gating is
-// on the critical path): the same selection rule and the same weights as gate_token, but the
-// top-k comes from ranking every expert against all others in parallel -- each thread counts
-// the experts that beat its own (score desc, id asc) -- instead of k + 1 dependent rounds of
-// warp arg-max.  When ids are forced, or the k-th and (k+1)-th fp32 scores lie within the
-// margin kTau, warp 0 runs gate_token instead (fp64 re-scoring).  raw: the token's C summed
-// router outputs (shared memory).  Every thread of the CTA must call it.
-template <int NT>
-static __device__ void gate_token_cta(const GateParams& p, int t, const float* raw, TailSmem& sm) {
+// Gating of token t by NT threads of a CTA (small batches, where one token's gating is on the
+// critical path): the same selection rule and the same weights as gate_token, but the top-k
+// comes from ranking every expert against all others in parallel -- each thread counts the
+// experts that beat its own (score desc, id asc) -- instead of k + 1 dependent rounds of warp
+// arg-max.  When ids are forced, or the k-th and (k+1)-th fp32 scores lie within the margin
+// kTau, the first warp runs gate_token instead (fp64 re-scoring).  raw: the token's C summed
+// router outputs (shared memory); sm.gc.lb / sm.gc.sb hold the biases (zero when absent).
+// Threads 0 .. NT-1 must all call it; `sync` is their barrier.
+template <int NT, class Sync>
+static __device__ __forceinline__ void gate_token_cta(const GateParams& p, int t, const float* raw,
+                                                      TailSmem& sm,
+                                      Sync sync) {
   const int tid = threadIdx.x, E = p.E, k = p.k;
   GateCtaSmem& g = sm.gc;
-  for (int e = tid; e < E; e += NT) {
-    float v = raw[e];
-    if (p.logit_bias) v += p.logit_bias[e];
-    float sc = v;
-    if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
-      sc = 1.f / (1.f + expf(-v));
-      if (p.sel_bias) sc += p.sel_bias[e];
+  const int E4 = (E + 3) & ~3;
+  for (int e = tid; e < E4; e += NT) {
+    float v = -CUDART_INF_F, sc = -CUDART_INF_F;
+    if (e < E) {
+      v = raw[e] + g.lb[e];
+      sc = v;
+      if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) sc = 1.f / (1.f + expf(-v)) + g.sb[e];
+      if (p.logits) p.logits[(size_t)t * E + e] = v;
     }
     g.l[e] = v;
     g.s[e] = sc;
-    if (p.logits) p.logits[(size_t)t * E + e] = v;
   }
   if (tid == 0 && p.shared_gate && p.C > E) p.shared_gate[t] = 1.f / (1.f + expf(-raw[E]));
   if (tid == 0) g.kth = g.nxt = -CUDART_INF_F;
-  __syncthreads();
+  sync();
   for (int e = tid; e < E; e += NT) {
     const float se = g.s[e];
     int r = 0;
-    for (int e2 = 0; e2 < E; ++e2) r += better(g.s[e2], e2, se, e) ? 1 : 0;
+    // four scores per shared-memory read; padding entries score -inf and never beat a real one
+    for (int e2 = 0; e2 < E4; e2 += 4) {
+      const float4 s4 = *reinterpret_cast<const float4*>(g.s + e2);
+      r += (s4.x > se || (s4.x == se && e2 < e)) ? 1 : 0;
+      r += (s4.y > se || (s4.y == se && e2 + 1 < e)) ? 1 : 0;
+      r += (s4.z > se || (s4.z == se && e2 + 2 < e)) ? 1 : 0;
+      r += (s4.w > se || (s4.w == se && e2 + 3 < e)) ? 1 : 0;
+    }
     g.rank[e] = r;
     if (r == k - 1) g.kth = se;
     if (r == k) g.nxt = se;
   }
-  __syncthreads();
+  sync();
   const bool slow = p.forced != nullptr || (k < E && g.kth - g.nxt <= kTau);
   if (threadIdx.x < 32) {
+    // (one gate_finish for both paths: the lane arrays then stay in registers)
+    float l[EC];
+    bool chosen[EC];
+    int flag = 0;
     if (slow) {
-      gate_token(p, t, raw, sm.lrow[0], sm.exact_s[0]);
+      gate_select(p, t, raw, sm.lrow[0], sm.exact_s[0], l, chosen, flag);
     } else {
       const int lane = threadIdx.x;
-      float l[EC];
-      bool chosen[EC];
 #pragma unroll
       for (int c = 0; c < EC; ++c) {
         const int e = lane + 32 * c;
         l[c] = e < E ? g.l[e] : -CUDART_INF_F;
         chosen[c] = e < E && g.rank[e] < k;
       }
-      gate_finish(p, t, l, chosen, g.l, 0);
     }
+    gate_finish(p, t, l, chosen, g.l, flag);
   }
-  __syncthreads();
+  sync();
 }
 
 // Histogram (already in sm.hist), exclusive scan, list of experts with rows, stable ranks

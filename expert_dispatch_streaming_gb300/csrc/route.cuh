@@ -27,6 +27,7 @@ struct GateParams {
   int32_t* tie_flags;
   int32_t* hist;
   int tok_per_warp;
+  int32_t* ids_local;        // or NULL: the chosen ids are also stored here (shared memory)
 };
 
 struct RoutePlan {

@@ -491,7 +491,8 @@ typedef struct moe_layer_stats {
   void* const* phase_events;
 } moe_layer_stats;
 
-/* Bytes of scratch moe_layer_forward needs for T tokens. */
+/* Bytes of scratch moe_layer_forward needs for T tokens (the scratch must start on a 256-byte
+ * boundary, as every device allocation does). */
 size_t moe_layer_workspace_size(const moe_layer* L, int T);
 
 /* The whole layer forward: out[T][H] (device bf16) from x[T][H] (device bf16).
@@ -505,6 +506,8 @@ size_t moe_layer_workspace_size(const moe_layer* L, int T);
  *             miss copies with the shared expert and with the experts that hit.
  *  st         host, or NULL (in: phase_events; out: counters).
  *  ids_out, w_out  device [T][k] or NULL: copies of the routing decision.
+ *  ws, ws_bytes    device scratch of moe_layer_workspace_size(L, T) bytes, 256-byte aligned
+ *             (MOE_ERR_INVALID_ARG otherwise).
  * With cache == NULL the call is fully asynchronous.
  * Defined by: "NovaLLM ...", "2. Why MoE Is a Natural Breakthrough Point" and "3. Optimization
  * #1 -- Expert-Level Streaming" (route, then run only the selected experts, whose weights are
