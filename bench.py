@@ -343,8 +343,9 @@ def run_ours(args, rank, world, local_rank):
                 "eager_ms_per_step": round(r.get("eager_ms_per_step", r["ms_per_step"]), 4),
                 "n_unique": r["n_unique"], "phase_ms": [round(v, 4) for v in r["phase_ms"]],
                 "layer_roofline": roofline_of(w["flops"], w["bytes"], r["ms_per_step"] / 1e3, pk),
+                # (the fused decode kernel has no separate gate/up phase)
                 "gate_up_roofline": (roofline_of(*w["gu"], r["phase_ms"][2] / 1e3, pk)
-                                     if r["phase_ms"][2] > 0 else None),
+                                     if r["phase_ms"][2] > 0 and not r.get("fused") else None),
                 "dominant_roofline": roof}
 
     head = measure(args.T, args.steps, args.warmup, True)

@@ -201,9 +201,15 @@ def set_ffn_kernel(name: str) -> None:
     moe_set_option(MOE_OPT_FFN_KERNEL, FFN_KERNEL[name])
 
 
-def set_decode_kernel(on: bool) -> None:
-    """The fused decode kernel for small batches with resident bundles (default on)."""
-    moe_set_option(MOE_OPT_DECODE_KERNEL, 1 if on else 0)
+DECODE_KERNEL = {"off": 0, "auto": 1, "always": 2}
+
+
+def set_decode_kernel(mode) -> None:
+    """The fused decode kernel for small batches with resident bundles: 'auto' (default; not
+    for INT4 weights), 'always', or 'off'.  True / False mean 'auto' / 'off'."""
+    if isinstance(mode, bool):
+        mode = "auto" if mode else "off"
+    moe_set_option(MOE_OPT_DECODE_KERNEL, DECODE_KERNEL[mode])
 
 
 def set_pdl(on: bool) -> None:

@@ -16,7 +16,7 @@
 namespace moe {
 
 static thread_local int g_last_cuda = 0;
-int g_decode_path = 1;   // MOE_OPT_DECODE_KERNEL
+int g_decode_path = 1;   // MOE_OPT_DECODE_KERNEL: 0 off, 1 auto, 2 always
 int g_use_pdl = 0;
 thread_local long long g_launches = 0;
 
@@ -275,7 +275,7 @@ int moe_set_option(int option, int value) {
     return MOE_OK;
   }
   if (option == MOE_OPT_DECODE_KERNEL) {
-    if (value < 0 || value > 1) return MOE_ERR_INVALID_ARG;
+    if (value < 0 || value > 2) return MOE_ERR_INVALID_ARG;
     g_decode_path = value;
     return MOE_OK;
   }
@@ -476,7 +476,10 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   // (the fused kernel bulk-copies the router slice: W_r and the gate column 16-byte aligned)
   const bool dec_aligned = aligned16(L->w_r) && (!L->w_gate || aligned16(L->w_gate)) &&
                            (!residual || aligned16(residual));
-  if (!cache && P.dec.ok && g_decode_path && dec_aligned && (!L->Is || (s.h_s && s.s))) {
+  // auto: not for INT4 weights, whose in-register dequantisation on the fused kernel's eight
+  // consumer warps per SM is slower than the step-by-step kernels' at these batch sizes
+  const bool dec_wanted = g_decode_path == 2 || (g_decode_path == 1 && L->wdtype != MOE_W_INT4_G128);
+  if (!cache && P.dec.ok && dec_wanted && dec_aligned && (!L->Is || (s.h_s && s.s))) {
     // small batch, every bundle resident: the whole layer in one cooperative launch
     DecodeArgs da{};
     da.x = x; da.residual = residual; da.forced = forced_ids; da.w_r = L->w_r;

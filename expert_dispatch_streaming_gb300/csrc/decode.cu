@@ -35,6 +35,8 @@
 #include "decode.cuh"
 #include "gate.cuh"
 
+#include <type_traits>
+
 namespace moe {
 namespace {
 
@@ -305,7 +307,7 @@ __device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, int32_
 
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -800,52 +802,44 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     if (r.type < 0) continue;
     if (r.type <= 1) {
       const bool fused = r.type == 0;
-      float acc[NT][4], accu[NT][4];
+      // accumulators: gate (or down) and up rows, even and odd k steps apart, so that the MMAs
+      // of a block form two independent chains per tile
+      float acc[NT][4], accu[NT][4], acc2[NT][4], accu2[NT][4];
 #pragma unroll
       for (int j = 0; j < NT; ++j)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) acc[j][q] = accu[j][q] = 0.f;
-      const int BPS = fused ? Fmt<WT, true>::BPS : Fmt<WT, false>::BPS;
-      const int BROW = fused ? Fmt<WT, true>::BROW : Fmt<WT, false>::BROW;
-      const int NG = fused ? 2 : 1;
+        for (int q = 0; q < 4; ++q) acc[j][q] = accu[j][q] = acc2[j][q] = accu2[j][q] = 0.f;
       constexpr int TILE = Fmt<WT, true>::TILE;
       constexpr int KW = Fmt<WT, true>::KW;
-      bool ok = true;
-      for (int kb = r.kb_lo; kb < r.kb_hi; kb += BPS) {
-        const int s = cs % kSlots;
-        if (!stage_wait(smem_u32(&full[s]), (fpar >> s) & 1u, p.err)) {
-          ok = false;
-          break;
-        }
-        fpar ^= 1u << s;
-        const uint32_t sbase = smem_u32(dsm) + s * kSlotBytes;
-        const int nkb = min(BPS, r.kb_hi - kb);
+      constexpr int XV = KW / 32;     // 16-byte pieces of a token row per lane and block
+      constexpr int STEPS = KW / 16;  // k steps of 16 per block
+      // One stage: NGc row groups (2: gate and up tiles, 1: down) of nkb blocks.  Plain
+      // shared-memory loads and non-volatile MMAs, so that the compiler may overlap the loads
+      // and dequantisation of one tile with the MMAs of the other.
+      auto run_stage = [&](auto ngc, const uint8_t* sl, int nkb) {
+        constexpr int NGc = decltype(ngc)::value;
+        constexpr int BROWc = Fmt<WT, NGc == 2>::BROW;
         for (int b = 0; b < nkb; ++b) {
           // token fragments: the lane's KW / 4 k of the block for token rows 8 j + g
-          constexpr int XV = KW / 32;   // 16-byte pieces per token row
           uint4 xb[NT][XV];
 #pragma unroll
           for (int j = 0; j < NT; ++j) {
             const int n = 8 * j + g;
 #pragma unroll
             for (int v = 0; v < XV; ++v) {
-              xb[j][v] = make_uint4(0, 0, 0, 0);
-              if (n < r.ne) {
-                const uint32_t addr =
-                    sbase + kBOff + n * BROW + (b * KW + (KW / 4) * tq) * 2 + v * 16;
-                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(xb[j][v].x), "=r"(xb[j][v].y), "=r"(xb[j][v].z),
-                               "=r"(xb[j][v].w)
-                             : "r"(addr));
-              }
+              // bf16: chunks 2 tq, 2 tq + 1 of the block (k = 16 tq ..); quantised: the lane's
+              // word v of each 32-k chunk (k = 32 v + 8 tq ..), the k order of its weight words
+              const int k0 = WT == 0 ? (KW / 4) * tq + 8 * v : 32 * v + 8 * tq;
+              xb[j][v] = n < r.ne ? *reinterpret_cast<const uint4*>(
+                                        sl + kBOff + n * BROWc + (b * KW + k0) * 2)
+                                  : make_uint4(0, 0, 0, 0);
             }
           }
 #pragma unroll
-          for (int q = 0; q < 2; ++q) {
-            if (q >= NG) break;
-            const uint32_t tb = sbase + (b * NG + q) * TILE;
+          for (int q = 0; q < NGc; ++q) {
+            const uint8_t* tb = sl + (b * NGc + q) * TILE;
             // weight fragments of rows w*16 + g (+8) of this tile
-            uint32_t af[8][2][2];
+            uint32_t af[STEPS][2][2];
 #pragma unroll
             for (int h2 = 0; h2 < 2; ++h2) {
               const int rr = warp * 16 + g + 8 * h2;
@@ -854,40 +848,42 @@ __global__ void __launch_bounds__(kDecThreads, 1)
 #pragma unroll
                 for (int v = 0; v < 2; ++v) {
                   const int c = 2 * tq + v;
-                  const uint32_t addr = tb + rr * 128 + ((c ^ (rr & 7)) << 4);
-                  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
-                               : "=r"(a4[v].x), "=r"(a4[v].y), "=r"(a4[v].z), "=r"(a4[v].w)
-                               : "r"(addr));
+                  a4[v] = *reinterpret_cast<const uint4*>(tb + rr * 128 + ((c ^ (rr & 7)) << 4));
                 }
 #pragma unroll
-                for (int st = 0; st < 4; ++st) {
+                for (int st = 0; st < STEPS; ++st) {
                   af[st][h2][0] = word_of(a4[st >> 1], (2 * st) & 3);
                   af[st][h2][1] = word_of(a4[st >> 1], (2 * st + 1) & 3);
                 }
               } else {
+                // One ldmatrix of four 8 x 16-byte matrices, matrix i = the 32-code chunks i of
+                // rows rr - g .. rr - g + 7: the lane gets word tq of chunk i of its row rr for
+                // i = 0..3 (codes k = 32 i + 8 tq .. + 7), with each matrix's eight rows in
+                // distinct bank groups (a lane's own chunk tq of its row would put the four
+                // lanes of a row on one bank group)
                 uint4 a4;
-                asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                              : "=r"(a4.x), "=r"(a4.y), "=r"(a4.z), "=r"(a4.w)
-                             : "r"(tb + (tq * 128 + rr) * 16));
-                uint32_t sp0, sp1;
+                             : "r"(smem_u32(tb) +
+                                   (((lane >> 3) * 128 + warp * 16 + (lane & 7) + 8 * h2) << 4)));
+                uint32_t scw[4];   // the scale pair of each of the lane's four words
                 if constexpr (WT == 1) {
-                  uint32_t sb;
-                  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(sb) : "r"(tb + 8192 + 2 * rr));
-                  sp0 = sp1 = int4_scale_pair((uint16_t)sb);
+                  scw[0] = int4_scale_pair(*reinterpret_cast<const uint16_t*>(tb + 8192 + 2 * rr));
+                  scw[1] = scw[2] = scw[3] = scw[0];
                 } else {
-                  // the row's 8 block scales: the lane's are 2 tq and 2 tq + 1 (word tq / 2)
-                  uint32_t four;
-                  asm volatile("ld.shared.u32 %0, [%1];"
-                               : "=r"(four)
-                               : "r"(tb + 8192 + 8 * rr + 4 * (tq >> 1)));
-                  sp0 = fp4_scale_pair(four, (2 * tq) & 3);
-                  sp1 = fp4_scale_pair(four, ((2 * tq) & 3) + 1);
+                  // the row's 8 block scales (16 k each): word i's is block 2 i + tq / 2
+                  const uint2 eight = *reinterpret_cast<const uint2*>(tb + 8192 + 8 * rr);
+                  const int hi = tq >> 1;
+                  scw[0] = fp4_scale_pair(eight.x, hi);
+                  scw[1] = fp4_scale_pair(eight.x, 2 + hi);
+                  scw[2] = fp4_scale_pair(eight.y, hi);
+                  scw[3] = fp4_scale_pair(eight.y, 2 + hi);
                 }
 #pragma unroll
-                for (int st = 0; st < 8; ++st) {
+                for (int st = 0; st < STEPS; ++st) {
                   // step st: codes 4st .. 4st+3 of the lane's 32 = word st / 2, pairs (st & 1) * 2, + 1
                   const uint32_t wq = word_of(a4, st >> 1);
-                  const uint32_t scp = st < 4 ? sp0 : sp1;
+                  const uint32_t scp = scw[st >> 1];
                   if constexpr (WT == 1) {
                     af[st][h2][0] = int4_pair_dyn(wq, (st & 1) * 2, scp);
                     af[st][h2][1] = int4_pair_dyn(wq, (st & 1) * 2 + 1, scp);
@@ -901,25 +897,43 @@ __global__ void __launch_bounds__(kDecThreads, 1)
                 }
               }
             }
-            constexpr int STEPS = KW / 16;
 #pragma unroll
             for (int st = 0; st < STEPS; ++st)
 #pragma unroll
               for (int j = 0; j < NT; ++j) {
                 const uint32_t b0 = word_of(xb[j][st >> 1], (2 * st) & 3);
                 const uint32_t b1 = word_of(xb[j][st >> 1], (2 * st + 1) & 3);
-                if (q == 0)
-                  mma16816(acc[j], af[st][0][0], af[st][1][0], af[st][0][1], af[st][1][1], b0, b1);
-                else
-                  mma16816(accu[j], af[st][0][0], af[st][1][0], af[st][0][1], af[st][1][1], b0, b1);
+                float(&d)[4] = q == 0 ? ((st & 1) ? acc2[j] : acc[j]) : ((st & 1) ? accu2[j] : accu[j]);
+                mma16816(d, af[st][0][0], af[st][1][0], af[st][0][1], af[st][1][1], b0, b1);
               }
           }
         }
+      };
+      const int BPS = fused ? Fmt<WT, true>::BPS : Fmt<WT, false>::BPS;
+      bool ok = true;
+      for (int kb = r.kb_lo; kb < r.kb_hi; kb += BPS) {
+        const int s = cs % kSlots;
+        if (!stage_wait(smem_u32(&full[s]), (fpar >> s) & 1u, p.err)) {
+          ok = false;
+          break;
+        }
+        fpar ^= 1u << s;
+        const uint8_t* sl = dsm + s * kSlotBytes;
+        const int nkb = min(BPS, r.kb_hi - kb);
+        if (fused) run_stage(std::integral_constant<int, 2>{}, sl, nkb);
+        else run_stage(std::integral_constant<int, 1>{}, sl, nkb);
         // the slot is read (the arrive releases the warp's reads of it to the producer)
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
         ++cs;
       }
+#pragma unroll
+      for (int j = 0; j < NT; ++j)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[j][q] += acc2[j][q];
+          accu[j][q] += accu2[j][q];
+        }
       if (!ok) break;
       // ---------------------------------------------- epilogue of a 128-row tile
       const int Mo = fused ? (r.sh ? Is : I) : H;

@@ -19,8 +19,9 @@ pytestmark = pytest.mark.gpu
 @pytest.fixture(scope="module")
 def moe():
     import expert_dispatch_streaming_gb300 as m
-    m.set_decode_kernel(True)
-    return m
+    m.set_decode_kernel("always")
+    yield m
+    m.set_decode_kernel("auto")
 
 
 @pytest.fixture(scope="module")
@@ -43,7 +44,7 @@ SMALL = [
 
 
 def _run(moe, syn, dl, cfg, xb, T, residual=None, normed=False, forced=None, decode=True):
-    moe.set_decode_kernel(decode)
+    moe.set_decode_kernel("always" if decode else "off")
     try:
         x = syn.to_device_bits(xb)
         ws = dl.workspace(T)
@@ -56,7 +57,7 @@ def _run(moe, syn, dl, cfg, xb, T, residual=None, normed=False, forced=None, dec
         assert moe.moe_workspace_error(ws) == 0
         return (syn.bits_of(out), ids.cpu().numpy(), syn.bits_of(un) if normed else None, st)
     finally:
-        moe.set_decode_kernel(True)
+        moe.set_decode_kernel("always")
 
 
 @pytest.mark.parametrize("cfg", SMALL, ids=lambda c: c.name)
