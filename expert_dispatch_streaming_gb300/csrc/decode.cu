@@ -56,7 +56,7 @@ constexpr int kSmemBytes = kSlots * kSlotBytes;      // the ring
 constexpr int kResSlots = 2;
 constexpr int kResOff = (kSlots - kResSlots) * kSlotBytes;
 constexpr int kResBytes = kResSlots * kSlotBytes;
-static_assert(sizeof(TailSmem) <= (size_t)kResBytes, "gating scratch fits in the reserved slots");
+static_assert(sizeof(CtaGateSmem) <= (size_t)kResBytes, "gating scratch fits in the reserved slots");
 static_assert(kResOff % 16 == 0, "the reserved region is 16-byte aligned");
 constexpr int kRouteEntry = 8;                       // route table words per expert slot
 constexpr unsigned kBackoffMaxNs = 256;              // polling back-off cap
@@ -369,7 +369,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   const float* rw = reinterpret_cast<const float*>(res);
   const uint16_t* rx = reinterpret_cast<const uint16_t*>(res + (size_t)p.hps * E * 4);
   const uint16_t* rg = rx + (size_t)T * p.hps;
-  TailSmem& sm = *reinterpret_cast<TailSmem*>(res);   // gating, after the router step
+  CtaGateSmem& cg = *reinterpret_cast<CtaGateSmem*>(res);   // gating, after the router step
+  TailSmem& sm = cg.tail;
   const bool producer = warp == kConsumerWarps;
 
   if (tid == 0) {
@@ -488,8 +489,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
       }
       for (int e = tid; e < kMaxExperts; e += kConsumerWarps * 32) {
         sm.hist[e] = 0;
-        sm.gc.lb[e] = real ? lbv : 0.f;
-        sm.gc.sb[e] = real ? sbv : 0.f;
+        cg.gc.lb[e] = real ? lbv : 0.f;
+        cg.gc.sb[e] = real ? sbv : 0.f;
       }
       cons_sync();
       GateParams q = p.g;
@@ -512,7 +513,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         q.shared_gate = nullptr;
         q.tie_flags = nullptr;
       }
-      gate_token_cta<kConsumerWarps * 32>(q, t, sm.lg, sm, [] { cons_sync(); });
+      gate_token_cta<kConsumerWarps * 32>(q, t, sm.lg, cg, [] { cons_sync(); });
       if (tid == 0) s_flag = Tn == 1 || atom_acq_rel_add(ctl + kCtlGateArrive, 1) == T - 1;
       cons_sync();
       if (s_flag) {
@@ -556,7 +557,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
             en[1] = off;
             en[2] = cnt;
             en[3] = en[4] = en[5] = en[6] = en[7] = 0;
-            sm.gc.rank[tid] = slot;                     // expert -> slot
+            cg.gc.rank[tid] = slot;                     // expert -> slot
           }
         }
         cons_sync();
@@ -569,7 +570,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           o_pos[i] = pp;
           o_src[pp] = i;
           if (rank < kDecodeMaxT)   // (forced ids may repeat an expert within a token)
-            reinterpret_cast<uint8_t*>(rt + sm.gc.rank[e] * kRouteEntry + 4)[rank] = (uint8_t)(i / k);
+            reinterpret_cast<uint8_t*>(rt + cg.gc.rank[e] * kRouteEntry + 4)[rank] = (uint8_t)(i / k);
         }
         cons_sync();
         const int n_act = s_flag;

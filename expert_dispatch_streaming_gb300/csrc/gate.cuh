@@ -361,7 +361,13 @@ struct alignas(16) GateCtaSmem {
   float l[kMaxExperts], s[kMaxExperts];   // one token's logits and selection scores
   float lb[kMaxExperts], sb[kMaxExperts]; // logit / selection biases (loaded ahead by the caller)
   int rank[kMaxExperts];
+  float cs[8 * (kMaxK + 1)];              // candidates: score, expert
+  int ci[8 * (kMaxK + 1)];
+  int wc[8];                              // per-warp counts
+  float vv[kMaxK];                        // unnormalised weights of the chosen, ascending id
+  int vid[kMaxK];
   float kth, nxt;                         // k-th and (k+1)-th selection scores
+  float M, Ssum, inv;
 };
 
 struct TailSmem {
@@ -369,72 +375,158 @@ struct TailSmem {
   float lrow[G_WARPS][kMaxExperts];
   double exact_s[G_WARPS][kMaxExperts];
   int hist[kMaxExperts], excl[kMaxExperts], srow[kSmallT * kMaxK];
+};
+
+// The scratch of gate_token_cta: the routing tail's and the CTA gating's own.
+struct CtaGateSmem {
+  TailSmem tail;
   GateCtaSmem gc;
 };
 
-// Gating of token t by NT threads of a CTA (small batches, where one token's gating is on the
-// critical path): the same selection rule and the same weights as gate_token, but the top-k
-// comes from ranking every expert against all others in parallel -- each thread counts the
-// experts that beat its own (score desc, id asc) -- instead of k + 1 dependent rounds of warp
-// arg-max.  When ids are forced, or the k-th and (k+1)-th fp32 scores lie within the margin
-// kTau, the first warp runs gate_token instead (fp64 re-scoring).  raw: the token's C summed
-// router outputs (shared memory); sm.gc.lb / sm.gc.sb hold the biases (zero when absent).
-// Threads 0 .. NT-1 must all call it; `sync` is their barrier.
+// Gating of token t by the 256 threads of eight warps (small batches, where one token's gating
+// is on the critical path): the same selection rule and the same weights as gate_token, with
+// the serial steps spread over the CTA.  Top-(k+1): thread e ranks expert e within its warp's
+// 32 (score desc, id asc); the at most k + 1 best of each warp are the candidates, and a
+// candidate's rank among the candidates is its rank among all experts whenever that is below
+// k + 1 (every expert that beats it beats it in its own warp too, so is a candidate).  The
+// weights are computed per chosen expert and normalised by one thread summing them in
+// ascending-id order, as gate_finish does.  When ids are forced, or the k-th and (k+1)-th fp32
+// scores lie within the margin kTau, the first warp runs gate_select / gate_finish instead
+// (fp64 re-scoring).  raw: the token's C summed router outputs (shared memory); cg.gc.lb /
+// cg.gc.sb hold the biases (zero when absent).  Threads 0 .. NT-1 must all call it; `sync` is
+// their barrier.
 template <int NT, class Sync>
 static __device__ __forceinline__ void gate_token_cta(const GateParams& p, int t, const float* raw,
-                                                      TailSmem& sm,
-                                      Sync sync) {
-  const int tid = threadIdx.x, E = p.E, k = p.k;
-  GateCtaSmem& g = sm.gc;
-  const int E4 = (E + 3) & ~3;
-  for (int e = tid; e < E4; e += NT) {
+                                                      CtaGateSmem& cg, Sync sync) {
+  TailSmem& sm = cg.tail;
+  static_assert(NT == kMaxExperts && NT == 8 * 32, "one thread per expert, eight warps");
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, E = p.E, k = p.k;
+  GateCtaSmem& g = cg.gc;
+  {
     float v = -CUDART_INF_F, sc = -CUDART_INF_F;
-    if (e < E) {
-      v = raw[e] + g.lb[e];
+    if (tid < E) {
+      v = raw[tid] + g.lb[tid];
       sc = v;
-      if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) sc = 1.f / (1.f + expf(-v)) + g.sb[e];
-      if (p.logits) p.logits[(size_t)t * E + e] = v;
+      if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) sc = 1.f / (1.f + expf(-v)) + g.sb[tid];
+      if (p.logits) p.logits[(size_t)t * E + tid] = v;
     }
-    g.l[e] = v;
-    g.s[e] = sc;
+    g.l[tid] = v;
+    g.s[tid] = sc;
+    g.rank[tid] = kMaxExperts;
   }
   if (tid == 0 && p.shared_gate && p.C > E) p.shared_gate[t] = 1.f / (1.f + expf(-raw[E]));
   if (tid == 0) g.kth = g.nxt = -CUDART_INF_F;
   sync();
-  for (int e = tid; e < E; e += NT) {
-    const float se = g.s[e];
-    int r = 0;
-    // four scores per shared-memory read; padding entries score -inf and never beat a real one
-    for (int e2 = 0; e2 < E4; e2 += 4) {
-      const float4 s4 = *reinterpret_cast<const float4*>(g.s + e2);
-      r += (s4.x > se || (s4.x == se && e2 < e)) ? 1 : 0;
-      r += (s4.y > se || (s4.y == se && e2 + 1 < e)) ? 1 : 0;
-      r += (s4.z > se || (s4.z == se && e2 + 2 < e)) ? 1 : 0;
-      r += (s4.w > se || (s4.w == se && e2 + 3 < e)) ? 1 : 0;
+  // ---- candidates: the k + 1 best of each warp's 32 experts
+  const int kp = min(k + 1, E);
+  const float se = g.s[tid];
+  int wr = 0;
+  if (w * 32 < E) {
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4) {
+      const float4 s4 = *reinterpret_cast<const float4*>(g.s + w * 32 + 4 * j4);
+      const int e0 = w * 32 + 4 * j4;
+      wr += better(s4.x, e0, se, tid) + better(s4.y, e0 + 1, se, tid) +
+            better(s4.z, e0 + 2, se, tid) + better(s4.w, e0 + 3, se, tid);
     }
-    g.rank[e] = r;
-    if (r == k - 1) g.kth = se;
-    if (r == k) g.nxt = se;
+  }
+  const bool cand = tid < E && wr < kp;
+  const unsigned cm = __ballot_sync(0xffffffffu, cand);
+  if (lane == 0) g.wc[w] = __popc(cm);
+  sync();
+  int base = 0, ncand = 0;
+#pragma unroll
+  for (int w2 = 0; w2 < 8; ++w2) {
+    const int c = g.wc[w2];
+    base += w2 < w ? c : 0;
+    ncand += c;
+  }
+  if (cand) {
+    const int idx = base + __popc(cm & ((1u << lane) - 1u));
+    g.cs[idx] = se;
+    g.ci[idx] = tid;
+  }
+  sync();
+  // ---- ranks of the candidates among the candidates
+  if (tid < ncand) {
+    const float sc = g.cs[tid];
+    const int id = g.ci[tid];
+    int r = 0;
+    for (int c = 0; c < ncand; ++c) r += better(g.cs[c], g.ci[c], sc, id);
+    g.rank[id] = r;
+    if (r == k - 1) g.kth = sc;
+    if (r == k) g.nxt = sc;
   }
   sync();
   const bool slow = p.forced != nullptr || (k < E && g.kth - g.nxt <= kTau);
-  if (threadIdx.x < 32) {
-    // (one gate_finish for both paths: the lane arrays then stay in registers)
-    float l[EC];
-    bool chosen[EC];
-    int flag = 0;
-    if (slow) {
+  if (slow) {
+    if (tid < 32) {
+      float l[EC];
+      bool chosen[EC];
+      int flag = 0;
       gate_select(p, t, raw, sm.lrow[0], sm.exact_s[0], l, chosen, flag);
-    } else {
-      const int lane = threadIdx.x;
-#pragma unroll
-      for (int c = 0; c < EC; ++c) {
-        const int e = lane + 32 * c;
-        l[c] = e < E ? g.l[e] : -CUDART_INF_F;
-        chosen[c] = e < E && g.rank[e] < k;
-      }
+      gate_finish(p, t, l, chosen, g.l, flag);
     }
-    gate_finish(p, t, l, chosen, g.l, flag);
+    sync();
+    return;
+  }
+  // ---- the chosen in ascending id order, their weights
+  const bool ch = tid < E && g.rank[tid] < k;
+  const unsigned m = __ballot_sync(0xffffffffu, ch);
+  if (lane == 0) g.wc[w] = __popc(m);
+  if (w == 0 && p.mode == MOE_GATING_SOFTMAX) {
+    // softmax over all E: the warp-wide max and sum, in gate_finish's order
+    float mx = -CUDART_INF_F;
+#pragma unroll
+    for (int c = 0; c < EC; ++c) mx = fmaxf(mx, lane + 32 * c < E ? g.l[lane + 32 * c] : -CUDART_INF_F);
+    const float Mx = warp_max(mx);
+    float sum = 0.f;
+#pragma unroll
+    for (int c = 0; c < EC; ++c)
+      if (lane + 32 * c < E) sum += expf(g.l[lane + 32 * c] - Mx);
+    sum = warp_sum(sum);
+    if (lane == 0) {
+      g.M = Mx;
+      g.Ssum = sum;
+    }
+  }
+  sync();
+  if (ch) {
+    int pos = __popc(m & ((1u << lane) - 1u));
+#pragma unroll
+    for (int w2 = 0; w2 < 8; ++w2) pos += w2 < w ? g.wc[w2] : 0;
+    g.vid[pos] = tid;
+  }
+  sync();
+  if (tid < k) {
+    const float lj = g.l[g.vid[tid]];
+    float v;
+    if (p.mode == MOE_GATING_SOFTMAX_RENORM) {
+      float mx = -CUDART_INF_F;
+      for (int j = 0; j < k; ++j) mx = fmaxf(mx, g.l[g.vid[j]]);
+      v = expf(lj - mx);
+    } else if (p.mode == MOE_GATING_SOFTMAX) {
+      v = expf(lj - g.M);
+    } else {
+      v = 1.f / (1.f + expf(-lj));
+    }
+    g.vv[tid] = v;
+  }
+  sync();
+  if (tid == 0) {
+    float denom = 0.f;
+    for (int j = 0; j < k; ++j) denom += g.vv[j];
+    if (p.mode == MOE_GATING_SOFTMAX) denom = g.Ssum;
+    g.inv = p.scale / denom;
+    if (p.tie_flags) p.tie_flags[t] = 0;
+  }
+  sync();
+  if (tid < k) {
+    const int e = g.vid[tid];
+    p.ids[(size_t)t * k + tid] = e;
+    if (p.ids_local) p.ids_local[tid] = e;
+    p.w[(size_t)t * k + tid] = g.vv[tid] * g.inv;
+    atomicAdd(&p.hist[(t / kTileT) * E + e], 1);
   }
   sync();
 }
