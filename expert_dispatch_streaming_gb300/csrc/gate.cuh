@@ -76,47 +76,96 @@ static __device__ __forceinline__ float sum_slices(const float* p, int S, size_t
   return (a0 + a1) + (a2 + a3);
 }
 
-// fp64 selection score of expert b for token t (the refinement of near-boundary experts)
+// Error-free transformations in fp32 (no fp64: GB300's fp64 rate is a small fraction of its
+// fp32 rate).  Each product x*w of a bf16 and an fp32 is split exactly into p + e (p the fp32
+// product, e = fma(x, w, -p)); each addition into a running sum hi is split exactly into the
+// new hi and its rounding error (Knuth's TwoSum), and the errors are gathered in lo.  The
+// intrinsics keep the compiler from contracting these steps into fused multiply-adds.
+static __device__ __forceinline__ void two_sum_into(float& hi, float& lo, float a) {
+  const float s = __fadd_rn(hi, a);
+  const float bp = __fsub_rn(s, hi);
+  const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(a, bp));
+  hi = s;
+  lo = __fadd_rn(lo, err);
+}
+static __device__ __forceinline__ void dot_term(float& hi, float& lo, float x, float w) {
+  const float p = __fmul_rn(x, w);
+  const float e = __fmaf_rn(x, w, -p);
+  two_sum_into(hi, lo, p);
+  lo = __fadd_rn(lo, e);
+}
+// (hi, lo) += (hi2, lo2)
+static __device__ __forceinline__ void df_add(float& hi, float& lo, float hi2, float lo2) {
+  two_sum_into(hi, lo, hi2);
+  lo = __fadd_rn(lo, lo2);
+}
+
+// Selection score of expert b for token t, accurate to far below the fp32 logit's error (the
+// refinement of near-boundary experts): the dot product x . W_r[:, b] in compensated fp32
+// (error of order H * 2^-48 * sum |x_h w_h|, about 1e-9 for the workloads' magnitudes against
+// the 1e-6 that decides a tie), then the bias and the sigmoid in fp64.
 static __device__ __forceinline__ double exact_score(const GateParams& p, int t, int b, int lane) {
   const uint16_t* xr = p.x + (size_t)t * p.H;
-  double d0 = 0.0, d1 = 0.0, d2 = 0.0, d3 = 0.0;
+  float hi[4] = {0.f, 0.f, 0.f, 0.f}, lo[4] = {0.f, 0.f, 0.f, 0.f};
   if (p.w_rT) {
-    // coalesced reads of the transposed router row; four interleaved fp64 sums (fixed order)
+    // the transposed router row: each lane takes 8 consecutive h per 256 (16-byte loads of x,
+    // 32 of W_r), four such chunks in flight before any arithmetic; four sums (fixed order)
     const float* wr = p.w_rT + (size_t)b * p.H;
-    int h = lane;
-    for (; h + 96 < p.H; h += 128) {
-      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wr[h], d0);
-      d1 = fma((double)bf16_bits_to_float(xr[h + 32]), (double)wr[h + 32], d1);
-      d2 = fma((double)bf16_bits_to_float(xr[h + 64]), (double)wr[h + 64], d2);
-      d3 = fma((double)bf16_bits_to_float(xr[h + 96]), (double)wr[h + 96], d3);
+    const int nch = p.H / 8;                   // 8-element chunks (H is a multiple of 8)
+    int c = lane;
+    for (; c + 96 < nch; c += 128) {
+      uint4 xq[4];
+      float4 wa[4], wb[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        xq[i] = *reinterpret_cast<const uint4*>(xr + 8 * (c + 32 * i));
+        wa[i] = *reinterpret_cast<const float4*>(wr + 8 * (c + 32 * i));
+        wb[i] = *reinterpret_cast<const float4*>(wr + 8 * (c + 32 * i) + 4);
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 x01 = bf16x2_to_float2(xq[i].x), x23 = bf16x2_to_float2(xq[i].y);
+        const float2 x45 = bf16x2_to_float2(xq[i].z), x67 = bf16x2_to_float2(xq[i].w);
+        dot_term(hi[i], lo[i], x01.x, wa[i].x);
+        dot_term(hi[i], lo[i], x01.y, wa[i].y);
+        dot_term(hi[i], lo[i], x23.x, wa[i].z);
+        dot_term(hi[i], lo[i], x23.y, wa[i].w);
+        dot_term(hi[i], lo[i], x45.x, wb[i].x);
+        dot_term(hi[i], lo[i], x45.y, wb[i].y);
+        dot_term(hi[i], lo[i], x67.x, wb[i].z);
+        dot_term(hi[i], lo[i], x67.y, wb[i].w);
+      }
     }
-    for (; h < p.H; h += 32) d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wr[h], d0);
+    for (; c < nch; c += 32)
+      for (int i = 0; i < 8; ++i) dot_term(hi[0], lo[0], bf16_bits_to_float(xr[8 * c + i]), wr[8 * c + i]);
   } else {
-    // strided column reads (one row of W_r per lane): eight independent sums keep eight loads
-    // in flight; fixed combination order
+    // strided column reads (one row of W_r per lane): eight loads in flight, four sums
     const float* wc = p.w_r + b;
     const size_t E = p.E;
-    double d4 = 0.0, d5 = 0.0, d6 = 0.0, d7 = 0.0;
     int h = lane;
     for (; h + 224 < p.H; h += 256) {
-      d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wc[(size_t)h * E], d0);
-      d1 = fma((double)bf16_bits_to_float(xr[h + 32]), (double)wc[(size_t)(h + 32) * E], d1);
-      d2 = fma((double)bf16_bits_to_float(xr[h + 64]), (double)wc[(size_t)(h + 64) * E], d2);
-      d3 = fma((double)bf16_bits_to_float(xr[h + 96]), (double)wc[(size_t)(h + 96) * E], d3);
-      d4 = fma((double)bf16_bits_to_float(xr[h + 128]), (double)wc[(size_t)(h + 128) * E], d4);
-      d5 = fma((double)bf16_bits_to_float(xr[h + 160]), (double)wc[(size_t)(h + 160) * E], d5);
-      d6 = fma((double)bf16_bits_to_float(xr[h + 192]), (double)wc[(size_t)(h + 192) * E], d6);
-      d7 = fma((double)bf16_bits_to_float(xr[h + 224]), (double)wc[(size_t)(h + 224) * E], d7);
-    }
-    for (; h < p.H; h += 32) d0 = fma((double)bf16_bits_to_float(xr[h]), (double)wc[(size_t)h * E], d0);
-    d0 += d4;
-    d1 += d5;
-    d2 += d6;
-    d3 += d7;
-  }
-  double d = (d0 + d1) + (d2 + d3);
+      float xv[8], wv[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+      for (int i = 0; i < 8; ++i) {
+        xv[i] = bf16_bits_to_float(xr[h + 32 * i]);
+        wv[i] = wc[(size_t)(h + 32 * i) * E];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dot_term(hi[i & 3], lo[i & 3], xv[i], wv[i]);
+    }
+    for (; h < p.H; h += 32) dot_term(hi[0], lo[0], bf16_bits_to_float(xr[h]), wc[(size_t)h * E]);
+  }
+  df_add(hi[0], lo[0], hi[1], lo[1]);
+  df_add(hi[2], lo[2], hi[3], lo[3]);
+  df_add(hi[0], lo[0], hi[2], lo[2]);
+  // warp sum by a butterfly (lane 0's result is the one the caller keeps: a fixed order)
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi[0], o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo[0], o);
+    df_add(hi[0], lo[0], h2, l2);
+  }
+  double d = (double)hi[0] + (double)lo[0];
   if (p.logit_bias) d += (double)p.logit_bias[b];
   if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
     d = 1.0 / (1.0 + exp(-d));
@@ -289,9 +338,16 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
           chosen[c] = d;
           n_def += __popc(__ballot_sync(0xffffffffu, d));
         }
+        // the band as eight warp-uniform words; one (not unrolled) loop over its members, so
+        // that exact_score is inlined once
+        unsigned bm[EC];
 #pragma unroll
+        for (int c = 0; c < EC; ++c) bm[c] = __ballot_sync(0xffffffffu, band[c]);
+#pragma unroll 1
         for (int c = 0; c < EC; ++c) {
-          unsigned m = __ballot_sync(0xffffffffu, band[c]);
+          unsigned m = 0;
+#pragma unroll
+          for (int c2 = 0; c2 < EC; ++c2) m = c2 == c ? bm[c2] : m;
           while (m) {
             const int b = 32 * c + __ffs(m) - 1;
             m &= m - 1;

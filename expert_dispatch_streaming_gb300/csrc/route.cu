@@ -116,17 +116,19 @@ reduce_slices_kernel(float* __restrict__ part, int S, int n) {
 // Tensor-core router input: the router (and shared-expert gate vector as row E) split into three
 // bf16 pieces hi + mid + lo (each the bf16 rounding of what the previous pieces leave), which
 // represent the fp32 weight; written as a tiled 128-byte-swizzled bf16 image of [Mpad x 3H]
-// (piece p of row m at k-tile p * H/64 + k/64), plus the transposed fp32 router for the fp64
+// (piece p of row m at k-tile p * H/64 + k/64), plus the transposed fp32 router for the exact
 // re-scoring.  Thread = (row m, 8-element chunk of k).  Block 0 also clears the histogram and
-// writes the one-group dispatch {0, T, 0, 1} the router GEMM runs over.
+// the router GEMM's split counters and writes the one-group dispatch {0, T, 0, 1} it runs over.
 __global__ void __launch_bounds__(256)
 router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w_gate, int H,
                    int E, int Mpad, int T, uint16_t* __restrict__ img, float* __restrict__ w_rT,
-                   int32_t* __restrict__ hist, int hist_n, int32_t* __restrict__ meta) {
+                   int32_t* __restrict__ hist, int hist_n, int32_t* __restrict__ meta,
+                   int32_t* __restrict__ ctr, int ctr_n) {
   pdl_trigger();
   pdl_wait();
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < hist_n; i += blockDim.x) hist[i] = 0;
+    for (int i = threadIdx.x; i < ctr_n; i += blockDim.x) ctr[i] = 0;
     if (threadIdx.x == 0) { meta[0] = 0; meta[1] = T; meta[2] = 0; meta[3] = 1; }
   }
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -311,6 +313,7 @@ RoutePlan plan_route(int T, int H, int E, int k, bool has_gate) {
     r.Mpad = (int)round_up(r.C, 128);
     r.S = 1;
     r.h_per_split = H;
+    r.tc_S = tc_router_splits(T, H, r.Mpad);
     return r;
   }
   const int tiles = ceil_div(T, R_BT) * ceil_div(r.C, R_BC);
@@ -335,9 +338,17 @@ size_t route_scratch(WsCursor& c, const RoutePlan& r, int T, int E, RouteScratch
   s.shared_meta = c.take<int32_t>(32);
   s.img = nullptr;
   s.w_rT = nullptr;
+  s.tc_part = nullptr;
+  s.tc_ctr = nullptr;
+  s.tc_ctr_n = 0;
   if (r.tc) {
     s.img = c.take<uint16_t>((size_t)3 * r.Mpad * r.h_per_split);
     s.w_rT = c.take<float>((size_t)E * r.h_per_split);
+    if (r.tc_S > 1) {
+      s.tc_part = c.take<float>((size_t)r.tc_S * T * r.Mpad);
+      s.tc_ctr_n = (r.Mpad / 128) * ceil_div(T, 128) * 4;
+      s.tc_ctr = c.take<int32_t>((size_t)s.tc_ctr_n);
+    }
   }
   if (out) *out = s;
   return c.used;
@@ -350,11 +361,11 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
       const size_t thr = (size_t)r.Mpad * (a.H / 8);
       MOE_LAUNCH_PDL(router_prep_kernel, dim3((unsigned)ceil_div((int)thr, 256)), dim3(256), 0, st,
                      a.w_r, a.w_gate, a.H, a.E, r.Mpad, a.T, s.img, s.w_rT, s.hist,
-                     r.ntiles * a.E, s.shared_meta);
+                     r.ntiles * a.E, s.shared_meta, s.tc_ctr, s.tc_ctr_n);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
       const int rr = launch_tc_router(a.x, a.T, a.H, s.img, r.Mpad, r.C, s.shared_meta, s.part,
-                                      a.err, st);
+                                      s.tc_part, s.tc_ctr, a.err, st);
       if (rr != MOE_OK) return rr;
     } else {
       dim3 g1(ceil_div(a.T, R_BT), ceil_div(r.C, R_BC), r.S);

@@ -37,6 +37,7 @@ struct RoutePlan {
   int ntiles;       // 128-token dispatch tiles
   int tc;           // 1: router product on the tensor cores (bf16 x 3 pieces), S = 1
   int Mpad;         // rows of the tensor-core router image (C rounded up to 128)
+  int tc_S;         // K splits of the tensor-core router product
   int small;        // 1: gating, scan, ranks and row copy in one CTA (T <= kSmallT)
 };
 
@@ -59,6 +60,9 @@ struct RouteScratch {
   int32_t* shared_meta;  // {0, T, 0, 1}: offsets / active list / count of the shared expert
   uint16_t* img;         // tensor-core router: [Mpad x 3H] tiled bf16 pieces
   float* w_rT;           // tensor-core router: [E][H] fp32
+  float* tc_part;        // tensor-core router, tc_S > 1: [tc_S][T][Mpad] fp32 partials
+  int32_t* tc_ctr;       // and its per-tile arrival counters [tiles][4] (cleared by the prep)
+  int tc_ctr_n;
 };
 
 struct RouteArgs {

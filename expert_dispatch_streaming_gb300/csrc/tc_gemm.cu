@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
           if (n < n_here) {
             const size_t row = (size_t)(x.r0 + x.nt * BN + n);
             const float gv = __uint_as_float(g[j]) * gsc;
-            if (ROUTER) {
+            if (ROUTER && x.S == 1) {
               if (m < p.m_limit) p.out_f32[row * p.ldo + m] = gv;
             } else if (x.S == 1) {
               const float o = FUSED ? silu_mul(gv, __uint_as_float(v[j]) * usc) : gv;
@@ -637,7 +637,50 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
           if (last) *ctr = 0;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
+        if (last && ROUTER) {
+          // router logits (up to 128 token columns): lane = (4-row group m4, column nn) takes
+          // 16-byte loads of four rows, 16 columns per pass, the splits summed in split order
+          // with four splits' loads in flight
+          __threadfence();
+          const int m4 = lane & 7, nn = lane >> 3, mq = x.mt * 128 + q * 32 + 4 * m4;
+          for (int n0 = 0; n0 < n_here; n0 += 16) {
+            float4 acc[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int sp0 = 0; sp0 < x.S; sp0 += 4) {
+              float4 v[4][4];
+#pragma unroll
+              for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const int n = n0 + nn + 4 * i, sp = sp0 + s4;
+                  v[s4][i] = (n < n_here && sp < x.S)
+                                 ? __ldcg(reinterpret_cast<const float4*>(
+                                       x.part + ((size_t)sp * x.max_rows + x.r0 + x.nt * BN + n) * MP + mq))
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+                }
+#pragma unroll
+              for (int s4 = 0; s4 < 4; ++s4)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  acc[i].x += v[s4][i].x;
+                  acc[i].y += v[s4][i].y;
+                  acc[i].z += v[s4][i].z;
+                  acc[i].w += v[s4][i].w;
+                }
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int n = n0 + nn + 4 * i;
+              if (n >= n_here) continue;
+              float* o = p.out_f32 + (size_t)(x.r0 + x.nt * BN + n) * p.ldo;
+              if (mq < p.m_limit) o[mq] = acc[i].x;
+              if (mq + 1 < p.m_limit) o[mq + 1] = acc[i].y;
+              if (mq + 2 < p.m_limit) o[mq + 2] = acc[i].z;
+              if (mq + 3 < p.m_limit) o[mq + 3] = acc[i].w;
+            }
+          }
+        } else if (last) {
           __threadfence();
           const size_t stride = (size_t)x.max_rows * MP;
           for (int n = 0; n < n_here; ++n) {
@@ -974,8 +1017,27 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
   return dispatch_wt(a1, pp.t1.BN, kp, st);
 }
 
+int tc_router_splits(int T, int H, int Mpad) {
+  // K splits of the router product: its tiles (Mpad / 128 x ceil(T / 128)) are few next to the
+  // SMs except at the largest batches.  Same rule as the expert GEMMs' split choice: the
+  // fewest waves of 1/S of the K range each, a little extra per split (the partial sums), at
+  // most 4 splits (one warp per 32-row quarter of a tile sums them) and 8 K steps per split.
+  const int tiles = (Mpad / 128) * ceil_div(T, 128), KT = 3 * H / 64, G = sm_count();
+  int best_s = 1;
+  double best = (double)ceil_div(tiles, G);
+  for (int S = 2; S <= std::min(4, KT / 8); ++S) {
+    const double c = (double)ceil_div(tiles * S, G) / S * (1.0 + 0.05 * (S - 1));
+    if (c < best * 0.97) {
+      best = c;
+      best_s = S;
+    }
+  }
+  return ceil_div(KT, ceil_div(KT, best_s));
+}
+
 int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,
-                     const int32_t* meta, float* logits, int32_t* err, cudaStream_t st) {
+                     const int32_t* meta, float* logits, float* part, int32_t* counters,
+                     int32_t* err, cudaStream_t st) {
   if (T <= 0) return MOE_OK;
   auto enc = encode_fn();
   if (!enc) return MOE_ERR_UNSUPPORTED;
@@ -997,8 +1059,10 @@ int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad,
   kp.w_off = 0;
   kp.K = 3 * H;
   kp.M = Mpad;
-  kp.S = 1;
-  kp.kt_per_split = 3 * H / 64;
+  kp.S = tc_router_splits(T, H, Mpad);
+  kp.kt_per_split = ceil_div(3 * H / 64, kp.S);
+  kp.part = part;          // [S][T][Mpad] fp32 when S > 1
+  kp.counters = counters;  // [tiles][4], zero on entry
   kp.max_rows = T;
   kp.err = err;
   kp.kb_mod = H / 64;

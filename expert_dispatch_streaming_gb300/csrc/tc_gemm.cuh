@@ -59,8 +59,12 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
 
 // Router logits on the tensor cores: logits[t][c] (c < C, fp32, row stride C) =
 // sum_k img[c][k] * x[t][k mod H] with img the [Mpad x 3H] tiled bf16 image of the three
-// router pieces (see router_prep in route.cu); one group of T rows (offsets {0, T}).
+// router pieces (see router_prep in route.cu); one group of T rows (offsets {0, T}).  The K
+// range is split tc_router_splits(T, H, Mpad) ways: part = [S][T][Mpad] fp32 partials and
+// counters = [Mpad / 128 * ceil(T / 128)][4] ints, zero on entry (left zero), when S > 1.
+int tc_router_splits(int T, int H, int Mpad);
 int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,
-                     const int32_t* meta, float* logits, int32_t* err, cudaStream_t st);
+                     const int32_t* meta, float* logits, float* part, int32_t* counters,
+                     int32_t* err, cudaStream_t st);
 
 }  // namespace moe
