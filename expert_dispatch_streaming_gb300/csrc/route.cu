@@ -287,6 +287,41 @@ gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ s
   for (int v = lane; v < nvec; v += 32) d[v] = __ldg(s + v);
 }
 
+// x_perm[pos[t k + j]] = x[t] for j < k: one warp per token, each 4 KB piece of the row read
+// once and stored to the token's k rows (the destination-order copy above reads every source
+// row k times, which the L2 stops absorbing once x_perm's stream evicts x)
+__global__ void __launch_bounds__(256)
+scatter_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ pos, int T, int k,
+                    int H, uint16_t* __restrict__ x_perm) {
+  pdl_trigger();
+  pdl_wait();
+  const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (t >= T) return;
+  const int nvec = H / 8;
+  const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  int dst[kMaxK];
+#pragma unroll
+  for (int j = 0; j < kMaxK; ++j) dst[j] = j < k ? __ldg(pos + (size_t)t * k + j) : 0;
+  for (int v0 = 0; v0 < nvec; v0 += 256) {
+    uint4 q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int v = v0 + lane + 32 * i;
+      q[i] = v < nvec ? __ldg(s + v) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      uint4* d = reinterpret_cast<uint4*>(x_perm + (size_t)dst[j] * H);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int v = v0 + lane + 32 * i;
+        if (v < nvec) d[v] = q[i];
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------ A2-A4, small T
 // Everything after the router product for a batch of at most kSmallT tokens, in one CTA (the
 // body is route_tail_block in gate.cuh, shared with the fused decode kernel).
@@ -425,8 +460,10 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
     if (a.x_perm && !fused_copy) {
-      const int rr = launch_gather(a.x, a.src, a.T * a.k, a.k, a.H, a.x_perm, st);
-      if (rr != MOE_OK) return rr;
+      MOE_LAUNCH_PDL(scatter_rows_kernel, dim3(ceil_div(a.T * 32, 256)), dim3(256), 0, st, a.x,
+                     a.pos, a.T, a.k, a.H, a.x_perm);
+      MOE_COUNT_LAUNCH();
+      MOE_LAUNCH_CHECK();
     }
   }
   return MOE_OK;
