@@ -460,10 +460,17 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
     if (a.x_perm && !fused_copy) {
-      MOE_LAUNCH_PDL(scatter_rows_kernel, dim3(ceil_div(a.T * 32, 256)), dim3(256), 0, st, a.x,
-                     a.pos, a.T, a.k, a.H, a.x_perm);
-      MOE_COUNT_LAUNCH();
-      MOE_LAUNCH_CHECK();
+      if (a.T >= kSeparateGatherMinT) {
+        // large batches: by token (every source row read once)
+        MOE_LAUNCH_PDL(scatter_rows_kernel, dim3(ceil_div(a.T * 32, 256)), dim3(256), 0, st,
+                       a.x, a.pos, a.T, a.k, a.H, a.x_perm);
+        MOE_COUNT_LAUNCH();
+        MOE_LAUNCH_CHECK();
+      } else {
+        // smaller ones: by destination row (k times the warps; x stays in L2)
+        const int rr = launch_gather(a.x, a.src, a.T * a.k, a.k, a.H, a.x_perm, st);
+        if (rr != MOE_OK) return rr;
+      }
     }
   }
   return MOE_OK;
