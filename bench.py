@@ -133,9 +133,9 @@ KERNEL_SOURCES = ["expert_dispatch_streaming_gb300/csrc/tc_gemm.cu",
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 
 
-def kernel_sources_sha256():
+def kernel_sources_sha256(files=None):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in (files or KERNEL_SOURCES):
         with open(os.path.join(ROOT, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()
@@ -151,10 +151,10 @@ def profiled_traffic(workload, T, E, kernel):
         entries = json.load(open(TRAFFIC_FILE))["entries"]
     except (ValueError, KeyError):
         return None
-    sha = kernel_sources_sha256()
     for e in entries:
         if (e.get("workload"), e.get("T"), e.get("kernel")) == (workload, T, kernel):
-            if e.get("kernel_source_sha256") != sha:
+            # the entry's own source list (default: the expert GEMM's)
+            if e.get("kernel_source_sha256") != kernel_sources_sha256(e.get("sources")):
                 return None
             return int(e["traffic_bytes_per_launch"])
     return None
@@ -325,7 +325,8 @@ def run_ours(args, rank, world, local_rank):
         w = layer_work(c, T, r["n_unique"], r["merged"])
         if r.get("fused"):
             roof = roofline_of(w["flops"], w["bytes"], sum(r["phase_ms"]) / 1e3, pk)
-            roof.update({"kernel": "decode_layer_kernel (whole layer)", "traffic": None,
+            roof.update({"kernel": "decode_layer_kernel (whole layer)",
+                         "traffic": profiled_traffic(wname, T, c.E, "decode_layer_kernel"),
                          "peak_source": pk["source"], "share_of_step": 1.0})
             return w, roof
         share = np.array(r["phase_ms"]) / max(sum(r["phase_ms"]), 1e-9)
