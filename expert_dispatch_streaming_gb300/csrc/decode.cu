@@ -600,9 +600,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   int32_t* dn_blk = ctl + p.o_dnblk;
   int32_t* comb_t = ctl + p.o_combt;
 
-  // The unit u of the static schedule, in the order shared gate/up, shared down, routed
-  // gate/up, routed down, combine, normalisation (the same decoding in the producer and the
-  // consumers): the shared expert needs no routing, so it streams while routing runs.  Routed
+  // The unit u of the schedule, in the order shared gate/up, routed gate/up, shared down,
+  // routed down, combine, normalisation (the same decoding in the producer and the consumers):
+  // the shared expert's gate/up needs no routing, so it streams while routing runs, and every
+  // gate/up unit is handed out before the down units that wait for it.  Routed
   // units resolve their expert from the route table (n_act >= 0: routing is over, n_act experts
   // have rows); a routed slot beyond them has nothing to do.
   auto unit_of = [&](int u, int n_act) -> UnitRef {
@@ -610,15 +611,21 @@ __global__ void __launch_bounds__(kDecThreads, 1)
     r.type = -1;
     int v = u;
     bool down;
-    if (v < nA + nC) {
+    if (v < nA) {
       r.sh = true;
-      down = v >= nA;
-      if (down) v -= nA;
-    } else if (v < nA + nC + nB + nD) {
+      down = false;
+    } else if (v < nA + nB) {
       r.sh = false;
-      v -= nA + nC;
-      down = v >= nB;
-      if (down) v -= nB;
+      down = false;
+      v -= nA;
+    } else if (v < nA + nB + nC) {
+      r.sh = true;
+      down = true;
+      v -= nA + nB;
+    } else if (v < nA + nB + nC + nD) {
+      r.sh = false;
+      down = true;
+      v -= nA + nB + nC;
     } else if (v < nA + nC + nB + nD + nE) {
       r.type = 2;
       r.t = v - (nA + nC + nB + nD);
