@@ -206,7 +206,7 @@ DECODE_KERNEL = {"off": 0, "auto": 1, "always": 2}
 
 def set_decode_kernel(mode) -> None:
     """The fused decode kernel for small batches with resident bundles: 'auto' (default; INT4
-    weights only up to 8 tokens), 'always', or 'off'.  True / False mean 'auto' / 'off'."""
+    weights only up to 4 tokens), 'always', or 'off'.  True / False mean 'auto' / 'off'."""
     if isinstance(mode, bool):
         mode = "auto" if mode else "off"
     moe_set_option(MOE_OPT_DECODE_KERNEL, DECODE_KERNEL[mode])

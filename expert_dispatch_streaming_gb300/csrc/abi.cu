@@ -476,10 +476,10 @@ int moe_layer_forward(const moe_layer* L, const uint16_t* x, int T, const int32_
   // (the fused kernel bulk-copies the router slice: W_r and the gate column 16-byte aligned)
   const bool dec_aligned = aligned16(L->w_r) && (!L->w_gate || aligned16(L->w_gate)) &&
                            (!residual || aligned16(residual));
-  // auto: INT4 weights only up to 8 tokens; above that the in-register dequantisation on the
+  // auto: INT4 weights only up to 4 tokens; above that the in-register dequantisation on the
   // fused kernel's eight consumer warps per SM is slower than the step-by-step kernels'
   const bool dec_wanted =
-      g_decode_path == 2 || (g_decode_path == 1 && (L->wdtype != MOE_W_INT4_G128 || T <= 8));
+      g_decode_path == 2 || (g_decode_path == 1 && (L->wdtype != MOE_W_INT4_G128 || T <= 4));
   if (!cache && P.dec.ok && dec_wanted && dec_aligned && (!L->Is || (s.h_s && s.s))) {
     // small batch, every bundle resident: the whole layer in one cooperative launch
     DecodeArgs da{};

@@ -35,6 +35,7 @@
 #include "decode.cuh"
 #include "gate.cuh"
 
+#include <cmath>
 #include <type_traits>
 
 namespace moe {
@@ -1185,10 +1186,14 @@ DecodePlan plan_decode(int T, int H, int E, int k, int I, int Is, int wdtype, bo
   }
   p.Umax = std::min(E, T * k);
   const int KW = wdtype == 0 ? 64 : 128;
-  const int ngu = p.Umax * (I / 128) + Is / 128;
+  // the splits are chosen for the expected number of experts with rows under uniform routing,
+  // E (1 - (1 - k/E)^T), not the bound Umax (the buffers are sized by Umax)
+  const double p_used = 1.0 - std::pow(1.0 - (double)k / E, (double)T);
+  const int U_est = std::max(1, std::min(p.Umax, (int)std::ceil(E * p_used - 1e-9)));
+  const int ngu = U_est * (I / 128) + Is / 128;
   p.Sg = best_split(ngu, H / KW, p.grid);
   p.Sgs = p.Sg;
-  const int ndn = (p.Umax + (Is ? 1 : 0)) * (H / 128);
+  const int ndn = (U_est + (Is ? 1 : 0)) * (H / 128);
   p.Sd = best_split(ndn, I / KW, p.grid);
   p.Sds = Is ? best_split(ndn, Is / KW, p.grid) : 1;
   p.NB = ceil_div(H, kColBlock);

@@ -73,7 +73,7 @@ int moe_version(void);
  *  MOE_OPT_DECODE_KERNEL: 2 = moe_layer_forward runs a batch of at most 16 tokens with every
  *    bundle resident (no cache) as one cooperative launch that routes, runs the shared and
  *    routed experts and combines; 1 (default) = the same except for INT4 weights with more
- *    than 8 tokens, which take the step-by-step kernels (faster for them there on GB300);
+ *    than 4 tokens, which take the step-by-step kernels (faster for them there on GB300);
  *    0 = always the step-by-step kernels.  Both compute the same layer (same roundings; sums in a different
  *    fixed order). */
 enum moe_option { MOE_OPT_FFN_KERNEL = 1, MOE_OPT_PDL = 2, MOE_OPT_DECODE_KERNEL = 3 };
