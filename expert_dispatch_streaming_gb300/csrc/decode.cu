@@ -9,20 +9,21 @@
 // overhead).  Here one persistent grid does everything and the steps meet at counters in
 // global memory instead of at kernel boundaries:
 //
-//   router    CTA b < S sums the router product over one H slice for all tokens (fp32
-//             partials); CTA t < T then sums token t's partials and gates it (the same
-//             device code as the routing kernels: top-k with fp64 re-scoring near the
-//             boundary); the last token to be gated builds the histogram, scan and stable
-//             ranks and raises a flag;
-//   experts   CTA units over one 128-row weight tile and a range of K: shared-expert gate/up
-//             (needs no routing, so it streams while routing runs), routed gate/up (after the
-//             flag), shared and routed down (each after the gate/up tiles of its expert).  A
-//             producer warp streams the unit's weight tiles with bulk asynchronous copies into
-//             a six-slot 216 KB shared-memory ring (full / empty mbarriers per slot); eight
-//             consumer warps each multiply 16 of the tile's rows on mma.m16n8k16 (weights as
-//             the M side, tokens on the narrow N side, INT4 / NVFP4 dequantised in registers).
-//             A unit's K range may be split: the last split to arrive sums the partials in
-//             split order;
+//   router    CTA b < S bulk-copies one H slice of W_r (and of x and the shared-gate column)
+//             and sums the router product over it for all tokens (fp32 partials); the last T
+//             CTAs then each sum one token's partials and gate it (top-k over eight warps,
+//             the exact re-scoring near the boundary as in the routing kernels); the last
+//             token to be gated builds the histogram, scan, stable ranks and a route table
+//             and raises a flag;
+//   experts   units of one 128-row weight tile and a range of K, handed out by a grid-wide
+//             counter in the order shared gate/up (needs no routing, so it streams while
+//             routing runs), routed gate/up (after the flag), shared and routed down (each
+//             after the gate/up tiles of its K range).  A producer warp streams the unit's
+//             weight tiles with bulk asynchronous copies into a six-slot 217 KB shared-memory
+//             ring (full / empty mbarriers per slot); eight consumer warps each multiply 16 of
+//             the tile's rows on mma.m16n8k16 (weights as the M side, tokens on the narrow N
+//             side, INT4 / NVFP4 dequantised in registers).  A unit's K range may be split:
+//             the last split to arrive sums the partials in split order;
 //   combine   per token, 256 columns per warp, once every down tile of the block has landed:
 //             the gate-weighted sum, the shared term and the residual, and the block's sum of
 //             squares; the optional RMS-normalised output once every block of the token is in.
