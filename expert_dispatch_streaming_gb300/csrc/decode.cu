@@ -736,13 +736,10 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         if (fused) brow = p.x + (size_t)tok * H;
         else brow = r.sh ? p.hs + (size_t)lane * Is : p.h + (size_t)(r.r0 + lane) * I;
       }
-      if (!fused) {
-        // the unit's K range of h comes from other CTAs' gate/up tiles: wait for those, then
-        // order their generic-proxy writes before this warp's bulk (async-proxy) reads
-        const int t_lo = r.kb_lo * KW / 128, t_hi = (r.kb_hi * KW + 127) / 128;
-        if (!warp_wait_flags(tdone + r.slot * p.mtg + t_lo, t_hi - t_lo, p.err)) break;
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-      }
+      // a down unit's K range of h comes from other CTAs' gate/up tiles; its first weight
+      // tiles are already on their way when the producer waits for those
+      bool h_ready = fused;
+      const int t_lo = r.kb_lo * KW / 128, t_hi = (r.kb_hi * KW + 127) / 128;
       if (!push(u, n_act)) break;
       for (int kb = r.kb_lo; kb < r.kb_hi; kb += BPS) {
         const int s = gs % kSlots;
@@ -772,6 +769,16 @@ __global__ void __launch_bounds__(kDecThreads, 1)
           const int rt = r.mt + (q ? Mup : 0);
           const char* src = r.wsec + ((size_t)rt * KT + kb + b) * TILE;
           bulk_g2s_hint(sb + (b * NG + q) * TILE, src, TILE, bar, wpol);
+        }
+        if (!h_ready) {
+          // wait for the gate/up tiles, then order their generic-proxy writes of h before
+          // this warp's bulk (async-proxy) reads of it
+          if (!warp_wait_flags(tdone + r.slot * p.mtg + t_lo, t_hi - t_lo, p.err)) {
+            ok = false;
+            break;
+          }
+          asm volatile("fence.proxy.async.global;" ::: "memory");
+          h_ready = true;
         }
         if (brow != nullptr) bulk_g2s(sb + kBOff + lane * BROW, brow + (size_t)kb * KW, brow_bytes, bar);
         ++gs;
