@@ -74,8 +74,9 @@ struct LayerPlan {
 };
 
 static GemmArgs gemm_args(const moe_bundle_layout& lay, int wdtype, bool fused, int K, int M,
-                          int E, int max_rows) {
+                          int E, int max_rows, int rows_cap = 0) {
   GemmArgs a{};
+  a.rows_cap = rows_cap;
   a.K = K;
   a.M = M;
   a.E = E;
@@ -100,8 +101,8 @@ static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
     return MOE_ERR_INVALID_ARG;
   const int rows = T * L->k;
   P->rp = plan_route(T, L->H, L->E, L->k, L->Is > 0 && L->shared_gate_sigmoid);
-  P->gu = plan_gemm(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows));
-  P->dn = plan_gemm(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows));
+  P->gu = plan_gemm(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows, T));
+  P->dn = plan_gemm(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows, T));
   if (L->Is) {
     GemmArgs sgu = gemm_args(P->slay, L->wdtype, true, L->H, L->Is, 1, T);
     GemmArgs sdn = gemm_args(P->slay, L->wdtype, false, L->Is, L->H, 1, T);
@@ -114,8 +115,8 @@ static int make_plan(const moe_layer* L, int T, LayerPlan* P) {
     }
     P->merged = P->gu.use_tc && P->dn.use_tc && P->sgu.use_tc && P->sdn.use_tc;
     if (P->merged) {
-      P->mgu = plan_tc_pair(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows), sgu);
-      P->mdn = plan_tc_pair(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows), sdn);
+      P->mgu = plan_tc_pair(gemm_args(P->lay, L->wdtype, true, L->H, L->I, L->E, rows, T), sgu);
+      P->mdn = plan_tc_pair(gemm_args(P->lay, L->wdtype, false, L->I, L->H, L->E, rows, T), sdn);
     }
   }
   P->dec = plan_decode(T, L->H, L->E, L->k, L->I, L->Is, L->wdtype,
@@ -182,7 +183,7 @@ static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratc
   const int rows = T * L->k;
   const int32_t* act = dx.active ? dx.active : s.rs.active;
   const int32_t* nact = dx.active ? dx.n_active : s.rs.n_active;
-  GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows);
+  GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows, T);
   gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = act;
   gu.n_active = nact; gu.tab = &tab; gu.out = s.h; gu.dev_tab = dx.tab;
   gu.host_n = host_n; gu.host_ids = host_ids;
@@ -190,7 +191,7 @@ static int run_experts(const moe_layer* L, const LayerPlan& P, const LayerScratc
   int r = launch_gemm(gu, pg, s.part, s.counters, s.err, st);
   if (r != MOE_OK) return r;
   if (between && (r = between()) != MOE_OK) return r;
-  GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
+  GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows, T);
   dn.xin = s.h; dn.offsets = s.offsets; dn.active = act;
   dn.n_active = nact; dn.tab = &tab; dn.out = s.y_perm; dn.dev_tab = dx.tab;
   dn.host_n = host_n; dn.host_ids = host_ids;
@@ -209,7 +210,7 @@ static int run_ffn_merged(const moe_layer* L, const LayerPlan& P, const LayerScr
   const int32_t* meta = s.rs.shared_meta;
   const int32_t* act = dx.active ? dx.active : s.rs.active;
   const int32_t* nact = dx.active ? dx.n_active : s.rs.n_active;
-  GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows);
+  GemmArgs gu = gemm_args(P.lay, L->wdtype, true, L->H, L->I, L->E, rows, T);
   gu.xin = s.x_perm; gu.offsets = s.offsets; gu.active = act;
   gu.n_active = nact; gu.tab = &tab; gu.out = s.h; gu.dev_tab = dx.tab;
   GemmArgs sgu = gemm_args(P.slay, L->wdtype, true, L->H, L->Is, 1, T);
@@ -218,7 +219,7 @@ static int run_ffn_merged(const moe_layer* L, const LayerPlan& P, const LayerScr
   int r = launch_tc_pair(gu, sgu, P.mgu, s.part, s.part_s, s.counters, s.err, st);
   if (r != MOE_OK) return r;
   if (between && (r = between()) != MOE_OK) return r;
-  GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows);
+  GemmArgs dn = gemm_args(P.lay, L->wdtype, false, L->I, L->H, L->E, rows, T);
   dn.xin = s.h; dn.offsets = s.offsets; dn.active = act;
   dn.n_active = nact; dn.tab = &tab; dn.out = s.y_perm; dn.dev_tab = dx.tab;
   GemmArgs sdn = gemm_args(P.slay, L->wdtype, false, L->Is, L->H, 1, T);

@@ -187,12 +187,9 @@ __device__ bool cons_wait_geq(const int32_t* ctr, int target, int32_t* err) {
   return ok != 0;
 }
 // The routing flag holds the number of experts with rows + 1 once routing is over.  The warp
-// (cons_: the consumer threads) waits for it and gets that number, or -1 when a wait gave up.
+// waits for it and gets that number, or -1 when a wait gave up.
 __device__ int warp_wait_route(const int32_t* flag, int32_t* err) {
   return warp_wait_geq(flag, 1, err) ? __ldcg(flag) - 1 : -1;
-}
-__device__ int cons_wait_route(const int32_t* flag, int32_t* err) {
-  return cons_wait_geq(flag, 1, err) ? __ldcg(flag) - 1 : -1;
 }
 // The warp waits until flags f[0 .. n) are all set (each lane polls its share).
 __device__ bool warp_wait_flags(const int32_t* f, int n, int32_t* err) {
@@ -515,7 +512,8 @@ __global__ void __launch_bounds__(kDecThreads, 1)
         q.shared_gate = nullptr;
         q.tie_flags = nullptr;
       }
-      gate_token_cta<kConsumerWarps * 32>(q, t, sm.lg, cg, [] { cons_sync(); });
+      gate_token_cta<kConsumerWarps * 32>(q, t, sm.lg, cg.gc, sm.lrow[0], sm.exact_s[0],
+                                          [] { cons_sync(); });
       if (tid == 0) s_flag = Tn == 1 || atom_acq_rel_add(ctl + kCtlGateArrive, 1) == T - 1;
       cons_sync();
       if (s_flag) {
@@ -1219,11 +1217,11 @@ int launch_decode(const DecodeArgs& a, const DecodePlan& pl, cudaStream_t st) {
   if (!pl.ok) return MOE_ERR_UNSUPPORTED;
   DecParams p{};
   GateParams& gp = p.g;
-  gp.part = a.part; gp.S = pl.S; gp.C = pl.C;
+  gp.part = a.part; gp.S = pl.S; gp.C = pl.C; gp.ldp = pl.C;
   gp.x = a.x; gp.w_r = a.w_r; gp.w_rT = nullptr; gp.logit_bias = a.logit_bias;
   gp.sel_bias = a.sel_bias; gp.forced = a.forced; gp.T = a.T; gp.H = a.H; gp.E = a.E; gp.k = a.k;
   gp.mode = a.gating; gp.scale = a.scale; gp.ids = a.ids; gp.w = a.w; gp.logits = nullptr;
-  gp.shared_gate = a.shared_gate; gp.tie_flags = a.tie; gp.hist = nullptr; gp.tok_per_warp = 1;
+  gp.shared_gate = a.shared_gate; gp.tie_flags = a.tie; gp.hist = nullptr;
   p.x = a.x; p.w_gate = a.w_gate; p.residual = a.residual; p.out = a.out; p.out_n = a.out_n;
   p.eps = a.eps;
   p.counts = a.counts; p.offsets = a.offsets; p.pos = a.pos; p.src = a.src;

@@ -28,6 +28,8 @@ struct GemmArgs {
   int K, M, E;
   int int4, fp4, fused;
   int max_rows;             // upper bound of offsets[E]
+  int rows_cap;             // upper bound of one expert's rows (T for a routed batch: a token
+                            // picks an expert at most once); 0: max_rows
   uint16_t* out;            // [rows][M]
 };
 

@@ -174,6 +174,76 @@ static __device__ __forceinline__ double exact_score(const GateParams& p, int t,
   return d;
 }
 
+// exact_score by the NT threads of a CTA: thread i takes the 8-element chunks i, i + NT, ...
+// of the dot product (compensated fp32), each warp combines its lanes by the butterfly, and
+// thread 0 the warps' pairs in warp order, then adds the bias and the sigmoid in fp64.  For
+// the one token whose selection waits on it, the H-long dot product spread over the CTA
+// costs about one memory latency instead of one per 256 elements.  `wpart` holds 2 floats
+// per warp; all NT threads must call it; `sync` is their barrier; the result is thread 0's.
+template <int NT, class Sync>
+static __device__ __forceinline__ double exact_score_cta(const GateParams& p, int t, int b,
+                                                         float* wpart, Sync sync) {
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const uint16_t* xr = p.x + (size_t)t * p.H;
+  float hi = 0.f, lo = 0.f;
+  const int nch = p.H / 8;
+  if (p.w_rT) {
+    const float* wr = p.w_rT + (size_t)b * p.H;
+    for (int c = tid; c < nch; c += NT) {
+      const uint4 xq = *reinterpret_cast<const uint4*>(xr + 8 * c);
+      const float4 wa = *reinterpret_cast<const float4*>(wr + 8 * c);
+      const float4 wb = *reinterpret_cast<const float4*>(wr + 8 * c + 4);
+      const float2 x01 = bf16x2_to_float2(xq.x), x23 = bf16x2_to_float2(xq.y);
+      const float2 x45 = bf16x2_to_float2(xq.z), x67 = bf16x2_to_float2(xq.w);
+      dot_term(hi, lo, x01.x, wa.x);
+      dot_term(hi, lo, x01.y, wa.y);
+      dot_term(hi, lo, x23.x, wa.z);
+      dot_term(hi, lo, x23.y, wa.w);
+      dot_term(hi, lo, x45.x, wb.x);
+      dot_term(hi, lo, x45.y, wb.y);
+      dot_term(hi, lo, x67.x, wb.z);
+      dot_term(hi, lo, x67.y, wb.w);
+    }
+  } else {
+    const float* wc = p.w_r + b;
+    const size_t E = p.E;
+    for (int c = tid; c < nch; c += NT) {
+      float xv[8], wv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        xv[i] = bf16_bits_to_float(xr[8 * c + i]);
+        wv[i] = wc[(size_t)(8 * c + i) * E];
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) dot_term(hi, lo, xv[i], wv[i]);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
+    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
+    df_add(hi, lo, h2, l2);
+  }
+  if (lane == 0) {
+    wpart[2 * w] = hi;
+    wpart[2 * w + 1] = lo;
+  }
+  sync();
+  double d = 0.0;
+  if (tid == 0) {
+    float h = wpart[0], l = wpart[1];
+    for (int w2 = 1; w2 < NT / 32; ++w2) df_add(h, l, wpart[2 * w2], wpart[2 * w2 + 1]);
+    d = (double)h + (double)l;
+    if (p.logit_bias) d += (double)p.logit_bias[b];
+    if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
+      d = 1.0 / (1.0 + exp(-d));
+      if (p.sel_bias) d += (double)p.sel_bias[b];
+    }
+  }
+  sync();
+  return d;
+}
+
 // Chosen list (ascending id, or the forced order) and weights of token t by one warp, from the
 // lane's logits l[c] (experts lane + 32 c), its chosen flags and the token's logits row lrow.
 static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
@@ -259,11 +329,13 @@ static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
 // experts.  Out: the lane's logits l[c] and chosen flags (experts lane + 32 c), the tie flag;
 // writes the token's logits row lrow, logits and shared gate.  `raw` = the token's C summed
 // router outputs (or NULL: sum the S slices of p.part); lrow / exact_s = this warp's
-// shared-memory rows.  Inlined into each kernel, so that the parameter block's fields and the
+// shared-memory rows; pre: exact_s already holds the re-scored band (NaN where not).
+// Inlined into each kernel, so that the parameter block's fields and the
 // lane arrays stay in registers.
 static __device__ __forceinline__ void gate_select(const GateParams& p, int t, const float* raw,
                                                    float* lrow, double* exact_s, float (&l)[EC],
-                                                   bool (&chosen)[EC], int& flag_out) {
+                                                   bool (&chosen)[EC], int& flag_out,
+                                                   bool pre = false) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   {
@@ -274,7 +346,7 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
       const int e = lane + 32 * c;
       float v = -CUDART_INF_F, s = -CUDART_INF_F;
       if (e < E) {
-        v = raw ? raw[e] : sum_slices(p.part + (size_t)t * p.C + e, p.S, (size_t)p.T * p.C);
+        v = raw ? raw[e] : sum_slices(p.part + (size_t)t * p.ldp + e, p.S, (size_t)p.T * p.ldp);
         if (p.logit_bias) v += p.logit_bias[e];
         s = v;
         if (p.mode == MOE_GATING_SIGMOID_BIAS_RENORM) {
@@ -289,7 +361,7 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
     }
     if (lane == 0 && p.shared_gate && p.C > E) {
       const float z =
-          raw ? raw[E] : sum_slices(p.part + (size_t)t * p.C + E, p.S, (size_t)p.T * p.C);
+          raw ? raw[E] : sum_slices(p.part + (size_t)t * p.ldp + E, p.S, (size_t)p.T * p.ldp);
       p.shared_gate[t] = 1.f / (1.f + expf(-z));
     }
 
@@ -351,7 +423,10 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
           while (m) {
             const int b = 32 * c + __ffs(m) - 1;
             m &= m - 1;
-            double s = exact_score(p, t, b, lane);
+            // (pre: the caller re-scored the band already; a NaN marks one it did not)
+            double s = pre ? exact_s[b] : CUDART_NAN;
+            if (s != s) s = exact_score(p, t, b, lane);
+            __syncwarp();
             if (lane == 0) exact_s[b] = s;
           }
         }
@@ -424,6 +499,8 @@ struct alignas(16) GateCtaSmem {
   int vid[kMaxK];
   float kth, nxt;                         // k-th and (k+1)-th selection scores
   float M, Ssum, inv;
+  float wpart[16];                        // per-warp (hi, lo) pairs of a re-scoring
+  unsigned band[8];                       // per-warp masks of the experts to re-score
 };
 
 struct TailSmem {
@@ -433,7 +510,7 @@ struct TailSmem {
   int hist[kMaxExperts], excl[kMaxExperts], srow[kSmallT * kMaxK];
 };
 
-// The scratch of gate_token_cta: the routing tail's and the CTA gating's own.
+// The fused decode kernel's gating scratch: the routing tail's and gate_token_cta's.
 struct CtaGateSmem {
   TailSmem tail;
   GateCtaSmem gc;
@@ -448,16 +525,15 @@ struct CtaGateSmem {
 // weights are computed per chosen expert and normalised by one thread summing them in
 // ascending-id order, as gate_finish does.  When ids are forced, or the k-th and (k+1)-th fp32
 // scores lie within the margin kTau, the first warp runs gate_select / gate_finish instead
-// (fp64 re-scoring).  raw: the token's C summed router outputs (shared memory); cg.gc.lb /
-// cg.gc.sb hold the biases (zero when absent).  Threads 0 .. NT-1 must all call it; `sync` is
-// their barrier.
+// (fp64 re-scoring, with lrow0 / exact0 as that warp's rows).  raw: the token's C summed
+// router outputs (shared memory); g.lb / g.sb hold the biases (zero when absent).  Threads
+// 0 .. NT-1 must all call it; `sync` is their barrier.
 template <int NT, class Sync>
 static __device__ __forceinline__ void gate_token_cta(const GateParams& p, int t, const float* raw,
-                                                      CtaGateSmem& cg, Sync sync) {
-  TailSmem& sm = cg.tail;
+                                                      GateCtaSmem& g, float* lrow0, double* exact0,
+                                                      Sync sync) {
   static_assert(NT == kMaxExperts && NT == 8 * 32, "one thread per expert, eight warps");
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5, E = p.E, k = p.k;
-  GateCtaSmem& g = cg.gc;
   {
     float v = -CUDART_INF_F, sc = -CUDART_INF_F;
     if (tid < E) {
@@ -516,11 +592,35 @@ static __device__ __forceinline__ void gate_token_cta(const GateParams& p, int t
   sync();
   const bool slow = p.forced != nullptr || (k < E && g.kth - g.nxt <= kTau);
   if (slow) {
+    const bool pre = p.forced == nullptr;
+    if (pre) {
+      // the experts gate_select re-scores (its band: not clear of the boundary by kTau, and
+      // within kTau of the k-th score), re-scored here by the whole CTA; gate_select's own
+      // fp32 scores and margins are these, so it finds them all (a NaN would make it score a
+      // missing one itself)
+      const float sc = g.s[tid];
+      const bool def = tid < E && g.rank[tid] < k && sc - g.nxt > kTau;
+      const bool band = tid < E && !def && sc >= g.kth - kTau;
+      exact0[tid] = CUDART_NAN;
+      const unsigned bm = __ballot_sync(0xffffffffu, band);
+      if (lane == 0) g.band[w] = bm;
+      sync();
+      for (int w2 = 0; w2 < 8; ++w2) {
+        unsigned m = g.band[w2];
+        while (m) {
+          const int b = 32 * w2 + __ffs(m) - 1;
+          m &= m - 1;
+          const double d = exact_score_cta<NT>(p, t, b, g.wpart, sync);
+          if (tid == 0) exact0[b] = d;
+        }
+      }
+      sync();
+    }
     if (tid < 32) {
       float l[EC];
       bool chosen[EC];
       int flag = 0;
-      gate_select(p, t, raw, sm.lrow[0], sm.exact_s[0], l, chosen, flag);
+      gate_select(p, t, raw, lrow0, exact0, l, chosen, flag, pre);
       gate_finish(p, t, l, chosen, g.l, flag);
     }
     sync();
@@ -679,9 +779,7 @@ static __device__ void route_tail_block(const GateParams& p, int32_t* __restrict
   static_assert(NT >= kMaxExperts, "the scan takes one thread per expert");
   float* lg = sm.lg;
   int* hist = sm.hist;
-  int* excl = sm.excl;
-  int* srow = sm.srow;
-  const int tid = threadIdx.x, lane = tid & 31, T = p.T, C = p.C, E = p.E, k = p.k;
+  const int tid = threadIdx.x, T = p.T, C = p.C, E = p.E, k = p.k;
   const int S = p.S, n = T * C;
   const size_t stride = (size_t)T * C;
 

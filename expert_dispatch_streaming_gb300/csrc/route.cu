@@ -9,10 +9,13 @@
 // Kernels
 //   router_partial_kernel  fp32 logits of a (token tile, column tile, H slice); the H slices
 //                          let a small batch spread the router read over every SM.
-//   gate_topk_kernel       one warp per token: sums the slices in fixed order, scores, picks the
-//                          top-k with warp shuffles, re-scores the experts whose fp32 score is
-//                          within the error margin of the k-th in fp64, writes ids / weights
-//                          and bumps the per-tile expert histogram.
+//   gate_cta_kernel        one CTA per token (grid-stride): sums the token's slices in fixed
+//                          order, scores, ranks the experts over the CTA (gate_token_cta),
+//                          re-scores the experts whose fp32 score is within the error margin of
+//                          the k-th (one warp, compensated sums), writes ids / weights and bumps
+//                          the per-tile expert histogram.
+//   gate_topk_kernel       the same gating by one warp per token (gate_token), for the largest
+//                          batches, where throughput rather than one token's latency counts.
 //   scan_kernel            one CTA: per-expert counts, exclusive offsets, per-tile bases and
 //                          the list of experts that received rows.
 //   rank_permute_kernel    one CTA per 128-token tile: stable rank of each (t, j) within its
@@ -49,37 +52,61 @@ router_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ 
   if (blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0)
     for (int i = tid; i < hist_n; i += blockDim.x) hist[i] = 0;
 
-  float acc[2][4] = {};
-  for (int h0 = h_lo; h0 < h_hi; h0 += R_KH) {
-    // x tile: 32 tokens x 32 h (bf16 -> fp32); 256 threads x 4 elements
-    for (int i = tid; i < R_BT * R_KH; i += 256) {
-      int tt = i / R_KH, hh = i % R_KH;
-      int t = t0 + tt, h = h0 + hh;
-      xs[hh][tt] = (t < T && h < h_hi) ? bf16_bits_to_float(x[(size_t)t * H + h]) : 0.f;
+  // The loads of up to kPf 32-row tiles are issued together, into registers, before any of
+  // them is used: a CTA's slice of a small batch is a few tiles, and one memory latency per
+  // tile (load, barrier, compute, barrier) would dominate it.
+  constexpr int kPf = 4;
+  float xv[kPf][R_BT * R_KH / 256], wv[kPf][R_KH * R_BC / 256];
+  auto load = [&](int h0, float (&xq)[R_BT * R_KH / 256], float (&wq)[R_KH * R_BC / 256]) {
+    // x tile: 32 tokens x 32 h (bf16 -> fp32); weight tile: 32 h x 64 columns, column E the
+    // shared-expert gate vector
+#pragma unroll
+    for (int j = 0; j < R_BT * R_KH / 256; ++j) {
+      const int i = tid + 256 * j, tt = i / R_KH, hh = i % R_KH, t = t0 + tt, h = h0 + hh;
+      xq[j] = (t < T && h < h_hi) ? bf16_bits_to_float(x[(size_t)t * H + h]) : 0.f;
     }
-    // weight tile: 32 h x 64 columns; column E is the shared-expert gate vector
-    for (int i = tid; i < R_KH * R_BC; i += 256) {
-      int hh = i / R_BC, cc = i % R_BC;
-      int h = h0 + hh, c = c0 + cc;
+#pragma unroll
+    for (int j = 0; j < R_KH * R_BC / 256; ++j) {
+      const int i = tid + 256 * j, hh = i / R_BC, cc = i % R_BC, h = h0 + hh, c = c0 + cc;
       float v = 0.f;
       if (h < h_hi) {
         if (c < E) v = w_r[(size_t)h * E + c];
         else if (c < C) v = bf16_bits_to_float(w_gate[h]);
       }
-      wsm[hh][cc] = v;
+      wq[j] = v;
     }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < R_KH; ++kk) {
-      float a0 = xs[kk][ty], a1 = xs[kk][ty + 16];
+  };
+  float acc[2][4] = {};
+  for (int hb = h_lo; hb < h_hi; hb += kPf * R_KH) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float b = wsm[kk][tx + 16 * q];
-        acc[0][q] = fmaf(a0, b, acc[0][q]);
-        acc[1][q] = fmaf(a1, b, acc[1][q]);
+    for (int f = 0; f < kPf; ++f)
+      if (hb + f * R_KH < h_hi) load(hb + f * R_KH, xv[f], wv[f]);
+#pragma unroll
+    for (int f = 0; f < kPf; ++f) {
+      if (hb + f * R_KH >= h_hi) break;
+#pragma unroll
+      for (int j = 0; j < R_BT * R_KH / 256; ++j) {
+        const int i = tid + 256 * j;
+        xs[i % R_KH][i / R_KH] = xv[f][j];
       }
+#pragma unroll
+      for (int j = 0; j < R_KH * R_BC / 256; ++j) {
+        const int i = tid + 256 * j;
+        wsm[i / R_BC][i % R_BC] = wv[f][j];
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int kk = 0; kk < R_KH; ++kk) {
+        float a0 = xs[kk][ty], a1 = xs[kk][ty + 16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float b = wsm[kk][tx + 16 * q];
+          acc[0][q] = fmaf(a0, b, acc[0][q]);
+          acc[1][q] = fmaf(a1, b, acc[1][q]);
+        }
+      }
+      __syncthreads();
     }
-    __syncthreads();
   }
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
@@ -93,24 +120,25 @@ router_partial_kernel(const uint16_t* __restrict__ x, const float* __restrict__ 
   }
 }
 
-// Sums the S H-slice partials of every logit into slice 0, in place (fixed order: eight
-// interleaved running sums over the slices, combined pairwise).  One thread per (token,
-// column); used when a small batch was spread over many slices, so that the gate kernel reads
-// one value per logit instead of S.
+// Sums the S H-slice partials of every logit into slice 0, in place: eight lanes per logit,
+// lane j summing slices j, j + 8, ... in order, the eight sums then combined pairwise by
+// shuffles (a fixed order).  Used when a small batch was spread over many slices, so that the
+// gate kernel reads one value per logit instead of S.
 __global__ void __launch_bounds__(256)
 reduce_slices_kernel(float* __restrict__ part, int S, int n) {
   pdl_trigger();
   pdl_wait();
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= n) return;
-  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  int sp = 0;
-  for (; sp + 8 <= S; sp += 8) {
-#pragma unroll
-    for (int j = 0; j < 8; ++j) a[j] += part[(size_t)(sp + j) * n + i];
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  const int i = g >> 3, j = g & 7;
+  float a = 0.f;
+  if (i < n) {
+#pragma unroll 4
+    for (int sp = j; sp < S; sp += 8) a += part[(size_t)sp * n + i];
   }
-  for (int j = 0; sp < S; ++sp, ++j) a[j] += part[(size_t)sp * n + i];
-  part[i] = ((a[0] + a[1]) + (a[2] + a[3])) + ((a[4] + a[5]) + (a[6] + a[7]));
+  a += __shfl_xor_sync(0xffffffffu, a, 1);
+  a += __shfl_xor_sync(0xffffffffu, a, 2);
+  a += __shfl_xor_sync(0xffffffffu, a, 4);
+  if (i < n && j == 0) part[i] = a;
 }
 
 // Tensor-core router input: the router (and shared-expert gate vector as row E) split into three
@@ -118,17 +146,15 @@ reduce_slices_kernel(float* __restrict__ part, int S, int n) {
 // represent the fp32 weight; written as a tiled 128-byte-swizzled bf16 image of [Mpad x 3H]
 // (piece p of row m at k-tile p * H/64 + k/64), plus the transposed fp32 router for the exact
 // re-scoring.  Thread = (row m, 8-element chunk of k).  Block 0 also clears the histogram and
-// the router GEMM's split counters and writes the one-group dispatch {0, T, 0, 1} it runs over.
+// writes the one-group dispatch {0, T, 0, 1} the router GEMM runs over.
 __global__ void __launch_bounds__(256)
 router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w_gate, int H,
                    int E, int Mpad, int T, uint16_t* __restrict__ img, float* __restrict__ w_rT,
-                   int32_t* __restrict__ hist, int hist_n, int32_t* __restrict__ meta,
-                   int32_t* __restrict__ ctr, int ctr_n) {
+                   int32_t* __restrict__ hist, int hist_n, int32_t* __restrict__ meta) {
   pdl_trigger();
   pdl_wait();
   if (blockIdx.x == 0) {
     for (int i = threadIdx.x; i < hist_n; i += blockDim.x) hist[i] = 0;
-    for (int i = threadIdx.x; i < ctr_n; i += blockDim.x) ctr[i] = 0;
     if (threadIdx.x == 0) { meta[0] = 0; meta[1] = T; meta[2] = 0; meta[3] = 1; }
   }
   const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -179,6 +205,34 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
     const int t = (blockIdx.x * G_WARPS + warp) * p.tok_per_warp + it;
     if (t >= p.T) break;
     gate_token(p, t, nullptr, lrow[warp], exact_s[warp]);
+  }
+}
+
+// A token's gating is a chain of dependent steps (scores, ranks, weights) that one warp runs
+// in thousands of serial instructions; spread over a CTA, one thread per expert, it takes a
+// few barriers, so a batch's gating time is about that of one token whenever the batch fits
+// on the GPU at once (the ranking, weights and tie flags are gate_token's).
+constexpr int kGateCtasPerSm = 4;
+// Above this many tokens the warp-per-token kernel gates faster (measured with 256 experts at
+// 8192 tokens): a CTA waits for its token's rare fp64-margin re-scoring with all 8 warps.
+constexpr int kGateCtaMaxT = 4096;
+__global__ void __launch_bounds__(kMaxExperts, kGateCtasPerSm) gate_cta_kernel(GateParams p) {
+  pdl_trigger();
+  pdl_wait();
+  __shared__ GateCtaSmem g;
+  __shared__ float raw[kMaxExperts + 1];
+  __shared__ float lrow0[kMaxExperts];
+  __shared__ double exact0[kMaxExperts];
+  const int tid = threadIdx.x;
+  if (tid < p.E) {
+    g.lb[tid] = p.logit_bias ? p.logit_bias[tid] : 0.f;
+    g.sb[tid] = p.sel_bias ? p.sel_bias[tid] : 0.f;
+  }
+  for (int t = blockIdx.x; t < p.T; t += gridDim.x) {
+    for (int c = tid; c < p.C; c += kMaxExperts)
+      raw[c] = sum_slices(p.part + (size_t)t * p.ldp + c, p.S, (size_t)p.T * p.ldp);
+    __syncthreads();
+    gate_token_cta<kMaxExperts>(p, t, raw, g, lrow0, exact0, [] { __syncthreads(); });
   }
 }
 
@@ -374,15 +428,11 @@ size_t route_scratch(WsCursor& c, const RoutePlan& r, int T, int E, RouteScratch
   s.img = nullptr;
   s.w_rT = nullptr;
   s.tc_part = nullptr;
-  s.tc_ctr = nullptr;
-  s.tc_ctr_n = 0;
   if (r.tc) {
     s.img = c.take<uint16_t>((size_t)3 * r.Mpad * r.h_per_split);
     s.w_rT = c.take<float>((size_t)E * r.h_per_split);
     if (r.tc_S > 1) {
       s.tc_part = c.take<float>((size_t)r.tc_S * T * r.Mpad);
-      s.tc_ctr_n = (r.Mpad / 128) * ceil_div(T, 128) * 4;
-      s.tc_ctr = c.take<int32_t>((size_t)s.tc_ctr_n);
     }
   }
   if (out) *out = s;
@@ -396,11 +446,11 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
       const size_t thr = (size_t)r.Mpad * (a.H / 8);
       MOE_LAUNCH_PDL(router_prep_kernel, dim3((unsigned)ceil_div((int)thr, 256)), dim3(256), 0, st,
                      a.w_r, a.w_gate, a.H, a.E, r.Mpad, a.T, s.img, s.w_rT, s.hist,
-                     r.ntiles * a.E, s.shared_meta, s.tc_ctr, s.tc_ctr_n);
+                     r.ntiles * a.E, s.shared_meta);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
       const int rr = launch_tc_router(a.x, a.T, a.H, s.img, r.Mpad, r.C, s.shared_meta, s.part,
-                                      s.tc_part, s.tc_ctr, a.err, st);
+                                      s.tc_part, a.err, st);
       if (rr != MOE_OK) return rr;
     } else {
       dim3 g1(ceil_div(a.T, R_BT), ceil_div(r.C, R_BC), r.S);
@@ -411,12 +461,11 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     }
     if (r.small) {
       GateParams p{};
-      p.part = s.part; p.S = r.S; p.C = r.C;
+      p.part = s.part; p.S = r.S; p.C = r.C; p.ldp = r.C;
       p.x = a.x; p.w_r = a.w_r; p.w_rT = nullptr; p.logit_bias = a.logit_bias;
       p.sel_bias = a.sel_bias; p.forced = a.forced; p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k;
       p.mode = a.gating; p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
       p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = nullptr;
-      p.tok_per_warp = 1;
       MOE_LAUNCH_PDL(route_tail_kernel, dim3(1), dim3(kTailThreads), 0, st, p, a.counts,
                      a.offsets, a.pos, a.src, s.active, s.n_active, s.shared_meta, a.x_perm);
       MOE_COUNT_LAUNCH();
@@ -426,22 +475,33 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     int S_gate = r.S;
     if (r.S > 4) {
       const int n = a.T * r.C;
-      MOE_LAUNCH_PDL(reduce_slices_kernel, dim3(ceil_div(n, 256)), dim3(256), 0, st, s.part, r.S,
-                     n);
+      MOE_LAUNCH_PDL(reduce_slices_kernel, dim3(ceil_div(8 * n, 256)), dim3(256), 0, st, s.part,
+                     r.S, n);
       MOE_COUNT_LAUNCH();
       MOE_LAUNCH_CHECK();
       S_gate = 1;
     }
     GateParams p{};
-    p.part = s.part; p.S = S_gate; p.C = r.C;
+    p.part = s.part; p.S = S_gate; p.C = r.C; p.ldp = r.C;
+    if (r.tc && r.tc_S > 1) {
+      // the router GEMM's split partials, [tc_S][T][Mpad]: summed here, in split order
+      p.part = s.tc_part;
+      p.S = r.tc_S;
+      p.ldp = r.Mpad;
+    }
     p.x = a.x; p.w_r = a.w_r; p.w_rT = s.w_rT; p.logit_bias = a.logit_bias; p.sel_bias = a.sel_bias;
     p.forced = a.forced; p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.mode = a.gating;
     p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
     p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = s.hist;
-    // small batches: one token per warp (more CTAs); large: four, to amortise the CTA
-    p.tok_per_warp = a.T <= 1024 ? 1 : 4;
-    const int per_cta = G_WARPS * p.tok_per_warp;
-    MOE_LAUNCH_PDL(gate_topk_kernel, dim3(ceil_div(a.T, per_cta)), dim3(G_WARPS * 32), 0, st, p);
+    if (a.T <= kGateCtaMaxT) {
+      const int ctas = std::min(a.T, kGateCtasPerSm * sm_count());
+      MOE_LAUNCH_PDL(gate_cta_kernel, dim3(ctas), dim3(kMaxExperts), 0, st, p);
+    } else {
+      // four tokens per warp, to amortise the CTA
+      p.tok_per_warp = 4;
+      MOE_LAUNCH_PDL(gate_topk_kernel, dim3(ceil_div(a.T, G_WARPS * p.tok_per_warp)),
+                     dim3(G_WARPS * 32), 0, st, p);
+    }
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
   }

@@ -10,8 +10,8 @@ constexpr int kMaxK = 8;          // top-k limit
 constexpr int kTileT = 128;       // tokens per dispatch tile (histogram granularity)
 
 struct GateParams {
-  const float* part;
-  int S, C;
+  const float* part;         // router outputs: S slices [S][T][ldp], C columns used per row
+  int S, C, ldp;
   const uint16_t* x;
   const float* w_r;
   const float* w_rT;         // [E][H] transposed router (tensor-core router path) or NULL
@@ -26,7 +26,7 @@ struct GateParams {
   float* shared_gate;
   int32_t* tie_flags;
   int32_t* hist;
-  int tok_per_warp;
+  int tok_per_warp;          // warp-per-token gating: tokens per warp
   int32_t* ids_local;        // or NULL: the chosen ids are also stored here (shared memory)
 };
 
@@ -61,8 +61,6 @@ struct RouteScratch {
   uint16_t* img;         // tensor-core router: [Mpad x 3H] tiled bf16 pieces
   float* w_rT;           // tensor-core router: [E][H] fp32
   float* tc_part;        // tensor-core router, tc_S > 1: [tc_S][T][Mpad] fp32 partials
-  int32_t* tc_ctr;       // and its per-tile arrival counters [tiles][4] (cleared by the prep)
-  int tc_ctr_n;
 };
 
 struct RouteArgs {

@@ -12,7 +12,8 @@
 //   warp 0      producer: per K step (64 wide; 128 for quantised weights), one 1-D bulk copy
 //               per 128-row weight tile (the bundle stores each tile as its 128-byte-swizzled
 //               shared-memory image; INT4 / NVFP4: the tile's codes and scales) and 2-D TMA
-//               loads of the BN token rows (128-byte swizzle), completing on an mbarrier;
+//               loads of the BN token rows (128-byte swizzle; quantised weights, a tile
+//               that is not full: 32-row boxes of the rows present), completing on an mbarrier;
 //   warp 1      MMA issuer: allocates TMEM, issues tcgen05.mma (M = 128 weight rows, N = BN
 //               tokens, K = 16), commits stage release and accumulator-ready to mbarriers;
 //   warps 2-5   epilogue: tcgen05.ld of the fp32 accumulators (each warp owns one 32-lane
@@ -179,17 +180,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
-      "%11, %12, %13, %14, %15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
 // 16-column TMEM load without the wait (tcgen05.wait::ld follows before any use of r).
 __device__ __forceinline__ void tmem_ld16_nw(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
@@ -283,10 +273,13 @@ struct Cfg {
   static_assert(SMEM <= 232448, "over the 227 KB shared-memory limit of a CTA");
 };
 
+static_assert(sizeof(TcParams) <= 4096, "kernel parameters stay within 4 KB");
+
 struct Unit {
   const char* w;            // weight section of this unit's expert
   const float* gs;          // NVFP4: the section's matrix scale(s) (gate, up or down)
-  const CUtensorMap* tm;    // its token rows
+  const CUtensorMap* tm;    // its token rows (tms: in 32-row boxes, quantised weights)
+  const CUtensorMap* tms;
   uint16_t* out;
   float* part;
   int M, KT, MT, S, kps, max_rows;
@@ -316,6 +309,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
     x.w = static_cast<const char*>(p.w2);
     x.gs = reinterpret_cast<const float*>(x.w + p.gs_rel2);
     x.tm = &p.tmap_b2;
+    x.tms = &p.tmap_bs2;
     x.out = p.out2;
     x.part = p.part2;
     x.M = p.M2;
@@ -338,6 +332,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* pref, 
     x.w = static_cast<const char*>(p.dev_tab ? p.dev_tab[e] : p.tab.p[e]) + p.w_off;
     x.gs = reinterpret_cast<const float*>(x.w + p.gs_rel);
     x.tm = &p.tmap_b;
+    x.tms = &p.tmap_bs;
     x.out = p.out;
     x.part = p.part;
     x.M = p.M;
@@ -455,8 +450,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
         if (!(ok = warp_wait(smem_u32(&empty[stage]), phase ^ 1, p.err, 1))) break;
         const uint32_t fb = smem_u32(&full[stage]);
         uint8_t* st = smem + stage * C::R1;
+        // token rows: one box of BN rows; quantised kernels load a tile that is not full in
+        // boxes of 32 rows, only those of the rows present
+        const int nsub = INT4 && x.ne - x.nt * BN < BN ? (x.ne - x.nt * BN + 31) >> 5 : 0;
         if (elect_one()) {
-          mbar_expect_tx(fb, C::TX);
+          mbar_expect_tx(fb, nsub ? C::NA * C::RAW_BYTES + (C::KSTEP / 64) * nsub * 4096 : C::TX);
           if (INT4) {
             // the whole 128-k quantised tile (codes + row scales) of each weight tile
 #pragma unroll
@@ -472,9 +470,18 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
                           wb + ((size_t)(x.mt + MTx) * KT + kt) * C::A_BYTES, C::A_BYTES, fb);
           }
 #pragma unroll
-          for (int b = 0; b < C::KSTEP / 64; ++b)
-            tma_2d(smem_u32(st + C::B_OFF + b * C::B_SUB), x.tm,
-                   (ROUTER ? kt % p.kb_mod : kt) * C::KSTEP + b * 64, x.r0 + x.nt * BN, fb);
+          for (int b = 0; b < C::KSTEP / 64; ++b) {
+            const int kc = (ROUTER ? kt % p.kb_mod : kt) * C::KSTEP + b * 64;
+            if (nsub) {
+              // 32-row boxes of 4 KB stacked at 4 KB steps: the same 128-byte-swizzled layout
+              // as one box of all the rows (the swizzle follows the address bits)
+              for (int sb = 0; sb < nsub; ++sb)
+                tma_2d(smem_u32(st + C::B_OFF + b * C::B_SUB + sb * 4096), x.tms, kc,
+                       x.r0 + x.nt * BN + 32 * sb, fb);
+            } else {
+              tma_2d(smem_u32(st + C::B_OFF + b * C::B_SUB), x.tm, kc, x.r0 + x.nt * BN, fb);
+            }
+          }
         }
         __syncwarp();
         if (++stage == C::D1) { stage = 0; phase ^= 1; }
@@ -623,10 +630,11 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
       if (lane == 0) mbar_arrive(smem_u32(&tempty[buf]));
       if (++buf == C::BUFS) { buf = 0; aphase ^= 1; }
 
-      if (x.S > 1) {
+      if (!ROUTER && x.S > 1) {
         // per (tile, lane quarter) arrival counter: the warp completing the S arrivals of its
         // quarter sums that quarter's 32 rows over the splits in split order (no barrier,
-        // nothing waits, the four quarters reduce in parallel)
+        // nothing waits, the four quarters reduce in parallel).  The router's split partials
+        // are summed by its consumer, the gating kernel.
         __threadfence();
         __syncwarp();
         int last = 0;
@@ -637,50 +645,7 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
           if (last) *ctr = 0;
         }
         last = __shfl_sync(0xffffffffu, last, 0);
-        if (last && ROUTER) {
-          // router logits (up to 128 token columns): lane = (4-row group m4, column nn) takes
-          // 16-byte loads of four rows, 16 columns per pass, the splits summed in split order
-          // with four splits' loads in flight
-          __threadfence();
-          const int m4 = lane & 7, nn = lane >> 3, mq = x.mt * 128 + q * 32 + 4 * m4;
-          for (int n0 = 0; n0 < n_here; n0 += 16) {
-            float4 acc[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int sp0 = 0; sp0 < x.S; sp0 += 4) {
-              float4 v[4][4];
-#pragma unroll
-              for (int s4 = 0; s4 < 4; ++s4)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int n = n0 + nn + 4 * i, sp = sp0 + s4;
-                  v[s4][i] = (n < n_here && sp < x.S)
-                                 ? __ldcg(reinterpret_cast<const float4*>(
-                                       x.part + ((size_t)sp * x.max_rows + x.r0 + x.nt * BN + n) * MP + mq))
-                                 : make_float4(0.f, 0.f, 0.f, 0.f);
-                }
-#pragma unroll
-              for (int s4 = 0; s4 < 4; ++s4)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  acc[i].x += v[s4][i].x;
-                  acc[i].y += v[s4][i].y;
-                  acc[i].z += v[s4][i].z;
-                  acc[i].w += v[s4][i].w;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int n = n0 + nn + 4 * i;
-              if (n >= n_here) continue;
-              float* o = p.out_f32 + (size_t)(x.r0 + x.nt * BN + n) * p.ldo;
-              if (mq < p.m_limit) o[mq] = acc[i].x;
-              if (mq + 1 < p.m_limit) o[mq + 1] = acc[i].y;
-              if (mq + 2 < p.m_limit) o[mq + 2] = acc[i].z;
-              if (mq + 3 < p.m_limit) o[mq + 3] = acc[i].w;
-            }
-          }
-        } else if (last) {
+        if (last) {
           __threadfence();
           const size_t stride = (size_t)x.max_rows * MP;
           for (int n = 0; n < n_here; ++n) {
@@ -868,7 +833,15 @@ int tc_bn_for(const GemmArgs& a) {
   // INT4 down tiles also stop at 128 tokens: at 256 the accumulator and the dequantised A
   // stages fill TMEM without a second accumulator buffer, so the epilogue would not overlap
   const int cap = (a.fused || a.int4 || a.fp4) ? 128 : 256;
-  const int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+  int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
+  if (a.int4 || a.fp4) {
+    // quantised weights are decoded once per token tile, so the tile is as wide as the most
+    // rows one expert can hold (a skewed batch puts most of its tokens on a few experts);
+    // its MMAs and token-row loads cover only the rows present, so a wide tile costs an
+    // expert with few rows nothing but the second accumulator buffer
+    const int most = a.rows_cap > 0 ? std::min(a.rows_cap, a.max_rows) : a.max_rows;
+    bn = std::max(bn, most <= 32 ? 32 : most <= 64 ? 64 : 128);
+  }
   return std::min(bn, cap);
 }
 
@@ -908,12 +881,12 @@ TcPlan plan_tc(const GemmArgs& a) {
   return t;
 }
 
-static bool encode_tokens(CUtensorMap* m, const uint16_t* base, int K, int rows, int BN) {
+static bool encode_tokens(CUtensorMap* m, const uint16_t* base, int K, int rows, int box_rows) {
   auto enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)BN};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<uint16_t*>(base), dims, strides,
              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -924,6 +897,8 @@ static int fill_params(TcParams& kp, const GemmArgs& a, const TcPlan& t, float* 
                        int32_t* counters, int32_t* err) {
   if (!encode_fn()) return MOE_ERR_UNSUPPORTED;
   if (!encode_tokens(&kp.tmap_b, a.xin, a.K, a.max_rows, t.BN)) return MOE_ERR_INVALID_ARG;
+  if ((a.int4 || a.fp4) && !encode_tokens(&kp.tmap_bs, a.xin, a.K, a.max_rows, 32))
+    return MOE_ERR_INVALID_ARG;
   kp.offsets = a.offsets;
   kp.active = a.active;
   kp.n_active = a.n_active;
@@ -1001,7 +976,8 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
   int r = fill_params(kp, a1, pp.t1, part1, counters, err);
   if (r != MOE_OK) return r;
   if (a2.max_rows > 0) {
-    if (!encode_tokens(&kp.tmap_b2, a2.xin, a2.K, a2.max_rows, pp.t1.BN))
+    if (!encode_tokens(&kp.tmap_b2, a2.xin, a2.K, a2.max_rows, pp.t1.BN) ||
+        ((a1.int4 || a1.fp4) && !encode_tokens(&kp.tmap_bs2, a2.xin, a2.K, a2.max_rows, 32)))
       return MOE_ERR_INVALID_ARG;
     kp.g2 = 1;
     kp.w2 = static_cast<const char*>(a2.tab->p[0]) + a2.w_off;
@@ -1020,12 +996,12 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
 int tc_router_splits(int T, int H, int Mpad) {
   // K splits of the router product: its tiles (Mpad / 128 x ceil(T / 128)) are few next to the
   // SMs except at the largest batches.  Same rule as the expert GEMMs' split choice: the
-  // fewest waves of 1/S of the K range each, a little extra per split (the partial sums), at
-  // most 4 splits (one warp per 32-row quarter of a tile sums them) and 8 K steps per split.
+  // fewest waves of 1/S of the K range each, a little extra per split (its partials, which the
+  // gating kernel sums), at most 16 splits and at least 8 K steps per split.
   const int tiles = (Mpad / 128) * ceil_div(T, 128), KT = 3 * H / 64, G = sm_count();
   int best_s = 1;
   double best = (double)ceil_div(tiles, G);
-  for (int S = 2; S <= std::min(4, KT / 8); ++S) {
+  for (int S = 2; S <= std::min(16, KT / 8); ++S) {
     const double c = (double)ceil_div(tiles * S, G) / S * (1.0 + 0.05 * (S - 1));
     if (c < best * 0.97) {
       best = c;
@@ -1036,8 +1012,8 @@ int tc_router_splits(int T, int H, int Mpad) {
 }
 
 int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,
-                     const int32_t* meta, float* logits, float* part, int32_t* counters,
-                     int32_t* err, cudaStream_t st) {
+                     const int32_t* meta, float* logits, float* part, int32_t* err,
+                     cudaStream_t st) {
   if (T <= 0) return MOE_OK;
   auto enc = encode_fn();
   if (!enc) return MOE_ERR_UNSUPPORTED;
@@ -1062,7 +1038,6 @@ int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad,
   kp.S = tc_router_splits(T, H, Mpad);
   kp.kt_per_split = ceil_div(3 * H / 64, kp.S);
   kp.part = part;          // [S][T][Mpad] fp32 when S > 1
-  kp.counters = counters;  // [tiles][4], zero on entry
   kp.max_rows = T;
   kp.err = err;
   kp.kb_mod = H / 64;

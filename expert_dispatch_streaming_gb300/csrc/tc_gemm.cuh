@@ -8,6 +8,8 @@ namespace moe {
 
 struct TcParams {
   CUtensorMap tmap_b;        // token rows [max_rows][K] bf16, box {64, BN}, 128-byte swizzle
+  CUtensorMap tmap_bs;       // quantised weights: the same rows in boxes of {64, 32}, for the
+                             // token tiles that are not full
   const int32_t* offsets;
   const int32_t* active;
   const int32_t* n_active;
@@ -30,7 +32,7 @@ struct TcParams {
   // optional second group after the routed experts (the shared expert): rows2 token rows of its
   // own token map, with its own weights (section base), shapes, split count and outputs
   int g2;
-  CUtensorMap tmap_b2;
+  CUtensorMap tmap_b2, tmap_bs2;
   const void* w2;
   int M2, K2, S2, kt_per_split2, rows2;
   uint16_t* out2;
@@ -60,11 +62,12 @@ int launch_tc_pair(const GemmArgs& a1, const GemmArgs& a2, const TcPair& pp, flo
 // Router logits on the tensor cores: logits[t][c] (c < C, fp32, row stride C) =
 // sum_k img[c][k] * x[t][k mod H] with img the [Mpad x 3H] tiled bf16 image of the three
 // router pieces (see router_prep in route.cu); one group of T rows (offsets {0, T}).  The K
-// range is split tc_router_splits(T, H, Mpad) ways: part = [S][T][Mpad] fp32 partials and
-// counters = [Mpad / 128 * ceil(T / 128)][4] ints, zero on entry (left zero), when S > 1.
+// range is split tc_router_splits(T, H, Mpad) ways; with S > 1 the launch writes only the
+// split partials part = [S][T][Mpad] fp32 (split order), which its consumer sums, and leaves
+// logits untouched.
 int tc_router_splits(int T, int H, int Mpad);
 int launch_tc_router(const uint16_t* x, int T, int H, const void* img, int Mpad, int C,
-                     const int32_t* meta, float* logits, float* part, int32_t* counters,
-                     int32_t* err, cudaStream_t st);
+                     const int32_t* meta, float* logits, float* part, int32_t* err,
+                     cudaStream_t st);
 
 }  // namespace moe

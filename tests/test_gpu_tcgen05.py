@@ -68,6 +68,16 @@ def test_grouped_tcgen05_bf16(moe, syn, counts):
     assert_close(got, ref, f"tcgen05 counts={counts}")
 
 
+@pytest.mark.parametrize("wdtype", ["int4_g128", "nvfp4"])
+def test_grouped_tcgen05_quantised_wide_token_tiles(moe, syn, wdtype):
+    """Quantised weights take 128-token tiles here (the grouped call bounds no expert's rows
+    below the batch): experts with 1, 5, 33 and 70 rows load only their 32-row boxes, and
+    300 / 129 rows span several tiles with ragged ends."""
+    cfg = wl.custom("tcq_" + wdtype, cfg_id=123, H=512, E=8, k=2, I=384, wdtype=wdtype)
+    got, ref = _grouped(moe, syn, cfg, [300, 5, 129, 0, 33, 1, 0, 70])
+    assert_close(got, ref, f"tcgen05 {wdtype} wide token tiles")
+
+
 def test_grouped_tcgen05_large_k(moe, syn):
     cfg = wl.custom("tck", cfg_id=121, H=2048, E=4, k=2, I=1408)
     got, ref = _grouped(moe, syn, cfg, [600, 3, 0, 257])
