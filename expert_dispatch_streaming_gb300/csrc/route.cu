@@ -145,53 +145,60 @@ reduce_slices_kernel(float* __restrict__ part, int S, int n) {
 // bf16 pieces hi + mid + lo (each the bf16 rounding of what the previous pieces leave), which
 // represent the fp32 weight; written as a tiled 128-byte-swizzled bf16 image of [Mpad x 3H]
 // (piece p of row m at k-tile p * H/64 + k/64), plus the transposed fp32 router for the exact
-// re-scoring.  Thread = (row m, 8-element chunk of k).  Block 0 also clears the histogram and
-// writes the one-group dispatch {0, T, 0, 1} the router GEMM runs over.
+// re-scoring.  Block = 64 rows m x 64 k: the fp32 router block is read row by row (coalesced)
+// into shared memory, then thread (row m, 8-element chunk c of the 64 k), c fastest, writes
+// its 16 bytes of each piece's image row -- eight threads one whole 128-byte row -- and its 32
+// bytes of the transposed copy (eight threads one 256-byte run).  Block (0, 0) also clears the
+// histogram and writes the one-group dispatch {0, T, 0, 1} the router GEMM runs over.
+constexpr int kPrepM = 64, kPrepK = 64;
 __global__ void __launch_bounds__(256)
 router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w_gate, int H,
                    int E, int Mpad, int T, uint16_t* __restrict__ img, float* __restrict__ w_rT,
                    int32_t* __restrict__ hist, int hist_n, int32_t* __restrict__ meta) {
   pdl_trigger();
   pdl_wait();
-  if (blockIdx.x == 0) {
-    for (int i = threadIdx.x; i < hist_n; i += blockDim.x) hist[i] = 0;
-    if (threadIdx.x == 0) { meta[0] = 0; meta[1] = T; meta[2] = 0; meta[3] = 1; }
+  __shared__ float blk[kPrepK][kPrepM + 1];
+  const int tid = threadIdx.x, m0 = blockIdx.x * kPrepM, h0 = blockIdx.y * kPrepK;
+  if (blockIdx.x == 0 && blockIdx.y == 0) {
+    for (int i = tid; i < hist_n; i += blockDim.x) hist[i] = 0;
+    if (tid == 0) { meta[0] = 0; meta[1] = T; meta[2] = 0; meta[3] = 1; }
   }
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  const int chunks = H / 8;
-  if (idx >= (size_t)Mpad * chunks) return;
-  const int m = (int)(idx % Mpad), ch = (int)(idx / Mpad);
-  const int KTB = H / 64, mt = m >> 7, r = m & 127;
-  uint32_t pc[3][4];
-  float v[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int h = ch * 8 + i;
-    v[i] = m < E ? w_r[(size_t)h * E + m]
-                 : (m == E && w_gate ? bf16_bits_to_float(w_gate[h]) : 0.f);
+  for (int i = tid; i < kPrepK * kPrepM; i += blockDim.x) {
+    const int hh = i / kPrepM, mm = i % kPrepM, m = m0 + mm, h = h0 + hh;
+    blk[hh][mm] = m < E ? w_r[(size_t)h * E + m]
+                        : (m == E && w_gate ? bf16_bits_to_float(w_gate[h]) : 0.f);
   }
+  __syncthreads();
+  const int KTB = H / 64, kt = h0 / 64;
+  for (int i = tid; i < kPrepM * 8; i += blockDim.x) {
+    const int c = i & 7, mm = i >> 3, m = m0 + mm, mt = m >> 7, r = m & 127;
+    float v[8];
 #pragma unroll
-  for (int i = 0; i < 8; i += 2) {
-    float a = v[i], b = v[i + 1];
+    for (int j = 0; j < 8; ++j) v[j] = blk[8 * c + j][mm];
+    uint32_t pc[3][4];
+#pragma unroll
+    for (int j = 0; j < 8; j += 2) {
+      float a = v[j], b = v[j + 1];
+#pragma unroll
+      for (int q = 0; q < 3; ++q) {
+        const uint32_t w = float2_to_bf16x2(a, b);
+        pc[q][j / 2] = w;
+        const float2 f = bf16x2_to_float2(w);
+        a -= f.x;
+        b -= f.y;
+      }
+    }
 #pragma unroll
     for (int q = 0; q < 3; ++q) {
-      const uint32_t w = float2_to_bf16x2(a, b);
-      pc[q][i / 2] = w;
-      const float2 f = bf16x2_to_float2(w);
-      a -= f.x;
-      b -= f.y;
+      uint16_t* tile = img + ((size_t)mt * (3 * KTB) + q * KTB + kt) * 8192;
+      *reinterpret_cast<uint4*>(tile + r * 64 + ((c ^ (r & 7)) << 3)) =
+          make_uint4(pc[q][0], pc[q][1], pc[q][2], pc[q][3]);
     }
-  }
-  const int kt = ch >> 3, c = ch & 7;
-#pragma unroll
-  for (int q = 0; q < 3; ++q) {
-    uint16_t* tile = img + ((size_t)mt * (3 * KTB) + q * KTB + kt) * 8192;
-    *reinterpret_cast<uint4*>(tile + r * 64 + ((c ^ (r & 7)) << 3)) =
-        make_uint4(pc[q][0], pc[q][1], pc[q][2], pc[q][3]);
-  }
-  if (m < E && w_rT) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) w_rT[(size_t)m * H + ch * 8 + i] = v[i];
+    if (m < E && w_rT) {
+      float4* o = reinterpret_cast<float4*>(w_rT + (size_t)m * H + h0 + 8 * c);
+      o[0] = make_float4(v[0], v[1], v[2], v[3]);
+      o[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
   }
 }
 
@@ -443,8 +450,7 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
                  cudaStream_t st) {
   if (a.T > 0) {
     if (r.tc) {
-      const size_t thr = (size_t)r.Mpad * (a.H / 8);
-      MOE_LAUNCH_PDL(router_prep_kernel, dim3((unsigned)ceil_div((int)thr, 256)), dim3(256), 0, st,
+      MOE_LAUNCH_PDL(router_prep_kernel, dim3(r.Mpad / kPrepM, a.H / kPrepK), dim3(256), 0, st,
                      a.w_r, a.w_gate, a.H, a.E, r.Mpad, a.T, s.img, s.w_rT, s.hist,
                      r.ntiles * a.E, s.shared_meta);
       MOE_COUNT_LAUNCH();

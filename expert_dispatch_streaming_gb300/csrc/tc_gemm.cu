@@ -267,7 +267,7 @@ struct Cfg {
   static_assert(USED <= 512, "tensor memory holds 512 columns");
   static constexpr int TMEM_COLS = USED <= 32 ? 32 : USED <= 64 ? 64 : USED <= 128 ? 128
                                  : USED <= 256 ? 256 : 512;
-  static constexpr int DQ_WARPS = 8;                          // INT4 dequant warps, 2 per quarter
+  static constexpr int DQ_WARPS = 8;                          // quantised: dequant warps, 2 per quarter
   static constexpr int THREADS = INT4 ? 192 + 32 * DQ_WARPS : 192;
   static constexpr int SMEM = D1 * R1 + 1024 /*align*/ + 4096 /*barriers, prefix*/;
   static_assert(SMEM <= 232448, "over the 227 KB shared-memory limit of a CTA");
@@ -678,13 +678,18 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
     }
     (void)et;
   } else if (INT4) {
-    // ------------------------------------------------------------ dequant (warps 6..13)
-    // A warp may only touch its own quarter of the TMEM lanes (warp % 4), so two warps share
-    // each quarter: thread = weight row r = 32 * (warp % 4) + lane.  Fused: warps 6-9 convert
-    // the gate tile and warps 10-13 the up tile, each the row's 128 codes of the step (64
-    // columns); not fused: warps 6-9 codes 0-63 and warps 10-13 codes 64-127 (32 columns).
-    const int q = warp & 3, half = (warp - 6) >> 2, r = q * 32 + lane;
-    const int tile = FUSED ? half : 0;
+    // ------------------------------------------------------------ dequant (warps 6 ..)
+    // A warp may only touch its own quarter of the TMEM lanes (warp % 4), so DQ_WARPS / 4 warps
+    // share each quarter: thread = weight row r = 32 * (warp % 4) + lane, and the warp's job
+    // (its rank among its quarter's warps) is CPW consecutive 32-code chunks of the step's
+    // NA * 4 (the row's 128 codes of each weight tile), all in one tile: 16 TMEM columns per
+    // chunk, pairs in k order.  Fused: the gate tile's 4 chunks, or the up tile's; not fused:
+    // chunks 0-1 or 2-3.  (Sixteen dequant warps, one pair of chunks each, measured no faster
+    // for the fused GEMMs and slower for the down GEMMs, at the 80 registers a thread they allow.)
+    constexpr int JOBS = C::DQ_WARPS / 4, CPW = C::NA * 4 / JOBS;
+    static_assert(CPW == 2 || CPW == 4, "whole pairs of chunks of one tile");
+    const int q = warp & 3, job = (warp - 6) >> 2, r = q * 32 + lane;
+    const int tile = job * CPW / 4, c_lo = job * CPW % 4;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
     int stage = 0, astage = 0;
     uint32_t phase = 0, a2phase = 0;
@@ -703,29 +708,38 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
         if (WT == kInt4) s2 = int4_scale_pair(*reinterpret_cast<const uint16_t*>(raw + 8192 + 2 * r));
         else s8 = *reinterpret_cast<const uint2*>(raw + 8192 + 8 * r);
         const uint32_t ta = tmem_base + lane_base + C::A_TMEM + (astage * C::NA + tile) * 64;
-        // 32-code chunks c0, c0 + 1 of row r -> 32 TMEM columns (pairs in k order)
-        auto convert = [&](int c0, uint32_t col) {
-          const uint4 a = *reinterpret_cast<const uint4*>(raw + (c0 * 128 + r) * 16);
-          const uint4 b = *reinterpret_cast<const uint4*>(raw + ((c0 + 1) * 128 + r) * 16);
-          const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-          uint32_t v[32];
-          if (WT == kInt4) {
+        // chunks c0 .. c0 + NCH - 1 of row r -> TMEM columns 16 c0 .. 16 (c0 + NCH) - 1
+        auto convert = [&](auto nch, int c0) {
+          constexpr int NCH = decltype(nch)::value;
+          uint32_t w[4 * NCH];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              v[4 * j + 0] = int4_pair<0>(w[j], s2);
-              v[4 * j + 1] = int4_pair<1>(w[j], s2);
-              v[4 * j + 2] = int4_pair<2>(w[j], s2);
-              v[4 * j + 3] = int4_pair<3>(w[j], s2);
+          for (int i = 0; i < NCH; ++i) {
+            const uint4 a = *reinterpret_cast<const uint4*>(raw + ((c0 + i) * 128 + r) * 16);
+            w[4 * i] = a.x;
+            w[4 * i + 1] = a.y;
+            w[4 * i + 2] = a.z;
+            w[4 * i + 3] = a.w;
+          }
+          uint32_t v[16 * NCH];
+#pragma unroll
+          for (int jp = 0; jp < 2 * NCH; ++jp) {
+            // words 2 jp, 2 jp + 1 (16 k) of chunk c = c0 + jp / 2 share one scale: NVFP4 block
+            // 2 c + jp % 2 of the row, byte 2 (c % 2) + jp % 2 of the scale word of blocks
+            // 4 (c / 2) .. 4 (c / 2) + 3
+            uint32_t sp = s2;
+            if (WT != kInt4) {
+              const int c = c0 + jp / 2;
+              sp = fp4_scale_pair(c < 2 ? s8.x : s8.y, 2 * (c & 1) + (jp & 1));
             }
-          } else {
-            // words 2j', 2j'+1 of the two chunks share block 2 * c0 + j' of the row (16 k)
-            const uint32_t sw = c0 == 0 ? s8.x : s8.y;   // blocks 4*(c0/2) .. +3
 #pragma unroll
-            for (int jb = 0; jb < 4; ++jb) {
-              const uint32_t sp = fp4_scale_pair(sw, jb);
-#pragma unroll
-              for (int jj = 0; jj < 2; ++jj) {
-                const int j = 2 * jb + jj;
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = 2 * jp + jj;
+              if (WT == kInt4) {
+                v[4 * j + 0] = int4_pair<0>(w[j], sp);
+                v[4 * j + 1] = int4_pair<1>(w[j], sp);
+                v[4 * j + 2] = int4_pair<2>(w[j], sp);
+                v[4 * j + 3] = int4_pair<3>(w[j], sp);
+              } else {
                 v[4 * j + 0] = fp4_pair<0>(w[j], sp);
                 v[4 * j + 1] = fp4_pair<1>(w[j], sp);
                 v[4 * j + 2] = fp4_pair<2>(w[j], sp);
@@ -733,13 +747,13 @@ __global__ void __launch_bounds__(Cfg<BN, FUSED, WT>::THREADS, 1)
               }
             }
           }
-          tmem_st32(ta + col, v);
+          tmem_st32(ta + 16 * c0, v);
         };
-        if (FUSED) {
-          convert(0, 0);
-          convert(2, 32);
+        if constexpr (CPW == 4) {
+          convert(std::integral_constant<int, 2>{}, 0);
+          convert(std::integral_constant<int, 2>{}, 2);
         } else {
-          convert(2 * half, 32 * half);
+          convert(std::integral_constant<int, 2>{}, c_lo);
         }
         tmem_wait_st();
         tc_fence_before();
