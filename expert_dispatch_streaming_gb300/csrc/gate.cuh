@@ -246,8 +246,9 @@ static __device__ __forceinline__ double exact_score_cta(const GateParams& p, in
 
 // Chosen list (ascending id, or the forced order) and weights of token t by one warp, from the
 // lane's logits l[c] (experts lane + 32 c), its chosen flags and the token's logits row lrow.
+template <int NC>
 static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
-                                                   const float (&l)[EC], const bool (&chosen)[EC],
+                                                   const float (&l)[NC], const bool (&chosen)[NC],
                                                    const float* lrow, int flag) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
@@ -263,7 +264,7 @@ static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) my_ids[j] = 0;
 #pragma unroll
-      for (int c = 0; c < EC; ++c) {
+      for (int c = 0; c < NC; ++c) {
         unsigned m = __ballot_sync(0xffffffffu, chosen[c]);
         while (m) {
           const int e = 32 * c + __ffs(m) - 1;
@@ -281,11 +282,11 @@ static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
     if (p.mode == MOE_GATING_SOFTMAX) {
       float mx = -CUDART_INF_F;
 #pragma unroll
-      for (int c = 0; c < EC; ++c) mx = fmaxf(mx, l[c]);
+      for (int c = 0; c < NC; ++c) mx = fmaxf(mx, l[c]);
       M = warp_max(mx);
       float s = 0.f;
 #pragma unroll
-      for (int c = 0; c < EC; ++c)
+      for (int c = 0; c < NC; ++c)
         if (lane + 32 * c < E) s += expf(l[c] - M);
       Ssum = warp_sum(s);
     }
@@ -329,20 +330,22 @@ static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
 // experts.  Out: the lane's logits l[c] and chosen flags (experts lane + 32 c), the tie flag;
 // writes the token's logits row lrow, logits and shared gate.  `raw` = the token's C summed
 // router outputs (or NULL: sum the S slices of p.part); lrow / exact_s = this warp's
-// shared-memory rows; pre: exact_s already holds the re-scored band (NaN where not).
+// shared-memory rows; pre: exact_s already holds the re-scored band (NaN where not).  NC =
+// expert slots per lane (E <= 32 NC): small expert counts run fewer slots' instructions.
 // Inlined into each kernel, so that the parameter block's fields and the
 // lane arrays stay in registers.
+template <int NC>
 static __device__ __forceinline__ void gate_select(const GateParams& p, int t, const float* raw,
-                                                   float* lrow, double* exact_s, float (&l)[EC],
-                                                   bool (&chosen)[EC], int& flag_out,
+                                                   float* lrow, double* exact_s, float (&l)[NC],
+                                                   bool (&chosen)[NC], int& flag_out,
                                                    bool pre = false) {
   const int lane = threadIdx.x & 31;
   const int E = p.E, k = p.k;
   {
     // ---- logits: fixed-order sum of the H slices (+ logit bias), scores
-    float sc[EC];
+    float sc[NC];
 #pragma unroll
-    for (int c = 0; c < EC; ++c) {
+    for (int c = 0; c < NC; ++c) {
       const int e = lane + 32 * c;
       float v = -CUDART_INF_F, s = -CUDART_INF_F;
       if (e < E) {
@@ -366,15 +369,15 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
     }
 
 #pragma unroll
-    for (int c = 0; c < EC; ++c) chosen[c] = false;
+    for (int c = 0; c < NC; ++c) chosen[c] = false;
     int flag = 0;
 
     if (p.forced == nullptr) {
       // ---- top-(k+1) by repeated warp argmax on (score desc, id asc); kth = the k-th score,
       // nxt = the best unchosen one (scalars, so that nothing here is indexed at run time)
-      bool taken[EC];
+      bool taken[NC];
 #pragma unroll
-      for (int c = 0; c < EC; ++c) taken[c] = (lane + 32 * c) >= E;
+      for (int c = 0; c < NC; ++c) taken[c] = (lane + 32 * c) >= E;
       float kth = -CUDART_INF_F, nxt = -CUDART_INF_F;
       const int nsel = min(k + 1, E);
 #pragma unroll
@@ -383,7 +386,7 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
           float bs = -CUDART_INF_F;
           int bi = 0x7fffffff;
 #pragma unroll
-          for (int c = 0; c < EC; ++c) {
+          for (int c = 0; c < NC; ++c) {
             const int e = lane + 32 * c;
             if (!taken[c] && better(sc[c], e, bs, bi)) { bs = sc[c]; bi = e; }
           }
@@ -391,7 +394,7 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
           if (r == k - 1) kth = bs;
           if (r == k) nxt = bs;
 #pragma unroll
-          for (int c = 0; c < EC; ++c)
+          for (int c = 0; c < NC; ++c)
             if (lane + 32 * c == bi) { taken[c] = true; if (r < k) chosen[c] = true; }
         }
       }
@@ -399,11 +402,11 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
         // ---- refinement: experts within the margin of the boundary are re-scored in fp64;
         // chosen experts clear of it (score - nxt > kTau) stay chosen
         flag = 1;
-        bool band[EC];
+        bool band[NC];
         int n_def = 0;
         const float thr = kth - kTau;
 #pragma unroll
-        for (int c = 0; c < EC; ++c) {
+        for (int c = 0; c < NC; ++c) {
           const int e = lane + 32 * c;
           const bool d = chosen[c] && sc[c] - nxt > kTau;
           band[c] = (e < E) && !d && sc[c] >= thr;
@@ -412,14 +415,14 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
         }
         // the band as eight warp-uniform words; one (not unrolled) loop over its members, so
         // that exact_score is inlined once
-        unsigned bm[EC];
+        unsigned bm[NC];
 #pragma unroll
-        for (int c = 0; c < EC; ++c) bm[c] = __ballot_sync(0xffffffffu, band[c]);
+        for (int c = 0; c < NC; ++c) bm[c] = __ballot_sync(0xffffffffu, band[c]);
 #pragma unroll 1
-        for (int c = 0; c < EC; ++c) {
+        for (int c = 0; c < NC; ++c) {
           unsigned m = 0;
 #pragma unroll
-          for (int c2 = 0; c2 < EC; ++c2) m = c2 == c ? bm[c2] : m;
+          for (int c2 = 0; c2 < NC; ++c2) m = c2 == c ? bm[c2] : m;
           while (m) {
             const int b = 32 * c + __ffs(m) - 1;
             m &= m - 1;
@@ -437,7 +440,7 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
           double bs = -CUDART_INF;
           int bi = 0x7fffffff;
 #pragma unroll
-          for (int c = 0; c < EC; ++c) {
+          for (int c = 0; c < NC; ++c) {
             const int e = lane + 32 * c;
             if (band[c] && !chosen[c] && better_d(exact_s[e], e, bs, bi)) {
               bs = exact_s[e];
@@ -447,14 +450,14 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
           warp_argmax_d(bs, bi);
           last = bs;
 #pragma unroll
-          for (int c = 0; c < EC; ++c)
+          for (int c = 0; c < NC; ++c)
             if (lane + 32 * c == bi) chosen[c] = true;
         }
         // exact gap to the best band member left out
         double bs = -CUDART_INF;
         int bi = 0x7fffffff;
 #pragma unroll
-        for (int c = 0; c < EC; ++c) {
+        for (int c = 0; c < NC; ++c) {
           const int e = lane + 32 * c;
           if (band[c] && !chosen[c] && better_d(exact_s[e], e, bs, bi)) {
             bs = exact_s[e];
@@ -473,13 +476,14 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
 // Gating of token t by one warp: gate_select, then the chosen list and weights (gate_finish);
 // writes ids / w / logits / shared gate / tie flag of t and adds the token's experts to
 // hist[(t / 128) * E + e].
+template <int NC = EC>
 static __device__ __forceinline__ void gate_token(const GateParams& p, int t, const float* raw,
                                                   float* lrow, double* exact_s) {
-  float l[EC];
-  bool chosen[EC];
+  float l[NC];
+  bool chosen[NC];
   int flag = 0;
-  gate_select(p, t, raw, lrow, exact_s, l, chosen, flag);
-  gate_finish(p, t, l, chosen, lrow, flag);
+  gate_select<NC>(p, t, raw, lrow, exact_s, l, chosen, flag);
+  gate_finish<NC>(p, t, l, chosen, lrow, flag);
 }
 
 // ------------------------------------------------------------------------------ A2-A4, small T
@@ -620,8 +624,8 @@ static __device__ __forceinline__ void gate_token_cta(const GateParams& p, int t
       float l[EC];
       bool chosen[EC];
       int flag = 0;
-      gate_select(p, t, raw, lrow0, exact0, l, chosen, flag, pre);
-      gate_finish(p, t, l, chosen, g.l, flag);
+      gate_select<EC>(p, t, raw, lrow0, exact0, l, chosen, flag, pre);
+      gate_finish<EC>(p, t, l, chosen, g.l, flag);
     }
     sync();
     return;

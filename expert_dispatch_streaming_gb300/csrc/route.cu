@@ -163,14 +163,23 @@ router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w
     for (int i = tid; i < hist_n; i += blockDim.x) hist[i] = 0;
     if (tid == 0) { meta[0] = 0; meta[1] = T; meta[2] = 0; meta[3] = 1; }
   }
-  for (int i = tid; i < kPrepK * kPrepM; i += blockDim.x) {
-    const int hh = i / kPrepM, mm = i % kPrepM, m = m0 + mm, h = h0 + hh;
-    blk[hh][mm] = m < E ? w_r[(size_t)h * E + m]
-                        : (m == E && w_gate ? bf16_bits_to_float(w_gate[h]) : 0.f);
+  // all 16 loads of a thread issued before the first use (one memory latency, not sixteen)
+  float ld[kPrepK * kPrepM / 256];
+#pragma unroll
+  for (int j = 0; j < kPrepK * kPrepM / 256; ++j) {
+    const int i = tid + 256 * j, hh = i / kPrepM, mm = i % kPrepM, m = m0 + mm, h = h0 + hh;
+    ld[j] = m < E ? w_r[(size_t)h * E + m]
+                  : (m == E && w_gate ? bf16_bits_to_float(w_gate[h]) : 0.f);
+  }
+#pragma unroll
+  for (int j = 0; j < kPrepK * kPrepM / 256; ++j) {
+    const int i = tid + 256 * j;
+    blk[i / kPrepM][i % kPrepM] = ld[j];
   }
   __syncthreads();
   const int KTB = H / 64, kt = h0 / 64;
-  for (int i = tid; i < kPrepM * 8; i += blockDim.x) {
+#pragma unroll
+  for (int i = tid; i < kPrepM * 8; i += 256) {
     const int c = i & 7, mm = i >> 3, m = m0 + mm, mt = m >> 7, r = m & 127;
     float v[8];
 #pragma unroll
@@ -202,6 +211,7 @@ router_prep_kernel(const float* __restrict__ w_r, const uint16_t* __restrict__ w
   }
 }
 
+template <int NC>
 __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
   pdl_trigger();
   pdl_wait();
@@ -211,7 +221,7 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
   for (int it = 0; it < p.tok_per_warp; ++it) {
     const int t = (blockIdx.x * G_WARPS + warp) * p.tok_per_warp + it;
     if (t >= p.T) break;
-    gate_token(p, t, nullptr, lrow[warp], exact_s[warp]);
+    gate_token<NC>(p, t, nullptr, lrow[warp], exact_s[warp]);
   }
 }
 
@@ -223,6 +233,11 @@ constexpr int kGateCtasPerSm = 4;
 // Above this many tokens the warp-per-token kernel gates faster (measured with 256 experts at
 // 8192 tokens): a CTA waits for its token's rare fp64-margin re-scoring with all 8 warps.
 constexpr int kGateCtaMaxT = 4096;
+// Up to this many experts a warp holds a token's scores in at most two slots per lane and the
+// warp-per-token kernel is the faster one from kGateWarpMinT tokens on (measured with 8 and 60
+// experts; below, the batch's tokens on as many CTAs finish sooner).
+constexpr int kGateWarpMaxE = 64;
+constexpr int kGateWarpMinT = 256;
 __global__ void __launch_bounds__(kMaxExperts, kGateCtasPerSm) gate_cta_kernel(GateParams p) {
   pdl_trigger();
   pdl_wait();
@@ -499,14 +514,17 @@ int launch_route(const RouteArgs& a, const RoutePlan& r, const RouteScratch& s,
     p.forced = a.forced; p.T = a.T; p.H = a.H; p.E = a.E; p.k = a.k; p.mode = a.gating;
     p.scale = a.scale; p.ids = a.ids; p.w = a.w; p.logits = a.logits;
     p.shared_gate = a.shared_gate; p.tie_flags = a.tie_flags; p.hist = s.hist;
-    if (a.T <= kGateCtaMaxT) {
+    if (a.T <= kGateCtaMaxT && (a.E > kGateWarpMaxE || a.T < kGateWarpMinT)) {
       const int ctas = std::min(a.T, kGateCtasPerSm * sm_count());
       MOE_LAUNCH_PDL(gate_cta_kernel, dim3(ctas), dim3(kMaxExperts), 0, st, p);
     } else {
-      // four tokens per warp, to amortise the CTA
-      p.tok_per_warp = 4;
-      MOE_LAUNCH_PDL(gate_topk_kernel, dim3(ceil_div(a.T, G_WARPS * p.tok_per_warp)),
-                     dim3(G_WARPS * 32), 0, st, p);
+      // one token per warp; four per warp at the largest batches, to amortise the CTA
+      p.tok_per_warp = a.T <= 1024 ? 1 : 4;
+      const dim3 grid(ceil_div(a.T, G_WARPS * p.tok_per_warp)), block(G_WARPS * 32);
+      if (a.E <= 32) MOE_LAUNCH_PDL(gate_topk_kernel<1>, grid, block, 0, st, p);
+      else if (a.E <= 64) MOE_LAUNCH_PDL(gate_topk_kernel<2>, grid, block, 0, st, p);
+      else if (a.E <= 128) MOE_LAUNCH_PDL(gate_topk_kernel<4>, grid, block, 0, st, p);
+      else MOE_LAUNCH_PDL(gate_topk_kernel<EC>, grid, block, 0, st, p);
     }
     MOE_COUNT_LAUNCH();
     MOE_LAUNCH_CHECK();
