@@ -846,7 +846,6 @@ int tc_bn_for(const GemmArgs& a) {
   // the dequantised weight stages); 128-token fused tiles measured faster at every bf16 shape
   // INT4 down tiles also stop at 128 tokens: at 256 the accumulator and the dequantised A
   // stages fill TMEM without a second accumulator buffer, so the epilogue would not overlap
-  // (measured: the DeepSeek-shaped down GEMM at 8192 tokens 2.38 -> 2.83 ms with 256)
   const int cap = (a.fused || a.int4 || a.fp4) ? 128 : 256;
   int bn = avg <= 32 ? 32 : avg <= 64 ? 64 : avg <= 128 ? 128 : 256;
   if (a.int4 || a.fp4) {
