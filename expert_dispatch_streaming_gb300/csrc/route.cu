@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(G_WARPS * 32) gate_topk_kernel(GateParams p) {
 // on the GPU at once (the ranking, weights and tie flags are gate_token's).
 constexpr int kGateCtasPerSm = 4;
 // Above this many tokens the warp-per-token kernel gates faster (measured with 256 experts at
-// 8192 tokens): a CTA waits for its token's rare fp64-margin re-scoring with all 8 warps.
+// 8192 tokens): a CTA waits for its token's rare near-boundary re-scoring with all 8 warps.
 constexpr int kGateCtaMaxT = 4096;
 // Up to this many experts a warp holds a token's scores in at most two slots per lane and the
 // warp-per-token kernel is the faster one from kGateWarpMinT tokens on (measured with 8 and 60

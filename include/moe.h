@@ -208,15 +208,19 @@ uint64_t moe_checksum64(const void* data, size_t bytes);
  *             src [T*k] int32 (src[pos[t][j]] = t*k + j),
  *             logits [T][E] fp32 or NULL (the fp32 logits incl. logit_bias),
  *             tie_flags [T] int32 or NULL: 0 = the k-th/(k+1)-th selection gap exceeded the
- *             fp32 error margin; 1 = the experts near the boundary were re-scored in fp64;
- *             2 = as 1 and the fp64 gap was still below 1e-6 (a logged near-tie).
+ *             fp32 error margin; 1 = the experts near the boundary were re-scored (see
+ *             below); 2 = as 1 and the re-scored gap was still below 1e-6 (a logged
+ *             near-tie).
  *  ws         device scratch of moe_route_workspace_size(T, H, E, k) bytes.  Its first 4 bytes
  *             hold an error word, cleared at the start of every call: 0 = no error; non-zero =
  *             a bounded wait inside the tensor-core router (batches of T >= 256 tokens) ran out
  *             of time and the call's outputs are invalid.  Read it with moe_workspace_error.
  * Limits: 1 <= k <= min(E, 8), E <= 256, T >= 0 (T == 0 writes zero counts/offsets),
  * H a multiple of 8.  Exact selection: experts whose fp32 selection score lies within 1e-4 of
- * the k-th are re-scored in fp64 on the GPU, so the chosen set equals that of exact arithmetic
+ * the k-th are re-scored on the GPU (the dot product x . W_r[:, e] in compensated fp32 -- each
+ * product and each addition split error-free into a sum and its rounding error, error of
+ * order H * 2^-48 * sum |x w| -- then the bias and the gating function in fp64), so the
+ * chosen set equals that of exact arithmetic
  * (except ties closer than 1e-6, flagged 2) whenever the fp32 logits are within 1e-4 of the
  * exact ones.  That holds for activations and router weights of the workloads' magnitudes
  * (|x| ~ N(0, 1), W_r ~ N(0, 0.02), H <= 16384: observed fp32 error below 1e-5); inputs whose
