@@ -12,10 +12,11 @@
 //   gate_cta_kernel        one CTA per token (grid-stride): sums the token's slices in fixed
 //                          order, scores, ranks the experts over the CTA (gate_token_cta),
 //                          re-scores the experts whose fp32 score is within the error margin of
-//                          the k-th (one warp, compensated sums), writes ids / weights and bumps
-//                          the per-tile expert histogram.
-//   gate_topk_kernel       the same gating by one warp per token (gate_token), for the largest
-//                          batches, where throughput rather than one token's latency counts.
+//                          the k-th (the whole CTA, compensated sums), writes ids / weights and
+//                          bumps the per-tile expert histogram.
+//   gate_topk_kernel       the same gating by one warp per token (gate_token, 1-8 expert slots
+//                          per lane), for the largest batches, where throughput rather than one
+//                          token's latency counts, and for a few dozen experts from 256 tokens.
 //   scan_kernel            one CTA: per-expert counts, exclusive offsets, per-tile bases and
 //                          the list of experts that received rows.
 //   rank_permute_kernel    one CTA per 128-token tile: stable rank of each (t, j) within its
