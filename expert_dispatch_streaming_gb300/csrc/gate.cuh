@@ -13,7 +13,8 @@
 
 namespace moe {
 
-// fp32 selection scores within this margin of the k-th are re-scored in fp64.  The fp32
+// fp32 selection scores within this margin of the k-th are re-scored (exact_score: a
+// compensated fp32 dot product, the gating function in fp64).  The fp32
 // logit is a sum of H <= 16384 products accumulated in fp32; for the workloads' magnitudes
 // its error stays below ~1e-5, so 1e-4 leaves a wide margin (sigmoid scores move by at most
 // a quarter of the logit error).
@@ -326,8 +327,8 @@ static __device__ __forceinline__ void gate_finish(const GateParams& p, int t,
     }
 }
 
-// Selection for token t by one warp: scores, top-k with the fp64 refinement of near-boundary
-// experts.  Out: the lane's logits l[c] and chosen flags (experts lane + 32 c), the tie flag;
+// Selection for token t by one warp: scores, top-k with the refinement of near-boundary
+// experts by exact_score.  Out: the lane's logits l[c] and chosen flags (experts lane + 32 c), the tie flag;
 // writes the token's logits row lrow, logits and shared gate.  `raw` = the token's C summed
 // router outputs (or NULL: sum the S slices of p.part); lrow / exact_s = this warp's
 // shared-memory rows; pre: exact_s already holds the re-scored band (NaN where not).  NC =
@@ -399,8 +400,8 @@ static __device__ __forceinline__ void gate_select(const GateParams& p, int t, c
         }
       }
       if (k < E && kth - nxt <= kTau) {
-        // ---- refinement: experts within the margin of the boundary are re-scored in fp64;
-        // chosen experts clear of it (score - nxt > kTau) stay chosen
+        // ---- refinement: experts within the margin of the boundary are re-scored
+        // (exact_score); chosen experts clear of it (score - nxt > kTau) stay chosen
         flag = 1;
         bool band[NC];
         int n_def = 0;
@@ -529,7 +530,7 @@ struct CtaGateSmem {
 // weights are computed per chosen expert and normalised by one thread summing them in
 // ascending-id order, as gate_finish does.  When ids are forced, or the k-th and (k+1)-th fp32
 // scores lie within the margin kTau, the first warp runs gate_select / gate_finish instead
-// (fp64 re-scoring, with lrow0 / exact0 as that warp's rows).  raw: the token's C summed
+// (with lrow0 / exact0 as that warp's rows; the CTA re-scores the margin's experts first).  raw: the token's C summed
 // router outputs (shared memory); g.lb / g.sb hold the biases (zero when absent).  Threads
 // 0 .. NT-1 must all call it; `sync` is their barrier.
 template <int NT, class Sync>
