@@ -17,6 +17,7 @@ It is a plain, slow, obviously-correct restatement in fp64 (NumPy) of what the l
   generator's encoder.
 
 Pins (closed forms, brute force, invariants) live in ``tests/test_oracle_*.py``.
-Parity unpinned: the realised Zipf popularity shape of the synthetic routers (logged only).
+The realised Zipf popularity of the synthetic routers has no closed form; it is pinned by
+properties of a routed batch (tests/test_workloads.py), not by exact shares.
 """
 from . import bf16, lru_sim, moe_ref  # noqa: F401

@@ -1,5 +1,6 @@
 """Host-side checks of the seeded input generators (shapes, determinism, encodings)."""
 import numpy as np
+import pytest
 import torch
 
 import workloads as wl
@@ -51,3 +52,53 @@ def test_stream_trace_locality():
     reuse = np.mean([np.array_equal(ids[s, l, t], ids[s - 1, l, t])
                      for s in range(1, 50) for l in range(2) for t in range(4)])
     assert 0.7 < reuse < 0.95
+
+
+def _realised_counts(cfg, T):
+    """Expert assignment counts of T tokens routed by the oracle (the workload's own routing)."""
+    from oracle import bf16, moe_ref
+    x = bf16.decode(wl.tokens(cfg, T))
+    b = wl.popularity_bias(cfg, 0)
+    l = moe_ref.router_logits(x, wl.router(cfg, 0).astype(np.float64),
+                              b if cfg.bias_kind == "logit" else None)
+    s = moe_ref.selection_scores(l, cfg.gating, b if cfg.bias_kind == "select" else None)
+    ids, _ = moe_ref.topk_select(s, cfg.k)
+    return np.bincount(ids.ravel(), minlength=cfg.E), ids.size
+
+
+def _rank_correlation(a, b):
+    """Spearman's rho (no ties handling needed beyond average ranks of equal values)."""
+    def ranks(v):
+        order = np.argsort(v, kind="stable")
+        r = np.empty(len(v))
+        r[order] = np.arange(len(v))
+        for val in np.unique(v):               # average ranks of ties
+            m = v == val
+            r[m] = r[m].mean()
+        return r
+    ra, rb = ranks(np.asarray(a, float)), ranks(np.asarray(b, float))
+    return float(np.corrcoef(ra, rb)[0, 1])
+
+
+@pytest.mark.parametrize("name", ["qwen", "deepseek"])
+def test_realised_popularity_follows_the_zipf_ranks(name):
+    """The realised expert popularity of a batch routed by the oracle follows the workload's
+    Zipf ranks: the most popular rank is the busiest expert, the first ranks' loads decrease,
+    popularity and load are strongly rank-correlated, and the busiest expert's share matches
+    the workload's definition -- Qwen: Zipf(1.0) over 60 experts as a logit bias, whose top
+    probability is 1 / H_60 = 0.214; DeepSeek: the selection bias calibrated (on another batch)
+    so that the top expert takes 1 / (2k) = 1/16 of the assignments.  A sign flip, a dropped
+    logarithm or a wrong rank permutation in the bias fails one of these."""
+    cfg = {"qwen": wl.QWEN, "deepseek": wl.DEEPSEEK}[name]
+    cnt, n = _realised_counts(cfg, 2048)
+    r = wl.popularity_ranks(cfg, 0)
+    by_rank = cnt[np.argsort(r)]
+    assert int(np.argmax(cnt)) == int(np.argmin(r))
+    assert np.all(np.diff(by_rank[:4]) < 0)
+    assert _rank_correlation(-r, cnt) > 0.85
+    share = by_rank[0] / n
+    if name == "qwen":
+        p1 = 1.0 / np.sum(1.0 / np.arange(1, 61))
+        assert abs(share - p1) < 0.04, share
+    else:
+        assert abs(share - 1.0 / 16) < 0.01, share
