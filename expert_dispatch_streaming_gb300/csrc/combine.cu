@@ -9,16 +9,21 @@
 #include "route.cuh"
 
 #include <algorithm>
+#include <type_traits>
 
 namespace moe {
 
 constexpr int kCombineThreads = 128;  // one 16-byte vector (8 bf16) per thread
 
 // grid (ceil(H / 1024), T): block (c, t) covers elements [1024c, 1024c + 1024) of token t, so
-// every load of a block is issued at once, whatever T is
+// every load of a block is issued at once, whatever T is.  K = the top-k, a template
+// parameter: the kernel moves a few bytes per instruction, and loops over the eight possible
+// expert rows with the unused ones predicated off made it instruction-bound (issue 70% busy at
+// 30% of HBM for the Mixtral shape's k = 2).
+template <int K>
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ pos,
-               const float* __restrict__ w, int T, int k, int H,
+               const float* __restrict__ w, int T, int H,
                const uint16_t* __restrict__ shared, const float* __restrict__ shared_gate,
                const uint16_t* __restrict__ residual, uint16_t* __restrict__ out) {
   pdl_trigger();
@@ -26,21 +31,20 @@ combine_kernel(const uint16_t* __restrict__ y, const int32_t* __restrict__ pos,
   const int v = blockIdx.x * kCombineThreads + threadIdx.x;
   if (v >= H / 8) return;
   for (int t = blockIdx.y; t < T; t += gridDim.y) {
-  int pj[kMaxK];
-  float wj[kMaxK];
+  int pj[K];
+  float wj[K];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    pj[j] = j < k ? __ldg(pos + (size_t)t * k + j) : 0;
-    wj[j] = j < k ? __ldg(w + (size_t)t * k + j) : 0.f;
+  for (int j = 0; j < K; ++j) {
+    pj[j] = __ldg(pos + (size_t)t * K + j);
+    wj[j] = __ldg(w + (size_t)t * K + j);
   }
-  uint4 q[kMaxK];
+  uint4 q[K];
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j)
-    if (j < k) q[j] = __ldg(reinterpret_cast<const uint4*>(y + (size_t)pj[j] * H) + v);
+  for (int j = 0; j < K; ++j)
+    q[j] = __ldg(reinterpret_cast<const uint4*>(y + (size_t)pj[j] * H) + v);
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int j = 0; j < kMaxK; ++j) {
-    if (j >= k) break;
+  for (int j = 0; j < K; ++j) {
     const uint32_t qw[4] = {q[j].x, q[j].y, q[j].z, q[j].w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
@@ -193,8 +197,26 @@ int launch_combine(const uint16_t* y, const int32_t* pos, const float* w, int T,
     return MOE_OK;
   }
   dim3 grid(ceil_div(H / 8, kCombineThreads), std::min(T, 65535));
-  MOE_LAUNCH_PDL(combine_kernel, grid, dim3(kCombineThreads), 0, st, y, pos, w, T, k, H, shared,
-                 shared_gate, residual, out);
+  const dim3 block(kCombineThreads);
+  auto go = [&](auto kc) -> int {
+    constexpr int K = decltype(kc)::value;
+    MOE_LAUNCH_PDL(combine_kernel<K>, grid, block, 0, st, y, pos, w, T, H, shared, shared_gate,
+                   residual, out);
+    return MOE_OK;
+  };
+  int r = MOE_ERR_INVALID_ARG;
+  switch (k) {
+    case 1: r = go(std::integral_constant<int, 1>{}); break;
+    case 2: r = go(std::integral_constant<int, 2>{}); break;
+    case 3: r = go(std::integral_constant<int, 3>{}); break;
+    case 4: r = go(std::integral_constant<int, 4>{}); break;
+    case 5: r = go(std::integral_constant<int, 5>{}); break;
+    case 6: r = go(std::integral_constant<int, 6>{}); break;
+    case 7: r = go(std::integral_constant<int, 7>{}); break;
+    case 8: r = go(std::integral_constant<int, 8>{}); break;
+    default: break;
+  }
+  if (r != MOE_OK) return r;
   MOE_COUNT_LAUNCH();
   MOE_LAUNCH_CHECK();
   return MOE_OK;
